@@ -1,0 +1,278 @@
+"""CPU oracle for the FP8 per-tensor-absmax block pipeline.
+
+TEST INFRASTRUCTURE ONLY.  Import this from ``tests/``, from
+``__graft_entry__.smoke()`` or from the CPU-baseline leg of ``bench.py``;
+nothing in the product path may load it.  It shares no code with the CUDA
+library (``fp8_absmax_reduce_gb300``); the two meet only through the seeded
+inputs from ``synth``.
+
+The arithmetic lives in ``fp8q_oracle.cpp`` (plain C++17, fp64 GEMM
+accumulation, software E4M3/E5M2 with round-to-nearest-even and saturation);
+this module compiles it with g++ on first use and marshals numpy arrays.
+
+Sources: "LLMQ: Efficient Lower-Precision Pretraining for Consumer GPUs"
+(paperlayer.ai summary), §1 (dynamic tensor-level FP8 scaling), §3/§3.1
+(fused non-matmul ops, retained absmax statistics), §5 Figure 2 (E4M3
+forward, E5M2 activation gradients); "Periodic Reporting for period 1 -
+FastML" (CORDIS), "FP8 training without delayed scaling" (just-in-time
+absmax scaling, no clipping).
+
+Parity pins: ``tests/test_oracle_*.py``.  Every function here is pinned;
+see the header of each test file for what pins it.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+E4M3, E5M2 = 0, 1
+NN, NT, TN = 0, 1, 2
+FMT_MAX = {E4M3: 448.0, E5M2: 57344.0}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fp8q_oracle.cpp")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libfp8q_oracle.so")
+_CXXFLAGS = ["-O3", "-std=c++17", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-pthread"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle shared library (g++) if missing or stale; return its path."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["g++", *_CXXFLAGS, _SRC, "-o", tmp], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _c(arr):
+    return arr.ctypes.data_as(ctypes.c_void_p)
+
+
+class _BlockIO(ctypes.Structure):
+    _fields_ = [
+        ("T", ctypes.c_int64), ("d", ctypes.c_int64), ("f", ctypes.c_int64),
+        ("eps", ctypes.c_float), ("exact", ctypes.c_int), ("nthreads", ctypes.c_int),
+        ("x", ctypes.c_void_p), ("g", ctypes.c_void_p), ("Wgu", ctypes.c_void_p),
+        ("Wd", ctypes.c_void_p), ("dY", ctypes.c_void_p),
+        ("y", ctypes.c_void_p), ("H", ctypes.c_void_p), ("rstd", ctypes.c_void_p),
+        ("Wgu8", ctypes.c_void_p), ("Wd8", ctypes.c_void_p), ("n8", ctypes.c_void_p),
+        ("a8", ctypes.c_void_p), ("scal_fwd", ctypes.c_void_p),
+        ("dX", ctypes.c_void_p), ("dWgu", ctypes.c_void_p), ("dWd", ctypes.c_void_p),
+        ("dg", ctypes.c_void_p), ("dN", ctypes.c_void_p), ("dH", ctypes.c_void_p),
+        ("dY8", ctypes.c_void_p), ("dH8", ctypes.c_void_p), ("scal_bwd", ctypes.c_void_p),
+    ]
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ctypes.CDLL(build())
+            vp, i64, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float
+            L.fo_fp8_encode.restype = ctypes.c_uint8
+            L.fo_fp8_encode.argtypes = [f32, ctypes.c_int]
+            L.fo_fp8_decode.restype = ctypes.c_double
+            L.fo_fp8_decode.argtypes = [ctypes.c_uint8, ctypes.c_int]
+            L.fo_fp8_encode_n.argtypes = [vp, i64, ctypes.c_int, vp]
+            L.fo_fp8_decode_n.argtypes = [vp, i64, ctypes.c_int, vp]
+            L.fo_bf16_round_n.argtypes = [vp, i64, vp]
+            L.fo_exp_ref.restype = f32
+            L.fo_exp_ref.argtypes = [f32]
+            L.fo_exp_ref_n.argtypes = [vp, i64, vp]
+            L.fo_pairwise_sum.restype = f32
+            L.fo_pairwise_sum.argtypes = [vp, i64]
+            L.fo_quantize_absmax.argtypes = [vp, ctypes.c_int, i64, ctypes.c_int, vp, vp]
+            L.fo_rmsnorm_quant.argtypes = [vp, vp, i64, i64, f32, vp, vp, vp]
+            L.fo_swiglu_quant.argtypes = [vp, i64, i64, ctypes.c_int, vp, vp]
+            L.fo_gemm_scaled.argtypes = [ctypes.c_int, i64, i64, i64, vp, ctypes.c_int, vp,
+                                         ctypes.c_int, f32, f32, vp, ctypes.c_int, vp, ctypes.c_int]
+            L.fo_block_forward.argtypes = [ctypes.POINTER(_BlockIO)]
+            L.fo_block_forward_backward.argtypes = [ctypes.POINTER(_BlockIO)]
+            _lib = L
+    return _lib
+
+
+# ----------------------------------------------------------------------------
+# bf16 helpers (bf16 tensors travel as uint16 bit patterns)
+# ----------------------------------------------------------------------------
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact value of bf16 bit patterns."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def bf16_round(v: np.ndarray) -> np.ndarray:
+    """One round-to-nearest-even rounding of real values (float64) to bf16 bits."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint16)
+    lib().fo_bf16_round_n(_c(v), v.size, _c(out))
+    return out
+
+
+# ----------------------------------------------------------------------------
+# FP8 codec and exp_ref
+# ----------------------------------------------------------------------------
+def fp8_encode(v: np.ndarray, fmt: int) -> np.ndarray:
+    """fp32 -> FP8 code, round-to-nearest-even, saturating to +-max, NaN -> 0x7F."""
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(v.shape, dtype=np.uint8)
+    lib().fo_fp8_encode_n(_c(v), v.size, fmt, _c(out))
+    return out
+
+
+def fp8_decode(codes: np.ndarray, fmt: int) -> np.ndarray:
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    lib().fo_fp8_decode_n(_c(c), c.size, fmt, _c(out))
+    return out
+
+
+def exp_ref(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.float32)
+    lib().fo_exp_ref_n(_c(x), x.size, _c(out))
+    return out
+
+
+def pairwise_sum_f32(v: np.ndarray) -> np.float32:
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    return np.float32(lib().fo_pairwise_sum(_c(v), v.size))
+
+
+# ----------------------------------------------------------------------------
+# Standalone operations
+# ----------------------------------------------------------------------------
+def quantize_absmax(x: np.ndarray, fmt: int):
+    """Per-tensor absmax quantization.  x: uint16 (bf16 bits) or float32.
+
+    Returns (codes uint8 same shape, scal float32[3] = amax, scale, scale_inv, status).
+    """
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.uint16:
+        dtype = 0
+    elif x.dtype == np.float32:
+        dtype = 1
+    else:
+        raise TypeError("quantize_absmax takes bf16 bits (uint16) or float32")
+    q = np.empty(x.shape, dtype=np.uint8)
+    scal = np.zeros(3, dtype=np.float32)
+    st = lib().fo_quantize_absmax(_c(x), dtype, x.size, fmt, _c(q), _c(scal))
+    return q, scal, st
+
+
+def rmsnorm_quant(x: np.ndarray, g: np.ndarray, eps: float):
+    """x [T,d] bf16 bits, g [d] bf16 bits -> (n8 [T,d], scal[3], rstd[T] fp32, status)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    g = np.ascontiguousarray(g, dtype=np.uint16)
+    T, d = x.shape
+    q = np.empty((T, d), dtype=np.uint8)
+    scal = np.zeros(3, dtype=np.float32)
+    rstd = np.empty(T, dtype=np.float32)
+    st = lib().fo_rmsnorm_quant(_c(x), _c(g), T, d, eps, _c(q), _c(scal), _c(rstd))
+    return q, scal, rstd, st
+
+
+def swiglu_quant(H: np.ndarray, fmt: int = E4M3):
+    """H [T,2f] bf16 bits (gate | up) -> (a8 [T,f], scal[3], status)."""
+    H = np.ascontiguousarray(H, dtype=np.uint16)
+    T, f2 = H.shape
+    f = f2 // 2
+    q = np.empty((T, f), dtype=np.uint8)
+    scal = np.zeros(3, dtype=np.float32)
+    st = lib().fo_swiglu_quant(_c(H), T, f, fmt, _c(q), _c(scal))
+    return q, scal, st
+
+
+def gemm_scaled(layout: int, A: np.ndarray, fmtA: int, B: np.ndarray, fmtB: int,
+                sinvA: float, sinvB: float, out: str = "f32", residual=None, nthreads: int = 1):
+    """C = fl32(sinvA*sinvB) * op(A) op(B) [+ residual], fp64 accumulation.
+
+    layout NN: A [M,K], B [K,N];  NT: A [M,K], B [N,K];  TN: A [K,M], B [K,N].
+    out: "bf16" (uint16 bits), "f32", or "f64" (alpha * acc before output rounding).
+    """
+    A = np.ascontiguousarray(A, dtype=np.uint8)
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    if layout == TN:
+        K, M = A.shape
+    else:
+        M, K = A.shape
+    N = B.shape[0] if layout == NT else B.shape[1]
+    kb = B.shape[1] if layout == NT else B.shape[0]
+    if kb != K:
+        raise ValueError("inner dimensions differ")
+    code = {"bf16": 0, "f32": 1, "f64": 2}[out]
+    C = np.empty((M, N), dtype={0: np.uint16, 1: np.float32, 2: np.float64}[code])
+    res = None
+    if residual is not None:
+        if code != 0:
+            raise ValueError("residual needs bf16 output")
+        res = np.ascontiguousarray(residual, dtype=np.uint16)
+    lib().fo_gemm_scaled(layout, M, N, K, _c(A), fmtA, _c(B), fmtB, sinvA, sinvB,
+                         None if res is None else _c(res), code, _c(C), nthreads)
+    return C
+
+
+# ----------------------------------------------------------------------------
+# The MLP block
+# ----------------------------------------------------------------------------
+def _as_f64(a, exact):
+    if exact:
+        return np.ascontiguousarray(a, dtype=np.float64)
+    return bf16_to_f64(a)
+
+
+def block(x, g, Wgu, Wd, dY=None, eps: float = 1e-6, exact: bool = False, nthreads: int = 1):
+    """MLP block forward (and backward when dY is given).
+
+    Quantized mode (exact=False): x, g, Wgu, Wd, dY are bf16 bit patterns
+    (uint16) of shapes [T,d], [d], [d,2f], [f,d], [T,d].  Returned float arrays
+    hold the stored values (bf16 tensors as their exact value, fp32 tensors as
+    fp32); codes are uint8.  scal_fwd rows: W_gu, W_d, n, a; scal_bwd rows: dY, dH.
+
+    Exact mode (exact=True): float64 inputs, no quantization and no rounding;
+    the backward is then the exact gradient of the forward.
+    """
+    x64, g64, Wgu64, Wd64 = (_as_f64(a, exact) for a in (x, g, Wgu, Wd))
+    T, d = x64.shape
+    f = Wd64.shape[0]
+    if Wgu64.shape != (d, 2 * f) or g64.shape != (d,):
+        raise ValueError("block shapes: x [T,d], g [d], Wgu [d,2f], Wd [f,d]")
+    out = {
+        "y": np.empty((T, d)), "H": np.empty((T, 2 * f)), "rstd": np.empty(T),
+        "Wgu8": np.empty((d, 2 * f), np.uint8), "Wd8": np.empty((f, d), np.uint8),
+        "n8": np.empty((T, d), np.uint8), "a8": np.empty((T, f), np.uint8),
+        "scal_fwd": np.zeros((4, 3), np.float32),
+    }
+    io = _BlockIO(T=T, d=d, f=f, eps=eps, exact=int(exact), nthreads=int(nthreads))
+    keep = [x64, g64, Wgu64, Wd64]
+    io.x, io.g, io.Wgu, io.Wd = (a.ctypes.data for a in keep)
+    for k in ("y", "H", "rstd", "Wgu8", "Wd8", "n8", "a8", "scal_fwd"):
+        setattr(io, k, out[k].ctypes.data)
+    if dY is None:
+        st = lib().fo_block_forward(ctypes.byref(io))
+    else:
+        dY64 = _as_f64(dY, exact)
+        keep.append(dY64)
+        io.dY = dY64.ctypes.data
+        out.update({
+            "dX": np.empty((T, d)), "dWgu": np.empty((d, 2 * f)), "dWd": np.empty((f, d)),
+            "dg": np.empty(d), "dN": np.empty((T, d)), "dH": np.empty((T, 2 * f)),
+            "dY8": np.empty((T, d), np.uint8), "dH8": np.empty((T, 2 * f), np.uint8),
+            "scal_bwd": np.zeros((2, 3), np.float32),
+        })
+        for k in ("dX", "dWgu", "dWd", "dg", "dN", "dH", "dY8", "dH8", "scal_bwd"):
+            setattr(io, k, out[k].ctypes.data)
+        st = lib().fo_block_forward_backward(ctypes.byref(io))
+    out["status"] = st
+    return out

@@ -1,0 +1,608 @@
+// CPU oracle for the FP8 per-tensor-absmax transformer-block pipeline.
+//
+// TEST INFRASTRUCTURE ONLY.  This library is loaded by the test-suite, by the
+// package's smoke() check and by the benchmark's CPU-baseline leg, nothing
+// else.  The CUDA library never links, includes or calls it, and it shares no
+// code, header, table or constant generator with the CUDA library.
+//
+// What it states, and where the statement comes from:
+//   * "LLMQ: Efficient Lower-Precision Pretraining for Consumer GPUs"
+//     (paperlayer.ai summary of arXiv 2512.15306), §1: FP8 training with
+//     dynamic tensor-level scaling.
+//   * "Periodic Reporting for period 1 - FastML" (CORDIS), paragraph "FP8
+//     training without delayed scaling": just-in-time tensor-level absmax
+//     scaling that guarantees no value clipping.
+//   * LLMQ §3.1 (activation checkpointing): absmax statistics are retained
+//     per tensor; quantization follows the nonlinearity (SwiGLU).
+//   * LLMQ §5, Figure 2: E4M3 for activations/weights, E5M2 for activation
+//     gradients.
+//   * LLMQ §3 / §3.1 / §3.2: non-matmul ops (RMSNorm, SwiGLU, residual) are
+//     fused around the GEMMs; kernels are deterministic.
+//   * FP8 encodings follow the OCP 8-bit floating point specification
+//     (E4M3 "FN": no infinities, max 448; E5M2: IEEE-like, max 57344).
+// The pages give no formula beyond these sentences; every concrete choice
+// below (scale = fmax/amax, fp32 product before the cast, RNE with
+// saturation, RMSNorm epsilon and pairwise fp32 sum of squares, SwiGLU in
+// fp32 with exp_ref, bf16 storage points) is a stated reading of them.
+//
+// Two arithmetic modes share one code path:
+//   quantized (exact == 0): the FP8 pipeline.  Every rounding point is an
+//     explicit call (to_bf16, fp32 expression, fp8 encode).  GEMMs accumulate
+//     in fp64 (exact for E4M3 x E4M3 at every size used here).
+//   exact (exact == 1): the same block with every rounding point removed and
+//     all arithmetic in fp64.  Used to pin the backward formulas against
+//     finite differences of the forward.
+//
+// Build: g++ -O2 -std=c++17 -ffp-contract=off -fno-fast-math -fPIC -shared
+// (-ffp-contract=off keeps every fp32 expression at one rounding per
+// operation on both x86-64 and aarch64).
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+namespace {
+
+// ----------------------------------------------------------------------------
+// Bit helpers, bf16
+// ----------------------------------------------------------------------------
+float f32_from_bits(uint32_t u) { float f; std::memcpy(&f, &u, 4); return f; }
+uint32_t bits_from_f32(float f) { uint32_t u; std::memcpy(&u, &f, 4); return u; }
+
+double bf16_value(uint16_t h) { return (double)f32_from_bits((uint32_t)h << 16); }
+
+// Round v to the nearest number with `frac` fraction bits whose exponent is at
+// least `emin` (so values below 2^emin land on the subnormal grid), ties to
+// even.  No overflow handling: callers saturate or overflow themselves.
+double round_binary(double v, int frac, int emin) {
+  if (v == 0.0 || !std::isfinite(v)) return v;
+  int e;
+  std::frexp(std::fabs(v), &e);            // |v| in [2^(e-1), 2^e)
+  int ex = std::max(e - 1, emin);
+  double quantum = std::ldexp(1.0, ex - frac);
+  return std::nearbyint(v / quantum) * quantum;   // default mode: ties-to-even
+}
+
+// One rounding from a real (given as double) to bf16, IEEE round-to-nearest-even,
+// overflow to infinity.
+uint16_t to_bf16_bits(double v) {
+  if (std::isnan(v)) return (uint16_t)(0x7FC0 | (std::signbit(v) ? 0x8000 : 0));
+  double r = round_binary(v, 7, -126);
+  float rf = (float)r;                      // exact, or +-inf when r = +-2^128
+  return (uint16_t)(bits_from_f32(rf) >> 16);
+}
+double to_bf16(double v) { return bf16_value(to_bf16_bits(v)); }
+
+// ----------------------------------------------------------------------------
+// FP8 codec (OCP E4M3 "FN" and E5M2), round-to-nearest-even, saturating
+// ----------------------------------------------------------------------------
+enum { FMT_E4M3 = 0, FMT_E5M2 = 1 };
+
+struct Fp8Format {
+  int frac;        // fraction bits
+  int emin;        // exponent of the smallest normal
+  int bias;
+  double maxv;     // largest finite magnitude
+  uint8_t nan_code;
+};
+
+const Fp8Format& fp8_format(int fmt) {
+  static const Fp8Format e4m3 = {3, -6, 7, 448.0, 0x7F};
+  static const Fp8Format e5m2 = {2, -14, 15, 57344.0, 0x7F};
+  return fmt == FMT_E5M2 ? e5m2 : e4m3;
+}
+
+double fp8_decode(uint8_t c, int fmt) {
+  const Fp8Format& F = fp8_format(fmt);
+  const int ebits = 7 - F.frac;
+  const int emask = (1 << ebits) - 1;
+  const int mmask = (1 << F.frac) - 1;
+  const double sign = (c & 0x80) ? -1.0 : 1.0;
+  const int e = (c >> F.frac) & emask;
+  const int m = c & mmask;
+  if (fmt == FMT_E4M3 && e == emask && m == mmask) return std::nan("");
+  if (fmt == FMT_E5M2 && e == emask) return m == 0 ? sign * HUGE_VAL : std::nan("");
+  if (e == 0) return sign * std::ldexp((double)m, F.emin - F.frac);
+  return sign * std::ldexp(1.0 + std::ldexp((double)m, -F.frac), e - F.bias);
+}
+
+// fp32 -> fp8 with round-to-nearest-even and saturation to +-max (so +-inf
+// saturates too); NaN -> the format's NaN code; the sign of zero is kept.
+uint8_t fp8_encode(float v, int fmt) {
+  const Fp8Format& F = fp8_format(fmt);
+  if (std::isnan(v)) return F.nan_code;
+  const uint8_t sign = std::signbit(v) ? 0x80 : 0x00;
+  double a = round_binary(std::fabs((double)v), F.frac, F.emin);
+  if (a > F.maxv) a = F.maxv;
+  if (a == 0.0) return sign;
+  int e;
+  std::frexp(a, &e);
+  const int ex = e - 1;
+  if (ex < F.emin) {                               // subnormal grid
+    int m = (int)(a / std::ldexp(1.0, F.emin - F.frac));
+    return (uint8_t)(sign | m);
+  }
+  int m = (int)(a / std::ldexp(1.0, ex - F.frac)) - (1 << F.frac);
+  return (uint8_t)(sign | ((ex + F.bias) << F.frac) | m);
+}
+
+// ----------------------------------------------------------------------------
+// exp_ref: fp32 exponential with a fixed operation sequence so that SwiGLU has
+// one bit-exact answer.  Method: Cody & Waite argument reduction
+// x = k ln2 + r with ln2 split in a short high part (exact k*hi) and a low
+// correction, |r| <= ln2/2, then the Taylor polynomial of e^r to degree 8 in
+// Horner form, then multiplication by 2^k built from exponent bits.  Every
+// operation is a single IEEE fp32 operation (no contraction).
+// ----------------------------------------------------------------------------
+float exp_ref(float x) {
+  if (std::isnan(x)) return x;
+  if (x > 88.72283935546875f) return HUGE_VALF;     // e^x > FLT_MAX
+  if (x < -103.972084045410156f) return 0.0f;       // e^x < half the smallest subnormal
+  const float log2e = 1.44269502162933349609375f;   // fp32(1/ln 2)
+  const float ln2_hi = 0.693359375f;                // 355/512, 9 significant bits
+  const float ln2_lo = -2.12194440e-4f;             // fp32(ln 2 - 355/512)
+  const float kf = std::nearbyint(x * log2e);
+  const float r = (x - kf * ln2_hi) - kf * ln2_lo;
+  float p = 1.0f / 40320.0f;                        // 1/8!
+  p = p * r + 1.0f / 5040.0f;
+  p = p * r + 1.0f / 720.0f;
+  p = p * r + 1.0f / 120.0f;
+  p = p * r + 1.0f / 24.0f;
+  p = p * r + 1.0f / 6.0f;
+  p = p * r + 0.5f;
+  p = p * r + 1.0f;
+  p = p * r + 1.0f;
+  const int k = (int)kf;                            // -150 <= k <= 128
+  if (k > 127) return (p * 2.0f) * f32_from_bits((uint32_t)(127 + 127) << 23);
+  if (k >= -126) return p * f32_from_bits((uint32_t)(k + 127) << 23);
+  // subnormal result: scale into the normal range first, then one rounding
+  return (p * f32_from_bits((uint32_t)(k + 64 + 127) << 23)) * f32_from_bits((uint32_t)(127 - 64) << 23);
+}
+
+// ----------------------------------------------------------------------------
+// Per-tensor absmax scaling
+// ----------------------------------------------------------------------------
+struct Scal { float amax, scale, scale_inv; };
+
+// s = fl32(fmax / amax): the tensor's absmax element lands exactly on +-fmax,
+// nothing is clipped.  amax == 0 gives s = 1.  Non-finite amax follows IEEE.
+Scal scale_from_amax(float amax, int fmt) {
+  Scal r;
+  r.amax = amax;
+  if (amax == 0.0f) { r.scale = 1.0f; r.scale_inv = 1.0f; return r; }
+  const float fmax = (float)fp8_format(fmt).maxv;
+  r.scale = fmax / amax;
+  r.scale_inv = 1.0f / r.scale;
+  return r;
+}
+
+float abs_max(const std::vector<double>& v) {
+  float m = 0.0f;
+  bool nan = false;
+  for (double x : v) {
+    if (std::isnan(x)) nan = true;
+    m = std::max(m, (float)std::fabs(x));
+  }
+  return nan ? std::nanf("") : m;
+}
+
+bool finite_scal(const Scal& s) { return std::isfinite(s.amax); }
+
+// A quantized operand: codes, the tensor's scalars, and the decoded codes as
+// doubles (unscaled; the GEMM applies scale_inv of both operands once).
+struct QTensor {
+  std::vector<uint8_t> code;
+  std::vector<double> deq;
+  Scal s;
+};
+
+// In quantized mode: amax -> s -> code = fp8(fl32(v * s)).  Every v must be an
+// fp32 value.  In exact mode the operand passes through with scale_inv = 1.
+QTensor quantize(const std::vector<double>& v, int fmt, bool exact) {
+  QTensor q;
+  if (exact) {
+    q.deq = v;
+    q.s = {abs_max(v), 1.0f, 1.0f};
+    return q;
+  }
+  q.s = scale_from_amax(abs_max(v), fmt);
+  q.code.resize(v.size());
+  q.deq.resize(v.size());
+  for (size_t i = 0; i < v.size(); ++i) {
+    const float p = (float)v[i] * q.s.scale;
+    q.code[i] = fp8_encode(p, fmt);
+    q.deq[i] = fp8_decode(q.code[i], fmt);
+  }
+  return q;
+}
+
+// ----------------------------------------------------------------------------
+// GEMM: C[M,N] = A[M,K] B[K,N] in fp64, row-major operands.  Rows of C may be
+// split over threads; every element's arithmetic and order is the same for
+// any thread count.
+// ----------------------------------------------------------------------------
+void matmul_rows(const double* A, const double* B, double* C, int64_t N, int64_t K,
+                 int64_t r0, int64_t r1) {
+  for (int64_t i = r0; i < r1; ++i) {
+    double* c = C + i * N;
+    std::fill(c, c + N, 0.0);
+    for (int64_t k = 0; k < K; ++k) {
+      const double a = A[i * K + k];
+      const double* b = B + k * N;
+      for (int64_t j = 0; j < N; ++j) c[j] += a * b[j];
+    }
+  }
+}
+
+std::vector<double> matmul(const std::vector<double>& A, const std::vector<double>& B,
+                           int64_t M, int64_t N, int64_t K, int nthreads) {
+  std::vector<double> C((size_t)(M * N));
+  nthreads = std::max(1, std::min<int>(nthreads, (int)std::max<int64_t>(M, 1)));
+  if (nthreads == 1) {
+    matmul_rows(A.data(), B.data(), C.data(), N, K, 0, M);
+    return C;
+  }
+  std::vector<std::thread> pool;
+  for (int t = 0; t < nthreads; ++t) {
+    int64_t r0 = M * t / nthreads, r1 = M * (t + 1) / nthreads;
+    pool.emplace_back(matmul_rows, A.data(), B.data(), C.data(), N, K, r0, r1);
+  }
+  for (auto& th : pool) th.join();
+  return C;
+}
+
+std::vector<double> transpose(const std::vector<double>& X, int64_t R, int64_t Cn) {
+  std::vector<double> Y((size_t)(R * Cn));
+  for (int64_t r = 0; r < R; ++r)
+    for (int64_t c = 0; c < Cn; ++c) Y[c * R + r] = X[r * Cn + c];
+  return Y;
+}
+
+// ----------------------------------------------------------------------------
+// RMSNorm forward
+// ----------------------------------------------------------------------------
+// Pairwise (recursive halving) sum in fp32: a range of length n > 1 is split
+// at the largest power of two below n and the two halves are added.
+float pairwise_sum(const float* v, int64_t n) {
+  if (n == 0) return 0.0f;
+  if (n == 1) return v[0];
+  int64_t m = 1;
+  while (m * 2 < n) m *= 2;
+  return pairwise_sum(v, m) + pairwise_sum(v + m, n - m);
+}
+
+// n = (x * rstd) * g with rstd = 1/sqrt(mean(x^2) + eps).
+// Quantized mode (all fp32, one rounding per op): sum of squares by pairwise
+// summation, mean = S/d, rstd = 1/sqrt(mean + eps).  Exact mode: fp64.
+void rmsnorm_fwd(const std::vector<double>& x, const std::vector<double>& g, int64_t T, int64_t d,
+                 float eps, bool exact, std::vector<double>& n, std::vector<double>& rstd) {
+  n.assign((size_t)(T * d), 0.0);
+  rstd.assign((size_t)T, 0.0);
+  std::vector<float> sq((size_t)d);
+  for (int64_t t = 0; t < T; ++t) {
+    const double* xr = &x[t * d];
+    if (!exact) {
+      for (int64_t j = 0; j < d; ++j) sq[j] = (float)xr[j] * (float)xr[j];
+      const float S = pairwise_sum(sq.data(), d);
+      const float mean = S / (float)d;
+      const float ms = mean + eps;
+      const float rs = 1.0f / std::sqrt(ms);
+      rstd[t] = rs;
+      for (int64_t j = 0; j < d; ++j) n[t * d + j] = ((float)xr[j] * rs) * (float)g[j];
+    } else {
+      double S = 0.0;
+      for (int64_t j = 0; j < d; ++j) S += xr[j] * xr[j];
+      const double rs = 1.0 / std::sqrt(S / (double)d + (double)eps);
+      rstd[t] = rs;
+      for (int64_t j = 0; j < d; ++j) n[t * d + j] = xr[j] * rs * g[j];
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// SwiGLU forward: a = silu(gate) * up, silu(h) = h / (1 + e^-h).
+// H is [T, 2f] with the gate half in columns [0, f) and the up half in [f, 2f).
+// Quantized mode: fp32, e = exp_ref(-h), den = 1 + e, sil = h / den, a = sil*u.
+// ----------------------------------------------------------------------------
+std::vector<double> swiglu_fwd(const std::vector<double>& H, int64_t T, int64_t f, bool exact) {
+  std::vector<double> a((size_t)(T * f));
+  for (int64_t t = 0; t < T; ++t)
+    for (int64_t j = 0; j < f; ++j) {
+      const double h = H[t * 2 * f + j], u = H[t * 2 * f + f + j];
+      if (!exact) {
+        const float hf = (float)h, uf = (float)u;
+        const float e = exp_ref(-hf);
+        const float den = 1.0f + e;
+        const float sil = hf / den;
+        a[t * f + j] = sil * uf;
+      } else {
+        a[t * f + j] = h / (1.0 + std::exp(-h)) * u;
+      }
+    }
+  return a;
+}
+
+// ----------------------------------------------------------------------------
+// The MLP block.  Forward (LLMQ §1, §3, §3.1; FastML report):
+//   Wgu8 = q(W_gu), Wd8 = q(W_d)                         E4M3, per tensor
+//   n = RMSNorm(x) * g ; n8 = q(n)                       E4M3
+//   H = bf16(alpha1 * n8 @ Wgu8)                         [T, 2f] gate | up
+//   a = silu(H_gate) * H_up ; a8 = q(a)                  E4M3
+//   y = bf16(x + alpha2 * a8 @ Wd8)                      residual
+// Backward (straight-through quantizers; gradients E5M2 per LLMQ §5 Fig. 2):
+//   dY8 = q5(dY)
+//   dA  = alpha3 * dY8 @ Wd8^T                           (fp32 in registers on a GPU)
+//   dH_gate = dA * up * s * (1 + h (1 - s)), dH_up = dA * silu(h), s = sigmoid(h)
+//   dH = bf16(dH) ; dH8 = q5(dH)
+//   dW_d  = alpha4 * a8^T @ dY8                          fp32
+//   dN    = alpha5 * dH8 @ Wgu8^T                        fp32
+//   dW_gu = alpha6 * n8^T @ dH8                          fp32
+//   nh = x * rstd ; u = dN * g
+//   dX = bf16(dY + rstd * (u - nh * mean_j(u * nh))) ; dg = sum_t dN * nh
+// ----------------------------------------------------------------------------
+struct BlockIO {
+  int64_t T, d, f;
+  float eps;
+  int exact;
+  int nthreads;
+  // inputs, [T,d] [d] [d,2f] [f,d] (and dY [T,d] for backward), as doubles
+  const double* x; const double* g; const double* Wgu; const double* Wd; const double* dY;
+  // forward outputs (doubles hold the stored value: bf16 / fp32 / decoded code)
+  double* y; double* H; double* rstd;
+  uint8_t* Wgu8; uint8_t* Wd8; uint8_t* n8; uint8_t* a8;
+  float* scal_fwd;   // 4 x (amax, scale, scale_inv): W_gu, W_d, n, a
+  // backward outputs
+  double* dX; double* dWgu; double* dWd; double* dg; double* dN; double* dH;
+  uint8_t* dY8; uint8_t* dH8;
+  float* scal_bwd;   // 2 x (amax, scale, scale_inv): dY, dH
+};
+
+void put_scal(float* dst, const Scal& s) { dst[0] = s.amax; dst[1] = s.scale; dst[2] = s.scale_inv; }
+
+template <class T> void put(T* dst, const std::vector<T>& v) {
+  if (dst) std::copy(v.begin(), v.end(), dst);
+}
+
+struct FwdState {
+  QTensor Wgu, Wd, n, a;
+  std::vector<double> nval, rstd, H, y;
+  int status = 0;
+};
+
+// status bit 1: a tensor's absmax was not finite
+FwdState block_forward(const BlockIO& io) {
+  const int64_t T = io.T, d = io.d, f = io.f;
+  const bool ex = io.exact != 0;
+  FwdState S;
+  std::vector<double> x(io.x, io.x + T * d), g(io.g, io.g + d);
+  std::vector<double> Wgu(io.Wgu, io.Wgu + d * 2 * f), Wd(io.Wd, io.Wd + f * d);
+
+  S.Wgu = quantize(Wgu, FMT_E4M3, ex);
+  S.Wd = quantize(Wd, FMT_E4M3, ex);
+  rmsnorm_fwd(x, g, T, d, io.eps, ex, S.nval, S.rstd);
+  S.n = quantize(S.nval, FMT_E4M3, ex);
+
+  const double alpha1 = ex ? 1.0 : (double)(S.n.s.scale_inv * S.Wgu.s.scale_inv);
+  std::vector<double> acc1 = matmul(S.n.deq, S.Wgu.deq, T, 2 * f, d, io.nthreads);
+  S.H.resize(acc1.size());
+  for (size_t i = 0; i < acc1.size(); ++i) S.H[i] = ex ? acc1[i] : to_bf16(alpha1 * acc1[i]);
+
+  S.a = quantize(swiglu_fwd(S.H, T, f, ex), FMT_E4M3, ex);
+
+  const double alpha2 = ex ? 1.0 : (double)(S.a.s.scale_inv * S.Wd.s.scale_inv);
+  std::vector<double> acc2 = matmul(S.a.deq, S.Wd.deq, T, d, f, io.nthreads);
+  S.y.resize(acc2.size());
+  for (size_t i = 0; i < acc2.size(); ++i)
+    S.y[i] = ex ? x[i] + acc2[i] : to_bf16(x[i] + alpha2 * acc2[i]);
+
+  for (const Scal* s : {&S.Wgu.s, &S.Wd.s, &S.n.s, &S.a.s})
+    if (!finite_scal(*s)) S.status |= 1;
+  return S;
+}
+
+void write_forward(const BlockIO& io, const FwdState& S) {
+  put(io.y, S.y);
+  put(io.H, S.H);
+  put(io.rstd, S.rstd);
+  if (!io.exact) {
+    put(io.Wgu8, S.Wgu.code); put(io.Wd8, S.Wd.code);
+    put(io.n8, S.n.code); put(io.a8, S.a.code);
+  }
+  if (io.scal_fwd) {
+    put_scal(io.scal_fwd + 0, S.Wgu.s); put_scal(io.scal_fwd + 3, S.Wd.s);
+    put_scal(io.scal_fwd + 6, S.n.s); put_scal(io.scal_fwd + 9, S.a.s);
+  }
+}
+
+int block_backward(const BlockIO& io, const FwdState& S) {
+  const int64_t T = io.T, d = io.d, f = io.f;
+  const bool ex = io.exact != 0;
+  int status = S.status;
+  std::vector<double> x(io.x, io.x + T * d), g(io.g, io.g + d), dY(io.dY, io.dY + T * d);
+
+  QTensor dY8 = quantize(dY, FMT_E5M2, ex);
+
+  // dA = alpha3 * dY8 @ Wd8^T   ([T,d] x [d,f])
+  const double alpha3 = ex ? 1.0 : (double)(dY8.s.scale_inv * S.Wd.s.scale_inv);
+  std::vector<double> WdT = transpose(S.Wd.deq, f, d);
+  std::vector<double> dA = matmul(dY8.deq, WdT, T, f, d, io.nthreads);
+  for (double& v : dA) v *= alpha3;
+
+  std::vector<double> dH((size_t)(T * 2 * f));
+  for (int64_t t = 0; t < T; ++t)
+    for (int64_t j = 0; j < f; ++j) {
+      const double h = S.H[t * 2 * f + j], u = S.H[t * 2 * f + f + j];
+      const double da = dA[t * f + j];
+      const double sg = 1.0 / (1.0 + std::exp(-h));
+      double dg_ = da * u * sg * (1.0 + h * (1.0 - sg));
+      double du_ = da * h * sg;
+      dH[t * 2 * f + j] = ex ? dg_ : to_bf16(dg_);
+      dH[t * 2 * f + f + j] = ex ? du_ : to_bf16(du_);
+    }
+  QTensor dH8 = quantize(dH, FMT_E5M2, ex);
+
+  auto out32 = [&](double v) { return ex ? v : (double)(float)v; };
+
+  // dW_d = alpha4 * a8^T @ dY8   ([f,T] x [T,d])
+  const double alpha4 = ex ? 1.0 : (double)(S.a.s.scale_inv * dY8.s.scale_inv);
+  std::vector<double> dWd = matmul(transpose(S.a.deq, T, f), dY8.deq, f, d, T, io.nthreads);
+  for (double& v : dWd) v = out32(alpha4 * v);
+
+  // dN = alpha5 * dH8 @ Wgu8^T   ([T,2f] x [2f,d])
+  const double alpha5 = ex ? 1.0 : (double)(dH8.s.scale_inv * S.Wgu.s.scale_inv);
+  std::vector<double> dN = matmul(dH8.deq, transpose(S.Wgu.deq, d, 2 * f), T, d, 2 * f, io.nthreads);
+  for (double& v : dN) v = out32(alpha5 * v);
+
+  // dW_gu = alpha6 * n8^T @ dH8  ([d,T] x [T,2f])
+  const double alpha6 = ex ? 1.0 : (double)(S.n.s.scale_inv * dH8.s.scale_inv);
+  std::vector<double> dWgu = matmul(transpose(S.n.deq, T, d), dH8.deq, d, 2 * f, T, io.nthreads);
+  for (double& v : dWgu) v = out32(alpha6 * v);
+
+  // RMSNorm backward + residual
+  std::vector<double> dX((size_t)(T * d)), dgv((size_t)d, 0.0);
+  for (int64_t t = 0; t < T; ++t) {
+    const double rs = S.rstd[t];
+    double dot = 0.0;
+    for (int64_t j = 0; j < d; ++j) {
+      const double nh = x[t * d + j] * rs;
+      dot += dN[t * d + j] * g[j] * nh;
+    }
+    dot /= (double)d;
+    for (int64_t j = 0; j < d; ++j) {
+      const double nh = x[t * d + j] * rs;
+      const double u = dN[t * d + j] * g[j];
+      const double v = dY[t * d + j] + rs * (u - nh * dot);
+      dX[t * d + j] = ex ? v : to_bf16(v);
+      dgv[j] += dN[t * d + j] * nh;
+    }
+  }
+  if (!ex) for (double& v : dgv) v = (double)(float)v;
+
+  for (const Scal* s : {&dY8.s, &dH8.s})
+    if (!finite_scal(*s)) status |= 1;
+
+  put(io.dX, dX); put(io.dWgu, dWgu); put(io.dWd, dWd); put(io.dg, dgv);
+  put(io.dN, dN); put(io.dH, dH);
+  if (!ex) { put(io.dY8, dY8.code); put(io.dH8, dH8.code); }
+  if (io.scal_bwd) { put_scal(io.scal_bwd + 0, dY8.s); put_scal(io.scal_bwd + 3, dH8.s); }
+  return status;
+}
+
+std::vector<double> load_input(const void* x, int dtype, int64_t n) {
+  // dtype 0: bf16 bits, 1: fp32
+  std::vector<double> v((size_t)n);
+  if (dtype == 0) {
+    const uint16_t* p = (const uint16_t*)x;
+    for (int64_t i = 0; i < n; ++i) v[i] = bf16_value(p[i]);
+  } else {
+    const float* p = (const float*)x;
+    for (int64_t i = 0; i < n; ++i) v[i] = (double)p[i];
+  }
+  return v;
+}
+
+}  // namespace
+
+// ============================================================================
+// C entry points (ctypes).  Status: 0 ok, bit 1 = non-finite absmax.
+// ============================================================================
+extern "C" {
+
+int fo_abi_version() { return 1; }
+
+uint8_t fo_fp8_encode(float v, int fmt) { return fp8_encode(v, fmt); }
+double fo_fp8_decode(uint8_t c, int fmt) { return fp8_decode(c, fmt); }
+
+void fo_fp8_encode_n(const float* v, int64_t n, int fmt, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = fp8_encode(v[i], fmt);
+}
+void fo_fp8_decode_n(const uint8_t* c, int64_t n, int fmt, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = fp8_decode(c[i], fmt);
+}
+void fo_bf16_round_n(const double* v, int64_t n, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = to_bf16_bits(v[i]);
+}
+
+float fo_exp_ref(float x) { return exp_ref(x); }
+void fo_exp_ref_n(const float* x, int64_t n, float* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = exp_ref(x[i]);
+}
+
+float fo_pairwise_sum(const float* v, int64_t n) { return pairwise_sum(v, n); }
+
+// Per-tensor absmax quantization of n values (dtype 0 bf16 bits, 1 fp32).
+// scal3 = (amax, scale, scale_inv).
+int fo_quantize_absmax(const void* x, int dtype, int64_t n, int fmt, uint8_t* q, float* scal3) {
+  QTensor t = quantize(load_input(x, dtype, n), fmt, false);
+  std::copy(t.code.begin(), t.code.end(), q);
+  put_scal(scal3, t.s);
+  return finite_scal(t.s) ? 0 : 1;
+}
+
+// RMSNorm (gain g, epsilon eps) followed by per-tensor E4M3 quantization.
+int fo_rmsnorm_quant(const uint16_t* x, const uint16_t* g, int64_t T, int64_t d, float eps,
+                     uint8_t* q, float* scal3, float* rstd) {
+  std::vector<double> n, rs;
+  rmsnorm_fwd(load_input(x, 0, T * d), load_input(g, 0, d), T, d, eps, false, n, rs);
+  QTensor t = quantize(n, FMT_E4M3, false);
+  std::copy(t.code.begin(), t.code.end(), q);
+  put_scal(scal3, t.s);
+  for (int64_t i = 0; i < T; ++i) rstd[i] = (float)rs[i];
+  return finite_scal(t.s) ? 0 : 1;
+}
+
+// SwiGLU of H [T, 2f] (gate | up, bf16 bits) followed by per-tensor quantization.
+int fo_swiglu_quant(const uint16_t* H, int64_t T, int64_t f, int fmt, uint8_t* q, float* scal3) {
+  QTensor t = quantize(swiglu_fwd(load_input(H, 0, T * 2 * f), T, f, false), fmt, false);
+  std::copy(t.code.begin(), t.code.end(), q);
+  put_scal(scal3, t.s);
+  return finite_scal(t.s) ? 0 : 1;
+}
+
+// C = alpha * op(A) op(B) (+ residual), alpha = fl32(sinvA * sinvB).
+//   layout 0 NN: A [M,K], B [K,N];  1 NT: A [M,K], B [N,K];  2 TN: A [K,M], B [K,N]
+// out_dtype 0: bf16 bits (with optional bf16 residual [M,N]), 1: fp32, 2: fp64
+// (the unrounded alpha * acc, for tests).
+int fo_gemm_scaled(int layout, int64_t M, int64_t N, int64_t K, const uint8_t* A, int fmtA,
+                   const uint8_t* B, int fmtB, float sinvA, float sinvB, const uint16_t* residual,
+                   int out_dtype, void* C, int nthreads) {
+  std::vector<double> a((size_t)(M * K)), b((size_t)(K * N));
+  for (int64_t i = 0; i < M; ++i)
+    for (int64_t k = 0; k < K; ++k)
+      a[i * K + k] = fp8_decode(layout == 2 ? A[k * M + i] : A[i * K + k], fmtA);
+  for (int64_t k = 0; k < K; ++k)
+    for (int64_t j = 0; j < N; ++j)
+      b[k * N + j] = fp8_decode(layout == 1 ? B[j * K + k] : B[k * N + j], fmtB);
+  std::vector<double> acc = matmul(a, b, M, N, K, nthreads);
+  const double alpha = (double)(sinvA * sinvB);
+  for (int64_t i = 0; i < M * N; ++i) {
+    double v = alpha * acc[i];
+    if (out_dtype == 0) {
+      if (residual) v += bf16_value(residual[i]);
+      ((uint16_t*)C)[i] = to_bf16_bits(v);
+    } else if (out_dtype == 1) {
+      ((float*)C)[i] = (float)v;
+    } else {
+      ((double*)C)[i] = v;
+    }
+  }
+  return 0;
+}
+
+// Block forward / backward.  The struct layout is mirrored by oracle/__init__.py.
+int fo_block_forward(const BlockIO* io) {
+  FwdState S = block_forward(*io);
+  write_forward(*io, S);
+  return S.status;
+}
+
+int fo_block_forward_backward(const BlockIO* io) {
+  FwdState S = block_forward(*io);
+  write_forward(*io, S);
+  return block_backward(*io, S);
+}
+
+}  // extern "C"
