@@ -1,0 +1,270 @@
+"""GB300 (sm_103a) FP8 transformer-block pipeline with just-in-time per-tensor absmax scaling.
+
+Thin Python binding of the C-ABI library ``libfp8q.so`` (``include/fp8q.h``).
+Every function here only marshals torch tensors (device memory, the current
+stream) into the C calls; all arithmetic runs in the library's CUDA kernels.
+There is no CPU fallback: without the built library, the first call raises.
+
+Build the library with ``python -m fp8_absmax_reduce_gb300.build``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+
+import torch
+
+from . import build as _build_mod
+
+E4M3, E5M2 = 0, 1
+BF16, F32 = 0, 1
+NN, NT, TN = 0, 1, 2
+STATUS_NONFINITE, STATUS_TIMEOUT = 0x1, 0x2
+
+_LIB_PATH = _build_mod.LIB
+
+
+class Fp8qError(RuntimeError):
+    pass
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"libfp8q.so is not built ({_LIB_PATH}); run python -m fp8_absmax_reduce_gb300.build")
+    L = ctypes.CDLL(_LIB_PATH)
+    vp, i64, f32, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int, ctypes.c_size_t
+    L.fp8_quantize_absmax_workspace_size.restype = sz
+    L.fp8_quantize_absmax_workspace_size.argtypes = [i64]
+    L.fp8_quantize_absmax.argtypes = [vp, i32, i64, i32, vp, vp, vp, sz, vp]
+    L.fp8_gemm_scaled.argtypes = [i32, i64, i64, i64, vp, i32, i64, vp, i32, i64, vp, vp, vp, i32, i64, vp, i64, vp]
+    L.rmsnorm_quant_workspace_size.restype = sz
+    L.rmsnorm_quant_workspace_size.argtypes = [i64, i64]
+    L.rmsnorm_quant.argtypes = [vp, vp, i64, i64, f32, vp, vp, vp, vp, sz, vp]
+    L.swiglu_quant_workspace_size.restype = sz
+    L.swiglu_quant_workspace_size.argtypes = [i64, i64]
+    L.swiglu_quant.argtypes = [vp, i64, i64, i32, vp, vp, vp, sz, vp]
+    L.mlp_block_workspace_size.restype = sz
+    L.mlp_block_workspace_size.argtypes = [i64, i64, i64, i32]
+    L.mlp_block_fwd.argtypes = [ctypes.POINTER(FP8QMlp), vp, sz, vp]
+    L.mlp_block_bwd.argtypes = [ctypes.POINTER(FP8QMlp), vp, sz, vp]
+    L.fp8q_get_status.argtypes = [i32]
+    L.fp8q_status_string.restype = ctypes.c_char_p
+    L.fp8q_status_string.argtypes = [i32]
+    L.fp8q_last_launch_count.restype = i32
+    return L
+
+
+class FP8QMlp(ctypes.Structure):
+    """Mirror of ``fp8q_mlp`` in include/fp8q.h."""
+    _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int64), ("f", ctypes.c_int64), ("eps", ctypes.c_float)] + [
+        (name, ctypes.c_void_p) for name in (
+            "x", "g", "W_gu", "W_d", "y", "W_gu8", "W_d8", "n8", "rstd", "H", "a8", "scal",
+            "dY", "dX", "dW_gu", "dW_d", "dg", "dY8", "dH", "dH8", "dN")
+    ]
+
+
+_lib_handle = None
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libfp8q.so (once).  Raises ImportError when it has not been built."""
+    global _lib_handle
+    if _lib_handle is None:
+        _lib_handle = _load()
+    return _lib_handle
+
+
+class _LazyLib:
+    def __getattr__(self, name):
+        return getattr(load_library(), name)
+
+
+lib = _LazyLib()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(name: str, rc: int):
+    if rc != 0:
+        raise Fp8qError(f"{name}: {lib.fp8q_status_string(rc).decode()} (status {rc})")
+
+
+def _ws(nbytes: int, device, ws=None):
+    if nbytes == 0:
+        return None
+    if ws is not None:
+        if ws.numel() * ws.element_size() < nbytes:
+            raise ValueError("workspace too small")
+        return ws
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _dev(t: torch.Tensor):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("tensors must be contiguous CUDA tensors")
+    return t.device
+
+
+# ---------------------------------------------------------------------------
+def fp8_quantize_absmax(x: torch.Tensor, fmt: int = E4M3, q=None, scal=None, ws=None, stream=None):
+    """Per-tensor absmax quantization. Returns (codes uint8 like x, scal float32[3] = amax, scale, scale_inv)."""
+    dev = _dev(x)
+    q = torch.empty(x.shape, dtype=torch.uint8, device=dev) if q is None else q
+    scal = torch.empty(3, dtype=torch.float32, device=dev) if scal is None else scal
+    nb = lib.fp8_quantize_absmax_workspace_size(x.numel())
+    w = _ws(nb, dev, ws)
+    _check("fp8_quantize_absmax", lib.fp8_quantize_absmax(_ptr(x), _dtype_code(x), x.numel(), fmt, _ptr(q),
+                                                          _ptr(scal), _ptr(w), nb, _stream(stream)))
+    return q, scal
+
+
+def fp8_gemm_scaled(layout: int, A: torch.Tensor, fmtA: int, B: torch.Tensor, fmtB: int, sinvA: torch.Tensor,
+                    sinvB: torch.Tensor, out_dtype=torch.bfloat16, residual=None, C=None, stream=None):
+    """C = (sinvA*sinvB) op(A) op(B) (+ residual).  NN: A [M,K], B [K,N]; NT: A [M,K], B [N,K];
+    TN: A [K,M], B [K,N].  sinvA/sinvB: one-element float32 device tensors (a scal[2:3] slice)."""
+    dev = _dev(A)
+    _dev(B)
+    if layout == TN:
+        K, M = A.shape
+    else:
+        M, K = A.shape
+    N = B.shape[0] if layout == NT else B.shape[1]
+    lda, ldb = A.shape[1], B.shape[1]
+    out_code = {torch.bfloat16: BF16, torch.float32: F32}[out_dtype]
+    C = torch.empty((M, N), dtype=out_dtype, device=dev) if C is None else C
+    ldr = residual.shape[1] if residual is not None else 0
+    _check("fp8_gemm_scaled", lib.fp8_gemm_scaled(layout, M, N, K, _ptr(A), fmtA, lda, _ptr(B), fmtB, ldb,
+                                                  _ptr(sinvA), _ptr(sinvB), _ptr(C), out_code, C.shape[1],
+                                                  _ptr(residual), ldr, _stream(stream)))
+    return C
+
+
+def rmsnorm_quant(x: torch.Tensor, g: torch.Tensor, eps: float = 1e-6, q=None, scal=None, rstd=None, ws=None,
+                  stream=None):
+    """RMSNorm + E4M3 quantization. Returns (codes [T,d], scal[3], rstd[T])."""
+    dev = _dev(x)
+    T, d = x.shape
+    q = torch.empty((T, d), dtype=torch.uint8, device=dev) if q is None else q
+    scal = torch.empty(3, dtype=torch.float32, device=dev) if scal is None else scal
+    rstd = torch.empty(T, dtype=torch.float32, device=dev) if rstd is None else rstd
+    nb = lib.rmsnorm_quant_workspace_size(T, d)
+    w = _ws(nb, dev, ws)
+    _check("rmsnorm_quant", lib.rmsnorm_quant(_ptr(x), _ptr(g), T, d, eps, _ptr(q), _ptr(scal), _ptr(rstd),
+                                              _ptr(w), nb, _stream(stream)))
+    return q, scal, rstd
+
+
+def swiglu_quant(H: torch.Tensor, fmt: int = E4M3, q=None, scal=None, ws=None, stream=None):
+    """SwiGLU of H [T,2f] (gate | up) + per-tensor quantization. Returns (codes [T,f], scal[3])."""
+    dev = _dev(H)
+    T, f2 = H.shape
+    f = f2 // 2
+    q = torch.empty((T, f), dtype=torch.uint8, device=dev) if q is None else q
+    scal = torch.empty(3, dtype=torch.float32, device=dev) if scal is None else scal
+    nb = lib.swiglu_quant_workspace_size(T, f)
+    w = _ws(nb, dev, ws)
+    _check("swiglu_quant", lib.swiglu_quant(_ptr(H), T, f, fmt, _ptr(q), _ptr(scal), _ptr(w), nb, _stream(stream)))
+    return q, scal
+
+
+# ---------------------------------------------------------------------------
+@dataclasses.dataclass
+class MlpBuffers:
+    """Caller-owned device buffers of one MLP block (see fp8q_mlp in include/fp8q.h)."""
+    T: int
+    d: int
+    f: int
+    eps: float
+    x: torch.Tensor
+    g: torch.Tensor
+    W_gu: torch.Tensor
+    W_d: torch.Tensor
+    y: torch.Tensor
+    W_gu8: torch.Tensor
+    W_d8: torch.Tensor
+    n8: torch.Tensor
+    rstd: torch.Tensor
+    H: torch.Tensor
+    a8: torch.Tensor
+    scal: torch.Tensor
+    dY: torch.Tensor | None = None
+    dX: torch.Tensor | None = None
+    dW_gu: torch.Tensor | None = None
+    dW_d: torch.Tensor | None = None
+    dg: torch.Tensor | None = None
+    dY8: torch.Tensor | None = None
+    dH: torch.Tensor | None = None
+    dH8: torch.Tensor | None = None
+    dN: torch.Tensor | None = None
+    ws: torch.Tensor | None = None
+
+    @staticmethod
+    def allocate(T: int, d: int, f: int, device="cuda", backward: bool = True, eps: float = 1e-6,
+                 keep_intermediates: bool = False) -> "MlpBuffers":
+        e = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)
+        b = MlpBuffers(
+            T=T, d=d, f=f, eps=eps,
+            x=e((T, d), torch.bfloat16), g=e((d,), torch.bfloat16), W_gu=e((d, 2 * f), torch.bfloat16),
+            W_d=e((f, d), torch.bfloat16), y=e((T, d), torch.bfloat16), W_gu8=e((d, 2 * f), torch.uint8),
+            W_d8=e((f, d), torch.uint8), n8=e((T, d), torch.uint8), rstd=e((T,), torch.float32),
+            H=e((T, 2 * f), torch.bfloat16), a8=e((T, f), torch.uint8), scal=torch.zeros((6, 3), device=device))
+        if backward:
+            b.dY = e((T, d), torch.bfloat16)
+            b.dX = e((T, d), torch.bfloat16)
+            b.dW_gu = e((d, 2 * f), torch.float32)
+            b.dW_d = e((f, d), torch.float32)
+            b.dg = e((d,), torch.float32)
+            if keep_intermediates:
+                b.dY8 = e((T, d), torch.uint8)
+                b.dH = e((T, 2 * f), torch.bfloat16)
+                b.dH8 = e((T, 2 * f), torch.uint8)
+                b.dN = e((T, d), torch.float32)
+        nb = lib.mlp_block_workspace_size(T, d, f, int(backward))
+        b.ws = torch.empty(nb, dtype=torch.uint8, device=device)
+        return b
+
+    def struct(self) -> FP8QMlp:
+        s = FP8QMlp(T=self.T, d=self.d, f=self.f, eps=self.eps)
+        for name, _ in FP8QMlp._fields_[4:]:
+            t = getattr(self, name)
+            setattr(s, name, None if t is None else t.data_ptr())
+        return s
+
+
+def mlp_block_fwd(b: MlpBuffers, stream=None):
+    s = b.struct()
+    _check("mlp_block_fwd", lib.mlp_block_fwd(ctypes.byref(s), _ptr(b.ws), b.ws.numel(), _stream(stream)))
+
+
+def mlp_block_bwd(b: MlpBuffers, stream=None):
+    s = b.struct()
+    _check("mlp_block_bwd", lib.mlp_block_bwd(ctypes.byref(s), _ptr(b.ws), b.ws.numel(), _stream(stream)))
+
+
+def get_status(clear: bool = False) -> int:
+    """Device status bits (STATUS_NONFINITE, STATUS_TIMEOUT); synchronize the stream first."""
+    v = lib.fp8q_get_status(int(clear))
+    if v < 0:
+        raise Fp8qError("fp8q_get_status failed")
+    return v
+
+
+def last_launch_count() -> int:
+    return lib.fp8q_last_launch_count()

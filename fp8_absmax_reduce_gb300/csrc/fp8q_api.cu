@@ -1,0 +1,555 @@
+// C ABI of the FP8 block pipeline (declared in include/fp8q.h): argument
+// validation, workspace carving and the forward/backward orchestration of the
+// MLP block.  Every call only enqueues kernels on the caller's stream.
+#include "fp8q.h"
+#include "fp8q_internal.h"
+
+#include <mutex>
+#include <vector>
+
+namespace {
+
+using namespace fp8q;
+
+__device__ unsigned g_status_word;
+
+thread_local int t_last_launches = 0;
+
+// ---- kernel-level trace (benchmarks) ------------------------------------------
+enum Kind {
+  kKAbsmaxPartial = 0, kKQuantCast, kKRmsnormStats, kKRmsnormCast, kKSwigluAmax, kKSwigluCast, kKRmsnormBwd,
+  kKGemmGateUp, kKGemmDown, kKGemmDownDgrad, kKGemmDownWgrad, kKGemmGateUpDgrad, kKGemmGateUpWgrad, kKGemm,
+  kKCount
+};
+const char* const kKindNames[kKCount] = {
+    "absmax_partial", "quant_cast", "rmsnorm_stats", "rmsnorm_cast", "swiglu_amax", "swiglu_cast",
+    "rmsnorm_bwd", "gemm_gate_up_swiglu", "gemm_down_residual", "gemm_down_dgrad_swiglu_bwd",
+    "gemm_down_wgrad", "gemm_gate_up_dgrad", "gemm_gate_up_wgrad", "gemm"};
+
+struct Trace {
+  bool on = false;
+  std::vector<cudaEvent_t> ev;
+  std::vector<int> kinds;
+  int n = 0;
+};
+thread_local Trace t_trace;
+
+struct TraceScope {
+  cudaStream_t s;
+  bool active;
+  TraceScope(cudaStream_t st, int kind) : s(st), active(false) {
+    Trace& t = t_trace;
+    if (t.on && t.n < (int)t.kinds.size()) {
+      active = true;
+      t.kinds[t.n] = kind;
+      cudaEventRecord(t.ev[2 * t.n], s);
+    }
+  }
+  ~TraceScope() {
+    if (active) {
+      cudaEventRecord(t_trace.ev[2 * t_trace.n + 1], s);
+      ++t_trace.n;
+    }
+  }
+};
+
+struct DevInfo {
+  int num_sms = 0;
+  unsigned* status = nullptr;
+};
+
+int device_info(DevInfo* out) {
+  static std::mutex mu;
+  static DevInfo cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8Q_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  DevInfo& d = cache[dev];
+  if (!d.status) {
+    int sms = 0;
+    void* st = nullptr;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FP8Q_ERR_CUDA;
+    if (cudaGetSymbolAddress(&st, g_status_word) != cudaSuccess) return FP8Q_ERR_CUDA;
+    d.num_sms = sms;
+    d.status = static_cast<unsigned*>(st);
+  }
+  *out = d;
+  return FP8Q_OK;
+}
+
+struct Ctx {
+  Launch L;
+  int launches = 0;
+};
+
+int make_ctx(Ctx* c, fp8q_stream stream) {
+  DevInfo d;
+  int e = device_info(&d);
+  if (e) return e;
+  c->L.stream = static_cast<cudaStream_t>(stream);
+  c->L.status = d.status;
+  c->L.num_sms = d.num_sms;
+  c->L.launches = &c->launches;
+  return FP8Q_OK;
+}
+
+inline bool al16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
+inline size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
+
+// Sequential carve-out of 256-byte aligned pieces from the caller's workspace.
+struct Carver {
+  uint8_t* base;
+  size_t cap, off = 0;
+  bool ok = true;
+  void* take(size_t bytes) {
+    void* p = base + off;
+    off += round256(bytes);
+    if (off > cap) ok = false;
+    return p;
+  }
+};
+
+constexpr size_t kPartialBytes = sizeof(uint32_t) * kMaxPartials;
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA; }
+
+// One traced kernel step: enqueue `expr` on c.L.stream, return FP8Q_ERR_CUDA on failure.
+#define FP8Q_STEP(kind, expr)                   \
+  do {                                          \
+    TraceScope _ts(c.L.stream, (kind));         \
+    int _st = cuda_status(expr);                \
+    if (_st != FP8Q_OK) return _st;             \
+  } while (0)
+
+int finish(const Ctx& c) {
+  t_last_launches = c.launches;
+  return FP8Q_OK;
+}
+
+int check_ws(const void* ws, size_t ws_bytes, size_t need) {
+  if (need == 0) return FP8Q_OK;
+  if (!ws || ((uintptr_t)ws & 255u) != 0 || ws_bytes < need) return FP8Q_ERR_WORKSPACE;
+  return FP8Q_OK;
+}
+
+// ---- workspace layouts -------------------------------------------------------
+struct MlpWs {
+  uint32_t* part_q;    // quantizer partials
+  uint32_t* part_g;    // GEMM epilogue partials
+  uint8_t* dY8;
+  uint16_t* dH;
+  uint8_t* dH8;
+  float* dN;
+  float* dg_part;
+};
+
+size_t mlp_ws_layout(int64_t T, int64_t d, int64_t f, int backward, uint8_t* base, MlpWs* w) {
+  Carver c{base, ~size_t(0)};
+  MlpWs tmp{};
+  tmp.part_q = (uint32_t*)c.take(kPartialBytes);
+  tmp.part_g = (uint32_t*)c.take(kPartialBytes);
+  if (backward) {
+    tmp.dY8 = (uint8_t*)c.take((size_t)(T * d));
+    tmp.dH = (uint16_t*)c.take((size_t)(T * 2 * f) * 2);
+    tmp.dH8 = (uint8_t*)c.take((size_t)(T * 2 * f));
+    tmp.dN = (float*)c.take((size_t)(T * d) * 4);
+    tmp.dg_part = (float*)c.take((size_t)((T + kBwdRows - 1) / kBwdRows) * (size_t)d * 4);
+  }
+  if (w) *w = tmp;
+  return c.off;
+}
+
+int validate_mlp(const fp8q_mlp* m, bool backward) {
+  if (!m) return FP8Q_ERR_INVALID_ARG;
+  if (m->T < 1 || m->d < 16 || m->f < 16 || m->d % 16 || m->f % 16 || m->d > 8192) return FP8Q_ERR_INVALID_ARG;
+  if (m->T > (int64_t)1 << 24 || m->f > (int64_t)1 << 20) return FP8Q_ERR_INVALID_ARG;
+  const void* must[] = {m->x, m->g, m->W_gu, m->W_d, m->W_gu8, m->W_d8, m->n8, m->rstd, m->H, m->a8, m->scal};
+  for (const void* p : must)
+    if (!al16(p)) return FP8Q_ERR_INVALID_ARG;
+  if (!backward) return al16(m->y) ? FP8Q_OK : FP8Q_ERR_INVALID_ARG;
+  const void* must_b[] = {m->dY, m->dX, m->dW_gu, m->dW_d, m->dg};
+  for (const void* p : must_b)
+    if (!al16(p)) return FP8Q_ERR_INVALID_ARG;
+  const void* opt[] = {m->dY8, m->dH, m->dH8, m->dN};
+  for (const void* p : opt)
+    if (p && !al16(p)) return FP8Q_ERR_INVALID_ARG;
+  return FP8Q_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+// ---------------------------------------------------------------------------
+size_t fp8_quantize_absmax_workspace_size(int64_t n) {
+  (void)n;
+  return round256(kPartialBytes);
+}
+
+int fp8_quantize_absmax(const void* x, fp8q_dtype x_dtype, int64_t n, fp8q_fmt fmt, uint8_t* q, float* scal,
+                        void* ws, size_t ws_bytes, fp8q_stream stream) {
+  if (n < 1 || !al16(x) || !al16(q) || !scal || ((uintptr_t)scal & 3u)) return FP8Q_ERR_INVALID_ARG;
+  if ((x_dtype != FP8Q_BF16 && x_dtype != FP8Q_F32) || (fmt != FP8Q_E4M3 && fmt != FP8Q_E5M2))
+    return FP8Q_ERR_INVALID_ARG;
+  int e = check_ws(ws, ws_bytes, fp8_quantize_absmax_workspace_size(n));
+  if (e) return e;
+  Ctx c;
+  if ((e = make_ctx(&c, stream))) return e;
+  uint32_t* part = static_cast<uint32_t*>(ws);
+  int P = 0;
+  FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(x, (int)x_dtype, n, part, &P, c.L));
+  FP8Q_STEP(kKQuantCast, launch_quant_cast(x, (int)x_dtype, n, (int)fmt, part, P, q, scal, c.L));
+  return finish(c);
+}
+
+// ---------------------------------------------------------------------------
+int fp8_gemm_scaled(fp8q_layout layout, int64_t M, int64_t N, int64_t K, const uint8_t* A, fp8q_fmt fmtA,
+                    int64_t lda, const uint8_t* B, fp8q_fmt fmtB, int64_t ldb, const float* sinvA,
+                    const float* sinvB, void* C, fp8q_dtype out_dtype, int64_t ldc, const void* residual,
+                    int64_t ldr, fp8q_stream stream) {
+  if (M < 1 || N < 1 || K < 1 || M > (1 << 30) || N > (1 << 30) || K > (1 << 30)) return FP8Q_ERR_INVALID_ARG;
+  if (!al16(A) || !al16(B) || !al16(C) || !sinvA || !sinvB) return FP8Q_ERR_INVALID_ARG;
+  if ((fmtA != FP8Q_E4M3 && fmtA != FP8Q_E5M2) || (fmtB != FP8Q_E4M3 && fmtB != FP8Q_E5M2))
+    return FP8Q_ERR_INVALID_ARG;
+  if (out_dtype != FP8Q_BF16 && out_dtype != FP8Q_F32) return FP8Q_ERR_INVALID_ARG;
+  if (layout != FP8Q_NN && layout != FP8Q_NT && layout != FP8Q_TN) return FP8Q_ERR_INVALID_ARG;
+  GemmProblem g{};
+  g.a_mn = layout == FP8Q_TN;
+  g.b_mn = layout != FP8Q_NT;
+  const int64_t a_inner = g.a_mn ? M : K, b_inner = g.b_mn ? N : K;
+  if (a_inner % 16 || b_inner % 16 || lda < a_inner || ldb < b_inner || lda % 16 || ldb % 16)
+    return FP8Q_ERR_INVALID_ARG;
+  if (ldc < N || ldc % 8) return FP8Q_ERR_INVALID_ARG;
+  if (residual) {
+    if (out_dtype != FP8Q_BF16 || !al16(residual) || ldr < N || ldr % 8) return FP8Q_ERR_INVALID_ARG;
+  }
+  Ctx c;
+  int e = make_ctx(&c, stream);
+  if (e) return e;
+  g.M = (int)M;
+  g.N = (int)N;
+  g.K = (int)K;
+  g.A = A;
+  g.lda = lda;
+  g.fmtA = (int)fmtA;
+  g.B = B;
+  g.ldb = ldb;
+  g.fmtB = (int)fmtB;
+  g.b_cols = N;
+  g.sinvA = sinvA;
+  g.sinvB = sinvB;
+  g.epi = residual ? kEpiResidual : kEpiStore;
+  g.out_f32 = out_dtype == FP8Q_F32;
+  g.C = C;
+  g.ldc = ldc;
+  g.R = static_cast<const uint16_t*>(residual);
+  g.ldr = ldr;
+  int P = 0;
+  FP8Q_STEP(kKGemm, launch_gemm(g, &P, c.L));
+  return finish(c);
+}
+
+// ---------------------------------------------------------------------------
+size_t rmsnorm_quant_workspace_size(int64_t T, int64_t d) {
+  (void)T;
+  (void)d;
+  return round256(kPartialBytes);
+}
+
+int rmsnorm_quant(const void* x, const void* g, int64_t T, int64_t d, float eps, uint8_t* q, float* scal,
+                  float* rstd, void* ws, size_t ws_bytes, fp8q_stream stream) {
+  if (T < 1 || d < 16 || d % 16 || d > 8192 || T > ((int64_t)1 << 28)) return FP8Q_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(g) || !al16(q) || !scal || !rstd || !(eps >= 0.0f)) return FP8Q_ERR_INVALID_ARG;
+  int e = check_ws(ws, ws_bytes, rmsnorm_quant_workspace_size(T, d));
+  if (e) return e;
+  Ctx c;
+  if ((e = make_ctx(&c, stream))) return e;
+  uint32_t* part = static_cast<uint32_t*>(ws);
+  int P = 0;
+  FP8Q_STEP(kKRmsnormStats, launch_rmsnorm_stats((const uint16_t*)x, (const uint16_t*)g, T, (int)d, eps, rstd, part, &P, c.L));
+  FP8Q_STEP(kKRmsnormCast, launch_rmsnorm_cast((const uint16_t*)x, (const uint16_t*)g, rstd, T, (int)d, part, P, q, scal, c.L));
+  return finish(c);
+}
+
+// ---------------------------------------------------------------------------
+size_t swiglu_quant_workspace_size(int64_t T, int64_t f) {
+  (void)T;
+  (void)f;
+  return round256(kPartialBytes);
+}
+
+int swiglu_quant(const void* H, int64_t T, int64_t f, fp8q_fmt fmt, uint8_t* q, float* scal, void* ws,
+                 size_t ws_bytes, fp8q_stream stream) {
+  if (T < 1 || f < 16 || f % 16 || f > (1 << 24) || T > ((int64_t)1 << 28)) return FP8Q_ERR_INVALID_ARG;
+  if (!al16(H) || !al16(q) || !scal || (fmt != FP8Q_E4M3 && fmt != FP8Q_E5M2)) return FP8Q_ERR_INVALID_ARG;
+  int e = check_ws(ws, ws_bytes, swiglu_quant_workspace_size(T, f));
+  if (e) return e;
+  Ctx c;
+  if ((e = make_ctx(&c, stream))) return e;
+  uint32_t* part = static_cast<uint32_t*>(ws);
+  int P = 0;
+  FP8Q_STEP(kKSwigluAmax, launch_swiglu_amax((const uint16_t*)H, T, (int)f, part, &P, c.L));
+  FP8Q_STEP(kKSwigluCast, launch_swiglu_cast((const uint16_t*)H, T, (int)f, (int)fmt, part, P, q, scal, c.L));
+  return finish(c);
+}
+
+// ---------------------------------------------------------------------------
+size_t mlp_block_workspace_size(int64_t T, int64_t d, int64_t f, int backward) {
+  return mlp_ws_layout(T, d, f, backward, nullptr, nullptr);
+}
+
+int mlp_block_fwd(const fp8q_mlp* m, void* ws, size_t ws_bytes, fp8q_stream stream) {
+  int e = validate_mlp(m, false);
+  if (e) return e;
+  if ((e = check_ws(ws, ws_bytes, mlp_block_workspace_size(m->T, m->d, m->f, 0)))) return e;
+  Ctx c;
+  if ((e = make_ctx(&c, stream))) return e;
+  MlpWs w;
+  mlp_ws_layout(m->T, m->d, m->f, 0, static_cast<uint8_t*>(ws), &w);
+  const int64_t T = m->T, d = m->d, f = m->f;
+  float* s_wgu = m->scal + 0;
+  float* s_wd = m->scal + 3;
+  float* s_n = m->scal + 6;
+  float* s_a = m->scal + 9;
+  int P = 0;
+  // weights: per-tensor E4M3 (re-quantized every step: weights change every step)
+  FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(m->W_gu, 0, d * 2 * f, w.part_q, &P, c.L));
+  FP8Q_STEP(kKQuantCast, launch_quant_cast(m->W_gu, 0, d * 2 * f, 0, w.part_q, P, m->W_gu8, s_wgu, c.L));
+  FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(m->W_d, 0, f * d, w.part_q, &P, c.L));
+  FP8Q_STEP(kKQuantCast, launch_quant_cast(m->W_d, 0, f * d, 0, w.part_q, P, m->W_d8, s_wd, c.L));
+  // RMSNorm + E4M3
+  FP8Q_STEP(kKRmsnormStats, launch_rmsnorm_stats((const uint16_t*)m->x, (const uint16_t*)m->g, T, (int)d, m->eps, m->rstd,
+                                w.part_q, &P, c.L));
+  FP8Q_STEP(kKRmsnormCast, launch_rmsnorm_cast((const uint16_t*)m->x, (const uint16_t*)m->g, m->rstd, T, (int)d, w.part_q, P,
+                               m->n8, s_n, c.L));
+  // G1: H = bf16(alpha n8 @ W_gu8) with the SwiGLU absmax fused in the epilogue
+  GemmProblem g1{};
+  g1.a_mn = 0;
+  g1.b_mn = 1;
+  g1.M = (int)T;
+  g1.N = (int)f;
+  g1.K = (int)d;
+  g1.A = m->n8;
+  g1.lda = d;
+  g1.fmtA = 0;
+  g1.B = m->W_gu8;
+  g1.ldb = 2 * f;
+  g1.fmtB = 0;
+  g1.b_cols = 2 * f;
+  g1.sinvA = s_n + 2;
+  g1.sinvB = s_wgu + 2;
+  g1.epi = kEpiSwiglu;
+  g1.C = m->H;
+  g1.ldc = 2 * f;
+  g1.amax_partial = w.part_g;
+  FP8Q_STEP(kKGemmGateUp, launch_gemm(g1, &P, c.L));
+  // a8 = q(SwiGLU(H)) from the epilogue's partials
+  FP8Q_STEP(kKSwigluCast, launch_swiglu_cast((const uint16_t*)m->H, T, (int)f, 0, w.part_g, P, m->a8, s_a, c.L));
+  // G2: y = bf16(x + alpha a8 @ W_d8)
+  GemmProblem g2{};
+  g2.a_mn = 0;
+  g2.b_mn = 1;
+  g2.M = (int)T;
+  g2.N = (int)d;
+  g2.K = (int)f;
+  g2.A = m->a8;
+  g2.lda = f;
+  g2.fmtA = 0;
+  g2.B = m->W_d8;
+  g2.ldb = d;
+  g2.fmtB = 0;
+  g2.b_cols = d;
+  g2.sinvA = s_a + 2;
+  g2.sinvB = s_wd + 2;
+  g2.epi = kEpiResidual;
+  g2.C = m->y;
+  g2.ldc = d;
+  g2.R = (const uint16_t*)m->x;
+  g2.ldr = d;
+  FP8Q_STEP(kKGemmDown, launch_gemm(g2, &P, c.L));
+  return finish(c);
+}
+
+int mlp_block_bwd(const fp8q_mlp* m, void* ws, size_t ws_bytes, fp8q_stream stream) {
+  int e = validate_mlp(m, true);
+  if (e) return e;
+  if ((e = check_ws(ws, ws_bytes, mlp_block_workspace_size(m->T, m->d, m->f, 1)))) return e;
+  Ctx c;
+  if ((e = make_ctx(&c, stream))) return e;
+  MlpWs w;
+  mlp_ws_layout(m->T, m->d, m->f, 1, static_cast<uint8_t*>(ws), &w);
+  const int64_t T = m->T, d = m->d, f = m->f;
+  const float* s_wgu = m->scal + 0;
+  const float* s_wd = m->scal + 3;
+  const float* s_n = m->scal + 6;
+  const float* s_a = m->scal + 9;
+  float* s_dy = m->scal + 12;
+  float* s_dh = m->scal + 15;
+  uint8_t* dY8 = m->dY8 ? m->dY8 : w.dY8;
+  uint16_t* dH = m->dH ? (uint16_t*)m->dH : w.dH;
+  uint8_t* dH8 = m->dH8 ? m->dH8 : w.dH8;
+  float* dN = m->dN ? m->dN : w.dN;
+  int P = 0;
+  // dY8 = q5(dY)
+  FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(m->dY, 0, T * d, w.part_q, &P, c.L));
+  FP8Q_STEP(kKQuantCast, launch_quant_cast(m->dY, 0, T * d, 1, w.part_q, P, dY8, s_dy, c.L));
+  // G3 (NT): dA = alpha dY8 @ W_d8^T, SwiGLU backward fused -> dH + absmax partials
+  GemmProblem g3{};
+  g3.a_mn = 0;
+  g3.b_mn = 0;
+  g3.M = (int)T;
+  g3.N = (int)f;
+  g3.K = (int)d;
+  g3.A = dY8;
+  g3.lda = d;
+  g3.fmtA = 1;
+  g3.B = m->W_d8;
+  g3.ldb = d;
+  g3.fmtB = 0;
+  g3.b_cols = f;
+  g3.sinvA = s_dy + 2;
+  g3.sinvB = s_wd + 2;
+  g3.epi = kEpiSwigluBwd;
+  g3.C = dH;
+  g3.ldc = 2 * f;
+  g3.R = (const uint16_t*)m->H;
+  g3.ldr = 2 * f;
+  g3.amax_partial = w.part_g;
+  FP8Q_STEP(kKGemmDownDgrad, launch_gemm(g3, &P, c.L));
+  // dH8 = q5(dH)
+  FP8Q_STEP(kKQuantCast, launch_quant_cast(dH, 0, T * 2 * f, 1, w.part_g, P, dH8, s_dh, c.L));
+  // G4 (TN): dW_d = alpha a8^T @ dY8
+  GemmProblem g4{};
+  g4.a_mn = 1;
+  g4.b_mn = 1;
+  g4.M = (int)f;
+  g4.N = (int)d;
+  g4.K = (int)T;
+  g4.A = m->a8;
+  g4.lda = f;
+  g4.fmtA = 0;
+  g4.B = dY8;
+  g4.ldb = d;
+  g4.fmtB = 1;
+  g4.b_cols = d;
+  g4.sinvA = s_a + 2;
+  g4.sinvB = s_dy + 2;
+  g4.epi = kEpiStore;
+  g4.out_f32 = 1;
+  g4.C = m->dW_d;
+  g4.ldc = d;
+  FP8Q_STEP(kKGemmDownWgrad, launch_gemm(g4, &P, c.L));
+  // G5 (NT): dN = alpha dH8 @ W_gu8^T
+  GemmProblem g5{};
+  g5.a_mn = 0;
+  g5.b_mn = 0;
+  g5.M = (int)T;
+  g5.N = (int)d;
+  g5.K = (int)(2 * f);
+  g5.A = dH8;
+  g5.lda = 2 * f;
+  g5.fmtA = 1;
+  g5.B = m->W_gu8;
+  g5.ldb = 2 * f;
+  g5.fmtB = 0;
+  g5.b_cols = d;
+  g5.sinvA = s_dh + 2;
+  g5.sinvB = s_wgu + 2;
+  g5.epi = kEpiStore;
+  g5.out_f32 = 1;
+  g5.C = dN;
+  g5.ldc = d;
+  FP8Q_STEP(kKGemmGateUpDgrad, launch_gemm(g5, &P, c.L));
+  // G6 (TN): dW_gu = alpha n8^T @ dH8
+  GemmProblem g6{};
+  g6.a_mn = 1;
+  g6.b_mn = 1;
+  g6.M = (int)d;
+  g6.N = (int)(2 * f);
+  g6.K = (int)T;
+  g6.A = m->n8;
+  g6.lda = d;
+  g6.fmtA = 0;
+  g6.B = dH8;
+  g6.ldb = 2 * f;
+  g6.fmtB = 1;
+  g6.b_cols = 2 * f;
+  g6.sinvA = s_n + 2;
+  g6.sinvB = s_dh + 2;
+  g6.epi = kEpiStore;
+  g6.out_f32 = 1;
+  g6.C = m->dW_gu;
+  g6.ldc = 2 * f;
+  FP8Q_STEP(kKGemmGateUpWgrad, launch_gemm(g6, &P, c.L));
+  // RMSNorm backward + residual
+  FP8Q_STEP(kKRmsnormBwd, launch_rmsnorm_bwd(dN, (const uint16_t*)m->x, (const uint16_t*)m->dY, (const uint16_t*)m->g, m->rstd,
+                              T, (int)d, (uint16_t*)m->dX, w.dg_part, m->dg, c.L));
+  return finish(c);
+}
+
+// ---------------------------------------------------------------------------
+int fp8q_get_status(int clear) {
+  DevInfo d;
+  if (device_info(&d)) return -1;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, d.status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
+  if (clear) {
+    const unsigned z = 0;
+    if (cudaMemcpy(d.status, &z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return -1;
+  }
+  return (int)v;
+}
+
+const char* fp8q_status_string(int status) {
+  switch (status) {
+    case FP8Q_OK: return "ok";
+    case FP8Q_ERR_INVALID_ARG: return "invalid argument";
+    case FP8Q_ERR_UNSUPPORTED: return "unsupported";
+    case FP8Q_ERR_CUDA: return "CUDA error";
+    case FP8Q_ERR_TIMEOUT: return "device wait timed out";
+    case FP8Q_ERR_NONFINITE: return "non-finite absmax";
+    case FP8Q_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    default: return "unknown status";
+  }
+}
+
+int fp8q_last_launch_count(void) { return t_last_launches; }
+
+int fp8q_trace_start(int capacity) {
+  Trace& t = t_trace;
+  if (capacity < 1) return FP8Q_ERR_INVALID_ARG;
+  for (cudaEvent_t e : t.ev) cudaEventDestroy(e);
+  t.ev.assign(2 * (size_t)capacity, nullptr);
+  for (auto& e : t.ev)
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      e = nullptr;
+      t.on = false;
+      return FP8Q_ERR_CUDA;
+    }
+  t.kinds.assign((size_t)capacity, -1);
+  t.n = 0;
+  t.on = true;
+  return FP8Q_OK;
+}
+
+int fp8q_trace_stop(void) {
+  t_trace.on = false;
+  return FP8Q_OK;
+}
+
+int fp8q_trace_read(float* ms, int* kinds, int capacity) {
+  Trace& t = t_trace;
+  const int n = t.n < capacity ? t.n : capacity;
+  for (int i = 0; i < n; ++i) {
+    if (cudaEventSynchronize(t.ev[2 * i + 1]) != cudaSuccess) return -1;
+    float v = 0.0f;
+    if (cudaEventElapsedTime(&v, t.ev[2 * i], t.ev[2 * i + 1]) != cudaSuccess) return -1;
+    ms[i] = v;
+    kinds[i] = t.kinds[i];
+  }
+  return n;
+}
+
+const char* fp8q_kernel_name(int kind) { return kind >= 0 && kind < kKCount ? kKindNames[kind] : "unknown"; }
+
+}  // extern "C"

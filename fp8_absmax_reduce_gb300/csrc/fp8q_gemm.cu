@@ -1,0 +1,476 @@
+// Persistent, warp-specialised FP8 GEMM for sm_103a on the 5th-generation
+// tensor cores (tcgen05.mma kind::f8f6f4), with the block pipeline's
+// epilogues fused in (LLMQ §3: non-matmul ops fused around the matmuls;
+// §3.1: quantization fused with the nonlinearity; §4: FP8 matmuls dominate).
+//
+// Tile 128 x 256 x 128 (M x N x K bytes), one CTA per SM, 4-stage TMA ring:
+//   warp 0      TMA producer: A tile 128x128 B and B tile as two 128x128 B
+//               halves (the halves let the gate/up GEMM pair column j of the
+//               gate with column f+j of the up projection inside one tile);
+//   warp 1      MMA issuer: 4 x tcgen05.mma 128x256x32 per stage into one of
+//               two TMEM accumulators (2 x 256 fp32 columns), tcgen05.commit
+//               frees the smem stage / hands the accumulator to the epilogue;
+//   warp 2      TMEM allocation (512 columns) and release;
+//   warps 4..7  epilogue: tcgen05.ld of their 32 TMEM lanes (= 32 rows),
+//               scale by alpha = sinvA * sinvB, fused op, vector stores.
+// Operands may be K-major or MN-major in global memory (NN/NT/TN layouts
+// without transpose copies): TMA boxes are 128 B wide along the contiguous
+// dimension with the 128-byte swizzle, and the UMMA shared-memory descriptors
+// declare the matching major-ness.
+// Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
+// FP8Q_STATUS_TIMEOUT, stops issuing work, drains what it issued, frees TMEM
+// and exits.
+#include "fp8q_common.cuh"
+#include "fp8q_internal.h"
+
+#include <mutex>
+
+namespace fp8q {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+constexpr int kATile = BM * BK;   // 16 KB
+constexpr int kBHalf = 128 * BK;  // 16 KB
+constexpr int kStage = kATile + 2 * kBHalf;
+constexpr int kThreads = 256;
+constexpr int kTmemCols = 512;
+constexpr int kBarOffset = STAGES * kStage;
+constexpr int kSmemBytes = kBarOffset + 256 + 1024;  // + barriers + alignment slack
+constexpr int kGroupM = 16;                          // M tiles per rasterisation group
+
+struct Args {
+  int M, N, K;
+  int m_tiles, n_tiles, k_blocks, num_tiles;
+  int b_step, b_half1;  // B's N coordinate of a tile = nb * b_step (+ b_half1 for the second half)
+  int epi, out_f32;
+  uint32_t idesc;
+  const float* sinvA;
+  const float* sinvB;
+  void* C;
+  int64_t ldc;
+  const uint16_t* R;
+  int64_t ldr;
+  uint32_t* amax_partial;
+  unsigned* status;
+};
+
+__device__ __forceinline__ void tile_coords(int tile, const Args& p, int& mb, int& nb) {
+  const int span = kGroupM * p.n_tiles;
+  const int grp = tile / span;
+  const int first_m = grp * kGroupM;
+  const int gm = min(kGroupM, p.m_tiles - first_m);
+  const int local = tile - grp * span;
+  mb = first_m + local % gm;
+  nb = local / gm;
+}
+
+// ---------------------------------------------------------------------------
+// Epilogue helpers: one thread = one output row, 32 consecutive columns.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    st_v4(dst + 8 * q, make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                                  pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7])));
+}
+__device__ __forceinline__ void load_bf16x32(const uint16_t* src, float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 w = ld_v4(src + 8 * q);
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) { v[8 * q + 2 * k] = bf16_lo(ww[k]); v[8 * q + 2 * k + 1] = bf16_hi(ww[k]); }
+  }
+}
+__device__ __forceinline__ float round_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+// Columns [col, col + ncol) of the chunk are valid (ncol <= 32); the full chunk
+// takes the vector path.
+__device__ __forceinline__ void epi_store(const Args& p, int row, int col, int ncol, const uint32_t (&acc)[32], float alpha) {
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(alpha, __uint_as_float(acc[j]));
+  if (p.epi == kEpiResidual) {
+    const uint16_t* r = p.R + (int64_t)row * p.ldr + col;
+    if (ncol == 32) {
+      float rv[32];
+      load_bf16x32(r, rv);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = __fadd_rn(rv[j], v[j]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < ncol) v[j] = __fadd_rn(__uint_as_float((uint32_t)r[j] << 16), v[j]);
+    }
+  }
+  if (p.out_f32) {
+    float* dst = reinterpret_cast<float*>(p.C) + (int64_t)row * p.ldc + col;
+    if (ncol == 32) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        st_v4(dst + 4 * q, make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
+                                      __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3])));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < ncol) dst[j] = v[j];
+    }
+  } else {
+    uint16_t* dst = reinterpret_cast<uint16_t*>(p.C) + (int64_t)row * p.ldc + col;
+    if (ncol == 32) {
+      store_bf16x32(dst, v);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < ncol) dst[j] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
+    }
+  }
+}
+
+// Gate columns [col, col+ncol) of f, with the matching up columns f + col.
+// H = bf16(alpha * acc); a = silu(H_gate) * H_up; running absmax of a.
+__device__ __forceinline__ void epi_swiglu(const Args& p, int row, int col, int ncol, const uint32_t (&ag)[32],
+                           const uint32_t (&au)[32], float alpha, uint32_t& amax) {
+  float hg[32], hu[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    hg[j] = round_bf16(__fmul_rn(alpha, __uint_as_float(ag[j])));
+    hu[j] = round_bf16(__fmul_rn(alpha, __uint_as_float(au[j])));
+  }
+  uint16_t* hrow = reinterpret_cast<uint16_t*>(p.C) + (int64_t)row * p.ldc;
+  if (ncol == 32) {
+    store_bf16x32(hrow + col, hg);
+    store_bf16x32(hrow + p.N + col, hu);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) amax = max(amax, abs_bits(swiglu_ref(hg[j], hu[j])));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j < ncol) {
+        hrow[col + j] = __bfloat16_as_ushort(__float2bfloat16_rn(hg[j]));
+        hrow[p.N + col + j] = __bfloat16_as_ushort(__float2bfloat16_rn(hu[j]));
+        amax = max(amax, abs_bits(swiglu_ref(hg[j], hu[j])));
+      }
+    }
+  }
+}
+
+// dA = alpha * acc for gate columns [col, col+ncol); with h = H_gate, u = H_up,
+// s = sigmoid(h): dH_gate = dA u s (1 + h (1 - s)), dH_up = dA h s (bf16), absmax.
+__device__ __forceinline__ void swiglu_bwd1(float da, float h, float u, float& dg, float& du) {
+  const float s = __fdiv_rn(1.0f, __fadd_rn(1.0f, exp_ref(-h)));
+  const float hs = h * s;
+  dg = round_bf16(da * u * (s + hs * (1.0f - s)));
+  du = round_bf16(da * hs);
+}
+
+__device__ __forceinline__ void epi_swiglu_bwd(const Args& p, int row, int col, int ncol, const uint32_t (&acc)[32], float alpha,
+                               uint32_t& amax) {
+  const uint16_t* hrow = p.R + (int64_t)row * p.ldr;
+  uint16_t* drow = reinterpret_cast<uint16_t*>(p.C) + (int64_t)row * p.ldc;
+  if (ncol == 32) {
+    float h[32], u[32], dg[32], du[32];
+    load_bf16x32(hrow + col, h);
+    load_bf16x32(hrow + p.N + col, u);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      swiglu_bwd1(__fmul_rn(alpha, __uint_as_float(acc[j])), h[j], u[j], dg[j], du[j]);
+      amax = max(amax, max(abs_bits(dg[j]), abs_bits(du[j])));
+    }
+    store_bf16x32(drow + col, dg);
+    store_bf16x32(drow + p.N + col, du);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j >= ncol) continue;
+      float dg, du;
+      swiglu_bwd1(__fmul_rn(alpha, __uint_as_float(acc[j])), __uint_as_float((uint32_t)hrow[col + j] << 16),
+                  __uint_as_float((uint32_t)hrow[p.N + col + j] << 16), dg, du);
+      amax = max(amax, max(abs_bits(dg), abs_bits(du)));
+      drow[col + j] = __bfloat16_as_ushort(__float2bfloat16_rn(dg));
+      drow[p.N + col + j] = __bfloat16_as_ushort(__float2bfloat16_rn(du));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+template <int A_MN, int B_MN>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_f8(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Args p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOffset);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;   // [2]
+  uint64_t* tempty = tfull + 2;       // [2]
+  uint64_t* drain = tempty + 2;       // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint32_t* cta_amax = reinterpret_cast<uint32_t*>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 128); }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    *cta_amax = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmA); tma_prefetch_desc(&tmB); }
+  if (warp == 2) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0;      // bit s: stage s has a load in flight or consumed
+      uint32_t issued_par = 0;  // bit s: parity of the full[] phase of that load
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, p, mb, nb);
+        const int m0 = mb * BM;
+        const int n0 = nb * p.b_step, n1 = n0 + p.b_half1;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+          uint8_t* sA = smem + stage * kStage;
+          uint8_t* sB = sA + kATile;
+          mbar_arrive_expect_tx(&full[stage], kStage);
+          const int k0 = kb * BK;
+          if (A_MN) tma_load_2d(sA, &tmA, &full[stage], m0, k0);
+          else tma_load_2d(sA, &tmA, &full[stage], k0, m0);
+          if (B_MN) {
+            tma_load_2d(sB, &tmB, &full[stage], n0, k0);
+            tma_load_2d(sB + kBHalf, &tmB, &full[stage], n1, k0);
+          } else {
+            tma_load_2d(sB, &tmB, &full[stage], k0, n0);
+            tma_load_2d(sB + kBHalf, &tmB, &full[stage], k0, n1);
+          }
+          issued |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        atomicOr(p.status, kStatusTimeout);
+        *abort_flag = 1;
+        // let every copy this thread started land before the CTA can exit
+        for (int s = 0; s < STAGES; ++s)
+          if (issued & (1u << s)) {
+            int dummy = 0;
+            mbar_wait(&full[s], (issued_par >> s) & 1u, &dummy);
+          }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sA = smem_addr(smem + stage * kStage);
+          const uint32_t sB = sA + kATile;
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk) {
+            // K-major: advance 32 bytes inside the 128-byte swizzle row; MN-major: 32 K-rows of 128 B.
+            const uint64_t ad = A_MN ? smem_desc_sw128(sA + kk * 4096, kBHalf, 1024) : smem_desc_sw128(sA + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? smem_desc_sw128(sB + kk * 4096, kBHalf, 1024) : smem_desc_sw128(sB + kk * 32, 16, 1024);
+            umma_f8(d_tmem, ad, bd, p.idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      if (!ok) {
+        atomicOr(p.status, kStatusTimeout);
+        *abort_flag = 1;
+      }
+      // wait for every MMA this thread issued before TMEM can be released
+      umma_commit(drain);
+      int dummy = 0;
+      mbar_wait(drain, 0, &dummy);
+    }
+  } else if (warp >= 4) {
+    // ---------------- epilogue ----------------
+    const int sub = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    uint32_t amax = 0;
+    const float alpha = __fmul_rn(*p.sinvA, *p.sinvB);
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+      int mb, nb;
+      tile_coords(tile, p, mb, nb);
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) {
+        atomicOr(p.status, kStatusTimeout);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(sub * 32) << 16);
+      const int row = mb * BM + sub * 32 + lane;
+      const bool row_ok = row < p.M;
+      if (p.epi == kEpiSwiglu) {
+        const int col0 = nb * 128;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t ag[32], au[32];
+          tmem_ld32x2(tbase + c * 32, tbase + 128 + c * 32, ag, au);
+          const int col = col0 + c * 32;
+          const int ncol = min(32, p.N - col);
+          if (row_ok && ncol > 0) epi_swiglu(p, row, col, ncol, ag, au, alpha, amax);
+        }
+      } else {
+        const int col0 = nb * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t a[32];
+          tmem_ld32(tbase + c * 32, a);
+          const int col = col0 + c * 32;
+          const int ncol = min(32, p.N - col);
+          if (row_ok && ncol > 0) {
+            if (p.epi == kEpiSwigluBwd) epi_swiglu_bwd(p, row, col, ncol, a, alpha, amax);
+            else epi_store(p, row, col, ncol, a, alpha);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+    amax = warp_max_u32(amax);
+    if (lane == 0) atomicMax(cta_amax, amax);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0 && p.amax_partial) p.amax_partial[blockIdx.x] = *cta_amax;
+  if (warp == 2) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 2D uint8 tensor [outer, inner] with row stride `ld` bytes, 128 x 128 byte boxes, 128-byte swizzle.
+bool make_tmap(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int64_t ld) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  const cuuint64_t strides[1] = {(cuuint64_t)ld};
+  const cuuint32_t box[2] = {128, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Instruction descriptor for kind::f8f6f4: fp32 accumulator, A/B formats
+// (E4M3 = 0, E5M2 = 1), operand major-ness (bit 15 A, bit 16 B; 1 = MN-major),
+// N >> 3 at bit 17, M >> 4 at bit 24.
+uint32_t make_idesc(int fmtA, int fmtB, int a_mn, int b_mn) {
+  return (1u << 4) | ((uint32_t)fmtA << 7) | ((uint32_t)fmtB << 10) | ((uint32_t)a_mn << 15) |
+         ((uint32_t)b_mn << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+template <int A_MN, int B_MN>
+cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const Args& a, int grid, cudaStream_t s) {
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_f8<A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  k_gemm_f8<A_MN, B_MN><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L) {
+  Args a{};
+  a.M = g.M;
+  a.N = g.N;
+  a.K = g.K;
+  a.epi = g.epi;
+  a.out_f32 = g.out_f32;
+  a.sinvA = g.sinvA;
+  a.sinvB = g.sinvB;
+  a.C = g.C;
+  a.ldc = g.ldc;
+  a.R = g.R;
+  a.ldr = g.ldr;
+  a.amax_partial = g.amax_partial;
+  a.status = L.status;
+  a.idesc = make_idesc(g.fmtA, g.fmtB, g.a_mn, g.b_mn);
+  a.m_tiles = (g.M + BM - 1) / BM;
+  if (g.epi == kEpiSwiglu) {
+    a.n_tiles = (g.N + 127) / 128;  // 128 gate + the matching 128 up columns per tile
+    a.b_step = 128;
+    a.b_half1 = g.N;
+  } else {
+    a.n_tiles = (g.N + BN - 1) / BN;
+    a.b_step = BN;
+    a.b_half1 = 128;
+  }
+  a.k_blocks = (g.K + BK - 1) / BK;
+  a.num_tiles = a.m_tiles * a.n_tiles;
+
+  CUtensorMap ta, tb;
+  const bool ok_a = g.a_mn ? make_tmap(&ta, g.A, g.M, g.K, g.lda) : make_tmap(&ta, g.A, g.K, g.M, g.lda);
+  const bool ok_b = g.b_mn ? make_tmap(&tb, g.B, g.b_cols, g.K, g.ldb) : make_tmap(&tb, g.B, g.K, g.b_cols, g.ldb);
+  if (!ok_a || !ok_b) return cudaErrorInvalidValue;
+
+  const int grid = a.num_tiles < L.num_sms ? a.num_tiles : L.num_sms;
+  *P = grid;
+  cudaError_t e;
+  if (g.a_mn == 0 && g.b_mn == 1) e = launch_t<0, 1>(ta, tb, a, grid, L.stream);
+  else if (g.a_mn == 0 && g.b_mn == 0) e = launch_t<0, 0>(ta, tb, a, grid, L.stream);
+  else if (g.a_mn == 1 && g.b_mn == 1) e = launch_t<1, 1>(ta, tb, a, grid, L.stream);
+  else e = launch_t<1, 0>(ta, tb, a, grid, L.stream);
+  if (L.launches) ++*L.launches;
+  return e;
+}
+
+}  // namespace fp8q

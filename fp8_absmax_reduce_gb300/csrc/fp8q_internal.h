@@ -1,0 +1,71 @@
+// Internal launch interface between the C ABI (fp8q_api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace fp8q {
+
+// Upper bound on the number of per-block absmax partials any reduction pass writes.
+constexpr int kMaxPartials = 1024;
+// Rows per block of the RMSNorm backward (one fp32 dg partial row per block).
+constexpr int kBwdRows = 16;
+
+struct Launch {
+  cudaStream_t stream;
+  unsigned* status;  // device status word (FP8Q_STATUS_* bits)
+  int num_sms;
+  int* launches;     // incremented once per kernel launch
+};
+
+// Per-tensor absmax quantization: pass 1 writes *P partials, pass 2 casts.
+cudaError_t launch_absmax_partial(const void* x, int dtype, int64_t n, uint32_t* partial, int* P,
+                                  const Launch& L);
+cudaError_t launch_quant_cast(const void* x, int dtype, int64_t n, int fmt, const uint32_t* partial, int P,
+                              uint8_t* q, float* scal, const Launch& L);
+
+// RMSNorm: pass 1 (rstd + absmax partials), pass 2 (cast to E4M3).
+cudaError_t launch_rmsnorm_stats(const uint16_t* x, const uint16_t* g, int64_t T, int d, float eps, float* rstd,
+                                 uint32_t* partial, int* P, const Launch& L);
+cudaError_t launch_rmsnorm_cast(const uint16_t* x, const uint16_t* g, const float* rstd, int64_t T, int d,
+                                const uint32_t* partial, int P, uint8_t* q, float* scal, const Launch& L);
+
+// SwiGLU of H [T,2f]: pass 1 (absmax partials of a), pass 2 (cast).
+cudaError_t launch_swiglu_amax(const uint16_t* H, int64_t T, int f, uint32_t* partial, int* P, const Launch& L);
+cudaError_t launch_swiglu_cast(const uint16_t* H, int64_t T, int f, int fmt, const uint32_t* partial, int P,
+                               uint8_t* q, float* scal, const Launch& L);
+
+// RMSNorm backward + residual: dX = dY + rstd (u - nh mean(u nh)), dg = sum_t dN nh.
+// dg_partial: ceil(T / kBwdRows) x d floats of workspace.
+cudaError_t launch_rmsnorm_bwd(const float* dN, const uint16_t* x, const uint16_t* dY, const uint16_t* g,
+                               const float* rstd, int64_t T, int d, uint16_t* dX, float* dg_partial, float* dg,
+                               const Launch& L);
+
+// ---------------------------------------------------------------------------
+// GEMM
+// ---------------------------------------------------------------------------
+enum GemmEpilogue {
+  kEpiStore = 0,      // C = alpha * acc (bf16 or fp32)
+  kEpiResidual = 1,   // C = bf16(R + alpha * acc)
+  kEpiSwiglu = 2,     // H = bf16(alpha * acc) for paired gate/up columns + absmax of SwiGLU(H)
+  kEpiSwigluBwd = 3,  // dH = bf16(SwiGLU'(H) * alpha * acc) + absmax of dH
+};
+
+struct GemmProblem {
+  int a_mn, b_mn;        // operand is MN-major (1) or K-major (0)
+  int M, N, K;           // output rows/cols (kEpiSwiglu: N = f gate columns), reduction length
+  const uint8_t* A; int64_t lda; int fmtA;
+  const uint8_t* B; int64_t ldb; int fmtB;
+  int64_t b_cols;        // extent of B's N dimension in storage (2f for the paired gate/up layout)
+  const float* sinvA; const float* sinvB;
+  int epi; int out_f32;
+  void* C; int64_t ldc;  // kEpiSwiglu/kEpiSwigluBwd: [M, 2f] gate | up
+  const uint16_t* R; int64_t ldr;  // residual (kEpiResidual) or H (kEpiSwigluBwd)
+  uint32_t* amax_partial;          // per-CTA partials for the two SwiGLU epilogues
+};
+// Launches the persistent tcgen05 GEMM; *P receives the number of partials written.
+cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L);
+
+}  // namespace fp8q

@@ -1,0 +1,490 @@
+// HBM-bound kernels of the FP8 block pipeline: per-tensor absmax quantization,
+// RMSNorm + quantization, SwiGLU + requantization, RMSNorm backward.
+//
+// Every quantizer is two passes over its input (LLMQ §4: "dynamic quantization
+// adds overhead"; the per-tensor scale needs the whole tensor's absmax before
+// the first code can be written):
+//   pass 1: 16-byte vector loads, |v| max as fp32 bit patterns (exact and
+//           order-independent), warp shuffle + block reduction, one partial
+//           per block;
+//   pass 2: every block reduces the partials itself (a few KB from L2), derives
+//           scale = fmax/amax, and casts with cvt.rn.satfinite to E4M3/E5M2.
+// No atomics on floating point, no counters to reset: deterministic and
+// re-entrant on one stream.
+#include "fp8q_common.cuh"
+#include "fp8q_internal.h"
+
+namespace fp8q {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+inline int grid_for(int64_t items, int cap) {
+  int64_t b = (items + kThreads - 1) / kThreads;
+  if (b < 1) b = 1;
+  return (int)(b < cap ? b : cap);
+}
+
+inline cudaError_t post_launch(const Launch& L) {
+  if (L.launches) ++*L.launches;
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Pass 1: absmax partials
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __forceinline__ uint32_t vec_absmax(uint4 v) {
+  if (DT == 0) {
+    return max(max(absmax_bf16x2(v.x), absmax_bf16x2(v.y)), max(absmax_bf16x2(v.z), absmax_bf16x2(v.w)));
+  } else {
+    return max(max(v.x & 0x7FFFFFFFu, v.y & 0x7FFFFFFFu), max(v.z & 0x7FFFFFFFu, v.w & 0x7FFFFFFFu));
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t elem_absbits(const uint8_t* x, int64_t e) {
+  if (DT == 0) return ((uint32_t)(reinterpret_cast<const uint16_t*>(x)[e]) & 0x7FFFu) << 16;
+  return reinterpret_cast<const uint32_t*>(x)[e] & 0x7FFFFFFFu;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads) k_absmax_partial(const uint8_t* __restrict__ x, int64_t n,
+                                                             uint32_t* __restrict__ partial) {
+  __shared__ uint32_t red[32];
+  constexpr int per = DT == 0 ? 8 : 4;  // elements per 16-byte vector
+  const int64_t nvec = n / per;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  uint32_t m = 0;
+  for (; i + 3 * stride < nvec; i += 4 * stride) {
+    const uint4 v0 = ld_nc_v4(x + 16 * i);
+    const uint4 v1 = ld_nc_v4(x + 16 * (i + stride));
+    const uint4 v2 = ld_nc_v4(x + 16 * (i + 2 * stride));
+    const uint4 v3 = ld_nc_v4(x + 16 * (i + 3 * stride));
+    m = max(m, max(max(vec_absmax<DT>(v0), vec_absmax<DT>(v1)), max(vec_absmax<DT>(v2), vec_absmax<DT>(v3))));
+  }
+  for (; i < nvec; i += stride) m = max(m, vec_absmax<DT>(ld_nc_v4(x + 16 * i)));
+  if (blockIdx.x == 0)
+    for (int64_t e = nvec * per + threadIdx.x; e < n; e += blockDim.x) m = max(m, elem_absbits<DT>(x, e));
+  m = block_max_u32(m, red);
+  if (threadIdx.x == 0) partial[blockIdx.x] = m;
+}
+
+// ---------------------------------------------------------------------------
+// Pass 2: finalize the scale (every block) and cast
+// ---------------------------------------------------------------------------
+// Reduces the partials in warp 0 and publishes the scale in shared memory; block 0
+// also writes {amax, scale, scale_inv} and flags a non-finite amax.
+__device__ __forceinline__ float finalize_scale(const uint32_t* partial, int P, int fmt, float* scal,
+                                                unsigned* status, float* s_shared) {
+  if (threadIdx.x < 32) {
+    const float amax = reduce_partials_warp(partial, P);
+    if (threadIdx.x == 0) {
+      float s, si;
+      scale_from_amax(amax, fmt, s, si);
+      *s_shared = s;
+      if (blockIdx.x == 0) {
+        scal[0] = amax;
+        scal[1] = s;
+        scal[2] = si;
+        if (!(__float_as_uint(amax) < 0x7F800000u)) atomicOr(status, kStatusNonfinite);
+      }
+    }
+  }
+  __syncthreads();
+  return *s_shared;
+}
+
+template <int DT>
+__device__ __forceinline__ void load16(const uint8_t* x, int64_t item, float (&v)[16]) {
+  if (DT == 0) {
+    const uint4 a = ld_nc_v4(x + 32 * item), b = ld_nc_v4(x + 32 * item + 16);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) { v[2 * k] = bf16_lo(w[k]); v[2 * k + 1] = bf16_hi(w[k]); }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 a = ld_nc_v4(x + 64 * item + 16 * k);
+      v[4 * k] = __uint_as_float(a.x); v[4 * k + 1] = __uint_as_float(a.y);
+      v[4 * k + 2] = __uint_as_float(a.z); v[4 * k + 3] = __uint_as_float(a.w);
+    }
+  }
+}
+
+template <int FMT>
+__device__ __forceinline__ uint4 cast16(const float (&v)[16], float s) {
+  uint4 o;
+  o.x = cvt_fp8x4<FMT>(__fmul_rn(v[0], s), __fmul_rn(v[1], s), __fmul_rn(v[2], s), __fmul_rn(v[3], s));
+  o.y = cvt_fp8x4<FMT>(__fmul_rn(v[4], s), __fmul_rn(v[5], s), __fmul_rn(v[6], s), __fmul_rn(v[7], s));
+  o.z = cvt_fp8x4<FMT>(__fmul_rn(v[8], s), __fmul_rn(v[9], s), __fmul_rn(v[10], s), __fmul_rn(v[11], s));
+  o.w = cvt_fp8x4<FMT>(__fmul_rn(v[12], s), __fmul_rn(v[13], s), __fmul_rn(v[14], s), __fmul_rn(v[15], s));
+  return o;
+}
+
+template <int FMT>
+__device__ __forceinline__ uint8_t cvt_fp8(float v) {
+  return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, FMT == 0 ? __NV_E4M3 : __NV_E5M2);
+}
+
+template <int DT, int FMT>
+__global__ void __launch_bounds__(kThreads) k_quant_cast(const uint8_t* __restrict__ x, int64_t n,
+                                                         const uint32_t* __restrict__ partial, int P,
+                                                         uint8_t* __restrict__ q, float* __restrict__ scal,
+                                                         unsigned* status) {
+  __shared__ float s_sh;
+  const float s = finalize_scale(partial, P, FMT, scal, status, &s_sh);
+  const int64_t items = n / 16;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < items; i += stride) {
+    float v[16];
+    load16<DT>(x, i, v);
+    st_v4(q + 16 * i, cast16<FMT>(v, s));
+  }
+  if (blockIdx.x == 0)
+    for (int64_t e = items * 16 + threadIdx.x; e < n; e += blockDim.x) {
+      const float v = DT == 0 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(x)[e] << 16)
+                              : reinterpret_cast<const float*>(x)[e];
+      q[e] = cvt_fp8<FMT>(__fmul_rn(v, s));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// RMSNorm
+// ---------------------------------------------------------------------------
+// One warp per row.  Lane l holds the squares of x[256c + 8l .. +8) of chunk c.
+// The fp32 sum of squares is the pairwise sum of the row (zero-padded to 8192
+// terms, which adds exact zeros only): an 8-leaf tree per lane, a butterfly
+// across lanes (each level adds adjacent subtrees), then a tree over the 32
+// chunk sums.
+__global__ void __launch_bounds__(kThreads) k_rmsnorm_stats(const uint16_t* __restrict__ x,
+                                                            const uint16_t* __restrict__ g, int64_t T, int d,
+                                                            float eps, float* __restrict__ rstd,
+                                                            uint32_t* __restrict__ partial) {
+  __shared__ uint32_t red[32];
+  const int lane = threadIdx.x & 31;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  uint32_t m = 0;
+  for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < T; row += nw) {
+    const uint16_t* xr = x + row * d;
+    float cs[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      float v = 0.0f;
+      if (c * 256 < d) {
+        const int j0 = c * 256 + lane * 8;
+        if (j0 < d) {
+          const uint4 w = ld_v4(xr + j0);
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+          float s[8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float lo = bf16_lo(ww[k]), hi = bf16_hi(ww[k]);
+            s[2 * k] = __fmul_rn(lo, lo);
+            s[2 * k + 1] = __fmul_rn(hi, hi);
+          }
+          v = __fadd_rn(__fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3])),
+                        __fadd_rn(__fadd_rn(s[4], s[5]), __fadd_rn(s[6], s[7])));
+        }
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+      }
+      cs[c] = v;
+    }
+#pragma unroll
+    for (int w = 1; w < 32; w <<= 1)
+#pragma unroll
+      for (int i = 0; i < 32; i += 2 * w) cs[i] = __fadd_rn(cs[i], cs[i + w]);
+    const float rs = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(cs[0], (float)d), eps)));
+    if (lane == 0) rstd[row] = rs;
+    for (int j0 = lane * 8; j0 < d; j0 += 256) {
+      const uint4 w = ld_v4(xr + j0), gw = ld_v4(g + j0);
+      const uint32_t xw[4] = {w.x, w.y, w.z, w.w}, gg[4] = {gw.x, gw.y, gw.z, gw.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        m = max(m, abs_bits(__fmul_rn(__fmul_rn(bf16_lo(xw[k]), rs), bf16_lo(gg[k]))));
+        m = max(m, abs_bits(__fmul_rn(__fmul_rn(bf16_hi(xw[k]), rs), bf16_hi(gg[k]))));
+      }
+    }
+  }
+  m = block_max_u32(m, red);
+  if (threadIdx.x == 0) partial[blockIdx.x] = m;
+}
+
+__global__ void __launch_bounds__(kThreads) k_rmsnorm_cast(const uint16_t* __restrict__ x,
+                                                           const uint16_t* __restrict__ g,
+                                                           const float* __restrict__ rstd, int64_t T, int d,
+                                                           const uint32_t* __restrict__ partial, int P,
+                                                           uint8_t* __restrict__ q, float* __restrict__ scal,
+                                                           unsigned* status) {
+  __shared__ float s_sh;
+  const float s = finalize_scale(partial, P, 0, scal, status, &s_sh);
+  const int gpr = d / 16;
+  const int64_t items = T * gpr;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < items; i += stride) {
+    const int64_t row = i / gpr;
+    const int j0 = (int)(i - row * gpr) * 16;
+    const float rs = rstd[row];
+    const uint16_t* xr = x + row * d + j0;
+    const uint4 a = ld_nc_v4(xr), b = ld_nc_v4(xr + 8), ga = ld_v4(g + j0), gb = ld_v4(g + j0 + 8);
+    const uint32_t xw[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const uint32_t gw[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+    float v[16];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      v[2 * k] = __fmul_rn(__fmul_rn(bf16_lo(xw[k]), rs), bf16_lo(gw[k]));
+      v[2 * k + 1] = __fmul_rn(__fmul_rn(bf16_hi(xw[k]), rs), bf16_hi(gw[k]));
+    }
+    st_v4(q + row * d + j0, cast16<0>(v, s));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// SwiGLU: a = silu(gate) * up over H [T, 2f]
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void swiglu8(const uint16_t* H, int64_t row, int f, int j0, float (&a)[8]) {
+  const uint16_t* hr = H + row * 2 * (int64_t)f + j0;
+  const uint4 gv = ld_nc_v4(hr), uv = ld_nc_v4(hr + f);
+  const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    a[2 * k] = swiglu_ref(bf16_lo(gw[k]), bf16_lo(uw[k]));
+    a[2 * k + 1] = swiglu_ref(bf16_hi(gw[k]), bf16_hi(uw[k]));
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) k_swiglu_amax(const uint16_t* __restrict__ H, int64_t T, int f,
+                                                          uint32_t* __restrict__ partial) {
+  __shared__ uint32_t red[32];
+  const int gpr = f / 8;
+  const int64_t items = T * gpr;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  uint32_t m = 0;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < items; i += stride) {
+    const int64_t row = i / gpr;
+    float a[8];
+    swiglu8(H, row, f, (int)(i - row * gpr) * 8, a);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m = max(m, abs_bits(a[k]));
+  }
+  m = block_max_u32(m, red);
+  if (threadIdx.x == 0) partial[blockIdx.x] = m;
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads) k_swiglu_cast(const uint16_t* __restrict__ H, int64_t T, int f,
+                                                          const uint32_t* __restrict__ partial, int P,
+                                                          uint8_t* __restrict__ q, float* __restrict__ scal,
+                                                          unsigned* status) {
+  __shared__ float s_sh;
+  const float s = finalize_scale(partial, P, FMT, scal, status, &s_sh);
+  const int gpr = f / 8;
+  const int64_t items = T * gpr;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < items; i += stride) {
+    const int64_t row = i / gpr;
+    const int j0 = (int)(i - row * gpr) * 8;
+    float a[8];
+    swiglu8(H, row, f, j0, a);
+    uint2 o;
+    o.x = cvt_fp8x4<FMT>(__fmul_rn(a[0], s), __fmul_rn(a[1], s), __fmul_rn(a[2], s), __fmul_rn(a[3], s));
+    o.y = cvt_fp8x4<FMT>(__fmul_rn(a[4], s), __fmul_rn(a[5], s), __fmul_rn(a[6], s), __fmul_rn(a[7], s));
+    *reinterpret_cast<uint2*>(q + row * (int64_t)f + j0) = o;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// RMSNorm backward + residual.  A block owns kBwdRows rows; thread t owns the
+// 8-column groups j = 8 (t + 256 c), c < NG.  Per row: nh = x rstd, u = dN g,
+// dot = sum_j u nh (block reduction, fixed order), dX = dY + rstd (u - nh dot/d).
+// dg partials accumulate per block in registers (fixed row order) and are
+// reduced over blocks in a fixed order by k_dg_finalize.
+// ---------------------------------------------------------------------------
+template <int NG>
+__global__ void __launch_bounds__(kThreads) k_rmsnorm_bwd(const float* __restrict__ dN,
+                                                          const uint16_t* __restrict__ x,
+                                                          const uint16_t* __restrict__ dY,
+                                                          const uint16_t* __restrict__ g,
+                                                          const float* __restrict__ rstd, int64_t T, int d,
+                                                          uint16_t* __restrict__ dX,
+                                                          float* __restrict__ dg_partial) {
+  __shared__ float red[2][kThreads / 32];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  float gv[NG][8], dga[NG][8];
+#pragma unroll
+  for (int c = 0; c < NG; ++c) {
+    const int j0 = 8 * (t + kThreads * c);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) { gv[c][k] = 0.0f; dga[c][k] = 0.0f; }
+    if (j0 < d) {
+      const uint4 w = ld_v4(g + j0);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) { gv[c][2 * k] = bf16_lo(ww[k]); gv[c][2 * k + 1] = bf16_hi(ww[k]); }
+    }
+  }
+  const float inv_d = 1.0f / (float)d;
+  for (int rr = 0; rr < kBwdRows; ++rr) {
+    const int64_t row = (int64_t)blockIdx.x * kBwdRows + rr;
+    if (row >= T) break;
+    const float rs = rstd[row];
+    float nh[NG][8], u[NG][8];
+    float dot = 0.0f;
+#pragma unroll
+    for (int c = 0; c < NG; ++c) {
+      const int j0 = 8 * (t + kThreads * c);
+      if (j0 < d) {
+        const float* dn = dN + row * d + j0;
+        const uint4 d0 = ld_nc_v4(dn), d1 = ld_nc_v4(dn + 4);
+        const uint4 xv = ld_nc_v4(x + row * d + j0);
+        const float dnv[8] = {__uint_as_float(d0.x), __uint_as_float(d0.y), __uint_as_float(d0.z),
+                              __uint_as_float(d0.w), __uint_as_float(d1.x), __uint_as_float(d1.y),
+                              __uint_as_float(d1.z), __uint_as_float(d1.w)};
+        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float xk = (k & 1) ? bf16_hi(xw[k >> 1]) : bf16_lo(xw[k >> 1]);
+          nh[c][k] = xk * rs;
+          u[c][k] = dnv[k] * gv[c][k];
+          dot += u[c][k] * nh[c][k];
+          dga[c][k] += dnv[k] * nh[c][k];
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) { nh[c][k] = 0.0f; u[c][k] = 0.0f; }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
+    if (lane == 0) red[rr & 1][warp] = dot;
+    __syncthreads();
+    float tot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) tot += red[rr & 1][w];
+    const float mean = tot * inv_d;
+#pragma unroll
+    for (int c = 0; c < NG; ++c) {
+      const int j0 = 8 * (t + kThreads * c);
+      if (j0 < d) {
+        const uint4 yv = ld_nc_v4(dY + row * d + j0);
+        const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float a = bf16_lo(yw[k]) + rs * (u[c][2 * k] - nh[c][2 * k] * mean);
+          const float b = bf16_hi(yw[k]) + rs * (u[c][2 * k + 1] - nh[c][2 * k + 1] * mean);
+          o[k] = pack_bf16x2(a, b);
+        }
+        st_v4(dX + row * d + j0, make_uint4(o[0], o[1], o[2], o[3]));
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < NG; ++c) {
+    const int j0 = 8 * (t + kThreads * c);
+    if (j0 < d) {
+      float* dst = dg_partial + (int64_t)blockIdx.x * d + j0;
+      st_v4(dst, make_uint4(__float_as_uint(dga[c][0]), __float_as_uint(dga[c][1]), __float_as_uint(dga[c][2]),
+                            __float_as_uint(dga[c][3])));
+      st_v4(dst + 4, make_uint4(__float_as_uint(dga[c][4]), __float_as_uint(dga[c][5]),
+                                __float_as_uint(dga[c][6]), __float_as_uint(dga[c][7])));
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) k_dg_finalize(const float* __restrict__ dg_partial, int nblk, int d,
+                                                          float* __restrict__ dg) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= d) return;
+  float s = 0.0f;
+  for (int b = 0; b < nblk; ++b) s += dg_partial[(int64_t)b * d + j];
+  dg[j] = s;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Launchers
+// ---------------------------------------------------------------------------
+cudaError_t launch_absmax_partial(const void* x, int dtype, int64_t n, uint32_t* partial, int* P,
+                                  const Launch& L) {
+  const int64_t nvec = dtype == 0 ? n / 8 : n / 4;
+  const int grid = grid_for(nvec / 4 > 0 ? nvec / 4 : 1, kMaxPartials);
+  *P = grid;
+  if (dtype == 0)
+    k_absmax_partial<0><<<grid, kThreads, 0, L.stream>>>((const uint8_t*)x, n, partial);
+  else
+    k_absmax_partial<1><<<grid, kThreads, 0, L.stream>>>((const uint8_t*)x, n, partial);
+  return post_launch(L);
+}
+
+cudaError_t launch_quant_cast(const void* x, int dtype, int64_t n, int fmt, const uint32_t* partial, int P,
+                              uint8_t* q, float* scal, const Launch& L) {
+  const int grid = grid_for(n / 16 > 0 ? n / 16 : 1, L.num_sms * 8);
+  const uint8_t* xb = (const uint8_t*)x;
+  if (dtype == 0 && fmt == 0)
+    k_quant_cast<0, 0><<<grid, kThreads, 0, L.stream>>>(xb, n, partial, P, q, scal, L.status);
+  else if (dtype == 0)
+    k_quant_cast<0, 1><<<grid, kThreads, 0, L.stream>>>(xb, n, partial, P, q, scal, L.status);
+  else if (fmt == 0)
+    k_quant_cast<1, 0><<<grid, kThreads, 0, L.stream>>>(xb, n, partial, P, q, scal, L.status);
+  else
+    k_quant_cast<1, 1><<<grid, kThreads, 0, L.stream>>>(xb, n, partial, P, q, scal, L.status);
+  return post_launch(L);
+}
+
+cudaError_t launch_rmsnorm_stats(const uint16_t* x, const uint16_t* g, int64_t T, int d, float eps, float* rstd,
+                                 uint32_t* partial, int* P, const Launch& L) {
+  const int warps_per_block = kThreads / 32;
+  int64_t blocks = (T + warps_per_block - 1) / warps_per_block;
+  const int grid = (int)(blocks < kMaxPartials ? blocks : kMaxPartials);
+  *P = grid;
+  k_rmsnorm_stats<<<grid, kThreads, 0, L.stream>>>(x, g, T, d, eps, rstd, partial);
+  return post_launch(L);
+}
+
+cudaError_t launch_rmsnorm_cast(const uint16_t* x, const uint16_t* g, const float* rstd, int64_t T, int d,
+                                const uint32_t* partial, int P, uint8_t* q, float* scal, const Launch& L) {
+  const int grid = grid_for(T * (d / 16), L.num_sms * 8);
+  k_rmsnorm_cast<<<grid, kThreads, 0, L.stream>>>(x, g, rstd, T, d, partial, P, q, scal, L.status);
+  return post_launch(L);
+}
+
+cudaError_t launch_swiglu_amax(const uint16_t* H, int64_t T, int f, uint32_t* partial, int* P, const Launch& L) {
+  const int grid = grid_for(T * (f / 8), kMaxPartials);
+  *P = grid;
+  k_swiglu_amax<<<grid, kThreads, 0, L.stream>>>(H, T, f, partial);
+  return post_launch(L);
+}
+
+cudaError_t launch_swiglu_cast(const uint16_t* H, int64_t T, int f, int fmt, const uint32_t* partial, int P,
+                               uint8_t* q, float* scal, const Launch& L) {
+  const int grid = grid_for(T * (f / 8), L.num_sms * 8);
+  if (fmt == 0)
+    k_swiglu_cast<0><<<grid, kThreads, 0, L.stream>>>(H, T, f, partial, P, q, scal, L.status);
+  else
+    k_swiglu_cast<1><<<grid, kThreads, 0, L.stream>>>(H, T, f, partial, P, q, scal, L.status);
+  return post_launch(L);
+}
+
+cudaError_t launch_rmsnorm_bwd(const float* dN, const uint16_t* x, const uint16_t* dY, const uint16_t* g,
+                               const float* rstd, int64_t T, int d, uint16_t* dX, float* dg_partial, float* dg,
+                               const Launch& L) {
+  const int nblk = (int)((T + kBwdRows - 1) / kBwdRows);
+  const int ng = (d + 8 * kThreads - 1) / (8 * kThreads);
+  switch (ng) {
+    case 1: k_rmsnorm_bwd<1><<<nblk, kThreads, 0, L.stream>>>(dN, x, dY, g, rstd, T, d, dX, dg_partial); break;
+    case 2: k_rmsnorm_bwd<2><<<nblk, kThreads, 0, L.stream>>>(dN, x, dY, g, rstd, T, d, dX, dg_partial); break;
+    case 3: k_rmsnorm_bwd<3><<<nblk, kThreads, 0, L.stream>>>(dN, x, dY, g, rstd, T, d, dX, dg_partial); break;
+    default: k_rmsnorm_bwd<4><<<nblk, kThreads, 0, L.stream>>>(dN, x, dY, g, rstd, T, d, dX, dg_partial); break;
+  }
+  cudaError_t e = post_launch(L);
+  if (e != cudaSuccess) return e;
+  k_dg_finalize<<<(d + kThreads - 1) / kThreads, kThreads, 0, L.stream>>>(dg_partial, nblk, d, dg);
+  return post_launch(L);
+}
+
+}  // namespace fp8q

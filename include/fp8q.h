@@ -1,0 +1,217 @@
+/*
+ * fp8q.h -- C ABI of the GB300 (sm_103a) FP8 transformer-block pipeline with
+ * just-in-time per-tensor absmax scaling.
+ *
+ * The operations follow the LLMQ pages:
+ *   "LLMQ: Efficient Lower-Precision Pretraining for Consumer GPUs"
+ *   (paperlayer.ai summary of arXiv 2512.15306), §1: FP8 training with dynamic
+ *   tensor-level scaling; §3/§3.1/§3.2: fused non-matmul ops, retained absmax
+ *   statistics for requantization, deterministic kernels; §4: dynamic
+ *   quantization and backward transposes are the FP8 overheads; §5 Figure 2:
+ *   E4M3 forward, E5M2 activation gradients.
+ *   "Periodic Reporting for period 1 - FastML" (CORDIS), "FP8 training
+ *   without delayed scaling": just-in-time tensor-level absmax scaling,
+ *   guaranteeing no value clipping.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Memory: every pointer is a DEVICE pointer unless stated otherwise.  The
+ *    caller owns all memory (inputs, outputs, workspace); the library never
+ *    allocates or frees device memory.  Tensors are dense and row-major.
+ *    bf16 tensors are passed as raw 16-bit storage.
+ *  - Alignment: tensor base pointers must be 16-byte aligned.
+ *  - Streams: every call only enqueues kernels on `stream` (a cudaStream_t;
+ *    NULL is the legacy default stream) and never synchronizes with the host.
+ *  - Scales: a "scal" argument points to 3 device floats
+ *    {amax, scale, scale_inv}: amax = max |v| over the whole tensor,
+ *    scale = fl32(fmt_max / amax) (1 when amax == 0), scale_inv = fl32(1/scale).
+ *    A tensor is quantized as code = fp8_rne_satfinite(fl32(v * scale)), so
+ *    the absmax element maps to +-fmt_max and nothing is clipped.
+ *    fmt_max: E4M3 448, E5M2 57344.
+ *  - Workspace: `ws`/`ws_bytes` is caller-provided device scratch of at least
+ *    the size the matching *_workspace_size() function returns, 256-byte
+ *    aligned; its contents need no initialisation and are garbage afterwards.
+ *    Two calls that are in flight at the same time need distinct workspaces.
+ *  - Synchronous errors (bad arguments) are returned before anything is
+ *    enqueued.  Kernel launch failures return FP8Q_ERR_CUDA.  Conditions that
+ *    are only known on the device (a non-finite amax; a bounded wait that ran
+ *    out) are recorded in a per-device status word that fp8q_get_status()
+ *    reads after the caller has synchronized the stream.
+ *  - Determinism: the same inputs give the same output bits on the same GPU
+ *    model (no floating-point atomics; fixed reduction orders).
+ */
+#ifndef FP8Q_H
+#define FP8Q_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FP8Q_API __attribute__((visibility("default")))
+#else
+#define FP8Q_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FP8Q_OK = 0,
+  FP8Q_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size or leading dimension   */
+  FP8Q_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement              */
+  FP8Q_ERR_CUDA = 3,         /* a CUDA runtime/driver call or a kernel launch failed      */
+  FP8Q_ERR_TIMEOUT = 4,      /* device status only: a bounded wait in a kernel ran out    */
+  FP8Q_ERR_NONFINITE = 5,    /* device status only: a tensor's amax was Inf or NaN        */
+  FP8Q_ERR_WORKSPACE = 6     /* workspace pointer null/misaligned or ws_bytes too small   */
+} fp8q_status;
+
+typedef enum { FP8Q_E4M3 = 0, FP8Q_E5M2 = 1 } fp8q_fmt;
+typedef enum { FP8Q_BF16 = 0, FP8Q_F32 = 1 } fp8q_dtype;
+/* Operand storage of fp8_gemm_scaled (C[M,N] = op(A) op(B), all row-major):
+ *   NN: A [M,K], B [K,N]      NT: A [M,K], B [N,K]      TN: A [K,M], B [K,N]   */
+typedef enum { FP8Q_NN = 0, FP8Q_NT = 1, FP8Q_TN = 2 } fp8q_layout;
+
+typedef void* fp8q_stream; /* cudaStream_t */
+
+/* Device status bits returned by fp8q_get_status. */
+#define FP8Q_STATUS_NONFINITE 0x1u
+#define FP8Q_STATUS_TIMEOUT 0x2u
+
+/* ------------------------------------------------------------------------ */
+/* Per-tensor absmax quantization (LLMQ §1 dynamic tensor-level scaling;    */
+/* FastML report: just-in-time absmax scaling, no clipping).                */
+/* ------------------------------------------------------------------------ */
+/* x: n elements of x_dtype (bf16 or fp32); q: n codes of fmt; scal: 3 floats.
+ * Two passes: a vectorised absmax reduction (warp shuffles, block reduction,
+ * one partial per block in ws), then a cast pass that finalises the scale
+ * from the partials and writes the codes.  Returns FP8Q_OK or a sync error. */
+FP8Q_API size_t fp8_quantize_absmax_workspace_size(int64_t n);
+FP8Q_API int fp8_quantize_absmax(const void* x, fp8q_dtype x_dtype, int64_t n, fp8q_fmt fmt, uint8_t* q,
+                        float* scal, void* ws, size_t ws_bytes, fp8q_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* Scaled FP8 GEMM (LLMQ §4: FP8 matmuls dominate; backward dgrad/wgrad use  */
+/* the transposed layouts without separate transpose buffers).              */
+/* ------------------------------------------------------------------------ */
+/* C = alpha * op(A) op(B) (+ residual), alpha = fl32(sinvA[0] * sinvB[0]),
+ * accumulated in fp32 on the tcgen05 tensor cores (kind::f8f6f4).
+ *   A, B: FP8 codes (formats fmtA/fmtB may differ), stored per `layout`, with
+ *         leading dimensions lda/ldb in elements (= bytes).
+ *   sinvA, sinvB: device pointers to one float each (a tensor's scale_inv).
+ *   C: [M,N] of out_dtype, leading dimension ldc elements.
+ *   residual: optional bf16 [M,N] (ldr elements) added in fp32 before the
+ *             bf16 rounding; requires out_dtype == FP8Q_BF16.
+ * Requirements: M,N,K >= 1; the contiguous dimension of each operand (K for a
+ * K-major operand, M or N for an MN-major one) and its leading dimension are
+ * multiples of 16; ldc, ldr multiples of 8.  */
+FP8Q_API int fp8_gemm_scaled(fp8q_layout layout, int64_t M, int64_t N, int64_t K, const uint8_t* A,
+                    fp8q_fmt fmtA, int64_t lda, const uint8_t* B, fp8q_fmt fmtB, int64_t ldb,
+                    const float* sinvA, const float* sinvB, void* C, fp8q_dtype out_dtype,
+                    int64_t ldc, const void* residual, int64_t ldr, fp8q_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* RMSNorm fused with the absmax reduction and the E4M3 cast (LLMQ §3).     */
+/* ------------------------------------------------------------------------ */
+/* x [T,d] bf16, g [d] bf16 -> q [T,d] E4M3, scal, rstd [T] fp32.
+ * rstd_t = fl32(1 / fl32(sqrt(fl32(fl32(S_t / d) + eps)))), S_t the fp32
+ * pairwise sum of x^2 over the row; n = fl32(fl32(x * rstd) * g).
+ * Requirements: T >= 1, d multiple of 16, 16 <= d <= 8192. */
+FP8Q_API size_t rmsnorm_quant_workspace_size(int64_t T, int64_t d);
+FP8Q_API int rmsnorm_quant(const void* x, const void* g, int64_t T, int64_t d, float eps, uint8_t* q,
+                  float* scal, float* rstd, void* ws, size_t ws_bytes, fp8q_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* SwiGLU fused with requantization (LLMQ §3.1: quantization fused with the */
+/* nonlinearity).                                                           */
+/* ------------------------------------------------------------------------ */
+/* H [T,2f] bf16 (gate in columns [0,f), up in [f,2f)) -> q [T,f] of fmt.
+ * a = fl32(fl32(h / fl32(1 + exp_ref(-h))) * u) in fp32; exp_ref is a fixed
+ * fp32 sequence (Cody-Waite reduction, degree-8 Taylor polynomial), so the
+ * result is bit-reproducible.  Requirements: T >= 1, f multiple of 16. */
+FP8Q_API size_t swiglu_quant_workspace_size(int64_t T, int64_t f);
+FP8Q_API int swiglu_quant(const void* H, int64_t T, int64_t f, fp8q_fmt fmt, uint8_t* q, float* scal,
+                 void* ws, size_t ws_bytes, fp8q_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* The MLP block, forward and backward (bias-free SwiGLU MLP with RMSNorm   */
+/* and bf16 residual; E4M3 activations/weights, E5M2 gradients).            */
+/* ------------------------------------------------------------------------ */
+/* Forward:  W_gu8 = q(W_gu), W_d8 = q(W_d), n8 = q(RMSNorm(x) * g),
+ *           H = bf16(alpha * n8 @ W_gu8)  [T,2f],  a8 = q(silu(H_gate) * H_up),
+ *           y = bf16(x + alpha * a8 @ W_d8).
+ * Backward: dY8 = q5(dY),  dA = alpha * dY8 @ W_d8^T,
+ *           dH = bf16(SwiGLU'(H) * dA), dH8 = q5(dH),
+ *           dW_d = alpha * a8^T @ dY8,  dN = alpha * dH8 @ W_gu8^T,
+ *           dW_gu = alpha * n8^T @ dH8  (fp32),
+ *           dX = bf16(dY + RMSNorm'(dN)),  dg = sum_t dN * x * rstd.
+ * Every alpha is the product of the two operands' scale_inv.
+ * W_gu holds [W_gate | W_up] as one tensor with one scale. */
+typedef struct fp8q_mlp {
+  int64_t T, d, f; /* tokens, model width, FFN width: d, f multiples of 16, d <= 8192 */
+  float eps;       /* RMSNorm epsilon */
+  /* inputs */
+  const void* x;    /* [T,d]  bf16 */
+  const void* g;    /* [d]    bf16 RMSNorm gain */
+  const void* W_gu; /* [d,2f] bf16 */
+  const void* W_d;  /* [f,d]  bf16 */
+  /* forward outputs, kept for the backward */
+  void* y;          /* [T,d]  bf16 */
+  uint8_t* W_gu8;   /* [d,2f] E4M3 */
+  uint8_t* W_d8;    /* [f,d]  E4M3 */
+  uint8_t* n8;      /* [T,d]  E4M3 */
+  float* rstd;      /* [T]    fp32 */
+  void* H;          /* [T,2f] bf16 */
+  uint8_t* a8;      /* [T,f]  E4M3 */
+  float* scal;      /* [6][3] {amax, scale, scale_inv} of W_gu, W_d, n, a, dY, dH */
+  /* backward input/outputs */
+  const void* dY;   /* [T,d]  bf16 */
+  void* dX;         /* [T,d]  bf16 */
+  float* dW_gu;     /* [d,2f] fp32 */
+  float* dW_d;      /* [f,d]  fp32 */
+  float* dg;        /* [d]    fp32 */
+  /* optional views of backward intermediates; NULL = kept in the workspace */
+  uint8_t* dY8;     /* [T,d]  E5M2 */
+  void* dH;         /* [T,2f] bf16 */
+  uint8_t* dH8;     /* [T,2f] E5M2 */
+  float* dN;        /* [T,d]  fp32 */
+} fp8q_mlp;
+
+/* backward != 0 sizes the workspace for mlp_block_bwd (which also suffices for mlp_block_fwd). */
+FP8Q_API size_t mlp_block_workspace_size(int64_t T, int64_t d, int64_t f, int backward);
+FP8Q_API int mlp_block_fwd(const fp8q_mlp* m, void* ws, size_t ws_bytes, fp8q_stream stream);
+/* Reads the forward's saved tensors (W_gu8, W_d8, n8, rstd, H, a8, scal[0..3]). */
+FP8Q_API int mlp_block_bwd(const fp8q_mlp* m, void* ws, size_t ws_bytes, fp8q_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* Status and introspection                                                 */
+/* ------------------------------------------------------------------------ */
+/* Reads (and with clear != 0 resets) the current device's status word
+ * (FP8Q_STATUS_* bits).  Call after synchronizing the streams that ran the
+ * library's kernels.  Returns the bits, or -1 if the read itself failed. */
+FP8Q_API int fp8q_get_status(int clear);
+/* Short description of an fp8q_status value (static storage). */
+FP8Q_API const char* fp8q_status_string(int status);
+/* Number of kernel launches the most recent successful call on this host
+ * thread enqueued. */
+FP8Q_API int fp8q_last_launch_count(void);
+
+/* Kernel-level timing for benchmarks.  While tracing is on for the calling
+ * host thread, each kernel step the library enqueues is bracketed by two CUDA
+ * events recorded on the stream it is launched on (host-side CUDA objects; no
+ * device memory).  fp8q_trace_start(capacity) creates 2*capacity events and
+ * turns tracing on (FP8Q_ERR_CUDA if event creation fails); steps beyond
+ * capacity are not traced.  fp8q_trace_stop() turns it off.
+ * fp8q_trace_read() waits for the recorded events, writes each step's
+ * duration in milliseconds and its kernel kind, and returns the count.
+ * fp8q_kernel_name(kind) names a kind (static storage). */
+FP8Q_API int fp8q_trace_start(int capacity);
+FP8Q_API int fp8q_trace_stop(void);
+FP8Q_API int fp8q_trace_read(float* ms, int* kinds, int capacity);
+FP8Q_API const char* fp8q_kernel_name(int kind);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8Q_H */

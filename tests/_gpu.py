@@ -1,0 +1,44 @@
+"""Helpers shared by the GPU parity tests: host <-> device conversion and the error metrics."""
+
+import numpy as np
+import torch
+
+
+def dev_bf16(bits: np.ndarray) -> torch.Tensor:
+    """uint16 bf16 bit patterns -> CUDA bfloat16 tensor (same bits)."""
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def dev_u8(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint8)).cuda()
+
+
+def host_bits(t: torch.Tensor) -> np.ndarray:
+    """CUDA bf16 tensor -> uint16 bit patterns."""
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def host_f64(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def row_rel(got: np.ndarray, ref: np.ndarray) -> float:
+    """max over rows of ||got_i - ref_i||_2 / ||ref_i||_2 (rows with a zero reference are skipped
+    unless got is non-zero there)."""
+    got = np.asarray(got, dtype=np.float64).reshape(ref.shape[0], -1)
+    ref = np.asarray(ref, dtype=np.float64).reshape(ref.shape[0], -1)
+    num = np.linalg.norm(got - ref, axis=1)
+    den = np.linalg.norm(ref, axis=1)
+    zero = den == 0
+    if (num[zero] > 0).any():
+        return float("inf")
+    return float((num[~zero] / den[~zero]).max()) if (~zero).any() else 0.0
+
+
+def code_step_diff(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """Distance in representable steps between FP8 codes of the same format (sign-magnitude)."""
+    def ordinal(c):
+        c = c.astype(np.int32)
+        mag = c & 0x7F
+        return np.where(c & 0x80, -mag, mag)
+    return np.abs(ordinal(a) - ordinal(b))
