@@ -53,6 +53,10 @@ def _load() -> ctypes.CDLL:
     L.fp8q_status_string.restype = ctypes.c_char_p
     L.fp8q_status_string.argtypes = [i32]
     L.fp8q_last_launch_count.restype = i32
+    L.fp8q_trace_start.argtypes = [i32]
+    L.fp8q_trace_read.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int), i32]
+    L.fp8q_kernel_name.restype = ctypes.c_char_p
+    L.fp8q_kernel_name.argtypes = [i32]
     return L
 
 
