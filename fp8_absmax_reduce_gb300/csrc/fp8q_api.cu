@@ -178,6 +178,14 @@ int validate_mlp(const fp8q_mlp* m, bool backward) {
 
 }  // namespace
 
+int fp8q::device_status_and_sms(unsigned** status, int* num_sms) {
+  DevInfo d;
+  if (device_info(&d)) return FP8Q_ERR_CUDA;
+  *status = d.status;
+  *num_sms = d.num_sms;
+  return FP8Q_OK;
+}
+
 extern "C" {
 
 // ---------------------------------------------------------------------------

@@ -20,6 +20,10 @@ struct Launch {
   int* launches;     // incremented once per kernel launch
 };
 
+// Device address of the library's status word and the SM count of the current
+// device (resolved once per device).  Returns 0 on success.
+int device_status_and_sms(unsigned** status, int* num_sms);
+
 // Per-tensor absmax quantization: pass 1 writes *P partials, pass 2 casts.
 cudaError_t launch_absmax_partial(const void* x, int dtype, int64_t n, uint32_t* partial, int* P,
                                   const Launch& L);

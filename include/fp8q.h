@@ -90,6 +90,29 @@ FP8Q_API size_t fp8_quantize_absmax_workspace_size(int64_t n);
 FP8Q_API int fp8_quantize_absmax(const void* x, fp8q_dtype x_dtype, int64_t n, fp8q_fmt fmt, uint8_t* q,
                         float* scal, void* ws, size_t ws_bytes, fp8q_stream stream);
 
+/* The same quantization for callers that cannot allocate device memory, so
+ * cannot provide the workspace above: code running while a CUDA graph is
+ * being captured (cudaMalloc is not allowed then), code inside a framework
+ * that owns every allocation through its own pool, and latency-critical loops
+ * that must avoid cudaMalloc/cudaFree because they synchronize the device.
+ * The pages have no counterpart; this is an interface convenience.
+ *
+ * The scratch (1024 absmax partials, 4 KiB) is a fixed array in the library's
+ * own device memory: one copy per GPU that loads the library, held until the
+ * process exits.  Every call on a device shares it and it keeps the last
+ * call's contents; nothing needs clearing (each call overwrites the partials
+ * it reads).  Two calls whose kernels overlap on the GPU (different streams
+ * without ordering) race on the array and give wrong results.  The first call
+ * on each device looks up the array's device address (cudaGetSymbolAddress);
+ * make that first call before any stream capture.  No cudaMalloc, cudaFree or
+ * other allocating routine is called.  Inputs and outputs are the caller's, as
+ * for fp8_quantize_absmax, with the same results bit for bit.  Returns
+ * FP8Q_ERR_INVALID_ARG for bad arguments or a tensor that would need more
+ * than the 1024 partials (the first pass is capped at 1024 blocks, so every
+ * n >= 1 fits); a non-finite amax sets FP8Q_STATUS_NONFINITE as usual. */
+FP8Q_API int fp8_quantize_absmax_noalloc(const void* x, fp8q_dtype x_dtype, int64_t n, fp8q_fmt fmt, uint8_t* q,
+                                         float* scal, fp8q_stream stream);
+
 /* ------------------------------------------------------------------------ */
 /* Scaled FP8 GEMM (LLMQ §4: FP8 matmuls dominate; backward dgrad/wgrad use  */
 /* the transposed layouts without separate transpose buffers).              */
