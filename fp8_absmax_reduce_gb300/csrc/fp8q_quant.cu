@@ -300,9 +300,32 @@ __global__ void __launch_bounds__(kThreads) k_swiglu_cast(const uint16_t* __rest
 // RMSNorm backward + residual.  A block owns kBwdRows rows; thread t owns the
 // 8-column groups j = 8 (t + 256 c), c < NG.  Per row: nh = x rstd, u = dN g,
 // dot = sum_j u nh (block reduction, fixed order), dX = dY + rstd (u - nh dot/d).
+// The next row's dN and x are loaded while the current row is reduced.
 // dg partials accumulate per block in registers (fixed row order) and are
 // reduced over blocks in a fixed order by k_dg_finalize.
 // ---------------------------------------------------------------------------
+template <int NG>
+struct BwdRow {
+  uint4 d0[NG], d1[NG], xv[NG];
+};
+
+template <int NG>
+__device__ __forceinline__ void bwd_load_row(BwdRow<NG>& r, const float* __restrict__ dN,
+                                             const uint16_t* __restrict__ x, int64_t row, int d, int t) {
+#pragma unroll
+  for (int c = 0; c < NG; ++c) {
+    const int j0 = 8 * (t + kThreads * c);
+    if (j0 < d) {
+      const float* dn = dN + row * d + j0;
+      r.d0[c] = ld_nc_v4(dn);
+      r.d1[c] = ld_nc_v4(dn + 4);
+      r.xv[c] = ld_nc_v4(x + row * d + j0);
+    } else {
+      r.d0[c] = r.d1[c] = r.xv[c] = make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
 template <int NG>
 __global__ void __launch_bounds__(kThreads) k_rmsnorm_bwd(const float* __restrict__ dN,
                                                           const uint16_t* __restrict__ x,
@@ -327,34 +350,37 @@ __global__ void __launch_bounds__(kThreads) k_rmsnorm_bwd(const float* __restric
     }
   }
   const float inv_d = 1.0f / (float)d;
-  for (int rr = 0; rr < kBwdRows; ++rr) {
-    const int64_t row = (int64_t)blockIdx.x * kBwdRows + rr;
-    if (row >= T) break;
+  const int64_t r0 = (int64_t)blockIdx.x * kBwdRows;
+  const int nrows = (int)((T - r0) < kBwdRows ? (T - r0) : kBwdRows);
+  BwdRow<NG> cur;
+  bwd_load_row<NG>(cur, dN, x, r0, d, t);
+  for (int rr = 0; rr < nrows; ++rr) {
+    const int64_t row = r0 + rr;
+    BwdRow<NG> nxt;
+    if (rr + 1 < nrows) bwd_load_row<NG>(nxt, dN, x, row + 1, d, t);
+    uint4 yv[NG];
+#pragma unroll
+    for (int c = 0; c < NG; ++c) {
+      const int j0 = 8 * (t + kThreads * c);
+      yv[c] = j0 < d ? ld_nc_v4(dY + row * d + j0) : make_uint4(0, 0, 0, 0);
+    }
     const float rs = rstd[row];
     float nh[NG][8], u[NG][8];
     float dot = 0.0f;
 #pragma unroll
     for (int c = 0; c < NG; ++c) {
-      const int j0 = 8 * (t + kThreads * c);
-      if (j0 < d) {
-        const float* dn = dN + row * d + j0;
-        const uint4 d0 = ld_nc_v4(dn), d1 = ld_nc_v4(dn + 4);
-        const uint4 xv = ld_nc_v4(x + row * d + j0);
-        const float dnv[8] = {__uint_as_float(d0.x), __uint_as_float(d0.y), __uint_as_float(d0.z),
-                              __uint_as_float(d0.w), __uint_as_float(d1.x), __uint_as_float(d1.y),
-                              __uint_as_float(d1.z), __uint_as_float(d1.w)};
-        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+      const float dnv[8] = {__uint_as_float(cur.d0[c].x), __uint_as_float(cur.d0[c].y),
+                            __uint_as_float(cur.d0[c].z), __uint_as_float(cur.d0[c].w),
+                            __uint_as_float(cur.d1[c].x), __uint_as_float(cur.d1[c].y),
+                            __uint_as_float(cur.d1[c].z), __uint_as_float(cur.d1[c].w)};
+      const uint32_t xw[4] = {cur.xv[c].x, cur.xv[c].y, cur.xv[c].z, cur.xv[c].w};
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float xk = (k & 1) ? bf16_hi(xw[k >> 1]) : bf16_lo(xw[k >> 1]);
-          nh[c][k] = xk * rs;
-          u[c][k] = dnv[k] * gv[c][k];
-          dot += u[c][k] * nh[c][k];
-          dga[c][k] += dnv[k] * nh[c][k];
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) { nh[c][k] = 0.0f; u[c][k] = 0.0f; }
+      for (int k = 0; k < 8; ++k) {
+        const float xk = (k & 1) ? bf16_hi(xw[k >> 1]) : bf16_lo(xw[k >> 1]);
+        nh[c][k] = xk * rs;
+        u[c][k] = dnv[k] * gv[c][k];
+        dot += u[c][k] * nh[c][k];
+        dga[c][k] += dnv[k] * nh[c][k];
       }
     }
 #pragma unroll
@@ -369,8 +395,7 @@ __global__ void __launch_bounds__(kThreads) k_rmsnorm_bwd(const float* __restric
     for (int c = 0; c < NG; ++c) {
       const int j0 = 8 * (t + kThreads * c);
       if (j0 < d) {
-        const uint4 yv = ld_nc_v4(dY + row * d + j0);
-        const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
+        const uint32_t yw[4] = {yv[c].x, yv[c].y, yv[c].z, yv[c].w};
         uint32_t o[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -381,6 +406,7 @@ __global__ void __launch_bounds__(kThreads) k_rmsnorm_bwd(const float* __restric
         st_v4(dX + row * d + j0, make_uint4(o[0], o[1], o[2], o[3]));
       }
     }
+    if (rr + 1 < nrows) cur = nxt;
   }
 #pragma unroll
   for (int c = 0; c < NG; ++c) {
@@ -395,13 +421,25 @@ __global__ void __launch_bounds__(kThreads) k_rmsnorm_bwd(const float* __restric
   }
 }
 
+// dg[j] = sum over the nblk partial rows, in a fixed order: a block owns 32 columns;
+// thread (ty, tx) sums rows ty, ty+8, ... of column j0+tx, then the 8 partial sums
+// are added in ty order.
 __global__ void __launch_bounds__(kThreads) k_dg_finalize(const float* __restrict__ dg_partial, int nblk, int d,
                                                           float* __restrict__ dg) {
-  const int j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= d) return;
+  __shared__ float part[8][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int j = blockIdx.x * 32 + tx;
   float s = 0.0f;
-  for (int b = 0; b < nblk; ++b) s += dg_partial[(int64_t)b * d + j];
-  dg[j] = s;
+  if (j < d)
+    for (int b = ty; b < nblk; b += 8) s += dg_partial[(int64_t)b * d + j];
+  part[ty][tx] = s;
+  __syncthreads();
+  if (ty == 0 && j < d) {
+    float tot = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) tot += part[k][tx];
+    dg[j] = tot;
+  }
 }
 
 }  // namespace
@@ -483,7 +521,7 @@ cudaError_t launch_rmsnorm_bwd(const float* dN, const uint16_t* x, const uint16_
   }
   cudaError_t e = post_launch(L);
   if (e != cudaSuccess) return e;
-  k_dg_finalize<<<(d + kThreads - 1) / kThreads, kThreads, 0, L.stream>>>(dg_partial, nblk, d, dg);
+  k_dg_finalize<<<(d + 31) / 32, kThreads, 0, L.stream>>>(dg_partial, nblk, d, dg);
   return post_launch(L);
 }
 
