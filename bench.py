@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--cpu-sample-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the workload's T (same d, f, distributions); for small profiling runs")
     return ap.parse_args()
 
 
@@ -131,8 +133,8 @@ def step_work(w: synth.Workload):
         ("absmax_partial", 2 * d * 2 * f, 0), ("quant_cast", 3 * d * 2 * f, 0),
         ("absmax_partial", 2 * f * d, 0), ("quant_cast", 3 * f * d, 0),
         ("rmsnorm_stats", 2 * T * d + 2 * d + 4 * T, 0), ("rmsnorm_cast", 3 * T * d + 4 * T + 2 * d, 0),
-        ("gemm_gate_up_swiglu", T * d + d * 2 * f + 2 * T * 2 * f, 2.0 * T * d * 2 * f),
-        ("swiglu_cast", 2 * T * 2 * f + T * f, 0),
+        ("gemm_gate_up_swiglu", T * d + d * 2 * f + 2 * T * 2 * f + 4 * T * f, 2.0 * T * d * 2 * f),
+        ("quant_cast", 5 * T * f, 0),
         ("gemm_down_residual", T * f + f * d + 4 * T * d, 2.0 * T * f * d),
     ]
     bwd = [
@@ -154,7 +156,7 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = synth.BY_NAME[args.workload]
+    w = args.w
     flops = w.gemm_flops()
     inp = synth.mlp_inputs(w, seed=rank)
     b = fq.MlpBuffers.allocate(w.T, w.d, w.f, device=dev, backward=w.backward)
@@ -298,6 +300,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     w = synth.BY_NAME[args.workload]
+    if args.tokens:
+        import dataclasses
+        w = dataclasses.replace(w, T=args.tokens)
     pk = peaks()
     fp8_peak = pk["bf16_sustained"] * FP8_PER_BF16
 
@@ -326,6 +331,7 @@ def main():
     import torch
     if world > 1:
         torch.distributed.init_process_group("nccl")
+    args.w = w
     r = run_ours(args, rank, world, local_rank)
     if rank != 0:
         if world > 1:

@@ -14,7 +14,10 @@
 //   warps 4..11 epilogue, two warpgroups: warp w reads TMEM lanes
 //               32*(w%4)..+31 (= 32 rows); warpgroup 0 takes the first half
 //               of the accumulator columns, warpgroup 1 the second half;
-//               scale by alpha = sinvA * sinvB, fused op, vector stores.
+//               scale by alpha = sinvA * sinvB, fused op, then each warp
+//               writes its 32x32 output block into a swizzled 4 KB shared
+//               staging buffer and stores it with one TMA tensor store
+//               (coalesced, clipped at the tensor edges).
 // Operands may be K-major or MN-major in global memory (NN/NT/TN layouts
 // without transpose copies): TMA boxes are 128 B wide along the contiguous
 // dimension with the 128-byte swizzle, and the UMMA shared-memory descriptors
@@ -38,8 +41,11 @@ constexpr int kStage = kATile + 2 * kBHalf;
 constexpr int kThreads = 384;   // warps 0-3: TMA / MMA / TMEM / idle; warps 4-11: epilogue
 constexpr int kEpiThreads = 256;
 constexpr int kTmemCols = 512;
-constexpr int kBarOffset = STAGES * kStage;
+constexpr int kStagingBytes = 4096;                  // per epilogue warp
+constexpr int kStagingOffset = STAGES * kStage;
+constexpr int kBarOffset = kStagingOffset + 8 * kStagingBytes;
 constexpr int kSmemBytes = kBarOffset + 256 + 1024;  // + barriers + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr int kGroupM = 16;                          // M tiles per rasterisation group
 
 struct Args {
@@ -54,6 +60,7 @@ struct Args {
   int64_t ldc;
   const uint16_t* R;
   int64_t ldr;
+  float* aux;  // kEpiSwiglu: the fp32 SwiGLU output a [M, N] (ld = N), or null
   uint32_t* amax_partial;
   unsigned* status;
 };
@@ -69,14 +76,53 @@ __device__ __forceinline__ void tile_coords(int tile, const Args& p, int& mb, in
 }
 
 // ---------------------------------------------------------------------------
-// Epilogue helpers: one thread = one output row, 32 consecutive columns.
+// Epilogue helpers.  One thread = one output row of its warp's 32-row slice;
+// a chunk is 32 consecutive columns.  Outputs go through the warp's staging
+// buffer: 32 x 32 bf16 in the 64-byte-swizzle layout (64 B rows) or 32 x 32
+// fp32 in the 128-byte-swizzle layout (128 B rows), matching the tensor maps.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float (&v)[32]) {
+__device__ __forceinline__ float round_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void stage_bf16(uint32_t buf, int r, const float (&v)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q)
-    st_v4(dst + 8 * q, make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                                  pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7])));
+    st_shared_v4(buf + r * 64 + ((q ^ ((r >> 1) & 3)) << 4),
+                 make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                            pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7])));
 }
+__device__ __forceinline__ void stage_f32(uint32_t buf, int r, const float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    st_shared_v4(buf + r * 128 + ((q ^ (r & 7)) << 4),
+                 make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]), __float_as_uint(v[4 * q + 2]),
+                            __float_as_uint(v[4 * q + 3])));
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tm), "r"(src),
+               "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// The staging buffer may be rewritten once the warp's previous stores have read it.
+__device__ __forceinline__ void staging_acquire(int lane) {
+  if (lane == 0) bulk_wait_read_all();
+  __syncwarp();
+}
+// Make this warp's shared-memory writes visible to the TMA engine.
+__device__ __forceinline__ void staging_publish() {
+  fence_async_shared();
+  __syncwarp();
+}
+
 __device__ __forceinline__ void load_bf16x32(const uint16_t* src, float (&v)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -86,115 +132,29 @@ __device__ __forceinline__ void load_bf16x32(const uint16_t* src, float (&v)[32]
     for (int k = 0; k < 4; ++k) { v[8 * q + 2 * k] = bf16_lo(ww[k]); v[8 * q + 2 * k + 1] = bf16_hi(ww[k]); }
   }
 }
-__device__ __forceinline__ float round_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
-// Columns [col, col + ncol) of the chunk are valid (ncol <= 32); the full chunk
-// takes the vector path.
-__device__ __forceinline__ void epi_store(const Args& p, int row, int col, int ncol, const uint32_t (&acc)[32], float alpha) {
-  float v[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(alpha, __uint_as_float(acc[j]));
-  if (p.epi == kEpiResidual) {
-    const uint16_t* r = p.R + (int64_t)row * p.ldr + col;
-    if (ncol == 32) {
-      float rv[32];
-      load_bf16x32(r, rv);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = __fadd_rn(rv[j], v[j]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < ncol) v[j] = __fadd_rn(__uint_as_float((uint32_t)r[j] << 16), v[j]);
-    }
-  }
-  if (p.out_f32) {
-    float* dst = reinterpret_cast<float*>(p.C) + (int64_t)row * p.ldc + col;
-    if (ncol == 32) {
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        st_v4(dst + 4 * q, make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
-                                      __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3])));
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < ncol) dst[j] = v[j];
-    }
-  } else {
-    uint16_t* dst = reinterpret_cast<uint16_t*>(p.C) + (int64_t)row * p.ldc + col;
-    if (ncol == 32) {
-      store_bf16x32(dst, v);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < ncol) dst[j] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
-    }
-  }
-}
-
-// Gate columns [col, col+ncol) of f, with the matching up columns f + col.
-// H = bf16(alpha * acc); a = silu(H_gate) * H_up; running absmax of a.
-__device__ __forceinline__ void epi_swiglu(const Args& p, int row, int col, int ncol, const uint32_t (&ag)[32],
-                           const uint32_t (&au)[32], float alpha, uint32_t& amax) {
-  float hg[32], hu[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    hg[j] = round_bf16(__fmul_rn(alpha, __uint_as_float(ag[j])));
-    hu[j] = round_bf16(__fmul_rn(alpha, __uint_as_float(au[j])));
-  }
-  uint16_t* hrow = reinterpret_cast<uint16_t*>(p.C) + (int64_t)row * p.ldc;
-  if (ncol == 32) {
-    store_bf16x32(hrow + col, hg);
-    store_bf16x32(hrow + p.N + col, hu);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) amax = max(amax, abs_bits(swiglu_ref(hg[j], hu[j])));
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      if (j < ncol) {
-        hrow[col + j] = __bfloat16_as_ushort(__float2bfloat16_rn(hg[j]));
-        hrow[p.N + col + j] = __bfloat16_as_ushort(__float2bfloat16_rn(hu[j]));
-        amax = max(amax, abs_bits(swiglu_ref(hg[j], hu[j])));
-      }
-    }
-  }
-}
-
-// dA = alpha * acc for gate columns [col, col+ncol); with h = H_gate, u = H_up,
-// s = sigmoid(h): dH_gate = dA u s (1 + h (1 - s)), dH_up = dA h s (bf16), absmax.
+// dA = alpha * acc; with h = H_gate, u = H_up, s = sigmoid(h):
+// dH_gate = dA u s (1 + h (1 - s)), dH_up = dA h s, both rounded to bf16.
+// dH is a GEMM output checked against the oracle with a tolerance, so the
+// sigmoid may use the fast hardware exponential and reciprocal.
 __device__ __forceinline__ void swiglu_bwd1(float da, float h, float u, float& dg, float& du) {
-  // dH is a GEMM output checked against the oracle with a tolerance, so the
-  // sigmoid may use the fast hardware exponential and reciprocal.
   const float s = __fdividef(1.0f, 1.0f + __expf(-h));
   const float hs = h * s;
   dg = round_bf16(da * u * (s + hs * (1.0f - s)));
   du = round_bf16(da * hs);
 }
 
-__device__ __forceinline__ void epi_swiglu_bwd(const Args& p, int row, int col, int ncol, const uint32_t (&acc)[32], float alpha,
-                               uint32_t& amax) {
+// H words of one 32-column chunk of a row: gate in h[0..3], up in h[4..7]
+// (8 bf16 each); columns at or beyond ncol read as zero.
+__device__ __forceinline__ void load_h_chunk(const Args& p, int row, int col, int ncol, uint4 (&h)[8]) {
   const uint16_t* hrow = p.R + (int64_t)row * p.ldr;
-  uint16_t* drow = reinterpret_cast<uint16_t*>(p.C) + (int64_t)row * p.ldc;
-  if (ncol == 32) {
-    float h[32], u[32], dg[32], du[32];
-    load_bf16x32(hrow + col, h);
-    load_bf16x32(hrow + p.N + col, u);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      swiglu_bwd1(__fmul_rn(alpha, __uint_as_float(acc[j])), h[j], u[j], dg[j], du[j]);
-      amax = max(amax, max(abs_bits(dg[j]), abs_bits(du[j])));
-    }
-    store_bf16x32(drow + col, dg);
-    store_bf16x32(drow + p.N + col, du);
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      if (j >= ncol) continue;
-      float dg, du;
-      swiglu_bwd1(__fmul_rn(alpha, __uint_as_float(acc[j])), __uint_as_float((uint32_t)hrow[col + j] << 16),
-                  __uint_as_float((uint32_t)hrow[p.N + col + j] << 16), dg, du);
-      amax = max(amax, max(abs_bits(dg), abs_bits(du)));
-      drow[col + j] = __bfloat16_as_ushort(__float2bfloat16_rn(dg));
-      drow[p.N + col + j] = __bfloat16_as_ushort(__float2bfloat16_rn(du));
+  for (int q = 0; q < 4; ++q) {
+    if (8 * q < ncol) {
+      h[q] = ld_v4(hrow + col + 8 * q);
+      h[4 + q] = ld_v4(hrow + p.N + col + 8 * q);
+    } else {
+      h[q] = h[4 + q] = make_uint4(0, 0, 0, 0);
     }
   }
 }
@@ -202,9 +162,13 @@ __device__ __forceinline__ void epi_swiglu_bwd(const Args& p, int row, int col, 
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
+// Output maps: tmC (C, or the gate half of H / dH), tmC2 (the up half), tmAux
+// (the fp32 SwiGLU output a); unused ones are copies of tmC.
 template <int A_MN, int B_MN>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_gemm_f8(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Args p) {
+    k_gemm_f8(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
+              const __grid_constant__ CUtensorMap tmAux, const Args p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOffset);
@@ -225,7 +189,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     *cta_amax = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmA); tma_prefetch_desc(&tmB); }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
+  }
   if (warp == 2) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
@@ -320,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue ----------------
     const int sub = warp & 3;
     const int half = (warp - 4) >> 2;  // which half of the accumulator columns
+    const uint32_t buf = smem_addr(smem + kStagingOffset + (warp - 4) * kStagingBytes);
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t amax = 0;
@@ -334,8 +303,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(sub * 32) << 16);
-      const int row = mb * BM + sub * 32 + lane;
+      const int row0 = mb * BM + sub * 32;
+      const int row = row0 + lane;
       const bool row_ok = row < p.M;
+      const bool warp_ok = row0 < p.M;  // any row of this warp's slice in range
       if (p.epi == kEpiSwiglu) {
         const int col0 = nb * 128;
 #pragma unroll 1
@@ -344,19 +315,110 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32x2(tbase + c * 32, tbase + 128 + c * 32, ag, au);
           const int col = col0 + c * 32;
           const int ncol = min(32, p.N - col);
-          if (row_ok && ncol > 0) epi_swiglu(p, row, col, ncol, ag, au, alpha, amax);
+          float hg[32], hu[32], a[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            hg[j] = round_bf16(__fmul_rn(alpha, __uint_as_float(ag[j])));
+            hu[j] = round_bf16(__fmul_rn(alpha, __uint_as_float(au[j])));
+            a[j] = swiglu_ref(hg[j], hu[j]);
+            if (row_ok && j < ncol) amax = max(amax, abs_bits(a[j]));
+          }
+          if (warp_ok && ncol > 0) {
+            staging_acquire(lane);
+            stage_bf16(buf, lane, hg);
+            stage_bf16(buf + 2048, lane, hu);
+            staging_publish();
+            if (lane == 0) {
+              tma_store_2d(&tmC, buf, col, row0);
+              tma_store_2d(&tmC2, buf + 2048, col, row0);
+              bulk_commit();
+            }
+            if (p.aux) {
+              staging_acquire(lane);
+              stage_f32(buf, lane, a);
+              staging_publish();
+              if (lane == 0) {
+                tma_store_2d(&tmAux, buf, col, row0);
+                bulk_commit();
+              }
+            }
+          }
+        }
+      } else if (p.epi == kEpiSwigluBwd) {
+        // the next chunk's H words are in flight while the current chunk is computed
+        const int col0 = nb * BN;
+        uint4 hn[8];
+        {
+          const int col = col0 + 4 * half * 32;
+          if (row_ok && col < p.N) load_h_chunk(p, row, col, min(32, p.N - col), hn);
+        }
+#pragma unroll 1
+        for (int c = 4 * half; c < 4 * half + 4; ++c) {
+          uint4 hc[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) hc[q] = hn[q];
+          const int col = col0 + c * 32;
+          if (c + 1 < 4 * half + 4 && row_ok && col + 32 < p.N) load_h_chunk(p, row, col + 32, min(32, p.N - col - 32), hn);
+          uint32_t acc32[32];
+          tmem_ld32(tbase + c * 32, acc32);
+          const int ncol = min(32, p.N - col);
+          if (!warp_ok || ncol <= 0) continue;
+          float dg[32], du[32];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t gw[4] = {hc[q].x, hc[q].y, hc[q].z, hc[q].w};
+            const uint32_t uw[4] = {hc[4 + q].x, hc[4 + q].y, hc[4 + q].z, hc[4 + q].w};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int j = 8 * q + k;
+              const float h = (k & 1) ? bf16_hi(gw[k >> 1]) : bf16_lo(gw[k >> 1]);
+              const float u = (k & 1) ? bf16_hi(uw[k >> 1]) : bf16_lo(uw[k >> 1]);
+              swiglu_bwd1(__fmul_rn(alpha, __uint_as_float(acc32[j])), h, u, dg[j], du[j]);
+              if (row_ok && j < ncol) amax = max(amax, max(abs_bits(dg[j]), abs_bits(du[j])));
+            }
+          }
+          staging_acquire(lane);
+          stage_bf16(buf, lane, dg);
+          stage_bf16(buf + 2048, lane, du);
+          staging_publish();
+          if (lane == 0) {
+            tma_store_2d(&tmC, buf, col, row0);
+            tma_store_2d(&tmC2, buf + 2048, col, row0);
+            bulk_commit();
+          }
         }
       } else {
         const int col0 = nb * BN;
 #pragma unroll 1
         for (int c = 4 * half; c < 4 * half + 4; ++c) {
-          uint32_t a[32];
-          tmem_ld32(tbase + c * 32, a);
+          uint32_t acc32[32];
+          tmem_ld32(tbase + c * 32, acc32);
           const int col = col0 + c * 32;
           const int ncol = min(32, p.N - col);
-          if (row_ok && ncol > 0) {
-            if (p.epi == kEpiSwigluBwd) epi_swiglu_bwd(p, row, col, ncol, a, alpha, amax);
-            else epi_store(p, row, col, ncol, a, alpha);
+          if (!warp_ok || ncol <= 0) continue;
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(alpha, __uint_as_float(acc32[j]));
+          if (p.epi == kEpiResidual && row_ok) {
+            const uint16_t* r = p.R + (int64_t)row * p.ldr + col;
+            if (ncol == 32) {
+              float rv[32];
+              load_bf16x32(r, rv);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = __fadd_rn(rv[j], v[j]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j < ncol) v[j] = __fadd_rn(__uint_as_float((uint32_t)r[j] << 16), v[j]);
+            }
+          }
+          staging_acquire(lane);
+          if (p.out_f32) stage_f32(buf, lane, v);
+          else stage_bf16(buf, lane, v);
+          staging_publish();
+          if (lane == 0) {
+            tma_store_2d(&tmC, buf, col, row0);
+            bulk_commit();
           }
         }
       }
@@ -364,6 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&tempty[acc]);
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
+    if (lane == 0) bulk_wait_all();  // every TMA store of this warp has completed
     amax = warp_max_u32(amax);
     if (lane == 0) atomicMax(cta_amax, amax);
   }
@@ -409,6 +472,23 @@ bool make_tmap(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, i
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Output tensor [rows, cols] (row stride ld elements) of bf16 or fp32, stored in
+// 32 x 32 element boxes: bf16 boxes are 64 B wide (64-byte swizzle), fp32 boxes
+// 128 B wide (128-byte swizzle), matching stage_bf16 / stage_f32.
+bool make_out_tmap(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t ld, bool f32) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  const int64_t es = f32 ? 4 : 2;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)(ld * es)};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Instruction descriptor for kind::f8f6f4: fp32 accumulator, A/B formats
 // (E4M3 = 0, E5M2 = 1), operand major-ness (bit 15 A, bit 16 B; 1 = MN-major),
 // N >> 3 at bit 17, M >> 4 at bit 24.
@@ -418,7 +498,8 @@ uint32_t make_idesc(int fmtA, int fmtB, int a_mn, int b_mn) {
 }
 
 template <int A_MN, int B_MN>
-cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const Args& a, int grid, cudaStream_t s) {
+cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tc2,
+                     const CUtensorMap& taux, const Args& a, int grid, cudaStream_t s) {
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -428,7 +509,7 @@ cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const Args& a
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  k_gemm_f8<A_MN, B_MN><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, a);
+  k_gemm_f8<A_MN, B_MN><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, tc, tc2, taux, a);
   return cudaGetLastError();
 }
 
@@ -447,6 +528,7 @@ cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L) {
   a.ldc = g.ldc;
   a.R = g.R;
   a.ldr = g.ldr;
+  a.aux = g.aux;
   a.amax_partial = g.amax_partial;
   a.status = L.status;
   a.idesc = make_idesc(g.fmtA, g.fmtB, g.a_mn, g.b_mn);
@@ -463,18 +545,29 @@ cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L) {
   a.k_blocks = (g.K + BK - 1) / BK;
   a.num_tiles = a.m_tiles * a.n_tiles;
 
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc, tc2, taux;
   const bool ok_a = g.a_mn ? make_tmap(&ta, g.A, g.M, g.K, g.lda) : make_tmap(&ta, g.A, g.K, g.M, g.lda);
   const bool ok_b = g.b_mn ? make_tmap(&tb, g.B, g.b_cols, g.K, g.ldb) : make_tmap(&tb, g.B, g.K, g.b_cols, g.ldb);
-  if (!ok_a || !ok_b) return cudaErrorInvalidValue;
+  bool ok_c;
+  if (g.epi == kEpiSwiglu || g.epi == kEpiSwigluBwd) {
+    // gate half [M, f] and up half [M, f] of the [M, 2f] output, each clipped at f
+    const uint16_t* c = static_cast<const uint16_t*>(g.C);
+    ok_c = make_out_tmap(&tc, c, g.N, g.M, g.ldc, false) && make_out_tmap(&tc2, c + g.N, g.N, g.M, g.ldc, false);
+    taux = tc;
+    if (ok_c && g.aux) ok_c = make_out_tmap(&taux, g.aux, g.N, g.M, g.N, true);
+  } else {
+    ok_c = make_out_tmap(&tc, g.C, g.N, g.M, g.ldc, g.out_f32 != 0);
+    tc2 = taux = tc;
+  }
+  if (!ok_a || !ok_b || !ok_c) return cudaErrorInvalidValue;
 
   const int grid = a.num_tiles < L.num_sms ? a.num_tiles : L.num_sms;
   *P = grid;
   cudaError_t e;
-  if (g.a_mn == 0 && g.b_mn == 1) e = launch_t<0, 1>(ta, tb, a, grid, L.stream);
-  else if (g.a_mn == 0 && g.b_mn == 0) e = launch_t<0, 0>(ta, tb, a, grid, L.stream);
-  else if (g.a_mn == 1 && g.b_mn == 1) e = launch_t<1, 1>(ta, tb, a, grid, L.stream);
-  else e = launch_t<1, 0>(ta, tb, a, grid, L.stream);
+  if (g.a_mn == 0 && g.b_mn == 1) e = launch_t<0, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
+  else if (g.a_mn == 0 && g.b_mn == 0) e = launch_t<0, 0>(ta, tb, tc, tc2, taux, a, grid, L.stream);
+  else if (g.a_mn == 1 && g.b_mn == 1) e = launch_t<1, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
+  else e = launch_t<1, 0>(ta, tb, tc, tc2, taux, a, grid, L.stream);
   if (L.launches) ++*L.launches;
   return e;
 }

@@ -53,7 +53,7 @@ cudaError_t launch_rmsnorm_bwd(const float* dN, const uint16_t* x, const uint16_
 enum GemmEpilogue {
   kEpiStore = 0,      // C = alpha * acc (bf16 or fp32)
   kEpiResidual = 1,   // C = bf16(R + alpha * acc)
-  kEpiSwiglu = 2,     // H = bf16(alpha * acc) for paired gate/up columns + absmax of SwiGLU(H)
+  kEpiSwiglu = 2,     // H = bf16(alpha * acc) for paired gate/up columns, a = SwiGLU(H), absmax of a
   kEpiSwigluBwd = 3,  // dH = bf16(SwiGLU'(H) * alpha * acc) + absmax of dH
 };
 
@@ -67,6 +67,7 @@ struct GemmProblem {
   int epi; int out_f32;
   void* C; int64_t ldc;  // kEpiSwiglu/kEpiSwigluBwd: [M, 2f] gate | up
   const uint16_t* R; int64_t ldr;  // residual (kEpiResidual) or H (kEpiSwigluBwd)
+  float* aux;                      // kEpiSwiglu: optional fp32 SwiGLU output a [M, N]
   uint32_t* amax_partial;          // per-CTA partials for the two SwiGLU epilogues
 };
 // Launches the persistent tcgen05 GEMM; *P receives the number of partials written.
