@@ -55,24 +55,25 @@ __device__ __forceinline__ void scale_from_amax(float amax, int fmt, float& s, f
 
 // e^x as a fixed sequence of single-rounding fp32 operations: Cody-Waite
 // reduction x = k*ln2 + r (ln2 split into a 9-bit high part, so k*hi is exact,
-// plus a low correction), the degree-8 Taylor polynomial of e^r in Horner
-// form, and multiplication by 2^k assembled from exponent bits (two steps
-// when the result is subnormal).  Same answer on every run and every GPU.
+// plus a low correction) and the degree-8 Taylor polynomial of e^r in Horner
+// form, both as fused multiply-adds, then multiplication by 2^k assembled
+// from exponent bits (two steps when the result is subnormal).  Same answer
+// on every run and every GPU.
 __device__ __forceinline__ float exp_ref(float x) {
   if (x != x) return x;
   if (x > 88.72283935546875f) return __int_as_float(0x7F800000);
   if (x < -103.972084045410156f) return 0.0f;
   const float kf = rintf(__fmul_rn(x, 1.44269502162933349609375f));
-  const float r = __fsub_rn(__fsub_rn(x, __fmul_rn(kf, 0.693359375f)), __fmul_rn(kf, -2.12194440e-4f));
+  const float r = __fmaf_rn(-kf, -2.12194440e-4f, __fmaf_rn(-kf, 0.693359375f, x));
   float p = 1.0f / 40320.0f;
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 5040.0f);
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 720.0f);
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 120.0f);
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 24.0f);
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f / 6.0f);
-  p = __fadd_rn(__fmul_rn(p, r), 0.5f);
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  p = __fmaf_rn(p, r, 1.0f / 5040.0f);
+  p = __fmaf_rn(p, r, 1.0f / 720.0f);
+  p = __fmaf_rn(p, r, 1.0f / 120.0f);
+  p = __fmaf_rn(p, r, 1.0f / 24.0f);
+  p = __fmaf_rn(p, r, 1.0f / 6.0f);
+  p = __fmaf_rn(p, r, 0.5f);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
   const int k = (int)kf;
   if (k > 127) return __fmul_rn(__fmul_rn(p, 2.0f), __uint_as_float((uint32_t)(127 + 127) << 23));
   if (k >= -126) return __fmul_rn(p, __uint_as_float((uint32_t)(k + 127) << 23));

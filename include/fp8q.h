@@ -150,8 +150,8 @@ FP8Q_API int rmsnorm_quant(const void* x, const void* g, int64_t T, int64_t d, f
 /* ------------------------------------------------------------------------ */
 /* H [T,2f] bf16 (gate in columns [0,f), up in [f,2f)) -> q [T,f] of fmt.
  * a = fl32(fl32(h / fl32(1 + exp_ref(-h))) * u) in fp32; exp_ref is a fixed
- * fp32 sequence (Cody-Waite reduction, degree-8 Taylor polynomial), so the
- * result is bit-reproducible.  Requirements: T >= 1, f multiple of 16. */
+ * fp32 sequence (Cody-Waite reduction and a degree-8 Taylor polynomial in
+ * fused multiply-adds), so the result is bit-reproducible.  Requirements: T >= 1, f multiple of 16. */
 FP8Q_API size_t swiglu_quant_workspace_size(int64_t T, int64_t f);
 FP8Q_API int swiglu_quant(const void* H, int64_t T, int64_t f, fp8q_fmt fmt, uint8_t* q, float* scal,
                  void* ws, size_t ws_bytes, fp8q_stream stream);

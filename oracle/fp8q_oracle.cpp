@@ -134,8 +134,10 @@ uint8_t fp8_encode(float v, int fmt) {
 // one bit-exact answer.  Method: Cody & Waite argument reduction
 // x = k ln2 + r with ln2 split in a short high part (exact k*hi) and a low
 // correction, |r| <= ln2/2, then the Taylor polynomial of e^r to degree 8 in
-// Horner form, then multiplication by 2^k built from exponent bits.  Every
-// operation is a single IEEE fp32 operation (no contraction).
+// Horner form, then multiplication by 2^k built from exponent bits.  The
+// reduction and every Horner step are IEEE-754 fused multiply-adds (one
+// rounding each, std::fma); every other operation is a single IEEE fp32
+// operation.
 // ----------------------------------------------------------------------------
 float exp_ref(float x) {
   if (std::isnan(x)) return x;
@@ -145,16 +147,16 @@ float exp_ref(float x) {
   const float ln2_hi = 0.693359375f;                // 355/512, 9 significant bits
   const float ln2_lo = -2.12194440e-4f;             // fp32(ln 2 - 355/512)
   const float kf = std::nearbyint(x * log2e);
-  const float r = (x - kf * ln2_hi) - kf * ln2_lo;
+  const float r = std::fma(-kf, ln2_lo, std::fma(-kf, ln2_hi, x));
   float p = 1.0f / 40320.0f;                        // 1/8!
-  p = p * r + 1.0f / 5040.0f;
-  p = p * r + 1.0f / 720.0f;
-  p = p * r + 1.0f / 120.0f;
-  p = p * r + 1.0f / 24.0f;
-  p = p * r + 1.0f / 6.0f;
-  p = p * r + 0.5f;
-  p = p * r + 1.0f;
-  p = p * r + 1.0f;
+  p = std::fma(p, r, 1.0f / 5040.0f);
+  p = std::fma(p, r, 1.0f / 720.0f);
+  p = std::fma(p, r, 1.0f / 120.0f);
+  p = std::fma(p, r, 1.0f / 24.0f);
+  p = std::fma(p, r, 1.0f / 6.0f);
+  p = std::fma(p, r, 0.5f);
+  p = std::fma(p, r, 1.0f);
+  p = std::fma(p, r, 1.0f);
   const int k = (int)kf;                            // -150 <= k <= 128
   if (k > 127) return (p * 2.0f) * f32_from_bits((uint32_t)(127 + 127) << 23);
   if (k >= -126) return p * f32_from_bits((uint32_t)(k + 127) << 23);
