@@ -125,6 +125,25 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# replicas across ranks (one process per GPU; no exchange in the data path)
+# ---------------------------------------------------------------------------
+def max_over_ranks(v: float, device=None) -> float:
+    """The largest value of v over all ranks (a time: the job is as slow as its slowest rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(v)
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, max_ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return world * units_per_rank / (max_ms * 1e-3)
+
+
+# ---------------------------------------------------------------------------
 # per-launch algorithmic work of one step (order = the library's launch order)
 # ---------------------------------------------------------------------------
 def step_work(w: synth.Workload):
@@ -210,10 +229,7 @@ def run_ours(args, rank, world, local_rank):
     n = lib.fp8q_trace_read(tms, kinds, cap)
     traced = [(lib.fp8q_kernel_name(kinds[i]).decode(), tms[i]) for i in range(max(n, 0))]
 
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
 
     # ---- e2e: pinned host inputs in, every output back out, inside the timed region
     e2e = None
@@ -240,12 +256,8 @@ def run_ours(args, rank, world, local_rank):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1) / Ke
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * flops / (ems * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ems,
+        ems = max_over_ranks(e0.elapsed_time(e1) / Ke, dev)
+        e2e = {"value": job_throughput(flops, world, ems) / 1e12, "unit": "TFLOP/s", "ms_per_step": ems,
                "tokens_per_s": world * w.T / (ems * 1e-3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": Ke}
     return {"ms": ms, "K": K, "launches": launches, "traced": traced, "plan": plan, "clocks": clk.summary(),
@@ -338,7 +350,7 @@ def main():
             torch.distributed.destroy_process_group()
         return
     ms_step = r["ms"] / r["K"]
-    value = world * r["flops"] / (ms_step * 1e-3) / 1e12
+    value = job_throughput(r["flops"], world, ms_step) / 1e12
     kernels, traced_total = kernel_table(r["traced"], r["plan"], r["K"], pk)
     gemm = {k: v for k, v in kernels.items() if k.startswith("gemm")}
     g_ms = sum(v["total_ms"] for v in gemm.values())

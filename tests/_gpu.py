@@ -42,3 +42,24 @@ def code_step_diff(a: np.ndarray, b: np.ndarray) -> np.ndarray:
         mag = c & 0x7F
         return np.where(c & 0x80, -mag, mag)
     return np.abs(ordinal(a) - ordinal(b))
+
+
+def fp8_table(fmt: int) -> np.ndarray:
+    """Values of all 256 FP8 codes, built for property checks without the oracle: the positive
+    finite values are the multiples of the smallest subnormal whose multiplier has at most
+    1 + frac significant bits, up to the format's maximum, in increasing code order."""
+    frac, lsub, vmax = (3, -9, 448.0) if fmt == 0 else (2, -16, 57344.0)
+    kmax = int(vmax / 2.0 ** lsub)
+    ks = sorted({m << j for m in range(1 << (frac + 1)) for j in range(64) if (m << j) <= kmax})
+    pos = np.array([k * 2.0 ** lsub for k in ks])
+    t = np.full(256, np.nan)
+    t[: pos.size] = pos
+    t[128: 128 + pos.size] = -pos
+    if fmt == 1:
+        t[0x7C], t[0xFC] = np.inf, -np.inf
+    return t
+
+
+def bf16_np(t: torch.Tensor) -> np.ndarray:
+    """CUDA bf16 tensor -> float64 values."""
+    return host_f64(t)
