@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--cpu-sample-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--measure-fp8-peak", action="store_true",
+                    help="time cuBLASLt FP8 (torch._scaled_mm) 8192^3, burst and sustained, and exit")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the workload's T (same d, f, distributions); for small profiling runs")
     return ap.parse_args()
@@ -306,8 +308,48 @@ def cpu_baseline(w, tokens):
                       f"({'forward+backward' if w.backward else 'forward'}), single-threaded oracle"}
 
 
+def measure_fp8_peak():
+    """Dense FP8 tensor throughput of the vendor library on this GPU, for context next to the
+    derived peak: torch._scaled_mm (cuBLASLt) E4M3 x E4M3 -> bf16, 8192^3, tensor-wise scales.
+    Burst: best of 10 single timed calls; sustained: back-to-back calls for 4 s."""
+    import torch
+    n = 8192
+    g = torch.Generator(device="cuda").manual_seed(0)
+    a = torch.randn(n, n, device="cuda", generator=g).to(torch.float8_e4m3fn)
+    b = torch.randn(n, n, device="cuda", generator=g).to(torch.float8_e4m3fn).t()
+    one = torch.ones((), device="cuda")
+    mm = lambda: torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+    for _ in range(5):
+        mm()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        mm()
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    flop = 2.0 * n ** 3
+    reps = max(1, int(4000.0 / best))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        e0.record()
+        for _ in range(reps):
+            mm()
+        e1.record()
+        torch.cuda.synchronize()
+    sus = e0.elapsed_time(e1) / reps
+    print(json.dumps({"fp8_cublaslt_tflops_burst": flop / (best * 1e-3) / 1e12,
+                      "fp8_cublaslt_tflops_sustained": flop / (sus * 1e-3) / 1e12, "n": n, "reps": reps,
+                      "clocks": clk.summary(), "torch": torch.__version__}))
+
+
 def main():
     args = parse_args()
+    if args.measure_fp8_peak:
+        measure_fp8_peak()
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
