@@ -74,6 +74,19 @@ class _BlockIO(ctypes.Structure):
     ]
 
 
+class _FullIO(ctypes.Structure):
+    _fields_ = [
+        ("T", ctypes.c_int64), ("d", ctypes.c_int64), ("f", ctypes.c_int64), ("nq", ctypes.c_int64),
+        ("eps", ctypes.c_float), ("exact", ctypes.c_int), ("nthreads", ctypes.c_int),
+        ("att", ctypes.c_void_p), ("g1", ctypes.c_void_p), ("Wqkv", ctypes.c_void_p), ("Wo", ctypes.c_void_p),
+        ("dQKV", ctypes.c_void_p), ("qkv", ctypes.c_void_p), ("h", ctypes.c_void_p), ("rstd1", ctypes.c_void_p),
+        ("Wqkv8", ctypes.c_void_p), ("Wo8", ctypes.c_void_p), ("n1_8", ctypes.c_void_p), ("att8", ctypes.c_void_p),
+        ("scal_attn", ctypes.c_void_p), ("dX", ctypes.c_void_p), ("dWqkv", ctypes.c_void_p),
+        ("dWo", ctypes.c_void_p), ("dg1", ctypes.c_void_p), ("d_att", ctypes.c_void_p), ("dh", ctypes.c_void_p),
+        ("dh8", ctypes.c_void_p), ("dqkv8", ctypes.c_void_p), ("mlp", _BlockIO), ("x", ctypes.c_void_p),
+    ]
+
+
 def lib() -> ctypes.CDLL:
     global _lib
     with _lock:
@@ -99,6 +112,7 @@ def lib() -> ctypes.CDLL:
                                          ctypes.c_int, f32, f32, vp, ctypes.c_int, vp, ctypes.c_int]
             L.fo_block_forward.argtypes = [ctypes.POINTER(_BlockIO)]
             L.fo_block_forward_backward.argtypes = [ctypes.POINTER(_BlockIO)]
+            L.fo_full_block.argtypes = [ctypes.POINTER(_FullIO), ctypes.c_int]
             _lib = L
     return _lib
 
@@ -275,4 +289,61 @@ def block(x, g, Wgu, Wd, dY=None, eps: float = 1e-6, exact: bool = False, nthrea
             setattr(io, k, out[k].ctypes.data)
         st = lib().fo_block_forward_backward(ctypes.byref(io))
     out["status"] = st
+    return out
+
+
+def full_block(x, g1, Wqkv, Wo, att, g2, Wgu, Wd, dY=None, dQKV=None, eps: float = 1e-6, exact: bool = False,
+               nthreads: int = 1):
+    """The full transformer block's matmuls around a given attention core.
+
+    Forward: qkv = bf16(alpha n1_8 @ W_qkv8) with n1 = RMSNorm(x) g1; h = bf16(x + alpha att8 @ W_o8);
+    y = MLP block on h (gain g2).  Backward (with dY [T,d] and the core's input gradient dQKV
+    [T,nq]): dh from the MLP; d_att = bf16(alpha dh8 @ W_o8^T); dW_o; dW_qkv; dX = bf16(dh +
+    RMSNorm'(alpha dQKV8 @ W_qkv8^T)); dg1.  Returned keys: the attention-side tensors plus every
+    key of block() for the MLP part; scal_attn rows: W_qkv, W_o, n1, att, dh, dQKV.
+    Inputs are bf16 bit patterns (quantized mode) or float64 (exact mode)."""
+    x64, g164, Wqkv64, Wo64, att64 = (_as_f64(a, exact) for a in (x, g1, Wqkv, Wo, att))
+    g264, Wgu64, Wd64 = (_as_f64(a, exact) for a in (g2, Wgu, Wd))
+    T, d = x64.shape
+    nq = Wqkv64.shape[1]
+    f = Wd64.shape[0]
+    backward = dY is not None
+    out = {
+        "qkv": np.empty((T, nq)), "h": np.empty((T, d)), "rstd1": np.empty(T),
+        "Wqkv8": np.empty((d, nq), np.uint8), "Wo8": np.empty((d, d), np.uint8),
+        "n1_8": np.empty((T, d), np.uint8), "att8": np.empty((T, d), np.uint8),
+        "scal_attn": np.zeros((6, 3), np.float32),
+        "y": np.empty((T, d)), "H": np.empty((T, 2 * f)), "rstd": np.empty(T),
+        "Wgu8": np.empty((d, 2 * f), np.uint8), "Wd8": np.empty((f, d), np.uint8),
+        "n8": np.empty((T, d), np.uint8), "a8": np.empty((T, f), np.uint8),
+        "scal_fwd": np.zeros((4, 3), np.float32),
+    }
+    keep = [x64, g164, Wqkv64, Wo64, att64, g264, Wgu64, Wd64]
+    io = _FullIO(T=T, d=d, f=f, nq=nq, eps=eps, exact=int(exact), nthreads=int(nthreads))
+    io.x, io.g1, io.Wqkv, io.Wo, io.att = (a.ctypes.data for a in keep[:5])
+    m = _BlockIO(T=T, d=d, f=f, eps=eps, exact=int(exact), nthreads=int(nthreads))
+    m.g, m.Wgu, m.Wd = (a.ctypes.data for a in keep[5:])
+    for k in ("qkv", "h", "rstd1", "Wqkv8", "Wo8", "n1_8", "att8", "scal_attn"):
+        setattr(io, k, out[k].ctypes.data)
+    for k in ("y", "H", "rstd", "Wgu8", "Wd8", "n8", "a8", "scal_fwd"):
+        setattr(m, k, out[k].ctypes.data)
+    if backward:
+        dY64, dQKV64 = _as_f64(dY, exact), _as_f64(dQKV, exact)
+        keep += [dY64, dQKV64]
+        m.dY = dY64.ctypes.data
+        io.dQKV = dQKV64.ctypes.data
+        out.update({
+            "dX": np.empty((T, d)), "dWqkv": np.empty((d, nq)), "dWo": np.empty((d, d)), "dg1": np.empty(d),
+            "d_att": np.empty((T, d)), "dh": np.empty((T, d)), "dh8": np.empty((T, d), np.uint8),
+            "dqkv8": np.empty((T, nq), np.uint8),
+            "dWgu": np.empty((d, 2 * f)), "dWd": np.empty((f, d)), "dg": np.empty(d), "dN": np.empty((T, d)),
+            "dH": np.empty((T, 2 * f)), "dY8": np.empty((T, d), np.uint8), "dH8": np.empty((T, 2 * f), np.uint8),
+            "scal_bwd": np.zeros((2, 3), np.float32),
+        })
+        for k in ("dX", "dWqkv", "dWo", "dg1", "d_att", "dh", "dh8", "dqkv8"):
+            setattr(io, k, out[k].ctypes.data)
+        for k in ("dWgu", "dWd", "dg", "dN", "dH", "dY8", "dH8", "scal_bwd"):
+            setattr(m, k, out[k].ctypes.data)
+    io.mlp = m
+    out["status"] = lib().fo_full_block(ctypes.byref(io), int(backward))
     return out

@@ -493,6 +493,134 @@ int block_backward(const BlockIO& io, const FwdState& S) {
   return status;
 }
 
+// ----------------------------------------------------------------------------
+// The full transformer block's matmuls (the 32B-class workload).  The attention
+// core itself is not part of this path: its output `att` [T,d] and the gradient
+// arriving at its input `dQKV` [T,nq] are given tensors.  Reading of the block:
+//   forward   W_qkv8 = q(W_qkv), W_o8 = q(W_o)                     E4M3
+//             n1 = RMSNorm(x) * g1, n1_8 = q(n1)
+//             qkv = bf16(alpha n1_8 @ W_qkv8)                      [T, nq], feeds the core
+//             att8 = q(att);  h = bf16(x + alpha att8 @ W_o8)      attention residual
+//             y = MLP block on h (gain g2)
+//   backward  dh = the MLP block's input gradient
+//             dh8 = q5(dh);  d_att = bf16(alpha dh8 @ W_o8^T);  dW_o = alpha att8^T @ dh8
+//             dQKV8 = q5(dQKV); dN1 = alpha dQKV8 @ W_qkv8^T;  dW_qkv = alpha n1_8^T @ dQKV8
+//             dX = bf16(dh + RMSNorm'(dN1));  dg1 = sum_t dN1 * x * rstd1
+// ----------------------------------------------------------------------------
+struct FullIO {
+  int64_t T, d, f, nq;
+  float eps;
+  int exact;
+  int nthreads;
+  const double* att;    // [T,d]
+  const double* g1;     // [d]
+  const double* Wqkv;   // [d,nq]
+  const double* Wo;     // [d,d]
+  const double* dQKV;   // [T,nq] (backward)
+  double* qkv;          // [T,nq]
+  double* h;            // [T,d]  (the MLP's input; io_mlp.x must point here)
+  double* rstd1;        // [T]
+  uint8_t* Wqkv8; uint8_t* Wo8; uint8_t* n1_8; uint8_t* att8;
+  float* scal_attn;     // 6 x 3: W_qkv, W_o, n1, att, dh, dQKV
+  double* dX; double* dWqkv; double* dWo; double* dg1; double* d_att; double* dh;
+  uint8_t* dh8; uint8_t* dqkv8;
+  BlockIO mlp;          // x = h (set by the caller), g, Wgu, Wd, dY and all MLP outputs
+  const double* x;      // [T,d] block input
+};
+
+// RMSNorm backward with a residual gradient: dx = dres + rstd (u - nh mean(u nh)), u = dN g.
+void rmsnorm_bwd(const std::vector<double>& x, const std::vector<double>& g, const std::vector<double>& rstd,
+                 const std::vector<double>& dN, const std::vector<double>& dres, int64_t T, int64_t d, bool ex,
+                 std::vector<double>& dX, std::vector<double>& dg) {
+  dX.assign((size_t)(T * d), 0.0);
+  dg.assign((size_t)d, 0.0);
+  for (int64_t t = 0; t < T; ++t) {
+    const double rs = rstd[t];
+    double dot = 0.0;
+    for (int64_t j = 0; j < d; ++j) dot += dN[t * d + j] * g[j] * (x[t * d + j] * rs);
+    dot /= (double)d;
+    for (int64_t j = 0; j < d; ++j) {
+      const double nh = x[t * d + j] * rs;
+      const double u = dN[t * d + j] * g[j];
+      const double v = dres[t * d + j] + rs * (u - nh * dot);
+      dX[t * d + j] = ex ? v : to_bf16(v);
+      dg[j] += dN[t * d + j] * nh;
+    }
+  }
+  if (!ex) for (double& v : dg) v = (double)(float)v;
+}
+
+int full_block(FullIO& io, bool backward) {
+  const int64_t T = io.T, d = io.d, nq = io.nq;
+  const bool ex = io.exact != 0;
+  int status = 0;
+  std::vector<double> x(io.x, io.x + T * d), g1(io.g1, io.g1 + d), att(io.att, io.att + T * d);
+  QTensor Wqkv = quantize(std::vector<double>(io.Wqkv, io.Wqkv + d * nq), FMT_E4M3, ex);
+  QTensor Wo = quantize(std::vector<double>(io.Wo, io.Wo + d * d), FMT_E4M3, ex);
+  std::vector<double> n1, rstd1;
+  rmsnorm_fwd(x, g1, T, d, io.eps, ex, n1, rstd1);
+  QTensor n1q = quantize(n1, FMT_E4M3, ex);
+  QTensor attq = quantize(att, FMT_E4M3, ex);
+
+  const double a_qkv = ex ? 1.0 : (double)(n1q.s.scale_inv * Wqkv.s.scale_inv);
+  std::vector<double> qkv = matmul(n1q.deq, Wqkv.deq, T, nq, d, io.nthreads);
+  for (double& v : qkv) v = ex ? a_qkv * v : to_bf16(a_qkv * v);
+  const double a_o = ex ? 1.0 : (double)(attq.s.scale_inv * Wo.s.scale_inv);
+  std::vector<double> h = matmul(attq.deq, Wo.deq, T, d, d, io.nthreads);
+  for (size_t i = 0; i < h.size(); ++i) h[i] = ex ? x[i] + a_o * h[i] : to_bf16(x[i] + a_o * h[i]);
+
+  put(io.qkv, qkv);
+  put(io.h, h);
+  put(io.rstd1, rstd1);
+  if (!ex) { put(io.Wqkv8, Wqkv.code); put(io.Wo8, Wo.code); put(io.n1_8, n1q.code); put(io.att8, attq.code); }
+  if (io.scal_attn) {
+    put_scal(io.scal_attn + 0, Wqkv.s); put_scal(io.scal_attn + 3, Wo.s);
+    put_scal(io.scal_attn + 6, n1q.s); put_scal(io.scal_attn + 9, attq.s);
+  }
+  for (const Scal* sc : {&Wqkv.s, &Wo.s, &n1q.s, &attq.s})
+    if (!finite_scal(*sc)) status |= 1;
+
+  // the MLP block on h
+  BlockIO m = io.mlp;
+  m.x = h.data();
+  FwdState S = block_forward(m);
+  write_forward(m, S);
+  status |= S.status;
+  if (!backward) return status;
+  std::vector<double> dh((size_t)(T * d));
+  m.dX = dh.data();
+  status |= block_backward(m, S);
+  put(io.dh, dh);
+
+  // O projection backward
+  QTensor dhq = quantize(dh, FMT_E5M2, ex);
+  const double a_od = ex ? 1.0 : (double)(dhq.s.scale_inv * Wo.s.scale_inv);
+  std::vector<double> datt = matmul(dhq.deq, transpose(Wo.deq, d, d), T, d, d, io.nthreads);
+  for (double& v : datt) v = ex ? a_od * v : to_bf16(a_od * v);
+  const double a_ow = ex ? 1.0 : (double)(attq.s.scale_inv * dhq.s.scale_inv);
+  std::vector<double> dWo = matmul(transpose(attq.deq, T, d), dhq.deq, d, d, T, io.nthreads);
+  for (double& v : dWo) v = ex ? a_ow * v : (double)(float)(a_ow * v);
+
+  // QKV projection backward
+  QTensor dqq = quantize(std::vector<double>(io.dQKV, io.dQKV + T * nq), FMT_E5M2, ex);
+  const double a_qd = ex ? 1.0 : (double)(dqq.s.scale_inv * Wqkv.s.scale_inv);
+  std::vector<double> dN1 = matmul(dqq.deq, transpose(Wqkv.deq, d, nq), T, d, nq, io.nthreads);
+  for (double& v : dN1) v = ex ? a_qd * v : (double)(float)(a_qd * v);
+  const double a_qw = ex ? 1.0 : (double)(n1q.s.scale_inv * dqq.s.scale_inv);
+  std::vector<double> dWqkv = matmul(transpose(n1q.deq, T, d), dqq.deq, d, nq, T, io.nthreads);
+  for (double& v : dWqkv) v = ex ? a_qw * v : (double)(float)(a_qw * v);
+
+  std::vector<double> dX, dg1;
+  rmsnorm_bwd(x, g1, rstd1, dN1, dh, T, d, ex, dX, dg1);
+
+  put(io.d_att, datt); put(io.dWo, dWo); put(io.dWqkv, dWqkv); put(io.dX, dX); put(io.dg1, dg1);
+  if (!ex) { put(io.dh8, dhq.code); put(io.dqkv8, dqq.code); }
+  if (io.scal_attn) { put_scal(io.scal_attn + 12, dhq.s); put_scal(io.scal_attn + 15, dqq.s); }
+  for (const Scal* sc : {&dhq.s, &dqq.s})
+    if (!finite_scal(*sc)) status |= 1;
+  return status;
+}
+
 std::vector<double> load_input(const void* x, int dtype, int64_t n) {
   // dtype 0: bf16 bits, 1: fp32
   std::vector<double> v((size_t)n);
@@ -600,6 +728,10 @@ int fo_block_forward(const BlockIO* io) {
   write_forward(*io, S);
   return S.status;
 }
+
+// The full block's matmuls (attention core given as att / dQKV); the struct is
+// mirrored by oracle/__init__.py.
+int fo_full_block(FullIO* io, int backward) { return full_block(*io, backward != 0); }
 
 int fo_block_forward_backward(const BlockIO* io) {
   FwdState S = block_forward(*io);

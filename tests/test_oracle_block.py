@@ -111,3 +111,83 @@ def test_quantized_close_to_exact_and_thread_invariant():
     for k in ("dWgu", "dWd", "dg"):
         rel = np.linalg.norm(q1[k] - ex[k]) / np.linalg.norm(ex[k])
         assert rel < 0.2, (k, rel)
+
+
+def test_full_block_exact_backward_matches_finite_differences():
+    """Attention-side matmuls of the full block (QKV and O projections around a given attention
+    core): with L = sum(y dY) + sum(qkv dQKV), the exact-mode gradients of x, g1, W_qkv, W_o and
+    the core output att equal central finite differences."""
+    T, d, f, nq = 3, 8, 8, 12
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((T, d))
+    g1 = 1 + 0.1 * rng.standard_normal(d)
+    Wqkv = 0.3 * rng.standard_normal((d, nq))
+    Wo = 0.3 * rng.standard_normal((d, d))
+    att = rng.standard_normal((T, d))
+    g2 = 1 + 0.1 * rng.standard_normal(d)
+    Wgu = 0.3 * rng.standard_normal((d, 2 * f))
+    Wd = 0.3 * rng.standard_normal((f, d))
+    dY = rng.standard_normal((T, d))
+    dQKV = rng.standard_normal((T, nq))
+    args = [x, g1, Wqkv, Wo, att]
+    out = oracle.full_block(*args, g2, Wgu, Wd, dY=dY, dQKV=dQKV, exact=True)
+
+    def loss(a):
+        o = oracle.full_block(*a, g2, Wgu, Wd, exact=True)
+        return float((o["y"] * dY).sum() + (o["qkv"] * dQKV).sum())
+
+    for which, key in enumerate(("dX", "dg1", "dWqkv", "dWo", "d_att")):
+        P = args[which]
+        fd = np.zeros_like(P)
+        for idx in np.ndindex(P.shape):
+            h = 1e-6 * max(1.0, abs(P[idx]))
+            a = [v.copy() for v in args]
+            a[which][idx] += h
+            lp = loss(a)
+            a[which][idx] -= 2 * h
+            lm = loss(a)
+            fd[idx] = (lp - lm) / (2 * h)
+        err = np.abs(fd - out[key]).max() / np.abs(fd).max()
+        assert err < 1e-6, (key, err)
+
+
+def test_full_block_quantized_wiring():
+    """Quantized full block = composition of the pinned primitives and of the MLP block on h."""
+    T, d, f, nq = 40, 64, 48, 96
+    w = synth.BY_NAME["32b-block-fwd-bwd"]
+    inp = synth.mlp_inputs(w, T=T, d=d, f=f)
+    g1 = synth.normal_bf16((d,), 0.1, 0, synth.TID_G1, mean=1.0)
+    Wqkv = synth.normal_bf16((d, nq), 0.01, 0, synth.TID_WQKV)
+    Wo = synth.normal_bf16((d, d), 0.01, 0, synth.TID_WO)
+    att = synth.normal_bf16((T, d), 1.0, 0, synth.TID_ATT)
+    dQKV = synth.normal_bf16((T, nq), 1e-3, 0, synth.TID_DQKV)
+    o = oracle.full_block(inp["x"], g1, Wqkv, Wo, att, inp["g"], inp["W_gu"], inp["W_d"], dY=inp["dY"],
+                          dQKV=dQKV)
+    assert o["status"] == 0
+    sa = o["scal_attn"]
+    n1, s, r1, _ = oracle.rmsnorm_quant(inp["x"], g1, 1e-6)
+    np.testing.assert_array_equal(o["n1_8"], n1); np.testing.assert_array_equal(sa[2], s)
+    wq, s, _ = oracle.quantize_absmax(Wqkv, 0)
+    np.testing.assert_array_equal(o["Wqkv8"], wq); np.testing.assert_array_equal(sa[0], s)
+    wo, s, _ = oracle.quantize_absmax(Wo, 0)
+    np.testing.assert_array_equal(o["Wo8"], wo); np.testing.assert_array_equal(sa[1], s)
+    a8, s, _ = oracle.quantize_absmax(att, 0)
+    np.testing.assert_array_equal(o["att8"], a8); np.testing.assert_array_equal(sa[3], s)
+    qkv = oracle.gemm_scaled(oracle.NN, n1, 0, wq, 0, sa[2, 2], sa[0, 2], out="bf16")
+    np.testing.assert_array_equal(oracle.bf16_round(o["qkv"]), qkv)
+    h = oracle.gemm_scaled(oracle.NN, a8, 0, wo, 0, sa[3, 2], sa[1, 2], out="bf16", residual=inp["x"])
+    np.testing.assert_array_equal(oracle.bf16_round(o["h"]), h)
+    mlp = oracle.block(h, inp["g"], inp["W_gu"], inp["W_d"], dY=inp["dY"])
+    for k in ("y", "H", "a8", "dWgu", "dWd", "dg"):
+        np.testing.assert_array_equal(o[k], mlp[k])
+    np.testing.assert_array_equal(o["dh"], mlp["dX"])
+    dh8, s, _ = oracle.quantize_absmax(oracle.bf16_round(o["dh"]), 1)
+    np.testing.assert_array_equal(o["dh8"], dh8); np.testing.assert_array_equal(sa[4], s)
+    d_att = oracle.gemm_scaled(oracle.NT, dh8, 1, wo, 0, sa[4, 2], sa[1, 2], out="bf16")
+    np.testing.assert_array_equal(oracle.bf16_round(o["d_att"]), d_att)
+    dWo = oracle.gemm_scaled(oracle.TN, a8, 0, dh8, 1, sa[3, 2], sa[4, 2], out="f32")
+    np.testing.assert_array_equal(o["dWo"], dWo.astype(np.float64))
+    dq8, s, _ = oracle.quantize_absmax(dQKV, 1)
+    np.testing.assert_array_equal(o["dqkv8"], dq8); np.testing.assert_array_equal(sa[5], s)
+    dWqkv = oracle.gemm_scaled(oracle.TN, n1, 0, dq8, 1, sa[2, 2], sa[5, 2], out="f32")
+    np.testing.assert_array_equal(o["dWqkv"], dWqkv.astype(np.float64))
