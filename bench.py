@@ -149,8 +149,9 @@ def job_throughput(units_per_rank: float, world: int, max_ms: float) -> float:
 # per-launch algorithmic work of one step (order = the library's launch order)
 # ---------------------------------------------------------------------------
 def step_work(w: synth.Workload):
+    """(kernel kind, algorithmic bytes, algorithmic flops) of every traced launch of one step."""
     T, d, f = w.T, w.d, w.f
-    fwd = [
+    mlp_fwd = [
         ("absmax_partial", 2 * d * 2 * f, 0), ("quant_cast", 3 * d * 2 * f, 0),
         ("absmax_partial", 2 * f * d, 0), ("quant_cast", 3 * f * d, 0),
         ("rmsnorm_stats", 2 * T * d + 2 * d + 4 * T, 0), ("rmsnorm_cast", 3 * T * d + 4 * T + 2 * d, 0),
@@ -158,7 +159,7 @@ def step_work(w: synth.Workload):
         ("quant_cast", 5 * T * f, 0),
         ("gemm_down_residual", T * f + f * d + 4 * T * d, 2.0 * T * f * d),
     ]
-    bwd = [
+    mlp_bwd = [
         ("absmax_partial", 2 * T * d, 0), ("quant_cast", 3 * T * d, 0),
         ("gemm_down_dgrad_swiglu_bwd", T * d + f * d + 2 * T * 2 * f * 2, 2.0 * T * d * f),
         ("quant_cast", 3 * T * 2 * f, 0),
@@ -167,7 +168,27 @@ def step_work(w: synth.Workload):
         ("gemm_gate_up_wgrad", T * d + T * 2 * f + 4 * d * 2 * f, 2.0 * d * T * 2 * f),
         ("rmsnorm_bwd", 10 * T * d, 0),
     ]
-    return fwd + (bwd if w.backward else [])
+    if not w.qkv:
+        return mlp_fwd + (mlp_bwd if w.backward else [])
+    q = w.qkv
+    attn_fwd = [
+        ("absmax_partial", 2 * d * q, 0), ("quant_cast", 3 * d * q, 0),
+        ("absmax_partial", 2 * d * d, 0), ("quant_cast", 3 * d * d, 0),
+        ("rmsnorm_stats", 2 * T * d + 2 * d + 4 * T, 0), ("rmsnorm_cast", 3 * T * d + 4 * T + 2 * d, 0),
+        ("gemm_qkv", T * d + d * q + 2 * T * q, 2.0 * T * d * q),
+        ("absmax_partial", 2 * T * d, 0), ("quant_cast", 3 * T * d, 0),
+        ("gemm_o_residual", T * d + d * d + 4 * T * d, 2.0 * T * d * d),
+    ]
+    attn_bwd = [
+        ("absmax_partial", 2 * T * d, 0), ("quant_cast", 3 * T * d, 0),
+        ("gemm_o_dgrad", T * d + d * d + 2 * T * d, 2.0 * T * d * d),
+        ("gemm_o_wgrad", 2 * T * d + 4 * d * d, 2.0 * T * d * d),
+        ("absmax_partial", 2 * T * q, 0), ("quant_cast", 3 * T * q, 0),
+        ("gemm_qkv_dgrad", T * q + d * q + 4 * T * d, 2.0 * T * q * d),
+        ("gemm_qkv_wgrad", T * d + T * q + 4 * d * q, 2.0 * T * d * q),
+        ("rmsnorm_bwd", 10 * T * d, 0),
+    ]
+    return attn_fwd + mlp_fwd + (mlp_bwd + attn_bwd if w.backward else [])
 
 
 # ---------------------------------------------------------------------------
@@ -179,21 +200,38 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     w = args.w
     flops = w.gemm_flops()
-    inp = synth.mlp_inputs(w, seed=rank)
-    b = fq.MlpBuffers.allocate(w.T, w.d, w.f, device=dev, backward=w.backward)
-    names = ["x", "g", "W_gu", "W_d"] + (["dY"] if w.backward else [])
-    host_in = {k: torch.from_numpy(inp[k].view(np.int16)).view(torch.bfloat16).pin_memory() for k in names}
-    for k in names:
-        getattr(b, k).copy_(host_in[k])
+    if w.qkv:
+        inp = synth.block_inputs(w, seed=rank)
+        b = fq.BlockBuffers.allocate(w.T, w.d, w.f, w.qkv, device=dev, backward=w.backward)
+        dev_in = {"x": b.x, "g1": b.g1, "W_qkv": b.W_qkv, "W_o": b.W_o, "att": b.att, "g": b.mlp.g,
+                  "W_gu": b.mlp.W_gu, "W_d": b.mlp.W_d}
+        if w.backward:
+            dev_in.update(dY=b.mlp.dY, dQKV=b.dQKV)
+        dev_out = {"y": b.mlp.y}
+        if w.backward:
+            dev_out.update(dX=b.dX, dW_qkv=b.dW_qkv, dW_o=b.dW_o, dg1=b.dg1, dW_gu=b.mlp.dW_gu, dW_d=b.mlp.dW_d,
+                           dg=b.mlp.dg, d_att=b.d_att)
+        fwd, bwd = fq.block_fwd, fq.block_bwd
+    else:
+        inp = synth.mlp_inputs(w, seed=rank)
+        b = fq.MlpBuffers.allocate(w.T, w.d, w.f, device=dev, backward=w.backward)
+        dev_in = {k: getattr(b, k) for k in ["x", "g", "W_gu", "W_d"] + (["dY"] if w.backward else [])}
+        dev_out = {"y": b.y}
+        if w.backward:
+            dev_out.update(dX=b.dX, dW_gu=b.dW_gu, dW_d=b.dW_d, dg=b.dg)
+        fwd, bwd = fq.mlp_block_fwd, fq.mlp_block_bwd
+    host_in = {k: torch.from_numpy(inp[k].view(np.int16)).view(torch.bfloat16).pin_memory() for k in dev_in}
+    for k, t in dev_in.items():
+        t.copy_(host_in[k])
     del inp
     stream = torch.cuda.current_stream()
     lib = fq.load_library()
 
     def step():
-        fq.mlp_block_fwd(b)
+        fwd(b)
         n = lib.fp8q_last_launch_count()
         if w.backward:
-            fq.mlp_block_bwd(b)
+            bwd(b)
             n += lib.fp8q_last_launch_count()
         return n
 
@@ -236,17 +274,16 @@ def run_ours(args, rank, world, local_rank):
     # ---- e2e: pinned host inputs in, every output back out, inside the timed region
     e2e = None
     if not args.no_e2e:
-        outs = ["y"] + (["dX", "dW_gu", "dW_d", "dg"] if w.backward else [])
-        host_out = {k: torch.empty(getattr(b, k).shape, dtype=getattr(b, k).dtype).pin_memory() for k in outs}
+        host_out = {k: torch.empty(t.shape, dtype=t.dtype).pin_memory() for k, t in dev_out.items()}
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())
         d2h = sum(t.numel() * t.element_size() for t in host_out.values())
 
         def e2e_step():
-            for k in names:
-                getattr(b, k).copy_(host_in[k], non_blocking=True)
+            for k, t in dev_in.items():
+                t.copy_(host_in[k], non_blocking=True)
             step()
-            for k in outs:
-                host_out[k].copy_(getattr(b, k), non_blocking=True)
+            for k, t in dev_out.items():
+                host_out[k].copy_(t, non_blocking=True)
 
         for _ in range(2):
             e2e_step()
@@ -293,13 +330,21 @@ def kernel_table(traced, plan, K, pk):
 
 def cpu_baseline(w, tokens):
     import oracle
-    inp = synth.mlp_inputs(w, seed=0)
-    x = inp["x"][:tokens]
-    dY = inp["dY"][:tokens] if w.backward else None
     oracle.build()
-    t0 = time.perf_counter()
-    oracle.block(x, inp["g"], inp["W_gu"], inp["W_d"], dY=dY, nthreads=1)
-    dt = time.perf_counter() - t0
+    if w.qkv:
+        inp = synth.block_inputs(w, seed=0)
+        sl = {k: inp[k][:tokens] for k in ("x", "att", "dY", "dQKV") if k in inp}
+        t0 = time.perf_counter()
+        oracle.full_block(sl["x"], inp["g1"], inp["W_qkv"], inp["W_o"], sl["att"], inp["g"], inp["W_gu"],
+                          inp["W_d"], dY=sl.get("dY"), dQKV=sl.get("dQKV"), nthreads=1)
+        dt = time.perf_counter() - t0
+    else:
+        inp = synth.mlp_inputs(w, seed=0)
+        x = inp["x"][:tokens]
+        dY = inp["dY"][:tokens] if w.backward else None
+        t0 = time.perf_counter()
+        oracle.block(x, inp["g"], inp["W_gu"], inp["W_d"], dY=dY, nthreads=1)
+        dt = time.perf_counter() - t0
     sub = synth.Workload(w.name, tokens, w.d, w.f, w.x_kind, w.x_scale, w.outlier_frac, w.outlier_mult,
                          w.w_std, w.dy_std, w.qkv)
     return {"value": sub.gemm_flops() / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",

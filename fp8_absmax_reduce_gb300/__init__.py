@@ -53,6 +53,10 @@ def _load() -> ctypes.CDLL:
     L.fp8q_status_string.restype = ctypes.c_char_p
     L.fp8q_status_string.argtypes = [i32]
     L.fp8q_last_launch_count.restype = i32
+    L.block_workspace_size.restype = sz
+    L.block_workspace_size.argtypes = [i64, i64, i64, i64, i32]
+    L.block_fwd.argtypes = [ctypes.POINTER(FP8QBlock), vp, sz, vp]
+    L.block_bwd.argtypes = [ctypes.POINTER(FP8QBlock), vp, sz, vp]
     L.fp8q_trace_start.argtypes = [i32]
     L.fp8q_trace_read.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int), i32]
     L.fp8q_kernel_name.restype = ctypes.c_char_p
@@ -67,6 +71,17 @@ class FP8QMlp(ctypes.Structure):
             "x", "g", "W_gu", "W_d", "y", "W_gu8", "W_d8", "n8", "rstd", "H", "a8", "scal",
             "dY", "dX", "dW_gu", "dW_d", "dg", "dY8", "dH", "dH8", "dN")
     ]
+
+
+class FP8QBlock(ctypes.Structure):
+    """Mirror of ``fp8q_block`` in include/fp8q.h."""
+    _fields_ = ([("T", ctypes.c_int64), ("d", ctypes.c_int64), ("f", ctypes.c_int64), ("n_qkv", ctypes.c_int64),
+                 ("eps", ctypes.c_float)]
+                + [(n, ctypes.c_void_p) for n in ("x", "g1", "W_qkv", "W_o", "att", "qkv", "h", "W_qkv8", "W_o8",
+                                                  "n1_8", "rstd1", "att8", "scal")]
+                + [("mlp", FP8QMlp)]
+                + [(n, ctypes.c_void_p) for n in ("dQKV", "d_att", "dX", "dW_qkv", "dW_o", "dg1", "dh8", "dQKV8",
+                                                  "dN1")])
 
 
 _lib_handle = None
@@ -272,3 +287,95 @@ def get_status(clear: bool = False) -> int:
 
 def last_launch_count() -> int:
     return lib.fp8q_last_launch_count()
+
+
+# ---------------------------------------------------------------------------
+@dataclasses.dataclass
+class BlockBuffers:
+    """Caller-owned device buffers of the full block (see fp8q_block in include/fp8q.h).
+    ``mlp`` holds the MLP sub-block's buffers; its ``x`` is the attention residual output h and,
+    in the backward, its ``dX`` receives dh."""
+    T: int
+    d: int
+    f: int
+    n_qkv: int
+    eps: float
+    x: torch.Tensor
+    g1: torch.Tensor
+    W_qkv: torch.Tensor
+    W_o: torch.Tensor
+    att: torch.Tensor
+    qkv: torch.Tensor
+    W_qkv8: torch.Tensor
+    W_o8: torch.Tensor
+    n1_8: torch.Tensor
+    rstd1: torch.Tensor
+    att8: torch.Tensor
+    scal: torch.Tensor
+    mlp: MlpBuffers
+    dQKV: torch.Tensor | None = None
+    d_att: torch.Tensor | None = None
+    dX: torch.Tensor | None = None
+    dW_qkv: torch.Tensor | None = None
+    dW_o: torch.Tensor | None = None
+    dg1: torch.Tensor | None = None
+    dh8: torch.Tensor | None = None
+    dQKV8: torch.Tensor | None = None
+    dN1: torch.Tensor | None = None
+    ws: torch.Tensor | None = None
+
+    @staticmethod
+    def allocate(T: int, d: int, f: int, n_qkv: int, device="cuda", backward: bool = True, eps: float = 1e-6,
+                 keep_intermediates: bool = False) -> "BlockBuffers":
+        e = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)
+        m = MlpBuffers.allocate(T, d, f, device=device, backward=backward, eps=eps,
+                                keep_intermediates=keep_intermediates)
+        m.ws = None  # the block's workspace holds the MLP's
+        b = BlockBuffers(
+            T=T, d=d, f=f, n_qkv=n_qkv, eps=eps, x=e((T, d), torch.bfloat16), g1=e((d,), torch.bfloat16),
+            W_qkv=e((d, n_qkv), torch.bfloat16), W_o=e((d, d), torch.bfloat16), att=e((T, d), torch.bfloat16),
+            qkv=e((T, n_qkv), torch.bfloat16), W_qkv8=e((d, n_qkv), torch.uint8), W_o8=e((d, d), torch.uint8),
+            n1_8=e((T, d), torch.uint8), rstd1=e((T,), torch.float32), att8=e((T, d), torch.uint8),
+            scal=torch.zeros((6, 3), device=device), mlp=m)
+        if backward:
+            b.dQKV = e((T, n_qkv), torch.bfloat16)
+            b.d_att = e((T, d), torch.bfloat16)
+            b.dX = e((T, d), torch.bfloat16)
+            b.dW_qkv = e((d, n_qkv), torch.float32)
+            b.dW_o = e((d, d), torch.float32)
+            b.dg1 = e((d,), torch.float32)
+            if keep_intermediates:
+                b.dh8 = e((T, d), torch.uint8)
+                b.dQKV8 = e((T, n_qkv), torch.uint8)
+                b.dN1 = e((T, d), torch.float32)
+        nb = lib.block_workspace_size(T, d, f, n_qkv, int(backward))
+        b.ws = torch.empty(nb, dtype=torch.uint8, device=device)
+        return b
+
+    @property
+    def h(self) -> torch.Tensor:
+        return self.mlp.x
+
+    @property
+    def dh(self) -> torch.Tensor:
+        return self.mlp.dX
+
+    def struct(self) -> FP8QBlock:
+        s = FP8QBlock(T=self.T, d=self.d, f=self.f, n_qkv=self.n_qkv, eps=self.eps)
+        for name in ("x", "g1", "W_qkv", "W_o", "att", "qkv", "W_qkv8", "W_o8", "n1_8", "rstd1", "att8", "scal",
+                     "dQKV", "d_att", "dX", "dW_qkv", "dW_o", "dg1", "dh8", "dQKV8", "dN1"):
+            t = getattr(self, name)
+            setattr(s, name, None if t is None else t.data_ptr())
+        s.h = self.mlp.x.data_ptr()
+        s.mlp = self.mlp.struct()
+        return s
+
+
+def block_fwd(b: BlockBuffers, stream=None):
+    s = b.struct()
+    _check("block_fwd", lib.block_fwd(ctypes.byref(s), _ptr(b.ws), b.ws.numel(), _stream(stream)))
+
+
+def block_bwd(b: BlockBuffers, stream=None):
+    s = b.struct()
+    _check("block_bwd", lib.block_bwd(ctypes.byref(s), _ptr(b.ws), b.ws.numel(), _stream(stream)))

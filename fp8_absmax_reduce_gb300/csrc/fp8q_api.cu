@@ -19,12 +19,14 @@ thread_local int t_last_launches = 0;
 enum Kind {
   kKAbsmaxPartial = 0, kKQuantCast, kKRmsnormStats, kKRmsnormCast, kKSwigluAmax, kKSwigluCast, kKRmsnormBwd,
   kKGemmGateUp, kKGemmDown, kKGemmDownDgrad, kKGemmDownWgrad, kKGemmGateUpDgrad, kKGemmGateUpWgrad, kKGemm,
+  kKGemmQkv, kKGemmOResidual, kKGemmODgrad, kKGemmOWgrad, kKGemmQkvDgrad, kKGemmQkvWgrad,
   kKCount
 };
 const char* const kKindNames[kKCount] = {
     "absmax_partial", "quant_cast", "rmsnorm_stats", "rmsnorm_cast", "swiglu_amax", "swiglu_cast",
     "rmsnorm_bwd", "gemm_gate_up_swiglu", "gemm_down_residual", "gemm_down_dgrad_swiglu_bwd",
-    "gemm_down_wgrad", "gemm_gate_up_dgrad", "gemm_gate_up_wgrad", "gemm"};
+    "gemm_down_wgrad", "gemm_gate_up_dgrad", "gemm_gate_up_wgrad", "gemm",
+    "gemm_qkv", "gemm_o_residual", "gemm_o_dgrad", "gemm_o_wgrad", "gemm_qkv_dgrad", "gemm_qkv_wgrad"};
 
 struct Trace {
   bool on = false;
@@ -178,6 +180,329 @@ int validate_mlp(const fp8q_mlp* m, bool backward) {
   return FP8Q_OK;
 }
 
+// The MLP block's kernel sequences, enqueued on c.L.stream (shared by
+// mlp_block_* and block_*).
+int mlp_fwd_run(const fp8q_mlp* m, const MlpWs& w, Ctx& c) {
+  const int64_t T = m->T, d = m->d, f = m->f;
+  float* s_wgu = m->scal + 0;
+  float* s_wd = m->scal + 3;
+  float* s_n = m->scal + 6;
+  float* s_a = m->scal + 9;
+  int P = 0;
+  // weights: per-tensor E4M3 (re-quantized every step: weights change every step)
+  FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(m->W_gu, 0, d * 2 * f, w.part_q, &P, c.L));
+  FP8Q_STEP(kKQuantCast, launch_quant_cast(m->W_gu, 0, d * 2 * f, 0, w.part_q, P, m->W_gu8, s_wgu, c.L));
+  FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(m->W_d, 0, f * d, w.part_q, &P, c.L));
+  FP8Q_STEP(kKQuantCast, launch_quant_cast(m->W_d, 0, f * d, 0, w.part_q, P, m->W_d8, s_wd, c.L));
+  // RMSNorm + E4M3
+  FP8Q_STEP(kKRmsnormStats, launch_rmsnorm_stats((const uint16_t*)m->x, (const uint16_t*)m->g, T, (int)d, m->eps, m->rstd,
+                                w.part_q, &P, c.L));
+  FP8Q_STEP(kKRmsnormCast, launch_rmsnorm_cast((const uint16_t*)m->x, (const uint16_t*)m->g, m->rstd, T, (int)d, w.part_q, P,
+                               m->n8, s_n, c.L));
+  // G1: H = bf16(alpha n8 @ W_gu8) with the SwiGLU absmax fused in the epilogue
+  GemmProblem g1{};
+  g1.a_mn = 0;
+  g1.b_mn = 1;
+  g1.M = (int)T;
+  g1.N = (int)f;
+  g1.K = (int)d;
+  g1.A = m->n8;
+  g1.lda = d;
+  g1.fmtA = 0;
+  g1.B = m->W_gu8;
+  g1.ldb = 2 * f;
+  g1.fmtB = 0;
+  g1.b_cols = 2 * f;
+  g1.sinvA = s_n + 2;
+  g1.sinvB = s_wgu + 2;
+  g1.epi = kEpiSwiglu;
+  g1.C = m->H;
+  g1.ldc = 2 * f;
+  g1.aux = w.a_f32;
+  g1.amax_partial = w.part_g;
+  FP8Q_STEP(kKGemmGateUp, launch_gemm(g1, &P, c.L));
+  // a8 = q(a) with a = SwiGLU(H) as the epilogue computed it, scale from its partials
+  FP8Q_STEP(kKQuantCast, launch_quant_cast(w.a_f32, 1, T * f, 0, w.part_g, P, m->a8, s_a, c.L));
+  // G2: y = bf16(x + alpha a8 @ W_d8)
+  GemmProblem g2{};
+  g2.a_mn = 0;
+  g2.b_mn = 1;
+  g2.M = (int)T;
+  g2.N = (int)d;
+  g2.K = (int)f;
+  g2.A = m->a8;
+  g2.lda = f;
+  g2.fmtA = 0;
+  g2.B = m->W_d8;
+  g2.ldb = d;
+  g2.fmtB = 0;
+  g2.b_cols = d;
+  g2.sinvA = s_a + 2;
+  g2.sinvB = s_wd + 2;
+  g2.epi = kEpiResidual;
+  g2.C = m->y;
+  g2.ldc = d;
+  g2.R = (const uint16_t*)m->x;
+  g2.ldr = d;
+  FP8Q_STEP(kKGemmDown, launch_gemm(g2, &P, c.L));
+  return FP8Q_OK;
+}
+
+int mlp_bwd_run(const fp8q_mlp* m, const MlpWs& w, Ctx& c) {
+  const int64_t T = m->T, d = m->d, f = m->f;
+  const float* s_wgu = m->scal + 0;
+  const float* s_wd = m->scal + 3;
+  const float* s_n = m->scal + 6;
+  const float* s_a = m->scal + 9;
+  float* s_dy = m->scal + 12;
+  float* s_dh = m->scal + 15;
+  uint8_t* dY8 = m->dY8 ? m->dY8 : w.dY8;
+  uint16_t* dH = m->dH ? (uint16_t*)m->dH : w.dH;
+  uint8_t* dH8 = m->dH8 ? m->dH8 : w.dH8;
+  float* dN = m->dN ? m->dN : w.dN;
+  int P = 0;
+  // dY8 = q5(dY)
+  FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(m->dY, 0, T * d, w.part_q, &P, c.L));
+  FP8Q_STEP(kKQuantCast, launch_quant_cast(m->dY, 0, T * d, 1, w.part_q, P, dY8, s_dy, c.L));
+  // G3 (NT): dA = alpha dY8 @ W_d8^T, SwiGLU backward fused -> dH + absmax partials
+  GemmProblem g3{};
+  g3.a_mn = 0;
+  g3.b_mn = 0;
+  g3.M = (int)T;
+  g3.N = (int)f;
+  g3.K = (int)d;
+  g3.A = dY8;
+  g3.lda = d;
+  g3.fmtA = 1;
+  g3.B = m->W_d8;
+  g3.ldb = d;
+  g3.fmtB = 0;
+  g3.b_cols = f;
+  g3.sinvA = s_dy + 2;
+  g3.sinvB = s_wd + 2;
+  g3.epi = kEpiSwigluBwd;
+  g3.C = dH;
+  g3.ldc = 2 * f;
+  g3.R = (const uint16_t*)m->H;
+  g3.ldr = 2 * f;
+  g3.amax_partial = w.part_g;
+  FP8Q_STEP(kKGemmDownDgrad, launch_gemm(g3, &P, c.L));
+  // dH8 = q5(dH)
+  FP8Q_STEP(kKQuantCast, launch_quant_cast(dH, 0, T * 2 * f, 1, w.part_g, P, dH8, s_dh, c.L));
+  // G4 (TN): dW_d = alpha a8^T @ dY8
+  GemmProblem g4{};
+  g4.a_mn = 1;
+  g4.b_mn = 1;
+  g4.M = (int)f;
+  g4.N = (int)d;
+  g4.K = (int)T;
+  g4.A = m->a8;
+  g4.lda = f;
+  g4.fmtA = 0;
+  g4.B = dY8;
+  g4.ldb = d;
+  g4.fmtB = 1;
+  g4.b_cols = d;
+  g4.sinvA = s_a + 2;
+  g4.sinvB = s_dy + 2;
+  g4.epi = kEpiStore;
+  g4.out_f32 = 1;
+  g4.C = m->dW_d;
+  g4.ldc = d;
+  FP8Q_STEP(kKGemmDownWgrad, launch_gemm(g4, &P, c.L));
+  // G5 (NT): dN = alpha dH8 @ W_gu8^T
+  GemmProblem g5{};
+  g5.a_mn = 0;
+  g5.b_mn = 0;
+  g5.M = (int)T;
+  g5.N = (int)d;
+  g5.K = (int)(2 * f);
+  g5.A = dH8;
+  g5.lda = 2 * f;
+  g5.fmtA = 1;
+  g5.B = m->W_gu8;
+  g5.ldb = 2 * f;
+  g5.fmtB = 0;
+  g5.b_cols = d;
+  g5.sinvA = s_dh + 2;
+  g5.sinvB = s_wgu + 2;
+  g5.epi = kEpiStore;
+  g5.out_f32 = 1;
+  g5.C = dN;
+  g5.ldc = d;
+  FP8Q_STEP(kKGemmGateUpDgrad, launch_gemm(g5, &P, c.L));
+  // G6 (TN): dW_gu = alpha n8^T @ dH8
+  GemmProblem g6{};
+  g6.a_mn = 1;
+  g6.b_mn = 1;
+  g6.M = (int)d;
+  g6.N = (int)(2 * f);
+  g6.K = (int)T;
+  g6.A = m->n8;
+  g6.lda = d;
+  g6.fmtA = 0;
+  g6.B = dH8;
+  g6.ldb = 2 * f;
+  g6.fmtB = 1;
+  g6.b_cols = 2 * f;
+  g6.sinvA = s_n + 2;
+  g6.sinvB = s_dh + 2;
+  g6.epi = kEpiStore;
+  g6.out_f32 = 1;
+  g6.C = m->dW_gu;
+  g6.ldc = 2 * f;
+  FP8Q_STEP(kKGemmGateUpWgrad, launch_gemm(g6, &P, c.L));
+  // RMSNorm backward + residual
+  FP8Q_STEP(kKRmsnormBwd, launch_rmsnorm_bwd(dN, (const uint16_t*)m->x, (const uint16_t*)m->dY, (const uint16_t*)m->g, m->rstd,
+                              T, (int)d, (uint16_t*)m->dX, w.dg_part, m->dg, c.L));
+  return FP8Q_OK;
+}
+
+// ---- the full block ---------------------------------------------------------
+struct BlockWs {
+  MlpWs mlp;
+  uint8_t* mlp_base;
+  uint32_t* part;   // attention-side quantizer partials
+  uint8_t* dh8;     // [T,d] E5M2
+  uint8_t* dqkv8;   // [T,nq] E5M2
+  float* dN1;       // [T,d]
+  float* dg1_part;  // dg partials of the attention-side RMSNorm backward
+};
+
+size_t block_ws_layout(int64_t T, int64_t d, int64_t f, int64_t nq, int backward, uint8_t* base, BlockWs* w) {
+  const size_t mlp_bytes = round256(mlp_ws_layout(T, d, f, backward, nullptr, nullptr));
+  Carver c{base, ~size_t(0)};
+  BlockWs tmp{};
+  tmp.mlp_base = (uint8_t*)c.take(mlp_bytes);
+  tmp.part = (uint32_t*)c.take(kPartialBytes);
+  if (backward) {
+    tmp.dh8 = (uint8_t*)c.take((size_t)(T * d));
+    tmp.dqkv8 = (uint8_t*)c.take((size_t)(T * nq));
+    tmp.dN1 = (float*)c.take((size_t)(T * d) * 4);
+    tmp.dg1_part = (float*)c.take((size_t)((T + kBwdRows - 1) / kBwdRows) * (size_t)d * 4);
+  }
+  if (base) mlp_ws_layout(T, d, f, backward, tmp.mlp_base, &tmp.mlp);
+  if (w) *w = tmp;
+  return c.off;
+}
+
+int validate_block(const fp8q_block* b, bool backward) {
+  if (!b) return FP8Q_ERR_INVALID_ARG;
+  const fp8q_mlp& m = b->mlp;
+  if (m.T != b->T || m.d != b->d || m.f != b->f || m.x != b->h) return FP8Q_ERR_INVALID_ARG;
+  if (b->n_qkv < 16 || b->n_qkv % 16 || b->n_qkv > (int64_t)1 << 20) return FP8Q_ERR_INVALID_ARG;
+  int e = validate_mlp(&m, backward);
+  if (e) return e;
+  const void* must[] = {b->x, b->g1, b->W_qkv, b->W_o, b->att, b->qkv, b->h, b->W_qkv8, b->W_o8, b->n1_8,
+                        b->rstd1, b->att8, b->scal};
+  for (const void* p : must)
+    if (!al16(p)) return FP8Q_ERR_INVALID_ARG;
+  if (!backward) return FP8Q_OK;
+  const void* must_b[] = {b->dQKV, b->d_att, b->dX, b->dW_qkv, b->dW_o, b->dg1};
+  for (const void* p : must_b)
+    if (!al16(p)) return FP8Q_ERR_INVALID_ARG;
+  const void* opt[] = {b->dh8, b->dQKV8, b->dN1};
+  for (const void* p : opt)
+    if (p && !al16(p)) return FP8Q_ERR_INVALID_ARG;
+  return FP8Q_OK;
+}
+
+GemmProblem gemm_problem(int a_mn, int b_mn, int64_t M, int64_t N, int64_t K, const uint8_t* A, int64_t lda,
+                         int fmtA, const uint8_t* B, int64_t ldb, int fmtB, int64_t b_cols, const float* sinvA,
+                         const float* sinvB, int epi, int out_f32, void* C, int64_t ldc) {
+  GemmProblem g{};
+  g.a_mn = a_mn;
+  g.b_mn = b_mn;
+  g.M = (int)M;
+  g.N = (int)N;
+  g.K = (int)K;
+  g.A = A;
+  g.lda = lda;
+  g.fmtA = fmtA;
+  g.B = B;
+  g.ldb = ldb;
+  g.fmtB = fmtB;
+  g.b_cols = b_cols;
+  g.sinvA = sinvA;
+  g.sinvB = sinvB;
+  g.epi = epi;
+  g.out_f32 = out_f32;
+  g.C = C;
+  g.ldc = ldc;
+  return g;
+}
+
+int block_fwd_run(const fp8q_block* b, const BlockWs& w, Ctx& c) {
+  const int64_t T = b->T, d = b->d, nq = b->n_qkv;
+  float* s_qkv = b->scal + 0;
+  float* s_o = b->scal + 3;
+  float* s_n1 = b->scal + 6;
+  float* s_att = b->scal + 9;
+  int P = 0;
+  FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(b->W_qkv, 0, d * nq, w.part, &P, c.L));
+  FP8Q_STEP(kKQuantCast, launch_quant_cast(b->W_qkv, 0, d * nq, 0, w.part, P, b->W_qkv8, s_qkv, c.L));
+  FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(b->W_o, 0, d * d, w.part, &P, c.L));
+  FP8Q_STEP(kKQuantCast, launch_quant_cast(b->W_o, 0, d * d, 0, w.part, P, b->W_o8, s_o, c.L));
+  FP8Q_STEP(kKRmsnormStats, launch_rmsnorm_stats((const uint16_t*)b->x, (const uint16_t*)b->g1, T, (int)d, b->eps,
+                                                 b->rstd1, w.part, &P, c.L));
+  FP8Q_STEP(kKRmsnormCast, launch_rmsnorm_cast((const uint16_t*)b->x, (const uint16_t*)b->g1, b->rstd1, T, (int)d,
+                                               w.part, P, b->n1_8, s_n1, c.L));
+  // qkv = bf16(alpha n1_8 @ W_qkv8)
+  GemmProblem gq = gemm_problem(0, 1, T, nq, d, b->n1_8, d, 0, b->W_qkv8, nq, 0, nq, s_n1 + 2, s_qkv + 2, kEpiStore,
+                                0, b->qkv, nq);
+  FP8Q_STEP(kKGemmQkv, launch_gemm(gq, &P, c.L));
+  // h = bf16(x + alpha q(att) @ W_o8)
+  FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(b->att, 0, T * d, w.part, &P, c.L));
+  FP8Q_STEP(kKQuantCast, launch_quant_cast(b->att, 0, T * d, 0, w.part, P, b->att8, s_att, c.L));
+  GemmProblem go = gemm_problem(0, 1, T, d, d, b->att8, d, 0, b->W_o8, d, 0, d, s_att + 2, s_o + 2, kEpiResidual, 0,
+                                b->h, d);
+  go.R = (const uint16_t*)b->x;
+  go.ldr = d;
+  FP8Q_STEP(kKGemmOResidual, launch_gemm(go, &P, c.L));
+  return mlp_fwd_run(&b->mlp, w.mlp, c);
+}
+
+int block_bwd_run(const fp8q_block* b, const BlockWs& w, Ctx& c) {
+  const int64_t T = b->T, d = b->d, nq = b->n_qkv;
+  const float* s_qkv = b->scal + 0;
+  const float* s_o = b->scal + 3;
+  const float* s_n1 = b->scal + 6;
+  const float* s_att = b->scal + 9;
+  float* s_dh = b->scal + 12;
+  float* s_dq = b->scal + 15;
+  int e = mlp_bwd_run(&b->mlp, w.mlp, c);
+  if (e) return e;
+  const void* dh = b->mlp.dX;
+  uint8_t* dh8 = b->dh8 ? b->dh8 : w.dh8;
+  uint8_t* dqkv8 = b->dQKV8 ? b->dQKV8 : w.dqkv8;
+  float* dN1 = b->dN1 ? b->dN1 : w.dN1;
+  int P = 0;
+  FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(dh, 0, T * d, w.part, &P, c.L));
+  FP8Q_STEP(kKQuantCast, launch_quant_cast(dh, 0, T * d, 1, w.part, P, dh8, s_dh, c.L));
+  // d_att = bf16(alpha dh8 @ W_o8^T): B = W_o8 [d_in, d_out] is K-major for this product
+  GemmProblem god = gemm_problem(0, 0, T, d, d, dh8, d, 1, b->W_o8, d, 0, d, s_dh + 2, s_o + 2, kEpiStore, 0,
+                                 b->d_att, d);
+  FP8Q_STEP(kKGemmODgrad, launch_gemm(god, &P, c.L));
+  // dW_o = alpha att8^T @ dh8
+  GemmProblem gow = gemm_problem(1, 1, d, d, T, b->att8, d, 0, dh8, d, 1, d, s_att + 2, s_dh + 2, kEpiStore, 1,
+                                 b->dW_o, d);
+  FP8Q_STEP(kKGemmOWgrad, launch_gemm(gow, &P, c.L));
+  // dQKV8 = q5(dQKV); dN1 = alpha dQKV8 @ W_qkv8^T; dW_qkv = alpha n1_8^T @ dQKV8
+  FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(b->dQKV, 0, T * nq, w.part, &P, c.L));
+  FP8Q_STEP(kKQuantCast, launch_quant_cast(b->dQKV, 0, T * nq, 1, w.part, P, dqkv8, s_dq, c.L));
+  GemmProblem gqd = gemm_problem(0, 0, T, d, nq, dqkv8, nq, 1, b->W_qkv8, nq, 0, d, s_dq + 2, s_qkv + 2, kEpiStore,
+                                 1, dN1, d);
+  FP8Q_STEP(kKGemmQkvDgrad, launch_gemm(gqd, &P, c.L));
+  GemmProblem gqw = gemm_problem(1, 1, d, nq, T, b->n1_8, d, 0, dqkv8, nq, 1, nq, s_n1 + 2, s_dq + 2, kEpiStore, 1,
+                                 b->dW_qkv, nq);
+  FP8Q_STEP(kKGemmQkvWgrad, launch_gemm(gqw, &P, c.L));
+  // dX = bf16(dh + RMSNorm_1'(dN1)), dg1
+  FP8Q_STEP(kKRmsnormBwd, launch_rmsnorm_bwd(dN1, (const uint16_t*)b->x, (const uint16_t*)dh,
+                                             (const uint16_t*)b->g1, b->rstd1, T, (int)d, (uint16_t*)b->dX,
+                                             w.dg1_part, b->dg1, c.L));
+  return FP8Q_OK;
+}
+
 }  // namespace
 
 int fp8q::device_status_and_sms(unsigned** status, int* num_sms) {
@@ -316,68 +641,7 @@ int mlp_block_fwd(const fp8q_mlp* m, void* ws, size_t ws_bytes, fp8q_stream stre
   if ((e = make_ctx(&c, stream))) return e;
   MlpWs w;
   mlp_ws_layout(m->T, m->d, m->f, 0, static_cast<uint8_t*>(ws), &w);
-  const int64_t T = m->T, d = m->d, f = m->f;
-  float* s_wgu = m->scal + 0;
-  float* s_wd = m->scal + 3;
-  float* s_n = m->scal + 6;
-  float* s_a = m->scal + 9;
-  int P = 0;
-  // weights: per-tensor E4M3 (re-quantized every step: weights change every step)
-  FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(m->W_gu, 0, d * 2 * f, w.part_q, &P, c.L));
-  FP8Q_STEP(kKQuantCast, launch_quant_cast(m->W_gu, 0, d * 2 * f, 0, w.part_q, P, m->W_gu8, s_wgu, c.L));
-  FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(m->W_d, 0, f * d, w.part_q, &P, c.L));
-  FP8Q_STEP(kKQuantCast, launch_quant_cast(m->W_d, 0, f * d, 0, w.part_q, P, m->W_d8, s_wd, c.L));
-  // RMSNorm + E4M3
-  FP8Q_STEP(kKRmsnormStats, launch_rmsnorm_stats((const uint16_t*)m->x, (const uint16_t*)m->g, T, (int)d, m->eps, m->rstd,
-                                w.part_q, &P, c.L));
-  FP8Q_STEP(kKRmsnormCast, launch_rmsnorm_cast((const uint16_t*)m->x, (const uint16_t*)m->g, m->rstd, T, (int)d, w.part_q, P,
-                               m->n8, s_n, c.L));
-  // G1: H = bf16(alpha n8 @ W_gu8) with the SwiGLU absmax fused in the epilogue
-  GemmProblem g1{};
-  g1.a_mn = 0;
-  g1.b_mn = 1;
-  g1.M = (int)T;
-  g1.N = (int)f;
-  g1.K = (int)d;
-  g1.A = m->n8;
-  g1.lda = d;
-  g1.fmtA = 0;
-  g1.B = m->W_gu8;
-  g1.ldb = 2 * f;
-  g1.fmtB = 0;
-  g1.b_cols = 2 * f;
-  g1.sinvA = s_n + 2;
-  g1.sinvB = s_wgu + 2;
-  g1.epi = kEpiSwiglu;
-  g1.C = m->H;
-  g1.ldc = 2 * f;
-  g1.aux = w.a_f32;
-  g1.amax_partial = w.part_g;
-  FP8Q_STEP(kKGemmGateUp, launch_gemm(g1, &P, c.L));
-  // a8 = q(a) with a = SwiGLU(H) as the epilogue computed it, scale from its partials
-  FP8Q_STEP(kKQuantCast, launch_quant_cast(w.a_f32, 1, T * f, 0, w.part_g, P, m->a8, s_a, c.L));
-  // G2: y = bf16(x + alpha a8 @ W_d8)
-  GemmProblem g2{};
-  g2.a_mn = 0;
-  g2.b_mn = 1;
-  g2.M = (int)T;
-  g2.N = (int)d;
-  g2.K = (int)f;
-  g2.A = m->a8;
-  g2.lda = f;
-  g2.fmtA = 0;
-  g2.B = m->W_d8;
-  g2.ldb = d;
-  g2.fmtB = 0;
-  g2.b_cols = d;
-  g2.sinvA = s_a + 2;
-  g2.sinvB = s_wd + 2;
-  g2.epi = kEpiResidual;
-  g2.C = m->y;
-  g2.ldc = d;
-  g2.R = (const uint16_t*)m->x;
-  g2.ldr = d;
-  FP8Q_STEP(kKGemmDown, launch_gemm(g2, &P, c.L));
+  if ((e = mlp_fwd_run(m, w, c))) return e;
   return finish(c);
 }
 
@@ -389,112 +653,36 @@ int mlp_block_bwd(const fp8q_mlp* m, void* ws, size_t ws_bytes, fp8q_stream stre
   if ((e = make_ctx(&c, stream))) return e;
   MlpWs w;
   mlp_ws_layout(m->T, m->d, m->f, 1, static_cast<uint8_t*>(ws), &w);
-  const int64_t T = m->T, d = m->d, f = m->f;
-  const float* s_wgu = m->scal + 0;
-  const float* s_wd = m->scal + 3;
-  const float* s_n = m->scal + 6;
-  const float* s_a = m->scal + 9;
-  float* s_dy = m->scal + 12;
-  float* s_dh = m->scal + 15;
-  uint8_t* dY8 = m->dY8 ? m->dY8 : w.dY8;
-  uint16_t* dH = m->dH ? (uint16_t*)m->dH : w.dH;
-  uint8_t* dH8 = m->dH8 ? m->dH8 : w.dH8;
-  float* dN = m->dN ? m->dN : w.dN;
-  int P = 0;
-  // dY8 = q5(dY)
-  FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(m->dY, 0, T * d, w.part_q, &P, c.L));
-  FP8Q_STEP(kKQuantCast, launch_quant_cast(m->dY, 0, T * d, 1, w.part_q, P, dY8, s_dy, c.L));
-  // G3 (NT): dA = alpha dY8 @ W_d8^T, SwiGLU backward fused -> dH + absmax partials
-  GemmProblem g3{};
-  g3.a_mn = 0;
-  g3.b_mn = 0;
-  g3.M = (int)T;
-  g3.N = (int)f;
-  g3.K = (int)d;
-  g3.A = dY8;
-  g3.lda = d;
-  g3.fmtA = 1;
-  g3.B = m->W_d8;
-  g3.ldb = d;
-  g3.fmtB = 0;
-  g3.b_cols = f;
-  g3.sinvA = s_dy + 2;
-  g3.sinvB = s_wd + 2;
-  g3.epi = kEpiSwigluBwd;
-  g3.C = dH;
-  g3.ldc = 2 * f;
-  g3.R = (const uint16_t*)m->H;
-  g3.ldr = 2 * f;
-  g3.amax_partial = w.part_g;
-  FP8Q_STEP(kKGemmDownDgrad, launch_gemm(g3, &P, c.L));
-  // dH8 = q5(dH)
-  FP8Q_STEP(kKQuantCast, launch_quant_cast(dH, 0, T * 2 * f, 1, w.part_g, P, dH8, s_dh, c.L));
-  // G4 (TN): dW_d = alpha a8^T @ dY8
-  GemmProblem g4{};
-  g4.a_mn = 1;
-  g4.b_mn = 1;
-  g4.M = (int)f;
-  g4.N = (int)d;
-  g4.K = (int)T;
-  g4.A = m->a8;
-  g4.lda = f;
-  g4.fmtA = 0;
-  g4.B = dY8;
-  g4.ldb = d;
-  g4.fmtB = 1;
-  g4.b_cols = d;
-  g4.sinvA = s_a + 2;
-  g4.sinvB = s_dy + 2;
-  g4.epi = kEpiStore;
-  g4.out_f32 = 1;
-  g4.C = m->dW_d;
-  g4.ldc = d;
-  FP8Q_STEP(kKGemmDownWgrad, launch_gemm(g4, &P, c.L));
-  // G5 (NT): dN = alpha dH8 @ W_gu8^T
-  GemmProblem g5{};
-  g5.a_mn = 0;
-  g5.b_mn = 0;
-  g5.M = (int)T;
-  g5.N = (int)d;
-  g5.K = (int)(2 * f);
-  g5.A = dH8;
-  g5.lda = 2 * f;
-  g5.fmtA = 1;
-  g5.B = m->W_gu8;
-  g5.ldb = 2 * f;
-  g5.fmtB = 0;
-  g5.b_cols = d;
-  g5.sinvA = s_dh + 2;
-  g5.sinvB = s_wgu + 2;
-  g5.epi = kEpiStore;
-  g5.out_f32 = 1;
-  g5.C = dN;
-  g5.ldc = d;
-  FP8Q_STEP(kKGemmGateUpDgrad, launch_gemm(g5, &P, c.L));
-  // G6 (TN): dW_gu = alpha n8^T @ dH8
-  GemmProblem g6{};
-  g6.a_mn = 1;
-  g6.b_mn = 1;
-  g6.M = (int)d;
-  g6.N = (int)(2 * f);
-  g6.K = (int)T;
-  g6.A = m->n8;
-  g6.lda = d;
-  g6.fmtA = 0;
-  g6.B = dH8;
-  g6.ldb = 2 * f;
-  g6.fmtB = 1;
-  g6.b_cols = 2 * f;
-  g6.sinvA = s_n + 2;
-  g6.sinvB = s_dh + 2;
-  g6.epi = kEpiStore;
-  g6.out_f32 = 1;
-  g6.C = m->dW_gu;
-  g6.ldc = 2 * f;
-  FP8Q_STEP(kKGemmGateUpWgrad, launch_gemm(g6, &P, c.L));
-  // RMSNorm backward + residual
-  FP8Q_STEP(kKRmsnormBwd, launch_rmsnorm_bwd(dN, (const uint16_t*)m->x, (const uint16_t*)m->dY, (const uint16_t*)m->g, m->rstd,
-                              T, (int)d, (uint16_t*)m->dX, w.dg_part, m->dg, c.L));
+  if ((e = mlp_bwd_run(m, w, c))) return e;
+  return finish(c);
+}
+
+// ---------------------------------------------------------------------------
+size_t block_workspace_size(int64_t T, int64_t d, int64_t f, int64_t n_qkv, int backward) {
+  return block_ws_layout(T, d, f, n_qkv, backward, nullptr, nullptr);
+}
+
+int block_fwd(const fp8q_block* b, void* ws, size_t ws_bytes, fp8q_stream stream) {
+  int e = validate_block(b, false);
+  if (e) return e;
+  if ((e = check_ws(ws, ws_bytes, block_workspace_size(b->T, b->d, b->f, b->n_qkv, 0)))) return e;
+  Ctx c;
+  if ((e = make_ctx(&c, stream))) return e;
+  BlockWs w;
+  block_ws_layout(b->T, b->d, b->f, b->n_qkv, 0, static_cast<uint8_t*>(ws), &w);
+  if ((e = block_fwd_run(b, w, c))) return e;
+  return finish(c);
+}
+
+int block_bwd(const fp8q_block* b, void* ws, size_t ws_bytes, fp8q_stream stream) {
+  int e = validate_block(b, true);
+  if (e) return e;
+  if ((e = check_ws(ws, ws_bytes, block_workspace_size(b->T, b->d, b->f, b->n_qkv, 1)))) return e;
+  Ctx c;
+  if ((e = make_ctx(&c, stream))) return e;
+  BlockWs w;
+  block_ws_layout(b->T, b->d, b->f, b->n_qkv, 1, static_cast<uint8_t*>(ws), &w);
+  if ((e = block_bwd_run(b, w, c))) return e;
   return finish(c);
 }
 

@@ -83,6 +83,34 @@ __device__ __forceinline__ void tile_coords(int tile, const Args& p, int& mb, in
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float round_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
+// bf16 round-to-nearest-even of the exact value s + e, where s is an fp32
+// rounding of it and e the rounding error (|e| <= half an fp32 ulp).  Only an
+// s exactly on a bf16 midpoint can round differently from the exact value;
+// there the sign of e decides.  This makes each bf16 storage point one rounding
+// of the exact result instead of two (fp32, then bf16).
+__device__ __forceinline__ float round_bf16_exact(float s, float e) {
+  const uint32_t u = __float_as_uint(s);
+  if ((u & 0xFFFFu) == 0x8000u && e != 0.0f && (u & 0x7F800000u) != 0x7F800000u) {
+    const bool away = (e > 0.0f) == ((u >> 31) == 0u);  // e pushes the magnitude up
+    return __uint_as_float((away ? u + 0x8000u : u - 0x8000u) & 0xFFFF0000u);
+  }
+  return round_bf16(s);
+}
+// bf16 of alpha * acc, one rounding of the exact product.
+__device__ __forceinline__ float bf16_of_product(float alpha, float acc) {
+  const float v = __fmul_rn(alpha, acc);
+  return round_bf16_exact(v, __fmaf_rn(alpha, acc, -v));
+}
+// bf16 of r + alpha * acc (r a bf16 value), one rounding of the exact sum.
+__device__ __forceinline__ float bf16_of_residual(float r, float alpha, float acc) {
+  const float v = __fmul_rn(alpha, acc);
+  const float ev = __fmaf_rn(alpha, acc, -v);  // alpha * acc = v + ev exactly
+  const float s = __fadd_rn(r, v);
+  const float bb = __fsub_rn(s, r);            // TwoSum: r + v = s + es exactly
+  const float es = __fadd_rn(__fsub_rn(r, __fsub_rn(s, bb)), __fsub_rn(v, bb));
+  return round_bf16_exact(s, __fadd_rn(es, ev));
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
@@ -318,6 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float hg[32], hu[32], a[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
+            // H = bf16 of the fp32 product (two roundings: its cost in this epilogue-bound
+            // GEMM outweighs the rare last-bit difference from one rounding)
             hg[j] = round_bf16(__fmul_rn(alpha, __uint_as_float(ag[j])));
             hu[j] = round_bf16(__fmul_rn(alpha, __uint_as_float(au[j])));
             a[j] = swiglu_ref(hg[j], hu[j]);
@@ -397,20 +427,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ncol = min(32, p.N - col);
           if (!warp_ok || ncol <= 0) continue;
           float v[32];
+          if (p.out_f32) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(alpha, __uint_as_float(acc32[j]));
-          if (p.epi == kEpiResidual && row_ok) {
+            for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(alpha, __uint_as_float(acc32[j]));
+          } else if (p.epi == kEpiResidual) {
+            // bf16(r + alpha * acc) as one rounding of the exact sum
+            float rv[32];
             const uint16_t* r = p.R + (int64_t)row * p.ldr + col;
-            if (ncol == 32) {
-              float rv[32];
+            if (row_ok && ncol == 32) {
               load_bf16x32(r, rv);
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = __fadd_rn(rv[j], v[j]);
             } else {
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (j < ncol) v[j] = __fadd_rn(__uint_as_float((uint32_t)r[j] << 16), v[j]);
+              for (int j = 0; j < 32; ++j) rv[j] = (row_ok && j < ncol) ? __uint_as_float((uint32_t)r[j] << 16) : 0.0f;
             }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = bf16_of_residual(rv[j], alpha, __uint_as_float(acc32[j]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = bf16_of_product(alpha, __uint_as_float(acc32[j]));
           }
           staging_acquire(lane);
           if (p.out_f32) stage_f32(buf, lane, v);

@@ -207,6 +207,54 @@ FP8Q_API int mlp_block_fwd(const fp8q_mlp* m, void* ws, size_t ws_bytes, fp8q_st
 FP8Q_API int mlp_block_bwd(const fp8q_mlp* m, void* ws, size_t ws_bytes, fp8q_stream stream);
 
 /* ------------------------------------------------------------------------ */
+/* The full transformer block's matmuls around an attention core computed   */
+/* elsewhere (the 32B-class workload): attention-side RMSNorm + QKV         */
+/* projection, O projection + residual, then the MLP block.                 */
+/* ------------------------------------------------------------------------ */
+/* Forward:  n1_8 = q(RMSNorm(x) * g1), qkv = bf16(alpha n1_8 @ W_qkv8) (the
+ *           core's input), att8 = q(att) (the core's output, given),
+ *           h = bf16(x + alpha att8 @ W_o8), then mlp_block_fwd on h
+ *           (mlp.x must be h; mlp.y is the block output).
+ * Backward: mlp_block_bwd with mlp.dY = the block's dY gives dh in mlp.dX;
+ *           dh8 = q5(dh), d_att = bf16(alpha dh8 @ W_o8^T) (to the core),
+ *           dW_o = alpha att8^T @ dh8; dQKV8 = q5(dQKV) (dQKV: the gradient
+ *           arriving at qkv from the core), dN1 = alpha dQKV8 @ W_qkv8^T,
+ *           dW_qkv = alpha n1_8^T @ dQKV8, dX = bf16(dh + RMSNorm'(dN1)), dg1.
+ * Requirements as for fp8q_mlp, plus n_qkv a multiple of 16. */
+typedef struct fp8q_block {
+  int64_t T, d, f, n_qkv;
+  float eps;
+  const void* x;      /* [T,d]     bf16 block input */
+  const void* g1;     /* [d]       bf16 attention-side RMSNorm gain */
+  const void* W_qkv;  /* [d,n_qkv] bf16 */
+  const void* W_o;    /* [d,d]     bf16 */
+  const void* att;    /* [T,d]     bf16 attention core output */
+  void* qkv;          /* [T,n_qkv] bf16 attention core input (forward output) */
+  void* h;            /* [T,d]     bf16 attention residual output = the MLP input */
+  uint8_t* W_qkv8;    /* [d,n_qkv] E4M3 */
+  uint8_t* W_o8;      /* [d,d]     E4M3 */
+  uint8_t* n1_8;      /* [T,d]     E4M3 */
+  float* rstd1;       /* [T]       fp32 */
+  uint8_t* att8;      /* [T,d]     E4M3 */
+  float* scal;        /* [6][3] {amax, scale, scale_inv} of W_qkv, W_o, n1, att, dh, dQKV */
+  fp8q_mlp mlp;       /* the MLP sub-block: mlp.x == h, mlp.dX receives dh */
+  const void* dQKV;   /* [T,n_qkv] bf16 gradient from the attention core */
+  void* d_att;        /* [T,d]     bf16 gradient to the attention core */
+  void* dX;           /* [T,d]     bf16 */
+  float* dW_qkv;      /* [d,n_qkv] fp32 */
+  float* dW_o;        /* [d,d]     fp32 */
+  float* dg1;         /* [d]       fp32 */
+  /* optional views of backward intermediates; NULL = kept in the workspace */
+  uint8_t* dh8;       /* [T,d]     E5M2 */
+  uint8_t* dQKV8;     /* [T,n_qkv] E5M2 */
+  float* dN1;         /* [T,d]     fp32 */
+} fp8q_block;
+
+FP8Q_API size_t block_workspace_size(int64_t T, int64_t d, int64_t f, int64_t n_qkv, int backward);
+FP8Q_API int block_fwd(const fp8q_block* b, void* ws, size_t ws_bytes, fp8q_stream stream);
+FP8Q_API int block_bwd(const fp8q_block* b, void* ws, size_t ws_bytes, fp8q_stream stream);
+
+/* ------------------------------------------------------------------------ */
 /* Status and introspection                                                 */
 /* ------------------------------------------------------------------------ */
 /* Reads (and with clear != 0 resets) the current device's status word

@@ -133,3 +133,20 @@ def mlp_inputs(w: Workload, seed: int = 0, T: int | None = None, d: int | None =
 def f32_from_bf16_bits(bits: np.ndarray) -> np.ndarray:
     """Exact fp32 value of bf16 bit patterns (for building device tensors)."""
     return (np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def block_inputs(w: Workload, seed: int = 0, T: int | None = None, d: int | None = None, f: int | None = None,
+                 n_qkv: int | None = None) -> dict:
+    """Inputs of the full block: the MLP's (x, g = the MLP gain, W_gu, W_d, dY) plus g1 [d],
+    W_qkv [d, n_qkv], W_o [d, d], the attention core's output att [T, d] (same distribution as x,
+    its own outlier channels) and the gradient arriving at the core's input dQKV [T, n_qkv]."""
+    out = mlp_inputs(w, seed, T, d, f)
+    T, d = out["x"].shape
+    nq = w.qkv if n_qkv is None else n_qkv
+    out["g1"] = normal_bf16((d,), 0.1, seed, TID_G1, mean=1.0)
+    out["W_qkv"] = normal_bf16((d, nq), w.w_std, seed, TID_WQKV)
+    out["W_o"] = normal_bf16((d, d), w.w_std, seed, TID_WO)
+    out["att"] = activations(w, T, d, seed, TID_ATT, TID_OUTLIER_ATT)
+    if w.backward:
+        out["dQKV"] = normal_bf16((T, nq), w.dy_std, seed, TID_DQKV)
+    return out
