@@ -57,6 +57,7 @@ def _load() -> ctypes.CDLL:
     L.block_workspace_size.argtypes = [i64, i64, i64, i64, i32]
     L.block_fwd.argtypes = [ctypes.POINTER(FP8QBlock), vp, sz, vp]
     L.block_bwd.argtypes = [ctypes.POINTER(FP8QBlock), vp, sz, vp]
+    L.fp8q_selftest_bounded_wait.argtypes = [i64, vp]
     L.fp8q_trace_start.argtypes = [i32]
     L.fp8q_trace_read.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int), i32]
     L.fp8q_kernel_name.restype = ctypes.c_char_p
@@ -379,3 +380,9 @@ def block_fwd(b: BlockBuffers, stream=None):
 def block_bwd(b: BlockBuffers, stream=None):
     s = b.struct()
     _check("block_bwd", lib.block_bwd(ctypes.byref(s), _ptr(b.ws), b.ws.numel(), _stream(stream)))
+
+
+def selftest_bounded_wait(limit_s: float = 0.02, stream=None):
+    """Make the library's bounded wait run out on purpose (an mbarrier nothing arrives at);
+    afterwards the device status carries STATUS_TIMEOUT.  Diagnostics only."""
+    _check("fp8q_selftest_bounded_wait", lib.fp8q_selftest_bounded_wait(int(limit_s * 1e9), _stream(stream)))

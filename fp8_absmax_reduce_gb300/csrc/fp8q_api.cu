@@ -714,6 +714,15 @@ const char* fp8q_status_string(int status) {
 
 int fp8q_last_launch_count(void) { return t_last_launches; }
 
+int fp8q_selftest_bounded_wait(int64_t limit_ns, fp8q_stream stream) {
+  if (limit_ns < 1000000 || limit_ns > 10000000000LL) return FP8Q_ERR_INVALID_ARG;
+  Ctx c;
+  int e = make_ctx(&c, stream);
+  if (e) return e;
+  if (launch_selftest_bounded_wait((uint64_t)limit_ns, c.L) != cudaSuccess) return FP8Q_ERR_CUDA;
+  return finish(c);
+}
+
 int fp8q_trace_start(int capacity) {
   Trace& t = t_trace;
   if (capacity < 1) return FP8Q_ERR_INVALID_ARG;

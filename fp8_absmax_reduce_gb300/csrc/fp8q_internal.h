@@ -47,6 +47,9 @@ cudaError_t launch_rmsnorm_bwd(const float* dN, const uint16_t* x, const uint16_
                                const float* rstd, int64_t T, int d, uint16_t* dX, float* dg_partial, float* dg,
                                const Launch& L);
 
+// Diagnostics: a bounded wait that is made to run out (see fp8q_selftest_bounded_wait).
+cudaError_t launch_selftest_bounded_wait(uint64_t limit_ns, const Launch& L);
+
 // ---------------------------------------------------------------------------
 // GEMM
 // ---------------------------------------------------------------------------

@@ -442,7 +442,23 @@ __global__ void __launch_bounds__(kThreads) k_dg_finalize(const float* __restric
   }
 }
 
+// One thread waits on an mbarrier that nothing ever arrives at, through the
+// same bounded wait the GEMM uses, and reports the expiry in the status word.
+__global__ void k_selftest_bounded_wait(unsigned* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int never;
+  mbar_init(&bar, 1);
+  never = 0;
+  fence_mbar_init();
+  if (!mbar_wait(&bar, 0, &never, limit_ns)) atomicOr(status, kStatusTimeout);
+}
+
 }  // namespace
+
+cudaError_t launch_selftest_bounded_wait(uint64_t limit_ns, const Launch& L) {
+  k_selftest_bounded_wait<<<1, 1, 0, L.stream>>>(L.status, limit_ns);
+  return post_launch(L);
+}
 
 // ---------------------------------------------------------------------------
 // Launchers

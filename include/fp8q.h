@@ -267,6 +267,14 @@ FP8Q_API const char* fp8q_status_string(int status);
  * thread enqueued. */
 FP8Q_API int fp8q_last_launch_count(void);
 
+/* Diagnostics for the failure-detection path (no page counterpart): enqueues
+ * one thread that waits on an mbarrier nothing ever arrives at, through the
+ * same bounded wait every pipelined kernel of the library uses, with the given
+ * limit (1 ms .. 10 s) instead of the production 2 s.  When the limit runs out
+ * the kernel sets FP8Q_STATUS_TIMEOUT and returns; the context stays usable.
+ * Returns FP8Q_OK once enqueued. */
+FP8Q_API int fp8q_selftest_bounded_wait(int64_t limit_ns, fp8q_stream stream);
+
 /* Kernel-level timing for benchmarks.  While tracing is on for the calling
  * host thread, each kernel step the library enqueues is bracketed by two CUDA
  * events recorded on the stream it is launched on (host-side CUDA objects; no
