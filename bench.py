@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--cpu-sample-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--recompute", action="store_true",
+                    help="recompute-mode backward (H and a8 recomputed from n8 with the retained scale)")
     ap.add_argument("--measure-fp8-peak", action="store_true",
                     help="time cuBLASLt FP8 (torch._scaled_mm) 8192^3, burst and sustained, and exit")
     ap.add_argument("--tokens", type=int, default=0,
@@ -148,8 +150,9 @@ def job_throughput(units_per_rank: float, world: int, max_ms: float) -> float:
 # ---------------------------------------------------------------------------
 # per-launch algorithmic work of one step (order = the library's launch order)
 # ---------------------------------------------------------------------------
-def step_work(w: synth.Workload):
-    """(kernel kind, algorithmic bytes, algorithmic flops) of every traced launch of one step."""
+def step_work(w: synth.Workload, recompute: bool = False):
+    """(kernel kind, algorithmic bytes, flops) of every traced launch of one step (the recompute
+    GEMM's flops are executed work on top of the algorithmic 18Tdf)."""
     T, d, f = w.T, w.d, w.f
     mlp_fwd = [
         ("absmax_partial", 2 * d * 2 * f, 0), ("quant_cast", 3 * d * 2 * f, 0),
@@ -168,6 +171,8 @@ def step_work(w: synth.Workload):
         ("gemm_gate_up_wgrad", T * d + T * 2 * f + 4 * d * 2 * f, 2.0 * d * T * 2 * f),
         ("rmsnorm_bwd", 10 * T * d, 0),
     ]
+    if recompute:
+        mlp_bwd = [("gemm_gate_up_recompute", T * d + d * 2 * f + 2 * T * 2 * f + T * f, 2.0 * T * d * 2 * f)] + mlp_bwd
     if not w.qkv:
         return mlp_fwd + (mlp_bwd if w.backward else [])
     q = w.qkv
@@ -220,6 +225,7 @@ def run_ours(args, rank, world, local_rank):
         if w.backward:
             dev_out.update(dX=b.dX, dW_gu=b.dW_gu, dW_d=b.dW_d, dg=b.dg)
         fwd, bwd = fq.mlp_block_fwd, fq.mlp_block_bwd
+    (b.mlp if w.qkv else b).recompute = bool(args.recompute)
     host_in = {k: torch.from_numpy(inp[k].view(np.int16)).view(torch.bfloat16).pin_memory() for k in dev_in}
     for k, t in dev_in.items():
         t.copy_(host_in[k])
@@ -244,7 +250,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
 
     K = args.steps
-    plan = step_work(w)
+    plan = step_work(w, args.recompute)
     if lib.fp8q_trace_start(K * len(plan)) != 0:
         raise RuntimeError("fp8q_trace_start failed")
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -457,6 +463,7 @@ def main():
         "vs_baseline": None, "dtype": "fp8 (e4m3/e5m2 operands, fp32 accumulation)",
         "data": "synthetic (seeded Philox, bf16 inputs)",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "f": w.f, "gemm_flops_per_step": w.gemm_flops(),
+                   "backward": "recompute H and a8 from n8 with the retained scale" if args.recompute else "stored H and a8",
                    "l2": "inputs larger than L2 (bf16 weights 407 MB per step), no flush",
                    "parallelism": "replicas" if world > 1 else "single"},
         "tokens_per_s": world * w.T / (ms_step * 1e-3),

@@ -20,13 +20,15 @@ enum Kind {
   kKAbsmaxPartial = 0, kKQuantCast, kKRmsnormStats, kKRmsnormCast, kKSwigluAmax, kKSwigluCast, kKRmsnormBwd,
   kKGemmGateUp, kKGemmDown, kKGemmDownDgrad, kKGemmDownWgrad, kKGemmGateUpDgrad, kKGemmGateUpWgrad, kKGemm,
   kKGemmQkv, kKGemmOResidual, kKGemmODgrad, kKGemmOWgrad, kKGemmQkvDgrad, kKGemmQkvWgrad,
+  kKGemmGateUpRecompute,
   kKCount
 };
 const char* const kKindNames[kKCount] = {
     "absmax_partial", "quant_cast", "rmsnorm_stats", "rmsnorm_cast", "swiglu_amax", "swiglu_cast",
     "rmsnorm_bwd", "gemm_gate_up_swiglu", "gemm_down_residual", "gemm_down_dgrad_swiglu_bwd",
     "gemm_down_wgrad", "gemm_gate_up_dgrad", "gemm_gate_up_wgrad", "gemm",
-    "gemm_qkv", "gemm_o_residual", "gemm_o_dgrad", "gemm_o_wgrad", "gemm_qkv_dgrad", "gemm_qkv_wgrad"};
+    "gemm_qkv", "gemm_o_residual", "gemm_o_dgrad", "gemm_o_wgrad", "gemm_qkv_dgrad", "gemm_qkv_wgrad",
+    "gemm_gate_up_recompute"};
 
 struct Trace {
   bool on = false;
@@ -256,6 +258,31 @@ int mlp_bwd_run(const fp8q_mlp* m, const MlpWs& w, Ctx& c) {
   const float* s_a = m->scal + 9;
   float* s_dy = m->scal + 12;
   float* s_dh = m->scal + 15;
+  if (m->recompute) {
+    // H and a8 again from the retained n8, W_gu8 and scales; SwiGLU + E4M3 cast fused
+    GemmProblem g1{};
+    g1.a_mn = 0;
+    g1.b_mn = 1;
+    g1.M = (int)T;
+    g1.N = (int)f;
+    g1.K = (int)d;
+    g1.A = m->n8;
+    g1.lda = d;
+    g1.fmtA = 0;
+    g1.B = m->W_gu8;
+    g1.ldb = 2 * f;
+    g1.fmtB = 0;
+    g1.b_cols = 2 * f;
+    g1.sinvA = s_n + 2;
+    g1.sinvB = s_wgu + 2;
+    g1.epi = kEpiSwiglu;
+    g1.C = m->H;
+    g1.ldc = 2 * f;
+    g1.qscale = s_a + 1;
+    g1.q8 = m->a8;
+    int Pr = 0;
+    FP8Q_STEP(kKGemmGateUpRecompute, launch_gemm(g1, &Pr, c.L));
+  }
   uint8_t* dY8 = m->dY8 ? m->dY8 : w.dY8;
   uint16_t* dH = m->dH ? (uint16_t*)m->dH : w.dH;
   uint8_t* dH8 = m->dH8 ? m->dH8 : w.dH8;

@@ -61,6 +61,7 @@ struct Args {
   const uint16_t* R;
   int64_t ldr;
   float* aux;  // kEpiSwiglu: the fp32 SwiGLU output a [M, N] (ld = N), or null
+  const float* qscale;  // kEpiSwiglu: with it, a is written as E4M3 codes fp8(fl32(a * *qscale)) instead
   uint32_t* amax_partial;
   unsigned* status;
 };
@@ -121,6 +122,12 @@ __device__ __forceinline__ void stage_bf16(uint32_t buf, int r, const float (&v)
     st_shared_v4(buf + r * 64 + ((q ^ ((r >> 1) & 3)) << 4),
                  make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
                             pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7])));
+}
+// 32 rows x 32 bytes of FP8 codes (32-byte rows, 32-byte swizzle).
+__device__ __forceinline__ void stage_u8(uint32_t buf, int r, const uint32_t (&w)[8]) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+    st_shared_v4(buf + r * 32 + ((q ^ ((r >> 2) & 1)) << 4), make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
 }
 __device__ __forceinline__ void stage_f32(uint32_t buf, int r, const float (&v)[32]) {
 #pragma unroll
@@ -371,6 +378,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_store_2d(&tmAux, buf, col, row0);
                 bulk_commit();
               }
+            } else if (p.qscale) {
+              // recomputation with the retained scale: SwiGLU fused with the E4M3 cast
+              const float sq = *p.qscale;
+              uint32_t w[8];
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                w[q] = cvt_fp8x4<0>(__fmul_rn(a[4 * q], sq), __fmul_rn(a[4 * q + 1], sq), __fmul_rn(a[4 * q + 2], sq),
+                                    __fmul_rn(a[4 * q + 3], sq));
+              staging_acquire(lane);
+              stage_u8(buf, lane, w);
+              staging_publish();
+              if (lane == 0) {
+                tma_store_2d(&tmAux, buf, col, row0);
+                bulk_commit();
+              }
             }
           }
         }
@@ -506,21 +528,27 @@ bool make_tmap(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, i
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Output tensor [rows, cols] (row stride ld elements) of bf16 or fp32, stored in
-// 32 x 32 element boxes: bf16 boxes are 64 B wide (64-byte swizzle), fp32 boxes
-// 128 B wide (128-byte swizzle), matching stage_bf16 / stage_f32.
-bool make_out_tmap(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t ld, bool f32) {
+// Output tensor [rows, cols] (row stride ld elements) stored in 32 x 32 element
+// boxes: bf16 boxes are 64 B wide (64-byte swizzle), fp32 boxes 128 B wide
+// (128-byte swizzle), uint8 boxes 32 B wide (32-byte swizzle), matching
+// stage_bf16 / stage_f32 / stage_u8.
+enum OutKind { kOutBf16, kOutF32, kOutU8 };
+bool make_out_tmap(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t ld, OutKind kind) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
-  const int64_t es = f32 ? 4 : 2;
+  const int64_t es = kind == kOutF32 ? 4 : (kind == kOutBf16 ? 2 : 1);
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)(ld * es)};
   const cuuint32_t box[2] = {32, 32};
   const cuuint32_t estr[2] = {1, 1};
-  return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
-             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const CUtensorMapDataType dt = kind == kOutF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : kind == kOutBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const CUtensorMapSwizzle sw = kind == kOutF32 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : kind == kOutBf16 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                   : CU_TENSOR_MAP_SWIZZLE_32B;
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Instruction descriptor for kind::f8f6f4: fp32 accumulator, A/B formats
@@ -563,6 +591,7 @@ cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L) {
   a.R = g.R;
   a.ldr = g.ldr;
   a.aux = g.aux;
+  a.qscale = g.aux ? nullptr : g.qscale;
   a.amax_partial = g.amax_partial;
   a.status = L.status;
   a.idesc = make_idesc(g.fmtA, g.fmtB, g.a_mn, g.b_mn);
@@ -586,11 +615,12 @@ cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L) {
   if (g.epi == kEpiSwiglu || g.epi == kEpiSwigluBwd) {
     // gate half [M, f] and up half [M, f] of the [M, 2f] output, each clipped at f
     const uint16_t* c = static_cast<const uint16_t*>(g.C);
-    ok_c = make_out_tmap(&tc, c, g.N, g.M, g.ldc, false) && make_out_tmap(&tc2, c + g.N, g.N, g.M, g.ldc, false);
+    ok_c = make_out_tmap(&tc, c, g.N, g.M, g.ldc, kOutBf16) && make_out_tmap(&tc2, c + g.N, g.N, g.M, g.ldc, kOutBf16);
     taux = tc;
-    if (ok_c && g.aux) ok_c = make_out_tmap(&taux, g.aux, g.N, g.M, g.N, true);
+    if (ok_c && g.aux) ok_c = make_out_tmap(&taux, g.aux, g.N, g.M, g.N, kOutF32);
+    else if (ok_c && g.qscale && g.q8) ok_c = make_out_tmap(&taux, g.q8, g.N, g.M, g.N, kOutU8);
   } else {
-    ok_c = make_out_tmap(&tc, g.C, g.N, g.M, g.ldc, g.out_f32 != 0);
+    ok_c = make_out_tmap(&tc, g.C, g.N, g.M, g.ldc, g.out_f32 ? kOutF32 : kOutBf16);
     tc2 = taux = tc;
   }
   if (!ok_a || !ok_b || !ok_c) return cudaErrorInvalidValue;

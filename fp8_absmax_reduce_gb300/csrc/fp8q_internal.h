@@ -71,6 +71,8 @@ struct GemmProblem {
   void* C; int64_t ldc;  // kEpiSwiglu/kEpiSwigluBwd: [M, 2f] gate | up
   const uint16_t* R; int64_t ldr;  // residual (kEpiResidual) or H (kEpiSwigluBwd)
   float* aux;                      // kEpiSwiglu: optional fp32 SwiGLU output a [M, N]
+  const float* qscale;             // kEpiSwiglu without aux: scale of a; a is written as E4M3 codes to q8
+  uint8_t* q8;                     //   [M, N] E4M3
   uint32_t* amax_partial;          // per-CTA partials for the two SwiGLU epilogues
 };
 // Launches the persistent tcgen05 GEMM; *P receives the number of partials written.

@@ -198,6 +198,14 @@ typedef struct fp8q_mlp {
   void* dH;         /* [T,2f] bf16 */
   uint8_t* dH8;     /* [T,2f] E5M2 */
   float* dN;        /* [T,d]  fp32 */
+  /* Recompute mode (LLMQ §3.1: activations are recomputed in the backward from
+   * what was retained, here n8 and the scales; the retained absmax scale of a
+   * lets SwiGLU and its E4M3 cast fuse into the recomputing GEMM's epilogue).
+   * Nonzero: mlp_block_bwd does not read the forward's H and a8; it recomputes
+   * H = bf16(alpha n8 @ W_gu8) into H and a8 = q(SwiGLU(H)) with scal's
+   * retained scale of a into a8, bit-identical to the forward's, so the
+   * caller need not keep H and a8 alive between the forward and backward. */
+  int recompute;
 } fp8q_mlp;
 
 /* backward != 0 sizes the workspace for mlp_block_bwd (which also suffices for mlp_block_fwd). */
