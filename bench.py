@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--recompute", action="store_true",
                     help="recompute-mode backward (H and a8 recomputed from n8 with the retained scale)")
+    ap.add_argument("--grad-e4m3", action="store_true",
+                    help="E4M3 gradients (dY, dH; dh, dQKV in the full block) instead of E5M2")
     ap.add_argument("--measure-fp8-peak", action="store_true",
                     help="time cuBLASLt FP8 (torch._scaled_mm) 8192^3, burst and sustained, and exit")
     ap.add_argument("--tokens", type=int, default=0,
@@ -226,6 +228,7 @@ def run_ours(args, rank, world, local_rank):
             dev_out.update(dX=b.dX, dW_gu=b.dW_gu, dW_d=b.dW_d, dg=b.dg)
         fwd, bwd = fq.mlp_block_fwd, fq.mlp_block_bwd
     (b.mlp if w.qkv else b).recompute = bool(args.recompute)
+    (b.mlp if w.qkv else b).grad_e4m3 = bool(args.grad_e4m3)
     host_in = {k: torch.from_numpy(inp[k].view(np.int16)).view(torch.bfloat16).pin_memory() for k in dev_in}
     for k, t in dev_in.items():
         t.copy_(host_in[k])
@@ -334,22 +337,23 @@ def kernel_table(traced, plan, K, pk):
     return out, total
 
 
-def cpu_baseline(w, tokens):
+def cpu_baseline(w, tokens, grad_e4m3=False):
     import oracle
     oracle.build()
+    gf = oracle.E4M3 if grad_e4m3 else oracle.E5M2
     if w.qkv:
         inp = synth.block_inputs(w, seed=0)
         sl = {k: inp[k][:tokens] for k in ("x", "att", "dY", "dQKV") if k in inp}
         t0 = time.perf_counter()
         oracle.full_block(sl["x"], inp["g1"], inp["W_qkv"], inp["W_o"], sl["att"], inp["g"], inp["W_gu"],
-                          inp["W_d"], dY=sl.get("dY"), dQKV=sl.get("dQKV"), nthreads=1)
+                          inp["W_d"], dY=sl.get("dY"), dQKV=sl.get("dQKV"), nthreads=1, grad_fmt=gf)
         dt = time.perf_counter() - t0
     else:
         inp = synth.mlp_inputs(w, seed=0)
         x = inp["x"][:tokens]
         dY = inp["dY"][:tokens] if w.backward else None
         t0 = time.perf_counter()
-        oracle.block(x, inp["g"], inp["W_gu"], inp["W_d"], dY=dY, nthreads=1)
+        oracle.block(x, inp["g"], inp["W_gu"], inp["W_d"], dY=dY, nthreads=1, grad_fmt=gf)
         dt = time.perf_counter() - t0
     sub = synth.Workload(w.name, tokens, w.d, w.f, w.x_kind, w.x_scale, w.outlier_frac, w.outlier_mult,
                          w.w_std, w.dy_std, w.qkv)
@@ -416,9 +420,9 @@ def main():
             return
         tokens = 2
         for _ in range(args.warmup):
-            cpu_baseline(w, tokens)
+            cpu_baseline(w, tokens, args.grad_e4m3)
         t0 = time.perf_counter()
-        res = [cpu_baseline(w, tokens) for _ in range(args.steps)]
+        res = [cpu_baseline(w, tokens, args.grad_e4m3) for _ in range(args.steps)]
         dt = time.perf_counter() - t0
         sub_flops = w.gemm_flops() * tokens / w.T
         value = sub_flops * args.steps / dt / 1e12
@@ -426,7 +430,8 @@ def main():
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic (seeded Philox, bf16)",
-                "config": {"workload": w.name, "T": w.T, "d": w.d, "f": w.f},
+                "config": {"workload": w.name, "T": w.T, "d": w.d, "f": w.f,
+                           "gradients": "e4m3" if args.grad_e4m3 else "e5m2"},
                 "cpu_baseline": {"kind": "oracle", "cores": 1, "value": value, "unit": "TFLOP/s",
                                  "sample": res[0]["sample"]},
                 "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -464,6 +469,7 @@ def main():
         "data": "synthetic (seeded Philox, bf16 inputs)",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "f": w.f, "gemm_flops_per_step": w.gemm_flops(),
                    "backward": "recompute H and a8 from n8 with the retained scale" if args.recompute else "stored H and a8",
+                   "gradients": "e4m3" if args.grad_e4m3 else "e5m2",
                    "l2": "inputs larger than L2 (bf16 weights 407 MB per step), no flush",
                    "parallelism": "replicas" if world > 1 else "single"},
         "tokens_per_s": world * w.T / (ms_step * 1e-3),
@@ -481,7 +487,7 @@ def main():
     if r["e2e"]:
         line["e2e"] = r["e2e"]
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, args.cpu_sample_tokens)
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_sample_tokens, args.grad_e4m3)
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

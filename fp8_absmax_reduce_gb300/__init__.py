@@ -71,7 +71,7 @@ class FP8QMlp(ctypes.Structure):
         (name, ctypes.c_void_p) for name in (
             "x", "g", "W_gu", "W_d", "y", "W_gu8", "W_d8", "n8", "rstd", "H", "a8", "scal",
             "dY", "dX", "dW_gu", "dW_d", "dg", "dY8", "dH", "dH8", "dN")
-    ] + [("recompute", ctypes.c_int)]
+    ] + [("recompute", ctypes.c_int), ("grad_e4m3", ctypes.c_int)]
 
 
 class FP8QBlock(ctypes.Structure):
@@ -235,6 +235,7 @@ class MlpBuffers:
     dN: torch.Tensor | None = None
     ws: torch.Tensor | None = None
     recompute: bool = False
+    grad_e4m3: bool = False
 
     @staticmethod
     def allocate(T: int, d: int, f: int, device="cuda", backward: bool = True, eps: float = 1e-6,
@@ -262,8 +263,9 @@ class MlpBuffers:
         return b
 
     def struct(self) -> FP8QMlp:
-        s = FP8QMlp(T=self.T, d=self.d, f=self.f, eps=self.eps, recompute=int(self.recompute))
-        for name, _ in FP8QMlp._fields_[4:-1]:
+        s = FP8QMlp(T=self.T, d=self.d, f=self.f, eps=self.eps, recompute=int(self.recompute),
+                    grad_e4m3=int(self.grad_e4m3))
+        for name, _ in FP8QMlp._fields_[4:-2]:
             t = getattr(self, name)
             setattr(s, name, None if t is None else t.data_ptr())
         return s

@@ -287,10 +287,11 @@ int mlp_bwd_run(const fp8q_mlp* m, const MlpWs& w, Ctx& c) {
   uint16_t* dH = m->dH ? (uint16_t*)m->dH : w.dH;
   uint8_t* dH8 = m->dH8 ? m->dH8 : w.dH8;
   float* dN = m->dN ? m->dN : w.dN;
+  const int gf = m->grad_e4m3 ? 0 : 1;  // gradient format: E5M2 unless the E4M3 recipe is asked for
   int P = 0;
   // dY8 = q5(dY)
   FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(m->dY, 0, T * d, w.part_q, &P, c.L));
-  FP8Q_STEP(kKQuantCast, launch_quant_cast(m->dY, 0, T * d, 1, w.part_q, P, dY8, s_dy, c.L));
+  FP8Q_STEP(kKQuantCast, launch_quant_cast(m->dY, 0, T * d, gf, w.part_q, P, dY8, s_dy, c.L));
   // G3 (NT): dA = alpha dY8 @ W_d8^T, SwiGLU backward fused -> dH + absmax partials
   GemmProblem g3{};
   g3.a_mn = 0;
@@ -300,7 +301,7 @@ int mlp_bwd_run(const fp8q_mlp* m, const MlpWs& w, Ctx& c) {
   g3.K = (int)d;
   g3.A = dY8;
   g3.lda = d;
-  g3.fmtA = 1;
+  g3.fmtA = gf;
   g3.B = m->W_d8;
   g3.ldb = d;
   g3.fmtB = 0;
@@ -315,7 +316,7 @@ int mlp_bwd_run(const fp8q_mlp* m, const MlpWs& w, Ctx& c) {
   g3.amax_partial = w.part_g;
   FP8Q_STEP(kKGemmDownDgrad, launch_gemm(g3, &P, c.L));
   // dH8 = q5(dH)
-  FP8Q_STEP(kKQuantCast, launch_quant_cast(dH, 0, T * 2 * f, 1, w.part_g, P, dH8, s_dh, c.L));
+  FP8Q_STEP(kKQuantCast, launch_quant_cast(dH, 0, T * 2 * f, gf, w.part_g, P, dH8, s_dh, c.L));
   // G4 (TN): dW_d = alpha a8^T @ dY8
   GemmProblem g4{};
   g4.a_mn = 1;
@@ -328,7 +329,7 @@ int mlp_bwd_run(const fp8q_mlp* m, const MlpWs& w, Ctx& c) {
   g4.fmtA = 0;
   g4.B = dY8;
   g4.ldb = d;
-  g4.fmtB = 1;
+  g4.fmtB = gf;
   g4.b_cols = d;
   g4.sinvA = s_a + 2;
   g4.sinvB = s_dy + 2;
@@ -346,7 +347,7 @@ int mlp_bwd_run(const fp8q_mlp* m, const MlpWs& w, Ctx& c) {
   g5.K = (int)(2 * f);
   g5.A = dH8;
   g5.lda = 2 * f;
-  g5.fmtA = 1;
+  g5.fmtA = gf;
   g5.B = m->W_gu8;
   g5.ldb = 2 * f;
   g5.fmtB = 0;
@@ -370,7 +371,7 @@ int mlp_bwd_run(const fp8q_mlp* m, const MlpWs& w, Ctx& c) {
   g6.fmtA = 0;
   g6.B = dH8;
   g6.ldb = 2 * f;
-  g6.fmtB = 1;
+  g6.fmtB = gf;
   g6.b_cols = 2 * f;
   g6.sinvA = s_n + 2;
   g6.sinvB = s_dh + 2;
@@ -503,24 +504,25 @@ int block_bwd_run(const fp8q_block* b, const BlockWs& w, Ctx& c) {
   uint8_t* dh8 = b->dh8 ? b->dh8 : w.dh8;
   uint8_t* dqkv8 = b->dQKV8 ? b->dQKV8 : w.dqkv8;
   float* dN1 = b->dN1 ? b->dN1 : w.dN1;
+  const int gf = b->mlp.grad_e4m3 ? 0 : 1;
   int P = 0;
   FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(dh, 0, T * d, w.part, &P, c.L));
-  FP8Q_STEP(kKQuantCast, launch_quant_cast(dh, 0, T * d, 1, w.part, P, dh8, s_dh, c.L));
+  FP8Q_STEP(kKQuantCast, launch_quant_cast(dh, 0, T * d, gf, w.part, P, dh8, s_dh, c.L));
   // d_att = bf16(alpha dh8 @ W_o8^T): B = W_o8 [d_in, d_out] is K-major for this product
-  GemmProblem god = gemm_problem(0, 0, T, d, d, dh8, d, 1, b->W_o8, d, 0, d, s_dh + 2, s_o + 2, kEpiStore, 0,
+  GemmProblem god = gemm_problem(0, 0, T, d, d, dh8, d, gf, b->W_o8, d, 0, d, s_dh + 2, s_o + 2, kEpiStore, 0,
                                  b->d_att, d);
   FP8Q_STEP(kKGemmODgrad, launch_gemm(god, &P, c.L));
   // dW_o = alpha att8^T @ dh8
-  GemmProblem gow = gemm_problem(1, 1, d, d, T, b->att8, d, 0, dh8, d, 1, d, s_att + 2, s_dh + 2, kEpiStore, 1,
+  GemmProblem gow = gemm_problem(1, 1, d, d, T, b->att8, d, 0, dh8, d, gf, d, s_att + 2, s_dh + 2, kEpiStore, 1,
                                  b->dW_o, d);
   FP8Q_STEP(kKGemmOWgrad, launch_gemm(gow, &P, c.L));
   // dQKV8 = q5(dQKV); dN1 = alpha dQKV8 @ W_qkv8^T; dW_qkv = alpha n1_8^T @ dQKV8
   FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(b->dQKV, 0, T * nq, w.part, &P, c.L));
-  FP8Q_STEP(kKQuantCast, launch_quant_cast(b->dQKV, 0, T * nq, 1, w.part, P, dqkv8, s_dq, c.L));
-  GemmProblem gqd = gemm_problem(0, 0, T, d, nq, dqkv8, nq, 1, b->W_qkv8, nq, 0, d, s_dq + 2, s_qkv + 2, kEpiStore,
+  FP8Q_STEP(kKQuantCast, launch_quant_cast(b->dQKV, 0, T * nq, gf, w.part, P, dqkv8, s_dq, c.L));
+  GemmProblem gqd = gemm_problem(0, 0, T, d, nq, dqkv8, nq, gf, b->W_qkv8, nq, 0, d, s_dq + 2, s_qkv + 2, kEpiStore,
                                  1, dN1, d);
   FP8Q_STEP(kKGemmQkvDgrad, launch_gemm(gqd, &P, c.L));
-  GemmProblem gqw = gemm_problem(1, 1, d, nq, T, b->n1_8, d, 0, dqkv8, nq, 1, nq, s_n1 + 2, s_dq + 2, kEpiStore, 1,
+  GemmProblem gqw = gemm_problem(1, 1, d, nq, T, b->n1_8, d, 0, dqkv8, nq, gf, nq, s_n1 + 2, s_dq + 2, kEpiStore, 1,
                                  b->dW_qkv, nq);
   FP8Q_STEP(kKGemmQkvWgrad, launch_gemm(gqw, &P, c.L));
   // dX = bf16(dh + RMSNorm_1'(dN1)), dg1

@@ -169,30 +169,32 @@ __global__ void __launch_bounds__(kThreads) k_rmsnorm_stats(const uint16_t* __re
   uint32_t m = 0;
   for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < T; row += nw) {
     const uint16_t* xr = x + row * d;
+    // all of the row's loads first, then the lane-level trees, then the butterflies
+    uint4 w[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const int j0 = c * 256 + lane * 8;
+      w[c] = (c * 256 < d && j0 < d) ? ld_v4(xr + j0) : make_uint4(0u, 0u, 0u, 0u);
+    }
     float cs[32];
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
-      float v = 0.0f;
-      if (c * 256 < d) {
-        const int j0 = c * 256 + lane * 8;
-        if (j0 < d) {
-          const uint4 w = ld_v4(xr + j0);
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-          float s[8];
+      const uint32_t ww[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
+      float s[8];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float lo = bf16_lo(ww[k]), hi = bf16_hi(ww[k]);
-            s[2 * k] = __fmul_rn(lo, lo);
-            s[2 * k + 1] = __fmul_rn(hi, hi);
-          }
-          v = __fadd_rn(__fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3])),
-                        __fadd_rn(__fadd_rn(s[4], s[5]), __fadd_rn(s[6], s[7])));
-        }
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+      for (int k = 0; k < 4; ++k) {
+        const float lo = bf16_lo(ww[k]), hi = bf16_hi(ww[k]);
+        s[2 * k] = __fmul_rn(lo, lo);
+        s[2 * k + 1] = __fmul_rn(hi, hi);
       }
-      cs[c] = v;
+      cs[c] = __fadd_rn(__fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3])),
+                        __fadd_rn(__fadd_rn(s[4], s[5]), __fadd_rn(s[6], s[7])));
     }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (c * 256 < d) cs[c] = __fadd_rn(cs[c], __shfl_xor_sync(0xFFFFFFFFu, cs[c], o));
 #pragma unroll
     for (int w = 1; w < 32; w <<= 1)
 #pragma unroll

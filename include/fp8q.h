@@ -163,7 +163,7 @@ FP8Q_API int swiglu_quant(const void* H, int64_t T, int64_t f, fp8q_fmt fmt, uin
 /* Forward:  W_gu8 = q(W_gu), W_d8 = q(W_d), n8 = q(RMSNorm(x) * g),
  *           H = bf16(alpha * n8 @ W_gu8)  [T,2f],  a8 = q(silu(H_gate) * H_up),
  *           y = bf16(x + alpha * a8 @ W_d8).
- * Backward: dY8 = q5(dY),  dA = alpha * dY8 @ W_d8^T,
+ * Backward: dY8 = q5(dY),  dA = alpha * dY8 @ W_d8^T   (q5: E5M2, or E4M3 with grad_e4m3),
  *           dH = bf16(SwiGLU'(H) * dA), dH8 = q5(dH),
  *           dW_d = alpha * a8^T @ dY8,  dN = alpha * dH8 @ W_gu8^T,
  *           dW_gu = alpha * n8^T @ dH8  (fp32),
@@ -206,6 +206,10 @@ typedef struct fp8q_mlp {
    * retained scale of a into a8, bit-identical to the forward's, so the
    * caller need not keep H and a8 alive between the forward and backward. */
   int recompute;
+  /* Nonzero: every gradient the backward quantizes (dY, dH; in fp8q_block also
+   * dh and dQKV) is E4M3 instead of E5M2 -- LLMQ §5 Figure 2's recipe with E4M3
+   * forward and backward.  Zero (default): E5M2 gradients. */
+  int grad_e4m3;
 } fp8q_mlp;
 
 /* backward != 0 sizes the workspace for mlp_block_bwd (which also suffices for mlp_block_fwd). */

@@ -62,7 +62,7 @@ def _c(arr):
 class _BlockIO(ctypes.Structure):
     _fields_ = [
         ("T", ctypes.c_int64), ("d", ctypes.c_int64), ("f", ctypes.c_int64),
-        ("eps", ctypes.c_float), ("exact", ctypes.c_int), ("nthreads", ctypes.c_int),
+        ("eps", ctypes.c_float), ("exact", ctypes.c_int), ("nthreads", ctypes.c_int), ("grad_fmt", ctypes.c_int),
         ("x", ctypes.c_void_p), ("g", ctypes.c_void_p), ("Wgu", ctypes.c_void_p),
         ("Wd", ctypes.c_void_p), ("dY", ctypes.c_void_p),
         ("y", ctypes.c_void_p), ("H", ctypes.c_void_p), ("rstd", ctypes.c_void_p),
@@ -246,7 +246,8 @@ def _as_f64(a, exact):
     return bf16_to_f64(a)
 
 
-def block(x, g, Wgu, Wd, dY=None, eps: float = 1e-6, exact: bool = False, nthreads: int = 1):
+def block(x, g, Wgu, Wd, dY=None, eps: float = 1e-6, exact: bool = False, nthreads: int = 1,
+          grad_fmt: int = E5M2):
     """MLP block forward (and backward when dY is given).
 
     Quantized mode (exact=False): x, g, Wgu, Wd, dY are bf16 bit patterns
@@ -268,7 +269,7 @@ def block(x, g, Wgu, Wd, dY=None, eps: float = 1e-6, exact: bool = False, nthrea
         "n8": np.empty((T, d), np.uint8), "a8": np.empty((T, f), np.uint8),
         "scal_fwd": np.zeros((4, 3), np.float32),
     }
-    io = _BlockIO(T=T, d=d, f=f, eps=eps, exact=int(exact), nthreads=int(nthreads))
+    io = _BlockIO(T=T, d=d, f=f, eps=eps, exact=int(exact), nthreads=int(nthreads), grad_fmt=int(grad_fmt))
     keep = [x64, g64, Wgu64, Wd64]
     io.x, io.g, io.Wgu, io.Wd = (a.ctypes.data for a in keep)
     for k in ("y", "H", "rstd", "Wgu8", "Wd8", "n8", "a8", "scal_fwd"):
@@ -293,7 +294,7 @@ def block(x, g, Wgu, Wd, dY=None, eps: float = 1e-6, exact: bool = False, nthrea
 
 
 def full_block(x, g1, Wqkv, Wo, att, g2, Wgu, Wd, dY=None, dQKV=None, eps: float = 1e-6, exact: bool = False,
-               nthreads: int = 1):
+               nthreads: int = 1, grad_fmt: int = E5M2):
     """The full transformer block's matmuls around a given attention core.
 
     Forward: qkv = bf16(alpha n1_8 @ W_qkv8) with n1 = RMSNorm(x) g1; h = bf16(x + alpha att8 @ W_o8);
@@ -321,7 +322,7 @@ def full_block(x, g1, Wqkv, Wo, att, g2, Wgu, Wd, dY=None, dQKV=None, eps: float
     keep = [x64, g164, Wqkv64, Wo64, att64, g264, Wgu64, Wd64]
     io = _FullIO(T=T, d=d, f=f, nq=nq, eps=eps, exact=int(exact), nthreads=int(nthreads))
     io.x, io.g1, io.Wqkv, io.Wo, io.att = (a.ctypes.data for a in keep[:5])
-    m = _BlockIO(T=T, d=d, f=f, eps=eps, exact=int(exact), nthreads=int(nthreads))
+    m = _BlockIO(T=T, d=d, f=f, eps=eps, exact=int(exact), nthreads=int(nthreads), grad_fmt=int(grad_fmt))
     m.g, m.Wgu, m.Wd = (a.ctypes.data for a in keep[5:])
     for k in ("qkv", "h", "rstd1", "Wqkv8", "Wo8", "n1_8", "att8", "scal_attn"):
         setattr(io, k, out[k].ctypes.data)

@@ -334,7 +334,8 @@ std::vector<double> swiglu_fwd(const std::vector<double>& H, int64_t T, int64_t 
 //   H = bf16(alpha1 * n8 @ Wgu8)                         [T, 2f] gate | up
 //   a = silu(H_gate) * H_up ; a8 = q(a)                  E4M3
 //   y = bf16(x + alpha2 * a8 @ Wd8)                      residual
-// Backward (straight-through quantizers; gradients E5M2 per LLMQ §5 Fig. 2):
+// Backward (straight-through quantizers; gradients E5M2 per LLMQ §5 Fig. 2, or
+// E4M3 -- the recipe that figure shows tracking BF16 -- when grad_fmt says so):
 //   dY8 = q5(dY)
 //   dA  = alpha3 * dY8 @ Wd8^T                           (fp32 in registers on a GPU)
 //   dH_gate = dA * up * s * (1 + h (1 - s)), dH_up = dA * silu(h), s = sigmoid(h)
@@ -350,6 +351,7 @@ struct BlockIO {
   float eps;
   int exact;
   int nthreads;
+  int grad_fmt;  // format of the quantized gradients (E5M2 by default, E4M3 for LLMQ's E4M3-everywhere recipe)
   // inputs, [T,d] [d] [d,2f] [f,d] (and dY [T,d] for backward), as doubles
   const double* x; const double* g; const double* Wgu; const double* Wd; const double* dY;
   // forward outputs (doubles hold the stored value: bf16 / fp32 / decoded code)
@@ -425,7 +427,8 @@ int block_backward(const BlockIO& io, const FwdState& S) {
   int status = S.status;
   std::vector<double> x(io.x, io.x + T * d), g(io.g, io.g + d), dY(io.dY, io.dY + T * d);
 
-  QTensor dY8 = quantize(dY, FMT_E5M2, ex);
+  const int gf = io.grad_fmt;
+  QTensor dY8 = quantize(dY, gf, ex);
 
   // dA = alpha3 * dY8 @ Wd8^T   ([T,d] x [d,f])
   const double alpha3 = ex ? 1.0 : (double)(dY8.s.scale_inv * S.Wd.s.scale_inv);
@@ -444,7 +447,7 @@ int block_backward(const BlockIO& io, const FwdState& S) {
       dH[t * 2 * f + j] = ex ? dg_ : to_bf16(dg_);
       dH[t * 2 * f + f + j] = ex ? du_ : to_bf16(du_);
     }
-  QTensor dH8 = quantize(dH, FMT_E5M2, ex);
+  QTensor dH8 = quantize(dH, gf, ex);
 
   auto out32 = [&](double v) { return ex ? v : (double)(float)v; };
 
@@ -593,7 +596,7 @@ int full_block(FullIO& io, bool backward) {
   put(io.dh, dh);
 
   // O projection backward
-  QTensor dhq = quantize(dh, FMT_E5M2, ex);
+  QTensor dhq = quantize(dh, io.mlp.grad_fmt, ex);
   const double a_od = ex ? 1.0 : (double)(dhq.s.scale_inv * Wo.s.scale_inv);
   std::vector<double> datt = matmul(dhq.deq, transpose(Wo.deq, d, d), T, d, d, io.nthreads);
   for (double& v : datt) v = ex ? a_od * v : to_bf16(a_od * v);
@@ -602,7 +605,7 @@ int full_block(FullIO& io, bool backward) {
   for (double& v : dWo) v = ex ? a_ow * v : (double)(float)(a_ow * v);
 
   // QKV projection backward
-  QTensor dqq = quantize(std::vector<double>(io.dQKV, io.dQKV + T * nq), FMT_E5M2, ex);
+  QTensor dqq = quantize(std::vector<double>(io.dQKV, io.dQKV + T * nq), io.mlp.grad_fmt, ex);
   const double a_qd = ex ? 1.0 : (double)(dqq.s.scale_inv * Wqkv.s.scale_inv);
   std::vector<double> dN1 = matmul(dqq.deq, transpose(Wqkv.deq, d, nq), T, d, nq, io.nthreads);
   for (double& v : dN1) v = ex ? a_qd * v : (double)(float)(a_qd * v);

@@ -23,12 +23,13 @@ from tests._gpu import code_step_diff, dev_bf16, host_bits, host_f64, row_rel
 pytestmark = pytest.mark.gpu
 
 
-def run_block(wname, T, d, f, backward=True, seed=0):
+def run_block(wname, T, d, f, backward=True, seed=0, grad_e4m3=False):
     w = synth.BY_NAME[wname]
     inp = synth.mlp_inputs(w, seed=seed, T=T, d=d, f=f)
     if backward and "dY" not in inp:
         inp["dY"] = synth.normal_bf16((T, d), 1e-3, seed, synth.TID_DY)
     b = fq.MlpBuffers.allocate(T, d, f, backward=backward, keep_intermediates=True)
+    b.grad_e4m3 = grad_e4m3
     for k in ("x", "g", "W_gu", "W_d") + (("dY",) if backward else ()):
         getattr(b, k).copy_(dev_bf16(inp[k]))
     fq.get_status(clear=True)
@@ -38,7 +39,7 @@ def run_block(wname, T, d, f, backward=True, seed=0):
     torch.cuda.synchronize()
     assert fq.get_status() == 0
     ref = oracle.block(inp["x"], inp["g"], inp["W_gu"], inp["W_d"], dY=inp["dY"] if backward else None,
-                       eps=b.eps, nthreads=16)
+                       eps=b.eps, nthreads=16, grad_fmt=oracle.E4M3 if grad_e4m3 else oracle.E5M2)
     return b, ref
 
 
@@ -102,3 +103,12 @@ def test_block_deterministic():
         outs.append([t.clone() for t in (b.y, b.dX, b.dW_gu, b.dW_d, b.dg, b.a8, b.dH8)])
     for a, c in zip(*outs):
         assert torch.equal(a, c)
+
+
+@pytest.mark.parametrize("T,d,f", [(272, 528, 400), (640, 1024, 1280)])
+def test_block_e4m3_gradients(T, d, f):
+    """LLMQ §5 Figure 2's E4M3-everywhere recipe: dY and dH quantized to E4M3."""
+    b, ref = run_block("7b-mlp-fwd-bwd", T, d, f, grad_e4m3=True)
+    assert float(b.scal[4, 1]) == float(np.float32(448.0) / np.float32(b.scal[4, 0].item()))
+    check_forward(b, ref)
+    check_backward(b, ref)

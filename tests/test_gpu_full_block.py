@@ -36,9 +36,10 @@ def upload(b, inp):
         t.copy_(dev_bf16(inp[k]))
 
 
-def run(T, d, f, nq, seed=0):
+def run(T, d, f, nq, seed=0, grad_e4m3=False):
     inp = synth.block_inputs(W32, seed=seed, T=T, d=d, f=f, n_qkv=nq)
     b = fq.BlockBuffers.allocate(T, d, f, nq, keep_intermediates=True)
+    b.mlp.grad_e4m3 = grad_e4m3
     upload(b, inp)
     fq.get_status(clear=True)
     fq.block_fwd(b)
@@ -54,11 +55,13 @@ def requant(gpu, ref, amax_gpu, amax_ref):
     assert abs(amax_gpu / amax_ref - 1) <= 2.0 ** -7
 
 
-@pytest.mark.parametrize("T,d,f,nq", [(192, 256, 384, 384), (272, 528, 400, 336), (64, 1024, 768, 1536)])
-def test_full_block_small_shapes(T, d, f, nq):
-    b, inp = run(T, d, f, nq)
+@pytest.mark.parametrize("T,d,f,nq,e4m3", [(192, 256, 384, 384, False), (272, 528, 400, 336, False),
+                                            (64, 1024, 768, 1536, False), (256, 512, 640, 768, True)])
+def test_full_block_small_shapes(T, d, f, nq, e4m3):
+    b, inp = run(T, d, f, nq, grad_e4m3=e4m3)
     ref = oracle.full_block(inp["x"], inp["g1"], inp["W_qkv"], inp["W_o"], inp["att"], inp["g"], inp["W_gu"],
-                            inp["W_d"], dY=inp["dY"], dQKV=inp["dQKV"], nthreads=16)
+                            inp["W_d"], dY=inp["dY"], dQKV=inp["dQKV"], nthreads=16,
+                            grad_fmt=oracle.E4M3 if e4m3 else oracle.E5M2)
     sa, sm = b.scal.cpu().numpy(), b.mlp.scal.cpu().numpy()
     for name, key in (("W_qkv8", "Wqkv8"), ("W_o8", "Wo8"), ("n1_8", "n1_8"), ("att8", "att8")):
         np.testing.assert_array_equal(getattr(b, name).cpu().numpy(), ref[key])

@@ -191,3 +191,25 @@ def test_full_block_quantized_wiring():
     np.testing.assert_array_equal(o["dqkv8"], dq8); np.testing.assert_array_equal(sa[5], s)
     dWqkv = oracle.gemm_scaled(oracle.TN, n1, 0, dq8, 1, sa[2, 2], sa[5, 2], out="f32")
     np.testing.assert_array_equal(o["dWqkv"], dWqkv.astype(np.float64))
+
+
+def test_e4m3_gradient_recipe_wiring():
+    """With grad_fmt = E4M3 the gradient quantizers and the dgrad/wgrad GEMM operands are E4M3
+    (LLMQ §5 Figure 2's E4M3 forward and backward)."""
+    T, d, f = 32, 64, 48
+    inp = small_inputs(T, d, f)
+    out = oracle.block(inp["x"], inp["g"], inp["W_gu"], inp["W_d"], dY=inp["dY"], grad_fmt=oracle.E4M3)
+    sf, sb = out["scal_fwd"], out["scal_bwd"]
+    dY8, s, _ = oracle.quantize_absmax(inp["dY"], oracle.E4M3)
+    np.testing.assert_array_equal(out["dY8"], dY8); np.testing.assert_array_equal(sb[0], s)
+    assert s[1] == np.float32(448.0) / s[0]
+    dH8, s, _ = oracle.quantize_absmax(oracle.bf16_round(out["dH"]), oracle.E4M3)
+    np.testing.assert_array_equal(out["dH8"], dH8); np.testing.assert_array_equal(sb[1], s)
+    dWd = oracle.gemm_scaled(oracle.TN, out["a8"], 0, dY8, 0, sf[3, 2], sb[0, 2], out="f32")
+    np.testing.assert_array_equal(out["dWd"], dWd.astype(np.float64))
+    dN = oracle.gemm_scaled(oracle.NT, dH8, 0, out["Wgu8"], 0, sb[1, 2], sf[0, 2], out="f32")
+    np.testing.assert_array_equal(out["dN"], dN.astype(np.float64))
+    e5 = oracle.block(inp["x"], inp["g"], inp["W_gu"], inp["W_d"], dY=inp["dY"])
+    for k in ("dX", "dWgu", "dWd"):   # both recipes approximate the same gradients
+        rel = np.linalg.norm(out[k] - e5[k]) / np.linalg.norm(e5[k])
+        assert 0 < rel < 0.2, (k, rel)
