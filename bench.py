@@ -57,6 +57,8 @@ def parse_args():
                     help="recompute-mode backward (H and a8 recomputed from n8 with the retained scale)")
     ap.add_argument("--grad-e4m3", action="store_true",
                     help="E4M3 gradients (dY, dH; dh, dQKV in the full block) instead of E5M2")
+    ap.add_argument("--bf16", action="store_true",
+                    help="the BF16 baseline (same block, bf16 operands, tcgen05 kind::f16) for the FP8/BF16 speedup")
     ap.add_argument("--measure-fp8-peak", action="store_true",
                     help="time cuBLASLt FP8 (torch._scaled_mm) 8192^3, burst and sustained, and exit")
     ap.add_argument("--tokens", type=int, default=0,
@@ -152,10 +154,24 @@ def job_throughput(units_per_rank: float, world: int, max_ms: float) -> float:
 # ---------------------------------------------------------------------------
 # per-launch algorithmic work of one step (order = the library's launch order)
 # ---------------------------------------------------------------------------
-def step_work(w: synth.Workload, recompute: bool = False):
+def step_work(w: synth.Workload, recompute: bool = False, bf16: bool = False):
     """(kernel kind, algorithmic bytes, flops) of every traced launch of one step (the recompute
     GEMM's flops are executed work on top of the algorithmic 18Tdf)."""
     T, d, f = w.T, w.d, w.f
+    if bf16:  # the BF16 baseline: 2-byte operands, no casts
+        fwd = [
+            ("rmsnorm_bf16", 4 * T * d + 2 * d + 4 * T, 0),
+            ("gemm_gate_up_swiglu", 2 * T * d + 2 * d * 2 * f + 2 * T * 2 * f + 2 * T * f, 2.0 * T * d * 2 * f),
+            ("gemm_down_residual", 2 * T * f + 2 * f * d + 4 * T * d, 2.0 * T * f * d),
+        ]
+        bwd = [
+            ("gemm_down_dgrad_swiglu_bwd", 2 * T * d + 2 * f * d + 2 * T * 2 * f * 2, 2.0 * T * d * f),
+            ("gemm_down_wgrad", 2 * T * f + 2 * T * d + 4 * f * d, 2.0 * f * T * d),
+            ("gemm_gate_up_dgrad", 2 * T * 2 * f + 2 * d * 2 * f + 4 * T * d, 2.0 * T * 2 * f * d),
+            ("gemm_gate_up_wgrad", 2 * T * d + 2 * T * 2 * f + 4 * d * 2 * f, 2.0 * d * T * 2 * f),
+            ("rmsnorm_bwd", 10 * T * d, 0),
+        ]
+        return fwd + (bwd if w.backward else [])
     mlp_fwd = [
         ("absmax_partial", 2 * d * 2 * f, 0), ("quant_cast", 3 * d * 2 * f, 0),
         ("absmax_partial", 2 * f * d, 0), ("quant_cast", 3 * f * d, 0),
@@ -221,7 +237,7 @@ def run_ours(args, rank, world, local_rank):
         fwd, bwd = fq.block_fwd, fq.block_bwd
     else:
         inp = synth.mlp_inputs(w, seed=rank)
-        b = fq.MlpBuffers.allocate(w.T, w.d, w.f, device=dev, backward=w.backward)
+        b = fq.MlpBuffers.allocate(w.T, w.d, w.f, device=dev, backward=w.backward, bf16=args.bf16)
         dev_in = {k: getattr(b, k) for k in ["x", "g", "W_gu", "W_d"] + (["dY"] if w.backward else [])}
         dev_out = {"y": b.y}
         if w.backward:
@@ -253,7 +269,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
 
     K = args.steps
-    plan = step_work(w, args.recompute)
+    plan = step_work(w, args.recompute, args.bf16)
     if lib.fp8q_trace_start(K * len(plan)) != 0:
         raise RuntimeError("fp8q_trace_start failed")
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -337,7 +353,7 @@ def kernel_table(traced, plan, K, pk):
     return out, total
 
 
-def cpu_baseline(w, tokens, grad_e4m3=False):
+def cpu_baseline(w, tokens, grad_e4m3=False, bf16=False):
     import oracle
     oracle.build()
     gf = oracle.E4M3 if grad_e4m3 else oracle.E5M2
@@ -353,7 +369,7 @@ def cpu_baseline(w, tokens, grad_e4m3=False):
         x = inp["x"][:tokens]
         dY = inp["dY"][:tokens] if w.backward else None
         t0 = time.perf_counter()
-        oracle.block(x, inp["g"], inp["W_gu"], inp["W_d"], dY=dY, nthreads=1, grad_fmt=gf)
+        oracle.block(x, inp["g"], inp["W_gu"], inp["W_d"], dY=dY, nthreads=1, grad_fmt=gf, bf16=bf16)
         dt = time.perf_counter() - t0
     sub = synth.Workload(w.name, tokens, w.d, w.f, w.x_kind, w.x_scale, w.outlier_frac, w.outlier_mult,
                          w.w_std, w.dy_std, w.qkv)
@@ -412,6 +428,8 @@ def main():
     if args.tokens:
         import dataclasses
         w = dataclasses.replace(w, T=args.tokens)
+    if args.bf16 and (w.qkv or args.recompute or args.grad_e4m3):
+        raise SystemExit("--bf16: MLP workloads only, without --recompute / --grad-e4m3")
     pk = peaks()
     fp8_peak = pk["bf16_sustained"] * FP8_PER_BF16
 
@@ -420,9 +438,9 @@ def main():
             return
         tokens = 2
         for _ in range(args.warmup):
-            cpu_baseline(w, tokens, args.grad_e4m3)
+            cpu_baseline(w, tokens, args.grad_e4m3, args.bf16)
         t0 = time.perf_counter()
-        res = [cpu_baseline(w, tokens, args.grad_e4m3) for _ in range(args.steps)]
+        res = [cpu_baseline(w, tokens, args.grad_e4m3, args.bf16) for _ in range(args.steps)]
         dt = time.perf_counter() - t0
         sub_flops = w.gemm_flops() * tokens / w.T
         value = sub_flops * args.steps / dt / 1e12
@@ -431,7 +449,8 @@ def main():
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic (seeded Philox, bf16)",
                 "config": {"workload": w.name, "T": w.T, "d": w.d, "f": w.f,
-                           "gradients": "e4m3" if args.grad_e4m3 else "e5m2"},
+                           "gradients": "e4m3" if args.grad_e4m3 else "e5m2",
+                           "precision": "bf16 baseline" if args.bf16 else "fp8"},
                 "cpu_baseline": {"kind": "oracle", "cores": 1, "value": value, "unit": "TFLOP/s",
                                  "sample": res[0]["sample"]},
                 "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -460,25 +479,30 @@ def main():
     if os.path.exists(tpath):
         with open(tpath) as fh:
             tj = json.load(fh)
-        if tj.get("workload") == w.name and tj.get("kernel_hash") == kernel_hash():
+        if tj.get("workload") == w.name and tj.get("kernel_hash") == kernel_hash() and not args.bf16:
             traffic = tj.get("bytes_per_launch")
+    peak = pk["bf16_sustained"] if args.bf16 else fp8_peak
+    peak_source = (f"{pk['source']} bf16 sustained {pk['bf16_sustained']}" if args.bf16 else
+                   f"{pk['source']} bf16 sustained {pk['bf16_sustained']} x nominal fp8/bf16 2")
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": r["K"],
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "fp8 (e4m3/e5m2 operands, fp32 accumulation)",
+        "vs_baseline": None,
+        "dtype": "bf16 (bf16 operands, fp32 accumulation)" if args.bf16 else "fp8 (e4m3/e5m2 operands, fp32 accumulation)",
         "data": "synthetic (seeded Philox, bf16 inputs)",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "f": w.f, "gemm_flops_per_step": w.gemm_flops(),
                    "backward": "recompute H and a8 from n8 with the retained scale" if args.recompute else "stored H and a8",
-                   "gradients": "e4m3" if args.grad_e4m3 else "e5m2",
+                   "gradients": "bf16" if args.bf16 else ("e4m3" if args.grad_e4m3 else "e5m2"),
+                   "precision": "bf16 baseline" if args.bf16 else "fp8",
                    "l2": "inputs larger than L2 (bf16 weights 407 MB per step), no flush",
                    "parallelism": "replicas" if world > 1 else "single"},
         "tokens_per_s": world * w.T / (ms_step * 1e-3),
         "pct_fp8_peak": round(100.0 * value / world / fp8_peak, 2),
         "roofline": {"kernel": "k_gemm_f8 (the six block GEMMs)", "bound": "tensor", "achieved": round(achieved, 1),
-                     "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
+                     "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "launches_per_step": g_launch // r["K"],
                      "share_of_step": round(g_ms / traced_total, 4),
-                     "peak_source": f"{pk['source']} bf16 sustained {pk['bf16_sustained']} x nominal fp8/bf16 2"},
+                     "peak_source": peak_source},
         "kernels": kernels,
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
@@ -487,7 +511,7 @@ def main():
     if r["e2e"]:
         line["e2e"] = r["e2e"]
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, args.cpu_sample_tokens, args.grad_e4m3)
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_sample_tokens, args.grad_e4m3, args.bf16)
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

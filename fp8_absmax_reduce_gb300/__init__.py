@@ -65,13 +65,16 @@ def _load() -> ctypes.CDLL:
     return L
 
 
+_MLP_PTRS = ("x", "g", "W_gu", "W_d", "y", "W_gu8", "W_d8", "n8", "rstd", "H", "a8", "scal",
+             "dY", "dX", "dW_gu", "dW_d", "dg", "dY8", "dH", "dH8", "dN")
+
+
 class FP8QMlp(ctypes.Structure):
     """Mirror of ``fp8q_mlp`` in include/fp8q.h."""
-    _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int64), ("f", ctypes.c_int64), ("eps", ctypes.c_float)] + [
-        (name, ctypes.c_void_p) for name in (
-            "x", "g", "W_gu", "W_d", "y", "W_gu8", "W_d8", "n8", "rstd", "H", "a8", "scal",
-            "dY", "dX", "dW_gu", "dW_d", "dg", "dY8", "dH", "dH8", "dN")
-    ] + [("recompute", ctypes.c_int), ("grad_e4m3", ctypes.c_int)]
+    _fields_ = ([("T", ctypes.c_int64), ("d", ctypes.c_int64), ("f", ctypes.c_int64), ("eps", ctypes.c_float)]
+                + [(name, ctypes.c_void_p) for name in _MLP_PTRS]
+                + [("recompute", ctypes.c_int), ("grad_e4m3", ctypes.c_int), ("bf16", ctypes.c_int),
+                   ("n16", ctypes.c_void_p), ("a16", ctypes.c_void_p)])
 
 
 class FP8QBlock(ctypes.Structure):
@@ -217,13 +220,13 @@ class MlpBuffers:
     W_gu: torch.Tensor
     W_d: torch.Tensor
     y: torch.Tensor
-    W_gu8: torch.Tensor
-    W_d8: torch.Tensor
-    n8: torch.Tensor
+    W_gu8: torch.Tensor | None
+    W_d8: torch.Tensor | None
+    n8: torch.Tensor | None
     rstd: torch.Tensor
     H: torch.Tensor
-    a8: torch.Tensor
-    scal: torch.Tensor
+    a8: torch.Tensor | None
+    scal: torch.Tensor | None
     dY: torch.Tensor | None = None
     dX: torch.Tensor | None = None
     dW_gu: torch.Tensor | None = None
@@ -236,17 +239,26 @@ class MlpBuffers:
     ws: torch.Tensor | None = None
     recompute: bool = False
     grad_e4m3: bool = False
+    bf16: bool = False
+    n16: torch.Tensor | None = None
+    a16: torch.Tensor | None = None
 
     @staticmethod
     def allocate(T: int, d: int, f: int, device="cuda", backward: bool = True, eps: float = 1e-6,
-                 keep_intermediates: bool = False) -> "MlpBuffers":
+                 keep_intermediates: bool = False, bf16: bool = False) -> "MlpBuffers":
+        """bf16=True: buffers of the BF16 baseline (n16, a16 instead of the FP8 codes and scales)."""
         e = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)
+        q8 = (lambda shape: None) if bf16 else (lambda shape: e(shape, torch.uint8))
         b = MlpBuffers(
             T=T, d=d, f=f, eps=eps,
             x=e((T, d), torch.bfloat16), g=e((d,), torch.bfloat16), W_gu=e((d, 2 * f), torch.bfloat16),
-            W_d=e((f, d), torch.bfloat16), y=e((T, d), torch.bfloat16), W_gu8=e((d, 2 * f), torch.uint8),
-            W_d8=e((f, d), torch.uint8), n8=e((T, d), torch.uint8), rstd=e((T,), torch.float32),
-            H=e((T, 2 * f), torch.bfloat16), a8=e((T, f), torch.uint8), scal=torch.zeros((6, 3), device=device))
+            W_d=e((f, d), torch.bfloat16), y=e((T, d), torch.bfloat16), W_gu8=q8((d, 2 * f)),
+            W_d8=q8((f, d)), n8=q8((T, d)), rstd=e((T,), torch.float32),
+            H=e((T, 2 * f), torch.bfloat16), a8=q8((T, f)),
+            scal=None if bf16 else torch.zeros((6, 3), device=device), bf16=bf16)
+        if bf16:
+            b.n16 = e((T, d), torch.bfloat16)
+            b.a16 = e((T, f), torch.bfloat16)
         if backward:
             b.dY = e((T, d), torch.bfloat16)
             b.dX = e((T, d), torch.bfloat16)
@@ -254,9 +266,9 @@ class MlpBuffers:
             b.dW_d = e((f, d), torch.float32)
             b.dg = e((d,), torch.float32)
             if keep_intermediates:
-                b.dY8 = e((T, d), torch.uint8)
+                b.dY8 = q8((T, d))
                 b.dH = e((T, 2 * f), torch.bfloat16)
-                b.dH8 = e((T, 2 * f), torch.uint8)
+                b.dH8 = q8((T, 2 * f))
                 b.dN = e((T, d), torch.float32)
         nb = lib.mlp_block_workspace_size(T, d, f, int(backward))
         b.ws = torch.empty(nb, dtype=torch.uint8, device=device)
@@ -264,8 +276,8 @@ class MlpBuffers:
 
     def struct(self) -> FP8QMlp:
         s = FP8QMlp(T=self.T, d=self.d, f=self.f, eps=self.eps, recompute=int(self.recompute),
-                    grad_e4m3=int(self.grad_e4m3))
-        for name, _ in FP8QMlp._fields_[4:-2]:
+                    grad_e4m3=int(self.grad_e4m3), bf16=int(self.bf16))
+        for name in _MLP_PTRS + ("n16", "a16"):
             t = getattr(self, name)
             setattr(s, name, None if t is None else t.data_ptr())
         return s

@@ -20,7 +20,7 @@ enum Kind {
   kKAbsmaxPartial = 0, kKQuantCast, kKRmsnormStats, kKRmsnormCast, kKSwigluAmax, kKSwigluCast, kKRmsnormBwd,
   kKGemmGateUp, kKGemmDown, kKGemmDownDgrad, kKGemmDownWgrad, kKGemmGateUpDgrad, kKGemmGateUpWgrad, kKGemm,
   kKGemmQkv, kKGemmOResidual, kKGemmODgrad, kKGemmOWgrad, kKGemmQkvDgrad, kKGemmQkvWgrad,
-  kKGemmGateUpRecompute,
+  kKGemmGateUpRecompute, kKRmsnormBf16,
   kKCount
 };
 const char* const kKindNames[kKCount] = {
@@ -28,7 +28,7 @@ const char* const kKindNames[kKCount] = {
     "rmsnorm_bwd", "gemm_gate_up_swiglu", "gemm_down_residual", "gemm_down_dgrad_swiglu_bwd",
     "gemm_down_wgrad", "gemm_gate_up_dgrad", "gemm_gate_up_wgrad", "gemm",
     "gemm_qkv", "gemm_o_residual", "gemm_o_dgrad", "gemm_o_wgrad", "gemm_qkv_dgrad", "gemm_qkv_wgrad",
-    "gemm_gate_up_recompute"};
+    "gemm_gate_up_recompute", "rmsnorm_bf16"};
 
 struct Trace {
   bool on = false;
@@ -169,6 +169,17 @@ int validate_mlp(const fp8q_mlp* m, bool backward) {
   if (!m) return FP8Q_ERR_INVALID_ARG;
   if (m->T < 1 || m->d < 16 || m->f < 16 || m->d % 16 || m->f % 16 || m->d > 8192) return FP8Q_ERR_INVALID_ARG;
   if (m->T > (int64_t)1 << 24 || m->f > (int64_t)1 << 20) return FP8Q_ERR_INVALID_ARG;
+  if (m->bf16) {
+    if (m->recompute || m->grad_e4m3) return FP8Q_ERR_UNSUPPORTED;
+    const void* must16[] = {m->x, m->g, m->W_gu, m->W_d, m->n16, m->rstd, m->H, m->a16};
+    for (const void* p : must16)
+      if (!al16(p)) return FP8Q_ERR_INVALID_ARG;
+    if (!backward) return al16(m->y) ? FP8Q_OK : FP8Q_ERR_INVALID_ARG;
+    const void* must16_b[] = {m->dY, m->dX, m->dW_gu, m->dW_d, m->dg};
+    for (const void* p : must16_b)
+      if (!al16(p)) return FP8Q_ERR_INVALID_ARG;
+    return ((m->dH && !al16(m->dH)) || (m->dN && !al16(m->dN))) ? FP8Q_ERR_INVALID_ARG : FP8Q_OK;
+  }
   const void* must[] = {m->x, m->g, m->W_gu, m->W_d, m->W_gu8, m->W_d8, m->n8, m->rstd, m->H, m->a8, m->scal};
   for (const void* p : must)
     if (!al16(p)) return FP8Q_ERR_INVALID_ARG;
@@ -182,9 +193,76 @@ int validate_mlp(const fp8q_mlp* m, bool backward) {
   return FP8Q_OK;
 }
 
+// A GEMM of the BF16 baseline: bf16 operands, alpha = 1.
+GemmProblem bf16_gemm(int a_mn, int b_mn, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                      const void* B, int64_t ldb, int64_t b_cols, int epi, int out_f32, void* C, int64_t ldc) {
+  GemmProblem g{};
+  g.op16 = 1;
+  g.a_mn = a_mn;
+  g.b_mn = b_mn;
+  g.M = (int)M;
+  g.N = (int)N;
+  g.K = (int)K;
+  g.A = static_cast<const uint8_t*>(A);
+  g.lda = lda;
+  g.B = static_cast<const uint8_t*>(B);
+  g.ldb = ldb;
+  g.b_cols = b_cols;
+  g.epi = epi;
+  g.out_f32 = out_f32;
+  g.C = C;
+  g.ldc = ldc;
+  return g;
+}
+
+// The BF16 baseline's forward: the FP8 sequence with every cast removed.
+int mlp_fwd_run_bf16(const fp8q_mlp* m, Ctx& c) {
+  const int64_t T = m->T, d = m->d, f = m->f;
+  int P = 0;
+  FP8Q_STEP(kKRmsnormBf16, launch_rmsnorm_bf16((const uint16_t*)m->x, (const uint16_t*)m->g, T, (int)d, m->eps, m->rstd,
+                                (uint16_t*)m->n16, c.L));
+  // G1: H = bf16(n16 @ W_gu), a16 = bf16(SwiGLU(H)) in the epilogue
+  GemmProblem g1 = bf16_gemm(0, 1, T, f, d, m->n16, d, m->W_gu, 2 * f, 2 * f, kEpiSwiglu, 0, m->H, 2 * f);
+  g1.a16 = (uint16_t*)m->a16;
+  FP8Q_STEP(kKGemmGateUp, launch_gemm(g1, &P, c.L));
+  // G2: y = bf16(x + a16 @ W_d)
+  GemmProblem g2 = bf16_gemm(0, 1, T, d, f, m->a16, f, m->W_d, d, d, kEpiResidual, 0, m->y, d);
+  g2.R = (const uint16_t*)m->x;
+  g2.ldr = d;
+  FP8Q_STEP(kKGemmDown, launch_gemm(g2, &P, c.L));
+  return FP8Q_OK;
+}
+
+// The BF16 baseline's backward (same layouts as the FP8 backward, no casts).
+int mlp_bwd_run_bf16(const fp8q_mlp* m, const MlpWs& w, Ctx& c) {
+  const int64_t T = m->T, d = m->d, f = m->f;
+  uint16_t* dH = m->dH ? (uint16_t*)m->dH : w.dH;
+  float* dN = m->dN ? m->dN : w.dN;
+  int P = 0;
+  // G3 (NT): dA = dY @ W_d^T, SwiGLU backward fused -> dH
+  GemmProblem g3 = bf16_gemm(0, 0, T, f, d, m->dY, d, m->W_d, d, f, kEpiSwigluBwd, 0, dH, 2 * f);
+  g3.R = (const uint16_t*)m->H;
+  g3.ldr = 2 * f;
+  FP8Q_STEP(kKGemmDownDgrad, launch_gemm(g3, &P, c.L));
+  // G4 (TN): dW_d = a16^T @ dY
+  FP8Q_STEP(kKGemmDownWgrad,
+            launch_gemm(bf16_gemm(1, 1, f, d, T, m->a16, f, m->dY, d, d, kEpiStore, 1, m->dW_d, d), &P, c.L));
+  // G5 (NT): dN = dH @ W_gu^T
+  FP8Q_STEP(kKGemmGateUpDgrad,
+            launch_gemm(bf16_gemm(0, 0, T, d, 2 * f, dH, 2 * f, m->W_gu, 2 * f, d, kEpiStore, 1, dN, d), &P, c.L));
+  // G6 (TN): dW_gu = n16^T @ dH
+  FP8Q_STEP(kKGemmGateUpWgrad, launch_gemm(bf16_gemm(1, 1, d, 2 * f, T, m->n16, d, dH, 2 * f, 2 * f, kEpiStore, 1,
+                                                     m->dW_gu, 2 * f),
+                                           &P, c.L));
+  FP8Q_STEP(kKRmsnormBwd, launch_rmsnorm_bwd(dN, (const uint16_t*)m->x, (const uint16_t*)m->dY, (const uint16_t*)m->g,
+                                             m->rstd, T, (int)d, (uint16_t*)m->dX, w.dg_part, m->dg, c.L));
+  return FP8Q_OK;
+}
+
 // The MLP block's kernel sequences, enqueued on c.L.stream (shared by
 // mlp_block_* and block_*).
 int mlp_fwd_run(const fp8q_mlp* m, const MlpWs& w, Ctx& c) {
+  if (m->bf16) return mlp_fwd_run_bf16(m, c);
   const int64_t T = m->T, d = m->d, f = m->f;
   float* s_wgu = m->scal + 0;
   float* s_wd = m->scal + 3;
@@ -251,6 +329,7 @@ int mlp_fwd_run(const fp8q_mlp* m, const MlpWs& w, Ctx& c) {
 }
 
 int mlp_bwd_run(const fp8q_mlp* m, const MlpWs& w, Ctx& c) {
+  if (m->bf16) return mlp_bwd_run_bf16(m, w, c);
   const int64_t T = m->T, d = m->d, f = m->f;
   const float* s_wgu = m->scal + 0;
   const float* s_wd = m->scal + 3;
@@ -417,6 +496,7 @@ size_t block_ws_layout(int64_t T, int64_t d, int64_t f, int64_t nq, int backward
 int validate_block(const fp8q_block* b, bool backward) {
   if (!b) return FP8Q_ERR_INVALID_ARG;
   const fp8q_mlp& m = b->mlp;
+  if (m.bf16) return FP8Q_ERR_UNSUPPORTED;
   if (m.T != b->T || m.d != b->d || m.f != b->f || m.x != b->h) return FP8Q_ERR_INVALID_ARG;
   if (b->n_qkv < 16 || b->n_qkv % 16 || b->n_qkv > (int64_t)1 << 20) return FP8Q_ERR_INVALID_ARG;
   int e = validate_mlp(&m, backward);

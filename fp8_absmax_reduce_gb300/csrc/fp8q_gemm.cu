@@ -22,6 +22,10 @@
 // without transpose copies): TMA boxes are 128 B wide along the contiguous
 // dimension with the 128-byte swizzle, and the UMMA shared-memory descriptors
 // declare the matching major-ness.
+// The same kernel with 16-bit operands (OP16: bf16, tcgen05.mma kind::f16,
+// K = 16 per instruction) is the BF16 baseline the FP8 path is compared with:
+// a stage still holds 128 bytes of K per row (64 bf16), so the ring, the
+// swizzle and the epilogues are unchanged; the scale factor alpha is 1.
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
 // FP8Q_STATUS_TIMEOUT, stops issuing work, drains what it issued, frees TMEM
 // and exits.
@@ -34,7 +38,7 @@ namespace fp8q {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;  // BK: bytes of K per stage
 constexpr int kATile = BM * BK;   // 16 KB
 constexpr int kBHalf = 128 * BK;  // 16 KB
 constexpr int kStage = kATile + 2 * kBHalf;
@@ -61,6 +65,7 @@ struct Args {
   const uint16_t* R;
   int64_t ldr;
   float* aux;  // kEpiSwiglu: the fp32 SwiGLU output a [M, N] (ld = N), or null
+  uint16_t* aux16;  // kEpiSwiglu: the bf16 SwiGLU output a [M, N] (ld = N), or null
   const float* qscale;  // kEpiSwiglu: with it, a is written as E4M3 codes fp8(fl32(a * *qscale)) instead
   uint32_t* amax_partial;
   unsigned* status;
@@ -198,8 +203,8 @@ __device__ __forceinline__ void load_h_chunk(const Args& p, int row, int col, in
 // The kernel
 // ---------------------------------------------------------------------------
 // Output maps: tmC (C, or the gate half of H / dH), tmC2 (the up half), tmAux
-// (the fp32 SwiGLU output a); unused ones are copies of tmC.
-template <int A_MN, int B_MN>
+// (the SwiGLU output a); unused ones are copies of tmC.
+template <int A_MN, int B_MN, int OP16>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_f8(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
@@ -253,12 +258,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sA = smem + stage * kStage;
           uint8_t* sB = sA + kATile;
           mbar_arrive_expect_tx(&full[stage], kStage);
-          const int k0 = kb * BK;
-          if (A_MN) tma_load_2d(sA, &tmA, &full[stage], m0, k0);
-          else tma_load_2d(sA, &tmA, &full[stage], k0, m0);
+          const int k0 = kb * (OP16 ? BK / 2 : BK);  // in elements
+          if (A_MN) {
+            if (OP16) {  // two 64-element-wide MN boxes of 64 K rows
+              tma_load_2d(sA, &tmA, &full[stage], m0, k0);
+              tma_load_2d(sA + kATile / 2, &tmA, &full[stage], m0 + 64, k0);
+            } else {
+              tma_load_2d(sA, &tmA, &full[stage], m0, k0);
+            }
+          } else {
+            tma_load_2d(sA, &tmA, &full[stage], k0, m0);
+          }
           if (B_MN) {
-            tma_load_2d(sB, &tmB, &full[stage], n0, k0);
-            tma_load_2d(sB + kBHalf, &tmB, &full[stage], n1, k0);
+            if (OP16) {
+              tma_load_2d(sB, &tmB, &full[stage], n0, k0);
+              tma_load_2d(sB + kBHalf / 2, &tmB, &full[stage], n0 + 64, k0);
+              tma_load_2d(sB + kBHalf, &tmB, &full[stage], n1, k0);
+              tma_load_2d(sB + kBHalf + kBHalf / 2, &tmB, &full[stage], n1 + 64, k0);
+            } else {
+              tma_load_2d(sB, &tmB, &full[stage], n0, k0);
+              tma_load_2d(sB + kBHalf, &tmB, &full[stage], n1, k0);
+            }
           } else {
             tma_load_2d(sB, &tmB, &full[stage], k0, n0);
             tma_load_2d(sB + kBHalf, &tmB, &full[stage], k0, n1);
@@ -298,10 +318,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sB = sA + kATile;
 #pragma unroll
           for (int kk = 0; kk < BK / 32; ++kk) {
-            // K-major: advance 32 bytes inside the 128-byte swizzle row; MN-major: 32 K-rows of 128 B.
-            const uint64_t ad = A_MN ? smem_desc_sw128(sA + kk * 4096, kBHalf, 1024) : smem_desc_sw128(sA + kk * 32, 16, 1024);
-            const uint64_t bd = B_MN ? smem_desc_sw128(sB + kk * 4096, kBHalf, 1024) : smem_desc_sw128(sB + kk * 32, 16, 1024);
-            umma_f8(d_tmem, ad, bd, p.idesc, (kb | kk) != 0 ? 1u : 0u);
+            // One MMA consumes 32 bytes of K (32 FP8 or 16 bf16 elements).  K-major: advance
+            // 32 bytes inside the 128-byte swizzle row.  MN-major: advance 32 (FP8) or 16 (bf16)
+            // K rows of 128 B; consecutive 128-byte-wide MN blocks lie one block (all K rows of
+            // the stage) apart.
+            constexpr uint32_t kMnStep = OP16 ? 2048 : 4096, kMnLbo = OP16 ? kBHalf / 2 : kBHalf;
+            const uint64_t ad = A_MN ? smem_desc_sw128(sA + kk * kMnStep, kMnLbo, 1024) : smem_desc_sw128(sA + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? smem_desc_sw128(sB + kk * kMnStep, kMnLbo, 1024) : smem_desc_sw128(sB + kk * 32, 16, 1024);
+            if (OP16) umma_bf16(d_tmem, ad, bd, p.idesc, (kb | kk) != 0 ? 1u : 0u);
+            else umma_f8(d_tmem, ad, bd, p.idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           umma_commit(&empty[stage]);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -327,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t amax = 0;
-    const float alpha = __fmul_rn(*p.sinvA, *p.sinvB);
+    const float alpha = p.sinvA ? __fmul_rn(*p.sinvA, *p.sinvB) : 1.0f;  // 1: unscaled (bf16) operands
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
       int mb, nb;
       tile_coords(tile, p, mb, nb);
@@ -370,7 +395,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_store_2d(&tmC2, buf + 2048, col, row0);
               bulk_commit();
             }
-            if (p.aux) {
+            if (p.aux16) {
+              staging_acquire(lane);
+              stage_bf16(buf, lane, a);
+              staging_publish();
+              if (lane == 0) {
+                tma_store_2d(&tmAux, buf, col, row0);
+                bulk_commit();
+              }
+            } else if (p.aux) {
               staging_acquire(lane);
               stage_f32(buf, lane, a);
               staging_publish();
@@ -515,15 +548,19 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// 2D uint8 tensor [outer, inner] with row stride `ld` bytes, 128 x 128 byte boxes, 128-byte swizzle.
-bool make_tmap(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int64_t ld) {
+// 2D operand [outer, inner] with row stride `ld` elements, 128-byte-swizzled boxes 128 bytes
+// wide: FP8 (es = 1) 128 x 128 elements; bf16 (es = 2) 64 elements x `box_outer` rows
+// (128 for a K-major operand, 64 = the K rows of one stage for an MN-major one).
+bool make_tmap(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int64_t ld, int es = 1,
+               int box_outer = 128) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
-  const cuuint64_t strides[1] = {(cuuint64_t)ld};
-  const cuuint32_t box[2] = {128, 128};
+  const cuuint64_t strides[1] = {(cuuint64_t)(ld * es)};
+  const cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+  return enc(m, es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+             const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -551,27 +588,27 @@ bool make_out_tmap(CUtensorMap* m, const void* base, int64_t cols, int64_t rows,
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Instruction descriptor for kind::f8f6f4: fp32 accumulator, A/B formats
-// (E4M3 = 0, E5M2 = 1), operand major-ness (bit 15 A, bit 16 B; 1 = MN-major),
-// N >> 3 at bit 17, M >> 4 at bit 24.
+// Instruction descriptor for kind::f8f6f4 and kind::f16: fp32 accumulator, A/B
+// formats (f8f6f4: E4M3 = 0, E5M2 = 1; f16: bf16 = 1), operand major-ness
+// (bit 15 A, bit 16 B; 1 = MN-major), N >> 3 at bit 17, M >> 4 at bit 24.
 uint32_t make_idesc(int fmtA, int fmtB, int a_mn, int b_mn) {
   return (1u << 4) | ((uint32_t)fmtA << 7) | ((uint32_t)fmtB << 10) | ((uint32_t)a_mn << 15) |
          ((uint32_t)b_mn << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
 
-template <int A_MN, int B_MN>
+template <int A_MN, int B_MN, int OP16>
 cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tc2,
                      const CUtensorMap& taux, const Args& a, int grid, cudaStream_t s) {
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_f8<A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_f8<A_MN, B_MN, OP16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  k_gemm_f8<A_MN, B_MN><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, tc, tc2, taux, a);
+  k_gemm_f8<A_MN, B_MN, OP16><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, tc, tc2, taux, a);
   return cudaGetLastError();
 }
 
@@ -590,11 +627,12 @@ cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L) {
   a.ldc = g.ldc;
   a.R = g.R;
   a.ldr = g.ldr;
-  a.aux = g.aux;
-  a.qscale = g.aux ? nullptr : g.qscale;
+  a.aux = g.op16 ? nullptr : g.aux;
+  a.aux16 = g.op16 ? g.a16 : nullptr;
+  a.qscale = (g.aux || g.op16) ? nullptr : g.qscale;
   a.amax_partial = g.amax_partial;
   a.status = L.status;
-  a.idesc = make_idesc(g.fmtA, g.fmtB, g.a_mn, g.b_mn);
+  a.idesc = g.op16 ? make_idesc(1, 1, g.a_mn, g.b_mn) : make_idesc(g.fmtA, g.fmtB, g.a_mn, g.b_mn);
   a.m_tiles = (g.M + BM - 1) / BM;
   if (g.epi == kEpiSwiglu) {
     a.n_tiles = (g.N + 127) / 128;  // 128 gate + the matching 128 up columns per tile
@@ -605,19 +643,24 @@ cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L) {
     a.b_step = BN;
     a.b_half1 = 128;
   }
-  a.k_blocks = (g.K + BK - 1) / BK;
+  const int bk = g.op16 ? BK / 2 : BK;  // K elements per stage
+  a.k_blocks = (g.K + bk - 1) / bk;
   a.num_tiles = a.m_tiles * a.n_tiles;
 
   CUtensorMap ta, tb, tc, tc2, taux;
-  const bool ok_a = g.a_mn ? make_tmap(&ta, g.A, g.M, g.K, g.lda) : make_tmap(&ta, g.A, g.K, g.M, g.lda);
-  const bool ok_b = g.b_mn ? make_tmap(&tb, g.B, g.b_cols, g.K, g.ldb) : make_tmap(&tb, g.B, g.K, g.b_cols, g.ldb);
+  const int es = g.op16 ? 2 : 1;
+  const int mn_rows = g.op16 ? 64 : 128;  // K rows of an MN-major box
+  const bool ok_a = g.a_mn ? make_tmap(&ta, g.A, g.M, g.K, g.lda, es, mn_rows) : make_tmap(&ta, g.A, g.K, g.M, g.lda, es);
+  const bool ok_b = g.b_mn ? make_tmap(&tb, g.B, g.b_cols, g.K, g.ldb, es, mn_rows)
+                           : make_tmap(&tb, g.B, g.K, g.b_cols, g.ldb, es);
   bool ok_c;
   if (g.epi == kEpiSwiglu || g.epi == kEpiSwigluBwd) {
     // gate half [M, f] and up half [M, f] of the [M, 2f] output, each clipped at f
     const uint16_t* c = static_cast<const uint16_t*>(g.C);
     ok_c = make_out_tmap(&tc, c, g.N, g.M, g.ldc, kOutBf16) && make_out_tmap(&tc2, c + g.N, g.N, g.M, g.ldc, kOutBf16);
     taux = tc;
-    if (ok_c && g.aux) ok_c = make_out_tmap(&taux, g.aux, g.N, g.M, g.N, kOutF32);
+    if (ok_c && g.op16 && g.a16) ok_c = make_out_tmap(&taux, g.a16, g.N, g.M, g.N, kOutBf16);
+    else if (ok_c && g.aux) ok_c = make_out_tmap(&taux, g.aux, g.N, g.M, g.N, kOutF32);
     else if (ok_c && g.qscale && g.q8) ok_c = make_out_tmap(&taux, g.q8, g.N, g.M, g.N, kOutU8);
   } else {
     ok_c = make_out_tmap(&tc, g.C, g.N, g.M, g.ldc, g.out_f32 ? kOutF32 : kOutBf16);
@@ -628,10 +671,17 @@ cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L) {
   const int grid = a.num_tiles < L.num_sms ? a.num_tiles : L.num_sms;
   *P = grid;
   cudaError_t e;
-  if (g.a_mn == 0 && g.b_mn == 1) e = launch_t<0, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
-  else if (g.a_mn == 0 && g.b_mn == 0) e = launch_t<0, 0>(ta, tb, tc, tc2, taux, a, grid, L.stream);
-  else if (g.a_mn == 1 && g.b_mn == 1) e = launch_t<1, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
-  else e = launch_t<1, 0>(ta, tb, tc, tc2, taux, a, grid, L.stream);
+  if (g.op16) {  // the three layouts of the block (NN, NT, TN)
+    if (g.a_mn == 0 && g.b_mn == 1) e = launch_t<0, 1, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
+    else if (g.a_mn == 0 && g.b_mn == 0) e = launch_t<0, 0, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
+    else if (g.a_mn == 1 && g.b_mn == 1) e = launch_t<1, 1, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
+    else return cudaErrorInvalidValue;
+  } else {
+    if (g.a_mn == 0 && g.b_mn == 1) e = launch_t<0, 1, 0>(ta, tb, tc, tc2, taux, a, grid, L.stream);
+    else if (g.a_mn == 0 && g.b_mn == 0) e = launch_t<0, 0, 0>(ta, tb, tc, tc2, taux, a, grid, L.stream);
+    else if (g.a_mn == 1 && g.b_mn == 1) e = launch_t<1, 1, 0>(ta, tb, tc, tc2, taux, a, grid, L.stream);
+    else e = launch_t<1, 0, 0>(ta, tb, tc, tc2, taux, a, grid, L.stream);
+  }
   if (L.launches) ++*L.launches;
   return e;
 }

@@ -33,6 +33,9 @@ cudaError_t launch_quant_cast(const void* x, int dtype, int64_t n, int fmt, cons
 // RMSNorm: pass 1 (rstd + absmax partials), pass 2 (cast to E4M3).
 cudaError_t launch_rmsnorm_stats(const uint16_t* x, const uint16_t* g, int64_t T, int d, float eps, float* rstd,
                                  uint32_t* partial, int* P, const Launch& L);
+// BF16 baseline: one pass, rstd and n = bf16((x rstd) g) (no absmax, no cast).
+cudaError_t launch_rmsnorm_bf16(const uint16_t* x, const uint16_t* g, int64_t T, int d, float eps, float* rstd,
+                                uint16_t* n16, const Launch& L);
 cudaError_t launch_rmsnorm_cast(const uint16_t* x, const uint16_t* g, const float* rstd, int64_t T, int d,
                                 const uint32_t* partial, int P, uint8_t* q, float* scal, const Launch& L);
 
@@ -74,6 +77,8 @@ struct GemmProblem {
   const float* qscale;             // kEpiSwiglu without aux: scale of a; a is written as E4M3 codes to q8
   uint8_t* q8;                     //   [M, N] E4M3
   uint32_t* amax_partial;          // per-CTA partials for the two SwiGLU epilogues
+  int op16;                        // 1: bf16 operands (lda/ldb in elements), no scales (alpha = 1)
+  uint16_t* a16;                   // op16 with kEpiSwiglu: bf16 SwiGLU output a [M, N]
 };
 // Launches the persistent tcgen05 GEMM; *P receives the number of partials written.
 cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L);

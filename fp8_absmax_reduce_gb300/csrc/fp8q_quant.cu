@@ -159,10 +159,14 @@ __global__ void __launch_bounds__(kThreads) k_quant_cast(const uint8_t* __restri
 // terms, which adds exact zeros only): an 8-leaf tree per lane, a butterfly
 // across lanes (each level adds adjacent subtrees), then a tree over the 32
 // chunk sums.
+// OUT16 (the BF16 baseline): instead of the absmax partials, the same pass
+// writes n = bf16((x rstd) g) -- there is no scale to wait for.
+template <bool OUT16>
 __global__ void __launch_bounds__(kThreads) k_rmsnorm_stats(const uint16_t* __restrict__ x,
                                                             const uint16_t* __restrict__ g, int64_t T, int d,
                                                             float eps, float* __restrict__ rstd,
-                                                            uint32_t* __restrict__ partial) {
+                                                            uint32_t* __restrict__ partial,
+                                                            uint16_t* __restrict__ n16) {
   __shared__ uint32_t red[32];
   const int lane = threadIdx.x & 31;
   const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -201,18 +205,34 @@ __global__ void __launch_bounds__(kThreads) k_rmsnorm_stats(const uint16_t* __re
       for (int i = 0; i < 32; i += 2 * w) cs[i] = __fadd_rn(cs[i], cs[i + w]);
     const float rs = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(cs[0], (float)d), eps)));
     if (lane == 0) rstd[row] = rs;
-    for (int j0 = lane * 8; j0 < d; j0 += 256) {
-      const uint4 w = ld_v4(xr + j0), gw = ld_v4(g + j0);
-      const uint32_t xw[4] = {w.x, w.y, w.z, w.w}, gg[4] = {gw.x, gw.y, gw.z, gw.w};
+    if (OUT16) {
+      // the row is re-read from L1 (holding it in registers across the sums spills)
+      for (int j0 = lane * 8; j0 < d; j0 += 256) {
+        const uint4 xv = ld_v4(xr + j0), gw = ld_v4(g + j0);
+        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, gg[4] = {gw.x, gw.y, gw.z, gw.w};
+        uint32_t o[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        m = max(m, abs_bits(__fmul_rn(__fmul_rn(bf16_lo(xw[k]), rs), bf16_lo(gg[k]))));
-        m = max(m, abs_bits(__fmul_rn(__fmul_rn(bf16_hi(xw[k]), rs), bf16_hi(gg[k]))));
+        for (int k = 0; k < 4; ++k)
+          o[k] = pack_bf16x2(__fmul_rn(__fmul_rn(bf16_lo(xw[k]), rs), bf16_lo(gg[k])),
+                             __fmul_rn(__fmul_rn(bf16_hi(xw[k]), rs), bf16_hi(gg[k])));
+        st_v4(n16 + row * d + j0, make_uint4(o[0], o[1], o[2], o[3]));
+      }
+    } else {
+      for (int j0 = lane * 8; j0 < d; j0 += 256) {
+        const uint4 w = ld_v4(xr + j0), gw = ld_v4(g + j0);
+        const uint32_t xw[4] = {w.x, w.y, w.z, w.w}, gg[4] = {gw.x, gw.y, gw.z, gw.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          m = max(m, abs_bits(__fmul_rn(__fmul_rn(bf16_lo(xw[k]), rs), bf16_lo(gg[k]))));
+          m = max(m, abs_bits(__fmul_rn(__fmul_rn(bf16_hi(xw[k]), rs), bf16_hi(gg[k]))));
+        }
       }
     }
   }
-  m = block_max_u32(m, red);
-  if (threadIdx.x == 0) partial[blockIdx.x] = m;
+  if (!OUT16) {
+    m = block_max_u32(m, red);
+    if (threadIdx.x == 0) partial[blockIdx.x] = m;
+  }
 }
 
 __global__ void __launch_bounds__(kThreads) k_rmsnorm_cast(const uint16_t* __restrict__ x,
@@ -498,7 +518,17 @@ cudaError_t launch_rmsnorm_stats(const uint16_t* x, const uint16_t* g, int64_t T
   int64_t blocks = (T + warps_per_block - 1) / warps_per_block;
   const int grid = (int)(blocks < kMaxPartials ? blocks : kMaxPartials);
   *P = grid;
-  k_rmsnorm_stats<<<grid, kThreads, 0, L.stream>>>(x, g, T, d, eps, rstd, partial);
+  k_rmsnorm_stats<false><<<grid, kThreads, 0, L.stream>>>(x, g, T, d, eps, rstd, partial, nullptr);
+  return post_launch(L);
+}
+
+cudaError_t launch_rmsnorm_bf16(const uint16_t* x, const uint16_t* g, int64_t T, int d, float eps, float* rstd,
+                                uint16_t* n16, const Launch& L) {
+  const int warps_per_block = kThreads / 32;
+  const int64_t blocks = (T + warps_per_block - 1) / warps_per_block;
+  const int64_t cap = (int64_t)L.num_sms * 16;
+  const int grid = (int)(blocks < cap ? blocks : cap);
+  k_rmsnorm_stats<true><<<grid, kThreads, 0, L.stream>>>(x, g, T, d, eps, rstd, nullptr, n16);
   return post_launch(L);
 }
 

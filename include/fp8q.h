@@ -210,6 +210,18 @@ typedef struct fp8q_mlp {
    * dh and dQKV) is E4M3 instead of E5M2 -- LLMQ §5 Figure 2's recipe with E4M3
    * forward and backward.  Zero (default): E5M2 gradients. */
   int grad_e4m3;
+  /* Nonzero: the BF16 baseline the FP8 path is measured against (LLMQ §4 and
+   * §5 compare FP8 training with BF16 training).  The same block with no
+   * quantization: the GEMMs (tcgen05 kind::f16) read bf16 operands -- W_gu,
+   * W_d, n16, a16, dY and dH -- with no scale factors; n16 = bf16((x rstd) g),
+   * H = bf16(n16 @ W_gu), a16 = bf16(SwiGLU(H)), y = bf16(x + a16 @ W_d) and
+   * the backward as above with every q() the identity.  W_gu8, W_d8, n8, a8,
+   * dY8, dH8 and scal are neither read nor written (may be NULL); n16 and a16
+   * are required.  Not combinable with recompute or grad_e4m3 (returns
+   * FP8Q_ERR_UNSUPPORTED); fp8q_block rejects it too. */
+  int bf16;
+  void* n16;        /* [T,d]  bf16 normalized input (bf16 != 0) */
+  void* a16;        /* [T,f]  bf16 SwiGLU output (bf16 != 0) */
 } fp8q_mlp;
 
 /* backward != 0 sizes the workspace for mlp_block_bwd (which also suffices for mlp_block_fwd). */

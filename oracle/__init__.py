@@ -71,6 +71,7 @@ class _BlockIO(ctypes.Structure):
         ("dX", ctypes.c_void_p), ("dWgu", ctypes.c_void_p), ("dWd", ctypes.c_void_p),
         ("dg", ctypes.c_void_p), ("dN", ctypes.c_void_p), ("dH", ctypes.c_void_p),
         ("dY8", ctypes.c_void_p), ("dH8", ctypes.c_void_p), ("scal_bwd", ctypes.c_void_p),
+        ("bf16", ctypes.c_int), ("n16", ctypes.c_void_p), ("a16", ctypes.c_void_p),
     ]
 
 
@@ -247,7 +248,7 @@ def _as_f64(a, exact):
 
 
 def block(x, g, Wgu, Wd, dY=None, eps: float = 1e-6, exact: bool = False, nthreads: int = 1,
-          grad_fmt: int = E5M2):
+          grad_fmt: int = E5M2, bf16: bool = False):
     """MLP block forward (and backward when dY is given).
 
     Quantized mode (exact=False): x, g, Wgu, Wd, dY are bf16 bit patterns
@@ -257,7 +258,13 @@ def block(x, g, Wgu, Wd, dY=None, eps: float = 1e-6, exact: bool = False, nthrea
 
     Exact mode (exact=True): float64 inputs, no quantization and no rounding;
     the backward is then the exact gradient of the forward.
+
+    BF16 baseline (bf16=True, bf16 inputs): no quantization; n and a are stored
+    as bf16 (returned as "n16", "a16") and every GEMM multiplies the bf16
+    operands unscaled; the storage points are those of the FP8 block.
     """
+    if bf16 and exact:
+        raise ValueError("bf16 and exact are separate modes")
     x64, g64, Wgu64, Wd64 = (_as_f64(a, exact) for a in (x, g, Wgu, Wd))
     T, d = x64.shape
     f = Wd64.shape[0]
@@ -269,9 +276,13 @@ def block(x, g, Wgu, Wd, dY=None, eps: float = 1e-6, exact: bool = False, nthrea
         "n8": np.empty((T, d), np.uint8), "a8": np.empty((T, f), np.uint8),
         "scal_fwd": np.zeros((4, 3), np.float32),
     }
-    io = _BlockIO(T=T, d=d, f=f, eps=eps, exact=int(exact), nthreads=int(nthreads), grad_fmt=int(grad_fmt))
+    io = _BlockIO(T=T, d=d, f=f, eps=eps, exact=int(exact), nthreads=int(nthreads), grad_fmt=int(grad_fmt),
+                  bf16=int(bf16))
     keep = [x64, g64, Wgu64, Wd64]
     io.x, io.g, io.Wgu, io.Wd = (a.ctypes.data for a in keep)
+    if bf16:
+        out.update({"n16": np.empty((T, d)), "a16": np.empty((T, f))})
+        io.n16, io.a16 = out["n16"].ctypes.data, out["a16"].ctypes.data
     for k in ("y", "H", "rstd", "Wgu8", "Wd8", "n8", "a8", "scal_fwd"):
         setattr(io, k, out[k].ctypes.data)
     if dY is None:

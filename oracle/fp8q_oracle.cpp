@@ -362,12 +362,29 @@ struct BlockIO {
   double* dX; double* dWgu; double* dWd; double* dg; double* dN; double* dH;
   uint8_t* dY8; uint8_t* dH8;
   float* scal_bwd;   // 2 x (amax, scale, scale_inv): dY, dH
+  // BF16 baseline (LLMQ §4/§5 measure FP8 training against BF16 training):
+  // every operand the FP8 block casts is instead stored as bf16, scale 1
+  int bf16;
+  double* n16;       // [T,d] the stored bf16 n (bf16 mode)
+  double* a16;       // [T,f] the stored bf16 a (bf16 mode)
 };
 
 void put_scal(float* dst, const Scal& s) { dst[0] = s.amax; dst[1] = s.scale; dst[2] = s.scale_inv; }
 
 template <class T> void put(T* dst, const std::vector<T>& v) {
   if (dst) std::copy(v.begin(), v.end(), dst);
+}
+
+// An operand of the block's GEMMs: in the FP8 block the per-tensor absmax
+// quantization; in the BF16 baseline one round-to-nearest-even to bf16 with
+// scale 1 (a no-op for tensors that already are bf16: weights, dY, dH).
+QTensor operand(const std::vector<double>& v, int fmt, const BlockIO& io) {
+  if (!io.bf16) return quantize(v, fmt, io.exact != 0);
+  QTensor q;
+  q.s = {abs_max(v), 1.0f, 1.0f};
+  q.deq.resize(v.size());
+  for (size_t i = 0; i < v.size(); ++i) q.deq[i] = to_bf16(v[i]);
+  return q;
 }
 
 struct FwdState {
@@ -384,17 +401,17 @@ FwdState block_forward(const BlockIO& io) {
   std::vector<double> x(io.x, io.x + T * d), g(io.g, io.g + d);
   std::vector<double> Wgu(io.Wgu, io.Wgu + d * 2 * f), Wd(io.Wd, io.Wd + f * d);
 
-  S.Wgu = quantize(Wgu, FMT_E4M3, ex);
-  S.Wd = quantize(Wd, FMT_E4M3, ex);
+  S.Wgu = operand(Wgu, FMT_E4M3, io);
+  S.Wd = operand(Wd, FMT_E4M3, io);
   rmsnorm_fwd(x, g, T, d, io.eps, ex, S.nval, S.rstd);
-  S.n = quantize(S.nval, FMT_E4M3, ex);
+  S.n = operand(S.nval, FMT_E4M3, io);
 
   const double alpha1 = ex ? 1.0 : (double)(S.n.s.scale_inv * S.Wgu.s.scale_inv);
   std::vector<double> acc1 = matmul(S.n.deq, S.Wgu.deq, T, 2 * f, d, io.nthreads);
   S.H.resize(acc1.size());
   for (size_t i = 0; i < acc1.size(); ++i) S.H[i] = ex ? acc1[i] : to_bf16(alpha1 * acc1[i]);
 
-  S.a = quantize(swiglu_fwd(S.H, T, f, ex), FMT_E4M3, ex);
+  S.a = operand(swiglu_fwd(S.H, T, f, ex), FMT_E4M3, io);
 
   const double alpha2 = ex ? 1.0 : (double)(S.a.s.scale_inv * S.Wd.s.scale_inv);
   std::vector<double> acc2 = matmul(S.a.deq, S.Wd.deq, T, d, f, io.nthreads);
@@ -415,6 +432,7 @@ void write_forward(const BlockIO& io, const FwdState& S) {
     put(io.Wgu8, S.Wgu.code); put(io.Wd8, S.Wd.code);
     put(io.n8, S.n.code); put(io.a8, S.a.code);
   }
+  if (io.bf16) { put(io.n16, S.n.deq); put(io.a16, S.a.deq); }
   if (io.scal_fwd) {
     put_scal(io.scal_fwd + 0, S.Wgu.s); put_scal(io.scal_fwd + 3, S.Wd.s);
     put_scal(io.scal_fwd + 6, S.n.s); put_scal(io.scal_fwd + 9, S.a.s);
@@ -428,7 +446,7 @@ int block_backward(const BlockIO& io, const FwdState& S) {
   std::vector<double> x(io.x, io.x + T * d), g(io.g, io.g + d), dY(io.dY, io.dY + T * d);
 
   const int gf = io.grad_fmt;
-  QTensor dY8 = quantize(dY, gf, ex);
+  QTensor dY8 = operand(dY, gf, io);
 
   // dA = alpha3 * dY8 @ Wd8^T   ([T,d] x [d,f])
   const double alpha3 = ex ? 1.0 : (double)(dY8.s.scale_inv * S.Wd.s.scale_inv);
@@ -447,7 +465,7 @@ int block_backward(const BlockIO& io, const FwdState& S) {
       dH[t * 2 * f + j] = ex ? dg_ : to_bf16(dg_);
       dH[t * 2 * f + f + j] = ex ? du_ : to_bf16(du_);
     }
-  QTensor dH8 = quantize(dH, gf, ex);
+  QTensor dH8 = operand(dH, gf, io);
 
   auto out32 = [&](double v) { return ex ? v : (double)(float)v; };
 

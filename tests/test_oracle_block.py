@@ -213,3 +213,68 @@ def test_e4m3_gradient_recipe_wiring():
     for k in ("dX", "dWgu", "dWd"):   # both recipes approximate the same gradients
         rel = np.linalg.norm(out[k] - e5[k]) / np.linalg.norm(e5[k])
         assert 0 < rel < 0.2, (k, rel)
+
+
+def _half_bf16_ulp(v):
+    """Half a bf16 ulp of |v| (normal range): 2^(floor(log2|v|) - 8)."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.ldexp(1.0, (e - 8).astype(int))
+
+
+def _is_bf16(v):
+    f32 = np.asarray(v, dtype=np.float32)
+    return np.array_equal(f32.astype(np.float64), np.asarray(v)) and not np.any(f32.view(np.uint32) & 0xFFFF)
+
+
+def test_bf16_baseline_wiring_and_storage_points():
+    """BF16 baseline (LLMQ §4/§5 compare FP8 with BF16 training): each stored tensor is bf16 and
+    within half a bf16 ulp (plus fp32 arithmetic slack) of the fp64 closed form of its inputs;
+    the fp32 GEMM outputs equal numpy's fp64 product of the stored bf16 operands rounded once to
+    fp32 (bf16 x bf16 products are exact in fp64 and these sums stay exact)."""
+    T, d, f = 32, 64, 48
+    inp = small_inputs(T, d, f)
+    out = oracle.block(inp["x"], inp["g"], inp["W_gu"], inp["W_d"], dY=inp["dY"], bf16=True)
+    x, g, Wgu, Wd, dY = (oracle.bf16_to_f64(inp[k]) for k in ("x", "g", "W_gu", "W_d", "dY"))
+    n16, a16, H, dH = out["n16"], out["a16"], out["H"], out["dH"]
+    for k in ("n16", "a16", "H", "y", "dH", "dX"):
+        assert _is_bf16(out[k]), k
+    # RMSNorm closed form
+    n_ref = x / np.sqrt((x * x).mean(axis=1, keepdims=True) + 1e-6) * g
+    assert np.all(np.abs(n16 - n_ref) <= _half_bf16_ulp(n_ref) * (1 + 2.0 ** -6)), "n16"
+    # H = bf16(n16 @ W_gu); a = bf16(silu(gate) * up); y = bf16(x + a16 @ W_d)
+    H_ref = n16 @ Wgu
+    assert np.all(np.abs(H - H_ref) <= _half_bf16_ulp(H_ref) * (1 + 2.0 ** -20)), "H"
+    hg, hu = H[:, :f], H[:, f:]
+    a_ref = hg / (1 + np.exp(-hg)) * hu
+    assert np.all(np.abs(a16 - a_ref) <= _half_bf16_ulp(a_ref) * (1 + 2.0 ** -6)), "a16"
+    y_ref = x + a16 @ Wd
+    assert np.all(np.abs(out["y"] - y_ref) <= _half_bf16_ulp(y_ref) * (1 + 2.0 ** -20)), "y"
+    # backward: unscaled products of the stored bf16 operands, rounded once to fp32
+    f32 = lambda v: v.astype(np.float32).astype(np.float64)  # noqa: E731
+    np.testing.assert_array_equal(out["dWd"], f32(a16.T @ dY))
+    np.testing.assert_array_equal(out["dN"], f32(dH @ Wgu.T))
+    np.testing.assert_array_equal(out["dWgu"], f32(n16.T @ dH))
+    dA = dY @ Wd.T
+    s = 1 / (1 + np.exp(-hg))
+    dg_ref, du_ref = dA * hu * s * (1 + hg * (1 - s)), dA * hg * s
+    assert np.all(np.abs(dH[:, :f] - dg_ref) <= _half_bf16_ulp(dg_ref) * (1 + 2.0 ** -20) + 1e-300)
+    assert np.all(np.abs(dH[:, f:] - du_ref) <= _half_bf16_ulp(du_ref) * (1 + 2.0 ** -20) + 1e-300)
+
+
+def test_bf16_baseline_accuracy_against_exact():
+    """The BF16 block tracks the exact block (itself pinned by finite differences) to the bf16
+    storage error -- a few 2^-9 relative -- and far closer than the FP8 block does."""
+    T, d, f = 32, 64, 48
+    inp = small_inputs(T, d, f)
+    args = [inp[k] for k in ("x", "g", "W_gu", "W_d")]
+    b = oracle.block(*args, dY=inp["dY"], bf16=True)
+    q = oracle.block(*args, dY=inp["dY"])
+    e = oracle.block(*(oracle.bf16_to_f64(a) for a in args), dY=oracle.bf16_to_f64(inp["dY"]), exact=True)
+    for k in ("H", "y", "dX", "dWgu", "dWd", "dg", "dN"):
+        rb = np.linalg.norm(b[k] - e[k]) / np.linalg.norm(e[k])
+        rq = np.linalg.norm(q[k] - e[k]) / np.linalg.norm(e[k])
+        assert rb < 8 * 2.0 ** -9, (k, rb)
+        assert rb <= rq, (k, rb, rq)
+        if k not in ("y", "dX"):  # y, dX are dominated by the exact residual terms x, dY
+            assert rb < rq / 5, (k, rb, rq)
