@@ -140,7 +140,6 @@ int check_ws(const void* ws, size_t ws_bytes, size_t need) {
 struct MlpWs {
   uint32_t* part_q;    // quantizer partials
   uint32_t* part_g;    // GEMM epilogue partials
-  float* a_f32;        // fp32 SwiGLU output of the gate/up GEMM epilogue [T, f]
   uint8_t* dY8;
   uint16_t* dH;
   uint8_t* dH8;
@@ -153,7 +152,6 @@ size_t mlp_ws_layout(int64_t T, int64_t d, int64_t f, int backward, uint8_t* bas
   MlpWs tmp{};
   tmp.part_q = (uint32_t*)c.take(kPartialBytes);
   tmp.part_g = (uint32_t*)c.take(kPartialBytes);
-  tmp.a_f32 = (float*)c.take((size_t)(T * f) * 4);
   if (backward) {
     tmp.dY8 = (uint8_t*)c.take((size_t)(T * d));
     tmp.dH = (uint16_t*)c.take((size_t)(T * 2 * f) * 2);
@@ -279,7 +277,7 @@ int mlp_fwd_run(const fp8q_mlp* m, const MlpWs& w, Ctx& c) {
                                 w.part_q, &P, c.L));
   FP8Q_STEP(kKRmsnormCast, launch_rmsnorm_cast((const uint16_t*)m->x, (const uint16_t*)m->g, m->rstd, T, (int)d, w.part_q, P,
                                m->n8, s_n, c.L));
-  // G1: H = bf16(alpha n8 @ W_gu8) with the SwiGLU absmax fused in the epilogue
+  // G1: H = bf16(alpha n8 @ W_gu8) with the absmax of a = SwiGLU(H) fused in the epilogue
   GemmProblem g1{};
   g1.a_mn = 0;
   g1.b_mn = 1;
@@ -298,11 +296,11 @@ int mlp_fwd_run(const fp8q_mlp* m, const MlpWs& w, Ctx& c) {
   g1.epi = kEpiSwiglu;
   g1.C = m->H;
   g1.ldc = 2 * f;
-  g1.aux = w.a_f32;
   g1.amax_partial = w.part_g;
   FP8Q_STEP(kKGemmGateUp, launch_gemm(g1, &P, c.L));
-  // a8 = q(a) with a = SwiGLU(H) as the epilogue computed it, scale from its partials
-  FP8Q_STEP(kKQuantCast, launch_quant_cast(w.a_f32, 1, T * f, 0, w.part_g, P, m->a8, s_a, c.L));
+  // a8 = q(a): a recomputed from the stored H by the epilogue's own SwiGLU (reading H costs the
+  // same bytes as reading an fp32 copy of a would), scale from the epilogue's partials
+  FP8Q_STEP(kKSwigluCast, launch_swiglu_cast((const uint16_t*)m->H, T, (int)f, 0, w.part_g, P, m->a8, s_a, c.L, true));
   // G2: y = bf16(x + alpha a8 @ W_d8)
   GemmProblem g2{};
   g2.a_mn = 0;

@@ -64,7 +64,6 @@ struct Args {
   int64_t ldc;
   const uint16_t* R;
   int64_t ldr;
-  float* aux;  // kEpiSwiglu: the fp32 SwiGLU output a [M, N] (ld = N), or null
   uint16_t* aux16;  // kEpiSwiglu: the bf16 SwiGLU output a [M, N] (ld = N), or null
   const float* qscale;  // kEpiSwiglu: with it, a is written as E4M3 codes fp8(fl32(a * *qscale)) instead
   uint32_t* amax_partial;
@@ -182,17 +181,6 @@ __device__ __forceinline__ void swiglu_bwd1(float da, float h, float u, float& d
   const float hs = h * s;
   dg = round_bf16(da * u * (s + hs * (1.0f - s)));
   du = round_bf16(da * hs);
-}
-
-// a = silu(h) * u with the hardware exponential and reciprocal: a few fp32 ulp
-// from the exactly rounded sequence (swiglu_ref), at a sixth of its instructions.
-// The fused forward's a only feeds the per-tensor E4M3 quantizer, whose codes
-// can differ only where a lies within those ulps of a rounding midpoint (about
-// 2^-18 of the codes, each by one step); the standalone swiglu_quant keeps the
-// exact form.  Large negative h: e^-h overflows to inf (or den > 2^126) and the
-// reciprocal flushes to 0, so a = -0 * u, as the exact form rounds to.
-__device__ __forceinline__ float swiglu_fast(float h, float u) {
-  return __fmul_rn(__fdividef(h, __fadd_rn(1.0f, __expf(-h))), u);
 }
 
 // H words of one 32-column chunk of a row: gate in h[0..3], up in h[4..7]
@@ -414,14 +402,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_store_2d(&tmAux, buf, col, row0);
                 bulk_commit();
               }
-            } else if (p.aux) {
-              staging_acquire(lane);
-              stage_f32(buf, lane, a);
-              staging_publish();
-              if (lane == 0) {
-                tma_store_2d(&tmAux, buf, col, row0);
-                bulk_commit();
-              }
             } else if (p.qscale) {
               // recomputation with the retained scale: SwiGLU fused with the E4M3 cast
               const float sq = *p.qscale;
@@ -638,9 +618,8 @@ cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L) {
   a.ldc = g.ldc;
   a.R = g.R;
   a.ldr = g.ldr;
-  a.aux = g.op16 ? nullptr : g.aux;
   a.aux16 = g.op16 ? g.a16 : nullptr;
-  a.qscale = (g.aux || g.op16) ? nullptr : g.qscale;
+  a.qscale = g.op16 ? nullptr : g.qscale;
   a.amax_partial = g.amax_partial;
   a.status = L.status;
   a.idesc = g.op16 ? make_idesc(1, 1, g.a_mn, g.b_mn) : make_idesc(g.fmtA, g.fmtB, g.a_mn, g.b_mn);
@@ -671,7 +650,6 @@ cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L) {
     ok_c = make_out_tmap(&tc, c, g.N, g.M, g.ldc, kOutBf16) && make_out_tmap(&tc2, c + g.N, g.N, g.M, g.ldc, kOutBf16);
     taux = tc;
     if (ok_c && g.op16 && g.a16) ok_c = make_out_tmap(&taux, g.a16, g.N, g.M, g.N, kOutBf16);
-    else if (ok_c && g.aux) ok_c = make_out_tmap(&taux, g.aux, g.N, g.M, g.N, kOutF32);
     else if (ok_c && g.qscale && g.q8) ok_c = make_out_tmap(&taux, g.q8, g.N, g.M, g.N, kOutU8);
   } else {
     ok_c = make_out_tmap(&tc, g.C, g.N, g.M, g.ldc, g.out_f32 ? kOutF32 : kOutBf16);

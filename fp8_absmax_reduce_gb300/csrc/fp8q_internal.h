@@ -41,8 +41,9 @@ cudaError_t launch_rmsnorm_cast(const uint16_t* x, const uint16_t* g, const floa
 
 // SwiGLU of H [T,2f]: pass 1 (absmax partials of a), pass 2 (cast).
 cudaError_t launch_swiglu_amax(const uint16_t* H, int64_t T, int f, uint32_t* partial, int* P, const Launch& L);
+// fast: the fused forward's E4M3 cast, with a = swiglu_fast (as the gate/up GEMM's absmax saw it).
 cudaError_t launch_swiglu_cast(const uint16_t* H, int64_t T, int f, int fmt, const uint32_t* partial, int P,
-                               uint8_t* q, float* scal, const Launch& L);
+                               uint8_t* q, float* scal, const Launch& L, bool fast = false);
 
 // RMSNorm backward + residual: dX = dY + rstd (u - nh mean(u nh)), dg = sum_t dN nh.
 // dg_partial: ceil(T / kBwdRows) x d floats of workspace.
@@ -59,7 +60,7 @@ cudaError_t launch_selftest_bounded_wait(uint64_t limit_ns, const Launch& L);
 enum GemmEpilogue {
   kEpiStore = 0,      // C = alpha * acc (bf16 or fp32)
   kEpiResidual = 1,   // C = bf16(R + alpha * acc)
-  kEpiSwiglu = 2,     // H = bf16(alpha * acc) for paired gate/up columns, a = SwiGLU(H), absmax of a
+  kEpiSwiglu = 2,     // H = bf16(alpha * acc) for paired gate/up columns, absmax of a = SwiGLU(H)
   kEpiSwigluBwd = 3,  // dH = bf16(SwiGLU'(H) * alpha * acc) + absmax of dH
 };
 
@@ -73,8 +74,7 @@ struct GemmProblem {
   int epi; int out_f32;
   void* C; int64_t ldc;  // kEpiSwiglu/kEpiSwigluBwd: [M, 2f] gate | up
   const uint16_t* R; int64_t ldr;  // residual (kEpiResidual) or H (kEpiSwigluBwd)
-  float* aux;                      // kEpiSwiglu: optional fp32 SwiGLU output a [M, N]
-  const float* qscale;             // kEpiSwiglu without aux: scale of a; a is written as E4M3 codes to q8
+  const float* qscale;             // kEpiSwiglu: optional scale of a; a is written as E4M3 codes to q8
   uint8_t* q8;                     //   [M, N] E4M3
   uint32_t* amax_partial;          // per-CTA partials for the two SwiGLU epilogues
   int op16;                        // 1: bf16 operands (lda/ldb in elements), no scales (alpha = 1)

@@ -267,14 +267,21 @@ __global__ void __launch_bounds__(kThreads) k_rmsnorm_cast(const uint16_t* __res
 // ---------------------------------------------------------------------------
 // SwiGLU: a = silu(gate) * up over H [T, 2f]
 // ---------------------------------------------------------------------------
+// FAST: swiglu_fast (the fused forward), else the exactly rounded swiglu_ref.
+template <bool FAST = false>
 __device__ __forceinline__ void swiglu8(const uint16_t* H, int64_t row, int f, int j0, float (&a)[8]) {
   const uint16_t* hr = H + row * 2 * (int64_t)f + j0;
   const uint4 gv = ld_nc_v4(hr), uv = ld_nc_v4(hr + f);
   const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    a[2 * k] = swiglu_ref(bf16_lo(gw[k]), bf16_lo(uw[k]));
-    a[2 * k + 1] = swiglu_ref(bf16_hi(gw[k]), bf16_hi(uw[k]));
+    if (FAST) {
+      a[2 * k] = swiglu_fast(bf16_lo(gw[k]), bf16_lo(uw[k]));
+      a[2 * k + 1] = swiglu_fast(bf16_hi(gw[k]), bf16_hi(uw[k]));
+    } else {
+      a[2 * k] = swiglu_ref(bf16_lo(gw[k]), bf16_lo(uw[k]));
+      a[2 * k + 1] = swiglu_ref(bf16_hi(gw[k]), bf16_hi(uw[k]));
+    }
   }
 }
 
@@ -296,7 +303,7 @@ __global__ void __launch_bounds__(kThreads) k_swiglu_amax(const uint16_t* __rest
   if (threadIdx.x == 0) partial[blockIdx.x] = m;
 }
 
-template <int FMT>
+template <int FMT, bool FAST>
 __global__ void __launch_bounds__(kThreads) k_swiglu_cast(const uint16_t* __restrict__ H, int64_t T, int f,
                                                           const uint32_t* __restrict__ partial, int P,
                                                           uint8_t* __restrict__ q, float* __restrict__ scal,
@@ -310,7 +317,7 @@ __global__ void __launch_bounds__(kThreads) k_swiglu_cast(const uint16_t* __rest
     const int64_t row = i / gpr;
     const int j0 = (int)(i - row * gpr) * 8;
     float a[8];
-    swiglu8(H, row, f, j0, a);
+    swiglu8<FAST>(H, row, f, j0, a);
     uint2 o;
     o.x = cvt_fp8x4<FMT>(__fmul_rn(a[0], s), __fmul_rn(a[1], s), __fmul_rn(a[2], s), __fmul_rn(a[3], s));
     o.y = cvt_fp8x4<FMT>(__fmul_rn(a[4], s), __fmul_rn(a[5], s), __fmul_rn(a[6], s), __fmul_rn(a[7], s));
@@ -547,12 +554,14 @@ cudaError_t launch_swiglu_amax(const uint16_t* H, int64_t T, int f, uint32_t* pa
 }
 
 cudaError_t launch_swiglu_cast(const uint16_t* H, int64_t T, int f, int fmt, const uint32_t* partial, int P,
-                               uint8_t* q, float* scal, const Launch& L) {
+                               uint8_t* q, float* scal, const Launch& L, bool fast) {
   const int grid = grid_for(T * (f / 8), L.num_sms * 8);
-  if (fmt == 0)
-    k_swiglu_cast<0><<<grid, kThreads, 0, L.stream>>>(H, T, f, partial, P, q, scal, L.status);
+  if (fast)
+    k_swiglu_cast<0, true><<<grid, kThreads, 0, L.stream>>>(H, T, f, partial, P, q, scal, L.status);
+  else if (fmt == 0)
+    k_swiglu_cast<0, false><<<grid, kThreads, 0, L.stream>>>(H, T, f, partial, P, q, scal, L.status);
   else
-    k_swiglu_cast<1><<<grid, kThreads, 0, L.stream>>>(H, T, f, partial, P, q, scal, L.status);
+    k_swiglu_cast<1, false><<<grid, kThreads, 0, L.stream>>>(H, T, f, partial, P, q, scal, L.status);
   return post_launch(L);
 }
 
