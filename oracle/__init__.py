@@ -85,6 +85,18 @@ class _FullIO(ctypes.Structure):
         ("scal_attn", ctypes.c_void_p), ("dX", ctypes.c_void_p), ("dWqkv", ctypes.c_void_p),
         ("dWo", ctypes.c_void_p), ("dg1", ctypes.c_void_p), ("d_att", ctypes.c_void_p), ("dh", ctypes.c_void_p),
         ("dh8", ctypes.c_void_p), ("dqkv8", ctypes.c_void_p), ("mlp", _BlockIO), ("x", ctypes.c_void_p),
+        ("n_heads", ctypes.c_int64), ("n_kv_heads", ctypes.c_int64), ("head_dim", ctypes.c_int64),
+        ("seq_len", ctypes.c_int64), ("att_out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("dqkv_out", ctypes.c_void_p),
+    ]
+
+
+class _AttnIO(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int64), ("S", ctypes.c_int64), ("Hq", ctypes.c_int64), ("Hkv", ctypes.c_int64),
+        ("dh", ctypes.c_int64), ("exact", ctypes.c_int), ("nthreads", ctypes.c_int),
+        ("qkv", ctypes.c_void_p), ("att", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("d_att", ctypes.c_void_p), ("dqkv", ctypes.c_void_p),
     ]
 
 
@@ -114,6 +126,7 @@ def lib() -> ctypes.CDLL:
             L.fo_block_forward.argtypes = [ctypes.POINTER(_BlockIO)]
             L.fo_block_forward_backward.argtypes = [ctypes.POINTER(_BlockIO)]
             L.fo_full_block.argtypes = [ctypes.POINTER(_FullIO), ctypes.c_int]
+            L.fo_attention.argtypes = [ctypes.POINTER(_AttnIO), ctypes.c_int]
             _lib = L
     return _lib
 
@@ -304,9 +317,40 @@ def block(x, g, Wgu, Wd, dY=None, eps: float = 1e-6, exact: bool = False, nthrea
     return out
 
 
+def attention(qkv, S: int, Hq: int, Hkv: int, dh: int, d_att=None, exact: bool = False, nthreads: int = 1):
+    """Causal grouped-query softmax attention (the core between the QKV and O projections).
+
+    qkv [T, (Hq + 2 Hkv) dh] (bf16 bits, or float64 in exact mode) holds B = T / S sequences of S
+    consecutive tokens; returns att [T, Hq dh] (bf16 values; exact mode unrounded), lse [Hq, T]
+    (natural log of each softmax denominator, relative to no shift), and with d_att [T, Hq dh]
+    the input gradient dqkv [T, (Hq + 2 Hkv) dh]."""
+    q64 = _as_f64(qkv, exact)
+    T, nq = q64.shape
+    if T % S or nq != (Hq + 2 * Hkv) * dh or Hq % Hkv:
+        raise ValueError("attention shapes")
+    out = {"att": np.empty((T, Hq * dh)), "lse": np.empty((Hq, T))}
+    io = _AttnIO(B=T // S, S=S, Hq=Hq, Hkv=Hkv, dh=dh, exact=int(exact), nthreads=int(nthreads))
+    keep = [q64]
+    io.qkv = q64.ctypes.data
+    io.att, io.lse = out["att"].ctypes.data, out["lse"].ctypes.data
+    if d_att is not None:
+        da64 = _as_f64(d_att, exact)
+        keep.append(da64)
+        out["dqkv"] = np.empty((T, nq))
+        io.d_att, io.dqkv = da64.ctypes.data, out["dqkv"].ctypes.data
+    st = lib().fo_attention(ctypes.byref(io), int(d_att is not None))
+    if st:
+        raise ValueError(f"fo_attention status {st}")
+    return out
+
+
 def full_block(x, g1, Wqkv, Wo, att, g2, Wgu, Wd, dY=None, dQKV=None, eps: float = 1e-6, exact: bool = False,
-               nthreads: int = 1, grad_fmt: int = E5M2):
+               nthreads: int = 1, grad_fmt: int = E5M2, core=None):
     """The full transformer block's matmuls around a given attention core.
+
+    core = (n_heads, n_kv_heads, head_dim, seq_len): the attention core (attention()) computes att
+    from qkv and, in the backward, dQKV from d_att; att and dQKV are then not read (may be None)
+    and the results hold "att", "lse" and "dqkv" as well.
 
     Forward: qkv = bf16(alpha n1_8 @ W_qkv8) with n1 = RMSNorm(x) g1; h = bf16(x + alpha att8 @ W_o8);
     y = MLP block on h (gain g2).  Backward (with dY [T,d] and the core's input gradient dQKV
@@ -314,7 +358,8 @@ def full_block(x, g1, Wqkv, Wo, att, g2, Wgu, Wd, dY=None, dQKV=None, eps: float
     RMSNorm'(alpha dQKV8 @ W_qkv8^T)); dg1.  Returned keys: the attention-side tensors plus every
     key of block() for the MLP part; scal_attn rows: W_qkv, W_o, n1, att, dh, dQKV.
     Inputs are bf16 bit patterns (quantized mode) or float64 (exact mode)."""
-    x64, g164, Wqkv64, Wo64, att64 = (_as_f64(a, exact) for a in (x, g1, Wqkv, Wo, att))
+    x64, g164, Wqkv64, Wo64 = (_as_f64(a, exact) for a in (x, g1, Wqkv, Wo))
+    att64 = _as_f64(att, exact) if att is not None else np.zeros(x64.shape)
     g264, Wgu64, Wd64 = (_as_f64(a, exact) for a in (g2, Wgu, Wd))
     T, d = x64.shape
     nq = Wqkv64.shape[1]
@@ -333,6 +378,10 @@ def full_block(x, g1, Wqkv, Wo, att, g2, Wgu, Wd, dY=None, dQKV=None, eps: float
     keep = [x64, g164, Wqkv64, Wo64, att64, g264, Wgu64, Wd64]
     io = _FullIO(T=T, d=d, f=f, nq=nq, eps=eps, exact=int(exact), nthreads=int(nthreads))
     io.x, io.g1, io.Wqkv, io.Wo, io.att = (a.ctypes.data for a in keep[:5])
+    if core is not None:
+        io.n_heads, io.n_kv_heads, io.head_dim, io.seq_len = (int(v) for v in core)
+        out.update({"att": np.empty((T, d)), "lse": np.empty((io.n_heads, T))})
+        io.att_out, io.lse = out["att"].ctypes.data, out["lse"].ctypes.data
     m = _BlockIO(T=T, d=d, f=f, eps=eps, exact=int(exact), nthreads=int(nthreads), grad_fmt=int(grad_fmt))
     m.g, m.Wgu, m.Wd = (a.ctypes.data for a in keep[5:])
     for k in ("qkv", "h", "rstd1", "Wqkv8", "Wo8", "n1_8", "att8", "scal_attn"):
@@ -340,10 +389,14 @@ def full_block(x, g1, Wqkv, Wo, att, g2, Wgu, Wd, dY=None, dQKV=None, eps: float
     for k in ("y", "H", "rstd", "Wgu8", "Wd8", "n8", "a8", "scal_fwd"):
         setattr(m, k, out[k].ctypes.data)
     if backward:
-        dY64, dQKV64 = _as_f64(dY, exact), _as_f64(dQKV, exact)
+        dY64 = _as_f64(dY, exact)
+        dQKV64 = _as_f64(dQKV, exact) if dQKV is not None else np.zeros((T, nq))
         keep += [dY64, dQKV64]
         m.dY = dY64.ctypes.data
         io.dQKV = dQKV64.ctypes.data
+        if core is not None:
+            out["dqkv"] = np.empty((T, nq))
+            io.dqkv_out = out["dqkv"].ctypes.data
         out.update({
             "dX": np.empty((T, d)), "dWqkv": np.empty((d, nq)), "dWo": np.empty((d, d)), "dg1": np.empty(d),
             "d_att": np.empty((T, d)), "dh": np.empty((T, d)), "dh8": np.empty((T, d), np.uint8),
@@ -358,4 +411,6 @@ def full_block(x, g1, Wqkv, Wo, att, g2, Wgu, Wd, dY=None, dQKV=None, eps: float
             setattr(m, k, out[k].ctypes.data)
     io.mlp = m
     out["status"] = lib().fo_full_block(ctypes.byref(io), int(backward))
+    if out["status"] & 2:
+        raise ValueError("full_block: inconsistent attention core shapes")
     return out

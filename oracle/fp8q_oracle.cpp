@@ -515,6 +515,136 @@ int block_backward(const BlockIO& io, const FwdState& S) {
 }
 
 // ----------------------------------------------------------------------------
+// The attention core between the QKV and O projections (LLMQ §2/§3 name the
+// transformer block's attention; the pages fix no attention arithmetic, so this
+// is plain causal softmax attention with grouped K/V heads, in fp64):
+//   qkv row of token t = [q_0 .. q_{Hq-1} | k_0 .. k_{Hkv-1} | v_0 .. v_{Hkv-1}], dh each
+//   tokens form B sequences of S consecutive tokens; query position i sees keys 0..i
+//   of its own sequence; q head h reads kv head h / (Hq / Hkv)
+//   s_ik = (q_i . k_k) / sqrt(dh);  P = softmax over k;  att_i = sum_k P_ik v_k
+//   att = bf16(att) (exact mode: unrounded);  lse_i = m_i + log(sum_k e^(s_ik - m_i))
+// Backward (d_att = dO given; the plain gradient of the definition above):
+//   dP_ik = dO_i . v_k;  D_i = sum_k P_ik dP_ik;  dS_ik = P_ik (dP_ik - D_i)
+//   dq_i = sum_k dS_ik k_k / sqrt(dh);  dk_k = sum over the group's heads and i of
+//   dS_ik q_i / sqrt(dh);  dv_k = sum over the group's heads and i of P_ik dO_i
+//   dqkv = bf16 (exact mode: unrounded)
+// ----------------------------------------------------------------------------
+struct AttnIO {
+  int64_t B, S, Hq, Hkv, dh;
+  int exact;
+  int nthreads;
+  const double* qkv;    // [B*S, (Hq + 2 Hkv) dh]
+  double* att;          // [B*S, Hq dh]
+  double* lse;          // [Hq, B*S]
+  const double* d_att;  // [B*S, Hq dh] (backward)
+  double* dqkv;         // [B*S, (Hq + 2 Hkv) dh] (backward)
+};
+
+// P row of (sequence b, head h, query i): probabilities of keys 0..i (fp64).
+void attn_probs(const AttnIO& io, int64_t b, int64_t h, int64_t i, std::vector<double>& p, double* lse) {
+  const int64_t nq = (io.Hq + 2 * io.Hkv) * io.dh, kvh = h / (io.Hq / io.Hkv);
+  const double sc = 1.0 / std::sqrt((double)io.dh);
+  const double* q = io.qkv + (b * io.S + i) * nq + h * io.dh;
+  p.assign((size_t)(i + 1), 0.0);
+  double m = -INFINITY;
+  for (int64_t k = 0; k <= i; ++k) {
+    const double* kr = io.qkv + (b * io.S + k) * nq + (io.Hq + kvh) * io.dh;
+    double dot = 0.0;
+    for (int64_t c = 0; c < io.dh; ++c) dot += q[c] * kr[c];
+    p[k] = dot * sc;
+    m = std::max(m, p[k]);
+  }
+  double l = 0.0;
+  for (int64_t k = 0; k <= i; ++k) { p[k] = std::exp(p[k] - m); l += p[k]; }
+  for (int64_t k = 0; k <= i; ++k) p[k] /= l;
+  if (lse) *lse = m + std::log(l);
+}
+
+void attn_fwd_heads(const AttnIO* io, int64_t w0, int64_t w1) {
+  const int64_t nq = (io->Hq + 2 * io->Hkv) * io->dh, da = io->Hq * io->dh, T = io->B * io->S;
+  std::vector<double> p;
+  for (int64_t w = w0; w < w1; ++w) {   // w = b * Hq + h
+    const int64_t b = w / io->Hq, h = w % io->Hq, kvh = h / (io->Hq / io->Hkv);
+    for (int64_t i = 0; i < io->S; ++i) {
+      double lse = 0.0;
+      attn_probs(*io, b, h, i, p, &lse);
+      double* o = io->att + (b * io->S + i) * da + h * io->dh;
+      for (int64_t c = 0; c < io->dh; ++c) {
+        double acc = 0.0;
+        for (int64_t k = 0; k <= i; ++k) acc += p[k] * io->qkv[(b * io->S + k) * nq + (io->Hq + io->Hkv + kvh) * io->dh + c];
+        o[c] = io->exact ? acc : to_bf16(acc);
+      }
+      if (io->lse) io->lse[h * T + b * io->S + i] = lse;
+    }
+  }
+}
+
+// One (sequence, kv head) group per work item: every dq of the group's heads and the
+// group's dk, dv (sums over its heads in a fixed order).
+void attn_bwd_groups(const AttnIO* io, int64_t w0, int64_t w1) {
+  const int64_t nq = (io->Hq + 2 * io->Hkv) * io->dh, da = io->Hq * io->dh, dh = io->dh;
+  const int64_t rep = io->Hq / io->Hkv;
+  const double sc = 1.0 / std::sqrt((double)dh);
+  std::vector<double> p, dp;
+  for (int64_t w = w0; w < w1; ++w) {   // w = b * Hkv + kvh
+    const int64_t b = w / io->Hkv, kvh = w % io->Hkv;
+    std::vector<double> dk((size_t)(io->S * dh), 0.0), dv((size_t)(io->S * dh), 0.0);
+    auto krow = [&](int64_t k) { return io->qkv + (b * io->S + k) * nq + (io->Hq + kvh) * dh; };
+    auto vrow = [&](int64_t k) { return io->qkv + (b * io->S + k) * nq + (io->Hq + io->Hkv + kvh) * dh; };
+    for (int64_t h = kvh * rep; h < (kvh + 1) * rep; ++h)
+      for (int64_t i = 0; i < io->S; ++i) {
+        attn_probs(*io, b, h, i, p, nullptr);
+        const double* q = io->qkv + (b * io->S + i) * nq + h * dh;
+        const double* dO = io->d_att + (b * io->S + i) * da + h * dh;
+        dp.assign((size_t)(i + 1), 0.0);
+        double D = 0.0;
+        for (int64_t k = 0; k <= i; ++k) {
+          const double* v = vrow(k);
+          double acc = 0.0;
+          for (int64_t c = 0; c < dh; ++c) acc += dO[c] * v[c];
+          dp[k] = acc;
+          D += p[k] * acc;
+        }
+        double* dq = io->dqkv + (b * io->S + i) * nq + h * dh;
+        for (int64_t c = 0; c < dh; ++c) dq[c] = 0.0;
+        for (int64_t k = 0; k <= i; ++k) {
+          const double ds = p[k] * (dp[k] - D);
+          const double* kr = krow(k);
+          for (int64_t c = 0; c < dh; ++c) {
+            dq[c] += ds * kr[c] * sc;
+            dk[k * dh + c] += ds * q[c] * sc;
+            dv[k * dh + c] += p[k] * dO[c];
+          }
+        }
+        if (!io->exact) for (int64_t c = 0; c < dh; ++c) dq[c] = to_bf16(dq[c]);
+      }
+    for (int64_t k = 0; k < io->S; ++k)
+      for (int64_t c = 0; c < dh; ++c) {
+        double* row = io->dqkv + (b * io->S + k) * nq;
+        row[(io->Hq + kvh) * dh + c] = io->exact ? dk[k * dh + c] : to_bf16(dk[k * dh + c]);
+        row[(io->Hq + io->Hkv + kvh) * dh + c] = io->exact ? dv[k * dh + c] : to_bf16(dv[k * dh + c]);
+      }
+  }
+}
+
+template <class F>
+void parallel_items(int64_t n, int nthreads, F fn) {
+  nthreads = std::max(1, std::min<int>(nthreads, (int)std::max<int64_t>(n, 1)));
+  if (nthreads == 1) { fn(0, n); return; }
+  std::vector<std::thread> pool;
+  for (int t = 0; t < nthreads; ++t) pool.emplace_back(fn, n * t / nthreads, n * (t + 1) / nthreads);
+  for (auto& th : pool) th.join();
+}
+
+int attention(const AttnIO& io, bool backward) {
+  if (io.B < 1 || io.S < 1 || io.Hq < 1 || io.Hkv < 1 || io.dh < 1 || io.Hq % io.Hkv) return 2;
+  parallel_items(io.B * io.Hq, io.nthreads, [&](int64_t a, int64_t b) { attn_fwd_heads(&io, a, b); });
+  if (backward)
+    parallel_items(io.B * io.Hkv, io.nthreads, [&](int64_t a, int64_t b) { attn_bwd_groups(&io, a, b); });
+  return 0;
+}
+
+// ----------------------------------------------------------------------------
 // The full transformer block's matmuls (the 32B-class workload).  The attention
 // core itself is not part of this path: its output `att` [T,d] and the gradient
 // arriving at its input `dQKV` [T,nq] are given tensors.  Reading of the block:
@@ -547,6 +677,12 @@ struct FullIO {
   uint8_t* dh8; uint8_t* dqkv8;
   BlockIO mlp;          // x = h (set by the caller), g, Wgu, Wd, dY and all MLP outputs
   const double* x;      // [T,d] block input
+  // attention core (nonzero n_heads): att and dQKV are computed from qkv and d_att by the
+  // core above instead of being given; d = n_heads * head_dim, T = n_seq * seq_len
+  int64_t n_heads, n_kv_heads, head_dim, seq_len;
+  double* att_out;      // [T,d] the core's output (bf16 values)
+  double* lse;          // [n_heads, T]
+  double* dqkv_out;     // [T,nq] the core's input gradient (bf16 values)
 };
 
 // RMSNorm backward with a residual gradient: dx = dres + rstd (u - nh mean(u nh)), u = dN g.
@@ -574,18 +710,36 @@ void rmsnorm_bwd(const std::vector<double>& x, const std::vector<double>& g, con
 int full_block(FullIO& io, bool backward) {
   const int64_t T = io.T, d = io.d, nq = io.nq;
   const bool ex = io.exact != 0;
+  const bool core = io.n_heads > 0;
   int status = 0;
-  std::vector<double> x(io.x, io.x + T * d), g1(io.g1, io.g1 + d), att(io.att, io.att + T * d);
+  std::vector<double> x(io.x, io.x + T * d), g1(io.g1, io.g1 + d);
   QTensor Wqkv = quantize(std::vector<double>(io.Wqkv, io.Wqkv + d * nq), FMT_E4M3, ex);
   QTensor Wo = quantize(std::vector<double>(io.Wo, io.Wo + d * d), FMT_E4M3, ex);
   std::vector<double> n1, rstd1;
   rmsnorm_fwd(x, g1, T, d, io.eps, ex, n1, rstd1);
   QTensor n1q = quantize(n1, FMT_E4M3, ex);
-  QTensor attq = quantize(att, FMT_E4M3, ex);
 
   const double a_qkv = ex ? 1.0 : (double)(n1q.s.scale_inv * Wqkv.s.scale_inv);
   std::vector<double> qkv = matmul(n1q.deq, Wqkv.deq, T, nq, d, io.nthreads);
   for (double& v : qkv) v = ex ? a_qkv * v : to_bf16(a_qkv * v);
+
+  std::vector<double> att, lse;
+  AttnIO aio{};
+  if (core) {
+    if (io.n_heads * io.head_dim != d || (io.n_heads + 2 * io.n_kv_heads) * io.head_dim != nq ||
+        io.seq_len < 1 || T % io.seq_len)
+      return 2;
+    att.assign((size_t)(T * d), 0.0);
+    lse.assign((size_t)(io.n_heads * T), 0.0);
+    aio = AttnIO{T / io.seq_len, io.seq_len, io.n_heads, io.n_kv_heads, io.head_dim, io.exact, io.nthreads,
+                 qkv.data(), att.data(), lse.data(), nullptr, nullptr};
+    if (attention(aio, false)) return 2;
+    put(io.att_out, att);
+    put(io.lse, lse);
+  } else {
+    att.assign(io.att, io.att + T * d);
+  }
+  QTensor attq = quantize(att, FMT_E4M3, ex);
   const double a_o = ex ? 1.0 : (double)(attq.s.scale_inv * Wo.s.scale_inv);
   std::vector<double> h = matmul(attq.deq, Wo.deq, T, d, d, io.nthreads);
   for (size_t i = 0; i < h.size(); ++i) h[i] = ex ? x[i] + a_o * h[i] : to_bf16(x[i] + a_o * h[i]);
@@ -622,8 +776,20 @@ int full_block(FullIO& io, bool backward) {
   std::vector<double> dWo = matmul(transpose(attq.deq, T, d), dhq.deq, d, d, T, io.nthreads);
   for (double& v : dWo) v = ex ? a_ow * v : (double)(float)(a_ow * v);
 
+  // the attention core's backward: dQKV from d_att (else dQKV is given)
+  std::vector<double> dqkv;
+  if (core) {
+    dqkv.assign((size_t)(T * nq), 0.0);
+    aio.d_att = datt.data();
+    aio.dqkv = dqkv.data();
+    parallel_items(aio.B * aio.Hkv, aio.nthreads, [&](int64_t a, int64_t b) { attn_bwd_groups(&aio, a, b); });
+    put(io.dqkv_out, dqkv);
+  } else {
+    dqkv.assign(io.dQKV, io.dQKV + T * nq);
+  }
+
   // QKV projection backward
-  QTensor dqq = quantize(std::vector<double>(io.dQKV, io.dQKV + T * nq), io.mlp.grad_fmt, ex);
+  QTensor dqq = quantize(dqkv, io.mlp.grad_fmt, ex);
   const double a_qd = ex ? 1.0 : (double)(dqq.s.scale_inv * Wqkv.s.scale_inv);
   std::vector<double> dN1 = matmul(dqq.deq, transpose(Wqkv.deq, d, nq), T, d, nq, io.nthreads);
   for (double& v : dN1) v = ex ? a_qd * v : (double)(float)(a_qd * v);
@@ -753,6 +919,7 @@ int fo_block_forward(const BlockIO* io) {
 // The full block's matmuls (attention core given as att / dQKV); the struct is
 // mirrored by oracle/__init__.py.
 int fo_full_block(FullIO* io, int backward) { return full_block(*io, backward != 0); }
+int fo_attention(const AttnIO* io, int backward) { return attention(*io, backward != 0); }
 
 int fo_block_forward_backward(const BlockIO* io) {
   FwdState S = block_forward(*io);
