@@ -48,6 +48,7 @@ def _load() -> ctypes.CDLL:
     L.mlp_block_workspace_size.restype = sz
     L.mlp_block_workspace_size.argtypes = [i64, i64, i64, i32]
     L.mlp_block_fwd.argtypes = [ctypes.POINTER(FP8QMlp), vp, sz, vp]
+    L.attention_fwd.argtypes = [vp, i64, i64, i32, i32, i32, vp, vp, vp]
     L.mlp_block_bwd.argtypes = [ctypes.POINTER(FP8QMlp), vp, sz, vp]
     L.fp8q_get_status.argtypes = [i32]
     L.fp8q_status_string.restype = ctypes.c_char_p
@@ -205,6 +206,19 @@ def swiglu_quant(H: torch.Tensor, fmt: int = E4M3, q=None, scal=None, ws=None, s
     w = _ws(nb, dev, ws)
     _check("swiglu_quant", lib.swiglu_quant(_ptr(H), T, f, fmt, _ptr(q), _ptr(scal), _ptr(w), nb, _stream(stream)))
     return q, scal
+
+
+def attention_fwd(qkv: torch.Tensor, seq_len: int, n_heads: int, n_kv_heads: int, att=None, lse=None,
+                  stream=None):
+    """Causal grouped-query attention of qkv [T, (n_heads + 2 n_kv_heads) 128] (bf16).
+    Returns (att [T, n_heads 128] bf16, lse [n_heads, T] fp32)."""
+    dev = _dev(qkv)
+    T = qkv.shape[0]
+    att = torch.empty((T, n_heads * 128), dtype=torch.bfloat16, device=dev) if att is None else att
+    lse = torch.empty((n_heads, T), dtype=torch.float32, device=dev) if lse is None else lse
+    _check("attention_fwd", lib.attention_fwd(_ptr(qkv), T, seq_len, n_heads, n_kv_heads, 128, _ptr(att), _ptr(lse),
+                                              _stream(stream)))
+    return att, lse
 
 
 # ---------------------------------------------------------------------------

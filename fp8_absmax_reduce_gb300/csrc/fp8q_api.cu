@@ -20,7 +20,7 @@ enum Kind {
   kKAbsmaxPartial = 0, kKQuantCast, kKRmsnormStats, kKRmsnormCast, kKSwigluAmax, kKSwigluCast, kKRmsnormBwd,
   kKGemmGateUp, kKGemmDown, kKGemmDownDgrad, kKGemmDownWgrad, kKGemmGateUpDgrad, kKGemmGateUpWgrad, kKGemm,
   kKGemmQkv, kKGemmOResidual, kKGemmODgrad, kKGemmOWgrad, kKGemmQkvDgrad, kKGemmQkvWgrad,
-  kKGemmGateUpRecompute, kKRmsnormBf16,
+  kKGemmGateUpRecompute, kKRmsnormBf16, kKAttnFwd,
   kKCount
 };
 const char* const kKindNames[kKCount] = {
@@ -28,7 +28,7 @@ const char* const kKindNames[kKCount] = {
     "rmsnorm_bwd", "gemm_gate_up_swiglu", "gemm_down_residual", "gemm_down_dgrad_swiglu_bwd",
     "gemm_down_wgrad", "gemm_gate_up_dgrad", "gemm_gate_up_wgrad", "gemm",
     "gemm_qkv", "gemm_o_residual", "gemm_o_dgrad", "gemm_o_wgrad", "gemm_qkv_dgrad", "gemm_qkv_wgrad",
-    "gemm_gate_up_recompute", "rmsnorm_bf16"};
+    "gemm_gate_up_recompute", "rmsnorm_bf16", "attn_fwd"};
 
 struct Trace {
   bool on = false;
@@ -790,6 +790,28 @@ int block_bwd(const fp8q_block* b, void* ws, size_t ws_bytes, fp8q_stream stream
   BlockWs w;
   block_ws_layout(b->T, b->d, b->f, b->n_qkv, 1, static_cast<uint8_t*>(ws), &w);
   if ((e = block_bwd_run(b, w, c))) return e;
+  return finish(c);
+}
+
+// ---------------------------------------------------------------------------
+// The attention core
+// ---------------------------------------------------------------------------
+int validate_attention(const void* qkv, int64_t T, int64_t S, int Hq, int Hkv, int dh) {
+  if (!al16(qkv) || T < 1 || S < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || T % S) return FP8Q_ERR_INVALID_ARG;
+  if (dh != 128 || S % 128) return FP8Q_ERR_UNSUPPORTED;
+  if (Hq > 65535 || T / S > 65535 || T > ((int64_t)1 << 31) - 1) return FP8Q_ERR_INVALID_ARG;
+  return FP8Q_OK;
+}
+
+int attention_fwd(const void* qkv, int64_t T, int64_t seq_len, int n_heads, int n_kv_heads, int head_dim,
+                  void* att, float* lse, fp8q_stream stream) {
+  int e = validate_attention(qkv, T, seq_len, n_heads, n_kv_heads, head_dim);
+  if (e) return e;
+  if (!al16(att) || !al16(lse)) return FP8Q_ERR_INVALID_ARG;
+  Ctx c;
+  if ((e = make_ctx(&c, stream))) return e;
+  FP8Q_STEP(kKAttnFwd, launch_attn_fwd(static_cast<const uint16_t*>(qkv), T, (int)seq_len, n_heads, n_kv_heads,
+                                       static_cast<uint16_t*>(att), lse, c.L));
   return finish(c);
 }
 

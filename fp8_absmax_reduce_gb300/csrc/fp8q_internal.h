@@ -51,6 +51,10 @@ cudaError_t launch_rmsnorm_bwd(const float* dN, const uint16_t* x, const uint16_
                                const float* rstd, int64_t T, int d, uint16_t* dX, float* dg_partial, float* dg,
                                const Launch& L);
 
+// Attention core (bf16, causal, grouped K/V heads, head dim 128, S a multiple of 128).
+cudaError_t launch_attn_fwd(const uint16_t* qkv, int64_t T, int S, int Hq, int Hkv, uint16_t* att, float* lse,
+                            const Launch& L);
+
 // Diagnostics: a bounded wait that is made to run out (see fp8q_selftest_bounded_wait).
 cudaError_t launch_selftest_bounded_wait(uint64_t limit_ns, const Launch& L);
 

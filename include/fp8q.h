@@ -279,6 +279,25 @@ FP8Q_API int block_fwd(const fp8q_block* b, void* ws, size_t ws_bytes, fp8q_stre
 FP8Q_API int block_bwd(const fp8q_block* b, void* ws, size_t ws_bytes, fp8q_stream stream);
 
 /* ------------------------------------------------------------------------ */
+/* The attention core between the QKV and O projections.  LLMQ §2/§3 name    */
+/* the transformer block's attention and custom kernels for it; the pages    */
+/* fix no attention arithmetic, so this is plain causal softmax attention    */
+/* with grouped K/V heads, bf16 in and out, fp32 softmax and accumulation.  */
+/* ------------------------------------------------------------------------ */
+/* qkv [T, (n_heads + 2 n_kv_heads) head_dim] bf16, row t = [q heads | k heads | v heads]
+ * (the QKV projection's output); the T tokens form T / seq_len sequences of seq_len
+ * consecutive tokens; query position i sees keys 0..i of its own sequence; query head h
+ * reads K/V head h / (n_heads / n_kv_heads); scale 1 / sqrt(head_dim).
+ *   att [T, n_heads head_dim] bf16: att_i = sum_k softmax_k(q_i . k_k / sqrt(head_dim)) v_k
+ *   lse [n_heads, T] fp32: natural log of each row's softmax denominator (kept for the backward)
+ * P is rounded to bf16 before it multiplies V (the tensor-core operand), its row sum is not.
+ * Requirements: head_dim = 128 and seq_len a positive multiple of 128 (else
+ * FP8Q_ERR_UNSUPPORTED); n_heads a multiple of n_kv_heads, T a multiple of seq_len, pointers
+ * 16-byte aligned (else FP8Q_ERR_INVALID_ARG).  Asynchronous; no workspace. */
+FP8Q_API int attention_fwd(const void* qkv, int64_t T, int64_t seq_len, int n_heads, int n_kv_heads, int head_dim,
+                           void* att, float* lse, fp8q_stream stream);
+
+/* ------------------------------------------------------------------------ */
 /* Status and introspection                                                 */
 /* ------------------------------------------------------------------------ */
 /* Reads (and with clear != 0 resets) the current device's status word

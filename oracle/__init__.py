@@ -96,7 +96,7 @@ class _AttnIO(ctypes.Structure):
         ("B", ctypes.c_int64), ("S", ctypes.c_int64), ("Hq", ctypes.c_int64), ("Hkv", ctypes.c_int64),
         ("dh", ctypes.c_int64), ("exact", ctypes.c_int), ("nthreads", ctypes.c_int),
         ("qkv", ctypes.c_void_p), ("att", ctypes.c_void_p), ("lse", ctypes.c_void_p),
-        ("d_att", ctypes.c_void_p), ("dqkv", ctypes.c_void_p),
+        ("d_att", ctypes.c_void_p), ("dqkv", ctypes.c_void_p), ("att_abs", ctypes.c_void_p),
     ]
 
 
@@ -317,13 +317,15 @@ def block(x, g, Wgu, Wd, dY=None, eps: float = 1e-6, exact: bool = False, nthrea
     return out
 
 
-def attention(qkv, S: int, Hq: int, Hkv: int, dh: int, d_att=None, exact: bool = False, nthreads: int = 1):
+def attention(qkv, S: int, Hq: int, Hkv: int, dh: int, d_att=None, exact: bool = False, nthreads: int = 1,
+              with_abs: bool = False):
     """Causal grouped-query softmax attention (the core between the QKV and O projections).
 
     qkv [T, (Hq + 2 Hkv) dh] (bf16 bits, or float64 in exact mode) holds B = T / S sequences of S
     consecutive tokens; returns att [T, Hq dh] (bf16 values; exact mode unrounded), lse [Hq, T]
     (natural log of each softmax denominator, relative to no shift), and with d_att [T, Hq dh]
-    the input gradient dqkv [T, (Hq + 2 Hkv) dh]."""
+    the input gradient dqkv [T, (Hq + 2 Hkv) dh].  with_abs: also "att_abs" = sum_k P_ik |v_k|, the
+    size of the terms of each output (the scale of an error bound for rounded probabilities)."""
     q64 = _as_f64(qkv, exact)
     T, nq = q64.shape
     if T % S or nq != (Hq + 2 * Hkv) * dh or Hq % Hkv:
@@ -333,6 +335,9 @@ def attention(qkv, S: int, Hq: int, Hkv: int, dh: int, d_att=None, exact: bool =
     keep = [q64]
     io.qkv = q64.ctypes.data
     io.att, io.lse = out["att"].ctypes.data, out["lse"].ctypes.data
+    if with_abs:
+        out["att_abs"] = np.empty((T, Hq * dh))
+        io.att_abs = out["att_abs"].ctypes.data
     if d_att is not None:
         da64 = _as_f64(d_att, exact)
         keep.append(da64)

@@ -538,6 +538,7 @@ struct AttnIO {
   double* lse;          // [Hq, B*S]
   const double* d_att;  // [B*S, Hq dh] (backward)
   double* dqkv;         // [B*S, (Hq + 2 Hkv) dh] (backward)
+  double* att_abs;      // optional [B*S, Hq dh]: sum_k P_ik |v_k| (the size of the terms of att_i)
 };
 
 // P row of (sequence b, head h, query i): probabilities of keys 0..i (fp64).
@@ -570,9 +571,14 @@ void attn_fwd_heads(const AttnIO* io, int64_t w0, int64_t w1) {
       attn_probs(*io, b, h, i, p, &lse);
       double* o = io->att + (b * io->S + i) * da + h * io->dh;
       for (int64_t c = 0; c < io->dh; ++c) {
-        double acc = 0.0;
-        for (int64_t k = 0; k <= i; ++k) acc += p[k] * io->qkv[(b * io->S + k) * nq + (io->Hq + io->Hkv + kvh) * io->dh + c];
+        double acc = 0.0, aabs = 0.0;
+        for (int64_t k = 0; k <= i; ++k) {
+          const double v = io->qkv[(b * io->S + k) * nq + (io->Hq + io->Hkv + kvh) * io->dh + c];
+          acc += p[k] * v;
+          aabs += p[k] * std::fabs(v);
+        }
         o[c] = io->exact ? acc : to_bf16(acc);
+        if (io->att_abs) io->att_abs[(b * io->S + i) * da + h * io->dh + c] = aabs;
       }
       if (io->lse) io->lse[h * T + b * io->S + i] = lse;
     }
@@ -732,7 +738,7 @@ int full_block(FullIO& io, bool backward) {
     att.assign((size_t)(T * d), 0.0);
     lse.assign((size_t)(io.n_heads * T), 0.0);
     aio = AttnIO{T / io.seq_len, io.seq_len, io.n_heads, io.n_kv_heads, io.head_dim, io.exact, io.nthreads,
-                 qkv.data(), att.data(), lse.data(), nullptr, nullptr};
+                 qkv.data(), att.data(), lse.data(), nullptr, nullptr, nullptr};
     if (attention(aio, false)) return 2;
     put(io.att_out, att);
     put(io.lse, lse);

@@ -77,12 +77,25 @@ def test_zero_queries_average_the_prefix():
     S, Hq, Hkv, dh = 9, 2, 1, 4
     qkv = rand_qkv(S, Hq, Hkv, dh, seed=5)
     qkv[:, :Hq * dh] = 0.0
-    out = oracle.attention(qkv, S, Hq, Hkv, dh, exact=True)
+    out = oracle.attention(qkv, S, Hq, Hkv, dh, exact=True, with_abs=True)
     v = qkv[:, (Hq + Hkv) * dh:]
     prefix_mean = np.cumsum(v, 0) / np.arange(1, S + 1)[:, None]
     for h in range(Hq):
         np.testing.assert_allclose(out["att"][:, h * dh:(h + 1) * dh], prefix_mean, rtol=1e-13)
+        np.testing.assert_allclose(out["att_abs"][:, h * dh:(h + 1) * dh],
+                                   np.cumsum(np.abs(v), 0) / np.arange(1, S + 1)[:, None], rtol=1e-13)
         np.testing.assert_allclose(out["lse"][h], np.log(np.arange(1, S + 1)), rtol=1e-13)
+
+
+def test_att_abs_bounds_att():
+    S, Hq, Hkv, dh = 12, 4, 2, 6
+    qkv = rand_qkv(3 * S, Hq, Hkv, dh, seed=7, scale=2.0)
+    out = oracle.attention(qkv, S, Hq, Hkv, dh, exact=True, with_abs=True)
+    assert np.all(out["att_abs"] >= np.abs(out["att"]) * (1 - 1e-14))
+    # a constant-sign V makes the two equal
+    qkv[:, (Hq + Hkv) * dh:] = np.abs(qkv[:, (Hq + Hkv) * dh:])
+    out = oracle.attention(qkv, S, Hq, Hkv, dh, exact=True, with_abs=True)
+    np.testing.assert_allclose(out["att_abs"], out["att"], rtol=1e-13)
 
 
 def test_causal_and_sequences_independent():
