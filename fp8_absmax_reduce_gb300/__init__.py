@@ -49,6 +49,9 @@ def _load() -> ctypes.CDLL:
     L.mlp_block_workspace_size.argtypes = [i64, i64, i64, i32]
     L.mlp_block_fwd.argtypes = [ctypes.POINTER(FP8QMlp), vp, sz, vp]
     L.attention_fwd.argtypes = [vp, i64, i64, i32, i32, i32, vp, vp, vp]
+    L.attention_bwd_workspace_size.restype = sz
+    L.attention_bwd_workspace_size.argtypes = [i64, i32]
+    L.attention_bwd.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, i32, vp, vp, sz, vp]
     L.mlp_block_bwd.argtypes = [ctypes.POINTER(FP8QMlp), vp, sz, vp]
     L.fp8q_get_status.argtypes = [i32]
     L.fp8q_status_string.restype = ctypes.c_char_p
@@ -219,6 +222,19 @@ def attention_fwd(qkv: torch.Tensor, seq_len: int, n_heads: int, n_kv_heads: int
     _check("attention_fwd", lib.attention_fwd(_ptr(qkv), T, seq_len, n_heads, n_kv_heads, 128, _ptr(att), _ptr(lse),
                                               _stream(stream)))
     return att, lse
+
+
+def attention_bwd(qkv: torch.Tensor, att: torch.Tensor, lse: torch.Tensor, d_att: torch.Tensor, seq_len: int,
+                  n_heads: int, n_kv_heads: int, dqkv=None, ws=None, stream=None):
+    """Input gradient dqkv [T, (n_heads + 2 n_kv_heads) 128] (bf16) of attention_fwd for d_att."""
+    dev = _dev(qkv)
+    T = qkv.shape[0]
+    dqkv = torch.empty_like(qkv) if dqkv is None else dqkv
+    nb = lib.attention_bwd_workspace_size(T, n_heads)
+    w = _ws(nb, dev, ws)
+    _check("attention_bwd", lib.attention_bwd(_ptr(qkv), _ptr(att), _ptr(lse), _ptr(d_att), T, seq_len, n_heads,
+                                              n_kv_heads, 128, _ptr(dqkv), _ptr(w), nb, _stream(stream)))
+    return dqkv
 
 
 # ---------------------------------------------------------------------------

@@ -20,7 +20,7 @@ enum Kind {
   kKAbsmaxPartial = 0, kKQuantCast, kKRmsnormStats, kKRmsnormCast, kKSwigluAmax, kKSwigluCast, kKRmsnormBwd,
   kKGemmGateUp, kKGemmDown, kKGemmDownDgrad, kKGemmDownWgrad, kKGemmGateUpDgrad, kKGemmGateUpWgrad, kKGemm,
   kKGemmQkv, kKGemmOResidual, kKGemmODgrad, kKGemmOWgrad, kKGemmQkvDgrad, kKGemmQkvWgrad,
-  kKGemmGateUpRecompute, kKRmsnormBf16, kKAttnFwd,
+  kKGemmGateUpRecompute, kKRmsnormBf16, kKAttnFwd, kKAttnBwdDelta, kKAttnBwdDkdv, kKAttnBwdDq,
   kKCount
 };
 const char* const kKindNames[kKCount] = {
@@ -28,7 +28,7 @@ const char* const kKindNames[kKCount] = {
     "rmsnorm_bwd", "gemm_gate_up_swiglu", "gemm_down_residual", "gemm_down_dgrad_swiglu_bwd",
     "gemm_down_wgrad", "gemm_gate_up_dgrad", "gemm_gate_up_wgrad", "gemm",
     "gemm_qkv", "gemm_o_residual", "gemm_o_dgrad", "gemm_o_wgrad", "gemm_qkv_dgrad", "gemm_qkv_wgrad",
-    "gemm_gate_up_recompute", "rmsnorm_bf16", "attn_fwd"};
+    "gemm_gate_up_recompute", "rmsnorm_bf16", "attn_fwd", "attn_bwd_delta", "attn_bwd_dkdv", "attn_bwd_dq"};
 
 struct Trace {
   bool on = false;
@@ -812,6 +812,33 @@ int attention_fwd(const void* qkv, int64_t T, int64_t seq_len, int n_heads, int 
   if ((e = make_ctx(&c, stream))) return e;
   FP8Q_STEP(kKAttnFwd, launch_attn_fwd(static_cast<const uint16_t*>(qkv), T, (int)seq_len, n_heads, n_kv_heads,
                                        static_cast<uint16_t*>(att), lse, c.L));
+  return finish(c);
+}
+
+size_t attention_bwd_workspace_size(int64_t T, int n_heads) {
+  if (T < 1 || n_heads < 1) return 0;
+  return 2 * round256((size_t)T * (size_t)n_heads * 4);
+}
+
+int attention_bwd(const void* qkv, const void* att, const float* lse, const void* d_att, int64_t T, int64_t seq_len,
+                  int n_heads, int n_kv_heads, int head_dim, void* dqkv, void* ws, size_t ws_bytes,
+                  fp8q_stream stream) {
+  int e = validate_attention(qkv, T, seq_len, n_heads, n_kv_heads, head_dim);
+  if (e) return e;
+  if (!al16(att) || !al16(lse) || !al16(d_att) || !al16(dqkv)) return FP8Q_ERR_INVALID_ARG;
+  if ((e = check_ws(ws, ws_bytes, attention_bwd_workspace_size(T, n_heads)))) return e;
+  Ctx c;
+  if ((e = make_ctx(&c, stream))) return e;
+  float* delta = static_cast<float*>(ws);
+  float* lse2 = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + round256((size_t)T * (size_t)n_heads * 4));
+  const uint16_t* q16 = static_cast<const uint16_t*>(qkv);
+  const uint16_t* do16 = static_cast<const uint16_t*>(d_att);
+  uint16_t* dq16 = static_cast<uint16_t*>(dqkv);
+  const int S = (int)seq_len;
+  FP8Q_STEP(kKAttnBwdDelta, launch_attn_bwd_delta(static_cast<const uint16_t*>(att), do16, lse, T, n_heads, delta,
+                                                  lse2, c.L));
+  FP8Q_STEP(kKAttnBwdDkdv, launch_attn_bwd_dkdv(q16, do16, T, S, n_heads, n_kv_heads, delta, lse2, dq16, c.L));
+  FP8Q_STEP(kKAttnBwdDq, launch_attn_bwd_dq(q16, do16, T, S, n_heads, n_kv_heads, delta, lse2, dq16, c.L));
   return finish(c);
 }
 

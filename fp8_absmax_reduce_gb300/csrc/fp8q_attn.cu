@@ -21,6 +21,18 @@
 //               the running sum, and O in registers, O = O 2^(m_old - m) + O_j;
 //               at the end O / l goes out through the Q tile with TMA stores
 //               and lse = ln 2 (m + log2 l).
+// Backward (dO = d_att), three kernels:
+//   k_attn_bwd_delta  D = rowsum(dO * O) over the stored att, and lse in the
+//                     log2 domain, per (token, head);
+//   k_attn_bwd_dkdv   one CTA per (128-key tile, K/V head, sequence): with its K
+//                     and V tiles in shared memory it walks the group's query
+//                     heads and the query tiles at or after it; S^T = K Q^T and
+//                     dP^T = V dO^T into TMEM, one thread per key row forms
+//                     P^T = 2^(s - lse) and dS^T = P^T (dP^T - D) as bf16 operand
+//                     tiles, and dV += P^T dO, dK += dS^T Q accumulate in TMEM
+//                     (the group's sum stays inside the CTA: deterministic);
+//   k_attn_bwd_dq     one CTA per (128-query tile, query head, sequence): S and
+//                     dP, then dS, then dQ += dS K over the key tiles 0 .. i.
 // Every mbarrier wait is bounded; on expiry the CTA records FP8Q_STATUS_TIMEOUT,
 // stops issuing work, drains what it issued, frees TMEM and exits.
 #include "fp8q_common.cuh"
@@ -335,6 +347,454 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Backward
+// ---------------------------------------------------------------------------
+struct AttnBwdArgs {
+  int T, S, Hq, Hkv;
+  int n_qt;
+  float scale_log2;   // log2(e) / sqrt(128)
+  float scale;        // 1 / sqrt(128)
+  const float* lse2;  // [Hq, T] lse in the log2 domain
+  const float* delta; // [Hq, T] D = rowsum(dO * O)
+  unsigned* status;
+};
+
+__device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+
+// D[h, t] = sum_c dO[t, h*128 + c] * O[t, h*128 + c] (fp32, fixed order), lse2 = lse * log2(e).
+// One warp per (t, h): lane l takes columns 4l .. 4l+3.
+__global__ void __launch_bounds__(256) k_attn_bwd_delta(const uint16_t* __restrict__ att,
+                                                        const uint16_t* __restrict__ datt,
+                                                        const float* __restrict__ lse, int T, int Hq,
+                                                        float* __restrict__ delta, float* __restrict__ lse2) {
+  const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= (int64_t)T * Hq) return;
+  const int t = (int)(wid / Hq), h = (int)(wid % Hq);
+  const int64_t off = (int64_t)t * Hq * kDh + h * kDh + lane * 4;
+  const uint2 o = *reinterpret_cast<const uint2*>(att + off);
+  const uint2 g = *reinterpret_cast<const uint2*>(datt + off);
+  float v = bf16_lo(o.x) * bf16_lo(g.x);
+  v = fmaf(bf16_hi(o.x), bf16_hi(g.x), v);
+  v = fmaf(bf16_lo(o.y), bf16_lo(g.y), v);
+  v = fmaf(bf16_hi(o.y), bf16_hi(g.y), v);
+#pragma unroll
+  for (int k = 16; k >= 1; k >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, k);
+  if (lane == 0) {
+    delta[(int64_t)h * T + t] = v;
+    lse2[(int64_t)h * T + t] = lse[(int64_t)h * T + t] * 1.44269504088896341f;
+  }
+}
+
+// dK, dV shared-memory layout
+constexpr int kKK = 0;
+constexpr int kKV = kKK + kTile;
+constexpr int kKQ = kKV + kTile;
+constexpr int kKO = kKQ + kTile;     // dO tile
+constexpr int kKPT = kKO + kTile;    // P^T tile (bf16, K-major over queries)
+constexpr int kKDST = kKPT + kTile;  // dS^T tile
+constexpr int kKVec = kKDST + kTile; // lse2[128], delta[128] of the current query tile
+constexpr int kKBar = kKVec + 1024;
+constexpr int kDkdvSmem = kKBar + 256 + 1024;
+static_assert(kDkdvSmem <= 232448, "shared memory per CTA");
+
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    k_attn_bwd_dkdv(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmDO,
+                    const __grid_constant__ CUtensorMap tmDQKV, const AttnBwdArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kKBar);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* qdo_full = bars + 1;
+  uint64_t* qdo_empty = bars + 2;
+  uint64_t* s_full = bars + 3;
+  uint64_t* s_free = bars + 4;
+  uint64_t* p_full = bars + 5;
+  uint64_t* p_free = bars + 6;
+  uint64_t* acc_full = bars + 7;
+  uint64_t* drain = bars + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* v_lse2 = reinterpret_cast<float*>(smem + kKVec);
+  float* v_delta = v_lse2 + 128;
+
+  const int jt = (int)blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int rep = p.Hq / p.Hkv;
+  const int nq_tiles = p.n_qt - jt;   // query tiles jt .. n_qt-1 see this key tile
+  const int n_items = rep * nq_tiles; // item u: head g*rep + u / nq_tiles, query tile jt + u % nq_tiles
+  const int k0 = b * p.S + jt * 128;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    mbar_init(qdo_full, 1);
+    mbar_init(qdo_empty, 1);
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 128);
+    mbar_init(p_full, 128);
+    mbar_init(p_free, 1);
+    mbar_init(acc_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQKV);
+    tma_prefetch_desc(&tmDO);
+    tma_prefetch_desc(&tmDQKV);
+  }
+  if (warp == 2) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t sbase = smem_addr(smem);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      bool ok = true;
+      int last = -1;  // last item whose Q/dO load was issued
+      const int xk = (p.Hq + g) * kDh, xv = (p.Hq + p.Hkv + g) * kDh;
+      mbar_arrive_expect_tx(kv_full, 2 * kTile);
+      tma_load_2d(smem + kKK, &tmQKV, kv_full, xk, k0);
+      tma_load_2d(smem + kKK + kAtom, &tmQKV, kv_full, xk + 64, k0);
+      tma_load_2d(smem + kKV, &tmQKV, kv_full, xv, k0);
+      tma_load_2d(smem + kKV + kAtom, &tmQKV, kv_full, xv + 64, k0);
+      for (int u = 0; u < n_items; ++u) {
+        if (!mbar_wait(qdo_empty, ((uint32_t)u & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+        const int h = g * rep + u / nq_tiles, it = jt + u % nq_tiles;
+        const int q0 = b * p.S + it * 128;
+        mbar_arrive_expect_tx(qdo_full, 2 * kTile + 1024);
+        tma_load_2d(smem + kKQ, &tmQKV, qdo_full, h * kDh, q0);
+        tma_load_2d(smem + kKQ + kAtom, &tmQKV, qdo_full, h * kDh + 64, q0);
+        tma_load_2d(smem + kKO, &tmDO, qdo_full, h * kDh, q0);
+        tma_load_2d(smem + kKO + kAtom, &tmDO, qdo_full, h * kDh + 64, q0);
+        bulk_load_1d(v_lse2, p.lse2 + (int64_t)h * p.T + q0, 512, qdo_full);
+        bulk_load_1d(v_delta, p.delta + (int64_t)h * p.T + q0, 512, qdo_full);
+        last = u;
+      }
+      if (!ok) {
+        atomicOr(p.status, kStatusTimeout);
+        *abort_flag = 1;
+        int dummy = 0;
+        mbar_wait(kv_full, 0, &dummy);
+        if (last >= 0) mbar_wait(qdo_full, (uint32_t)last & 1u, &dummy);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      const uint32_t tSt = tmem, tdPt = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+      bool ok = mbar_wait(kv_full, 0, abort_flag);
+      for (int u = 0; u < n_items && ok; ++u) {
+        const uint32_t par = (uint32_t)u & 1u;
+        if (!mbar_wait(qdo_full, par, abort_flag) || !mbar_wait(s_free, par ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        mma_tile_kk(tSt, sbase + kKK, sbase + kKQ, false);   // S^T = K Q^T
+        mma_tile_kk(tdPt, sbase + kKV, sbase + kKO, false);  // dP^T = V dO^T
+        umma_commit(s_full);
+        if (!mbar_wait(p_full, par, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        mma_tile_kmn(tdV, sbase + kKPT, sbase + kKO, u > 0);   // dV += P^T dO
+        mma_tile_kmn(tdK, sbase + kKDST, sbase + kKQ, u > 0);  // dK += dS^T Q
+        umma_commit(qdo_empty);
+        umma_commit(p_free);
+      }
+      if (ok) umma_commit(acc_full);
+      else {
+        atomicOr(p.status, kStatusTimeout);
+        *abort_flag = 1;
+      }
+      umma_commit(drain);
+      int dummy = 0;
+      mbar_wait(drain, 0, &dummy);
+    }
+  } else if (warp >= 4) {
+    // ---------------- P^T, dS^T (one key row per thread) ----------------
+    const int r = threadIdx.x - 128;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tSt = tmem + lane_off, tdPt = tmem + 128 + lane_off;
+    bool ok = true;
+    for (int u = 0; u < n_items; ++u) {
+      const uint32_t par = (uint32_t)u & 1u;
+      const bool diag = (u % nq_tiles) == 0;  // query tile jt: mask queries before this key
+      // qdo_full: this thread reads the lse2 / delta vectors that arrived with the Q/dO tiles
+      if (!mbar_wait(qdo_full, par, abort_flag) || !mbar_wait(s_full, par, abort_flag) ||
+          !mbar_wait(p_free, par ^ 1u, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sv[32], dv[32], wp[16], ws[16];
+        tmem_ld32(tSt + c * 32, sv);
+        tmem_ld32(tdPt + c * 32, dv);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          float pp[2], dd[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = c * 32 + 2 * k + e;
+            const float pt = (diag && col < r) ? 0.0f
+                                               : ex2_approx(__uint_as_float(sv[2 * k + e]) * p.scale_log2 - v_lse2[col]);
+            pp[e] = pt;
+            dd[e] = pt * (__uint_as_float(dv[2 * k + e]) - v_delta[col]);
+          }
+          wp[k] = pack_bf16x2(pp[0], pp[1]);
+          ws[k] = pack_bf16x2(dd[0], dd[1]);
+        }
+        tile_put32(sbase + kKPT, r, c, wp);
+        tile_put32(sbase + kKDST, r, c, ws);
+      }
+      tc_fence_before();
+      mbar_arrive(s_free);
+      fence_async_shared();
+      mbar_arrive(p_full);
+    }
+    if (ok && !mbar_wait(acc_full, 0, abort_flag)) ok = false;
+    if (!ok) {
+      atomicOr(p.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
+    // dV and dK rows (dK scaled by 1/sqrt(128)) out through the P^T and dS^T tiles
+    if (ok) {
+      tc_fence_after();
+      const uint32_t tdV = tmem + 256 + lane_off, tdK = tmem + 384 + lane_off;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t vv[32], kv[32], wv[16], wk[16];
+        tmem_ld32(tdV + c * 32, vv);
+        tmem_ld32(tdK + c * 32, kv);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          wv[k] = pack_bf16x2(__uint_as_float(vv[2 * k]), __uint_as_float(vv[2 * k + 1]));
+          wk[k] = pack_bf16x2(__uint_as_float(kv[2 * k]) * p.scale, __uint_as_float(kv[2 * k + 1]) * p.scale);
+        }
+        tile_put32(sbase + kKPT, r, c, wv);
+        tile_put32(sbase + kKDST, r, c, wk);
+      }
+    }
+    fence_async_shared();
+    named_bar_sync(1, 128);
+    if (r == 0 && !*abort_flag) {
+      const int xk = (p.Hq + g) * kDh, xv = (p.Hq + p.Hkv + g) * kDh;
+      tma_store_2d(&tmDQKV, sbase + kKDST, xk, k0);
+      tma_store_2d(&tmDQKV, sbase + kKDST + kAtom, xk + 64, k0);
+      tma_store_2d(&tmDQKV, sbase + kKPT, xv, k0);
+      tma_store_2d(&tmDQKV, sbase + kKPT + kAtom, xv + 64, k0);
+      bulk_commit_and_wait();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) tmem_dealloc(tmem, kTmemCols);
+}
+
+// dQ shared-memory layout
+constexpr int kQQ = 0;
+constexpr int kQO = kQQ + kTile;
+constexpr int kQK = kQO + kTile;      // [2] stages
+constexpr int kQV = kQK + 2 * kTile;  // [2] stages
+constexpr int kQDS = kQV + 2 * kTile;
+constexpr int kQBar = kQDS + kTile;
+constexpr int kDqSmem = kQBar + 256 + 1024;
+static_assert(kDqSmem <= 232448, "shared memory per CTA");
+
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    k_attn_bwd_dq(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmDO,
+                  const __grid_constant__ CUtensorMap tmDQKV, const AttnBwdArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQBar);
+  uint64_t* q_full = bars + 0;
+  uint64_t* kv_full = bars + 1;   // [2]
+  uint64_t* kv_empty = bars + 3;  // [2]
+  uint64_t* s_full = bars + 5;
+  uint64_t* s_free = bars + 6;
+  uint64_t* ds_full = bars + 7;
+  uint64_t* ds_free = bars + 8;
+  uint64_t* acc_full = bars + 9;
+  uint64_t* drain = bars + 10;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int qt = p.n_qt - 1 - (int)blockIdx.x;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int g = h / (p.Hq / p.Hkv);
+  const int t0 = b * p.S + qt * 128;
+  const int n = qt + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < 2; ++s) { mbar_init(&kv_full[s], 1); mbar_init(&kv_empty[s], 1); }
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 128);
+    mbar_init(ds_full, 128);
+    mbar_init(ds_free, 1);
+    mbar_init(acc_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQKV);
+    tma_prefetch_desc(&tmDO);
+    tma_prefetch_desc(&tmDQKV);
+  }
+  if (warp == 2) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t sbase = smem_addr(smem);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      bool ok = true;
+      uint32_t issued = 0, issued_par = 0;
+      mbar_arrive_expect_tx(q_full, 2 * kTile);
+      tma_load_2d(smem + kQQ, &tmQKV, q_full, h * kDh, t0);
+      tma_load_2d(smem + kQQ + kAtom, &tmQKV, q_full, h * kDh + 64, t0);
+      tma_load_2d(smem + kQO, &tmDO, q_full, h * kDh, t0);
+      tma_load_2d(smem + kQO + kAtom, &tmDO, q_full, h * kDh + 64, t0);
+      const int xk = (p.Hq + g) * kDh, xv = (p.Hq + p.Hkv + g) * kDh;
+      for (int j = 0; j < n; ++j) {
+        const int st = j & 1;
+        const uint32_t u = (uint32_t)(j >> 1) & 1u;
+        if (!mbar_wait(&kv_empty[st], u ^ 1u, abort_flag)) { ok = false; break; }
+        uint8_t* sk = smem + kQK + st * kTile;
+        uint8_t* sv = smem + kQV + st * kTile;
+        const int y = b * p.S + j * 128;
+        mbar_arrive_expect_tx(&kv_full[st], 2 * kTile);
+        tma_load_2d(sk, &tmQKV, &kv_full[st], xk, y);
+        tma_load_2d(sk + kAtom, &tmQKV, &kv_full[st], xk + 64, y);
+        tma_load_2d(sv, &tmQKV, &kv_full[st], xv, y);
+        tma_load_2d(sv + kAtom, &tmQKV, &kv_full[st], xv + 64, y);
+        issued |= 1u << st;
+        issued_par = (issued_par & ~(1u << st)) | (u << st);
+      }
+      if (!ok) {
+        atomicOr(p.status, kStatusTimeout);
+        *abort_flag = 1;
+        int dummy = 0;
+        mbar_wait(q_full, 0, &dummy);
+        for (int s = 0; s < 2; ++s)
+          if (issued & (1u << s)) mbar_wait(&kv_full[s], (issued_par >> s) & 1u, &dummy);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256;
+      bool ok = mbar_wait(q_full, 0, abort_flag);
+      for (int j = 0; j < n && ok; ++j) {
+        const int st = j & 1;
+        const uint32_t u = (uint32_t)(j >> 1) & 1u, par = (uint32_t)j & 1u;
+        if (!mbar_wait(&kv_full[st], u, abort_flag) || !mbar_wait(s_free, par ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        mma_tile_kk(tS, sbase + kQQ, sbase + kQK + st * kTile, false);   // S = Q K^T
+        mma_tile_kk(tdP, sbase + kQO, sbase + kQV + st * kTile, false);  // dP = dO V^T
+        umma_commit(s_full);
+        if (!mbar_wait(ds_full, par, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        mma_tile_kmn(tdQ, sbase + kQDS, sbase + kQK + st * kTile, j > 0);  // dQ += dS K
+        umma_commit(&kv_empty[st]);
+        umma_commit(ds_free);
+      }
+      if (ok) umma_commit(acc_full);
+      else {
+        atomicOr(p.status, kStatusTimeout);
+        *abort_flag = 1;
+      }
+      umma_commit(drain);
+      int dummy = 0;
+      mbar_wait(drain, 0, &dummy);
+    }
+  } else if (warp >= 4) {
+    const int r = threadIdx.x - 128;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off, tdP = tmem + 128 + lane_off;
+    const float lse2 = p.lse2[(int64_t)h * p.T + t0 + r];
+    const float dlt = p.delta[(int64_t)h * p.T + t0 + r];
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      const uint32_t par = (uint32_t)j & 1u;
+      const bool diag = j == qt;
+      if (!mbar_wait(s_full, par, abort_flag) || !mbar_wait(ds_free, par ^ 1u, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sv[32], dv[32], w[16];
+        tmem_ld32(tS + c * 32, sv);
+        tmem_ld32(tdP + c * 32, dv);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          float dd[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = c * 32 + 2 * k + e;
+            const float pp =
+                (diag && col > r) ? 0.0f : ex2_approx(__uint_as_float(sv[2 * k + e]) * p.scale_log2 - lse2);
+            dd[e] = pp * (__uint_as_float(dv[2 * k + e]) - dlt);
+          }
+          w[k] = pack_bf16x2(dd[0], dd[1]);
+        }
+        tile_put32(sbase + kQDS, r, c, w);
+      }
+      tc_fence_before();
+      mbar_arrive(s_free);
+      fence_async_shared();
+      mbar_arrive(ds_full);
+    }
+    if (ok && !mbar_wait(acc_full, 0, abort_flag)) ok = false;
+    if (!ok) {
+      atomicOr(p.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
+    // dQ row (scaled by 1/sqrt(128)) out through the Q tile (every MMA has completed)
+    if (ok) {
+      tc_fence_after();
+      const uint32_t tdQ = tmem + 256 + lane_off;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t qv[32], w[16];
+        tmem_ld32(tdQ + c * 32, qv);
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          w[k] = pack_bf16x2(__uint_as_float(qv[2 * k]) * p.scale, __uint_as_float(qv[2 * k + 1]) * p.scale);
+        tile_put32(sbase + kQQ, r, c, w);
+      }
+    }
+    fence_async_shared();
+    named_bar_sync(1, 128);
+    if (r == 0 && !*abort_flag) {
+      tma_store_2d(&tmDQKV, sbase + kQQ, h * kDh, t0);
+      tma_store_2d(&tmDQKV, sbase + kQQ + kAtom, h * kDh + 64, t0);
+      bulk_commit_and_wait();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -368,15 +828,31 @@ bool make_tile_map(CUtensorMap* m, const void* base, int64_t cols, int64_t rows,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Opt a kernel into its dynamic shared memory once per device; `configured` is that kernel's own flag.
 template <class K>
-cudaError_t set_smem(K kernel, int bytes) {
-  static int configured_device = -1;
+cudaError_t set_smem(K kernel, int bytes, int& configured) {
   int dev = 0;
   cudaGetDevice(&dev);
-  if (configured_device == dev) return cudaSuccess;
+  if (configured == dev) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) configured_device = dev;
+  if (e == cudaSuccess) configured = dev;
   return e;
+}
+int g_cfg_fwd = -1, g_cfg_dkdv = -1, g_cfg_dq = -1;
+
+AttnBwdArgs bwd_args(int64_t T, int S, int Hq, int Hkv, const float* delta, const float* lse2, const Launch& L) {
+  AttnBwdArgs a{};
+  a.T = (int)T;
+  a.S = S;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.n_qt = S / 128;
+  a.scale_log2 = 1.44269504088896341f / 11.3137084989847604f;  // log2(e) / sqrt(128)
+  a.scale = 1.0f / 11.3137084989847604f;
+  a.lse2 = lse2;
+  a.delta = delta;
+  a.status = L.status;
+  return a;
 }
 
 }  // namespace
@@ -396,10 +872,50 @@ cudaError_t launch_attn_fwd(const uint16_t* qkv, int64_t T, int S, int Hq, int H
   a.scale_log2 = 1.44269504088896341f / 11.3137084989847604f;  // log2(e) / sqrt(128)
   a.lse = lse;
   a.status = L.status;
-  cudaError_t e = set_smem(k_attn_fwd, kFwdSmem);
+  cudaError_t e = set_smem(k_attn_fwd, kFwdSmem, g_cfg_fwd);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)a.n_qt, (unsigned)Hq, (unsigned)(T / S));
   k_attn_fwd<<<grid, kAttnThreads, kFwdSmem, L.stream>>>(tq, ta, a);
+  if (L.launches) ++*L.launches;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd_delta(const uint16_t* att, const uint16_t* datt, const float* lse, int64_t T, int Hq,
+                                  float* delta, float* lse2, const Launch& L) {
+  const int64_t rows = T * Hq;
+  k_attn_bwd_delta<<<(unsigned)((rows * 32 + 255) / 256), 256, 0, L.stream>>>(att, datt, lse, (int)T, Hq, delta, lse2);
+  if (L.launches) ++*L.launches;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd_dkdv(const uint16_t* qkv, const uint16_t* datt, int64_t T, int S, int Hq, int Hkv,
+                                 const float* delta, const float* lse2, uint16_t* dqkv, const Launch& L) {
+  const int64_t nq = (int64_t)(Hq + 2 * Hkv) * kDh, da = (int64_t)Hq * kDh;
+  CUtensorMap tq, tdo, tdq;
+  if (!make_tile_map(&tq, qkv, nq, T, nq) || !make_tile_map(&tdo, datt, da, T, da) ||
+      !make_tile_map(&tdq, dqkv, nq, T, nq))
+    return cudaErrorInvalidValue;
+  const AttnBwdArgs a = bwd_args(T, S, Hq, Hkv, delta, lse2, L);
+  cudaError_t e = set_smem(k_attn_bwd_dkdv, kDkdvSmem, g_cfg_dkdv);
+  if (e != cudaSuccess) return e;
+  k_attn_bwd_dkdv<<<dim3((unsigned)a.n_qt, (unsigned)Hkv, (unsigned)(T / S)), kAttnThreads, kDkdvSmem, L.stream>>>(
+      tq, tdo, tdq, a);
+  if (L.launches) ++*L.launches;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd_dq(const uint16_t* qkv, const uint16_t* datt, int64_t T, int S, int Hq, int Hkv,
+                               const float* delta, const float* lse2, uint16_t* dqkv, const Launch& L) {
+  const int64_t nq = (int64_t)(Hq + 2 * Hkv) * kDh, da = (int64_t)Hq * kDh;
+  CUtensorMap tq, tdo, tdq;
+  if (!make_tile_map(&tq, qkv, nq, T, nq) || !make_tile_map(&tdo, datt, da, T, da) ||
+      !make_tile_map(&tdq, dqkv, nq, T, nq))
+    return cudaErrorInvalidValue;
+  const AttnBwdArgs a = bwd_args(T, S, Hq, Hkv, delta, lse2, L);
+  cudaError_t e = set_smem(k_attn_bwd_dq, kDqSmem, g_cfg_dq);
+  if (e != cudaSuccess) return e;
+  k_attn_bwd_dq<<<dim3((unsigned)a.n_qt, (unsigned)Hq, (unsigned)(T / S)), kAttnThreads, kDqSmem, L.stream>>>(
+      tq, tdo, tdq, a);
   if (L.launches) ++*L.launches;
   return cudaGetLastError();
 }

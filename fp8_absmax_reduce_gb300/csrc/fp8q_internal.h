@@ -54,6 +54,13 @@ cudaError_t launch_rmsnorm_bwd(const float* dN, const uint16_t* x, const uint16_
 // Attention core (bf16, causal, grouped K/V heads, head dim 128, S a multiple of 128).
 cudaError_t launch_attn_fwd(const uint16_t* qkv, int64_t T, int S, int Hq, int Hkv, uint16_t* att, float* lse,
                             const Launch& L);
+// Backward: D = rowsum(dO * att) and lse2 = lse log2(e) ([Hq, T] each), then dK/dV and dQ into dqkv.
+cudaError_t launch_attn_bwd_delta(const uint16_t* att, const uint16_t* datt, const float* lse, int64_t T, int Hq,
+                                  float* delta, float* lse2, const Launch& L);
+cudaError_t launch_attn_bwd_dkdv(const uint16_t* qkv, const uint16_t* datt, int64_t T, int S, int Hq, int Hkv,
+                                 const float* delta, const float* lse2, uint16_t* dqkv, const Launch& L);
+cudaError_t launch_attn_bwd_dq(const uint16_t* qkv, const uint16_t* datt, int64_t T, int S, int Hq, int Hkv,
+                               const float* delta, const float* lse2, uint16_t* dqkv, const Launch& L);
 
 // Diagnostics: a bounded wait that is made to run out (see fp8q_selftest_bounded_wait).
 cudaError_t launch_selftest_bounded_wait(uint64_t limit_ns, const Launch& L);

@@ -296,6 +296,19 @@ FP8Q_API int block_bwd(const fp8q_block* b, void* ws, size_t ws_bytes, fp8q_stre
  * 16-byte aligned (else FP8Q_ERR_INVALID_ARG).  Asynchronous; no workspace. */
 FP8Q_API int attention_fwd(const void* qkv, int64_t T, int64_t seq_len, int n_heads, int n_kv_heads, int head_dim,
                            void* att, float* lse, fp8q_stream stream);
+/* Backward of attention_fwd: the plain gradient of the definition above, with d_att = dO
+ * [T, n_heads head_dim] bf16 given, att and lse as attention_fwd wrote them:
+ *   dP = dO V^T, D = rowsum(dO * att), dS = P (dP - D);  dq = dS K / sqrt(head_dim),
+ *   dk = dS^T Q / sqrt(head_dim) and dv = P^T dO summed over the query heads of each K/V head.
+ * dqkv [T, (n_heads + 2 n_kv_heads) head_dim] bf16 (same layout as qkv) is overwritten in full.
+ * P and dS are rounded to bf16 as tensor-core operands.  Deterministic (no atomics: a K/V
+ * head's gradient is summed over its query heads inside one CTA).  Workspace:
+ * attention_bwd_workspace_size(T, n_heads) bytes (D and lse in the log2 domain), 256-byte
+ * aligned.  Requirements and errors as attention_fwd. */
+FP8Q_API size_t attention_bwd_workspace_size(int64_t T, int n_heads);
+FP8Q_API int attention_bwd(const void* qkv, const void* att, const float* lse, const void* d_att, int64_t T,
+                           int64_t seq_len, int n_heads, int n_kv_heads, int head_dim, void* dqkv, void* ws,
+                           size_t ws_bytes, fp8q_stream stream);
 
 /* ------------------------------------------------------------------------ */
 /* Status and introspection                                                 */

@@ -97,6 +97,7 @@ class _AttnIO(ctypes.Structure):
         ("dh", ctypes.c_int64), ("exact", ctypes.c_int), ("nthreads", ctypes.c_int),
         ("qkv", ctypes.c_void_p), ("att", ctypes.c_void_p), ("lse", ctypes.c_void_p),
         ("d_att", ctypes.c_void_p), ("dqkv", ctypes.c_void_p), ("att_abs", ctypes.c_void_p),
+        ("dqkv_abs", ctypes.c_void_p),
     ]
 
 
@@ -325,7 +326,8 @@ def attention(qkv, S: int, Hq: int, Hkv: int, dh: int, d_att=None, exact: bool =
     consecutive tokens; returns att [T, Hq dh] (bf16 values; exact mode unrounded), lse [Hq, T]
     (natural log of each softmax denominator, relative to no shift), and with d_att [T, Hq dh]
     the input gradient dqkv [T, (Hq + 2 Hkv) dh].  with_abs: also "att_abs" = sum_k P_ik |v_k|, the
-    size of the terms of each output (the scale of an error bound for rounded probabilities)."""
+    size of the terms of each output (the scale of an error bound for rounded probabilities), and
+    with d_att "dqkv_abs", the same for each gradient (see the oracle's AttnIO)."""
     q64 = _as_f64(qkv, exact)
     T, nq = q64.shape
     if T % S or nq != (Hq + 2 * Hkv) * dh or Hq % Hkv:
@@ -343,6 +345,9 @@ def attention(qkv, S: int, Hq: int, Hkv: int, dh: int, d_att=None, exact: bool =
         keep.append(da64)
         out["dqkv"] = np.empty((T, nq))
         io.d_att, io.dqkv = da64.ctypes.data, out["dqkv"].ctypes.data
+        if with_abs:
+            out["dqkv_abs"] = np.empty((T, nq))
+            io.dqkv_abs = out["dqkv_abs"].ctypes.data
     st = lib().fo_attention(ctypes.byref(io), int(d_att is not None))
     if st:
         raise ValueError(f"fo_attention status {st}")

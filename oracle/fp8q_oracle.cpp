@@ -539,6 +539,11 @@ struct AttnIO {
   const double* d_att;  // [B*S, Hq dh] (backward)
   double* dqkv;         // [B*S, (Hq + 2 Hkv) dh] (backward)
   double* att_abs;      // optional [B*S, Hq dh]: sum_k P_ik |v_k| (the size of the terms of att_i)
+  // optional [B*S, (Hq + 2 Hkv) dh], the size of the terms of each gradient when P, dS and att
+  // carry relative errors (Dabs_i = sum_c |dO_ic| (att_abs_ic + |att_ic|) bounds D's error scale):
+  //   dq: sum_k |k_k| (|dS_ik| + P_ik Dabs_i) / sqrt(dh); dk: the same over i with |q_i|;
+  //   dv: sum_i P_ik |dO_i|
+  double* dqkv_abs;
 };
 
 // P row of (sequence b, head h, query i): probabilities of keys 0..i (fp64).
@@ -595,6 +600,7 @@ void attn_bwd_groups(const AttnIO* io, int64_t w0, int64_t w1) {
   for (int64_t w = w0; w < w1; ++w) {   // w = b * Hkv + kvh
     const int64_t b = w / io->Hkv, kvh = w % io->Hkv;
     std::vector<double> dk((size_t)(io->S * dh), 0.0), dv((size_t)(io->S * dh), 0.0);
+    std::vector<double> dka(io->dqkv_abs ? (size_t)(io->S * dh) : 0, 0.0), dva(dka.size(), 0.0);
     auto krow = [&](int64_t k) { return io->qkv + (b * io->S + k) * nq + (io->Hq + kvh) * dh; };
     auto vrow = [&](int64_t k) { return io->qkv + (b * io->S + k) * nq + (io->Hq + io->Hkv + kvh) * dh; };
     for (int64_t h = kvh * rep; h < (kvh + 1) * rep; ++h)
@@ -610,6 +616,28 @@ void attn_bwd_groups(const AttnIO* io, int64_t w0, int64_t w1) {
           for (int64_t c = 0; c < dh; ++c) acc += dO[c] * v[c];
           dp[k] = acc;
           D += p[k] * acc;
+        }
+        double Dabs = 0.0;
+        if (io->dqkv_abs) {
+          for (int64_t c = 0; c < dh; ++c) {
+            double o = 0.0, oa = 0.0;
+            for (int64_t k = 0; k <= i; ++k) {
+              o += p[k] * vrow(k)[c];
+              oa += p[k] * std::fabs(vrow(k)[c]);
+            }
+            Dabs += std::fabs(dO[c]) * (oa + std::fabs(o));
+          }
+          double* dqa = io->dqkv_abs + (b * io->S + i) * nq + h * dh;
+          for (int64_t c = 0; c < dh; ++c) dqa[c] = 0.0;
+          for (int64_t k = 0; k <= i; ++k) {
+            const double w = std::fabs(p[k] * (dp[k] - D)) + p[k] * Dabs;
+            const double* kr = krow(k);
+            for (int64_t c = 0; c < dh; ++c) {
+              dqa[c] += w * std::fabs(kr[c]) * sc;
+              dka[k * dh + c] += w * std::fabs(q[c]) * sc;
+              dva[k * dh + c] += p[k] * std::fabs(dO[c]);
+            }
+          }
         }
         double* dq = io->dqkv + (b * io->S + i) * nq + h * dh;
         for (int64_t c = 0; c < dh; ++c) dq[c] = 0.0;
@@ -629,6 +657,11 @@ void attn_bwd_groups(const AttnIO* io, int64_t w0, int64_t w1) {
         double* row = io->dqkv + (b * io->S + k) * nq;
         row[(io->Hq + kvh) * dh + c] = io->exact ? dk[k * dh + c] : to_bf16(dk[k * dh + c]);
         row[(io->Hq + io->Hkv + kvh) * dh + c] = io->exact ? dv[k * dh + c] : to_bf16(dv[k * dh + c]);
+        if (io->dqkv_abs) {
+          double* ra = io->dqkv_abs + (b * io->S + k) * nq;
+          ra[(io->Hq + kvh) * dh + c] = dka[k * dh + c];
+          ra[(io->Hq + io->Hkv + kvh) * dh + c] = dva[k * dh + c];
+        }
       }
   }
 }
@@ -738,7 +771,7 @@ int full_block(FullIO& io, bool backward) {
     att.assign((size_t)(T * d), 0.0);
     lse.assign((size_t)(io.n_heads * T), 0.0);
     aio = AttnIO{T / io.seq_len, io.seq_len, io.n_heads, io.n_kv_heads, io.head_dim, io.exact, io.nthreads,
-                 qkv.data(), att.data(), lse.data(), nullptr, nullptr, nullptr};
+                 qkv.data(), att.data(), lse.data(), nullptr, nullptr, nullptr, nullptr};
     if (attention(aio, false)) return 2;
     put(io.att_out, att);
     put(io.lse, lse);

@@ -92,6 +92,10 @@ def test_att_abs_bounds_att():
     qkv = rand_qkv(3 * S, Hq, Hkv, dh, seed=7, scale=2.0)
     out = oracle.attention(qkv, S, Hq, Hkv, dh, exact=True, with_abs=True)
     assert np.all(out["att_abs"] >= np.abs(out["att"]) * (1 - 1e-14))
+    dO = np.random.default_rng(8).standard_normal((3 * S, Hq * dh))
+    g = oracle.attention(qkv, S, Hq, Hkv, dh, d_att=dO, exact=True, with_abs=True)
+    assert np.all(g["dqkv_abs"] >= np.abs(g["dqkv"]) * (1 - 1e-12))
+    np.testing.assert_array_equal(g["dqkv"], oracle.attention(qkv, S, Hq, Hkv, dh, d_att=dO, exact=True)["dqkv"])
     # a constant-sign V makes the two equal
     qkv[:, (Hq + Hkv) * dh:] = np.abs(qkv[:, (Hq + Hkv) * dh:])
     out = oracle.attention(qkv, S, Hq, Hkv, dh, exact=True, with_abs=True)
