@@ -89,7 +89,9 @@ class FP8QBlock(ctypes.Structure):
                                                   "n1_8", "rstd1", "att8", "scal")]
                 + [("mlp", FP8QMlp)]
                 + [(n, ctypes.c_void_p) for n in ("dQKV", "d_att", "dX", "dW_qkv", "dW_o", "dg1", "dh8", "dQKV8",
-                                                  "dN1")])
+                                                  "dN1")]
+                + [("n_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int), ("seq_len", ctypes.c_int64),
+                   ("lse", ctypes.c_void_p)])
 
 
 _lib_handle = None
@@ -369,10 +371,16 @@ class BlockBuffers:
     dQKV8: torch.Tensor | None = None
     dN1: torch.Tensor | None = None
     ws: torch.Tensor | None = None
+    n_heads: int = 0
+    n_kv_heads: int = 0
+    seq_len: int = 0
+    lse: torch.Tensor | None = None
 
     @staticmethod
     def allocate(T: int, d: int, f: int, n_qkv: int, device="cuda", backward: bool = True, eps: float = 1e-6,
-                 keep_intermediates: bool = False) -> "BlockBuffers":
+                 keep_intermediates: bool = False, core=None) -> "BlockBuffers":
+        """core = (n_heads, n_kv_heads, seq_len): the attention core runs inside the block (att and
+        dQKV become outputs); None: att and dQKV are given."""
         e = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)
         m = MlpBuffers.allocate(T, d, f, device=device, backward=backward, eps=eps,
                                 keep_intermediates=keep_intermediates)
@@ -394,6 +402,9 @@ class BlockBuffers:
                 b.dh8 = e((T, d), torch.uint8)
                 b.dQKV8 = e((T, n_qkv), torch.uint8)
                 b.dN1 = e((T, d), torch.float32)
+        if core is not None:
+            b.n_heads, b.n_kv_heads, b.seq_len = (int(v) for v in core)
+            b.lse = e((b.n_heads, T), torch.float32)
         nb = lib.block_workspace_size(T, d, f, n_qkv, int(backward))
         b.ws = torch.empty(nb, dtype=torch.uint8, device=device)
         return b
@@ -407,7 +418,9 @@ class BlockBuffers:
         return self.mlp.dX
 
     def struct(self) -> FP8QBlock:
-        s = FP8QBlock(T=self.T, d=self.d, f=self.f, n_qkv=self.n_qkv, eps=self.eps)
+        s = FP8QBlock(T=self.T, d=self.d, f=self.f, n_qkv=self.n_qkv, eps=self.eps, n_heads=self.n_heads,
+                      n_kv_heads=self.n_kv_heads, seq_len=self.seq_len)
+        s.lse = None if self.lse is None else self.lse.data_ptr()
         for name in ("x", "g1", "W_qkv", "W_o", "att", "qkv", "W_qkv8", "W_o8", "n1_8", "rstd1", "att8", "scal",
                      "dQKV", "d_att", "dX", "dW_qkv", "dW_o", "dg1", "dh8", "dQKV8", "dN1"):
             t = getattr(self, name)

@@ -472,6 +472,8 @@ struct BlockWs {
   uint8_t* dqkv8;   // [T,nq] E5M2
   float* dN1;       // [T,d]
   float* dg1_part;  // dg partials of the attention-side RMSNorm backward
+  float* attn_delta;  // [d/128, T] the attention core backward's D (core mode)
+  float* attn_lse2;   // [d/128, T] its lse in the log2 domain
 };
 
 size_t block_ws_layout(int64_t T, int64_t d, int64_t f, int64_t nq, int backward, uint8_t* base, BlockWs* w) {
@@ -485,10 +487,20 @@ size_t block_ws_layout(int64_t T, int64_t d, int64_t f, int64_t nq, int backward
     tmp.dqkv8 = (uint8_t*)c.take((size_t)(T * nq));
     tmp.dN1 = (float*)c.take((size_t)(T * d) * 4);
     tmp.dg1_part = (float*)c.take((size_t)((T + kBwdRows - 1) / kBwdRows) * (size_t)d * 4);
+    tmp.attn_delta = (float*)c.take((size_t)T * (size_t)(d / 128) * 4);
+    tmp.attn_lse2 = (float*)c.take((size_t)T * (size_t)(d / 128) * 4);
   }
   if (base) mlp_ws_layout(T, d, f, backward, tmp.mlp_base, &tmp.mlp);
   if (w) *w = tmp;
   return c.off;
+}
+
+// The attention core's shape conditions (see attention_fwd in fp8q.h).
+int validate_attention(const void* qkv, int64_t T, int64_t S, int Hq, int Hkv, int dh) {
+  if (!al16(qkv) || T < 1 || S < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || T % S) return FP8Q_ERR_INVALID_ARG;
+  if (dh != 128 || S % 128) return FP8Q_ERR_UNSUPPORTED;
+  if (Hq > 65535 || T / S > 65535 || T > ((int64_t)1 << 31) - 1) return FP8Q_ERR_INVALID_ARG;
+  return FP8Q_OK;
 }
 
 int validate_block(const fp8q_block* b, bool backward) {
@@ -499,6 +511,12 @@ int validate_block(const fp8q_block* b, bool backward) {
   if (b->n_qkv < 16 || b->n_qkv % 16 || b->n_qkv > (int64_t)1 << 20) return FP8Q_ERR_INVALID_ARG;
   int e = validate_mlp(&m, backward);
   if (e) return e;
+  if (b->n_heads) {
+    if (b->n_kv_heads < 1 || (int64_t)b->n_heads * 128 != b->d ||
+        (int64_t)(b->n_heads + 2 * b->n_kv_heads) * 128 != b->n_qkv || !al16(b->lse))
+      return FP8Q_ERR_INVALID_ARG;
+    if ((e = validate_attention(b->qkv, b->T, b->seq_len, b->n_heads, b->n_kv_heads, 128))) return e;
+  }
   const void* must[] = {b->x, b->g1, b->W_qkv, b->W_o, b->att, b->qkv, b->h, b->W_qkv8, b->W_o8, b->n1_8,
                         b->rstd1, b->att8, b->scal};
   for (const void* p : must)
@@ -557,6 +575,10 @@ int block_fwd_run(const fp8q_block* b, const BlockWs& w, Ctx& c) {
   GemmProblem gq = gemm_problem(0, 1, T, nq, d, b->n1_8, d, 0, b->W_qkv8, nq, 0, nq, s_n1 + 2, s_qkv + 2, kEpiStore,
                                 0, b->qkv, nq);
   FP8Q_STEP(kKGemmQkv, launch_gemm(gq, &P, c.L));
+  // the attention core: att (and lse) from qkv
+  if (b->n_heads)
+    FP8Q_STEP(kKAttnFwd, launch_attn_fwd((const uint16_t*)b->qkv, T, (int)b->seq_len, b->n_heads, b->n_kv_heads,
+                                         (uint16_t*)b->att, b->lse, c.L));
   // h = bf16(x + alpha q(att) @ W_o8)
   FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(b->att, 0, T * d, w.part, &P, c.L));
   FP8Q_STEP(kKQuantCast, launch_quant_cast(b->att, 0, T * d, 0, w.part, P, b->att8, s_att, c.L));
@@ -594,6 +616,18 @@ int block_bwd_run(const fp8q_block* b, const BlockWs& w, Ctx& c) {
   GemmProblem gow = gemm_problem(1, 1, d, d, T, b->att8, d, 0, dh8, d, gf, d, s_att + 2, s_dh + 2, kEpiStore, 1,
                                  b->dW_o, d);
   FP8Q_STEP(kKGemmOWgrad, launch_gemm(gow, &P, c.L));
+  // the attention core's backward: dQKV from d_att
+  if (b->n_heads) {
+    const uint16_t* q16 = (const uint16_t*)b->qkv;
+    const uint16_t* do16 = (const uint16_t*)b->d_att;
+    const int S = (int)b->seq_len;
+    FP8Q_STEP(kKAttnBwdDelta, launch_attn_bwd_delta((const uint16_t*)b->att, do16, b->lse, T, b->n_heads,
+                                                    w.attn_delta, w.attn_lse2, c.L));
+    FP8Q_STEP(kKAttnBwdDkdv, launch_attn_bwd_dkdv(q16, do16, T, S, b->n_heads, b->n_kv_heads, w.attn_delta,
+                                                  w.attn_lse2, (uint16_t*)b->dQKV, c.L));
+    FP8Q_STEP(kKAttnBwdDq, launch_attn_bwd_dq(q16, do16, T, S, b->n_heads, b->n_kv_heads, w.attn_delta, w.attn_lse2,
+                                              (uint16_t*)b->dQKV, c.L));
+  }
   // dQKV8 = q5(dQKV); dN1 = alpha dQKV8 @ W_qkv8^T; dW_qkv = alpha n1_8^T @ dQKV8
   FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(b->dQKV, 0, T * nq, w.part, &P, c.L));
   FP8Q_STEP(kKQuantCast, launch_quant_cast(b->dQKV, 0, T * nq, gf, w.part, P, dqkv8, s_dq, c.L));
@@ -796,13 +830,6 @@ int block_bwd(const fp8q_block* b, void* ws, size_t ws_bytes, fp8q_stream stream
 // ---------------------------------------------------------------------------
 // The attention core
 // ---------------------------------------------------------------------------
-int validate_attention(const void* qkv, int64_t T, int64_t S, int Hq, int Hkv, int dh) {
-  if (!al16(qkv) || T < 1 || S < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || T % S) return FP8Q_ERR_INVALID_ARG;
-  if (dh != 128 || S % 128) return FP8Q_ERR_UNSUPPORTED;
-  if (Hq > 65535 || T / S > 65535 || T > ((int64_t)1 << 31) - 1) return FP8Q_ERR_INVALID_ARG;
-  return FP8Q_OK;
-}
-
 int attention_fwd(const void* qkv, int64_t T, int64_t seq_len, int n_heads, int n_kv_heads, int head_dim,
                   void* att, float* lse, fp8q_stream stream) {
   int e = validate_attention(qkv, T, seq_len, n_heads, n_kv_heads, head_dim);

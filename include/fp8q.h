@@ -252,7 +252,7 @@ typedef struct fp8q_block {
   const void* g1;     /* [d]       bf16 attention-side RMSNorm gain */
   const void* W_qkv;  /* [d,n_qkv] bf16 */
   const void* W_o;    /* [d,d]     bf16 */
-  const void* att;    /* [T,d]     bf16 attention core output */
+  void* att;          /* [T,d]     bf16 attention core output (input; written by block_fwd when n_heads != 0) */
   void* qkv;          /* [T,n_qkv] bf16 attention core input (forward output) */
   void* h;            /* [T,d]     bf16 attention residual output = the MLP input */
   uint8_t* W_qkv8;    /* [d,n_qkv] E4M3 */
@@ -262,7 +262,8 @@ typedef struct fp8q_block {
   uint8_t* att8;      /* [T,d]     E4M3 */
   float* scal;        /* [6][3] {amax, scale, scale_inv} of W_qkv, W_o, n1, att, dh, dQKV */
   fp8q_mlp mlp;       /* the MLP sub-block: mlp.x == h, mlp.dX receives dh */
-  const void* dQKV;   /* [T,n_qkv] bf16 gradient from the attention core */
+  void* dQKV;         /* [T,n_qkv] bf16 gradient from the attention core (input; written by block_bwd
+                       * when n_heads != 0) */
   void* d_att;        /* [T,d]     bf16 gradient to the attention core */
   void* dX;           /* [T,d]     bf16 */
   float* dW_qkv;      /* [d,n_qkv] fp32 */
@@ -272,6 +273,14 @@ typedef struct fp8q_block {
   uint8_t* dh8;       /* [T,d]     E5M2 */
   uint8_t* dQKV8;     /* [T,n_qkv] E5M2 */
   float* dN1;         /* [T,d]     fp32 */
+  /* The attention core inside the block (nonzero n_heads): block_fwd computes att = attention_fwd(qkv)
+   * (and lse) right after the QKV projection, block_bwd computes dQKV = attention_bwd(qkv, att, lse,
+   * d_att) right after the O projection's dgrad; att and dQKV are then outputs.  Requires
+   * n_heads * 128 = d, (n_heads + 2 n_kv_heads) * 128 = n_qkv and attention_fwd's conditions on
+   * seq_len.  Zero: att and dQKV are given (an attention core computed elsewhere). */
+  int n_heads, n_kv_heads;
+  int64_t seq_len;
+  float* lse;         /* [n_heads,T] fp32, written by block_fwd, read by block_bwd (n_heads != 0) */
 } fp8q_block;
 
 FP8Q_API size_t block_workspace_size(int64_t T, int64_t d, int64_t f, int64_t n_qkv, int backward);

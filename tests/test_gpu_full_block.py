@@ -191,3 +191,62 @@ def test_full_block_full_size():
     assert row_rel(bf16_np(b.dX[rows_t]), dX_ref) < 5e-3
     dg1_ref = (dN1 * (x * r1d[:, None])).sum(axis=0)
     assert row_rel(b.dg1.cpu().numpy()[None, :].astype(np.float64), dg1_ref[None, :]) < 5e-3
+
+
+def run_core(T, S, Hq, Hkv, f, seed=0):
+    d, nq = Hq * 128, (Hq + 2 * Hkv) * 128
+    inp = synth.block_inputs(W32, seed=seed, T=T, d=d, f=f, n_qkv=nq)
+    b = fq.BlockBuffers.allocate(T, d, f, nq, keep_intermediates=True, core=(Hq, Hkv, S))
+    for k, t in (("x", b.x), ("g1", b.g1), ("W_qkv", b.W_qkv), ("W_o", b.W_o), ("g", b.mlp.g),
+                 ("W_gu", b.mlp.W_gu), ("W_d", b.mlp.W_d), ("dY", b.mlp.dY)):
+        t.copy_(dev_bf16(inp[k]))
+    fq.get_status(clear=True)
+    fq.block_fwd(b)
+    fq.block_bwd(b)
+    torch.cuda.synchronize()
+    assert fq.get_status() == 0
+    return b, inp
+
+
+@pytest.mark.parametrize("T,S,Hq,Hkv,f", [(256, 128, 4, 2, 640), (512, 256, 4, 1, 768), (384, 384, 2, 2, 512)])
+def test_full_block_with_attention_core(T, S, Hq, Hkv, f):
+    """The block with its attention core (fp8q_block.n_heads != 0).
+
+    Wiring, bit for bit: the block's att / lse / dQKV equal attention_fwd / attention_bwd applied
+    to the block's own qkv, att, lse and d_att.  Against the oracle (full_block with the core):
+    qkv within 2e-3; att within the attention core's elementwise bound (test_gpu_attention.py)
+    around the oracle's attention of the oracle's qkv; the block's outputs y, dX within 2e-3 /
+    5e-3 and h, dh within 2e-3 / 5e-3.  Internal tensors behind the coarse gradient format get
+    cascade bars: dh differs from the oracle's by ~1e-3 (fp32 accumulation order plus the core's
+    bf16 probabilities carried through h), which flips about 2e-3 / 2^-2 ~ 1 % of dh8's E5M2 codes
+    by one step (a quarter of the element); d_att and dQKV, products of those codes, then move by
+    ~1e-2 (bar 3e-2), and the weight gradients and gain gradients fed by the flipped E5M2 codes
+    of d_att / dQKV (and by a8, second-level) by a few 1e-2 (bar 8e-2).  The components
+    themselves are held to the tight bars in test_gpu_attention.py and the block without the
+    core above."""
+    b, inp = run_core(T, S, Hq, Hkv, f)
+    # wiring against the standalone core on the block's own tensors
+    att2, lse2 = fq.attention_fwd(b.qkv, S, Hq, Hkv)
+    dqkv2 = fq.attention_bwd(b.qkv, b.att, b.lse, b.d_att, S, Hq, Hkv)
+    torch.cuda.synchronize()
+    assert torch.equal(att2, b.att) and torch.equal(lse2, b.lse) and torch.equal(dqkv2, b.dQKV)
+    # against the oracle
+    ref = oracle.full_block(inp["x"], inp["g1"], inp["W_qkv"], inp["W_o"], None, inp["g"], inp["W_gu"],
+                            inp["W_d"], dY=inp["dY"], nthreads=16, core=(Hq, Hkv, 128, S))
+    assert row_rel(bf16_np(b.qkv), ref["qkv"]) < 2e-3
+    ra = oracle.attention(synth.bf16_bits(ref["qkv"].astype(np.float32)), S, Hq, Hkv, 128, nthreads=16,
+                          with_abs=True)
+    np.testing.assert_array_equal(ra["att"], ref["att"])
+    bound = 2.0 ** -8 * (ra["att_abs"] + 2 * np.abs(ra["att"])) * (1 + 2.0 ** -6)
+    assert np.all(np.abs(bf16_np(b.att) - ref["att"]) <= bound)
+    np.testing.assert_allclose(b.lse.cpu().numpy(), ref["lse"], atol=1e-4, rtol=0)
+    assert row_rel(bf16_np(b.h), ref["h"]) < 2e-3
+    assert row_rel(bf16_np(b.mlp.y), ref["y"]) < 2e-3
+    assert row_rel(bf16_np(b.dh), ref["dh"]) < 5e-3
+    assert row_rel(bf16_np(b.dX), ref["dX"]) < 5e-3
+    assert row_rel(bf16_np(b.d_att), ref["d_att"]) < 3e-2
+    assert row_rel(bf16_np(b.dQKV), ref["dqkv"]) < 3e-2
+    for got, key in ((b.dW_o, "dWo"), (b.dW_qkv, "dWqkv"), (b.mlp.dW_gu, "dWgu"), (b.mlp.dW_d, "dWd")):
+        assert row_rel(got.cpu().numpy(), ref[key]) < 8e-2, key
+    for got, key in ((b.dg1, "dg1"), (b.mlp.dg, "dg")):
+        assert row_rel(got.cpu().numpy()[None, :], ref[key][None, :]) < 8e-2, key
