@@ -202,10 +202,25 @@ def step_work(w: synth.Workload, recompute: bool = False, bf16: bool = False):
         ("absmax_partial", 2 * T * d, 0), ("quant_cast", 3 * T * d, 0),
         ("gemm_o_residual", T * d + d * d + 4 * T * d, 2.0 * T * d * d),
     ]
+    core_fwd, core_bwd = [], []
+    if w.n_heads:
+        # the attention core: bytes read/written once; FLOPs executed (2 * 128 per causal pair and
+        # product: 2 products forward; dK/dV recomputes S and forms dP, dV, dK (4), dQ recomputes
+        # S and dP and forms dQ (3) -- the algorithmic count in the headline uses 5)
+        hq, hkv = w.n_heads, w.n_kv_heads
+        pairs = (T // w.seq_len) * w.seq_len * (w.seq_len + 1) / 2 * hq
+        core_fwd = [("attn_fwd", 2 * T * q + 2 * T * d + 4 * T * hq, 4.0 * 128 * pairs)]
+        core_bwd = [
+            ("attn_bwd_delta", 4 * T * d + 12 * T * hq, 0),
+            ("attn_bwd_dkdv", 2 * T * q + 2 * T * d + 8 * T * hq + 4 * T * hkv * 128, 8.0 * 128 * pairs),
+            ("attn_bwd_dq", 2 * T * q + 4 * T * d + 8 * T * hq, 6.0 * 128 * pairs),
+        ]
+        attn_fwd = attn_fwd[:7] + core_fwd + attn_fwd[7:]
     attn_bwd = [
         ("absmax_partial", 2 * T * d, 0), ("quant_cast", 3 * T * d, 0),
         ("gemm_o_dgrad", T * d + d * d + 2 * T * d, 2.0 * T * d * d),
         ("gemm_o_wgrad", 2 * T * d + 4 * d * d, 2.0 * T * d * d),
+        *core_bwd,
         ("absmax_partial", 2 * T * q, 0), ("quant_cast", 3 * T * q, 0),
         ("gemm_qkv_dgrad", T * q + d * q + 4 * T * d, 2.0 * T * q * d),
         ("gemm_qkv_wgrad", T * d + T * q + 4 * d * q, 2.0 * T * d * q),
@@ -222,14 +237,19 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     w = args.w
-    flops = w.gemm_flops()
+    flops = w.gemm_flops() + w.attention_flops()
     if w.qkv:
         inp = synth.block_inputs(w, seed=rank)
-        b = fq.BlockBuffers.allocate(w.T, w.d, w.f, w.qkv, device=dev, backward=w.backward)
-        dev_in = {"x": b.x, "g1": b.g1, "W_qkv": b.W_qkv, "W_o": b.W_o, "att": b.att, "g": b.mlp.g,
+        core = (w.n_heads, w.n_kv_heads, w.seq_len) if w.n_heads else None
+        b = fq.BlockBuffers.allocate(w.T, w.d, w.f, w.qkv, device=dev, backward=w.backward, core=core)
+        dev_in = {"x": b.x, "g1": b.g1, "W_qkv": b.W_qkv, "W_o": b.W_o, "g": b.mlp.g,
                   "W_gu": b.mlp.W_gu, "W_d": b.mlp.W_d}
+        if not core:
+            dev_in["att"] = b.att    # the attention core's output is given
         if w.backward:
-            dev_in.update(dY=b.mlp.dY, dQKV=b.dQKV)
+            dev_in["dY"] = b.mlp.dY
+            if not core:
+                dev_in["dQKV"] = b.dQKV
         dev_out = {"y": b.mlp.y}
         if w.backward:
             dev_out.update(dX=b.dX, dW_qkv=b.dW_qkv, dW_o=b.dW_o, dg1=b.dg1, dW_gu=b.mlp.dW_gu, dW_d=b.mlp.dW_d,
@@ -360,9 +380,12 @@ def cpu_baseline(w, tokens, grad_e4m3=False, bf16=False):
     if w.qkv:
         inp = synth.block_inputs(w, seed=0)
         sl = {k: inp[k][:tokens] for k in ("x", "att", "dY", "dQKV") if k in inp}
+        # with the attention core the sample is one sequence of `tokens` tokens
+        core = (w.n_heads, w.n_kv_heads, 128, tokens) if w.n_heads else None
         t0 = time.perf_counter()
-        oracle.full_block(sl["x"], inp["g1"], inp["W_qkv"], inp["W_o"], sl["att"], inp["g"], inp["W_gu"],
-                          inp["W_d"], dY=sl.get("dY"), dQKV=sl.get("dQKV"), nthreads=1, grad_fmt=gf)
+        oracle.full_block(sl["x"], inp["g1"], inp["W_qkv"], inp["W_o"], None if core else sl["att"], inp["g"],
+                          inp["W_gu"], inp["W_d"], dY=sl.get("dY"), dQKV=None if core else sl.get("dQKV"),
+                          nthreads=1, grad_fmt=gf, core=core)
         dt = time.perf_counter() - t0
     else:
         inp = synth.mlp_inputs(w, seed=0)
@@ -371,12 +394,13 @@ def cpu_baseline(w, tokens, grad_e4m3=False, bf16=False):
         t0 = time.perf_counter()
         oracle.block(x, inp["g"], inp["W_gu"], inp["W_d"], dY=dY, nthreads=1, grad_fmt=gf, bf16=bf16)
         dt = time.perf_counter() - t0
-    sub = synth.Workload(w.name, tokens, w.d, w.f, w.x_kind, w.x_scale, w.outlier_frac, w.outlier_mult,
-                         w.w_std, w.dy_std, w.qkv)
-    return {"value": sub.gemm_flops() / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-            "seconds": round(dt, 2), "tokens_per_s": tokens / dt,
+    import dataclasses
+    sub = dataclasses.replace(w, T=tokens, seq_len=tokens if w.n_heads else 0)
+    core_note = f"; attention over one sequence of {tokens} tokens" if w.n_heads else ""
+    return {"value": (sub.gemm_flops() + sub.attention_flops()) / dt / 1e12, "unit": "TFLOP/s", "cores": 1,
+            "kind": "oracle", "seconds": round(dt, 2), "tokens_per_s": tokens / dt,
             "sample": f"{tokens} of {w.T} tokens of {w.name} with the full weights "
-                      f"({'forward+backward' if w.backward else 'forward'}), single-threaded oracle"}
+                      f"({'forward+backward' if w.backward else 'forward'}{core_note}), single-threaded oracle"}
 
 
 def measure_fp8_peak():
@@ -442,7 +466,9 @@ def main():
         t0 = time.perf_counter()
         res = [cpu_baseline(w, tokens, args.grad_e4m3, args.bf16) for _ in range(args.steps)]
         dt = time.perf_counter() - t0
-        sub_flops = w.gemm_flops() * tokens / w.T
+        import dataclasses
+        sub = dataclasses.replace(w, T=tokens, seq_len=tokens if w.n_heads else 0)
+        sub_flops = sub.gemm_flops() + sub.attention_flops()  # the work the sample does
         value = sub_flops * args.steps / dt / 1e12
         line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
@@ -472,7 +498,7 @@ def main():
     gemm = {k: v for k, v in kernels.items() if k.startswith("gemm")}
     g_ms = sum(v["total_ms"] for v in gemm.values())
     g_launch = sum(v["launches"] for v in gemm.values())
-    g_flops = sum(fl for (_, _, fl) in r["plan"]) * r["K"]
+    g_flops = sum(fl for (name, _, fl) in r["plan"] if name.startswith("gemm")) * r["K"]
     achieved = g_flops / (g_ms * 1e-3) / 1e12
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "gemm_traffic.json")
@@ -491,6 +517,7 @@ def main():
         "dtype": "bf16 (bf16 operands, fp32 accumulation)" if args.bf16 else "fp8 (e4m3/e5m2 operands, fp32 accumulation)",
         "data": "synthetic (seeded Philox, bf16 inputs)",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "f": w.f, "gemm_flops_per_step": w.gemm_flops(),
+                   "attention_flops_per_step": w.attention_flops(),
                    "backward": "recompute H and a8 from n8 with the retained scale" if args.recompute else "stored H and a8",
                    "gradients": "bf16" if args.bf16 else ("e4m3" if args.grad_e4m3 else "e5m2"),
                    "precision": "bf16 baseline" if args.bf16 else "fp8",

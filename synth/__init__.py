@@ -20,6 +20,8 @@ gradients):
   7b-mlp-fwd-bwd       T=8192,  d=3584, f=18944  forward+backward, 1% outlier channels x20
   14b-mlp-fwd-bwd      T=8192,  d=5120, f=13824  forward+backward, x = 0.5 * Student-t(4)
   32b-block-fwd-bwd    T=16384, d=5120, f=27648  forward+backward, QKV 7168, 0.5% outliers x30
+  32b-block-attn-fwd-bwd  the same block with its attention core computed inside: 40 query heads,
+                       8 K/V heads of 128, 4 sequences of 4096 tokens (causal)
 """
 
 from __future__ import annotations
@@ -46,6 +48,9 @@ class Workload:
     w_std: float
     dy_std: float          # 0: forward only
     qkv: int = 0           # QKV output width (full-block workload), 0: MLP only
+    n_heads: int = 0       # attention core inside the block (0: att / dQKV are given tensors)
+    n_kv_heads: int = 0
+    seq_len: int = 0
 
     @property
     def backward(self) -> bool:
@@ -59,6 +64,15 @@ class Workload:
             per += 2.0 * self.T * self.d * self.qkv + 2.0 * self.T * self.d * self.d
         return per * (3.0 if self.backward else 1.0)
 
+    def attention_flops(self) -> float:
+        """Algorithmic FLOPs of the causal attention core (0 without it): S(S+1)/2 query-key pairs
+        per sequence and head, 2 products (Q K^T, P V) forward and 5 (S, dP, dV, dK, dQ) backward,
+        2 * 128 FLOPs per pair and product."""
+        if not self.n_heads:
+            return 0.0
+        pairs = (self.T // self.seq_len) * self.seq_len * (self.seq_len + 1) / 2
+        return pairs * self.n_heads * 2.0 * 128 * (7 if self.backward else 2)
+
 
 WORKLOADS = [
     Workload("tiny-mlp-fwd", 256, 512, 1408, "normal", 1.0, 0.0, 1.0, 0.02, 0.0),
@@ -66,6 +80,8 @@ WORKLOADS = [
     Workload("7b-mlp-fwd-bwd", 8192, 3584, 18944, "normal", 1.0, 0.01, 20.0, 0.02, 1e-3),
     Workload("14b-mlp-fwd-bwd", 8192, 5120, 13824, "student_t4", 0.5, 0.0, 1.0, 0.015, 1e-3),
     Workload("32b-block-fwd-bwd", 16384, 5120, 27648, "normal", 1.0, 0.005, 30.0, 0.01, 1e-3, qkv=7168),
+    Workload("32b-block-attn-fwd-bwd", 16384, 5120, 27648, "normal", 1.0, 0.005, 30.0, 0.01, 1e-3, qkv=7168,
+             n_heads=40, n_kv_heads=8, seq_len=4096),
 ]
 BY_NAME = {w.name: w for w in WORKLOADS}
 
