@@ -12,15 +12,16 @@
 //   warp 0      TMA producer: the Q tile once, K and V tiles of 128 keys into a
 //               2-stage ring (128 x 128 bf16 tiles as two 64-element-wide
 //               128-byte-swizzled boxes);
-//   warp 1      MMA issuer: S_j = Q K_j^T into one of two TMEM buffers, then
-//               O_j = P_j V_j into a third (V is the MN-major operand);
+//   warp 1      MMA issuer: S_j = Q K_j^T into one of two TMEM buffers, and one
+//               step behind O += P_{j-1} V_{j-1} into a third (V MN-major);
 //   warp 2      TMEM allocation (512 columns);
-//   warps 4..7  softmax, one thread per query row (TMEM lane): row max of S_j
-//               (scores pre-multiplied by log2(e)/sqrt(128)), p = 2^(s - m),
-//               P_j as bf16 into a swizzled shared tile for the second MMA,
-//               the running sum, and O in registers, O = O 2^(m_old - m) + O_j;
-//               at the end O / l goes out through the Q tile with TMA stores
-//               and lse = ln 2 (m + log2 l).
+//   warps 4..7  softmax, one thread per query row (TMEM lane): S_j read once into
+//               registers (scores times log2(e)/sqrt(128)), p = 2^(s - m_ref) as bf16
+//               into one of two swizzled shared P tiles, the running sum l; the
+//               reference max m_ref moves (and O in TMEM is rescaled) only when a
+//               tile's max exceeds it by more than 8, so most steps touch only S;
+//               at the end O / l goes out through the Q tile with TMA stores and
+//               lse = ln 2 (m_ref + log2 l).
 // Backward (dO = d_att), three kernels:
 //   k_attn_bwd_delta  D = rowsum(dO * O) over the stored att, and lse in the
 //                     log2 domain, per (token, head);
@@ -54,8 +55,8 @@ constexpr int kTmemCols = 512;
 constexpr int kFQ = 0;
 constexpr int kFK = kFQ + kTile;         // [2] stages
 constexpr int kFV = kFK + 2 * kTile;     // [2] stages
-constexpr int kFP = kFV + 2 * kTile;
-constexpr int kFBar = kFP + kTile;
+constexpr int kFP = kFV + 2 * kTile;     // [2] P buffers
+constexpr int kFBar = kFP + 2 * kTile;
 constexpr int kFwdSmem = kFBar + 256 + 1024;
 static_assert(kFwdSmem <= 232448, "shared memory per CTA");
 
@@ -90,6 +91,12 @@ __device__ __forceinline__ void mma_tile_kmn(uint32_t d, uint32_t a, uint32_t b,
     umma_bf16(d, smem_desc_sw128(a + aoff, 16, 1024), smem_desc_sw128(b + kk * 2048, kAtom, 1024),
               idesc_bf16_128(1), (accumulate || kk) ? 1u : 0u);
   }
+}
+
+// A wait in the warps that use warp-collective tcgen05.ld/st: every lane waits, and the whole
+// warp goes on only if every lane's wait succeeded (so a time-out leaves the warp together).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort)) != 0;
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -128,6 +135,24 @@ __device__ __forceinline__ void bulk_commit_and_wait() {
 // ---------------------------------------------------------------------------
 // Forward
 // ---------------------------------------------------------------------------
+// 32 consecutive fp32 columns of this thread's TMEM lane from registers, then the wait.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+// A row's reference maximum (log2 domain) moves only when a tile's maximum exceeds it by more
+// than this: the probabilities 2^(s - m_ref) then stay below 2^8 (exact in fp32, in bf16's range)
+// and O, accumulated by the tensor core in TMEM, is rescaled only on those rare steps.
+constexpr float kRescaleSlack = 8.0f;
+
 __global__ void __launch_bounds__(kAttnThreads, 1)
     k_attn_fwd(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmAtt,
                const AttnArgs p) {
@@ -139,12 +164,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* kv_empty = bars + 3;   // [2]
   uint64_t* s_full = bars + 5;     // [2]
   uint64_t* s_free = bars + 7;     // [2]
-  uint64_t* p_full = bars + 9;
-  uint64_t* p_free = bars + 10;
-  uint64_t* o_full = bars + 11;
-  uint64_t* o_free = bars + 12;
-  uint64_t* drain = bars + 13;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  uint64_t* p_full = bars + 9;     // [2]
+  uint64_t* p_free = bars + 11;    // [2]
+  uint64_t* o_full = bars + 13;    // one phase per P V product
+  uint64_t* drain = bars + 14;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int qt = p.n_qt - 1 - (int)blockIdx.x;  // the longest rows first
@@ -161,11 +185,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(&kv_empty[s], 1);
       mbar_init(&s_full[s], 1);
       mbar_init(&s_free[s], 128);
+      mbar_init(&p_full[s], 128);
+      mbar_init(&p_free[s], 1);
     }
-    mbar_init(p_full, 128);
-    mbar_init(p_free, 1);
     mbar_init(o_full, 1);
-    mbar_init(o_free, 128);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -216,7 +239,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---------------- MMA issuer ----------------
+      // ---------------- MMA issuer: S_j, then (one step behind) O += P_{j-1} V_{j-1} ----------------
       const uint32_t tS = tmem, tO = tmem + 256;
       bool ok = mbar_wait(q_full, 0, abort_flag);
       for (int j = 0; j <= n && ok; ++j) {
@@ -232,17 +255,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           umma_commit(&s_full[st]);
         }
         if (j >= 1) {
-          const int i = j - 1, st = i & 1;
-          const uint32_t par = (uint32_t)i & 1u;
-          if (!mbar_wait(p_full, par, abort_flag) || !mbar_wait(o_free, par ^ 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
+          const int i = j - 1, pb = i & 1;
+          if (!mbar_wait(&p_full[pb], (uint32_t)(i >> 1) & 1u, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          mma_tile_kmn(tO, sbase + kFP, sbase + kFV + st * kTile, false);
+          mma_tile_kmn(tO, sbase + kFP + pb * kTile, sbase + kFV + (i & 1) * kTile, i > 0);
           umma_commit(o_full);
-          umma_commit(p_free);
-          umma_commit(&kv_empty[st]);
+          umma_commit(&p_free[pb]);
+          umma_commit(&kv_empty[i & 1]);
         }
       }
       if (!ok) {
@@ -254,85 +273,92 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_wait(drain, 0, &dummy);
     }
   } else if (warp >= 4) {
-    // ---------------- softmax + O ----------------
-    const int r = threadIdx.x - 128;  // query row of the tile = TMEM lane
+    // ---------------- softmax (one query row per thread) ----------------
+    const int r = threadIdx.x - 128;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off, tO = tmem + 256 + lane_off;
-    float o[kDh];
-#pragma unroll
-    for (int c = 0; c < kDh; ++c) o[c] = 0.0f;
-    float m = -INFINITY, l = 0.0f;
+    float m_ref = -INFINITY, l = 0.0f;
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      const int st = j & 1;
+    for (int j = 0; j < n && ok; ++j) {
+      const int st = j & 1, pb = j & 1;
       const uint32_t u = (uint32_t)(j >> 1) & 1u;
       const bool diag = j == qt;
-      if (!mbar_wait(&s_full[st], u, abort_flag)) { ok = false; break; }
+      if (!warp_wait(&s_full[st], u, abort_flag)) { ok = false; break; }
       tc_fence_after();
+      float sv[128];
       float mx = -INFINITY;
-#pragma unroll 1
+#pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t sv[32];
-        tmem_ld32(tS + st * 128 + c * 32, sv);
+        uint32_t w[32];
+        tmem_ld32(tS + st * 128 + c * 32, w);
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const float s = __uint_as_float(sv[k]) * p.scale_log2;
-          if (!(diag && c * 32 + k > r)) mx = fmaxf(mx, s);
+          const float x = (diag && c * 32 + k > r) ? -INFINITY : __uint_as_float(w[k]) * p.scale_log2;
+          sv[c * 32 + k] = x;
+          mx = fmaxf(mx, x);
         }
       }
-      const float m_new = fmaxf(m, mx);
-      const float alpha = ex2_approx(m - m_new);
-      if (!mbar_wait(p_free, ((uint32_t)j & 1u) ^ 1u, abort_flag)) { ok = false; break; }
-      float rs = 0.0f;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sv[32], w[16];
-        tmem_ld32(tS + st * 128 + c * 32, sv);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int c0 = c * 32 + 2 * k;
-          const float p0 = (diag && c0 > r) ? 0.0f : ex2_approx(__uint_as_float(sv[2 * k]) * p.scale_log2 - m_new);
-          const float p1 =
-              (diag && c0 + 1 > r) ? 0.0f : ex2_approx(__uint_as_float(sv[2 * k + 1]) * p.scale_log2 - m_new);
-          rs += p0 + p1;
-          w[k] = pack_bf16x2(p0, p1);
-        }
-        tile_put32(sbase + kFP, r, c, w);
-      }
+      // S_j is in registers: the MMA may overwrite this buffer with S_{j+2}
       tc_fence_before();
       mbar_arrive(&s_free[st]);
-      fence_async_shared();
-      mbar_arrive(p_full);
-      l = l * alpha + rs;
-      m = m_new;
-      if (!mbar_wait(o_full, (uint32_t)j & 1u, abort_flag)) { ok = false; break; }
-      tc_fence_after();
+      if (__any_sync(0xFFFFFFFFu, mx > m_ref + kRescaleSlack)) {
+        const float m_new = fmaxf(m_ref, mx);
+        const float alpha = ex2_approx(m_ref - m_new);  // 0 on the first tile, 1 where nothing moves
+        if (j > 0) {
+          // O holds the products up to j-1: wait for the last one, then rescale this lane's row
+          if (!warp_wait(o_full, (uint32_t)(j - 1) & 1u, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t w[32];
+            tmem_ld32(tO + c * 32, w);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t ov[32];
-        tmem_ld32(tO + c * 32, ov);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) o[c * 32 + k] = fmaf(o[c * 32 + k], alpha, __uint_as_float(ov[k]));
+            for (int k = 0; k < 32; ++k) w[k] = __float_as_uint(__uint_as_float(w[k]) * alpha);
+            tmem_st32(tO + c * 32, w);
+          }
+        }
+        l *= alpha;
+        m_ref = m_new;
       }
-      tc_fence_before();
-      mbar_arrive(o_free);
-    }
-    if (!ok) {
-      atomicOr(p.status, kStatusTimeout);
-      *abort_flag = 1;
-    }
-    // O / l goes out through the Q tile: every S MMA (the tile's readers) has completed once
-    // the last s_full was seen.  Each of the 128 threads reaches the named barrier once.
-    if (ok) {
-      const float inv = 1.0f / l;  // l >= 1: the row maximum contributes 2^0
+      if (!warp_wait(&p_free[pb], u ^ 1u, abort_flag)) { ok = false; break; }
+      float rs = 0.0f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t w[16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(o[c * 32 + 2 * k] * inv, o[c * 32 + 2 * k + 1] * inv);
+        for (int k = 0; k < 16; ++k) {
+          const float p0 = ex2_approx(sv[c * 32 + 2 * k] - m_ref);  // 2^-inf = 0 for masked keys
+          const float p1 = ex2_approx(sv[c * 32 + 2 * k + 1] - m_ref);
+          rs += p0 + p1;
+          w[k] = pack_bf16x2(p0, p1);
+        }
+        tile_put32(sbase + kFP + pb * kTile, r, c, w);
+      }
+      l += rs;
+      tc_fence_before();
+      fence_async_shared();
+      mbar_arrive(&p_full[pb]);
+    }
+    if (ok && !warp_wait(o_full, (uint32_t)(n - 1) & 1u, abort_flag)) ok = false;
+    if (!ok) {
+      atomicOr(p.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
+    // O / l goes out through the Q tile: every MMA (the tile's readers) has completed once the
+    // last product was seen.  Each of the 128 threads reaches the named barrier once.
+    if (ok) {
+      tc_fence_after();
+      const float inv = 1.0f / l;  // l >= 1: the row's maximum M contributes 2^(M - m_ref) >= 1
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t ov[32], w[16];
+        tmem_ld32(tO + c * 32, ov);
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          w[k] = pack_bf16x2(__uint_as_float(ov[2 * k]) * inv, __uint_as_float(ov[2 * k + 1]) * inv);
         tile_put32(sbase + kFQ, r, c, w);
       }
-      p.lse[(int64_t)h * p.T + t0 + r] = (m + log2f(l)) * 0.693147180559945309f;
+      p.lse[(int64_t)h * p.T + t0 + r] = (m_ref + log2f(l)) * 0.693147180559945309f;
     }
     fence_async_shared();
     named_bar_sync(1, 128);
@@ -342,6 +368,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       bulk_commit_and_wait();
     }
   }
+  tc_fence_before();
   __syncthreads();
   if (warp == 2) tmem_dealloc(tmem, kTmemCols);
 }
@@ -528,8 +555,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const uint32_t par = (uint32_t)u & 1u;
       const bool diag = (u % nq_tiles) == 0;  // query tile jt: mask queries before this key
       // qdo_full: this thread reads the lse2 / delta vectors that arrived with the Q/dO tiles
-      if (!mbar_wait(qdo_full, par, abort_flag) || !mbar_wait(s_full, par, abort_flag) ||
-          !mbar_wait(p_free, par ^ 1u, abort_flag)) {
+      if (!warp_wait(qdo_full, par, abort_flag) || !warp_wait(s_full, par, abort_flag) ||
+          !warp_wait(p_free, par ^ 1u, abort_flag)) {
         ok = false;
         break;
       }
@@ -561,7 +588,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       fence_async_shared();
       mbar_arrive(p_full);
     }
-    if (ok && !mbar_wait(acc_full, 0, abort_flag)) ok = false;
+    if (ok && !warp_wait(acc_full, 0, abort_flag)) ok = false;
     if (!ok) {
       atomicOr(p.status, kStatusTimeout);
       *abort_flag = 1;
@@ -733,7 +760,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int j = 0; j < n; ++j) {
       const uint32_t par = (uint32_t)j & 1u;
       const bool diag = j == qt;
-      if (!mbar_wait(s_full, par, abort_flag) || !mbar_wait(ds_free, par ^ 1u, abort_flag)) {
+      if (!warp_wait(s_full, par, abort_flag) || !warp_wait(ds_free, par ^ 1u, abort_flag)) {
         ok = false;
         break;
       }
@@ -762,7 +789,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       fence_async_shared();
       mbar_arrive(ds_full);
     }
-    if (ok && !mbar_wait(acc_full, 0, abort_flag)) ok = false;
+    if (ok && !warp_wait(acc_full, 0, abort_flag)) ok = false;
     if (!ok) {
       atomicOr(p.status, kStatusTimeout);
       *abort_flag = 1;

@@ -355,7 +355,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
       int mb, nb;
       tile_coords(tile, p, mb, nb);
-      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) {
+      // lane 0 waits and the warp follows its result: the tcgen05.ld below is warp-collective,
+      // so a time-out must take the whole warp out together
+      int full_ok = 0;
+      if (lane == 0) full_ok = mbar_wait(&tfull[acc], acc_phase, abort_flag) ? 1 : 0;
+      if (!__shfl_sync(0xFFFFFFFFu, full_ok, 0)) {
         atomicOr(p.status, kStatusTimeout);
         *abort_flag = 1;
         break;
@@ -374,15 +378,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32x2(tbase + c * 32, tbase + 128 + c * 32, ag, au);
           const int col = col0 + c * 32;
           const int ncol = min(32, p.N - col);
-          float hg[32], hu[32], a[32];
+          float hg[32], hu[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             // H = bf16 of the fp32 product (two roundings: its cost in this epilogue-bound
             // GEMM outweighs the rare last-bit difference from one rounding)
             hg[j] = round_bf16(__fmul_rn(alpha, __uint_as_float(ag[j])));
             hu[j] = round_bf16(__fmul_rn(alpha, __uint_as_float(au[j])));
-            a[j] = swiglu_fast(hg[j], hu[j]);
-            if (row_ok && j < ncol) amax = max(amax, abs_bits(a[j]));
           }
           if (warp_ok && ncol > 0) {
             staging_acquire(lane);
@@ -394,30 +396,40 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_store_2d(&tmC2, buf + 2048, col, row0);
               bulk_commit();
             }
-            if (p.aux16) {
-              staging_acquire(lane);
-              stage_bf16(buf, lane, a);
-              staging_publish();
-              if (lane == 0) {
-                tma_store_2d(&tmAux, buf, col, row0);
-                bulk_commit();
-              }
-            } else if (p.qscale) {
-              // recomputation with the retained scale: SwiGLU fused with the E4M3 cast
-              const float sq = *p.qscale;
-              uint32_t w[8];
+          }
+          if (p.aux16 || p.qscale) {
+            // a = SwiGLU(H) is written too: bf16 (the BF16 baseline) or, recomputing with the
+            // retained scale, as E4M3 codes (SwiGLU fused with the cast)
+            float a[32];
 #pragma unroll
-              for (int q = 0; q < 8; ++q)
-                w[q] = cvt_fp8x4<0>(__fmul_rn(a[4 * q], sq), __fmul_rn(a[4 * q + 1], sq), __fmul_rn(a[4 * q + 2], sq),
-                                    __fmul_rn(a[4 * q + 3], sq));
+            for (int j = 0; j < 32; ++j) {
+              a[j] = swiglu_fast(hg[j], hu[j]);
+              if (row_ok && j < ncol) amax = max(amax, abs_bits(a[j]));
+            }
+            if (warp_ok && ncol > 0) {
               staging_acquire(lane);
-              stage_u8(buf, lane, w);
+              if (p.aux16) {
+                stage_bf16(buf, lane, a);
+              } else {
+                const float sq = *p.qscale;
+                uint32_t w[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                  w[q] = cvt_fp8x4<0>(__fmul_rn(a[4 * q], sq), __fmul_rn(a[4 * q + 1], sq),
+                                      __fmul_rn(a[4 * q + 2], sq), __fmul_rn(a[4 * q + 3], sq));
+                stage_u8(buf, lane, w);
+              }
               staging_publish();
               if (lane == 0) {
                 tma_store_2d(&tmAux, buf, col, row0);
                 bulk_commit();
               }
             }
+          } else {
+            // only the absmax of a (the cast pass recomputes a from the stored H)
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (row_ok && j < ncol) amax = max(amax, abs_bits(swiglu_fast(hg[j], hu[j])));
           }
         }
       } else if (p.epi == kEpiSwigluBwd) {
