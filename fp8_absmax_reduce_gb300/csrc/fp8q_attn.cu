@@ -57,7 +57,7 @@ constexpr int kFK = kFQ + kTile;         // [2] stages
 constexpr int kFV = kFK + 2 * kTile;     // [2] stages
 constexpr int kFP = kFV + 2 * kTile;     // [2] P buffers
 constexpr int kFBar = kFP + 2 * kTile;
-constexpr int kFwdSmem = kFBar + 256 + 1024;
+constexpr int kFwdSmem = kFBar + 256 + 1024;  // 19 barriers, the TMEM slot and the abort flag fit in 256 B
 static_assert(kFwdSmem <= 232448, "shared memory per CTA");
 
 struct AttnArgs {
@@ -153,6 +153,29 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 // and O, accumulated by the tensor core in TMEM, is rescaled only on those rare steps.
 constexpr float kRescaleSlack = 8.0f;
 
+// S row of this thread (128 scores, times log2(e)/sqrt(128)) into registers and its maximum.
+// MASK (the diagonal tile): keys after the query row r become -inf.  Eight partial maxima keep
+// the reduction's dependency chain short.
+template <bool MASK>
+__device__ __forceinline__ float load_scores(uint32_t tS, int r, float scale_log2, float (&sv)[128]) {
+  float mp[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t w[32];
+    tmem_ld32(tS + c * 32, w);
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      float x = __uint_as_float(w[k]) * scale_log2;
+      if (MASK && c * 32 + k > r) x = -INFINITY;
+      sv[c * 32 + k] = x;
+      mp[k & 7] = fmaxf(mp[k & 7], x);
+    }
+  }
+  return fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+}
+
 __global__ void __launch_bounds__(kAttnThreads, 1)
     k_attn_fwd(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmAtt,
                const AttnArgs p) {
@@ -160,15 +183,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kFBar);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;    // [2]
-  uint64_t* kv_empty = bars + 3;   // [2]
+  uint64_t* k_full = bars + 1;     // [2]
+  uint64_t* k_empty = bars + 3;    // [2] K_j is free once S_j is computed
   uint64_t* s_full = bars + 5;     // [2]
   uint64_t* s_free = bars + 7;     // [2]
   uint64_t* p_full = bars + 9;     // [2]
   uint64_t* p_free = bars + 11;    // [2]
   uint64_t* o_full = bars + 13;    // one phase per P V product
   uint64_t* drain = bars + 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  uint64_t* v_full = bars + 15;    // [2]
+  uint64_t* v_empty = bars + 17;   // [2] V_j is free once P_j V_j is computed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int qt = p.n_qt - 1 - (int)blockIdx.x;  // the longest rows first
@@ -181,8 +206,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
       mbar_init(&s_full[s], 1);
       mbar_init(&s_free[s], 128);
       mbar_init(&p_full[s], 128);
@@ -208,7 +235,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (lane == 0) {
       // ---------------- TMA producer ----------------
       bool ok = true;
-      uint32_t issued = 0, issued_par = 0;  // kv stages with a load in flight, and its phase parity
+      // K and V stages with a load in flight, and its phase parity (bits 0-1: K, 2-3: V)
+      uint32_t issued = 0, issued_par = 0;
       mbar_arrive_expect_tx(q_full, kTile);
       tma_load_2d(smem + kFQ, &tmQKV, q_full, h * kDh, t0);
       tma_load_2d(smem + kFQ + kAtom, &tmQKV, q_full, h * kDh + 64, t0);
@@ -216,25 +244,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int j = 0; j < n; ++j) {
         const int st = j & 1;
         const uint32_t u = (uint32_t)(j >> 1) & 1u;
-        if (!mbar_wait(&kv_empty[st], u ^ 1u, abort_flag)) { ok = false; break; }
-        uint8_t* sk = smem + kFK + st * kTile;
-        uint8_t* sv = smem + kFV + st * kTile;
         const int y = b * p.S + j * 128;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * kTile);
-        tma_load_2d(sk, &tmQKV, &kv_full[st], xk, y);
-        tma_load_2d(sk + kAtom, &tmQKV, &kv_full[st], xk + 64, y);
-        tma_load_2d(sv, &tmQKV, &kv_full[st], xv, y);
-        tma_load_2d(sv + kAtom, &tmQKV, &kv_full[st], xv + 64, y);
+        if (!mbar_wait(&k_empty[st], u ^ 1u, abort_flag)) { ok = false; break; }
+        uint8_t* sk = smem + kFK + st * kTile;
+        mbar_arrive_expect_tx(&k_full[st], kTile);
+        tma_load_2d(sk, &tmQKV, &k_full[st], xk, y);
+        tma_load_2d(sk + kAtom, &tmQKV, &k_full[st], xk + 64, y);
         issued |= 1u << st;
         issued_par = (issued_par & ~(1u << st)) | (u << st);
+        if (!mbar_wait(&v_empty[st], u ^ 1u, abort_flag)) { ok = false; break; }
+        uint8_t* sv = smem + kFV + st * kTile;
+        mbar_arrive_expect_tx(&v_full[st], kTile);
+        tma_load_2d(sv, &tmQKV, &v_full[st], xv, y);
+        tma_load_2d(sv + kAtom, &tmQKV, &v_full[st], xv + 64, y);
+        issued |= 4u << st;
+        issued_par = (issued_par & ~(4u << st)) | (u << (st + 2));
       }
       if (!ok) {
         atomicOr(p.status, kStatusTimeout);
         *abort_flag = 1;
         int dummy = 0;
         mbar_wait(q_full, 0, &dummy);
-        for (int s = 0; s < 2; ++s)
-          if (issued & (1u << s)) mbar_wait(&kv_full[s], (issued_par >> s) & 1u, &dummy);
+        for (int s = 0; s < 2; ++s) {
+          if (issued & (1u << s)) mbar_wait(&k_full[s], (issued_par >> s) & 1u, &dummy);
+          if (issued & (4u << s)) mbar_wait(&v_full[s], (issued_par >> (s + 2)) & 1u, &dummy);
+        }
       }
     }
   } else if (warp == 1) {
@@ -246,22 +280,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (j < n) {
           const int st = j & 1;
           const uint32_t u = (uint32_t)(j >> 1) & 1u;
-          if (!mbar_wait(&kv_full[st], u, abort_flag) || !mbar_wait(&s_free[st], u ^ 1u, abort_flag)) {
+          if (!mbar_wait(&k_full[st], u, abort_flag) || !mbar_wait(&s_free[st], u ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           mma_tile_kk(tS + st * 128, sbase + kFQ, sbase + kFK + st * kTile, false);
           umma_commit(&s_full[st]);
+          umma_commit(&k_empty[st]);
         }
         if (j >= 1) {
           const int i = j - 1, pb = i & 1;
-          if (!mbar_wait(&p_full[pb], (uint32_t)(i >> 1) & 1u, abort_flag)) { ok = false; break; }
+          const uint32_t ui = (uint32_t)(i >> 1) & 1u;
+          if (!mbar_wait(&p_full[pb], ui, abort_flag) || !mbar_wait(&v_full[i & 1], ui, abort_flag)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           mma_tile_kmn(tO, sbase + kFP + pb * kTile, sbase + kFV + (i & 1) * kTile, i > 0);
           umma_commit(o_full);
           umma_commit(&p_free[pb]);
-          umma_commit(&kv_empty[i & 1]);
+          umma_commit(&v_empty[i & 1]);
         }
       }
       if (!ok) {
@@ -286,18 +325,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!warp_wait(&s_full[st], u, abort_flag)) { ok = false; break; }
       tc_fence_after();
       float sv[128];
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t w[32];
-        tmem_ld32(tS + st * 128 + c * 32, w);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float x = (diag && c * 32 + k > r) ? -INFINITY : __uint_as_float(w[k]) * p.scale_log2;
-          sv[c * 32 + k] = x;
-          mx = fmaxf(mx, x);
-        }
-      }
+      const float mx = diag ? load_scores<true>(tS + st * 128, r, p.scale_log2, sv)
+                            : load_scores<false>(tS + st * 128, r, p.scale_log2, sv);
       // S_j is in registers: the MMA may overwrite this buffer with S_{j+2}
       tc_fence_before();
       mbar_arrive(&s_free[st]);
@@ -321,7 +350,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         m_ref = m_new;
       }
       if (!warp_wait(&p_free[pb], u ^ 1u, abort_flag)) { ok = false; break; }
-      float rs = 0.0f;
+      float rp[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) rp[i] = 0.0f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t w[16];
@@ -329,12 +360,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int k = 0; k < 16; ++k) {
           const float p0 = ex2_approx(sv[c * 32 + 2 * k] - m_ref);  // 2^-inf = 0 for masked keys
           const float p1 = ex2_approx(sv[c * 32 + 2 * k + 1] - m_ref);
-          rs += p0 + p1;
+          rp[(2 * k) & 7] += p0;
+          rp[(2 * k + 1) & 7] += p1;
           w[k] = pack_bf16x2(p0, p1);
         }
         tile_put32(sbase + kFP + pb * kTile, r, c, w);
       }
-      l += rs;
+      l += ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
       tc_fence_before();
       fence_async_shared();
       mbar_arrive(&p_full[pb]);
@@ -415,6 +447,43 @@ __global__ void __launch_bounds__(256) k_attn_bwd_delta(const uint16_t* __restri
   if (lane == 0) {
     delta[(int64_t)h * T + t] = v;
     lse2[(int64_t)h * T + t] = lse[(int64_t)h * T + t] * 1.44269504088896341f;
+  }
+}
+
+// 32 columns of a dS row (bf16 pairs) from the S and dP columns: P = 2^(s scale - lse2),
+// dS = P (dP - D).  dQ (per row lse2, D): MASK drops keys after the query row r.  dK/dV
+// (per column lse2, D from shared memory): MASK drops queries before the key row r.
+template <bool MASK>
+__device__ __forceinline__ void ds_row_chunk(const uint32_t (&sv)[32], const uint32_t (&dv)[32], int c, int r,
+                                             float scale_log2, float lse2, float dlt, uint32_t (&w)[16]) {
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    float dd[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int col = c * 32 + 2 * k + e;
+      const float pp = (MASK && col > r) ? 0.0f : ex2_approx(__uint_as_float(sv[2 * k + e]) * scale_log2 - lse2);
+      dd[e] = pp * (__uint_as_float(dv[2 * k + e]) - dlt);
+    }
+    w[k] = pack_bf16x2(dd[0], dd[1]);
+  }
+}
+template <bool MASK>
+__device__ __forceinline__ void pds_col_chunk(const uint32_t (&sv)[32], const uint32_t (&dv)[32], int c, int r,
+                                              float scale_log2, const float* lse2, const float* dlt,
+                                              uint32_t (&wp)[16], uint32_t (&ws)[16]) {
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    float pp[2], dd[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int col = c * 32 + 2 * k + e;
+      const float pt = (MASK && col < r) ? 0.0f : ex2_approx(__uint_as_float(sv[2 * k + e]) * scale_log2 - lse2[col]);
+      pp[e] = pt;
+      dd[e] = pt * (__uint_as_float(dv[2 * k + e]) - dlt[col]);
+    }
+    wp[k] = pack_bf16x2(pp[0], pp[1]);
+    ws[k] = pack_bf16x2(dd[0], dd[1]);
   }
 }
 
@@ -566,20 +635,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         uint32_t sv[32], dv[32], wp[16], ws[16];
         tmem_ld32(tSt + c * 32, sv);
         tmem_ld32(tdPt + c * 32, dv);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          float pp[2], dd[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = c * 32 + 2 * k + e;
-            const float pt = (diag && col < r) ? 0.0f
-                                               : ex2_approx(__uint_as_float(sv[2 * k + e]) * p.scale_log2 - v_lse2[col]);
-            pp[e] = pt;
-            dd[e] = pt * (__uint_as_float(dv[2 * k + e]) - v_delta[col]);
-          }
-          wp[k] = pack_bf16x2(pp[0], pp[1]);
-          ws[k] = pack_bf16x2(dd[0], dd[1]);
-        }
+        if (diag) pds_col_chunk<true>(sv, dv, c, r, p.scale_log2, v_lse2, v_delta, wp, ws);
+        else pds_col_chunk<false>(sv, dv, c, r, p.scale_log2, v_lse2, v_delta, wp, ws);
         tile_put32(sbase + kKPT, r, c, wp);
         tile_put32(sbase + kKDST, r, c, ws);
       }
@@ -770,18 +827,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         uint32_t sv[32], dv[32], w[16];
         tmem_ld32(tS + c * 32, sv);
         tmem_ld32(tdP + c * 32, dv);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          float dd[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = c * 32 + 2 * k + e;
-            const float pp =
-                (diag && col > r) ? 0.0f : ex2_approx(__uint_as_float(sv[2 * k + e]) * p.scale_log2 - lse2);
-            dd[e] = pp * (__uint_as_float(dv[2 * k + e]) - dlt);
-          }
-          w[k] = pack_bf16x2(dd[0], dd[1]);
-        }
+        if (diag) ds_row_chunk<true>(sv, dv, c, r, p.scale_log2, lse2, dlt, w);
+        else ds_row_chunk<false>(sv, dv, c, r, p.scale_log2, lse2, dlt, w);
         tile_put32(sbase + kQDS, r, c, w);
       }
       tc_fence_before();
