@@ -53,6 +53,8 @@ def _load() -> ctypes.CDLL:
     L.attention_bwd_workspace_size.argtypes = [i64, i32]
     L.attention_bwd.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, i32, vp, vp, sz, vp]
     L.mlp_block_bwd.argtypes = [ctypes.POINTER(FP8QMlp), vp, sz, vp]
+    L.mlp_block_run_steps.argtypes = [ctypes.POINTER(FP8QMlp), ctypes.POINTER(FP8QMlp), ctypes.POINTER(FP8QMlpHostIO),
+                                      i32, vp, sz, vp]
     L.fp8q_get_status.argtypes = [i32]
     L.fp8q_status_string.restype = ctypes.c_char_p
     L.fp8q_status_string.argtypes = [i32]
@@ -79,6 +81,11 @@ class FP8QMlp(ctypes.Structure):
                 + [(name, ctypes.c_void_p) for name in _MLP_PTRS]
                 + [("recompute", ctypes.c_int), ("grad_e4m3", ctypes.c_int), ("bf16", ctypes.c_int),
                    ("n16", ctypes.c_void_p), ("a16", ctypes.c_void_p)])
+
+
+class FP8QMlpHostIO(ctypes.Structure):
+    """Mirror of ``fp8q_mlp_host_io`` in include/fp8q.h."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("x", "g", "W_gu", "W_d", "dY", "y", "dX", "dW_gu", "dW_d", "dg")]
 
 
 class FP8QBlock(ctypes.Structure):
@@ -323,6 +330,20 @@ def mlp_block_fwd(b: MlpBuffers, stream=None):
 def mlp_block_bwd(b: MlpBuffers, stream=None):
     s = b.struct()
     _check("mlp_block_bwd", lib.mlp_block_bwd(ctypes.byref(s), _ptr(b.ws), b.ws.numel(), _stream(stream)))
+
+
+def mlp_block_run_steps(b0: MlpBuffers, b1: MlpBuffers, host: list, stream=None):
+    """Pipelined training steps from and to host memory (mlp_block_run_steps in include/fp8q.h).
+    host: one dict per step with CPU tensors x, g, W_gu, W_d, dY (inputs) and y, dX, dW_gu, dW_d,
+    dg (outputs), ideally pinned.  Device sets b0, b1 alternate; b0's workspace is used."""
+    n = len(host)
+    arr = (FP8QMlpHostIO * n)()
+    for i, h in enumerate(host):
+        for name, _ in FP8QMlpHostIO._fields_:
+            setattr(arr[i], name, h[name].data_ptr())
+    s0, s1 = b0.struct(), b1.struct()
+    _check("mlp_block_run_steps", lib.mlp_block_run_steps(ctypes.byref(s0), ctypes.byref(s1), arr, n, _ptr(b0.ws),
+                                                          b0.ws.numel(), _stream(stream)))
 
 
 def get_status(clear: bool = False) -> int:

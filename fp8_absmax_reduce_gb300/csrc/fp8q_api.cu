@@ -799,6 +799,110 @@ int mlp_block_bwd(const fp8q_mlp* m, void* ws, size_t ws_bytes, fp8q_stream stre
 }
 
 // ---------------------------------------------------------------------------
+// Pipelined steps from and to host memory
+// ---------------------------------------------------------------------------
+namespace {
+
+// Two copy streams and the events that order the pipeline, created once per device.
+struct CopyEngines {
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t in_done[2], compute_done[2], out_done[2];
+  bool ready = false;
+};
+
+int copy_engines(CopyEngines** out) {
+  static std::mutex mu;
+  static CopyEngines cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8Q_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  CopyEngines& c = cache[dev];
+  if (!c.ready) {
+    if (cudaStreamCreateWithFlags(&c.h2d, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&c.d2h, cudaStreamNonBlocking) != cudaSuccess)
+      return FP8Q_ERR_CUDA;
+    for (int s = 0; s < 2; ++s)
+      if (cudaEventCreateWithFlags(&c.in_done[s], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&c.compute_done[s], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&c.out_done[s], cudaEventDisableTiming) != cudaSuccess)
+        return FP8Q_ERR_CUDA;
+    c.ready = true;
+  }
+  *out = &c;
+  return FP8Q_OK;
+}
+
+bool same_shape(const fp8q_mlp* a, const fp8q_mlp* b) {
+  return a->T == b->T && a->d == b->d && a->f == b->f && a->recompute == b->recompute &&
+         a->grad_e4m3 == b->grad_e4m3 && a->bf16 == b->bf16;
+}
+
+}  // namespace
+
+int mlp_block_run_steps(const fp8q_mlp* dev0, const fp8q_mlp* dev1, const fp8q_mlp_host_io* host, int n_steps,
+                        void* ws, size_t ws_bytes, fp8q_stream stream) {
+  const fp8q_mlp* dev[2] = {dev0, dev1};
+  int e;
+  for (const fp8q_mlp* m : dev)
+    if ((e = validate_mlp(m, true))) return e;
+  if (!same_shape(dev0, dev1) || !host || n_steps < 1) return FP8Q_ERR_INVALID_ARG;
+  if (dev0->x == dev1->x || dev0->dY == dev1->dY || dev0->W_gu == dev1->W_gu || dev0->W_d == dev1->W_d ||
+      dev0->g == dev1->g || dev0->y == dev1->y || dev0->dX == dev1->dX || dev0->dW_gu == dev1->dW_gu ||
+      dev0->dW_d == dev1->dW_d || dev0->dg == dev1->dg)
+    return FP8Q_ERR_INVALID_ARG;
+  for (int i = 0; i < n_steps; ++i) {
+    const fp8q_mlp_host_io& h = host[i];
+    if (!h.x || !h.g || !h.W_gu || !h.W_d || !h.dY || !h.y || !h.dX || !h.dW_gu || !h.dW_d || !h.dg)
+      return FP8Q_ERR_INVALID_ARG;
+  }
+  if ((e = check_ws(ws, ws_bytes, mlp_block_workspace_size(dev0->T, dev0->d, dev0->f, 1)))) return e;
+  CopyEngines* ce = nullptr;
+  if ((e = copy_engines(&ce))) return e;
+  Ctx c;
+  if ((e = make_ctx(&c, stream))) return e;
+  MlpWs w;
+  mlp_ws_layout(dev0->T, dev0->d, dev0->f, 1, static_cast<uint8_t*>(ws), &w);
+  const size_t T = (size_t)dev0->T, d = (size_t)dev0->d, f = (size_t)dev0->f;
+  cudaStream_t cs = c.L.stream;
+#define FP8Q_CUDA(expr)                                  \
+  do {                                                   \
+    if ((expr) != cudaSuccess) return FP8Q_ERR_CUDA;     \
+  } while (0)
+  for (int i = 0; i < n_steps; ++i) {
+    const int s = i & 1;
+    const fp8q_mlp* m = dev[s];
+    const fp8q_mlp_host_io& h = host[i];
+    // inputs into set s once step i-2 (the set's last user) has finished computing
+    if (i >= 2) FP8Q_CUDA(cudaStreamWaitEvent(ce->h2d, ce->compute_done[s], 0));
+    FP8Q_CUDA(cudaMemcpyAsync((void*)m->x, h.x, T * d * 2, cudaMemcpyHostToDevice, ce->h2d));
+    FP8Q_CUDA(cudaMemcpyAsync((void*)m->g, h.g, d * 2, cudaMemcpyHostToDevice, ce->h2d));
+    FP8Q_CUDA(cudaMemcpyAsync((void*)m->W_gu, h.W_gu, d * 2 * f * 2, cudaMemcpyHostToDevice, ce->h2d));
+    FP8Q_CUDA(cudaMemcpyAsync((void*)m->W_d, h.W_d, f * d * 2, cudaMemcpyHostToDevice, ce->h2d));
+    FP8Q_CUDA(cudaMemcpyAsync((void*)m->dY, h.dY, T * d * 2, cudaMemcpyHostToDevice, ce->h2d));
+    FP8Q_CUDA(cudaEventRecord(ce->in_done[s], ce->h2d));
+    // compute once the inputs are in and step i-2's outputs have left this set
+    FP8Q_CUDA(cudaStreamWaitEvent(cs, ce->in_done[s], 0));
+    if (i >= 2) FP8Q_CUDA(cudaStreamWaitEvent(cs, ce->out_done[s], 0));
+    if ((e = mlp_fwd_run(m, w, c))) return e;
+    if ((e = mlp_bwd_run(m, w, c))) return e;
+    FP8Q_CUDA(cudaEventRecord(ce->compute_done[s], cs));
+    // outputs back to the host
+    FP8Q_CUDA(cudaStreamWaitEvent(ce->d2h, ce->compute_done[s], 0));
+    FP8Q_CUDA(cudaMemcpyAsync(h.y, m->y, T * d * 2, cudaMemcpyDeviceToHost, ce->d2h));
+    FP8Q_CUDA(cudaMemcpyAsync(h.dX, m->dX, T * d * 2, cudaMemcpyDeviceToHost, ce->d2h));
+    FP8Q_CUDA(cudaMemcpyAsync(h.dW_gu, m->dW_gu, d * 2 * f * 4, cudaMemcpyDeviceToHost, ce->d2h));
+    FP8Q_CUDA(cudaMemcpyAsync(h.dW_d, m->dW_d, f * d * 4, cudaMemcpyDeviceToHost, ce->d2h));
+    FP8Q_CUDA(cudaMemcpyAsync(h.dg, m->dg, d * 4, cudaMemcpyDeviceToHost, ce->d2h));
+    FP8Q_CUDA(cudaEventRecord(ce->out_done[s], ce->d2h));
+  }
+  // the caller's stream ends after the last outputs (and every earlier copy) have landed
+  FP8Q_CUDA(cudaStreamWaitEvent(cs, ce->out_done[(n_steps - 1) & 1], 0));
+  if (n_steps >= 2) FP8Q_CUDA(cudaStreamWaitEvent(cs, ce->out_done[n_steps & 1], 0));
+#undef FP8Q_CUDA
+  return finish(c);
+}
+
+// ---------------------------------------------------------------------------
 size_t block_workspace_size(int64_t T, int64_t d, int64_t f, int64_t n_qkv, int backward) {
   return block_ws_layout(T, d, f, n_qkv, backward, nullptr, nullptr);
 }

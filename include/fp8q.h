@@ -230,6 +230,32 @@ FP8Q_API int mlp_block_fwd(const fp8q_mlp* m, void* ws, size_t ws_bytes, fp8q_st
 /* Reads the forward's saved tensors (W_gu8, W_d8, n8, rstd, H, a8, scal[0..3]). */
 FP8Q_API int mlp_block_bwd(const fp8q_mlp* m, void* ws, size_t ws_bytes, fp8q_stream stream);
 
+/* Training steps from and to host memory, pipelined.  Step i copies its inputs (x, g, W_gu, W_d,
+ * dY) from host[i] into device set i % 2 (dev0 or dev1), runs mlp_block_fwd + mlp_block_bwd on
+ * `stream`, and copies the outputs (y, dX, dW_gu, dW_d, dg) back into host[i].  The copies run on
+ * two streams of the library's own, ordered by events, so step i+1's inputs arrive and step
+ * i-1's outputs leave while step i computes; the kernels stay in order on `stream`, so one
+ * workspace serves both sets (mlp_block_workspace_size(T, d, f, 1) bytes).  dev0 and dev1 must
+ * have the same sizes and switches, distinct input and output buffers (their intermediates may
+ * be shared); host buffers should be pinned (pageable memory makes the copies synchronous).
+ * Returns once everything is enqueued; `stream` is ordered after the last copy, so a
+ * synchronisation of `stream` (or an event recorded on it) covers the whole run.  The pages
+ * describe no such runtime; this is the executor a trainer feeding the block from the host uses. */
+typedef struct fp8q_mlp_host_io {
+  const void* x;    /* [T,d]  bf16 */
+  const void* g;    /* [d]    bf16 */
+  const void* W_gu; /* [d,2f] bf16 */
+  const void* W_d;  /* [f,d]  bf16 */
+  const void* dY;   /* [T,d]  bf16 */
+  void* y;          /* [T,d]  bf16 */
+  void* dX;         /* [T,d]  bf16 */
+  float* dW_gu;     /* [d,2f] fp32 */
+  float* dW_d;      /* [f,d]  fp32 */
+  float* dg;        /* [d]    fp32 */
+} fp8q_mlp_host_io;
+FP8Q_API int mlp_block_run_steps(const fp8q_mlp* dev0, const fp8q_mlp* dev1, const fp8q_mlp_host_io* host,
+                                 int n_steps, void* ws, size_t ws_bytes, fp8q_stream stream);
+
 /* ------------------------------------------------------------------------ */
 /* The full transformer block's matmuls around an attention core computed   */
 /* elsewhere (the 32B-class workload): attention-side RMSNorm + QKV         */
