@@ -162,16 +162,19 @@ __device__ __forceinline__ float load_scores(uint32_t tS, int r, float scale_log
 #pragma unroll
   for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t w[32];
-    tmem_ld32(tS + c * 32, w);
+  for (int c2 = 0; c2 < 4; c2 += 2) {
+    uint32_t w[2][32];
+    tmem_ld32x2(tS + c2 * 32, tS + c2 * 32 + 32, w[0], w[1]);
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      float x = __uint_as_float(w[k]) * scale_log2;
-      if (MASK && c * 32 + k > r) x = -INFINITY;
-      sv[c * 32 + k] = x;
-      mp[k & 7] = fmaxf(mp[k & 7], x);
-    }
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const int col = (c2 + h) * 32 + k;
+        float x = __uint_as_float(w[h][k]) * scale_log2;
+        if (MASK && col > r) x = -INFINITY;
+        sv[col] = x;
+        mp[k & 7] = fmaxf(mp[k & 7], x);
+      }
   }
   return fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
 }
@@ -452,7 +455,8 @@ __global__ void __launch_bounds__(256) k_attn_bwd_delta(const uint16_t* __restri
 
 // 32 columns of a dS row (bf16 pairs) from the S and dP columns: P = 2^(s scale - lse2),
 // dS = P (dP - D).  dQ (per row lse2, D): MASK drops keys after the query row r.  dK/dV
-// (per column lse2, D from shared memory): MASK drops queries before the key row r.
+// (per column lse2, D from shared memory): MASK drops the columns before r, which the caller
+// sets to the key row minus the query sub-tile's offset from the key tile.
 template <bool MASK>
 __device__ __forceinline__ void ds_row_chunk(const uint32_t (&sv)[32], const uint32_t (&dv)[32], int c, int r,
                                              float scale_log2, float lse2, float dlt, uint32_t (&w)[16]) {
@@ -487,53 +491,81 @@ __device__ __forceinline__ void pds_col_chunk(const uint32_t (&sv)[32], const ui
   }
 }
 
-// dK, dV shared-memory layout
-constexpr int kKK = 0;
-constexpr int kKV = kKK + kTile;
-constexpr int kKQ = kKV + kTile;
-constexpr int kKO = kKQ + kTile;     // dO tile
-constexpr int kKPT = kKO + kTile;    // P^T tile (bf16, K-major over queries)
-constexpr int kKDST = kKPT + kTile;  // dS^T tile
-constexpr int kKVec = kKDST + kTile; // lse2[128], delta[128] of the current query tile
-constexpr int kKBar = kKVec + 1024;
+// dK, dV: 64-query sub-tiles, so that two S^T / dP^T buffers (128 x 64 fp32 each) fit in TMEM
+// beside the dV and dK accumulators and the Q / dO sub-tiles and the P^T / dS^T operand tiles are
+// double-buffered: the next sub-tile's MMAs run while the current one's element-wise pass does.
+constexpr int kSubAtom = 8192;            // 64 rows x 128 bytes
+constexpr int kSubTile = 2 * kSubAtom;    // 64 x 128 bf16 (Q or dO sub-tile)
+constexpr int kOpTile = 16384;            // 128 x 64 bf16 (P^T or dS^T): one 128-row swizzle atom column
+constexpr int kKK = 0;                    // K tile (128 x 128)
+constexpr int kKV = kKK + kTile;          // V tile
+constexpr int kQdoStages = 3;             // a sub-tile's load starts three items ahead of its use
+constexpr int kKQ = kKV + kTile;          // [3] Q sub-tiles
+constexpr int kKO = kKQ + kQdoStages * kSubTile;  // [3] dO sub-tiles
+constexpr int kKPT = kKO + kQdoStages * kSubTile; // [2] P^T tiles (contiguous: 32 KB staging for dV at the end)
+constexpr int kKDST = kKPT + 2 * kOpTile; // [2] dS^T tiles (the same for dK)
+constexpr int kKVec = kKDST + 2 * kOpTile; // [3] x (lse2[64], delta[64])
+constexpr int kKBar = kKVec + kQdoStages * 512;
 constexpr int kDkdvSmem = kKBar + 256 + 1024;
 static_assert(kDkdvSmem <= 232448, "shared memory per CTA");
 
+__host__ __device__ constexpr uint32_t idesc_bf16_n(int n, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) | (((uint32_t)n >> 3) << 17) | ((128u >> 4) << 24);
+}
+// D (+)= A B^T, K = 128: A a K-major 128-row tile (16 KB atoms), B a K-major 64-row sub-tile (8 KB atoms).
+__device__ __forceinline__ void mma_sub_kk(uint32_t d, uint32_t a, uint32_t b) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    umma_bf16(d, smem_desc_sw128(a + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
+              smem_desc_sw128(b + (kk >> 2) * kSubAtom + (kk & 3) * 32, 16, 1024), idesc_bf16_n(64, 0),
+              kk ? 1u : 0u);
+}
+// D (+)= A B, K = 64: A a K-major 128 x 64 tile (one atom), B an MN-major 64-row sub-tile (N = 128).
+__device__ __forceinline__ void mma_sub_kmn(uint32_t d, uint32_t a, uint32_t b, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+    umma_bf16(d, smem_desc_sw128(a + kk * 32, 16, 1024), smem_desc_sw128(b + kk * 2048, kSubAtom, 1024),
+              idesc_bf16_n(128, 1), (accumulate || kk) ? 1u : 0u);
+}
+
 __global__ void __launch_bounds__(kAttnThreads, 1)
-    k_attn_bwd_dkdv(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmDO,
-                    const __grid_constant__ CUtensorMap tmDQKV, const AttnBwdArgs p) {
+    k_attn_bwd_dkdv(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmQ64,
+                    const __grid_constant__ CUtensorMap tmDO64, const __grid_constant__ CUtensorMap tmDQKV,
+                    const AttnBwdArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kKBar);
   uint64_t* kv_full = bars + 0;
-  uint64_t* qdo_full = bars + 1;
-  uint64_t* qdo_empty = bars + 2;
-  uint64_t* s_full = bars + 3;
-  uint64_t* s_free = bars + 4;
-  uint64_t* p_full = bars + 5;
-  uint64_t* p_free = bars + 6;
-  uint64_t* acc_full = bars + 7;
-  uint64_t* drain = bars + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9);
+  uint64_t* qdo_full = bars + 1;   // [3]
+  uint64_t* qdo_empty = bars + 4;  // [3]
+  uint64_t* s_full = bars + 7;     // [2]
+  uint64_t* s_free = bars + 9;     // [2]
+  uint64_t* p_full = bars + 11;    // [2]
+  uint64_t* p_free = bars + 13;    // [2]
+  uint64_t* acc_full = bars + 15;
+  uint64_t* drain = bars + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* v_lse2 = reinterpret_cast<float*>(smem + kKVec);
-  float* v_delta = v_lse2 + 128;
 
   const int jt = (int)blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int rep = p.Hq / p.Hkv;
-  const int nq_tiles = p.n_qt - jt;   // query tiles jt .. n_qt-1 see this key tile
-  const int n_items = rep * nq_tiles; // item u: head g*rep + u / nq_tiles, query tile jt + u % nq_tiles
+  const int n_sub = 2 * (p.n_qt - jt);  // 64-query sub-tiles at or after this key tile
+  const int n_items = rep * n_sub;      // item u: head g*rep + u / n_sub, sub-tile u % n_sub
   const int k0 = b * p.S + jt * 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    mbar_init(qdo_full, 1);
-    mbar_init(qdo_empty, 1);
-    mbar_init(s_full, 1);
-    mbar_init(s_free, 128);
-    mbar_init(p_full, 128);
-    mbar_init(p_free, 1);
+    for (int s = 0; s < kQdoStages; ++s) {
+      mbar_init(&qdo_full[s], 1);
+      mbar_init(&qdo_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_free[s], 128);
+      mbar_init(&p_full[s], 128);
+      mbar_init(&p_free[s], 1);
+    }
     mbar_init(acc_full, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -541,7 +573,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmQKV);
-    tma_prefetch_desc(&tmDO);
+    tma_prefetch_desc(&tmQ64);
+    tma_prefetch_desc(&tmDO64);
     tma_prefetch_desc(&tmDQKV);
   }
   if (warp == 2) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
@@ -555,7 +588,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (lane == 0) {
       // ---------------- TMA producer ----------------
       bool ok = true;
-      int last = -1;  // last item whose Q/dO load was issued
+      uint32_t issued = 0, issued_par = 0;  // sub-tile stages with a load in flight, and its parity
       const int xk = (p.Hq + g) * kDh, xv = (p.Hq + p.Hkv + g) * kDh;
       mbar_arrive_expect_tx(kv_full, 2 * kTile);
       tma_load_2d(smem + kKK, &tmQKV, kv_full, xk, k0);
@@ -563,47 +596,60 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tma_load_2d(smem + kKV, &tmQKV, kv_full, xv, k0);
       tma_load_2d(smem + kKV + kAtom, &tmQKV, kv_full, xv + 64, k0);
       for (int u = 0; u < n_items; ++u) {
-        if (!mbar_wait(qdo_empty, ((uint32_t)u & 1u) ^ 1u, abort_flag)) { ok = false; break; }
-        const int h = g * rep + u / nq_tiles, it = jt + u % nq_tiles;
-        const int q0 = b * p.S + it * 128;
-        mbar_arrive_expect_tx(qdo_full, 2 * kTile + 1024);
-        tma_load_2d(smem + kKQ, &tmQKV, qdo_full, h * kDh, q0);
-        tma_load_2d(smem + kKQ + kAtom, &tmQKV, qdo_full, h * kDh + 64, q0);
-        tma_load_2d(smem + kKO, &tmDO, qdo_full, h * kDh, q0);
-        tma_load_2d(smem + kKO + kAtom, &tmDO, qdo_full, h * kDh + 64, q0);
-        bulk_load_1d(v_lse2, p.lse2 + (int64_t)h * p.T + q0, 512, qdo_full);
-        bulk_load_1d(v_delta, p.delta + (int64_t)h * p.T + q0, 512, qdo_full);
-        last = u;
+        const int st = u % kQdoStages;
+        const uint32_t par = (uint32_t)(u / kQdoStages) & 1u;
+        if (!mbar_wait(&qdo_empty[st], par ^ 1u, abort_flag)) { ok = false; break; }
+        const int h = g * rep + u / n_sub;
+        const int q0 = k0 + (u % n_sub) * 64;
+        uint8_t* sq = smem + kKQ + st * kSubTile;
+        uint8_t* so = smem + kKO + st * kSubTile;
+        float* vec = reinterpret_cast<float*>(smem + kKVec + st * 512);  // st: the Q/dO stage
+        mbar_arrive_expect_tx(&qdo_full[st], 2 * kSubTile + 512);
+        tma_load_2d(sq, &tmQ64, &qdo_full[st], h * kDh, q0);
+        tma_load_2d(sq + kSubAtom, &tmQ64, &qdo_full[st], h * kDh + 64, q0);
+        tma_load_2d(so, &tmDO64, &qdo_full[st], h * kDh, q0);
+        tma_load_2d(so + kSubAtom, &tmDO64, &qdo_full[st], h * kDh + 64, q0);
+        bulk_load_1d(vec, p.lse2 + (int64_t)h * p.T + q0, 256, &qdo_full[st]);
+        bulk_load_1d(vec + 64, p.delta + (int64_t)h * p.T + q0, 256, &qdo_full[st]);
+        issued |= 1u << st;
+        issued_par = (issued_par & ~(1u << st)) | (par << st);
       }
       if (!ok) {
         atomicOr(p.status, kStatusTimeout);
         *abort_flag = 1;
         int dummy = 0;
         mbar_wait(kv_full, 0, &dummy);
-        if (last >= 0) mbar_wait(qdo_full, (uint32_t)last & 1u, &dummy);
+        for (int s = 0; s < kQdoStages; ++s)
+          if (issued & (1u << s)) mbar_wait(&qdo_full[s], (issued_par >> s) & 1u, &dummy);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---------------- MMA issuer ----------------
-      const uint32_t tSt = tmem, tdPt = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+      // ---------------- MMA issuer: S^T, dP^T of item u; dV, dK of item u-1 ----------------
+      const uint32_t tdV = tmem + 256, tdK = tmem + 384;
       bool ok = mbar_wait(kv_full, 0, abort_flag);
-      for (int u = 0; u < n_items && ok; ++u) {
-        const uint32_t par = (uint32_t)u & 1u;
-        if (!mbar_wait(qdo_full, par, abort_flag) || !mbar_wait(s_free, par ^ 1u, abort_flag)) {
-          ok = false;
-          break;
+      for (int u = 0; u <= n_items && ok; ++u) {
+        if (u < n_items) {
+          const int qs = u % kQdoStages, sb = u & 1;
+          if (!mbar_wait(&qdo_full[qs], (uint32_t)(u / kQdoStages) & 1u, abort_flag) ||
+              !mbar_wait(&s_free[sb], ((uint32_t)(u >> 1) & 1u) ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_sub_kk(tmem + sb * 64, sbase + kKK, sbase + kKQ + qs * kSubTile);        // S^T = K Q^T
+          mma_sub_kk(tmem + 128 + sb * 64, sbase + kKV, sbase + kKO + qs * kSubTile);  // dP^T = V dO^T
+          umma_commit(&s_full[sb]);
         }
-        tc_fence_after();
-        mma_tile_kk(tSt, sbase + kKK, sbase + kKQ, false);   // S^T = K Q^T
-        mma_tile_kk(tdPt, sbase + kKV, sbase + kKO, false);  // dP^T = V dO^T
-        umma_commit(s_full);
-        if (!mbar_wait(p_full, par, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        mma_tile_kmn(tdV, sbase + kKPT, sbase + kKO, u > 0);   // dV += P^T dO
-        mma_tile_kmn(tdK, sbase + kKDST, sbase + kKQ, u > 0);  // dK += dS^T Q
-        umma_commit(qdo_empty);
-        umma_commit(p_free);
+        if (u >= 1) {
+          const int i = u - 1, pb = i & 1, qs = i % kQdoStages;
+          if (!mbar_wait(&p_full[pb], (uint32_t)(i >> 1) & 1u, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          mma_sub_kmn(tdV, sbase + kKPT + pb * kOpTile, sbase + kKO + qs * kSubTile, i > 0);   // dV += P^T dO
+          mma_sub_kmn(tdK, sbase + kKDST + pb * kOpTile, sbase + kKQ + qs * kSubTile, i > 0);  // dK += dS^T Q
+          umma_commit(&qdo_empty[qs]);
+          umma_commit(&p_free[pb]);
+        }
       }
       if (ok) umma_commit(acc_full);
       else {
@@ -615,50 +661,50 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_wait(drain, 0, &dummy);
     }
   } else if (warp >= 4) {
-    // ---------------- P^T, dS^T (one key row per thread) ----------------
+    // ---------------- P^T, dS^T (one key row per thread, 64 query columns) ----------------
     const int r = threadIdx.x - 128;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tSt = tmem + lane_off, tdPt = tmem + 128 + lane_off;
     bool ok = true;
     for (int u = 0; u < n_items; ++u) {
-      const uint32_t par = (uint32_t)u & 1u;
-      const bool diag = (u % nq_tiles) == 0;  // query tile jt: mask queries before this key
-      // qdo_full: this thread reads the lse2 / delta vectors that arrived with the Q/dO tiles
-      if (!warp_wait(qdo_full, par, abort_flag) || !warp_wait(s_full, par, abort_flag) ||
-          !warp_wait(p_free, par ^ 1u, abort_flag)) {
+      const int st = u & 1, qs = u % kQdoStages, v = u % n_sub;
+      const uint32_t par = (uint32_t)(u >> 1) & 1u;
+      // qdo_full: this thread reads the lse2 / delta vectors that arrived with the sub-tiles
+      if (!warp_wait(&qdo_full[qs], (uint32_t)(u / kQdoStages) & 1u, abort_flag) ||
+          !warp_wait(&s_full[st], par, abort_flag) || !warp_wait(&p_free[st], par ^ 1u, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      const float* vec = reinterpret_cast<const float*>(smem + kKVec + qs * 512);
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t sv[32], dv[32], wp[16], ws[16];
-        tmem_ld32(tSt + c * 32, sv);
-        tmem_ld32(tdPt + c * 32, dv);
-        if (diag) pds_col_chunk<true>(sv, dv, c, r, p.scale_log2, v_lse2, v_delta, wp, ws);
-        else pds_col_chunk<false>(sv, dv, c, r, p.scale_log2, v_lse2, v_delta, wp, ws);
-        tile_put32(sbase + kKPT, r, c, wp);
-        tile_put32(sbase + kKDST, r, c, ws);
+        tmem_ld32x2(tmem + lane_off + st * 64 + c * 32, tmem + lane_off + 128 + st * 64 + c * 32, sv, dv);
+        // sub-tiles 0 and 1 overlap the key tile: query q0 + col sees key k0 + r iff col >= r - 64 v
+        if (v < 2) pds_col_chunk<true>(sv, dv, c, r - 64 * v, p.scale_log2, vec, vec + 64, wp, ws);
+        else pds_col_chunk<false>(sv, dv, c, 0, p.scale_log2, vec, vec + 64, wp, ws);
+        tile_put32(sbase + kKPT + st * kOpTile, r, c, wp);
+        tile_put32(sbase + kKDST + st * kOpTile, r, c, ws);
       }
       tc_fence_before();
-      mbar_arrive(s_free);
+      mbar_arrive(&s_free[st]);
       fence_async_shared();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[st]);
     }
     if (ok && !warp_wait(acc_full, 0, abort_flag)) ok = false;
     if (!ok) {
       atomicOr(p.status, kStatusTimeout);
       *abort_flag = 1;
     }
-    // dV and dK rows (dK scaled by 1/sqrt(128)) out through the P^T and dS^T tiles
+    // dV and dK rows (dK scaled by 1/sqrt(128)) out through the P^T and dS^T regions (32 KB each,
+    // the two 64-column halves of a 128 x 128 tile); every MMA has completed
     if (ok) {
       tc_fence_after();
-      const uint32_t tdV = tmem + 256 + lane_off, tdK = tmem + 384 + lane_off;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t vv[32], kv[32], wv[16], wk[16];
-        tmem_ld32(tdV + c * 32, vv);
-        tmem_ld32(tdK + c * 32, kv);
+        tmem_ld32(tmem + lane_off + 256 + c * 32, vv);
+        tmem_ld32(tmem + lane_off + 384 + c * 32, kv);
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           wv[k] = pack_bf16x2(__uint_as_float(vv[2 * k]), __uint_as_float(vv[2 * k + 1]));
@@ -889,13 +935,14 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// bf16 matrix [rows, cols] (row stride ld elements) in 64 x 128 boxes (128-byte rows, 128-byte swizzle).
-bool make_tile_map(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t ld) {
+// bf16 matrix [rows, cols] (row stride ld elements) in boxes 64 elements (128 bytes) wide and
+// box_rows high, 128-byte swizzle.
+bool make_tile_map(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t ld, int box_rows = 128) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
-  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -965,15 +1012,15 @@ cudaError_t launch_attn_bwd_delta(const uint16_t* att, const uint16_t* datt, con
 cudaError_t launch_attn_bwd_dkdv(const uint16_t* qkv, const uint16_t* datt, int64_t T, int S, int Hq, int Hkv,
                                  const float* delta, const float* lse2, uint16_t* dqkv, const Launch& L) {
   const int64_t nq = (int64_t)(Hq + 2 * Hkv) * kDh, da = (int64_t)Hq * kDh;
-  CUtensorMap tq, tdo, tdq;
-  if (!make_tile_map(&tq, qkv, nq, T, nq) || !make_tile_map(&tdo, datt, da, T, da) ||
-      !make_tile_map(&tdq, dqkv, nq, T, nq))
+  CUtensorMap tq, tq64, tdo64, tdq;
+  if (!make_tile_map(&tq, qkv, nq, T, nq) || !make_tile_map(&tq64, qkv, nq, T, nq, 64) ||
+      !make_tile_map(&tdo64, datt, da, T, da, 64) || !make_tile_map(&tdq, dqkv, nq, T, nq))
     return cudaErrorInvalidValue;
   const AttnBwdArgs a = bwd_args(T, S, Hq, Hkv, delta, lse2, L);
   cudaError_t e = set_smem(k_attn_bwd_dkdv, kDkdvSmem, g_cfg_dkdv);
   if (e != cudaSuccess) return e;
   k_attn_bwd_dkdv<<<dim3((unsigned)a.n_qt, (unsigned)Hkv, (unsigned)(T / S)), kAttnThreads, kDkdvSmem, L.stream>>>(
-      tq, tdo, tdq, a);
+      tq, tq64, tdo64, tdq, a);
   if (L.launches) ++*L.launches;
   return cudaGetLastError();
 }
