@@ -171,7 +171,26 @@ def step_work(w: synth.Workload, recompute: bool = False, bf16: bool = False):
             ("gemm_gate_up_wgrad", 2 * T * d + 2 * T * 2 * f + 4 * d * 2 * f, 2.0 * d * T * 2 * f),
             ("rmsnorm_bwd", 10 * T * d, 0),
         ]
-        return fwd + (bwd if w.backward else [])
+        if not w.qkv:
+            return fwd + (bwd if w.backward else [])
+        q = w.qkv
+        core_f, core_b = [], []
+        if w.n_heads:
+            hq, hkv = w.n_heads, w.n_kv_heads
+            pairs = (T // w.seq_len) * w.seq_len * (w.seq_len + 1) / 2 * hq
+            core_f = [("attn_fwd", 2 * T * q + 2 * T * d + 4 * T * hq, 4.0 * 128 * pairs)]
+            core_b = [("attn_bwd_delta", 4 * T * d + 12 * T * hq, 0),
+                      ("attn_bwd_dkdv", 2 * T * q + 2 * T * d + 8 * T * hq + 4 * T * hkv * 128, 8.0 * 128 * pairs),
+                      ("attn_bwd_dq", 2 * T * q + 4 * T * d + 8 * T * hq, 6.0 * 128 * pairs)]
+        a_fwd = [("rmsnorm_bf16", 4 * T * d + 2 * d + 4 * T, 0),
+                 ("gemm_qkv", 2 * T * d + 2 * d * q + 2 * T * q, 2.0 * T * d * q), *core_f,
+                 ("gemm_o_residual", 2 * T * d + 2 * d * d + 4 * T * d, 2.0 * T * d * d)]
+        a_bwd = [("gemm_o_dgrad", 2 * T * d + 2 * d * d + 2 * T * d, 2.0 * T * d * d),
+                 ("gemm_o_wgrad", 4 * T * d + 4 * d * d, 2.0 * T * d * d), *core_b,
+                 ("gemm_qkv_dgrad", 2 * T * q + 2 * d * q + 4 * T * d, 2.0 * T * q * d),
+                 ("gemm_qkv_wgrad", 2 * T * d + 2 * T * q + 4 * d * q, 2.0 * T * d * q),
+                 ("rmsnorm_bwd", 10 * T * d, 0)]
+        return a_fwd + fwd + (bwd + a_bwd if w.backward else [])
     mlp_fwd = [
         ("absmax_partial", 2 * d * 2 * f, 0), ("quant_cast", 3 * d * 2 * f, 0),
         ("absmax_partial", 2 * f * d, 0), ("quant_cast", 3 * f * d, 0),
@@ -241,7 +260,8 @@ def run_ours(args, rank, world, local_rank):
     if w.qkv:
         inp = synth.block_inputs(w, seed=rank)
         core = (w.n_heads, w.n_kv_heads, w.seq_len) if w.n_heads else None
-        b = fq.BlockBuffers.allocate(w.T, w.d, w.f, w.qkv, device=dev, backward=w.backward, core=core)
+        b = fq.BlockBuffers.allocate(w.T, w.d, w.f, w.qkv, device=dev, backward=w.backward, core=core,
+                                     bf16=args.bf16)
         dev_in = {"x": b.x, "g1": b.g1, "W_qkv": b.W_qkv, "W_o": b.W_o, "g": b.mlp.g,
                   "W_gu": b.mlp.W_gu, "W_d": b.mlp.W_d}
         if not core:
@@ -404,7 +424,7 @@ def cpu_baseline(w, tokens, grad_e4m3=False, bf16=False):
         t0 = time.perf_counter()
         oracle.full_block(sl["x"], inp["g1"], inp["W_qkv"], inp["W_o"], None if core else sl["att"], inp["g"],
                           inp["W_gu"], inp["W_d"], dY=sl.get("dY"), dQKV=None if core else sl.get("dQKV"),
-                          nthreads=1, grad_fmt=gf, core=core)
+                          nthreads=1, grad_fmt=gf, core=core, bf16=bf16)
         dt = time.perf_counter() - t0
     else:
         inp = synth.mlp_inputs(w, seed=0)
@@ -471,8 +491,8 @@ def main():
     if args.tokens:
         import dataclasses
         w = dataclasses.replace(w, T=args.tokens)
-    if args.bf16 and (w.qkv or args.recompute or args.grad_e4m3):
-        raise SystemExit("--bf16: MLP workloads only, without --recompute / --grad-e4m3")
+    if args.bf16 and (args.recompute or args.grad_e4m3):
+        raise SystemExit("--bf16: without --recompute / --grad-e4m3")
     pk = peaks()
     fp8_peak = pk["bf16_sustained"] * FP8_PER_BF16
 

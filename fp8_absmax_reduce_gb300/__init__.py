@@ -98,7 +98,7 @@ class FP8QBlock(ctypes.Structure):
                 + [(n, ctypes.c_void_p) for n in ("dQKV", "d_att", "dX", "dW_qkv", "dW_o", "dg1", "dh8", "dQKV8",
                                                   "dN1")]
                 + [("n_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int), ("seq_len", ctypes.c_int64),
-                   ("lse", ctypes.c_void_p)])
+                   ("lse", ctypes.c_void_p), ("n1_16", ctypes.c_void_p)])
 
 
 _lib_handle = None
@@ -396,22 +396,26 @@ class BlockBuffers:
     n_kv_heads: int = 0
     seq_len: int = 0
     lse: torch.Tensor | None = None
+    n1_16: torch.Tensor | None = None
 
     @staticmethod
     def allocate(T: int, d: int, f: int, n_qkv: int, device="cuda", backward: bool = True, eps: float = 1e-6,
-                 keep_intermediates: bool = False, core=None) -> "BlockBuffers":
+                 keep_intermediates: bool = False, core=None, bf16: bool = False) -> "BlockBuffers":
         """core = (n_heads, n_kv_heads, seq_len): the attention core runs inside the block (att and
-        dQKV become outputs); None: att and dQKV are given."""
+        dQKV become outputs); None: att and dQKV are given.  bf16: the BF16 baseline's buffers."""
         e = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)
+        q8 = (lambda shape: None) if bf16 else (lambda shape: e(shape, torch.uint8))
         m = MlpBuffers.allocate(T, d, f, device=device, backward=backward, eps=eps,
-                                keep_intermediates=keep_intermediates)
+                                keep_intermediates=keep_intermediates, bf16=bf16)
         m.ws = None  # the block's workspace holds the MLP's
         b = BlockBuffers(
             T=T, d=d, f=f, n_qkv=n_qkv, eps=eps, x=e((T, d), torch.bfloat16), g1=e((d,), torch.bfloat16),
             W_qkv=e((d, n_qkv), torch.bfloat16), W_o=e((d, d), torch.bfloat16), att=e((T, d), torch.bfloat16),
-            qkv=e((T, n_qkv), torch.bfloat16), W_qkv8=e((d, n_qkv), torch.uint8), W_o8=e((d, d), torch.uint8),
-            n1_8=e((T, d), torch.uint8), rstd1=e((T,), torch.float32), att8=e((T, d), torch.uint8),
-            scal=torch.zeros((6, 3), device=device), mlp=m)
+            qkv=e((T, n_qkv), torch.bfloat16), W_qkv8=q8((d, n_qkv)), W_o8=q8((d, d)),
+            n1_8=q8((T, d)), rstd1=e((T,), torch.float32), att8=q8((T, d)),
+            scal=None if bf16 else torch.zeros((6, 3), device=device), mlp=m)
+        if bf16:
+            b.n1_16 = e((T, d), torch.bfloat16)
         if backward:
             b.dQKV = e((T, n_qkv), torch.bfloat16)
             b.d_att = e((T, d), torch.bfloat16)
@@ -420,8 +424,8 @@ class BlockBuffers:
             b.dW_o = e((d, d), torch.float32)
             b.dg1 = e((d,), torch.float32)
             if keep_intermediates:
-                b.dh8 = e((T, d), torch.uint8)
-                b.dQKV8 = e((T, n_qkv), torch.uint8)
+                b.dh8 = q8((T, d))
+                b.dQKV8 = q8((T, n_qkv))
                 b.dN1 = e((T, d), torch.float32)
         if core is not None:
             b.n_heads, b.n_kv_heads, b.seq_len = (int(v) for v in core)
@@ -442,6 +446,7 @@ class BlockBuffers:
         s = FP8QBlock(T=self.T, d=self.d, f=self.f, n_qkv=self.n_qkv, eps=self.eps, n_heads=self.n_heads,
                       n_kv_heads=self.n_kv_heads, seq_len=self.seq_len)
         s.lse = None if self.lse is None else self.lse.data_ptr()
+        s.n1_16 = None if self.n1_16 is None else self.n1_16.data_ptr()
         for name in ("x", "g1", "W_qkv", "W_o", "att", "qkv", "W_qkv8", "W_o8", "n1_8", "rstd1", "att8", "scal",
                      "dQKV", "d_att", "dX", "dW_qkv", "dW_o", "dg1", "dh8", "dQKV8", "dN1"):
             t = getattr(self, name)

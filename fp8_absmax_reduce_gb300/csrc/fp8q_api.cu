@@ -506,7 +506,6 @@ int validate_attention(const void* qkv, int64_t T, int64_t S, int Hq, int Hkv, i
 int validate_block(const fp8q_block* b, bool backward) {
   if (!b) return FP8Q_ERR_INVALID_ARG;
   const fp8q_mlp& m = b->mlp;
-  if (m.bf16) return FP8Q_ERR_UNSUPPORTED;
   if (m.T != b->T || m.d != b->d || m.f != b->f || m.x != b->h) return FP8Q_ERR_INVALID_ARG;
   if (b->n_qkv < 16 || b->n_qkv % 16 || b->n_qkv > (int64_t)1 << 20) return FP8Q_ERR_INVALID_ARG;
   int e = validate_mlp(&m, backward);
@@ -517,10 +516,16 @@ int validate_block(const fp8q_block* b, bool backward) {
       return FP8Q_ERR_INVALID_ARG;
     if ((e = validate_attention(b->qkv, b->T, b->seq_len, b->n_heads, b->n_kv_heads, 128))) return e;
   }
-  const void* must[] = {b->x, b->g1, b->W_qkv, b->W_o, b->att, b->qkv, b->h, b->W_qkv8, b->W_o8, b->n1_8,
-                        b->rstd1, b->att8, b->scal};
-  for (const void* p : must)
-    if (!al16(p)) return FP8Q_ERR_INVALID_ARG;
+  if (m.bf16) {
+    const void* must16[] = {b->x, b->g1, b->W_qkv, b->W_o, b->att, b->qkv, b->h, b->rstd1, b->n1_16};
+    for (const void* p : must16)
+      if (!al16(p)) return FP8Q_ERR_INVALID_ARG;
+  } else {
+    const void* must[] = {b->x, b->g1, b->W_qkv, b->W_o, b->att, b->qkv, b->h, b->W_qkv8, b->W_o8, b->n1_8,
+                          b->rstd1, b->att8, b->scal};
+    for (const void* p : must)
+      if (!al16(p)) return FP8Q_ERR_INVALID_ARG;
+  }
   if (!backward) return FP8Q_OK;
   const void* must_b[] = {b->dQKV, b->d_att, b->dX, b->dW_qkv, b->dW_o, b->dg1};
   for (const void* p : must_b)
@@ -556,7 +561,59 @@ GemmProblem gemm_problem(int a_mn, int b_mn, int64_t M, int64_t N, int64_t K, co
   return g;
 }
 
+// The block's BF16 baseline: the FP8 sequences with every cast removed (bf16 operands, alpha = 1).
+int block_fwd_run_bf16(const fp8q_block* b, const BlockWs& w, Ctx& c) {
+  const int64_t T = b->T, d = b->d, nq = b->n_qkv;
+  int P = 0;
+  FP8Q_STEP(kKRmsnormBf16, launch_rmsnorm_bf16((const uint16_t*)b->x, (const uint16_t*)b->g1, T, (int)d, b->eps,
+                                               b->rstd1, (uint16_t*)b->n1_16, c.L));
+  FP8Q_STEP(kKGemmQkv,
+            launch_gemm(bf16_gemm(0, 1, T, nq, d, b->n1_16, d, b->W_qkv, nq, nq, kEpiStore, 0, b->qkv, nq), &P, c.L));
+  if (b->n_heads)
+    FP8Q_STEP(kKAttnFwd, launch_attn_fwd((const uint16_t*)b->qkv, T, (int)b->seq_len, b->n_heads, b->n_kv_heads,
+                                         (uint16_t*)b->att, b->lse, c.L));
+  GemmProblem go = bf16_gemm(0, 1, T, d, d, b->att, d, b->W_o, d, d, kEpiResidual, 0, b->h, d);
+  go.R = (const uint16_t*)b->x;
+  go.ldr = d;
+  FP8Q_STEP(kKGemmOResidual, launch_gemm(go, &P, c.L));
+  return mlp_fwd_run(&b->mlp, w.mlp, c);
+}
+
+int block_bwd_run_bf16(const fp8q_block* b, const BlockWs& w, Ctx& c) {
+  const int64_t T = b->T, d = b->d, nq = b->n_qkv;
+  int e = mlp_bwd_run(&b->mlp, w.mlp, c);
+  if (e) return e;
+  const void* dh = b->mlp.dX;
+  float* dN1 = b->dN1 ? b->dN1 : w.dN1;
+  int P = 0;
+  FP8Q_STEP(kKGemmODgrad,
+            launch_gemm(bf16_gemm(0, 0, T, d, d, dh, d, b->W_o, d, d, kEpiStore, 0, b->d_att, d), &P, c.L));
+  FP8Q_STEP(kKGemmOWgrad,
+            launch_gemm(bf16_gemm(1, 1, d, d, T, b->att, d, dh, d, d, kEpiStore, 1, b->dW_o, d), &P, c.L));
+  if (b->n_heads) {
+    const uint16_t* q16 = (const uint16_t*)b->qkv;
+    const uint16_t* do16 = (const uint16_t*)b->d_att;
+    const int S = (int)b->seq_len;
+    FP8Q_STEP(kKAttnBwdDelta, launch_attn_bwd_delta((const uint16_t*)b->att, do16, b->lse, T, b->n_heads,
+                                                    w.attn_delta, w.attn_lse2, c.L));
+    FP8Q_STEP(kKAttnBwdDkdv, launch_attn_bwd_dkdv(q16, do16, T, S, b->n_heads, b->n_kv_heads, w.attn_delta,
+                                                  w.attn_lse2, (uint16_t*)b->dQKV, c.L));
+    FP8Q_STEP(kKAttnBwdDq, launch_attn_bwd_dq(q16, do16, T, S, b->n_heads, b->n_kv_heads, w.attn_delta, w.attn_lse2,
+                                              (uint16_t*)b->dQKV, c.L));
+  }
+  FP8Q_STEP(kKGemmQkvDgrad,
+            launch_gemm(bf16_gemm(0, 0, T, d, nq, b->dQKV, nq, b->W_qkv, nq, d, kEpiStore, 1, dN1, d), &P, c.L));
+  FP8Q_STEP(kKGemmQkvWgrad, launch_gemm(bf16_gemm(1, 1, d, nq, T, b->n1_16, d, b->dQKV, nq, nq, kEpiStore, 1,
+                                                  b->dW_qkv, nq),
+                                        &P, c.L));
+  FP8Q_STEP(kKRmsnormBwd, launch_rmsnorm_bwd(dN1, (const uint16_t*)b->x, (const uint16_t*)dh,
+                                             (const uint16_t*)b->g1, b->rstd1, T, (int)d, (uint16_t*)b->dX,
+                                             w.dg1_part, b->dg1, c.L));
+  return FP8Q_OK;
+}
+
 int block_fwd_run(const fp8q_block* b, const BlockWs& w, Ctx& c) {
+  if (b->mlp.bf16) return block_fwd_run_bf16(b, w, c);
   const int64_t T = b->T, d = b->d, nq = b->n_qkv;
   float* s_qkv = b->scal + 0;
   float* s_o = b->scal + 3;
@@ -591,6 +648,7 @@ int block_fwd_run(const fp8q_block* b, const BlockWs& w, Ctx& c) {
 }
 
 int block_bwd_run(const fp8q_block* b, const BlockWs& w, Ctx& c) {
+  if (b->mlp.bf16) return block_bwd_run_bf16(b, w, c);
   const int64_t T = b->T, d = b->d, nq = b->n_qkv;
   const float* s_qkv = b->scal + 0;
   const float* s_o = b->scal + 3;

@@ -307,6 +307,10 @@ typedef struct fp8q_block {
   int n_heads, n_kv_heads;
   int64_t seq_len;
   float* lse;         /* [n_heads,T] fp32, written by block_fwd, read by block_bwd (n_heads != 0) */
+  /* BF16 baseline of the whole block (mlp.bf16 != 0; see fp8q_mlp.bf16): every GEMM reads bf16
+   * operands with no scale factors -- W_qkv, W_o, att, dh, dQKV and n1_16 = bf16((x rstd1) g1);
+   * W_qkv8, W_o8, n1_8, att8, scal, dh8 and dQKV8 are neither read nor written (may be NULL). */
+  void* n1_16;        /* [T,d] bf16 (mlp.bf16 != 0) */
 } fp8q_block;
 
 FP8Q_API size_t block_workspace_size(int64_t T, int64_t d, int64_t f, int64_t n_qkv, int backward);

@@ -87,7 +87,7 @@ class _FullIO(ctypes.Structure):
         ("dh8", ctypes.c_void_p), ("dqkv8", ctypes.c_void_p), ("mlp", _BlockIO), ("x", ctypes.c_void_p),
         ("n_heads", ctypes.c_int64), ("n_kv_heads", ctypes.c_int64), ("head_dim", ctypes.c_int64),
         ("seq_len", ctypes.c_int64), ("att_out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
-        ("dqkv_out", ctypes.c_void_p),
+        ("dqkv_out", ctypes.c_void_p), ("n1_16", ctypes.c_void_p),
     ]
 
 
@@ -355,12 +355,13 @@ def attention(qkv, S: int, Hq: int, Hkv: int, dh: int, d_att=None, exact: bool =
 
 
 def full_block(x, g1, Wqkv, Wo, att, g2, Wgu, Wd, dY=None, dQKV=None, eps: float = 1e-6, exact: bool = False,
-               nthreads: int = 1, grad_fmt: int = E5M2, core=None):
+               nthreads: int = 1, grad_fmt: int = E5M2, core=None, bf16: bool = False):
     """The full transformer block's matmuls around a given attention core.
 
     core = (n_heads, n_kv_heads, head_dim, seq_len): the attention core (attention()) computes att
     from qkv and, in the backward, dQKV from d_att; att and dQKV are then not read (may be None)
-    and the results hold "att", "lse" and "dqkv" as well.
+    and the results hold "att", "lse" and "dqkv" as well.  bf16: the BF16 baseline (every operand
+    stored as bf16 instead of quantized, see block()); the results then hold "n1_16", "n16", "a16".
 
     Forward: qkv = bf16(alpha n1_8 @ W_qkv8) with n1 = RMSNorm(x) g1; h = bf16(x + alpha att8 @ W_o8);
     y = MLP block on h (gain g2).  Backward (with dY [T,d] and the core's input gradient dQKV
@@ -392,8 +393,13 @@ def full_block(x, g1, Wqkv, Wo, att, g2, Wgu, Wd, dY=None, dQKV=None, eps: float
         io.n_heads, io.n_kv_heads, io.head_dim, io.seq_len = (int(v) for v in core)
         out.update({"att": np.empty((T, d)), "lse": np.empty((io.n_heads, T))})
         io.att_out, io.lse = out["att"].ctypes.data, out["lse"].ctypes.data
-    m = _BlockIO(T=T, d=d, f=f, eps=eps, exact=int(exact), nthreads=int(nthreads), grad_fmt=int(grad_fmt))
+    m = _BlockIO(T=T, d=d, f=f, eps=eps, exact=int(exact), nthreads=int(nthreads), grad_fmt=int(grad_fmt),
+                 bf16=int(bf16))
     m.g, m.Wgu, m.Wd = (a.ctypes.data for a in keep[5:])
+    if bf16:
+        out.update({"n1_16": np.empty((T, d)), "n16": np.empty((T, d)), "a16": np.empty((T, f))})
+        io.n1_16 = out["n1_16"].ctypes.data
+        m.n16, m.a16 = out["n16"].ctypes.data, out["a16"].ctypes.data
     for k in ("qkv", "h", "rstd1", "Wqkv8", "Wo8", "n1_8", "att8", "scal_attn"):
         setattr(io, k, out[k].ctypes.data)
     for k in ("y", "H", "rstd", "Wgu8", "Wd8", "n8", "a8", "scal_fwd"):

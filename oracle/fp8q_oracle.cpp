@@ -722,6 +722,7 @@ struct FullIO {
   double* att_out;      // [T,d] the core's output (bf16 values)
   double* lse;          // [n_heads, T]
   double* dqkv_out;     // [T,nq] the core's input gradient (bf16 values)
+  double* n1_16;        // [T,d] the stored bf16 n1 (BF16 baseline, mlp.bf16)
 };
 
 // RMSNorm backward with a residual gradient: dx = dres + rstd (u - nh mean(u nh)), u = dN g.
@@ -752,11 +753,12 @@ int full_block(FullIO& io, bool backward) {
   const bool core = io.n_heads > 0;
   int status = 0;
   std::vector<double> x(io.x, io.x + T * d), g1(io.g1, io.g1 + d);
-  QTensor Wqkv = quantize(std::vector<double>(io.Wqkv, io.Wqkv + d * nq), FMT_E4M3, ex);
-  QTensor Wo = quantize(std::vector<double>(io.Wo, io.Wo + d * d), FMT_E4M3, ex);
+  // every operand goes through the MLP block's codec: per-tensor FP8, or bf16 in the BF16 baseline
+  QTensor Wqkv = operand(std::vector<double>(io.Wqkv, io.Wqkv + d * nq), FMT_E4M3, io.mlp);
+  QTensor Wo = operand(std::vector<double>(io.Wo, io.Wo + d * d), FMT_E4M3, io.mlp);
   std::vector<double> n1, rstd1;
   rmsnorm_fwd(x, g1, T, d, io.eps, ex, n1, rstd1);
-  QTensor n1q = quantize(n1, FMT_E4M3, ex);
+  QTensor n1q = operand(n1, FMT_E4M3, io.mlp);
 
   const double a_qkv = ex ? 1.0 : (double)(n1q.s.scale_inv * Wqkv.s.scale_inv);
   std::vector<double> qkv = matmul(n1q.deq, Wqkv.deq, T, nq, d, io.nthreads);
@@ -778,7 +780,7 @@ int full_block(FullIO& io, bool backward) {
   } else {
     att.assign(io.att, io.att + T * d);
   }
-  QTensor attq = quantize(att, FMT_E4M3, ex);
+  QTensor attq = operand(att, FMT_E4M3, io.mlp);
   const double a_o = ex ? 1.0 : (double)(attq.s.scale_inv * Wo.s.scale_inv);
   std::vector<double> h = matmul(attq.deq, Wo.deq, T, d, d, io.nthreads);
   for (size_t i = 0; i < h.size(); ++i) h[i] = ex ? x[i] + a_o * h[i] : to_bf16(x[i] + a_o * h[i]);
@@ -786,6 +788,7 @@ int full_block(FullIO& io, bool backward) {
   put(io.qkv, qkv);
   put(io.h, h);
   put(io.rstd1, rstd1);
+  if (io.mlp.bf16) put(io.n1_16, n1q.deq);
   if (!ex) { put(io.Wqkv8, Wqkv.code); put(io.Wo8, Wo.code); put(io.n1_8, n1q.code); put(io.att8, attq.code); }
   if (io.scal_attn) {
     put_scal(io.scal_attn + 0, Wqkv.s); put_scal(io.scal_attn + 3, Wo.s);
@@ -807,7 +810,7 @@ int full_block(FullIO& io, bool backward) {
   put(io.dh, dh);
 
   // O projection backward
-  QTensor dhq = quantize(dh, io.mlp.grad_fmt, ex);
+  QTensor dhq = operand(dh, io.mlp.grad_fmt, io.mlp);
   const double a_od = ex ? 1.0 : (double)(dhq.s.scale_inv * Wo.s.scale_inv);
   std::vector<double> datt = matmul(dhq.deq, transpose(Wo.deq, d, d), T, d, d, io.nthreads);
   for (double& v : datt) v = ex ? a_od * v : to_bf16(a_od * v);
@@ -828,7 +831,7 @@ int full_block(FullIO& io, bool backward) {
   }
 
   // QKV projection backward
-  QTensor dqq = quantize(dqkv, io.mlp.grad_fmt, ex);
+  QTensor dqq = operand(dqkv, io.mlp.grad_fmt, io.mlp);
   const double a_qd = ex ? 1.0 : (double)(dqq.s.scale_inv * Wqkv.s.scale_inv);
   std::vector<double> dN1 = matmul(dqq.deq, transpose(Wqkv.deq, d, nq), T, d, nq, io.nthreads);
   for (double& v : dN1) v = ex ? a_qd * v : (double)(float)(a_qd * v);

@@ -101,3 +101,44 @@ def test_bf16_full_size_7b():
     nh = x * b.rstd.cpu().numpy().astype(np.float64)[:, None]
     dg_ref = (host_f64(b.dN) * nh).sum(axis=0)
     assert row_rel(host_f64(b.dg)[None, :], dg_ref[None, :]) < 5e-3
+
+
+@pytest.mark.parametrize("T,d,f,nq,core", [(192, 256, 384, 512, None), (256, 512, 640, 1024, (4, 2, 128))])
+def test_bf16_full_block(T, d, f, nq, core):
+    """The full block's BF16 baseline (and with its attention core inside) against the oracle's
+    BF16 full block: rstd1 and n1_16 bit-exact; qkv, h, y within 2e-3; gradients within 5e-3 (no
+    FP8 requantization, so no cascade bars); with the core, att within the core's elementwise bound
+    around the oracle's attention of the oracle's qkv."""
+    w = synth.BY_NAME["32b-block-fwd-bwd"]
+    inp = synth.block_inputs(w, seed=0, T=T, d=d, f=f, n_qkv=nq)
+    b = fq.BlockBuffers.allocate(T, d, f, nq, keep_intermediates=True, bf16=True, core=core)
+    names = ["x", "g1", "W_qkv", "W_o", "g", "W_gu", "W_d", "dY"] + ([] if core else ["att", "dQKV"])
+    for k in names:
+        t = {"g": b.mlp.g, "W_gu": b.mlp.W_gu, "W_d": b.mlp.W_d, "dY": b.mlp.dY}.get(k, None)
+        (t if t is not None else getattr(b, k)).copy_(dev_bf16(inp[k]))
+    fq.get_status(clear=True)
+    fq.block_fwd(b)
+    fq.block_bwd(b)
+    torch.cuda.synchronize()
+    assert fq.get_status() == 0
+    oc = None if core is None else (core[0], core[1], 128, core[2])
+    ref = oracle.full_block(inp["x"], inp["g1"], inp["W_qkv"], inp["W_o"], None if core else inp["att"], inp["g"],
+                            inp["W_gu"], inp["W_d"], dY=inp["dY"], dQKV=None if core else inp["dQKV"],
+                            nthreads=16, bf16=True, core=oc)
+    np.testing.assert_array_equal(b.rstd1.cpu().numpy(), ref["rstd1"].astype(np.float32))
+    np.testing.assert_array_equal(host_f64(b.n1_16), ref["n1_16"])
+    for t, k in ((b.qkv, "qkv"), (b.h, "h"), (b.mlp.y, "y")):
+        assert row_rel(host_f64(t), ref[k]) < 2e-3, k
+    if core:
+        ra = oracle.attention(synth.bf16_bits(ref["qkv"].astype(np.float32)), core[2], core[0], core[1], 128,
+                              nthreads=16, with_abs=True)
+        bound = 2.0 ** -8 * (ra["att_abs"] + 2 * np.abs(ra["att"])) * (1 + 2.0 ** -6)
+        assert np.all(np.abs(host_f64(b.att) - ref["att"]) <= bound)
+    for t, k in ((b.dX, "dX"), (b.d_att, "d_att"), (b.mlp.dX, "dh")):
+        assert row_rel(host_f64(t), ref[k]) < 5e-3, k
+    if core:
+        assert row_rel(host_f64(b.dQKV), ref["dqkv"]) < 5e-3
+    for t, k in ((b.dW_qkv, "dWqkv"), (b.dW_o, "dWo"), (b.mlp.dW_gu, "dWgu"), (b.mlp.dW_d, "dWd")):
+        assert row_rel(host_f64(t), ref[k]) < 5e-3, k
+    for t, k in ((b.dg1, "dg1"), (b.mlp.dg, "dg")):
+        assert row_rel(host_f64(t)[None, :], ref[k][None, :]) < 5e-3, k

@@ -278,3 +278,25 @@ def test_bf16_baseline_accuracy_against_exact():
         assert rb <= rq, (k, rb, rq)
         if k not in ("y", "dX"):  # y, dX are dominated by the exact residual terms x, dY
             assert rb < rq / 5, (k, rb, rq)
+
+
+def test_full_block_bf16_baseline_accuracy():
+    """The full block's BF16 baseline (every operand stored as bf16): close to the exact block
+    (pinned by finite differences), several times closer than the FP8 block, and its stored
+    n1 is the bf16 closed form of the attention-side RMSNorm."""
+    w = synth.BY_NAME["32b-block-fwd-bwd"]
+    T, d, f, nq = 64, 256, 192, 512
+    inp = synth.block_inputs(w, seed=0, T=T, d=d, f=f, n_qkv=nq)
+    args = [inp[k] for k in ("x", "g1", "W_qkv", "W_o", "att", "g", "W_gu", "W_d")]
+    b = oracle.full_block(*args, dY=inp["dY"], dQKV=inp["dQKV"], bf16=True)
+    q = oracle.full_block(*args, dY=inp["dY"], dQKV=inp["dQKV"])
+    e = oracle.full_block(*(oracle.bf16_to_f64(a) for a in args), dY=oracle.bf16_to_f64(inp["dY"]),
+                          dQKV=oracle.bf16_to_f64(inp["dQKV"]), exact=True)
+    for k in ("qkv", "h", "y", "dX", "dWqkv", "dWo", "dWgu", "dWd"):
+        rb = np.linalg.norm(b[k] - e[k]) / np.linalg.norm(e[k])
+        rq = np.linalg.norm(q[k] - e[k]) / np.linalg.norm(e[k])
+        assert rb < 8 * 2.0 ** -9, (k, rb)
+        assert rb < rq / 2, (k, rb, rq)
+    x, g1 = oracle.bf16_to_f64(inp["x"]), oracle.bf16_to_f64(inp["g1"])
+    n1 = x / np.sqrt((x * x).mean(axis=1, keepdims=True) + 1e-6) * g1
+    assert np.all(np.abs(b["n1_16"] - n1) <= _half_bf16_ulp(n1) * (1 + 2.0 ** -6))
