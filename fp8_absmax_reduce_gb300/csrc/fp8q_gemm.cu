@@ -531,6 +531,228 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// The wide variant for the long-K GEMMs with plain epilogues (store, residual):
+// a 256 x 256 CTA tile made of two 128-row halves that share the B tile (two
+// tcgen05.mma per k-step into two accumulators, all 512 TMEM columns), so a
+// stage moves 64 KB for twice the MMA work of a 48 KB 128 x 256 stage -- a
+// third fewer operand bytes per FLOP reaching the SM, which is what bounds the
+// 128 x 256 mainloop.  The price: no second accumulator, so the epilogue of a
+// tile does not overlap the next tile's MMAs; with K >= kWideMinK the MMAs of
+// a tile take 10x or more the epilogue's time.  launch_gemm picks it per GEMM
+// by the estimate in wide_pays (wave quantization included).
+// ---------------------------------------------------------------------------
+constexpr int kWideStages = 3;
+constexpr int kWideStage = 2 * kATile + 2 * kBHalf;  // 64 KB
+constexpr int kWideStagingOffset = kWideStages * kWideStage;
+constexpr int kWideBarOffset = kWideStagingOffset + 8 * kStagingBytes;
+constexpr int kWideSmemBytes = kWideBarOffset + 256 + 1024;
+static_assert(kWideSmemBytes <= 232448, "shared memory per CTA");
+constexpr int kWideMinK = 8192;
+
+// Whether the wide tile is expected to finish first.  A wide tile does the work of two 128 x 256
+// tiles in ~0.86 of their time (measured on the 7B-class GEMMs: a third fewer operand bytes per
+// FLOP) plus its exposed epilogue (~5 us against 2 * 256 * 256 * K flops at ~23 TFLOP/s per SM);
+// both variants run in waves of one tile per SM, so the last, partial wave decides as much as the
+// per-tile speed.
+bool wide_pays(int64_t M, int n_tiles, int64_t K, int num_sms) {
+  const int64_t tiles_w = (M + 255) / 256 * n_tiles, tiles_n = (M + 127) / 128 * n_tiles;
+  const double waves_w = (double)((tiles_w + num_sms - 1) / num_sms);
+  const double waves_n = (double)((tiles_n + num_sms - 1) / num_sms);
+  const double epi = 5e-6 * 23e12 / (2.0 * 256 * 256 * (double)K);
+  return waves_w * 2.0 * 0.86 * (1.0 + epi) < waves_n;
+}
+
+template <int A_MN, int B_MN>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_f8_wide(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const Args p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kWideBarOffset);
+  uint64_t* empty = full + kWideStages;
+  uint64_t* tfull = empty + kWideStages;  // [1]
+  uint64_t* tempty = tfull + 1;           // [1]
+  uint64_t* drain = tempty + 1;           // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kWideStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, kEpiThreads);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
+  }
+  if (warp == 2) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, issued_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, p, mb, nb);
+        const int m0 = mb * 256;
+        const int n0 = nb * p.b_step, n1 = n0 + p.b_half1;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+          uint8_t* sA = smem + stage * kWideStage;
+          uint8_t* sB = sA + 2 * kATile;
+          mbar_arrive_expect_tx(&full[stage], kWideStage);
+          const int k0 = kb * BK;
+          if (A_MN) {
+            tma_load_2d(sA, &tmA, &full[stage], m0, k0);
+            tma_load_2d(sA + kATile, &tmA, &full[stage], m0 + 128, k0);
+          } else {
+            tma_load_2d(sA, &tmA, &full[stage], k0, m0);
+            tma_load_2d(sA + kATile, &tmA, &full[stage], k0, m0 + 128);
+          }
+          if (B_MN) {
+            tma_load_2d(sB, &tmB, &full[stage], n0, k0);
+            tma_load_2d(sB + kBHalf, &tmB, &full[stage], n1, k0);
+          } else {
+            tma_load_2d(sB, &tmB, &full[stage], k0, n0);
+            tma_load_2d(sB + kBHalf, &tmB, &full[stage], k0, n1);
+          }
+          issued |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == kWideStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        atomicOr(p.status, kStatusTimeout);
+        *abort_flag = 1;
+        for (int s = 0; s < kWideStages; ++s)
+          if (issued & (1u << s)) {
+            int dummy = 0;
+            mbar_wait(&full[s], (issued_par >> s) & 1u, &dummy);
+          }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer: two 128 x 256 x 32 MMAs per k-step ----------------
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(tempty, acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sA = smem_addr(smem + stage * kWideStage);
+          const uint32_t sB = sA + 2 * kATile;
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk) {
+            const uint64_t bd = B_MN ? smem_desc_sw128(sB + kk * 4096, kBHalf, 1024) : smem_desc_sw128(sB + kk * 32, 16, 1024);
+#pragma unroll
+            for (int hm = 0; hm < 2; ++hm) {
+              const uint32_t a = sA + hm * kATile;
+              const uint64_t ad = A_MN ? smem_desc_sw128(a + kk * 4096, kBHalf, 1024) : smem_desc_sw128(a + kk * 32, 16, 1024);
+              umma_f8(tmem_base + hm * BN, ad, bd, p.idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == kWideStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(tfull);
+        acc_phase ^= 1u;
+      }
+      if (!ok) {
+        atomicOr(p.status, kStatusTimeout);
+        *abort_flag = 1;
+      }
+      umma_commit(drain);
+      int dummy = 0;
+      mbar_wait(drain, 0, &dummy);
+    }
+  } else if (warp >= 4) {
+    // ---------------- epilogue: warpgroup hm drains accumulator hm (rows 128 hm ..) ----------------
+    const int sub = warp & 3;
+    const int hm = (warp - 4) >> 2;
+    const uint32_t buf = smem_addr(smem + kWideStagingOffset + (warp - 4) * kStagingBytes);
+    uint32_t acc_phase = 0;
+    const float alpha = __fmul_rn(*p.sinvA, *p.sinvB);
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+      int mb, nb;
+      tile_coords(tile, p, mb, nb);
+      int full_ok = 0;
+      if (lane == 0) full_ok = mbar_wait(tfull, acc_phase, abort_flag) ? 1 : 0;
+      if (!__shfl_sync(0xFFFFFFFFu, full_ok, 0)) {
+        atomicOr(p.status, kStatusTimeout);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (uint32_t)(hm * BN) + ((uint32_t)(sub * 32) << 16);
+      const int row0 = mb * 256 + hm * 128 + sub * 32;
+      const int row = row0 + lane;
+      const bool row_ok = row < p.M;
+      const bool warp_ok = row0 < p.M;
+      const int col0 = nb * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t acc32[32];
+        tmem_ld32(tbase + c * 32, acc32);
+        const int col = col0 + c * 32;
+        const int ncol = min(32, p.N - col);
+        if (!warp_ok || ncol <= 0) continue;
+        float v[32];
+        if (p.out_f32) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(alpha, __uint_as_float(acc32[j]));
+        } else if (p.epi == kEpiResidual) {
+          float rv[32];
+          const uint16_t* r = p.R + (int64_t)row * p.ldr + col;
+          if (row_ok && ncol == 32) {
+            load_bf16x32(r, rv);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) rv[j] = (row_ok && j < ncol) ? __uint_as_float((uint32_t)r[j] << 16) : 0.0f;
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = bf16_of_residual(rv[j], alpha, __uint_as_float(acc32[j]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = bf16_of_product(alpha, __uint_as_float(acc32[j]));
+        }
+        staging_acquire(lane);
+        if (p.out_f32) stage_f32(buf, lane, v);
+        else stage_bf16(buf, lane, v);
+        staging_publish();
+        if (lane == 0) {
+          tma_store_2d(&tmC, buf, col, row0);
+          bulk_commit();
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty);
+      acc_phase ^= 1u;
+    }
+    if (lane == 0) bulk_wait_all();  // every TMA store of this warp has completed
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -615,6 +837,22 @@ cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtenso
   return cudaGetLastError();
 }
 
+template <int A_MN, int B_MN>
+cudaError_t launch_wide_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const Args& a, int grid,
+                          cudaStream_t s) {
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_f8_wide<A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kWideSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  k_gemm_f8_wide<A_MN, B_MN><<<grid, kThreads, kWideSmemBytes, s>>>(ta, tb, tc, a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L) {
@@ -669,9 +907,24 @@ cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L) {
   }
   if (!ok_a || !ok_b || !ok_c) return cudaErrorInvalidValue;
 
+  // long-K FP8 GEMMs with plain epilogues take the 256 x 256 tile
+  const bool wide = !g.op16 && (g.epi == kEpiStore || g.epi == kEpiResidual) && g.K >= kWideMinK && g.M >= 256 &&
+                    wide_pays(g.M, a.n_tiles, g.K, L.num_sms);
+  if (wide) {
+    a.m_tiles = (g.M + 255) / 256;
+    a.num_tiles = a.m_tiles * a.n_tiles;
+  }
   const int grid = a.num_tiles < L.num_sms ? a.num_tiles : L.num_sms;
   *P = grid;
   cudaError_t e;
+  if (wide) {
+    if (g.a_mn == 0 && g.b_mn == 1) e = launch_wide_t<0, 1>(ta, tb, tc, a, grid, L.stream);
+    else if (g.a_mn == 0 && g.b_mn == 0) e = launch_wide_t<0, 0>(ta, tb, tc, a, grid, L.stream);
+    else if (g.a_mn == 1 && g.b_mn == 1) e = launch_wide_t<1, 1>(ta, tb, tc, a, grid, L.stream);
+    else return cudaErrorInvalidValue;
+    if (L.launches) ++*L.launches;
+    return e;
+  }
   if (g.op16) {  // the three layouts of the block (NN, NT, TN)
     if (g.a_mn == 0 && g.b_mn == 1) e = launch_t<0, 1, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
     else if (g.a_mn == 0 && g.b_mn == 0) e = launch_t<0, 0, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);

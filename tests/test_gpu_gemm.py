@@ -76,3 +76,15 @@ def test_gemm_nt_ragged_rows(M, N, K):
     # NT keeps both operands K-major, so M and N need no alignment at all
     got, ref = run_case(fq.NT, M, N, K, 1, 0, "f32", False, seed=M * N)
     assert row_rel(got, ref) < 2e-3
+
+
+@pytest.mark.parametrize("layout", [fq.NN, fq.NT, fq.TN])
+@pytest.mark.parametrize("M,N,K,out,residual", [(400, 528, 8320, "f32", False), (256, 256, 8192, "bf16", False),
+                                                (300, 608, 9008, "bf16", True)])
+def test_gemm_long_k_wide_tiles(layout, M, N, K, out, residual):
+    """K >= 8192 with a plain or residual epilogue: the 256 x 256 tile variant (two 128-row halves
+    sharing the B tile), with ragged M (a half-empty second half), N and K tails."""
+    if residual and layout == fq.TN:
+        pytest.skip("the residual epilogue is used with NN / NT")
+    got, ref = run_case(layout, M, N, K, 0, 1 if layout == fq.TN else 0, out, residual, seed=M + K)
+    assert row_rel(got, ref) < 2e-3
