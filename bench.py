@@ -564,7 +564,7 @@ def main():
                    "parallelism": "replicas" if world > 1 else "single"},
         "tokens_per_s": world * w.T / (ms_step * 1e-3),
         "pct_fp8_peak": round(100.0 * value / world / fp8_peak, 2),
-        "roofline": {"kernel": "k_gemm_f8 (the six block GEMMs)", "bound": "tensor", "achieved": round(achieved, 1),
+        "roofline": {"kernel": "k_gemm_f8 / k_gemm_f8_wide (the six block GEMMs)", "bound": "tensor", "achieved": round(achieved, 1),
                      "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "launches_per_step": g_launch // r["K"],
                      "share_of_step": round(g_ms / traced_total, 4),
