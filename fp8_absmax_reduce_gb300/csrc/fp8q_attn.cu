@@ -49,6 +49,10 @@ constexpr int kDh = 128;                 // head dimension
 constexpr int kAtom = 16384;             // 128 rows x 128 bytes: one 64-element-wide swizzle atom column
 constexpr int kTile = 2 * kAtom;         // a 128 x 128 bf16 operand tile
 constexpr int kAttnThreads = 256;
+// The backward kernels run two element-wise warpgroups (warps 4-7 and 8-11) that split every
+// tile's columns: their passes need no row reductions, and two warps per SM sub-partition hide
+// each other's latencies.
+constexpr int kAttnBwdThreads = 384;
 constexpr int kTmemCols = 512;
 
 // forward shared-memory layout (bytes from the 1024-aligned base)
@@ -528,7 +532,7 @@ __device__ __forceinline__ void mma_sub_kmn(uint32_t d, uint32_t a, uint32_t b, 
               idesc_bf16_n(128, 1), (accumulate || kk) ? 1u : 0u);
 }
 
-__global__ void __launch_bounds__(kAttnThreads, 1)
+__global__ void __launch_bounds__(kAttnBwdThreads, 1)
     k_attn_bwd_dkdv(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmQ64,
                     const __grid_constant__ CUtensorMap tmDO64, const __grid_constant__ CUtensorMap tmDQKV,
                     const AttnBwdArgs p) {
@@ -562,8 +566,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&s_free[s], 128);
-      mbar_init(&p_full[s], 128);
+      mbar_init(&s_free[s], 256);
+      mbar_init(&p_full[s], 256);
       mbar_init(&p_free[s], 1);
     }
     mbar_init(acc_full, 1);
@@ -661,8 +665,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_wait(drain, 0, &dummy);
     }
   } else if (warp >= 4) {
-    // ---------------- P^T, dS^T (one key row per thread, 64 query columns) ----------------
-    const int r = threadIdx.x - 128;
+    // ---------------- P^T, dS^T (one key row per thread; warpgroup wg takes 32 of the 64 query columns) ----------------
+    const int wg = (warp - 4) >> 2;
+    const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     bool ok = true;
     for (int u = 0; u < n_items; ++u) {
@@ -676,8 +681,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       tc_fence_after();
       const float* vec = reinterpret_cast<const float*>(smem + kKVec + qs * 512);
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
+      {
+        const int c = wg;
         uint32_t sv[32], dv[32], wp[16], ws[16];
         tmem_ld32x2(tmem + lane_off + st * 64 + c * 32, tmem + lane_off + 128 + st * 64 + c * 32, sv, dv);
         // sub-tiles 0 and 1 overlap the key tile: query q0 + col sees key k0 + r iff col >= r - 64 v
@@ -701,7 +706,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (ok) {
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
         uint32_t vv[32], kv[32], wv[16], wk[16];
         tmem_ld32(tmem + lane_off + 256 + c * 32, vv);
         tmem_ld32(tmem + lane_off + 384 + c * 32, kv);
@@ -715,8 +720,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
     }
     fence_async_shared();
-    named_bar_sync(1, 128);
-    if (r == 0 && !*abort_flag) {
+    named_bar_sync(1, 256);
+    if (wg == 0 && r == 0 && !*abort_flag) {
       const int xk = (p.Hq + g) * kDh, xv = (p.Hq + p.Hkv + g) * kDh;
       tma_store_2d(&tmDQKV, sbase + kKDST, xk, k0);
       tma_store_2d(&tmDQKV, sbase + kKDST + kAtom, xk + 64, k0);
@@ -740,7 +745,7 @@ constexpr int kQBar = kQDS + kTile;
 constexpr int kDqSmem = kQBar + 256 + 1024;
 static_assert(kDqSmem <= 232448, "shared memory per CTA");
 
-__global__ void __launch_bounds__(kAttnThreads, 1)
+__global__ void __launch_bounds__(kAttnBwdThreads, 1)
     k_attn_bwd_dq(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmDO,
                   const __grid_constant__ CUtensorMap tmDQKV, const AttnBwdArgs p) {
   extern __shared__ uint8_t smem_raw[];
@@ -769,8 +774,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_init(q_full, 1);
     for (int s = 0; s < 2; ++s) { mbar_init(&kv_full[s], 1); mbar_init(&kv_empty[s], 1); }
     mbar_init(s_full, 1);
-    mbar_init(s_free, 128);
-    mbar_init(ds_full, 128);
+    mbar_init(s_free, 256);
+    mbar_init(ds_full, 256);
     mbar_init(ds_free, 1);
     mbar_init(acc_full, 1);
     mbar_init(drain, 1);
@@ -854,7 +859,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_wait(drain, 0, &dummy);
     }
   } else if (warp >= 4) {
-    const int r = threadIdx.x - 128;
+    // one query row per thread; warpgroup wg takes the key columns 64 wg .. 64 wg + 63
+    const int wg = (warp - 4) >> 2;
+    const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off, tdP = tmem + 128 + lane_off;
     const float lse2 = p.lse2[(int64_t)h * p.T + t0 + r];
@@ -869,7 +876,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
         uint32_t sv[32], dv[32], w[16];
         tmem_ld32(tS + c * 32, sv);
         tmem_ld32(tdP + c * 32, dv);
@@ -892,7 +899,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc_fence_after();
       const uint32_t tdQ = tmem + 256 + lane_off;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
         uint32_t qv[32], w[16];
         tmem_ld32(tdQ + c * 32, qv);
 #pragma unroll
@@ -902,8 +909,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
     }
     fence_async_shared();
-    named_bar_sync(1, 128);
-    if (r == 0 && !*abort_flag) {
+    named_bar_sync(1, 256);
+    if (wg == 0 && r == 0 && !*abort_flag) {
       tma_store_2d(&tmDQKV, sbase + kQQ, h * kDh, t0);
       tma_store_2d(&tmDQKV, sbase + kQQ + kAtom, h * kDh + 64, t0);
       bulk_commit_and_wait();
@@ -1019,7 +1026,7 @@ cudaError_t launch_attn_bwd_dkdv(const uint16_t* qkv, const uint16_t* datt, int6
   const AttnBwdArgs a = bwd_args(T, S, Hq, Hkv, delta, lse2, L);
   cudaError_t e = set_smem(k_attn_bwd_dkdv, kDkdvSmem, g_cfg_dkdv);
   if (e != cudaSuccess) return e;
-  k_attn_bwd_dkdv<<<dim3((unsigned)a.n_qt, (unsigned)Hkv, (unsigned)(T / S)), kAttnThreads, kDkdvSmem, L.stream>>>(
+  k_attn_bwd_dkdv<<<dim3((unsigned)a.n_qt, (unsigned)Hkv, (unsigned)(T / S)), kAttnBwdThreads, kDkdvSmem, L.stream>>>(
       tq, tq64, tdo64, tdq, a);
   if (L.launches) ++*L.launches;
   return cudaGetLastError();
@@ -1035,7 +1042,7 @@ cudaError_t launch_attn_bwd_dq(const uint16_t* qkv, const uint16_t* datt, int64_
   const AttnBwdArgs a = bwd_args(T, S, Hq, Hkv, delta, lse2, L);
   cudaError_t e = set_smem(k_attn_bwd_dq, kDqSmem, g_cfg_dq);
   if (e != cudaSuccess) return e;
-  k_attn_bwd_dq<<<dim3((unsigned)a.n_qt, (unsigned)Hq, (unsigned)(T / S)), kAttnThreads, kDqSmem, L.stream>>>(
+  k_attn_bwd_dq<<<dim3((unsigned)a.n_qt, (unsigned)Hq, (unsigned)(T / S)), kAttnBwdThreads, kDqSmem, L.stream>>>(
       tq, tdo, tdq, a);
   if (L.launches) ++*L.launches;
   return cudaGetLastError();
