@@ -1,0 +1,79 @@
+"""bench.py's per-launch work plan (CPU, no GPU): the plan maps every traced launch of a step to
+its algorithmic bytes and FLOPs, from which the bench derives the roofline and the per-kernel
+table, so it must stay in step with the library and the workloads.
+  * every plan entry names a kernel kind the library's trace reports;
+  * the GEMM FLOPs of a step add up to the workload's algorithmic count (6Tdf forward, 18Tdf
+    forward + backward, plus the QKV and O projections), in every precision mode; the recompute
+    mode adds exactly one gate/up GEMM of executed work;
+  * the attention kernels' executed FLOPs are 18 products per causal pair and head against the
+    algorithmic 14 (the backward kernels recompute S and dP), 128 x 2 FLOPs each.
+"""
+
+import dataclasses
+
+import pytest
+
+import bench
+import synth
+
+
+@pytest.fixture(scope="module")
+def kernel_names():
+    from fp8_absmax_reduce_gb300 import build as b
+    b.build()
+    import fp8_absmax_reduce_gb300 as fq
+    lib = fq.load_library()
+    names = set()
+    for k in range(64):
+        n = lib.fp8q_kernel_name(k).decode()
+        if n != "unknown":
+            names.add(n)
+    return names
+
+
+def modes(w):
+    out = [dict()]
+    if w.backward:
+        out += [dict(recompute=True)]
+    out += [dict(bf16=True)]
+    return out
+
+
+@pytest.mark.parametrize("w", synth.WORKLOADS, ids=lambda w: w.name)
+def test_plan_names_are_library_kernels(w, kernel_names):
+    for m in modes(w):
+        plan = bench.step_work(w, **m)
+        assert plan
+        for name, nbytes, flops in plan:
+            assert name in kernel_names, (w.name, m, name)
+            assert nbytes > 0 and flops >= 0
+
+
+@pytest.mark.parametrize("w", synth.WORKLOADS, ids=lambda w: w.name)
+def test_plan_gemm_flops_match_the_workload(w):
+    T, d, f = w.T, w.d, w.f
+    for m in modes(w):
+        plan = bench.step_work(w, **m)
+        gemm = sum(fl for name, _, fl in plan if name.startswith("gemm"))
+        want = w.gemm_flops() + (2.0 * T * d * 2 * f if m.get("recompute") else 0.0)
+        assert gemm == pytest.approx(want, rel=1e-12), (w.name, m)
+
+
+def test_plan_attention_flops():
+    w = synth.BY_NAME["32b-block-attn-fwd-bwd"]
+    for m in (dict(), dict(bf16=True)):
+        plan = bench.step_work(w, **m)
+        attn = sum(fl for name, _, fl in plan if name.startswith("attn"))
+        assert attn == pytest.approx(w.attention_flops() * 18 / 14, rel=1e-12)
+    fwd_only = dataclasses.replace(w, dy_std=0.0)
+    plan = bench.step_work(fwd_only)
+    attn = sum(fl for name, _, fl in plan if name.startswith("attn"))
+    assert attn == pytest.approx(fwd_only.attention_flops(), rel=1e-12)
+
+
+def test_attention_flops_closed_form():
+    """S(S+1)/2 causal pairs per sequence and head, 128 x 2 FLOPs per pair and product."""
+    w = dataclasses.replace(synth.BY_NAME["32b-block-attn-fwd-bwd"], T=8, seq_len=4, n_heads=2)
+    pairs = 2 * (4 * 5 // 2)  # two sequences of 4 tokens
+    assert w.attention_flops() == pairs * 2 * 256 * 7
+    assert dataclasses.replace(w, dy_std=0.0).attention_flops() == pairs * 2 * 256 * 2
