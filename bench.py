@@ -7,9 +7,12 @@ One step = mlp_block_fwd + mlp_block_bwd of the chosen workload (default: the
 epilogues, SwiGLU requantization and the RMSNorm backward.
 
 Prints one JSON line.  value = algorithmic GEMM TFLOP/s of the whole job
-(18*T*d*f per step, summed over ranks); e2e = the same metric with every
-step's inputs copied from pinned host memory and every output copied back
-inside the timed region.  The roofline object is for the dominant kernel (the
+(18*T*d*f per step, summed over ranks); e2e = the same metric with each
+step's batch (activations and upstream gradients in, block output and input
+gradients out) copied between pinned host memory and the device inside the
+timed region, the model state resident in HBM; e2e_all_io = the same with
+every input and output, weights and weight gradients included, through the
+host.  The roofline object is for the dominant kernel (the
 tcgen05 GEMM), timed live with CUDA events recorded by the library around each
 of its launches inside the timed region.
 
@@ -336,55 +339,71 @@ def run_ours(args, rank, world, local_rank):
 
     ms = max_over_ranks(ms, dev)
 
-    # ---- e2e: pinned host inputs in, every output back out, inside the timed region
-    e2e = None
+    # ---- e2e: each step's inputs in from pinned host memory and its outputs back out, inside
+    # the timed region.  "batch": the tensors a training step exchanges with the host -- the
+    # activations and upstream gradients in, the block output and input gradients out -- with the
+    # model state (weights, gains, weight gradients) resident in HBM; "all": every input and
+    # output through the host, weights and fp32 weight gradients included.
+    e2e = e2e_all = None
     if not args.no_e2e:
+        batch_in = [k for k in ("x", "dY", "att", "dQKV") if k in dev_in]
+        batch_out = [k for k in ("y", "dX", "d_att") if k in dev_out]
         host_out = {k: torch.empty(t.shape, dtype=t.dtype).pin_memory() for k, t in dev_out.items()}
-        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
-
         Ke = max(3, min(K, 20))
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b2 = None
         if not w.qkv and w.backward:
-            # the library's pipelined executor: every step copies its inputs in from pinned host
-            # memory and its outputs back out, overlapped with the neighbouring steps' compute
             b2 = fq.MlpBuffers.allocate(w.T, w.d, w.f, device=dev, backward=w.backward, bf16=args.bf16)
             b2.recompute, b2.grad_e4m3 = b.recompute, b.grad_e4m3
-            hio = dict(host_in)
-            hio.update({k: host_out[k] for k in host_out})
-            steps = [hio] * Ke
-            fq.mlp_block_run_steps(b, b2, steps[:2])
-            torch.cuda.synchronize()
-            e0.record(stream)
-            fq.mlp_block_run_steps(b, b2, steps)
-            e1.record(stream)
-            torch.cuda.synchronize()
-            del b2
-            e2e_mode = "pipelined: mlp_block_run_steps (step i+1's inputs in and step i-1's outputs out during step i)"
-        else:
-            def e2e_step():
-                for k, t in dev_in.items():
-                    t.copy_(host_in[k], non_blocking=True)
-                step()
-                for k, t in dev_out.items():
-                    host_out[k].copy_(t, non_blocking=True)
+            b2_own = {k: getattr(b2, k) for k in ("g", "W_gu", "W_d", "dW_gu", "dW_d", "dg")}
 
-            for _ in range(2):
-                e2e_step()
-            torch.cuda.synchronize()
-            e0.record(stream)
-            for _ in range(Ke):
-                e2e_step()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            e2e_mode = "serial on one stream: copy in, block_fwd + block_bwd, copy out"
-        ems = max_over_ranks(e0.elapsed_time(e1) / Ke, dev)
-        e2e = {"value": job_throughput(flops, world, ems) / 1e12, "unit": "TFLOP/s", "ms_per_step": ems,
-               "tokens_per_s": world * w.T / (ems * 1e-3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "mode": e2e_mode,
-               "steps": Ke}
+        def measure(keys_in, keys_out):
+            h2d = sum(host_in[k].numel() * host_in[k].element_size() for k in keys_in)
+            d2h = sum(host_out[k].numel() * host_out[k].element_size() for k in keys_out)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            if b2 is not None:
+                # the library's pipelined executor: step i+1's inputs arrive and step i-1's outputs
+                # leave while step i computes; tensors that stay in HBM are shared by both sets
+                resident = [k for k in b2_own if k not in keys_in and k not in keys_out]
+                for k, t in b2_own.items():
+                    setattr(b2, k, getattr(b, k) if k in resident else t)
+                hio = {k: host_in[k] for k in keys_in}
+                hio.update({k: host_out[k] for k in keys_out})
+                steps = [hio] * Ke
+                fq.mlp_block_run_steps(b, b2, steps[:2])
+                torch.cuda.synchronize()
+                e0.record(stream)
+                fq.mlp_block_run_steps(b, b2, steps)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                mode = "pipelined: mlp_block_run_steps (step i+1's inputs in and step i-1's outputs out during step i)"
+            else:
+                def e2e_step():
+                    for k in keys_in:
+                        dev_in[k].copy_(host_in[k], non_blocking=True)
+                    step()
+                    for k in keys_out:
+                        host_out[k].copy_(dev_out[k], non_blocking=True)
+
+                for _ in range(2):
+                    e2e_step()
+                torch.cuda.synchronize()
+                e0.record(stream)
+                for _ in range(Ke):
+                    e2e_step()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                mode = "serial on one stream: copy in, forward (+ backward), copy out"
+            ems = max_over_ranks(e0.elapsed_time(e1) / Ke, dev)
+            return {"value": job_throughput(flops, world, ems) / 1e12, "unit": "TFLOP/s", "ms_per_step": ems,
+                    "tokens_per_s": world * w.T / (ems * 1e-3), "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "h2d": keys_in, "d2h": keys_out, "mode": mode, "steps": Ke}
+
+        e2e = measure(batch_in, batch_out)
+        e2e["resident"] = "model state (weights, gains, weight gradients) in HBM across steps"
+        e2e_all = measure(list(dev_in), list(dev_out))
+        del b2
     return {"ms": ms, "K": K, "launches": launches, "traced": traced, "plan": plan, "clocks": clk.summary(),
-            "status": status, "e2e": e2e, "w": w, "flops": flops}
+            "status": status, "e2e": e2e, "e2e_all": e2e_all, "w": w, "flops": flops}
 
 
 def kernel_table(traced, plan, K, pk):
@@ -576,6 +595,7 @@ def main():
     }
     if r["e2e"]:
         line["e2e"] = r["e2e"]
+        line["e2e_all_io"] = r["e2e_all"]
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_sample_tokens, args.grad_e4m3, args.bf16)
     print(json.dumps(line))

@@ -335,12 +335,14 @@ def mlp_block_bwd(b: MlpBuffers, stream=None):
 def mlp_block_run_steps(b0: MlpBuffers, b1: MlpBuffers, host: list, stream=None):
     """Pipelined training steps from and to host memory (mlp_block_run_steps in include/fp8q.h).
     host: one dict per step with CPU tensors x, g, W_gu, W_d, dY (inputs) and y, dX, dW_gu, dW_d,
-    dg (outputs), ideally pinned.  Device sets b0, b1 alternate; b0's workspace is used."""
+    dg (outputs), ideally pinned; a missing (or None) entry stays on the device in that step.
+    Device sets b0, b1 alternate; b0's workspace is used."""
     n = len(host)
     arr = (FP8QMlpHostIO * n)()
     for i, h in enumerate(host):
         for name, _ in FP8QMlpHostIO._fields_:
-            setattr(arr[i], name, h[name].data_ptr())
+            t = h.get(name)
+            setattr(arr[i], name, t.data_ptr() if t is not None else None)
     s0, s1 = b0.struct(), b1.struct()
     _check("mlp_block_run_steps", lib.mlp_block_run_steps(ctypes.byref(s0), ctypes.byref(s1), arr, n, _ptr(b0.ws),
                                                           b0.ws.numel(), _stream(stream)))

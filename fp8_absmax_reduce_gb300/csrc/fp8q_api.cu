@@ -904,15 +904,20 @@ int mlp_block_run_steps(const fp8q_mlp* dev0, const fp8q_mlp* dev1, const fp8q_m
   for (const fp8q_mlp* m : dev)
     if ((e = validate_mlp(m, true))) return e;
   if (!same_shape(dev0, dev1) || !host || n_steps < 1) return FP8Q_ERR_INVALID_ARG;
-  if (dev0->x == dev1->x || dev0->dY == dev1->dY || dev0->W_gu == dev1->W_gu || dev0->W_d == dev1->W_d ||
-      dev0->g == dev1->g || dev0->y == dev1->y || dev0->dX == dev1->dX || dev0->dW_gu == dev1->dW_gu ||
-      dev0->dW_d == dev1->dW_d || dev0->dg == dev1->dg)
-    return FP8Q_ERR_INVALID_ARG;
+  // A buffer both sets share must stay on the device: a copy into or out of it would race with
+  // the other set's step.
+  bool moved[10] = {};
   for (int i = 0; i < n_steps; ++i) {
     const fp8q_mlp_host_io& h = host[i];
-    if (!h.x || !h.g || !h.W_gu || !h.W_d || !h.dY || !h.y || !h.dX || !h.dW_gu || !h.dW_d || !h.dg)
-      return FP8Q_ERR_INVALID_ARG;
+    const void* hp[10] = {h.x, h.g, h.W_gu, h.W_d, h.dY, h.y, h.dX, h.dW_gu, h.dW_d, h.dg};
+    for (int k = 0; k < 10; ++k) moved[k] = moved[k] || hp[k] != nullptr;
   }
+  const void* d0[10] = {dev0->x, dev0->g, dev0->W_gu, dev0->W_d, dev0->dY, dev0->y, dev0->dX, dev0->dW_gu,
+                        dev0->dW_d, dev0->dg};
+  const void* d1[10] = {dev1->x, dev1->g, dev1->W_gu, dev1->W_d, dev1->dY, dev1->y, dev1->dX, dev1->dW_gu,
+                        dev1->dW_d, dev1->dg};
+  for (int k = 0; k < 10; ++k)
+    if (moved[k] && d0[k] == d1[k]) return FP8Q_ERR_INVALID_ARG;
   if ((e = check_ws(ws, ws_bytes, mlp_block_workspace_size(dev0->T, dev0->d, dev0->f, 1)))) return e;
   CopyEngines* ce = nullptr;
   if ((e = copy_engines(&ce))) return e;
@@ -932,11 +937,11 @@ int mlp_block_run_steps(const fp8q_mlp* dev0, const fp8q_mlp* dev1, const fp8q_m
     const fp8q_mlp_host_io& h = host[i];
     // inputs into set s once step i-2 (the set's last user) has finished computing
     if (i >= 2) FP8Q_CUDA(cudaStreamWaitEvent(ce->h2d, ce->compute_done[s], 0));
-    FP8Q_CUDA(cudaMemcpyAsync((void*)m->x, h.x, T * d * 2, cudaMemcpyHostToDevice, ce->h2d));
-    FP8Q_CUDA(cudaMemcpyAsync((void*)m->g, h.g, d * 2, cudaMemcpyHostToDevice, ce->h2d));
-    FP8Q_CUDA(cudaMemcpyAsync((void*)m->W_gu, h.W_gu, d * 2 * f * 2, cudaMemcpyHostToDevice, ce->h2d));
-    FP8Q_CUDA(cudaMemcpyAsync((void*)m->W_d, h.W_d, f * d * 2, cudaMemcpyHostToDevice, ce->h2d));
-    FP8Q_CUDA(cudaMemcpyAsync((void*)m->dY, h.dY, T * d * 2, cudaMemcpyHostToDevice, ce->h2d));
+    const struct { void* dst; const void* src; size_t bytes; } in[5] = {
+        {(void*)m->x, h.x, T * d * 2}, {(void*)m->g, h.g, d * 2}, {(void*)m->W_gu, h.W_gu, d * 2 * f * 2},
+        {(void*)m->W_d, h.W_d, f * d * 2}, {(void*)m->dY, h.dY, T * d * 2}};
+    for (const auto& cp : in)
+      if (cp.src) FP8Q_CUDA(cudaMemcpyAsync(cp.dst, cp.src, cp.bytes, cudaMemcpyHostToDevice, ce->h2d));
     FP8Q_CUDA(cudaEventRecord(ce->in_done[s], ce->h2d));
     // compute once the inputs are in and step i-2's outputs have left this set
     FP8Q_CUDA(cudaStreamWaitEvent(cs, ce->in_done[s], 0));
@@ -946,11 +951,11 @@ int mlp_block_run_steps(const fp8q_mlp* dev0, const fp8q_mlp* dev1, const fp8q_m
     FP8Q_CUDA(cudaEventRecord(ce->compute_done[s], cs));
     // outputs back to the host
     FP8Q_CUDA(cudaStreamWaitEvent(ce->d2h, ce->compute_done[s], 0));
-    FP8Q_CUDA(cudaMemcpyAsync(h.y, m->y, T * d * 2, cudaMemcpyDeviceToHost, ce->d2h));
-    FP8Q_CUDA(cudaMemcpyAsync(h.dX, m->dX, T * d * 2, cudaMemcpyDeviceToHost, ce->d2h));
-    FP8Q_CUDA(cudaMemcpyAsync(h.dW_gu, m->dW_gu, d * 2 * f * 4, cudaMemcpyDeviceToHost, ce->d2h));
-    FP8Q_CUDA(cudaMemcpyAsync(h.dW_d, m->dW_d, f * d * 4, cudaMemcpyDeviceToHost, ce->d2h));
-    FP8Q_CUDA(cudaMemcpyAsync(h.dg, m->dg, d * 4, cudaMemcpyDeviceToHost, ce->d2h));
+    const struct { void* dst; const void* src; size_t bytes; } out[5] = {
+        {h.y, m->y, T * d * 2}, {h.dX, m->dX, T * d * 2}, {h.dW_gu, m->dW_gu, d * 2 * f * 4},
+        {h.dW_d, m->dW_d, f * d * 4}, {h.dg, m->dg, d * 4}};
+    for (const auto& cp : out)
+      if (cp.dst) FP8Q_CUDA(cudaMemcpyAsync(cp.dst, cp.src, cp.bytes, cudaMemcpyDeviceToHost, ce->d2h));
     FP8Q_CUDA(cudaEventRecord(ce->out_done[s], ce->d2h));
   }
   // the caller's stream ends after the last outputs (and every earlier copy) have landed

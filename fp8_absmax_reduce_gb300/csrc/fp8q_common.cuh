@@ -136,6 +136,12 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   return r;
 }
 __device__ __forceinline__ uint4 ld_v4(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+// Requests the L2 lines of the `bytes` bytes at p (bytes > 0, all inside one allocation).
+__device__ __forceinline__ void prefetch_l2_span(const void* p, int bytes) {
+  const char* c = static_cast<const char*>(p);
+  for (int b = 0; b < bytes; b += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(c + b));
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(c + bytes - 1));
+}
 __device__ __forceinline__ void st_v4(void* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 
 // --------------------------------------------------------------------------

@@ -355,6 +355,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
       int mb, nb;
       tile_coords(tile, p, mb, nb);
+      const int row0 = mb * BM + sub * 32;
+      const int row = row0 + lane;
+      const bool row_ok = row < p.M;
+      const bool warp_ok = row0 < p.M;  // any row of this warp's slice in range
+      // The SwiGLU backward's first H chunk is requested before the accumulator is ready.  (An
+      // L2 prefetch of the warp's whole part of the tile measured slower: one request per lane
+      // and line through the same load path as the chunks themselves.)
+      uint4 hn[8];
+      if (p.epi == kEpiSwigluBwd) {
+        const int cs = nb * BN + 128 * half;
+        if (row_ok && cs < p.N) load_h_chunk(p, row, cs, min(32, p.N - cs), hn);
+      }
       // lane 0 waits and the warp follows its result: the tcgen05.ld below is warp-collective,
       // so a time-out must take the whole warp out together
       int full_ok = 0;
@@ -366,10 +378,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(sub * 32) << 16);
-      const int row0 = mb * BM + sub * 32;
-      const int row = row0 + lane;
-      const bool row_ok = row < p.M;
-      const bool warp_ok = row0 < p.M;  // any row of this warp's slice in range
       if (p.epi == kEpiSwiglu) {
         const int col0 = nb * 128;
 #pragma unroll 1
@@ -433,13 +441,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else if (p.epi == kEpiSwigluBwd) {
-        // the next chunk's H words are in flight while the current chunk is computed
+        // the next chunk's H words are in flight while the current chunk is computed (the
+        // first chunk's were requested before the accumulator wait)
         const int col0 = nb * BN;
-        uint4 hn[8];
-        {
-          const int col = col0 + 4 * half * 32;
-          if (row_ok && col < p.N) load_h_chunk(p, row, col, min(32, p.N - col), hn);
-        }
 #pragma unroll 1
         for (int c = 4 * half; c < 4 * half + 4; ++c) {
           uint4 hc[8];
@@ -691,6 +695,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
       int mb, nb;
       tile_coords(tile, p, mb, nb);
+      const int row0 = mb * 256 + hm * 128 + sub * 32;
+      const int row = row0 + lane;
+      const bool row_ok = row < p.M;
+      const bool warp_ok = row0 < p.M;
+      const int col0 = nb * BN;
+      // The residual is requested before the accumulator is ready (this epilogue does not overlap
+      // the next tile's MMAs, so its read latency would be exposed): the L2 lines of the lane's
+      // row segment, and the first chunk's words into registers; chunk c + 1's words are then in
+      // flight while chunk c is computed.
+      const bool res = !p.out_f32 && p.epi == kEpiResidual;
+      uint4 rn[4];
+      if (res && row_ok && col0 < p.N) {
+        const uint16_t* r = p.R + (int64_t)row * p.ldr + col0;
+        prefetch_l2_span(r, 2 * min(BN, p.N - col0));
+        if (p.N - col0 >= 32)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) rn[q] = ld_v4(r + 8 * q);
+      }
       int full_ok = 0;
       if (lane == 0) full_ok = mbar_wait(tfull, acc_phase, abort_flag) ? 1 : 0;
       if (!__shfl_sync(0xFFFFFFFFu, full_ok, 0)) {
@@ -700,17 +722,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t tbase = tmem_base + (uint32_t)(hm * BN) + ((uint32_t)(sub * 32) << 16);
-      const int row0 = mb * 256 + hm * 128 + sub * 32;
-      const int row = row0 + lane;
-      const bool row_ok = row < p.M;
-      const bool warp_ok = row0 < p.M;
-      const int col0 = nb * BN;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t acc32[32];
         tmem_ld32(tbase + c * 32, acc32);
         const int col = col0 + c * 32;
         const int ncol = min(32, p.N - col);
+        uint4 rc[4];
+        if (res) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) rc[q] = rn[q];
+          if (c + 1 < BN / 32 && row_ok && p.N - (col + 32) >= 32) {
+            const uint16_t* r = p.R + (int64_t)row * p.ldr + col + 32;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) rn[q] = ld_v4(r + 8 * q);
+          }
+        }
         if (!warp_ok || ncol <= 0) continue;
         float v[32];
         if (p.out_f32) {
@@ -720,7 +747,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           float rv[32];
           const uint16_t* r = p.R + (int64_t)row * p.ldr + col;
           if (row_ok && ncol == 32) {
-            load_bf16x32(r, rv);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t ww[4] = {rc[q].x, rc[q].y, rc[q].z, rc[q].w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) { rv[8 * q + 2 * k] = bf16_lo(ww[k]); rv[8 * q + 2 * k + 1] = bf16_hi(ww[k]); }
+            }
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) rv[j] = (row_ok && j < ncol) ? __uint_as_float((uint32_t)r[j] << 16) : 0.0f;

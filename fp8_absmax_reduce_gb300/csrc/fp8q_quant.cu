@@ -11,6 +11,9 @@
 //           scale = fmax/amax, and casts with cvt.rn.satfinite to E4M3/E5M2.
 // No atomics on floating point, no counters to reset: deterministic and
 // re-entrant on one stream.
+#include <algorithm>
+#include <climits>
+
 #include "fp8q_common.cuh"
 #include "fp8q_internal.h"
 
@@ -158,81 +161,112 @@ __global__ void __launch_bounds__(kThreads) k_quant_cast(const uint8_t* __restri
 // The fp32 sum of squares is the pairwise sum of the row (zero-padded to 8192
 // terms, which adds exact zeros only): an 8-leaf tree per lane, a butterfly
 // across lanes (each level adds adjacent subtrees), then a tree over the 32
-// chunk sums.
+// chunk sums.  NC (even, >= the row's 256-element chunks) bounds the chunks:
+// the chunks from NC to 32 are all zero, so the tree's additions of a chunk at
+// or beyond NC add exact zeros and are left out.
+// The kernel is latency-bound (a row's work is one dependent chain per warp),
+// so it runs many warps (64 registers a thread) and does two chunks per
+// instruction with the packed fp32 operations (__fmul2_rn / __fadd2_rn: each
+// half rounds exactly like __fmul_rn / __fadd_rn, so the sums are unchanged).
+// The second half of the pass re-reads the row (from L1).
 // OUT16 (the BF16 baseline): instead of the absmax partials, the same pass
 // writes n = bf16((x rstd) g) -- there is no scale to wait for.
-template <bool OUT16>
-__global__ void __launch_bounds__(kThreads) k_rmsnorm_stats(const uint16_t* __restrict__ x,
-                                                            const uint16_t* __restrict__ g, int64_t T, int d,
-                                                            float eps, float* __restrict__ rstd,
-                                                            uint32_t* __restrict__ partial,
-                                                            uint16_t* __restrict__ n16) {
+constexpr int kStatsWarps = 8;
+// resident blocks per SM: 64 registers a thread up to 16 chunks, more for longer rows
+constexpr int stats_blocks_per_sm(int nc) { return nc <= 16 ? 4 : nc <= 24 ? 3 : 2; }
+
+template <bool OUT16, int NC>
+__global__ void __launch_bounds__(kStatsWarps * 32, stats_blocks_per_sm(NC))
+    k_rmsnorm_stats(const uint16_t* __restrict__ x, const uint16_t* __restrict__ g, int64_t T, int d, float eps,
+                    float* __restrict__ rstd, uint32_t* __restrict__ partial, uint16_t* __restrict__ n16) {
   __shared__ uint32_t red[32];
   const int lane = threadIdx.x & 31;
-  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t nw = (int64_t)gridDim.x * kStatsWarps;
   uint32_t m = 0;
-  for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < T; row += nw) {
+  for (int64_t row = (int64_t)blockIdx.x * kStatsWarps + (threadIdx.x >> 5); row < T; row += nw) {
     const uint16_t* xr = x + row * d;
-    // all of the row's loads first, then the lane-level trees, then the butterflies
-    uint4 w[32];
+    float cs[NC];
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      const int j0 = c * 256 + lane * 8;
-      w[c] = (c * 256 < d && j0 < d) ? ld_v4(xr + j0) : make_uint4(0u, 0u, 0u, 0u);
-    }
-    float cs[32];
-#pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      const uint32_t ww[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
-      float s[8];
+    for (int c = 0; c < NC; c += 2) {
+      // chunk c in the .x halves, chunk c + 1 in the .y halves
+      const int j0 = c * 256 + lane * 8, j1 = j0 + 256;
+      const uint4 a = j0 < d ? ld_v4(xr + j0) : make_uint4(0u, 0u, 0u, 0u);
+      const uint4 b = j1 < d ? ld_v4(xr + j1) : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+      float2 q[8];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float lo = bf16_lo(ww[k]), hi = bf16_hi(ww[k]);
-        s[2 * k] = __fmul_rn(lo, lo);
-        s[2 * k + 1] = __fmul_rn(hi, hi);
+        const float2 lo = make_float2(bf16_lo(aw[k]), bf16_lo(bw[k]));
+        const float2 hi = make_float2(bf16_hi(aw[k]), bf16_hi(bw[k]));
+        q[2 * k] = __fmul2_rn(lo, lo);
+        q[2 * k + 1] = __fmul2_rn(hi, hi);
       }
-      cs[c] = __fadd_rn(__fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3])),
-                        __fadd_rn(__fadd_rn(s[4], s[5]), __fadd_rn(s[6], s[7])));
+      const float2 t = __fadd2_rn(__fadd2_rn(__fadd2_rn(q[0], q[1]), __fadd2_rn(q[2], q[3])),
+                                  __fadd2_rn(__fadd2_rn(q[4], q[5]), __fadd2_rn(q[6], q[7])));
+      cs[c] = t.x;
+      cs[c + 1] = t.y;
     }
+    // (a chunk past the row's end holds zeros, and zero + zero is exact)
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1)
 #pragma unroll
-      for (int c = 0; c < 32; ++c)
-        if (c * 256 < d) cs[c] = __fadd_rn(cs[c], __shfl_xor_sync(0xFFFFFFFFu, cs[c], o));
+      for (int c = 0; c < NC; c += 2)
+        if (c * 256 < d) {
+          const float2 sh = make_float2(__shfl_xor_sync(0xFFFFFFFFu, cs[c], o),
+                                        __shfl_xor_sync(0xFFFFFFFFu, cs[c + 1], o));
+          const float2 t = __fadd2_rn(make_float2(cs[c], cs[c + 1]), sh);
+          cs[c] = t.x;
+          cs[c + 1] = t.y;
+        }
 #pragma unroll
-    for (int w = 1; w < 32; w <<= 1)
+    for (int v = 1; v < 32; v <<= 1)
 #pragma unroll
-      for (int i = 0; i < 32; i += 2 * w) cs[i] = __fadd_rn(cs[i], cs[i + w]);
+      for (int k = 0; k < 32; k += 2 * v)
+        if (k + v < NC) cs[k] = __fadd_rn(cs[k], cs[k + v]);
     const float rs = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(cs[0], (float)d), eps)));
     if (lane == 0) rstd[row] = rs;
-    if (OUT16) {
-      // the row is re-read from L1 (holding it in registers across the sums spills)
-      for (int j0 = lane * 8; j0 < d; j0 += 256) {
-        const uint4 xv = ld_v4(xr + j0), gw = ld_v4(g + j0);
-        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, gg[4] = {gw.x, gw.y, gw.z, gw.w};
-        uint32_t o[4];
+    const float2 rs2 = make_float2(rs, rs);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          o[k] = pack_bf16x2(__fmul_rn(__fmul_rn(bf16_lo(xw[k]), rs), bf16_lo(gg[k])),
-                             __fmul_rn(__fmul_rn(bf16_hi(xw[k]), rs), bf16_hi(gg[k])));
-        st_v4(n16 + row * d + j0, make_uint4(o[0], o[1], o[2], o[3]));
-      }
-    } else {
-      for (int j0 = lane * 8; j0 < d; j0 += 256) {
-        const uint4 w = ld_v4(xr + j0), gw = ld_v4(g + j0);
-        const uint32_t xw[4] = {w.x, w.y, w.z, w.w}, gg[4] = {gw.x, gw.y, gw.z, gw.w};
+    for (int c = 0; c < NC; ++c) {
+      const int j0 = c * 256 + lane * 8;
+      if (j0 >= d) continue;
+      const uint4 gw = ld_v4(g + j0), xv = ld_v4(xr + j0);
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, gg[4] = {gw.x, gw.y, gw.z, gw.w};
+      uint32_t o[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          m = max(m, abs_bits(__fmul_rn(__fmul_rn(bf16_lo(xw[k]), rs), bf16_lo(gg[k]))));
-          m = max(m, abs_bits(__fmul_rn(__fmul_rn(bf16_hi(xw[k]), rs), bf16_hi(gg[k]))));
-        }
+      for (int k = 0; k < 4; ++k) {
+        const float2 n = __fmul2_rn(__fmul2_rn(make_float2(bf16_lo(xw[k]), bf16_hi(xw[k])), rs2),
+                                    make_float2(bf16_lo(gg[k]), bf16_hi(gg[k])));
+        if (OUT16) o[k] = pack_bf16x2(n.x, n.y);
+        else m = max(m, max(abs_bits(n.x), abs_bits(n.y)));
       }
+      if (OUT16) st_v4(n16 + row * d + j0, make_uint4(o[0], o[1], o[2], o[3]));
     }
   }
   if (!OUT16) {
     m = block_max_u32(m, red);
     if (threadIdx.x == 0) partial[blockIdx.x] = m;
   }
+}
+
+// Launches k_rmsnorm_stats with the smallest chunk bound that holds a row of d elements, on a
+// grid of at most one wave of resident blocks and at most `cap`; returns the grid size.
+template <bool OUT16>
+int rmsnorm_stats_dispatch(int64_t T, int d, int64_t cap, const Launch& L, const uint16_t* x, const uint16_t* g,
+                           float eps, float* rstd, uint32_t* partial, uint16_t* n16) {
+  const int nc = d <= 1024 ? 4 : d <= 2048 ? 8 : d <= 4096 ? 16 : d <= 6144 ? 24 : 32;
+  const int64_t blocks = (T + kStatsWarps - 1) / kStatsWarps;
+  const int64_t fit = (int64_t)L.num_sms * stats_blocks_per_sm(nc);
+  const int grid = (int)std::min<int64_t>(blocks, std::min<int64_t>(fit, cap));
+  const int th = kStatsWarps * 32;
+  switch (nc) {
+    case 4: k_rmsnorm_stats<OUT16, 4><<<grid, th, 0, L.stream>>>(x, g, T, d, eps, rstd, partial, n16); break;
+    case 8: k_rmsnorm_stats<OUT16, 8><<<grid, th, 0, L.stream>>>(x, g, T, d, eps, rstd, partial, n16); break;
+    case 16: k_rmsnorm_stats<OUT16, 16><<<grid, th, 0, L.stream>>>(x, g, T, d, eps, rstd, partial, n16); break;
+    case 24: k_rmsnorm_stats<OUT16, 24><<<grid, th, 0, L.stream>>>(x, g, T, d, eps, rstd, partial, n16); break;
+    default: k_rmsnorm_stats<OUT16, 32><<<grid, th, 0, L.stream>>>(x, g, T, d, eps, rstd, partial, n16); break;
+  }
+  return grid;
 }
 
 __global__ void __launch_bounds__(kThreads) k_rmsnorm_cast(const uint16_t* __restrict__ x,
@@ -521,21 +555,17 @@ cudaError_t launch_quant_cast(const void* x, int dtype, int64_t n, int fmt, cons
 
 cudaError_t launch_rmsnorm_stats(const uint16_t* x, const uint16_t* g, int64_t T, int d, float eps, float* rstd,
                                  uint32_t* partial, int* P, const Launch& L) {
-  const int warps_per_block = kThreads / 32;
-  int64_t blocks = (T + warps_per_block - 1) / warps_per_block;
-  const int grid = (int)(blocks < kMaxPartials ? blocks : kMaxPartials);
+  // one wave of resident blocks, each warp looping over rows; one absmax partial per block
+  const int grid = rmsnorm_stats_dispatch<false>(T, d, kMaxPartials, L, x, g, eps, rstd, partial, nullptr);
+  if (grid < 1) return cudaErrorInvalidConfiguration;
   *P = grid;
-  k_rmsnorm_stats<false><<<grid, kThreads, 0, L.stream>>>(x, g, T, d, eps, rstd, partial, nullptr);
   return post_launch(L);
 }
 
 cudaError_t launch_rmsnorm_bf16(const uint16_t* x, const uint16_t* g, int64_t T, int d, float eps, float* rstd,
                                 uint16_t* n16, const Launch& L) {
-  const int warps_per_block = kThreads / 32;
-  const int64_t blocks = (T + warps_per_block - 1) / warps_per_block;
-  const int64_t cap = (int64_t)L.num_sms * 16;
-  const int grid = (int)(blocks < cap ? blocks : cap);
-  k_rmsnorm_stats<true><<<grid, kThreads, 0, L.stream>>>(x, g, T, d, eps, rstd, nullptr, n16);
+  if (rmsnorm_stats_dispatch<true>(T, d, INT32_MAX, L, x, g, eps, rstd, nullptr, n16) < 1)
+    return cudaErrorInvalidConfiguration;
   return post_launch(L);
 }
 

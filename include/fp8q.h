@@ -235,9 +235,12 @@ FP8Q_API int mlp_block_bwd(const fp8q_mlp* m, void* ws, size_t ws_bytes, fp8q_st
  * `stream`, and copies the outputs (y, dX, dW_gu, dW_d, dg) back into host[i].  The copies run on
  * two streams of the library's own, ordered by events, so step i+1's inputs arrive and step
  * i-1's outputs leave while step i computes; the kernels stay in order on `stream`, so one
- * workspace serves both sets (mlp_block_workspace_size(T, d, f, 1) bytes).  dev0 and dev1 must
- * have the same sizes and switches, distinct input and output buffers (their intermediates may
- * be shared); host buffers should be pinned (pageable memory makes the copies synchronous).
+ * workspace serves both sets (mlp_block_workspace_size(T, d, f, 1) bytes).  A null host pointer
+ * means that tensor does not cross the host link in that step: an input already resident on the
+ * device (the weights and gain of a model kept in HBM), an output left there (weight gradients
+ * for an optimizer on the device).  dev0 and dev1 must have the same sizes and switches; a buffer
+ * they share must have a null host pointer in every step (their intermediates may be shared
+ * freely).  Host buffers should be pinned (pageable memory makes the copies synchronous).
  * Returns once everything is enqueued; `stream` is ordered after the last copy, so a
  * synchronisation of `stream` (or an event recorded on it) covers the whole run.  The pages
  * describe no such runtime; this is the executor a trainer feeding the block from the host uses. */

@@ -77,7 +77,10 @@ def test_quantize_zero_and_nonfinite_status():
     np.testing.assert_array_equal(q, qo)
 
 
-@pytest.mark.parametrize("T,d", [(1, 16), (37, 528), (256, 512), (1000, 3584), (64, 8192)])
+# d spans every chunk bound of the row kernel (<= 1024, 2048, 4096, 6144, 8192 elements); T = 5000
+# gives its warps several rows each.
+@pytest.mark.parametrize("T,d", [(1, 16), (37, 528), (256, 512), (1000, 3584), (64, 8192), (5000, 1040),
+                                 (150, 2064), (200, 4112), (300, 5120), (100, 6160)])
 def test_rmsnorm_quant_bit_exact(T, d):
     w = synth.BY_NAME["3b-mlp-fwd"]
     x = synth.activations(w, T, d, seed=T, tensor_id=synth.TID_X, outlier_id=synth.TID_OUTLIER)
