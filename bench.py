@@ -350,60 +350,67 @@ def run_ours(args, rank, world, local_rank):
         batch_out = [k for k in ("y", "dX", "d_att") if k in dev_out]
         host_out = {k: torch.empty(t.shape, dtype=t.dtype).pin_memory() for k, t in dev_out.items()}
         Ke = max(3, min(K, 20))
-        b2 = None
-        if not w.qkv and w.backward:
+        # the second device set of the library's pipelined executor (step i+1's inputs arrive and
+        # step i-1's outputs leave while step i computes); tensors that stay in HBM are shared
+        if w.qkv:
+            b2 = fq.BlockBuffers.allocate(w.T, w.d, w.f, w.qkv, device=dev, backward=w.backward, core=core,
+                                          bf16=args.bf16)
+            run, run_name = (lambda bb, steps: fq.block_run_steps(bb[0], bb[1], steps, backward=w.backward)), \
+                "block_run_steps"
+            state = ("g1", "W_qkv", "W_o", "g", "W_gu", "W_d") + (
+                ("dW_qkv", "dW_o", "dg1", "dW_gu", "dW_d", "dg") if w.backward else ())
+        else:
             b2 = fq.MlpBuffers.allocate(w.T, w.d, w.f, device=dev, backward=w.backward, bf16=args.bf16)
-            b2.recompute, b2.grad_e4m3 = b.recompute, b.grad_e4m3
-            b2_own = {k: getattr(b2, k) for k in ("g", "W_gu", "W_d", "dW_gu", "dW_d", "dg")}
+            if w.backward:
+                run, run_name = (lambda bb, steps: fq.mlp_block_run_steps(bb[0], bb[1], steps)), "mlp_block_run_steps"
+            else:
+                run, run_name = (lambda bb, steps: fq.mlp_block_fwd_run_steps(bb[0], bb[1], steps)), \
+                    "mlp_block_fwd_run_steps"
+            state = ("g", "W_gu", "W_d") + (("dW_gu", "dW_d", "dg") if w.backward else ())
+        (b2.mlp if w.qkv else b2).recompute = bool(args.recompute)
+        (b2.mlp if w.qkv else b2).grad_e4m3 = bool(args.grad_e4m3)
+        b2_own = {k: buf_get(b2, k) for k in state}
 
         def measure(keys_in, keys_out):
             h2d = sum(host_in[k].numel() * host_in[k].element_size() for k in keys_in)
             d2h = sum(host_out[k].numel() * host_out[k].element_size() for k in keys_out)
+            for k in state:
+                buf_set(b2, k, b2_own[k] if k in keys_in or k in keys_out else buf_get(b, k))
+            hio = {k: host_in[k] for k in keys_in}
+            hio.update({k: host_out[k] for k in keys_out})
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            if b2 is not None:
-                # the library's pipelined executor: step i+1's inputs arrive and step i-1's outputs
-                # leave while step i computes; tensors that stay in HBM are shared by both sets
-                resident = [k for k in b2_own if k not in keys_in and k not in keys_out]
-                for k, t in b2_own.items():
-                    setattr(b2, k, getattr(b, k) if k in resident else t)
-                hio = {k: host_in[k] for k in keys_in}
-                hio.update({k: host_out[k] for k in keys_out})
-                steps = [hio] * Ke
-                fq.mlp_block_run_steps(b, b2, steps[:2])
-                torch.cuda.synchronize()
-                e0.record(stream)
-                fq.mlp_block_run_steps(b, b2, steps)
-                e1.record(stream)
-                torch.cuda.synchronize()
-                mode = "pipelined: mlp_block_run_steps (step i+1's inputs in and step i-1's outputs out during step i)"
-            else:
-                def e2e_step():
-                    for k in keys_in:
-                        dev_in[k].copy_(host_in[k], non_blocking=True)
-                    step()
-                    for k in keys_out:
-                        host_out[k].copy_(dev_out[k], non_blocking=True)
-
-                for _ in range(2):
-                    e2e_step()
-                torch.cuda.synchronize()
-                e0.record(stream)
-                for _ in range(Ke):
-                    e2e_step()
-                e1.record(stream)
-                torch.cuda.synchronize()
-                mode = "serial on one stream: copy in, forward (+ backward), copy out"
+            run((b, b2), [hio] * 2)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            run((b, b2), [hio] * Ke)
+            e1.record(stream)
+            torch.cuda.synchronize()
             ems = max_over_ranks(e0.elapsed_time(e1) / Ke, dev)
             return {"value": job_throughput(flops, world, ems) / 1e12, "unit": "TFLOP/s", "ms_per_step": ems,
                     "tokens_per_s": world * w.T / (ems * 1e-3), "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "h2d": keys_in, "d2h": keys_out, "mode": mode, "steps": Ke}
+                    "d2h_bytes_per_step": d2h, "h2d": keys_in, "d2h": keys_out,
+                    "mode": f"pipelined: {run_name} (step i+1's inputs in and step i-1's outputs out during step i)",
+                    "steps": Ke}
 
         e2e = measure(batch_in, batch_out)
         e2e["resident"] = "model state (weights, gains, weight gradients) in HBM across steps"
         e2e_all = measure(list(dev_in), list(dev_out))
-        del b2
+        del b2, b2_own
     return {"ms": ms, "K": K, "launches": launches, "traced": traced, "plan": plan, "clocks": clk.summary(),
             "status": status, "e2e": e2e, "e2e_all": e2e_all, "w": w, "flops": flops}
+
+
+_MLP_KEYS = ("g", "W_gu", "W_d", "dY", "y", "dW_gu", "dW_d", "dg")
+
+
+def buf_get(b, k):
+    """A tensor of MlpBuffers or BlockBuffers by its host-IO name (the block's MLP-side ones live
+    in b.mlp)."""
+    return getattr(b.mlp, k) if hasattr(b, "n_qkv") and k in _MLP_KEYS else getattr(b, k)
+
+
+def buf_set(b, k, t):
+    setattr(b.mlp if hasattr(b, "n_qkv") and k in _MLP_KEYS else b, k, t)
 
 
 def kernel_table(traced, plan, K, pk):

@@ -55,6 +55,7 @@ def _load() -> ctypes.CDLL:
     L.mlp_block_bwd.argtypes = [ctypes.POINTER(FP8QMlp), vp, sz, vp]
     L.mlp_block_run_steps.argtypes = [ctypes.POINTER(FP8QMlp), ctypes.POINTER(FP8QMlp), ctypes.POINTER(FP8QMlpHostIO),
                                       i32, vp, sz, vp]
+    L.mlp_block_fwd_run_steps.argtypes = L.mlp_block_run_steps.argtypes
     L.fp8q_get_status.argtypes = [i32]
     L.fp8q_status_string.restype = ctypes.c_char_p
     L.fp8q_status_string.argtypes = [i32]
@@ -63,6 +64,8 @@ def _load() -> ctypes.CDLL:
     L.block_workspace_size.argtypes = [i64, i64, i64, i64, i32]
     L.block_fwd.argtypes = [ctypes.POINTER(FP8QBlock), vp, sz, vp]
     L.block_bwd.argtypes = [ctypes.POINTER(FP8QBlock), vp, sz, vp]
+    L.block_run_steps.argtypes = [ctypes.POINTER(FP8QBlock), ctypes.POINTER(FP8QBlock),
+                                  ctypes.POINTER(FP8QBlockHostIO), i32, i32, vp, sz, vp]
     L.fp8q_selftest_bounded_wait.argtypes = [i64, vp]
     L.fp8q_trace_start.argtypes = [i32]
     L.fp8q_trace_read.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int), i32]
@@ -86,6 +89,12 @@ class FP8QMlp(ctypes.Structure):
 class FP8QMlpHostIO(ctypes.Structure):
     """Mirror of ``fp8q_mlp_host_io`` in include/fp8q.h."""
     _fields_ = [(n, ctypes.c_void_p) for n in ("x", "g", "W_gu", "W_d", "dY", "y", "dX", "dW_gu", "dW_d", "dg")]
+
+
+class FP8QBlockHostIO(ctypes.Structure):
+    """Mirror of ``fp8q_block_host_io`` in include/fp8q.h."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("x", "g1", "W_qkv", "W_o", "att", "g", "W_gu", "W_d", "dY", "dQKV",
+                                               "y", "dX", "d_att", "dW_qkv", "dW_o", "dg1", "dW_gu", "dW_d", "dg")]
 
 
 class FP8QBlock(ctypes.Structure):
@@ -337,15 +346,29 @@ def mlp_block_run_steps(b0: MlpBuffers, b1: MlpBuffers, host: list, stream=None)
     host: one dict per step with CPU tensors x, g, W_gu, W_d, dY (inputs) and y, dX, dW_gu, dW_d,
     dg (outputs), ideally pinned; a missing (or None) entry stays on the device in that step.
     Device sets b0, b1 alternate; b0's workspace is used."""
+    _check("mlp_block_run_steps", lib.mlp_block_run_steps(*_steps_args(b0, b1, host, FP8QMlpHostIO), _ptr(b0.ws),
+                                                          b0.ws.numel(), _stream(stream)))
+
+
+def mlp_block_fwd_run_steps(b0: MlpBuffers, b1: MlpBuffers, host: list, stream=None):
+    """Pipelined forward-only steps from and to host memory (mlp_block_fwd_run_steps in
+    include/fp8q.h): x, g, W_gu, W_d in, y out; entries that are missing stay on the device."""
+    _check("mlp_block_fwd_run_steps", lib.mlp_block_fwd_run_steps(*_steps_args(b0, b1, host, FP8QMlpHostIO),
+                                                                  _ptr(b0.ws), b0.ws.numel(), _stream(stream)))
+
+
+def _steps_args(b0, b1, host, io_type):
+    """(set 0, set 1, host array, step count) for the pipelined executors; a host dict's missing or
+    None entries become null pointers (the tensor stays on the device)."""
     n = len(host)
-    arr = (FP8QMlpHostIO * n)()
+    arr = (io_type * n)()
     for i, h in enumerate(host):
-        for name, _ in FP8QMlpHostIO._fields_:
+        for name, _ in io_type._fields_:
             t = h.get(name)
             setattr(arr[i], name, t.data_ptr() if t is not None else None)
     s0, s1 = b0.struct(), b1.struct()
-    _check("mlp_block_run_steps", lib.mlp_block_run_steps(ctypes.byref(s0), ctypes.byref(s1), arr, n, _ptr(b0.ws),
-                                                          b0.ws.numel(), _stream(stream)))
+    # (each byref keeps its struct alive for the call)
+    return ctypes.byref(s0), ctypes.byref(s1), arr, n
 
 
 def get_status(clear: bool = False) -> int:
@@ -466,6 +489,15 @@ def block_fwd(b: BlockBuffers, stream=None):
 def block_bwd(b: BlockBuffers, stream=None):
     s = b.struct()
     _check("block_bwd", lib.block_bwd(ctypes.byref(s), _ptr(b.ws), b.ws.numel(), _stream(stream)))
+
+
+def block_run_steps(b0: BlockBuffers, b1: BlockBuffers, host: list, backward: bool = True, stream=None):
+    """Pipelined full-block steps from and to host memory (block_run_steps in include/fp8q.h).
+    host: one dict per step, keys as fp8q_block_host_io (x, g1, W_qkv, W_o, att, g, W_gu, W_d, dY,
+    dQKV in; y, dX, d_att, dW_qkv, dW_o, dg1, dW_gu, dW_d, dg out); missing entries stay on the
+    device.  Device sets b0, b1 alternate; b0's workspace is used."""
+    _check("block_run_steps", lib.block_run_steps(*_steps_args(b0, b1, host, FP8QBlockHostIO), int(bool(backward)),
+                                                  _ptr(b0.ws), b0.ws.numel(), _stream(stream)))
 
 
 def selftest_bounded_wait(limit_s: float = 0.02, stream=None):

@@ -857,8 +857,39 @@ int mlp_block_bwd(const fp8q_mlp* m, void* ws, size_t ws_bytes, fp8q_stream stre
 }
 
 // ---------------------------------------------------------------------------
+size_t block_workspace_size(int64_t T, int64_t d, int64_t f, int64_t n_qkv, int backward) {
+  return block_ws_layout(T, d, f, n_qkv, backward, nullptr, nullptr);
+}
+
+int block_fwd(const fp8q_block* b, void* ws, size_t ws_bytes, fp8q_stream stream) {
+  int e = validate_block(b, false);
+  if (e) return e;
+  if ((e = check_ws(ws, ws_bytes, block_workspace_size(b->T, b->d, b->f, b->n_qkv, 0)))) return e;
+  Ctx c;
+  if ((e = make_ctx(&c, stream))) return e;
+  BlockWs w;
+  block_ws_layout(b->T, b->d, b->f, b->n_qkv, 0, static_cast<uint8_t*>(ws), &w);
+  if ((e = block_fwd_run(b, w, c))) return e;
+  return finish(c);
+}
+
+int block_bwd(const fp8q_block* b, void* ws, size_t ws_bytes, fp8q_stream stream) {
+  int e = validate_block(b, true);
+  if (e) return e;
+  if ((e = check_ws(ws, ws_bytes, block_workspace_size(b->T, b->d, b->f, b->n_qkv, 1)))) return e;
+  Ctx c;
+  if ((e = make_ctx(&c, stream))) return e;
+  BlockWs w;
+  block_ws_layout(b->T, b->d, b->f, b->n_qkv, 1, static_cast<uint8_t*>(ws), &w);
+  if ((e = block_bwd_run(b, w, c))) return e;
+  return finish(c);
+}
+
+// ---------------------------------------------------------------------------
 // Pipelined steps from and to host memory
 // ---------------------------------------------------------------------------
+}  // extern "C"
+
 namespace {
 
 // Two copy streams and the events that order the pipeline, created once per device.
@@ -890,107 +921,203 @@ int copy_engines(CopyEngines** out) {
   return FP8Q_OK;
 }
 
-bool same_shape(const fp8q_mlp* a, const fp8q_mlp* b) {
-  return a->T == b->T && a->d == b->d && a->f == b->f && a->recompute == b->recompute &&
-         a->grad_e4m3 == b->grad_e4m3 && a->bf16 == b->bf16;
-}
-
-}  // namespace
-
-int mlp_block_run_steps(const fp8q_mlp* dev0, const fp8q_mlp* dev1, const fp8q_mlp_host_io* host, int n_steps,
-                        void* ws, size_t ws_bytes, fp8q_stream stream) {
-  const fp8q_mlp* dev[2] = {dev0, dev1};
-  int e;
-  for (const fp8q_mlp* m : dev)
-    if ((e = validate_mlp(m, true))) return e;
-  if (!same_shape(dev0, dev1) || !host || n_steps < 1) return FP8Q_ERR_INVALID_ARG;
-  // A buffer both sets share must stay on the device: a copy into or out of it would race with
-  // the other set's step.
-  bool moved[10] = {};
-  for (int i = 0; i < n_steps; ++i) {
-    const fp8q_mlp_host_io& h = host[i];
-    const void* hp[10] = {h.x, h.g, h.W_gu, h.W_d, h.dY, h.y, h.dX, h.dW_gu, h.dW_d, h.dg};
-    for (int k = 0; k < 10; ++k) moved[k] = moved[k] || hp[k] != nullptr;
+// The tensors a step exchanges with the host: n_in inputs, then n_out outputs, each with its
+// size and its device buffer in set 0 and set 1.
+constexpr int kMaxIo = 20;
+struct IoList {
+  int n_in = 0, n_out = 0;
+  size_t bytes[kMaxIo] = {};
+  const void* dev[2][kMaxIo] = {};
+  void add(const void* d0, const void* d1, size_t n) {
+    dev[0][n_in + n_out] = d0;
+    dev[1][n_in + n_out] = d1;
+    bytes[n_in + n_out] = n;
   }
-  const void* d0[10] = {dev0->x, dev0->g, dev0->W_gu, dev0->W_d, dev0->dY, dev0->y, dev0->dX, dev0->dW_gu,
-                        dev0->dW_d, dev0->dg};
-  const void* d1[10] = {dev1->x, dev1->g, dev1->W_gu, dev1->W_d, dev1->dY, dev1->y, dev1->dX, dev1->dW_gu,
-                        dev1->dW_d, dev1->dg};
-  for (int k = 0; k < 10; ++k)
-    if (moved[k] && d0[k] == d1[k]) return FP8Q_ERR_INVALID_ARG;
-  if ((e = check_ws(ws, ws_bytes, mlp_block_workspace_size(dev0->T, dev0->d, dev0->f, 1)))) return e;
+  void in(const void* d0, const void* d1, size_t n) { add(d0, d1, n), ++n_in; }
+  void out(const void* d0, const void* d1, size_t n) { add(d0, d1, n), ++n_out; }
+};
+
+// Step i runs on set i % 2: its inputs are copied in on the h2d stream once step i - 2 (the set's
+// last user) has computed, compute(set) runs on the caller's stream once they are in and step
+// i - 2's outputs have left, and the outputs go out on the d2h stream.  host(i, k) is step i's
+// host pointer of tensor k (null: the tensor stays on the device).  A device buffer both sets
+// share must never move.
+template <class Host, class Compute>
+int run_pipelined(const IoList& io, int n_steps, Host host, Compute compute, const Ctx& c) {
+  const int n = io.n_in + io.n_out;
+  for (int k = 0; k < n; ++k) {
+    bool moved = false;
+    for (int i = 0; i < n_steps; ++i) moved = moved || host(i, k) != nullptr;
+    if (moved && (!io.dev[0][k] || !io.dev[1][k] || io.dev[0][k] == io.dev[1][k])) return FP8Q_ERR_INVALID_ARG;
+  }
   CopyEngines* ce = nullptr;
+  int e;
   if ((e = copy_engines(&ce))) return e;
-  Ctx c;
-  if ((e = make_ctx(&c, stream))) return e;
-  MlpWs w;
-  mlp_ws_layout(dev0->T, dev0->d, dev0->f, 1, static_cast<uint8_t*>(ws), &w);
-  const size_t T = (size_t)dev0->T, d = (size_t)dev0->d, f = (size_t)dev0->f;
   cudaStream_t cs = c.L.stream;
-#define FP8Q_CUDA(expr)                                  \
-  do {                                                   \
-    if ((expr) != cudaSuccess) return FP8Q_ERR_CUDA;     \
+#define FP8Q_CUDA(expr)                              \
+  do {                                               \
+    if ((expr) != cudaSuccess) return FP8Q_ERR_CUDA; \
   } while (0)
   for (int i = 0; i < n_steps; ++i) {
     const int s = i & 1;
-    const fp8q_mlp* m = dev[s];
-    const fp8q_mlp_host_io& h = host[i];
-    // inputs into set s once step i-2 (the set's last user) has finished computing
     if (i >= 2) FP8Q_CUDA(cudaStreamWaitEvent(ce->h2d, ce->compute_done[s], 0));
-    const struct { void* dst; const void* src; size_t bytes; } in[5] = {
-        {(void*)m->x, h.x, T * d * 2}, {(void*)m->g, h.g, d * 2}, {(void*)m->W_gu, h.W_gu, d * 2 * f * 2},
-        {(void*)m->W_d, h.W_d, f * d * 2}, {(void*)m->dY, h.dY, T * d * 2}};
-    for (const auto& cp : in)
-      if (cp.src) FP8Q_CUDA(cudaMemcpyAsync(cp.dst, cp.src, cp.bytes, cudaMemcpyHostToDevice, ce->h2d));
+    for (int k = 0; k < io.n_in; ++k)
+      if (const void* h = host(i, k))
+        FP8Q_CUDA(cudaMemcpyAsync(const_cast<void*>(io.dev[s][k]), h, io.bytes[k], cudaMemcpyHostToDevice, ce->h2d));
     FP8Q_CUDA(cudaEventRecord(ce->in_done[s], ce->h2d));
-    // compute once the inputs are in and step i-2's outputs have left this set
     FP8Q_CUDA(cudaStreamWaitEvent(cs, ce->in_done[s], 0));
     if (i >= 2) FP8Q_CUDA(cudaStreamWaitEvent(cs, ce->out_done[s], 0));
-    if ((e = mlp_fwd_run(m, w, c))) return e;
-    if ((e = mlp_bwd_run(m, w, c))) return e;
+    if ((e = compute(s))) return e;
     FP8Q_CUDA(cudaEventRecord(ce->compute_done[s], cs));
-    // outputs back to the host
     FP8Q_CUDA(cudaStreamWaitEvent(ce->d2h, ce->compute_done[s], 0));
-    const struct { void* dst; const void* src; size_t bytes; } out[5] = {
-        {h.y, m->y, T * d * 2}, {h.dX, m->dX, T * d * 2}, {h.dW_gu, m->dW_gu, d * 2 * f * 4},
-        {h.dW_d, m->dW_d, f * d * 4}, {h.dg, m->dg, d * 4}};
-    for (const auto& cp : out)
-      if (cp.dst) FP8Q_CUDA(cudaMemcpyAsync(cp.dst, cp.src, cp.bytes, cudaMemcpyDeviceToHost, ce->d2h));
+    for (int k = io.n_in; k < n; ++k)
+      if (const void* h = host(i, k))
+        FP8Q_CUDA(cudaMemcpyAsync(const_cast<void*>(h), io.dev[s][k], io.bytes[k], cudaMemcpyDeviceToHost, ce->d2h));
     FP8Q_CUDA(cudaEventRecord(ce->out_done[s], ce->d2h));
   }
   // the caller's stream ends after the last outputs (and every earlier copy) have landed
   FP8Q_CUDA(cudaStreamWaitEvent(cs, ce->out_done[(n_steps - 1) & 1], 0));
   if (n_steps >= 2) FP8Q_CUDA(cudaStreamWaitEvent(cs, ce->out_done[n_steps & 1], 0));
 #undef FP8Q_CUDA
+  return FP8Q_OK;
+}
+
+bool same_shape(const fp8q_mlp* a, const fp8q_mlp* b) {
+  return a->T == b->T && a->d == b->d && a->f == b->f && a->recompute == b->recompute &&
+         a->grad_e4m3 == b->grad_e4m3 && a->bf16 == b->bf16;
+}
+
+bool same_shape(const fp8q_block* a, const fp8q_block* b) {
+  return a->T == b->T && a->d == b->d && a->f == b->f && a->n_qkv == b->n_qkv && a->n_heads == b->n_heads &&
+         a->n_kv_heads == b->n_kv_heads && a->seq_len == b->seq_len && same_shape(&a->mlp, &b->mlp);
+}
+
+// The MLP block's host tensors in fp8q_mlp_host_io order: x, g, W_gu, W_d, dY in; y, dX, dW_gu,
+// dW_d, dg out.
+IoList mlp_io(const fp8q_mlp* m0, const fp8q_mlp* m1) {
+  const size_t T = (size_t)m0->T, d = (size_t)m0->d, f = (size_t)m0->f;
+  IoList io;
+  io.in(m0->x, m1->x, T * d * 2);
+  io.in(m0->g, m1->g, d * 2);
+  io.in(m0->W_gu, m1->W_gu, d * 2 * f * 2);
+  io.in(m0->W_d, m1->W_d, f * d * 2);
+  io.in(m0->dY, m1->dY, T * d * 2);
+  io.out(m0->y, m1->y, T * d * 2);
+  io.out(m0->dX, m1->dX, T * d * 2);
+  io.out(m0->dW_gu, m1->dW_gu, d * 2 * f * 4);
+  io.out(m0->dW_d, m1->dW_d, f * d * 4);
+  io.out(m0->dg, m1->dg, d * 4);
+  return io;
+}
+
+const void* mlp_host(const fp8q_mlp_host_io& h, int k) {
+  const void* p[10] = {h.x, h.g, h.W_gu, h.W_d, h.dY, h.y, h.dX, h.dW_gu, h.dW_d, h.dg};
+  return p[k];
+}
+
+int mlp_run_steps(const fp8q_mlp* dev0, const fp8q_mlp* dev1, const fp8q_mlp_host_io* host, int n_steps,
+                  bool backward, void* ws, size_t ws_bytes, fp8q_stream stream) {
+  const fp8q_mlp* dev[2] = {dev0, dev1};
+  int e;
+  if (!dev0 || !dev1 || !host || n_steps < 1) return FP8Q_ERR_INVALID_ARG;
+  for (const fp8q_mlp* m : dev)
+    if ((e = validate_mlp(m, backward))) return e;
+  if (!same_shape(dev0, dev1)) return FP8Q_ERR_INVALID_ARG;
+  if (!backward)
+    for (int i = 0; i < n_steps; ++i)
+      for (int k : {4, 6, 7, 8, 9})  // dY, dX, dW_gu, dW_d, dg
+        if (mlp_host(host[i], k)) return FP8Q_ERR_INVALID_ARG;
+  if ((e = check_ws(ws, ws_bytes, mlp_block_workspace_size(dev0->T, dev0->d, dev0->f, backward ? 1 : 0)))) return e;
+  Ctx c;
+  if ((e = make_ctx(&c, stream))) return e;
+  MlpWs w;
+  mlp_ws_layout(dev0->T, dev0->d, dev0->f, backward ? 1 : 0, static_cast<uint8_t*>(ws), &w);
+  if ((e = run_pipelined(
+           mlp_io(dev0, dev1), n_steps, [&](int i, int k) { return mlp_host(host[i], k); },
+           [&](int s) {
+             int r = mlp_fwd_run(dev[s], w, c);
+             return r || !backward ? r : mlp_bwd_run(dev[s], w, c);
+           },
+           c)))
+    return e;
   return finish(c);
 }
 
-// ---------------------------------------------------------------------------
-size_t block_workspace_size(int64_t T, int64_t d, int64_t f, int64_t n_qkv, int backward) {
-  return block_ws_layout(T, d, f, n_qkv, backward, nullptr, nullptr);
+// The full block's host tensors in fp8q_block_host_io order.
+IoList block_io(const fp8q_block* b0, const fp8q_block* b1) {
+  const size_t T = (size_t)b0->T, d = (size_t)b0->d, f = (size_t)b0->f, nq = (size_t)b0->n_qkv;
+  IoList io;
+  io.in(b0->x, b1->x, T * d * 2);
+  io.in(b0->g1, b1->g1, d * 2);
+  io.in(b0->W_qkv, b1->W_qkv, d * nq * 2);
+  io.in(b0->W_o, b1->W_o, d * d * 2);
+  io.in(b0->att, b1->att, T * d * 2);
+  io.in(b0->mlp.g, b1->mlp.g, d * 2);
+  io.in(b0->mlp.W_gu, b1->mlp.W_gu, d * 2 * f * 2);
+  io.in(b0->mlp.W_d, b1->mlp.W_d, f * d * 2);
+  io.in(b0->mlp.dY, b1->mlp.dY, T * d * 2);
+  io.in(b0->dQKV, b1->dQKV, T * nq * 2);
+  io.out(b0->mlp.y, b1->mlp.y, T * d * 2);
+  io.out(b0->dX, b1->dX, T * d * 2);
+  io.out(b0->d_att, b1->d_att, T * d * 2);
+  io.out(b0->dW_qkv, b1->dW_qkv, d * nq * 4);
+  io.out(b0->dW_o, b1->dW_o, d * d * 4);
+  io.out(b0->dg1, b1->dg1, d * 4);
+  io.out(b0->mlp.dW_gu, b1->mlp.dW_gu, d * 2 * f * 4);
+  io.out(b0->mlp.dW_d, b1->mlp.dW_d, f * d * 4);
+  io.out(b0->mlp.dg, b1->mlp.dg, d * 4);
+  return io;
 }
 
-int block_fwd(const fp8q_block* b, void* ws, size_t ws_bytes, fp8q_stream stream) {
-  int e = validate_block(b, false);
-  if (e) return e;
-  if ((e = check_ws(ws, ws_bytes, block_workspace_size(b->T, b->d, b->f, b->n_qkv, 0)))) return e;
+const void* block_host(const fp8q_block_host_io& h, int k) {
+  const void* p[19] = {h.x,  h.g1, h.W_qkv, h.W_o,   h.att,  h.g,   h.W_gu,   h.W_d,  h.dY, h.dQKV,
+                       h.y,  h.dX, h.d_att, h.dW_qkv, h.dW_o, h.dg1, h.dW_gu, h.dW_d, h.dg};
+  return p[k];
+}
+
+}  // namespace
+
+extern "C" {
+
+int mlp_block_run_steps(const fp8q_mlp* dev0, const fp8q_mlp* dev1, const fp8q_mlp_host_io* host, int n_steps,
+                        void* ws, size_t ws_bytes, fp8q_stream stream) {
+  return mlp_run_steps(dev0, dev1, host, n_steps, true, ws, ws_bytes, stream);
+}
+
+int mlp_block_fwd_run_steps(const fp8q_mlp* dev0, const fp8q_mlp* dev1, const fp8q_mlp_host_io* host, int n_steps,
+                            void* ws, size_t ws_bytes, fp8q_stream stream) {
+  return mlp_run_steps(dev0, dev1, host, n_steps, false, ws, ws_bytes, stream);
+}
+
+int block_run_steps(const fp8q_block* dev0, const fp8q_block* dev1, const fp8q_block_host_io* host, int n_steps,
+                    int backward, void* ws, size_t ws_bytes, fp8q_stream stream) {
+  const fp8q_block* dev[2] = {dev0, dev1};
+  int e;
+  if (!dev0 || !dev1 || !host || n_steps < 1) return FP8Q_ERR_INVALID_ARG;
+  for (const fp8q_block* b : dev)
+    if ((e = validate_block(b, backward != 0))) return e;
+  if (!same_shape(dev0, dev1)) return FP8Q_ERR_INVALID_ARG;
+  for (int i = 0; i < n_steps; ++i) {
+    // with the attention core inside, att and dQKV are the block's own results, not inputs
+    if (dev0->n_heads && (host[i].att || host[i].dQKV)) return FP8Q_ERR_INVALID_ARG;
+    if (!backward)
+      for (int k : {8, 9, 11, 12, 13, 14, 15, 16, 17, 18})  // the backward's inputs and outputs
+        if (block_host(host[i], k)) return FP8Q_ERR_INVALID_ARG;
+  }
+  const int bw = backward ? 1 : 0;
+  if ((e = check_ws(ws, ws_bytes, block_workspace_size(dev0->T, dev0->d, dev0->f, dev0->n_qkv, bw)))) return e;
   Ctx c;
   if ((e = make_ctx(&c, stream))) return e;
   BlockWs w;
-  block_ws_layout(b->T, b->d, b->f, b->n_qkv, 0, static_cast<uint8_t*>(ws), &w);
-  if ((e = block_fwd_run(b, w, c))) return e;
-  return finish(c);
-}
-
-int block_bwd(const fp8q_block* b, void* ws, size_t ws_bytes, fp8q_stream stream) {
-  int e = validate_block(b, true);
-  if (e) return e;
-  if ((e = check_ws(ws, ws_bytes, block_workspace_size(b->T, b->d, b->f, b->n_qkv, 1)))) return e;
-  Ctx c;
-  if ((e = make_ctx(&c, stream))) return e;
-  BlockWs w;
-  block_ws_layout(b->T, b->d, b->f, b->n_qkv, 1, static_cast<uint8_t*>(ws), &w);
-  if ((e = block_bwd_run(b, w, c))) return e;
+  block_ws_layout(dev0->T, dev0->d, dev0->f, dev0->n_qkv, bw, static_cast<uint8_t*>(ws), &w);
+  if ((e = run_pipelined(
+           block_io(dev0, dev1), n_steps, [&](int i, int k) { return block_host(host[i], k); },
+           [&](int s) {
+             int r = block_fwd_run(dev[s], w, c);
+             return r || !backward ? r : block_bwd_run(dev[s], w, c);
+           },
+           c)))
+    return e;
   return finish(c);
 }
 

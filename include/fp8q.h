@@ -258,6 +258,11 @@ typedef struct fp8q_mlp_host_io {
 } fp8q_mlp_host_io;
 FP8Q_API int mlp_block_run_steps(const fp8q_mlp* dev0, const fp8q_mlp* dev1, const fp8q_mlp_host_io* host,
                                  int n_steps, void* ws, size_t ws_bytes, fp8q_stream stream);
+/* The same for forward-only steps (mlp_block_fwd alone): x, g, W_gu, W_d in, y out; the host
+ * pointers of the backward's tensors (dY, dX, dW_gu, dW_d, dg) must be null; workspace
+ * mlp_block_workspace_size(T, d, f, 0) bytes. */
+FP8Q_API int mlp_block_fwd_run_steps(const fp8q_mlp* dev0, const fp8q_mlp* dev1, const fp8q_mlp_host_io* host,
+                                     int n_steps, void* ws, size_t ws_bytes, fp8q_stream stream);
 
 /* ------------------------------------------------------------------------ */
 /* The full transformer block's matmuls around an attention core computed   */
@@ -319,6 +324,40 @@ typedef struct fp8q_block {
 FP8Q_API size_t block_workspace_size(int64_t T, int64_t d, int64_t f, int64_t n_qkv, int backward);
 FP8Q_API int block_fwd(const fp8q_block* b, void* ws, size_t ws_bytes, fp8q_stream stream);
 FP8Q_API int block_bwd(const fp8q_block* b, void* ws, size_t ws_bytes, fp8q_stream stream);
+
+/* Pipelined steps of the full block from and to host memory, as mlp_block_run_steps: step i
+ * copies its inputs from host[i] into device set i % 2, runs block_fwd (and block_bwd when
+ * backward != 0) on `stream`, and copies its outputs back into host[i], step i + 1's inputs and
+ * step i - 1's outputs moving while step i computes.  A null host pointer keeps that tensor on
+ * the device in that step; a buffer both sets share must be null in every step.  Without
+ * backward, the backward's host pointers (dY, dQKV, dX, d_att and the gradients) must be null;
+ * with the attention core inside (n_heads != 0), att and dQKV are the block's own results and
+ * their host pointers must be null.  Host tensors have the device tensors' shapes and types (y
+ * is mlp.y; g, W_gu, W_d, dY, dW_gu, dW_d, dg those of mlp).  Workspace
+ * block_workspace_size(T, d, f, n_qkv, backward) bytes. */
+typedef struct fp8q_block_host_io {
+  const void* x;
+  const void* g1;
+  const void* W_qkv;
+  const void* W_o;
+  const void* att;
+  const void* g;
+  const void* W_gu;
+  const void* W_d;
+  const void* dY;
+  const void* dQKV;
+  void* y;
+  void* dX;
+  void* d_att;
+  float* dW_qkv;
+  float* dW_o;
+  float* dg1;
+  float* dW_gu;
+  float* dW_d;
+  float* dg;
+} fp8q_block_host_io;
+FP8Q_API int block_run_steps(const fp8q_block* dev0, const fp8q_block* dev1, const fp8q_block_host_io* host,
+                             int n_steps, int backward, void* ws, size_t ws_bytes, fp8q_stream stream);
 
 /* ------------------------------------------------------------------------ */
 /* The attention core between the QKV and O projections.  LLMQ §2/§3 name    */
