@@ -360,8 +360,9 @@ __global__ void __launch_bounds__(kThreads) k_swiglu_cast(const uint16_t* __rest
 }
 
 // ---------------------------------------------------------------------------
-// RMSNorm backward + residual.  A block owns kBwdRows rows; thread t owns the
-// 8-column groups j = 8 (t + 256 c), c < NG.  Per row: nh = x rstd, u = dN g,
+// RMSNorm backward + residual.  A block owns `rows` consecutive rows (one wave
+// of resident blocks covers all T rows, so no partial last wave idles SMs);
+// thread t owns the 8-column groups j = 8 (t + 256 c), c < NG.  Per row: nh = x rstd, u = dN g,
 // dot = sum_j u nh (block reduction, fixed order), dX = dY + rstd (u - nh dot/d).
 // The next row's dN and x are loaded while the current row is reduced.
 // dg partials accumulate per block in registers (fixed row order) and are
@@ -395,7 +396,7 @@ __global__ void __launch_bounds__(kThreads) k_rmsnorm_bwd(const float* __restric
                                                           const uint16_t* __restrict__ dY,
                                                           const uint16_t* __restrict__ g,
                                                           const float* __restrict__ rstd, int64_t T, int d,
-                                                          uint16_t* __restrict__ dX,
+                                                          int rows, uint16_t* __restrict__ dX,
                                                           float* __restrict__ dg_partial) {
   __shared__ float red[2][kThreads / 32];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -413,8 +414,8 @@ __global__ void __launch_bounds__(kThreads) k_rmsnorm_bwd(const float* __restric
     }
   }
   const float inv_d = 1.0f / (float)d;
-  const int64_t r0 = (int64_t)blockIdx.x * kBwdRows;
-  const int nrows = (int)((T - r0) < kBwdRows ? (T - r0) : kBwdRows);
+  const int64_t r0 = (int64_t)blockIdx.x * rows;
+  const int nrows = (int)((T - r0) < rows ? (T - r0) : rows);
   BwdRow<NG> cur;
   bwd_load_row<NG>(cur, dN, x, r0, d, t);
   for (int rr = 0; rr < nrows; ++rr) {
@@ -598,13 +599,23 @@ cudaError_t launch_swiglu_cast(const uint16_t* H, int64_t T, int f, int fmt, con
 cudaError_t launch_rmsnorm_bwd(const float* dN, const uint16_t* x, const uint16_t* dY, const uint16_t* g,
                                const float* rstd, int64_t T, int d, uint16_t* dX, float* dg_partial, float* dg,
                                const Launch& L) {
-  const int nblk = (int)((T + kBwdRows - 1) / kBwdRows);
   const int ng = (d + 8 * kThreads - 1) / (8 * kThreads);
+  const void* fn = ng == 1 ? (const void*)k_rmsnorm_bwd<1>
+                 : ng == 2 ? (const void*)k_rmsnorm_bwd<2>
+                 : ng == 3 ? (const void*)k_rmsnorm_bwd<3> : (const void*)k_rmsnorm_bwd<4>;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, 0) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  // rows per block: at least kBwdRows (the dg partials' workspace holds ceil(T / kBwdRows) rows),
+  // else as few as let one wave of resident blocks cover T
+  const int64_t wave = (int64_t)L.num_sms * per_sm;
+  const int rows = (int)std::max<int64_t>(kBwdRows, (T + wave - 1) / wave);
+  const int nblk = (int)((T + rows - 1) / rows);
   switch (ng) {
-    case 1: k_rmsnorm_bwd<1><<<nblk, kThreads, 0, L.stream>>>(dN, x, dY, g, rstd, T, d, dX, dg_partial); break;
-    case 2: k_rmsnorm_bwd<2><<<nblk, kThreads, 0, L.stream>>>(dN, x, dY, g, rstd, T, d, dX, dg_partial); break;
-    case 3: k_rmsnorm_bwd<3><<<nblk, kThreads, 0, L.stream>>>(dN, x, dY, g, rstd, T, d, dX, dg_partial); break;
-    default: k_rmsnorm_bwd<4><<<nblk, kThreads, 0, L.stream>>>(dN, x, dY, g, rstd, T, d, dX, dg_partial); break;
+    case 1: k_rmsnorm_bwd<1><<<nblk, kThreads, 0, L.stream>>>(dN, x, dY, g, rstd, T, d, rows, dX, dg_partial); break;
+    case 2: k_rmsnorm_bwd<2><<<nblk, kThreads, 0, L.stream>>>(dN, x, dY, g, rstd, T, d, rows, dX, dg_partial); break;
+    case 3: k_rmsnorm_bwd<3><<<nblk, kThreads, 0, L.stream>>>(dN, x, dY, g, rstd, T, d, rows, dX, dg_partial); break;
+    default: k_rmsnorm_bwd<4><<<nblk, kThreads, 0, L.stream>>>(dN, x, dY, g, rstd, T, d, rows, dX, dg_partial); break;
   }
   cudaError_t e = post_launch(L);
   if (e != cudaSuccess) return e;
