@@ -831,23 +831,31 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256;
+      // S_j and dP_j are issued as soon as the element-wise warps have taken S_{j-1} and dP_{j-1}
+      // into registers, ahead of dQ += dS_{j-1} K_{j-1}: the tensor core works on tile j while the
+      // element-wise pass forms dS_{j-1}
       bool ok = mbar_wait(q_full, 0, abort_flag);
-      for (int j = 0; j < n && ok; ++j) {
-        const int st = j & 1;
-        const uint32_t u = (uint32_t)(j >> 1) & 1u, par = (uint32_t)j & 1u;
-        if (!mbar_wait(&kv_full[st], u, abort_flag) || !mbar_wait(s_free, par ^ 1u, abort_flag)) {
-          ok = false;
-          break;
+      for (int j = 0; j <= n && ok; ++j) {
+        if (j < n) {
+          const int st = j & 1;
+          const uint32_t u = (uint32_t)(j >> 1) & 1u, par = (uint32_t)j & 1u;
+          if (!mbar_wait(&kv_full[st], u, abort_flag) || !mbar_wait(s_free, par ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_tile_kk(tS, sbase + kQQ, sbase + kQK + st * kTile, false);   // S = Q K^T
+          mma_tile_kk(tdP, sbase + kQO, sbase + kQV + st * kTile, false);  // dP = dO V^T
+          umma_commit(s_full);
         }
-        tc_fence_after();
-        mma_tile_kk(tS, sbase + kQQ, sbase + kQK + st * kTile, false);   // S = Q K^T
-        mma_tile_kk(tdP, sbase + kQO, sbase + kQV + st * kTile, false);  // dP = dO V^T
-        umma_commit(s_full);
-        if (!mbar_wait(ds_full, par, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        mma_tile_kmn(tdQ, sbase + kQDS, sbase + kQK + st * kTile, j > 0);  // dQ += dS K
-        umma_commit(&kv_empty[st]);
-        umma_commit(ds_free);
+        if (j > 0) {
+          const int jj = j - 1, st = jj & 1;
+          if (!mbar_wait(ds_full, (uint32_t)jj & 1u, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          mma_tile_kmn(tdQ, sbase + kQDS, sbase + kQK + st * kTile, jj > 0);  // dQ += dS K
+          umma_commit(&kv_empty[st]);
+          umma_commit(ds_free);
+        }
       }
       if (ok) umma_commit(acc_full);
       else {
@@ -870,22 +878,30 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
     for (int j = 0; j < n; ++j) {
       const uint32_t par = (uint32_t)j & 1u;
       const bool diag = j == qt;
-      if (!warp_wait(s_full, par, abort_flag) || !warp_wait(ds_free, par ^ 1u, abort_flag)) {
+      if (!warp_wait(s_full, par, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-#pragma unroll 1
-      for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
-        uint32_t sv[32], dv[32], w[16];
-        tmem_ld32(tS + c * 32, sv);
-        tmem_ld32(tdP + c * 32, dv);
-        if (diag) ds_row_chunk<true>(sv, dv, c, r, p.scale_log2, lse2, dlt, w);
-        else ds_row_chunk<false>(sv, dv, c, r, p.scale_log2, lse2, dlt, w);
-        tile_put32(sbase + kQDS, r, c, w);
-      }
+      // this warpgroup's 64 columns of S_j and dP_j into registers, then TMEM is free for S_{j+1}
+      const int c0 = 2 * wg, c1 = c0 + 1;
+      uint32_t s0[32], d0[32], s1[32], d1[32];
+      tmem_ld32x2(tS + c0 * 32, tdP + c0 * 32, s0, d0);
+      tmem_ld32x2(tS + c1 * 32, tdP + c1 * 32, s1, d1);
       tc_fence_before();
       mbar_arrive(s_free);
+      // the dS tile is rewritten once dQ += dS_{j-1} K_{j-1} has read it
+      if (!warp_wait(ds_free, par ^ 1u, abort_flag)) {
+        ok = false;
+        break;
+      }
+      uint32_t w[16];
+      if (diag) ds_row_chunk<true>(s0, d0, c0, r, p.scale_log2, lse2, dlt, w);
+      else ds_row_chunk<false>(s0, d0, c0, r, p.scale_log2, lse2, dlt, w);
+      tile_put32(sbase + kQDS, r, c0, w);
+      if (diag) ds_row_chunk<true>(s1, d1, c1, r, p.scale_log2, lse2, dlt, w);
+      else ds_row_chunk<false>(s1, d1, c1, r, p.scale_log2, lse2, dlt, w);
+      tile_put32(sbase + kQDS, r, c1, w);
       fence_async_shared();
       mbar_arrive(ds_full);
     }
