@@ -363,7 +363,7 @@ def run_ours(args, rank, world, local_rank):
         batch_in = [k for k in ("x", "dY", "att", "dQKV") if k in dev_in]
         batch_out = [k for k in ("y", "dX", "d_att") if k in dev_out]
         host_out = {k: torch.empty(t.shape, dtype=t.dtype).pin_memory() for k, t in dev_out.items()}
-        Ke = max(3, min(K, 20))
+        Ke = max(3, K)  # as many steps as the device-timed region, under the same clocks
         # the second device set of the library's pipelined executor (step i+1's inputs arrive and
         # step i-1's outputs leave while step i computes); tensors that stay in HBM are shared
         if w.qkv:
