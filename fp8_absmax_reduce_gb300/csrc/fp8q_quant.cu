@@ -29,6 +29,28 @@ inline int grid_for(int64_t items, int cap) {
   return (int)(b < cap ? b : cap);
 }
 
+// The grid-stride items i = first, first + stride, ... of a [rows, per_row] item grid as (row, col)
+// pairs, without a 64-bit division per item: the stride is split once into whole rows and a
+// remainder column step.
+struct RowWalk {
+  int64_t row, drow;
+  int col, dcol, per_row;
+  __device__ RowWalk(int64_t first, int64_t stride, int per_row_) : per_row(per_row_) {
+    row = first / per_row;
+    col = (int)(first - row * per_row);
+    drow = stride / per_row;
+    dcol = (int)(stride - drow * per_row);
+  }
+  __device__ void next() {
+    row += drow;
+    col += dcol;
+    if (col >= per_row) {
+      col -= per_row;
+      ++row;
+    }
+  }
+};
+
 inline cudaError_t post_launch(const Launch& L) {
   if (L.launches) ++*L.launches;
   return cudaGetLastError();
@@ -277,12 +299,10 @@ __global__ void __launch_bounds__(kThreads) k_rmsnorm_cast(const uint16_t* __res
                                                            unsigned* status) {
   __shared__ float s_sh;
   const float s = finalize_scale(partial, P, 0, scal, status, &s_sh);
-  const int gpr = d / 16;
-  const int64_t items = T * gpr;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < items; i += stride) {
-    const int64_t row = i / gpr;
-    const int j0 = (int)(i - row * gpr) * 16;
+  for (RowWalk w((int64_t)blockIdx.x * blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x, d / 16); w.row < T;
+       w.next()) {
+    const int64_t row = w.row;
+    const int j0 = w.col * 16;
     const float rs = rstd[row];
     const uint16_t* xr = x + row * d + j0;
     const uint4 a = ld_nc_v4(xr), b = ld_nc_v4(xr + 8), ga = ld_v4(g + j0), gb = ld_v4(g + j0 + 8);
@@ -322,14 +342,11 @@ __device__ __forceinline__ void swiglu8(const uint16_t* H, int64_t row, int f, i
 __global__ void __launch_bounds__(kThreads) k_swiglu_amax(const uint16_t* __restrict__ H, int64_t T, int f,
                                                           uint32_t* __restrict__ partial) {
   __shared__ uint32_t red[32];
-  const int gpr = f / 8;
-  const int64_t items = T * gpr;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   uint32_t m = 0;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < items; i += stride) {
-    const int64_t row = i / gpr;
+  for (RowWalk w((int64_t)blockIdx.x * blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x, f / 8); w.row < T;
+       w.next()) {
     float a[8];
-    swiglu8(H, row, f, (int)(i - row * gpr) * 8, a);
+    swiglu8(H, w.row, f, w.col * 8, a);
 #pragma unroll
     for (int k = 0; k < 8; ++k) m = max(m, abs_bits(a[k]));
   }
@@ -344,12 +361,10 @@ __global__ void __launch_bounds__(kThreads) k_swiglu_cast(const uint16_t* __rest
                                                           unsigned* status) {
   __shared__ float s_sh;
   const float s = finalize_scale(partial, P, FMT, scal, status, &s_sh);
-  const int gpr = f / 8;
-  const int64_t items = T * gpr;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < items; i += stride) {
-    const int64_t row = i / gpr;
-    const int j0 = (int)(i - row * gpr) * 8;
+  for (RowWalk w((int64_t)blockIdx.x * blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x, f / 8); w.row < T;
+       w.next()) {
+    const int64_t row = w.row;
+    const int j0 = w.col * 8;
     float a[8];
     swiglu8<FAST>(H, row, f, j0, a);
     uint2 o;
