@@ -376,13 +376,20 @@ __global__ void __launch_bounds__(kThreads) k_swiglu_cast(const uint16_t* __rest
 
 // ---------------------------------------------------------------------------
 // RMSNorm backward + residual.  A block owns `rows` consecutive rows (one wave
-// of resident blocks covers all T rows, so no partial last wave idles SMs);
-// thread t owns the 8-column groups j = 8 (t + 256 c), c < NG.  Per row: nh = x rstd, u = dN g,
+// of resident blocks covers all T rows); thread t owns the 8-column groups
+// j = 8 (t + 256 c), c < NG.  Per row: nh = x rstd, u = dN g,
 // dot = sum_j u nh (block reduction, fixed order), dX = dY + rstd (u - nh dot/d).
-// The next row's dN and x are loaded while the current row is reduced.
+// A row's dN, x and dY reach shared memory through a ring of kBwdRing slots
+// filled by asynchronous 16-byte copies, kBwdRing - 1 rows ahead of their use
+// (one row of prefetch cannot cover the DRAM latency behind a row's short
+// dependent chain); each thread copies and reads back only its own pieces, so
+// the ring needs no barrier beyond the thread's cp.async.wait_group.
 // dg partials accumulate per block in registers (fixed row order) and are
 // reduced over blocks in a fixed order by k_dg_finalize.
 // ---------------------------------------------------------------------------
+// Rows of up to 4096 columns (at most two 8-column groups per thread): the next row's dN and x
+// in registers while the current one is reduced, two blocks per SM -- at these sizes this
+// measured faster than the shared-memory ring below, which wins for longer rows.
 template <int NG>
 struct BwdRow {
   uint4 d0[NG], d1[NG], xv[NG];
@@ -406,7 +413,7 @@ __device__ __forceinline__ void bwd_load_row(BwdRow<NG>& r, const float* __restr
 }
 
 template <int NG>
-__global__ void __launch_bounds__(kThreads) k_rmsnorm_bwd(const float* __restrict__ dN,
+__global__ void __launch_bounds__(kThreads) k_rmsnorm_bwd_reg(const float* __restrict__ dN,
                                                           const uint16_t* __restrict__ x,
                                                           const uint16_t* __restrict__ dY,
                                                           const uint16_t* __restrict__ g,
@@ -487,6 +494,136 @@ __global__ void __launch_bounds__(kThreads) k_rmsnorm_bwd(const float* __restric
     }
     if (rr + 1 < nrows) cur = nxt;
   }
+#pragma unroll
+  for (int c = 0; c < NG; ++c) {
+    const int j0 = 8 * (t + kThreads * c);
+    if (j0 < d) {
+      float* dst = dg_partial + (int64_t)blockIdx.x * d + j0;
+      st_v4(dst, make_uint4(__float_as_uint(dga[c][0]), __float_as_uint(dga[c][1]), __float_as_uint(dga[c][2]),
+                            __float_as_uint(dga[c][3])));
+      st_v4(dst + 4, make_uint4(__float_as_uint(dga[c][4]), __float_as_uint(dga[c][5]),
+                                __float_as_uint(dga[c][6]), __float_as_uint(dga[c][7])));
+    }
+  }
+}
+
+constexpr int kBwdRing = 3;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Shared memory of one k_rmsnorm_bwd block: kBwdRing slots of NG x 4 pieces (dN lo, dN hi, x, dY)
+// of 16 bytes per thread.
+inline size_t rmsnorm_bwd_smem(int ng) { return (size_t)kBwdRing * ng * 4 * kThreads * 16; }
+
+template <int NG>
+__global__ void __launch_bounds__(kThreads, 2) k_rmsnorm_bwd(const float* __restrict__ dN,
+                                                             const uint16_t* __restrict__ x,
+                                                             const uint16_t* __restrict__ dY,
+                                                             const uint16_t* __restrict__ g,
+                                                             const float* __restrict__ rstd, int64_t T, int d,
+                                                             int rows, uint16_t* __restrict__ dX,
+                                                             float* __restrict__ dg_partial) {
+  extern __shared__ uint4 bwd_ring[];  // [slot][group][piece][thread]
+  __shared__ float red[2][kThreads / 32];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  float gv[NG][8], dga[NG][8];
+#pragma unroll
+  for (int c = 0; c < NG; ++c) {
+    const int j0 = 8 * (t + kThreads * c);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) { gv[c][k] = 0.0f; dga[c][k] = 0.0f; }
+    if (j0 < d) {
+      const uint4 w = ld_v4(g + j0);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) { gv[c][2 * k] = bf16_lo(ww[k]); gv[c][2 * k + 1] = bf16_hi(ww[k]); }
+    }
+  }
+  const float inv_d = 1.0f / (float)d;
+  const int64_t r0 = (int64_t)blockIdx.x * rows;
+  const int nrows = (int)((T - r0) < rows ? (T - r0) : rows);
+  const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(bwd_ring);
+  // piece q of group c of slot sl, this thread's 16 bytes
+  auto piece = [&](int sl, int c, int q) { return ((sl * NG + c) * 4 + q) * kThreads + t; };
+  auto issue = [&](int rr) {
+    if (rr < nrows) {
+      const int64_t row = r0 + rr;
+      const int sl = rr % kBwdRing;
+#pragma unroll
+      for (int c = 0; c < NG; ++c) {
+        const int j0 = 8 * (t + kThreads * c);
+        if (j0 < d) {
+          const float* dn = dN + row * d + j0;
+          cp_async16(ring_s + 16u * piece(sl, c, 0), dn);
+          cp_async16(ring_s + 16u * piece(sl, c, 1), dn + 4);
+          cp_async16(ring_s + 16u * piece(sl, c, 2), x + row * d + j0);
+          cp_async16(ring_s + 16u * piece(sl, c, 3), dY + row * d + j0);
+        }
+      }
+    }
+    cp_async_commit();  // an empty group keeps the group count uniform
+  };
+#pragma unroll
+  for (int k = 0; k < kBwdRing - 1; ++k) issue(k);
+  for (int rr = 0; rr < nrows; ++rr) {
+    const int64_t row = r0 + rr;
+    issue(rr + kBwdRing - 1);
+    cp_async_wait<kBwdRing - 1>();  // this thread's pieces of row rr have landed
+    const int sl = rr % kBwdRing;
+    const float rs = rstd[row];
+    float dot = 0.0f;
+#pragma unroll
+    for (int c = 0; c < NG; ++c) {
+      const int j0 = 8 * (t + kThreads * c);
+      if (j0 >= d) continue;
+      const uint4 d0 = bwd_ring[piece(sl, c, 0)], d1 = bwd_ring[piece(sl, c, 1)], xv = bwd_ring[piece(sl, c, 2)];
+      const float dnv[8] = {__uint_as_float(d0.x), __uint_as_float(d0.y), __uint_as_float(d0.z), __uint_as_float(d0.w),
+                            __uint_as_float(d1.x), __uint_as_float(d1.y), __uint_as_float(d1.z), __uint_as_float(d1.w)};
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float xk = (k & 1) ? bf16_hi(xw[k >> 1]) : bf16_lo(xw[k >> 1]);
+        const float nh = xk * rs;
+        dot += (dnv[k] * gv[c][k]) * nh;
+        dga[c][k] += dnv[k] * nh;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
+    if (lane == 0) red[rr & 1][warp] = dot;
+    __syncthreads();
+    float tot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) tot += red[rr & 1][w];
+    const float mean = tot * inv_d;
+#pragma unroll
+    for (int c = 0; c < NG; ++c) {
+      const int j0 = 8 * (t + kThreads * c);
+      if (j0 >= d) continue;
+      const uint4 d0 = bwd_ring[piece(sl, c, 0)], d1 = bwd_ring[piece(sl, c, 1)], xv = bwd_ring[piece(sl, c, 2)],
+                  yv = bwd_ring[piece(sl, c, 3)];
+      const float dnv[8] = {__uint_as_float(d0.x), __uint_as_float(d0.y), __uint_as_float(d0.z), __uint_as_float(d0.w),
+                            __uint_as_float(d1.x), __uint_as_float(d1.y), __uint_as_float(d1.z), __uint_as_float(d1.w)};
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, yw[4] = {yv.x, yv.y, yv.z, yv.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float nlo = bf16_lo(xw[k]) * rs, nhi = bf16_hi(xw[k]) * rs;
+        const float a = bf16_lo(yw[k]) + rs * (dnv[2 * k] * gv[c][2 * k] - nlo * mean);
+        const float bb = bf16_hi(yw[k]) + rs * (dnv[2 * k + 1] * gv[c][2 * k + 1] - nhi * mean);
+        o[k] = pack_bf16x2(a, bb);
+      }
+      st_v4(dX + row * d + j0, make_uint4(o[0], o[1], o[2], o[3]));
+    }
+  }
+  cp_async_wait<0>();
 #pragma unroll
   for (int c = 0; c < NG; ++c) {
     const int j0 = 8 * (t + kThreads * c);
@@ -615,23 +752,45 @@ cudaError_t launch_rmsnorm_bwd(const float* dN, const uint16_t* x, const uint16_
                                const float* rstd, int64_t T, int d, uint16_t* dX, float* dg_partial, float* dg,
                                const Launch& L) {
   const int ng = (d + 8 * kThreads - 1) / (8 * kThreads);
-  const void* fn = ng == 1 ? (const void*)k_rmsnorm_bwd<1>
-                 : ng == 2 ? (const void*)k_rmsnorm_bwd<2>
-                 : ng == 3 ? (const void*)k_rmsnorm_bwd<3> : (const void*)k_rmsnorm_bwd<4>;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, 0) != cudaSuccess || per_sm < 1)
-    per_sm = 1;
-  // rows per block: at least kBwdRows (the dg partials' workspace holds ceil(T / kBwdRows) rows),
-  // else as few as let one wave of resident blocks cover T
-  const int64_t wave = (int64_t)L.num_sms * per_sm;
+  if (ng <= 2) {
+    int per_sm = 0;
+    const void* fn = ng == 1 ? (const void*)k_rmsnorm_bwd_reg<1> : (const void*)k_rmsnorm_bwd_reg<2>;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, 0) != cudaSuccess || per_sm < 1)
+      per_sm = 1;
+    const int64_t wave = (int64_t)L.num_sms * per_sm;
+    const int rows = (int)std::max<int64_t>(kBwdRows, (T + wave - 1) / wave);
+    const int nblk = (int)((T + rows - 1) / rows);
+    if (ng == 1) k_rmsnorm_bwd_reg<1><<<nblk, kThreads, 0, L.stream>>>(dN, x, dY, g, rstd, T, d, rows, dX, dg_partial);
+    else k_rmsnorm_bwd_reg<2><<<nblk, kThreads, 0, L.stream>>>(dN, x, dY, g, rstd, T, d, rows, dX, dg_partial);
+    cudaError_t e = post_launch(L);
+    if (e != cudaSuccess) return e;
+    k_dg_finalize<<<(d + 31) / 32, kThreads, 0, L.stream>>>(dg_partial, nblk, d, dg);
+    return post_launch(L);
+  }
+  const size_t smem = rmsnorm_bwd_smem(ng <= 4 ? ng : 4);
+  // one wave of resident blocks (two per SM when their rings fit), consecutive rows each (at least
+  // kBwdRows: the dg partials' workspace holds ceil(T / kBwdRows) rows)
+  const int64_t wave = (int64_t)L.num_sms * (smem <= 110 * 1024 ? 2 : 1);
   const int rows = (int)std::max<int64_t>(kBwdRows, (T + wave - 1) / wave);
   const int nblk = (int)((T + rows - 1) / rows);
+  static int configured_device[5] = {-1, -1, -1, -1, -1};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  auto go = [&](auto kernel, int which) -> cudaError_t {
+    if (configured_device[which] != dev) {
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      configured_device[which] = dev;
+    }
+    kernel<<<nblk, kThreads, smem, L.stream>>>(dN, x, dY, g, rstd, T, d, rows, dX, dg_partial);
+    return cudaSuccess;
+  };
+  cudaError_t le;
   switch (ng) {
-    case 1: k_rmsnorm_bwd<1><<<nblk, kThreads, 0, L.stream>>>(dN, x, dY, g, rstd, T, d, rows, dX, dg_partial); break;
-    case 2: k_rmsnorm_bwd<2><<<nblk, kThreads, 0, L.stream>>>(dN, x, dY, g, rstd, T, d, rows, dX, dg_partial); break;
-    case 3: k_rmsnorm_bwd<3><<<nblk, kThreads, 0, L.stream>>>(dN, x, dY, g, rstd, T, d, rows, dX, dg_partial); break;
-    default: k_rmsnorm_bwd<4><<<nblk, kThreads, 0, L.stream>>>(dN, x, dY, g, rstd, T, d, rows, dX, dg_partial); break;
+    case 3: le = go(k_rmsnorm_bwd<3>, 3); break;
+    default: le = go(k_rmsnorm_bwd<4>, 4); break;
   }
+  if (le != cudaSuccess) return le;
   cudaError_t e = post_launch(L);
   if (e != cudaSuccess) return e;
   k_dg_finalize<<<(d + 31) / 32, kThreads, 0, L.stream>>>(dg_partial, nblk, d, dg);
