@@ -433,25 +433,36 @@ __device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_
 }
 
 // D[h, t] = sum_c dO[t, h*128 + c] * O[t, h*128 + c] (fp32, fixed order), lse2 = lse * log2(e).
-// One warp per (t, h): lane l takes columns 4l .. 4l+3.
+// Lane l of a half-warp takes columns 8l .. 8l+7 of its head.
 __global__ void __launch_bounds__(256) k_attn_bwd_delta(const uint16_t* __restrict__ att,
                                                         const uint16_t* __restrict__ datt,
                                                         const float* __restrict__ lse, int T, int Hq,
                                                         float* __restrict__ delta, float* __restrict__ lse2) {
+  // one warp per (token, pair of heads): each half-warp reads one head's 128 elements of O and dO
+  // as 16-byte pieces and reduces over its 16 lanes; consecutive warps take consecutive tokens of
+  // the same head pair, so the per-head outputs (head-major) are written in runs
+  const int hp_count = (Hq + 1) >> 1;
   const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (wid >= (int64_t)T * Hq) return;
-  const int t = (int)(wid / Hq), h = (int)(wid % Hq);
-  const int64_t off = (int64_t)t * Hq * kDh + h * kDh + lane * 4;
-  const uint2 o = *reinterpret_cast<const uint2*>(att + off);
-  const uint2 g = *reinterpret_cast<const uint2*>(datt + off);
-  float v = bf16_lo(o.x) * bf16_lo(g.x);
-  v = fmaf(bf16_hi(o.x), bf16_hi(g.x), v);
-  v = fmaf(bf16_lo(o.y), bf16_lo(g.y), v);
-  v = fmaf(bf16_hi(o.y), bf16_hi(g.y), v);
+  if (wid >= (int64_t)T * hp_count) return;
+  const int hp = (int)(wid / T), t = (int)(wid - (int64_t)hp * T);
+  const int h = 2 * hp + (lane >> 4);
+  const bool live = h < Hq;
+  float v = 0.0f;
+  if (live) {
+    const int64_t off = (int64_t)t * Hq * kDh + h * kDh + (lane & 15) * 8;
+    const uint4 o = *reinterpret_cast<const uint4*>(att + off);
+    const uint4 gd = *reinterpret_cast<const uint4*>(datt + off);
+    const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {gd.x, gd.y, gd.z, gd.w};
 #pragma unroll
-  for (int k = 16; k >= 1; k >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, k);
-  if (lane == 0) {
+    for (int k = 0; k < 4; ++k) {
+      v = fmaf(bf16_lo(ow[k]), bf16_lo(gw[k]), v);
+      v = fmaf(bf16_hi(ow[k]), bf16_hi(gw[k]), v);
+    }
+  }
+#pragma unroll
+  for (int k = 8; k >= 1; k >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, k);
+  if (live && (lane & 15) == 0) {
     delta[(int64_t)h * T + t] = v;
     lse2[(int64_t)h * T + t] = lse[(int64_t)h * T + t] * 1.44269504088896341f;
   }
@@ -1026,8 +1037,8 @@ cudaError_t launch_attn_fwd(const uint16_t* qkv, int64_t T, int S, int Hq, int H
 
 cudaError_t launch_attn_bwd_delta(const uint16_t* att, const uint16_t* datt, const float* lse, int64_t T, int Hq,
                                   float* delta, float* lse2, const Launch& L) {
-  const int64_t rows = T * Hq;
-  k_attn_bwd_delta<<<(unsigned)((rows * 32 + 255) / 256), 256, 0, L.stream>>>(att, datt, lse, (int)T, Hq, delta, lse2);
+  const int64_t warps = T * ((Hq + 1) / 2);
+  k_attn_bwd_delta<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, L.stream>>>(att, datt, lse, (int)T, Hq, delta, lse2);
   if (L.launches) ++*L.launches;
   return cudaGetLastError();
 }
