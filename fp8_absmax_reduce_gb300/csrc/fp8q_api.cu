@@ -937,19 +937,25 @@ struct IoList {
   void out(const void* d0, const void* d1, size_t n) { add(d0, d1, n), ++n_out; }
 };
 
-// Step i runs on set i % 2: its inputs are copied in on the h2d stream once step i - 2 (the set's
-// last user) has computed, compute(set) runs on the caller's stream once they are in and step
-// i - 2's outputs have left, and the outputs go out on the d2h stream.  host(i, k) is step i's
-// host pointer of tensor k (null: the tensor stays on the device).  A device buffer both sets
-// share must never move.
-template <class Host, class Compute>
-int run_pipelined(const IoList& io, int n_steps, Host host, Compute compute, const Ctx& c) {
-  const int n = io.n_in + io.n_out;
-  for (int k = 0; k < n; ++k) {
+// A device buffer both sets share must never move: host(i, k), step i's host pointer of tensor k,
+// is null in every step for such a buffer (and a tensor that moves needs both device buffers).
+template <class Host>
+int check_io(const IoList& io, int n_steps, Host host) {
+  for (int k = 0; k < io.n_in + io.n_out; ++k) {
     bool moved = false;
     for (int i = 0; i < n_steps; ++i) moved = moved || host(i, k) != nullptr;
     if (moved && (!io.dev[0][k] || !io.dev[1][k] || io.dev[0][k] == io.dev[1][k])) return FP8Q_ERR_INVALID_ARG;
   }
+  return FP8Q_OK;
+}
+
+// Step i runs on set i % 2: its inputs are copied in on the h2d stream once step i - 2 (the set's
+// last user) has computed, compute(set) runs on the caller's stream once they are in and step
+// i - 2's outputs have left, and the outputs go out on the d2h stream.  host(i, k) is step i's
+// host pointer of tensor k (null: the tensor stays on the device).  check_io has passed.
+template <class Host, class Compute>
+int run_pipelined(const IoList& io, int n_steps, Host host, Compute compute, const Ctx& c) {
+  const int n = io.n_in + io.n_out;
   CopyEngines* ce = nullptr;
   int e;
   if ((e = copy_engines(&ce))) return e;
@@ -1028,12 +1034,15 @@ int mlp_run_steps(const fp8q_mlp* dev0, const fp8q_mlp* dev1, const fp8q_mlp_hos
       for (int k : {4, 6, 7, 8, 9})  // dY, dX, dW_gu, dW_d, dg
         if (mlp_host(host[i], k)) return FP8Q_ERR_INVALID_ARG;
   if ((e = check_ws(ws, ws_bytes, mlp_block_workspace_size(dev0->T, dev0->d, dev0->f, backward ? 1 : 0)))) return e;
+  const IoList io = mlp_io(dev0, dev1);
+  auto host_at = [&](int i, int k) { return mlp_host(host[i], k); };
+  if ((e = check_io(io, n_steps, host_at))) return e;
   Ctx c;
   if ((e = make_ctx(&c, stream))) return e;
   MlpWs w;
   mlp_ws_layout(dev0->T, dev0->d, dev0->f, backward ? 1 : 0, static_cast<uint8_t*>(ws), &w);
   if ((e = run_pipelined(
-           mlp_io(dev0, dev1), n_steps, [&](int i, int k) { return mlp_host(host[i], k); },
+           io, n_steps, host_at,
            [&](int s) {
              int r = mlp_fwd_run(dev[s], w, c);
              return r || !backward ? r : mlp_bwd_run(dev[s], w, c);
@@ -1106,12 +1115,15 @@ int block_run_steps(const fp8q_block* dev0, const fp8q_block* dev1, const fp8q_b
   }
   const int bw = backward ? 1 : 0;
   if ((e = check_ws(ws, ws_bytes, block_workspace_size(dev0->T, dev0->d, dev0->f, dev0->n_qkv, bw)))) return e;
+  const IoList io = block_io(dev0, dev1);
+  auto host_at = [&](int i, int k) { return block_host(host[i], k); };
+  if ((e = check_io(io, n_steps, host_at))) return e;
   Ctx c;
   if ((e = make_ctx(&c, stream))) return e;
   BlockWs w;
   block_ws_layout(dev0->T, dev0->d, dev0->f, dev0->n_qkv, bw, static_cast<uint8_t*>(ws), &w);
   if ((e = run_pipelined(
-           block_io(dev0, dev1), n_steps, [&](int i, int k) { return block_host(host[i], k); },
+           io, n_steps, host_at,
            [&](int s) {
              int r = block_fwd_run(dev[s], w, c);
              return r || !backward ? r : block_bwd_run(dev[s], w, c);
