@@ -413,6 +413,323 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Forward, two query tiles per CTA
+// ---------------------------------------------------------------------------
+// One CTA per (pair of query tiles 2i, 2i+1, query head, sequence), 384 threads.  The two tiles
+// (A = 2i, B = 2i + 1) share every K/V tile (B needs one more, its diagonal), and each has its
+// own S and O in TMEM (S_A, S_B, O_A, O_B: all 512 columns) and its own softmax warpgroup
+// (warps 4-7 for A, 8-11 for B), so one tile's softmax runs while the tensor core works on the
+// other's products:
+//   warp 0      lane 0: both Q tiles once, K tiles into a 2-stage ring; lane 1: V tiles into a
+//               single stage (each lane waits only on its own ring);
+//   warp 1      MMA issuer, per key tile j: S_A(j), O_A += P_A(j-1) V_{j-1}, S_B(j),
+//               O_B += P_B(j-1) V_{j-1} (K_j released after both S, V_{j-1} after both P V);
+//   warp 2      TMEM allocation;
+//   warps 4-11  softmax as in k_attn_fwd (scores in the log2 domain, lazy rescale of O with
+//               slack kRescaleSlack), but S is read from TMEM twice -- once for the row maximum,
+//               once for the probabilities -- so a thread holds 32-64 scores at a time, not 128.
+// Shared memory: Q_A, Q_B, two K stages, one V stage, P_A, P_B (7 x 32 KB).
+constexpr int kPQA = 0;
+constexpr int kPQB = kPQA + kTile;
+constexpr int kPK = kPQB + kTile;        // [2] stages
+constexpr int kPV = kPK + 2 * kTile;     // [1] stage
+constexpr int kPPA = kPV + kTile;
+constexpr int kPPB = kPPA + kTile;
+constexpr int kPBar = kPPB + kTile;
+constexpr int kPairSmem = kPBar + 256 + 1024;
+static_assert(kPairSmem <= 232448, "shared memory per CTA");
+constexpr int kPairThreads = 384;
+
+// Maximum of this thread's row of S times log2(e)/sqrt(128); MASK: keys after row r are -inf.
+// The scale is positive, so the maximum of the raw scores times the scale is the maximum of the
+// scaled scores (rounding is monotonic): one multiply per row, not per score.
+template <bool MASK>
+__device__ __forceinline__ float row_max(uint32_t tS, int r, float scale_log2) {
+  float mp[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
+#pragma unroll
+  for (int c2 = 0; c2 < 4; c2 += 2) {
+    uint32_t w[2][32];
+    tmem_ld32x2(tS + c2 * 32, tS + c2 * 32 + 32, w[0], w[1]);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const int col = (c2 + h) * 32 + k;
+        const float x = (MASK && col > r) ? -INFINITY : __uint_as_float(w[h][k]);
+        mp[k & 7] = fmaxf(mp[k & 7], x);
+      }
+  }
+  const float m = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+  return m * scale_log2;
+}
+
+// p = 2^(s scale - m_ref) of this thread's row of S as bf16 into the K-major P tile (two scores
+// per packed fused multiply-add); returns the row sum of the unrounded probabilities.  The thread
+// arrives on s_free right after its last TMEM load, so the next S product can start while the
+// last chunk's probabilities are formed.
+template <bool MASK>
+__device__ __forceinline__ float row_probs(uint32_t tS, int r, float scale_log2, float m_ref, uint32_t ptile,
+                                           uint64_t* s_free) {
+  float2 rp[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) rp[i] = make_float2(0.0f, 0.0f);
+  const float2 sc = make_float2(scale_log2, scale_log2), nm = make_float2(-m_ref, -m_ref);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t sw[32], w[16];
+    tmem_ld32(tS + c * 32, sw);
+    if (c == 3) {
+      tc_fence_before();
+      mbar_arrive(s_free);
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int col = c * 32 + 2 * k;
+      const float2 x = __ffma2_rn(make_float2(__uint_as_float(sw[2 * k]), __uint_as_float(sw[2 * k + 1])), sc, nm);
+      const float p0 = (MASK && col > r) ? 0.0f : ex2_approx(x.x);
+      const float p1 = (MASK && col + 1 > r) ? 0.0f : ex2_approx(x.y);
+      rp[k & 3] = __fadd2_rn(rp[k & 3], make_float2(p0, p1));
+      w[k] = pack_bf16x2(p0, p1);
+    }
+    tile_put32(ptile, r, c, w);
+  }
+  const float2 t = __fadd2_rn(__fadd2_rn(rp[0], rp[1]), __fadd2_rn(rp[2], rp[3]));
+  return t.x + t.y;
+}
+
+__global__ void __launch_bounds__(kPairThreads, 1)
+    k_attn_fwd_pair(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmAtt,
+                    const AttnArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPBar);
+  uint64_t* q_full = bars + 0;
+  uint64_t* k_full = bars + 1;   // [2]
+  uint64_t* k_empty = bars + 3;  // [2] K_j is free once S_A(j), S_B(j) are computed
+  uint64_t* v_full = bars + 5;
+  uint64_t* v_empty = bars + 6;  // V_j is free once both P V_j products are computed
+  uint64_t* s_full = bars + 7;   // [2] per tile (A, B)
+  uint64_t* s_free = bars + 9;   // [2] the softmax has read S
+  uint64_t* p_full = bars + 11;  // [2] P written
+  uint64_t* p_free = bars + 13;  // [2] P V read P (and O holds every product so far)
+  uint64_t* o_full = bars + 15;  // [2] one phase per P V product
+  uint64_t* drain = bars + 17;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int pr = p.n_qt / 2 - 1 - (int)blockIdx.x;  // the longest pairs first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int g = h / (p.Hq / p.Hkv);
+  const int qa = 2 * pr;
+  const int na = qa + 1, nb = qa + 2;  // key tiles of A (0 .. qa) and of B (0 .. qa + 1)
+  const int t0a = b * p.S + qa * 128, t0b = t0a + 128;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s2 = 0; s2 < 2; ++s2) {
+      mbar_init(&k_full[s2], 1);
+      mbar_init(&k_empty[s2], 1);
+      mbar_init(&s_full[s2], 1);
+      mbar_init(&s_free[s2], 128);
+      mbar_init(&p_full[s2], 128);
+      mbar_init(&p_free[s2], 1);
+      mbar_init(&o_full[s2], 1);
+    }
+    mbar_init(v_full, 1);
+    mbar_init(v_empty, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQKV);
+    tma_prefetch_desc(&tmAtt);
+  }
+  if (warp == 2) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t sbase = smem_addr(smem);
+  const int xk = (p.Hq + g) * kDh, xv = (p.Hq + p.Hkv + g) * kDh;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- Q tiles, then the K ring ----------------
+      bool ok = true;
+      uint32_t issued = 0, issued_par = 0;
+      mbar_arrive_expect_tx(q_full, 2 * kTile);
+      tma_load_2d(smem + kPQA, &tmQKV, q_full, h * kDh, t0a);
+      tma_load_2d(smem + kPQA + kAtom, &tmQKV, q_full, h * kDh + 64, t0a);
+      tma_load_2d(smem + kPQB, &tmQKV, q_full, h * kDh, t0b);
+      tma_load_2d(smem + kPQB + kAtom, &tmQKV, q_full, h * kDh + 64, t0b);
+      for (int j = 0; j < nb; ++j) {
+        const int st = j & 1;
+        const uint32_t u = (uint32_t)(j >> 1) & 1u;
+        if (!mbar_wait(&k_empty[st], u ^ 1u, abort_flag)) { ok = false; break; }
+        uint8_t* sk = smem + kPK + st * kTile;
+        const int y = b * p.S + j * 128;
+        mbar_arrive_expect_tx(&k_full[st], kTile);
+        tma_load_2d(sk, &tmQKV, &k_full[st], xk, y);
+        tma_load_2d(sk + kAtom, &tmQKV, &k_full[st], xk + 64, y);
+        issued |= 1u << st;
+        issued_par = (issued_par & ~(1u << st)) | (u << st);
+      }
+      if (!ok) {
+        atomicOr(p.status, kStatusTimeout);
+        *abort_flag = 1;
+        int dummy = 0;
+        mbar_wait(q_full, 0, &dummy);
+        for (int s2 = 0; s2 < 2; ++s2)
+          if (issued & (1u << s2)) mbar_wait(&k_full[s2], (issued_par >> s2) & 1u, &dummy);
+      }
+    } else if (lane == 1) {
+      // ---------------- the V stage ----------------
+      bool ok = true;
+      int last = -1;  // the last V load issued
+      for (int j = 0; j < nb; ++j) {
+        if (!mbar_wait(v_empty, ((uint32_t)j & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+        mbar_arrive_expect_tx(v_full, kTile);
+        const int y = b * p.S + j * 128;
+        tma_load_2d(smem + kPV, &tmQKV, v_full, xv, y);
+        tma_load_2d(smem + kPV + kAtom, &tmQKV, v_full, xv + 64, y);
+        last = j;
+      }
+      if (!ok) {
+        atomicOr(p.status, kStatusTimeout);
+        *abort_flag = 1;
+        int dummy = 0;
+        if (last >= 0) mbar_wait(v_full, (uint32_t)last & 1u, &dummy);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      const uint32_t tSa = tmem, tSb = tmem + 128, tOa = tmem + 256, tOb = tmem + 384;
+      bool ok = mbar_wait(q_full, 0, abort_flag);
+      // per key tile j: S_A(j), then O_A += P_A(j-1) V_{j-1} (both wait only on tile A's softmax),
+      // then S_B(j) and O_B += P_B(j-1) V_{j-1} -- each tile's chain is independent of the other's
+      for (int j = 0; j <= nb && ok; ++j) {
+        const int st = j & 1, i = j - 1;
+        const uint32_t u = (uint32_t)(j >> 1) & 1u, par = (uint32_t)j & 1u, pi = (uint32_t)i & 1u;
+        if (j < nb && !mbar_wait(&k_full[st], u, abort_flag)) { ok = false; break; }
+        if (j < na) {
+          if (!mbar_wait(&s_free[0], par ^ 1u, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          mma_tile_kk(tSa, sbase + kPQA, sbase + kPK + st * kTile, false);  // S_A = Q_A K_j^T
+          umma_commit(&s_full[0]);
+        }
+        if (j >= 1 && i < na) {
+          if (!mbar_wait(v_full, pi, abort_flag) || !mbar_wait(&p_full[0], pi, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          mma_tile_kmn(tOa, sbase + kPPA, sbase + kPV, i > 0);  // O_A += P_A V_i
+          umma_commit(&o_full[0]);
+          umma_commit(&p_free[0]);
+        }
+        if (j < nb) {
+          if (!mbar_wait(&s_free[1], par ^ 1u, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          mma_tile_kk(tSb, sbase + kPQB, sbase + kPK + st * kTile, false);    // S_B = Q_B K_j^T
+          umma_commit(&s_full[1]);
+          umma_commit(&k_empty[st]);
+        }
+        if (j >= 1) {
+          if (!mbar_wait(v_full, pi, abort_flag) || !mbar_wait(&p_full[1], pi, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          mma_tile_kmn(tOb, sbase + kPPB, sbase + kPV, i > 0);    // O_B += P_B V_i
+          umma_commit(&o_full[1]);
+          umma_commit(&p_free[1]);
+          umma_commit(v_empty);
+        }
+      }
+      if (!ok) {
+        atomicOr(p.status, kStatusTimeout);
+        *abort_flag = 1;
+      }
+      umma_commit(drain);
+      int dummy = 0;
+      mbar_wait(drain, 0, &dummy);
+    }
+  } else if (warp >= 4) {
+    // ---------------- softmax: warps 4-7 tile A, warps 8-11 tile B ----------------
+    const int side = (warp - 4) >> 2;
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + (uint32_t)(side * 128) + lane_off, tO = tmem + 256 + (uint32_t)(side * 128) + lane_off;
+    const uint32_t ptile = sbase + (side ? kPPB : kPPA);
+    const int nx = side ? nb : na;
+    const int diag = nx - 1;
+    float m_ref = -INFINITY, l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < nx && ok; ++j) {
+      const uint32_t par = (uint32_t)j & 1u;
+      if (!warp_wait(&s_full[side], par, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      const bool dg = j == diag;
+      const float mx = dg ? row_max<true>(tS, r, p.scale_log2) : row_max<false>(tS, r, p.scale_log2);
+      // P V_{j-1} has read P and O holds every product up to j - 1
+      if (!warp_wait(&p_free[side], par ^ 1u, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      if (__any_sync(0xFFFFFFFFu, mx > m_ref + kRescaleSlack)) {
+        const float m_new = fmaxf(m_ref, mx);
+        const float alpha = ex2_approx(m_ref - m_new);  // 0 on the first tile, 1 where nothing moves
+        if (j > 0) {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t w[32];
+            tmem_ld32(tO + c * 32, w);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) w[k] = __float_as_uint(__uint_as_float(w[k]) * alpha);
+            tmem_st32(tO + c * 32, w);
+          }
+        }
+        l *= alpha;
+        m_ref = m_new;
+      }
+      l += dg ? row_probs<true>(tS, r, p.scale_log2, m_ref, ptile, &s_free[side])
+              : row_probs<false>(tS, r, p.scale_log2, m_ref, ptile, &s_free[side]);
+      fence_async_shared();
+      mbar_arrive(&p_full[side]);
+    }
+    if (ok && !warp_wait(&o_full[side], (uint32_t)(nx - 1) & 1u, abort_flag)) ok = false;
+    if (!ok) {
+      atomicOr(p.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
+    // O / l goes out through this tile's Q buffer (its last reader, S(nx - 1), has completed)
+    const uint32_t qtile = sbase + (side ? kPQB : kPQA);
+    const int t0 = side ? t0b : t0a;
+    if (ok) {
+      tc_fence_after();
+      const float inv = 1.0f / l;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t ov[32], w[16];
+        tmem_ld32(tO + c * 32, ov);
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          w[k] = pack_bf16x2(__uint_as_float(ov[2 * k]) * inv, __uint_as_float(ov[2 * k + 1]) * inv);
+        tile_put32(qtile, r, c, w);
+      }
+      p.lse[(int64_t)h * p.T + t0 + r] = (m_ref + log2f(l)) * 0.693147180559945309f;
+    }
+    fence_async_shared();
+    named_bar_sync(1 + side, 128);
+    if (r == 0 && !*abort_flag) {
+      tma_store_2d(&tmAtt, qtile, h * kDh, t0);
+      tma_store_2d(&tmAtt, qtile + kAtom, h * kDh + 64, t0);
+      bulk_commit_and_wait();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
 // Backward
 // ---------------------------------------------------------------------------
 struct AttnBwdArgs {
@@ -993,7 +1310,7 @@ cudaError_t set_smem(K kernel, int bytes, int& configured) {
   if (e == cudaSuccess) configured = dev;
   return e;
 }
-int g_cfg_fwd = -1, g_cfg_dkdv = -1, g_cfg_dq = -1;
+int g_cfg_fwd = -1, g_cfg_fwd_pair = -1, g_cfg_dkdv = -1, g_cfg_dq = -1;
 
 AttnBwdArgs bwd_args(int64_t T, int S, int Hq, int Hkv, const float* delta, const float* lse2, const Launch& L) {
   AttnBwdArgs a{};
@@ -1027,10 +1344,18 @@ cudaError_t launch_attn_fwd(const uint16_t* qkv, int64_t T, int S, int Hq, int H
   a.scale_log2 = 1.44269504088896341f / 11.3137084989847604f;  // log2(e) / sqrt(128)
   a.lse = lse;
   a.status = L.status;
-  cudaError_t e = set_smem(k_attn_fwd, kFwdSmem, g_cfg_fwd);
-  if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)a.n_qt, (unsigned)Hq, (unsigned)(T / S));
-  k_attn_fwd<<<grid, kAttnThreads, kFwdSmem, L.stream>>>(tq, ta, a);
+  if (a.n_qt % 2 == 0) {
+    // pairs of query tiles share their K/V tiles and overlap each other's softmax
+    cudaError_t e = set_smem(k_attn_fwd_pair, kPairSmem, g_cfg_fwd_pair);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)(a.n_qt / 2), (unsigned)Hq, (unsigned)(T / S));
+    k_attn_fwd_pair<<<grid, kPairThreads, kPairSmem, L.stream>>>(tq, ta, a);
+  } else {
+    cudaError_t e = set_smem(k_attn_fwd, kFwdSmem, g_cfg_fwd);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)a.n_qt, (unsigned)Hq, (unsigned)(T / S));
+    k_attn_fwd<<<grid, kAttnThreads, kFwdSmem, L.stream>>>(tq, ta, a);
+  }
   if (L.launches) ++*L.launches;
   return cudaGetLastError();
 }
