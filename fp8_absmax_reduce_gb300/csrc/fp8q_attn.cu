@@ -789,37 +789,40 @@ __global__ void __launch_bounds__(256) k_attn_bwd_delta(const uint16_t* __restri
 // dS = P (dP - D).  dQ (per row lse2, D): MASK drops keys after the query row r.  dK/dV
 // (per column lse2, D from shared memory): MASK drops the columns before r, which the caller
 // sets to the key row minus the query sub-tile's offset from the key tile.
+// dS row chunk of the dQ pass: p = 2^(s scale - lse2), dS = p (dP - D), two columns per packed
+// fused multiply-add / add / multiply.
 template <bool MASK>
 __device__ __forceinline__ void ds_row_chunk(const uint32_t (&sv)[32], const uint32_t (&dv)[32], int c, int r,
                                              float scale_log2, float lse2, float dlt, uint32_t (&w)[16]) {
+  const float2 sc = make_float2(scale_log2, scale_log2), nl = make_float2(-lse2, -lse2), nd = make_float2(-dlt, -dlt);
 #pragma unroll
   for (int k = 0; k < 16; ++k) {
-    float dd[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int col = c * 32 + 2 * k + e;
-      const float pp = (MASK && col > r) ? 0.0f : ex2_approx(__uint_as_float(sv[2 * k + e]) * scale_log2 - lse2);
-      dd[e] = pp * (__uint_as_float(dv[2 * k + e]) - dlt);
-    }
-    w[k] = pack_bf16x2(dd[0], dd[1]);
+    const int col = c * 32 + 2 * k;
+    const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1])), sc, nl);
+    const float2 pp = make_float2((MASK && col > r) ? 0.0f : ex2_approx(x.x), (MASK && col + 1 > r) ? 0.0f : ex2_approx(x.y));
+    const float2 dd =
+        __fmul2_rn(pp, __fadd2_rn(make_float2(__uint_as_float(dv[2 * k]), __uint_as_float(dv[2 * k + 1])), nd));
+    w[k] = pack_bf16x2(dd.x, dd.y);
   }
 }
+// P^T and dS^T column chunk of the dK/dV pass (one key row per thread, query columns): lse2 and D
+// per column from shared memory.
 template <bool MASK>
 __device__ __forceinline__ void pds_col_chunk(const uint32_t (&sv)[32], const uint32_t (&dv)[32], int c, int r,
                                               float scale_log2, const float* lse2, const float* dlt,
                                               uint32_t (&wp)[16], uint32_t (&ws)[16]) {
+  const float2 sc = make_float2(scale_log2, scale_log2);
 #pragma unroll
   for (int k = 0; k < 16; ++k) {
-    float pp[2], dd[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int col = c * 32 + 2 * k + e;
-      const float pt = (MASK && col < r) ? 0.0f : ex2_approx(__uint_as_float(sv[2 * k + e]) * scale_log2 - lse2[col]);
-      pp[e] = pt;
-      dd[e] = pt * (__uint_as_float(dv[2 * k + e]) - dlt[col]);
-    }
-    wp[k] = pack_bf16x2(pp[0], pp[1]);
-    ws[k] = pack_bf16x2(dd[0], dd[1]);
+    const int col = c * 32 + 2 * k;
+    const float2 l2 = *reinterpret_cast<const float2*>(lse2 + col), d2 = *reinterpret_cast<const float2*>(dlt + col);
+    const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1])), sc,
+                                make_float2(-l2.x, -l2.y));
+    const float2 pt = make_float2((MASK && col < r) ? 0.0f : ex2_approx(x.x), (MASK && col + 1 < r) ? 0.0f : ex2_approx(x.y));
+    const float2 dd = __fmul2_rn(
+        pt, __fadd2_rn(make_float2(__uint_as_float(dv[2 * k]), __uint_as_float(dv[2 * k + 1])), make_float2(-d2.x, -d2.y)));
+    wp[k] = pack_bf16x2(pt.x, pt.y);
+    ws[k] = pack_bf16x2(dd.x, dd.y);
   }
 }
 
