@@ -157,7 +157,8 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 // and O, accumulated by the tensor core in TMEM, is rescaled only on those rare steps.
 constexpr float kRescaleSlack = 8.0f;
 
-// S row of this thread (128 scores, times log2(e)/sqrt(128)) into registers and its maximum.
+// S row of this thread (128 raw scores) into registers and the maximum of the scaled scores
+// (times log2(e)/sqrt(128); the scale is positive, so it is applied once to the raw maximum).
 // MASK (the diagonal tile): keys after the query row r become -inf.  Eight partial maxima keep
 // the reduction's dependency chain short.
 template <bool MASK>
@@ -174,13 +175,13 @@ __device__ __forceinline__ float load_scores(uint32_t tS, int r, float scale_log
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
         const int col = (c2 + h) * 32 + k;
-        float x = __uint_as_float(w[h][k]) * scale_log2;
-        if (MASK && col > r) x = -INFINITY;
+        const float x = (MASK && col > r) ? -INFINITY : __uint_as_float(w[h][k]);
         sv[col] = x;
         mp[k & 7] = fmaxf(mp[k & 7], x);
       }
   }
-  return fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+  const float m = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+  return m * scale_log2;
 }
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -357,23 +358,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         m_ref = m_new;
       }
       if (!warp_wait(&p_free[pb], u ^ 1u, abort_flag)) { ok = false; break; }
-      float rp[8];
+      float2 rp[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) rp[i] = 0.0f;
+      for (int i = 0; i < 4; ++i) rp[i] = make_float2(0.0f, 0.0f);
+      const float2 sc = make_float2(p.scale_log2, p.scale_log2), nm = make_float2(-m_ref, -m_ref);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t w[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const float p0 = ex2_approx(sv[c * 32 + 2 * k] - m_ref);  // 2^-inf = 0 for masked keys
-          const float p1 = ex2_approx(sv[c * 32 + 2 * k + 1] - m_ref);
-          rp[(2 * k) & 7] += p0;
-          rp[(2 * k + 1) & 7] += p1;
+          // 2^(s scale - m_ref), two scores per packed fused multiply-add; 2^-inf = 0 for masked keys
+          const float2 x = __ffma2_rn(make_float2(sv[c * 32 + 2 * k], sv[c * 32 + 2 * k + 1]), sc, nm);
+          const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+          rp[k & 3] = __fadd2_rn(rp[k & 3], make_float2(p0, p1));
           w[k] = pack_bf16x2(p0, p1);
         }
         tile_put32(sbase + kFP + pb * kTile, r, c, w);
       }
-      l += ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
+      {
+        const float2 t = __fadd2_rn(__fadd2_rn(rp[0], rp[1]), __fadd2_rn(rp[2], rp[3]));
+        l += t.x + t.y;
+      }
       tc_fence_before();
       fence_async_shared();
       mbar_arrive(&p_full[pb]);
