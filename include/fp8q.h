@@ -59,7 +59,7 @@ extern "C" {
 typedef enum {
   FP8Q_OK = 0,
   FP8Q_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size or leading dimension   */
-  FP8Q_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement              */
+  FP8Q_ERR_UNSUPPORTED = 2,  /* valid request the library does not implement            */
   FP8Q_ERR_CUDA = 3,         /* a CUDA runtime/driver call or a kernel launch failed      */
   FP8Q_ERR_TIMEOUT = 4,      /* device status only: a bounded wait in a kernel ran out    */
   FP8Q_ERR_NONFINITE = 5,    /* device status only: a tensor's amax was Inf or NaN        */
