@@ -7,6 +7,8 @@
 #include <mutex>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 namespace {
 
 using namespace fp8q;
@@ -38,10 +40,13 @@ struct Trace {
 };
 thread_local Trace t_trace;
 
+// One kernel step: an NVTX range named for the kernel kind (seen by profilers, free otherwise)
+// and, while the trace is on, a pair of CUDA events around its launches.
 struct TraceScope {
   cudaStream_t s;
   bool active;
   TraceScope(cudaStream_t st, int kind) : s(st), active(false) {
+    nvtxRangePushA(kKindNames[kind]);
     Trace& t = t_trace;
     if (t.on && t.n < (int)t.kinds.size()) {
       active = true;
@@ -54,6 +59,7 @@ struct TraceScope {
       cudaEventRecord(t_trace.ev[2 * t_trace.n + 1], s);
       ++t_trace.n;
     }
+    nvtxRangePop();
   }
 };
 
