@@ -48,7 +48,7 @@ def check_rows(b, ref, rows=None):
         assert row_rel(sel(host_f64(t)), ref[k]) < tol, k
 
 
-@pytest.mark.parametrize("T,d,f", [(192, 256, 384), (272, 528, 400), (1, 16, 16), (640, 1024, 1280)])
+@pytest.mark.parametrize("T,d,f", [(192, 256, 384), (272, 528, 400), (1, 16, 16), (640, 1024, 1280), (96, 5136, 1024)])
 def test_bf16_block_small_shapes(T, d, f):
     b, inp = run_bf16(synth.BY_NAME["7b-mlp-fwd-bwd"], T, d, f)
     ref = oracle.block(inp["x"], inp["g"], inp["W_gu"], inp["W_d"], dY=inp["dY"], eps=b.eps, nthreads=16,
