@@ -100,3 +100,12 @@ def test_gemm_cluster_pairs(layout, M, N, K):
     assert row_rel(got, ref) < 2e-3
     got2, _ = run_case(layout, M, N, K, 0, 1 if layout == fq.TN else 0, "f32", False, seed=M + N + K + layout)
     assert np.array_equal(got, got2)
+
+
+@pytest.mark.parametrize("layout", [fq.NN, fq.NT, fq.TN])
+@pytest.mark.parametrize("fa,fb", [(0, 0), (1, 0), (0, 1)])
+def test_gemm_cluster_formats(layout, fa, fb):
+    """The two-CTA cluster path (4 M tiles, the last ragged) with every E4M3/E5M2 operand mix and
+    bf16 output."""
+    got, ref = run_case(layout, 400, 528, 272, fa, fb, "bf16", False, seed=7 * layout + 3 * fa + fb)
+    assert row_rel(got, ref) < 2e-3
