@@ -50,12 +50,13 @@ constexpr int kStagingOffset = STAGES * kStage;
 constexpr int kBarOffset = kStagingOffset + 8 * kStagingBytes;
 constexpr int kSmemBytes = kBarOffset + 256 + 1024;  // + barriers + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-constexpr int kGroupM = 16;                          // M tiles per rasterisation group
+constexpr int kGroupRows = 2048;                     // rows of A per rasterisation group (the default)
 
 struct Args {
   int M, N, K;
   int m_tiles, n_tiles, k_blocks;
   int m_units, num_tiles;  // scheduling units: M tiles (one CTA) or M-tile pairs (a 2-CTA cluster); units x n_tiles
+  int group;               // M units per rasterisation group
   int b_step, b_half1;  // B's N coordinate of a tile = nb * b_step (+ b_half1 for the second half)
   int epi, out_f32;
   uint32_t idesc;
@@ -71,9 +72,10 @@ struct Args {
   unsigned* status;
 };
 
-// Unit -> (M unit, N tile), rasterised in groups of G M units (all N tiles of a group before the
-// next group) so that the group's A rows stay in L2.
-__device__ __forceinline__ void tile_coords(int tile, const Args& p, int& mb, int& nb, int G = kGroupM) {
+// Unit -> (M unit, N tile), rasterised in groups of p.group M units: all N tiles of a group before
+// the next group, M fastest inside it, so that the group's A rows stay in L2 while B streams.
+__device__ __forceinline__ void tile_coords(int tile, const Args& p, int& mb, int& nb) {
+  const int G = p.group;
   const int span = G * p.n_tiles;
   const int grp = tile / span;
   const int first_m = grp * G;
@@ -236,7 +238,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // this CTA's scheduling units: u = first, first + step, ...; M tile = u * CL + crank
   const int u_first = CL == 2 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int u_step = CL == 2 ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-  constexpr int kGroupU = kGroupM / CL;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], CL); }
     for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], kEpiThreads); }
@@ -267,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int tile = u_first; tile < p.num_tiles && ok; tile += u_step) {
         int mb, nb;
-        tile_coords(tile, p, mb, nb, kGroupU);
+        tile_coords(tile, p, mb, nb);
         const int m0 = (mb * CL + crank) * BM;
         const int n0 = nb * p.b_step, n1 = n0 + p.b_half1;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -381,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float alpha = p.sinvA ? __fmul_rn(*p.sinvA, *p.sinvB) : 1.0f;  // 1: unscaled (bf16) operands
     for (int tile = u_first; tile < p.num_tiles; tile += u_step) {
       int mb, nb;
-      tile_coords(tile, p, mb, nb, kGroupU);
+      tile_coords(tile, p, mb, nb);
       mb = mb * CL + crank;
       const int row0 = mb * BM + sub * 32;
       const int row = row0 + lane;
@@ -965,6 +966,20 @@ cudaError_t launch_wide_t(const CUtensorMap& ta, const CUtensorMap& tb, const CU
   return cudaGetLastError();
 }
 
+// The rasterisation group of a GEMM, in M units of unit_rows rows.  A group walks its M units for
+// each N tile in turn, so its A rows are re-read from L2 while B passes once per group.  When all of
+// A fits comfortably in L2 (and is the smaller operand), one group spanning every M unit reads each
+// operand byte from DRAM once; when B does instead, groups of one M unit walk N fastest and keep B
+// resident; otherwise groups of kGroupRows rows bound A's share of L2.  "Comfortably": half the
+// L2 or less, leaving room for the streamed operand's tiles in flight and the output.
+int raster_group(int64_t a_bytes, int64_t b_bytes, int m_units, int unit_rows) {
+  constexpr int64_t kResident = 48ll << 20;
+  if (a_bytes <= b_bytes && a_bytes <= kResident) return m_units;
+  if (b_bytes < a_bytes && b_bytes <= kResident) return 1;
+  const int g = kGroupRows / unit_rows;
+  return g < 1 ? 1 : g;
+}
+
 }  // namespace
 
 cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L) {
@@ -1045,6 +1060,9 @@ cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L) {
     a.num_tiles = a.m_units * a.n_tiles;
     grid = a.num_tiles < L.num_sms ? a.num_tiles : L.num_sms;
   }
+  const int64_t es_bytes = g.op16 ? 2 : 1;
+  a.group = raster_group((int64_t)g.M * g.K * es_bytes, (int64_t)g.b_cols * g.K * es_bytes, a.m_units,
+                         wide ? 256 : (clusters > 0 ? 2 * BM : BM));
   *P = grid;
   cudaError_t e;
   if (wide) {
