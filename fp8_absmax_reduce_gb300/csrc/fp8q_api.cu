@@ -505,7 +505,8 @@ size_t block_ws_layout(int64_t T, int64_t d, int64_t f, int64_t nq, int backward
 int validate_attention(const void* qkv, int64_t T, int64_t S, int Hq, int Hkv, int dh) {
   if (!al16(qkv) || T < 1 || S < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || T % S) return FP8Q_ERR_INVALID_ARG;
   if (dh != 128 || S % 128) return FP8Q_ERR_UNSUPPORTED;
-  if (Hq > 65535 || T / S > 65535 || T > ((int64_t)1 << 31) - 1) return FP8Q_ERR_INVALID_ARG;
+  // the kernels' one-dimensional grids count (T / 128) x n_heads CTAs in an int
+  if (T > ((int64_t)1 << 31) - 1 || T / 128 * Hq > ((int64_t)1 << 31) - 1) return FP8Q_ERR_INVALID_ARG;
   return FP8Q_OK;
 }
 

@@ -72,6 +72,35 @@ struct AttnArgs {
   unsigned* status;
 };
 
+// CTA order.  A CTA's work depends on its tile's place on the causal diagonal, so a grid walked
+// tile by tile inside each (head, sequence) pair leaves the longest CTAs of the last pairs to run
+// alone at the end (in a greedy schedule of 32 tiles per pair on 152 SMs: 17 % over the ideal for
+// dK/dV, 3 % for dQ, 7 % for the paired forward).  The grids are one-dimensional instead and hand
+// the tiles out in bands of BAND, the longest band first, every (head, sequence) pair of a band
+// before the next band, each pair's tiles of the band together: the longest CTAs start first and
+// the last ones dispatched are short, while the CTAs of a band that share a pair run at the same
+// time and share its re-read tiles in L2.  Wider bands keep more of that sharing, narrower ones
+// balance better.  rank 0 is the longest tile of a pair; the last band may be narrower.
+template <int BAND>
+__device__ __forceinline__ void cta_order(int n_tiles, int heads, int n_seq, int& rank, int& h, int& b) {
+  const int pairs = heads * n_seq;
+  const int band = (int)blockIdx.x / (BAND * pairs);
+  const int k0 = band * BAND;
+  const int width = min(BAND, n_tiles - k0);
+  const int rem = (int)blockIdx.x - band * BAND * pairs;
+  const int pair = rem / width;
+  rank = k0 + rem % width;
+  h = pair % heads;
+  b = pair / heads;
+}
+// Band widths, measured on 32 tiles per pair (32B block: 40 query / 8 K/V heads, 4 sequences of
+// 4096), as each kernel's time over the forward's in the same step (the clocks move with the power
+// cap): the forward re-reads only K and V (67 MB in all, L2-resident whatever the order) and takes
+// bands of one tile (~1 % faster than pairs walked in order); dK/dV, which re-reads the group's Q
+// and dO (335 MB), 2.49 with one band of all -> 2.18 with bands of 2 (2.19 with 4, 2.24 with 8);
+// dQ, which re-reads K and V, 1.65 with one band of all, 1.72 / 1.67 / 1.64 with bands of 4 / 8 / 16.
+constexpr int kFwdBand = 1, kDkdvBand = 2, kDqBand = 16;
+
 // Instruction descriptor: kind::f16 with bf16 A and B, fp32 accumulator, M = N = 128,
 // A K-major, B K-major (b_mn = 0) or MN-major (1).
 __host__ __device__ constexpr uint32_t idesc_bf16_128(int b_mn) {
@@ -204,8 +233,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  const int qt = p.n_qt - 1 - (int)blockIdx.x;  // the longest rows first
-  const int h = blockIdx.y, b = blockIdx.z;
+  int rank, h, b;
+  cta_order<kFwdBand>(p.n_qt, p.Hq, p.T / p.S, rank, h, b);
+  const int qt = p.n_qt - 1 - rank;
   const int g = h / (p.Hq / p.Hkv);
   const int t0 = b * p.S + qt * 128;
   const int n = qt + 1;  // key tiles 0 .. qt (causal)
@@ -524,8 +554,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  const int pr = p.n_qt / 2 - 1 - (int)blockIdx.x;  // the longest pairs first
-  const int h = blockIdx.y, b = blockIdx.z;
+  int rank, h, b;
+  cta_order<kFwdBand>(p.n_qt / 2, p.Hq, p.T / p.S, rank, h, b);
+  const int pr = p.n_qt / 2 - 1 - rank;
   const int g = h / (p.Hq / p.Hkv);
   const int qa = 2 * pr;
   const int na = qa + 1, nb = qa + 2;  // key tiles of A (0 .. qa) and of B (0 .. qa + 1)
@@ -887,7 +918,8 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  const int jt = (int)blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  int jt, g, b;  // key tile jt sees the query sub-tiles at or after it: jt = 0 is the longest
+  cta_order<kDkdvBand>(p.n_qt, p.Hkv, p.T / p.S, jt, g, b);
   const int rep = p.Hq / p.Hkv;
   const int n_sub = 2 * (p.n_qt - jt);  // 64-query sub-tiles at or after this key tile
   const int n_items = rep * n_sub;      // item u: head g*rep + u / n_sub, sub-tile u % n_sub
@@ -1099,8 +1131,9 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  const int qt = p.n_qt - 1 - (int)blockIdx.x;
-  const int h = blockIdx.y, b = blockIdx.z;
+  int rank, h, b;
+  cta_order<kDqBand>(p.n_qt, p.Hq, p.T / p.S, rank, h, b);
+  const int qt = p.n_qt - 1 - rank;
   const int g = h / (p.Hq / p.Hkv);
   const int t0 = b * p.S + qt * 128;
   const int n = qt + 1;
@@ -1356,12 +1389,12 @@ cudaError_t launch_attn_fwd(const uint16_t* qkv, int64_t T, int S, int Hq, int H
     // pairs of query tiles share their K/V tiles and overlap each other's softmax
     cudaError_t e = set_smem(k_attn_fwd_pair, kPairSmem, g_cfg_fwd_pair);
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)(a.n_qt / 2), (unsigned)Hq, (unsigned)(T / S));
+    const unsigned grid = (unsigned)(a.n_qt / 2) * (unsigned)Hq * (unsigned)(T / S);
     k_attn_fwd_pair<<<grid, kPairThreads, kPairSmem, L.stream>>>(tq, ta, a);
   } else {
     cudaError_t e = set_smem(k_attn_fwd, kFwdSmem, g_cfg_fwd);
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)a.n_qt, (unsigned)Hq, (unsigned)(T / S));
+    const unsigned grid = (unsigned)a.n_qt * (unsigned)Hq * (unsigned)(T / S);
     k_attn_fwd<<<grid, kAttnThreads, kFwdSmem, L.stream>>>(tq, ta, a);
   }
   if (L.launches) ++*L.launches;
@@ -1386,7 +1419,7 @@ cudaError_t launch_attn_bwd_dkdv(const uint16_t* qkv, const uint16_t* datt, int6
   const AttnBwdArgs a = bwd_args(T, S, Hq, Hkv, delta, lse2, L);
   cudaError_t e = set_smem(k_attn_bwd_dkdv, kDkdvSmem, g_cfg_dkdv);
   if (e != cudaSuccess) return e;
-  k_attn_bwd_dkdv<<<dim3((unsigned)a.n_qt, (unsigned)Hkv, (unsigned)(T / S)), kAttnBwdThreads, kDkdvSmem, L.stream>>>(
+  k_attn_bwd_dkdv<<<(unsigned)a.n_qt * (unsigned)Hkv * (unsigned)(T / S), kAttnBwdThreads, kDkdvSmem, L.stream>>>(
       tq, tq64, tdo64, tdq, a);
   if (L.launches) ++*L.launches;
   return cudaGetLastError();
@@ -1402,7 +1435,7 @@ cudaError_t launch_attn_bwd_dq(const uint16_t* qkv, const uint16_t* datt, int64_
   const AttnBwdArgs a = bwd_args(T, S, Hq, Hkv, delta, lse2, L);
   cudaError_t e = set_smem(k_attn_bwd_dq, kDqSmem, g_cfg_dq);
   if (e != cudaSuccess) return e;
-  k_attn_bwd_dq<<<dim3((unsigned)a.n_qt, (unsigned)Hq, (unsigned)(T / S)), kAttnBwdThreads, kDqSmem, L.stream>>>(
+  k_attn_bwd_dq<<<(unsigned)a.n_qt * (unsigned)Hq * (unsigned)(T / S), kAttnBwdThreads, kDqSmem, L.stream>>>(
       tq, tdo, tdq, a);
   if (L.launches) ++*L.launches;
   return cudaGetLastError();

@@ -373,8 +373,9 @@ FP8Q_API int block_run_steps(const fp8q_block* dev0, const fp8q_block* dev1, con
  *   lse [n_heads, T] fp32: natural log of each row's softmax denominator (kept for the backward)
  * P is rounded to bf16 before it multiplies V (the tensor-core operand), its row sum is not.
  * Requirements: head_dim = 128 and seq_len a positive multiple of 128 (else
- * FP8Q_ERR_UNSUPPORTED); n_heads a multiple of n_kv_heads, T a multiple of seq_len, pointers
- * 16-byte aligned (else FP8Q_ERR_INVALID_ARG).  Asynchronous; no workspace. */
+ * FP8Q_ERR_UNSUPPORTED); n_heads a multiple of n_kv_heads, T a multiple of seq_len, T and
+ * (T / 128) n_heads below 2^31, pointers 16-byte aligned (else FP8Q_ERR_INVALID_ARG).
+ * Asynchronous; no workspace. */
 FP8Q_API int attention_fwd(const void* qkv, int64_t T, int64_t seq_len, int n_heads, int n_kv_heads, int head_dim,
                            void* att, float* lse, fp8q_stream stream);
 /* Backward of attention_fwd: the plain gradient of the definition above, with d_att = dO
