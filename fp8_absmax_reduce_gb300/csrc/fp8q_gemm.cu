@@ -970,12 +970,14 @@ cudaError_t launch_wide_t(const CUtensorMap& ta, const CUtensorMap& tb, const CU
 // each N tile in turn, so its A rows are re-read from L2 while B passes once per group.  When all of
 // A fits comfortably in L2 (and is the smaller operand), one group spanning every M unit reads each
 // operand byte from DRAM once; when B does instead, groups of one M unit walk N fastest and keep B
-// resident; otherwise groups of kGroupRows rows bound A's share of L2.  "Comfortably": half the
-// L2 or less, leaving room for the streamed operand's tiles in flight and the output.
-int raster_group(int64_t a_bytes, int64_t b_bytes, int m_units, int unit_rows) {
+// resident; otherwise groups of kGroupRows rows bound A's share of L2.  "Comfortably": 48 MB or
+// less (a 96 MB A measured slower: the streamed B and the output evict it), and no epilogue
+// side input as large as the output streaming through L2 beside it (the SwiGLU backward reads H,
+// 2 x 2 bytes per output element: with a resident 29 MB A its DRAM reads grew by 92 MB per launch).
+int raster_group(int64_t a_bytes, int64_t b_bytes, int m_units, int unit_rows, bool side_stream) {
   constexpr int64_t kResident = 48ll << 20;
-  if (a_bytes <= b_bytes && a_bytes <= kResident) return m_units;
-  if (b_bytes < a_bytes && b_bytes <= kResident) return 1;
+  if (!side_stream && a_bytes <= b_bytes && a_bytes <= kResident) return m_units;
+  if (!side_stream && b_bytes < a_bytes && b_bytes <= kResident) return 1;
   const int g = kGroupRows / unit_rows;
   return g < 1 ? 1 : g;
 }
@@ -1062,7 +1064,7 @@ cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L) {
   }
   const int64_t es_bytes = g.op16 ? 2 : 1;
   a.group = raster_group((int64_t)g.M * g.K * es_bytes, (int64_t)g.b_cols * g.K * es_bytes, a.m_units,
-                         wide ? 256 : (clusters > 0 ? 2 * BM : BM));
+                         wide ? 256 : (clusters > 0 ? 2 * BM : BM), g.epi == kEpiSwigluBwd);
   *P = grid;
   cudaError_t e;
   if (wide) {
