@@ -33,7 +33,8 @@
 //                     tiles, and dV += P^T dO, dK += dS^T Q accumulate in TMEM
 //                     (the group's sum stays inside the CTA: deterministic);
 //   k_attn_bwd_dq     one CTA per (128-query tile, query head, sequence): S and
-//                     dP, then dS, then dQ += dS K over the key tiles 0 .. i.
+//                     dP, then dS, then dQ += dS K over the key tiles 0 .. i, with dS
+//                     double-buffered in TMEM as the MMA's A operand.
 // Every mbarrier wait is bounded; on expiry the CTA records FP8Q_STATUS_TIMEOUT,
 // stops issuing work, drains what it issued, frees TMEM and exits.
 #include "fp8q_common.cuh"
@@ -1104,14 +1105,56 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
 }
 
 // dQ shared-memory layout
+// K_j feeds S_j and, a step later, dQ += dS_j K_j, so its stage is held the longest: three K
+// stages let K_{j+3} load while the tensor core works on tiles j+1 and j+2.  V_j feeds only dP_j and
+// its stage is released as soon as that product completes: two V stages.  (With one ring of two
+// K/V stages released by dQ += dS_j K_j, the MMA that follows it, S_{j+2}, waited for the ring's
+// reload on every tile.)
+constexpr int kDqKStages = 3;
 constexpr int kQQ = 0;
 constexpr int kQO = kQQ + kTile;
-constexpr int kQK = kQO + kTile;      // [2] stages
-constexpr int kQV = kQK + 2 * kTile;  // [2] stages
-constexpr int kQDS = kQV + 2 * kTile;
-constexpr int kQBar = kQDS + kTile;
+constexpr int kQK = kQO + kTile;                // [3] stages
+constexpr int kQV = kQK + kDqKStages * kTile;  // [2] stages
+constexpr int kQBar = kQV + 2 * kTile;
 constexpr int kDqSmem = kQBar + 256 + 1024;
 static_assert(kDqSmem <= 232448, "shared memory per CTA");
+
+// dQ TMEM columns: S, dP and the dQ accumulator (128 fp32 columns each), then two dS buffers of
+// 128 x 128 bf16 (64 columns each, two keys per 32-bit column, the lower key in the low half):
+// dQ += dS K takes dS as its A operand straight from TMEM, so the element-wise warps write it with
+// tcgen05.st and no shared-memory tile or proxy fence sits between them and the MMA, and with two
+// buffers dS_j is written while dQ += dS_{j-1} K_{j-1} still reads the other.
+constexpr uint32_t kDqColS = 0, kDqColDP = 128, kDqColDQ = 256, kDqColDS = 384;
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane from registers (no wait).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// D (+)= A B, kind::f16 with A (bf16, K-major: row i in TMEM lane i, K along the columns) in TMEM
+// at a_tmem and B (bf16) described in shared memory.
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D (+)= A B over K = 128: A a 128 x 128 bf16 tile in TMEM (64 columns), B MN-major in shared
+// memory (rows = K, two 64-wide N atoms).  K step kk: A columns 8 kk .. 8 kk + 7, B rows 16 kk ..
+__device__ __forceinline__ void mma_tile_tmn(uint32_t d, uint32_t a_tmem, uint32_t b, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    umma_bf16_ts(d, a_tmem + (uint32_t)(kk * 8), smem_desc_sw128(b + kk * 2048, kAtom, 1024), idesc_bf16_128(1),
+                 (accumulate || kk) ? 1u : 0u);
+}
 
 __global__ void __launch_bounds__(kAttnBwdThreads, 1)
     k_attn_bwd_dq(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmDO,
@@ -1120,15 +1163,17 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQBar);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;
-  uint64_t* s_free = bars + 6;
-  uint64_t* ds_full = bars + 7;
-  uint64_t* ds_free = bars + 8;
-  uint64_t* acc_full = bars + 9;
-  uint64_t* drain = bars + 10;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+  uint64_t* k_full = bars + 1;    // [3]
+  uint64_t* k_empty = bars + 4;   // [3]
+  uint64_t* v_full = bars + 7;    // [2]
+  uint64_t* v_empty = bars + 9;   // [2]
+  uint64_t* s_full = bars + 11;
+  uint64_t* s_free = bars + 12;
+  uint64_t* ds_full = bars + 13;  // [2]
+  uint64_t* ds_free = bars + 15;  // [2]
+  uint64_t* acc_full = bars + 17;
+  uint64_t* drain = bars + 18;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   int rank, h, b;
@@ -1141,11 +1186,11 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) { mbar_init(&kv_full[s], 1); mbar_init(&kv_empty[s], 1); }
+    for (int s = 0; s < kDqKStages; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
+    for (int s = 0; s < 2; ++s) { mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1); }
     mbar_init(s_full, 1);
     mbar_init(s_free, 256);
-    mbar_init(ds_full, 256);
-    mbar_init(ds_free, 1);
+    for (int s = 0; s < 2; ++s) { mbar_init(&ds_full[s], 256); mbar_init(&ds_free[s], 1); }
     mbar_init(acc_full, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -1166,6 +1211,7 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       bool ok = true;
+      // loads in flight, and the parity of their full[] phase: K stages in bits 0..2, V in 3..4
       uint32_t issued = 0, issued_par = 0;
       mbar_arrive_expect_tx(q_full, 2 * kTile);
       tma_load_2d(smem + kQQ, &tmQKV, q_full, h * kDh, t0);
@@ -1174,56 +1220,64 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
       tma_load_2d(smem + kQO + kAtom, &tmDO, q_full, h * kDh + 64, t0);
       const int xk = (p.Hq + g) * kDh, xv = (p.Hq + p.Hkv + g) * kDh;
       for (int j = 0; j < n; ++j) {
-        const int st = j & 1;
-        const uint32_t u = (uint32_t)(j >> 1) & 1u;
-        if (!mbar_wait(&kv_empty[st], u ^ 1u, abort_flag)) { ok = false; break; }
-        uint8_t* sk = smem + kQK + st * kTile;
-        uint8_t* sv = smem + kQV + st * kTile;
         const int y = b * p.S + j * 128;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * kTile);
-        tma_load_2d(sk, &tmQKV, &kv_full[st], xk, y);
-        tma_load_2d(sk + kAtom, &tmQKV, &kv_full[st], xk + 64, y);
-        tma_load_2d(sv, &tmQKV, &kv_full[st], xv, y);
-        tma_load_2d(sv + kAtom, &tmQKV, &kv_full[st], xv + 64, y);
-        issued |= 1u << st;
-        issued_par = (issued_par & ~(1u << st)) | (u << st);
+        const int ks = j % kDqKStages, vs = j & 1;
+        const uint32_t ku = (uint32_t)(j / kDqKStages) & 1u, vu = (uint32_t)(j >> 1) & 1u;
+        if (!mbar_wait(&k_empty[ks], ku ^ 1u, abort_flag)) { ok = false; break; }
+        uint8_t* sk = smem + kQK + ks * kTile;
+        mbar_arrive_expect_tx(&k_full[ks], kTile);
+        tma_load_2d(sk, &tmQKV, &k_full[ks], xk, y);
+        tma_load_2d(sk + kAtom, &tmQKV, &k_full[ks], xk + 64, y);
+        issued |= 1u << ks;
+        issued_par = (issued_par & ~(1u << ks)) | (ku << ks);
+        if (!mbar_wait(&v_empty[vs], vu ^ 1u, abort_flag)) { ok = false; break; }
+        uint8_t* sv = smem + kQV + vs * kTile;
+        mbar_arrive_expect_tx(&v_full[vs], kTile);
+        tma_load_2d(sv, &tmQKV, &v_full[vs], xv, y);
+        tma_load_2d(sv + kAtom, &tmQKV, &v_full[vs], xv + 64, y);
+        issued |= 1u << (3 + vs);
+        issued_par = (issued_par & ~(1u << (3 + vs))) | (vu << (3 + vs));
       }
       if (!ok) {
         atomicOr(p.status, kStatusTimeout);
         *abort_flag = 1;
         int dummy = 0;
         mbar_wait(q_full, 0, &dummy);
+        for (int s = 0; s < kDqKStages; ++s)
+          if (issued & (1u << s)) mbar_wait(&k_full[s], (issued_par >> s) & 1u, &dummy);
         for (int s = 0; s < 2; ++s)
-          if (issued & (1u << s)) mbar_wait(&kv_full[s], (issued_par >> s) & 1u, &dummy);
+          if (issued & (1u << (3 + s))) mbar_wait(&v_full[s], (issued_par >> (3 + s)) & 1u, &dummy);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256;
+      const uint32_t tS = tmem + kDqColS, tdP = tmem + kDqColDP, tdQ = tmem + kDqColDQ;
       // S_j and dP_j are issued as soon as the element-wise warps have taken S_{j-1} and dP_{j-1}
       // into registers, ahead of dQ += dS_{j-1} K_{j-1}: the tensor core works on tile j while the
       // element-wise pass forms dS_{j-1}
       bool ok = mbar_wait(q_full, 0, abort_flag);
       for (int j = 0; j <= n && ok; ++j) {
         if (j < n) {
-          const int st = j & 1;
-          const uint32_t u = (uint32_t)(j >> 1) & 1u, par = (uint32_t)j & 1u;
-          if (!mbar_wait(&kv_full[st], u, abort_flag) || !mbar_wait(s_free, par ^ 1u, abort_flag)) {
+          const int ks = j % kDqKStages, vs = j & 1;
+          const uint32_t ku = (uint32_t)(j / kDqKStages) & 1u, vu = (uint32_t)(j >> 1) & 1u, par = (uint32_t)j & 1u;
+          if (!mbar_wait(&k_full[ks], ku, abort_flag) || !mbar_wait(&v_full[vs], vu, abort_flag) ||
+              !mbar_wait(s_free, par ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          mma_tile_kk(tS, sbase + kQQ, sbase + kQK + st * kTile, false);   // S = Q K^T
-          mma_tile_kk(tdP, sbase + kQO, sbase + kQV + st * kTile, false);  // dP = dO V^T
+          mma_tile_kk(tS, sbase + kQQ, sbase + kQK + ks * kTile, false);   // S = Q K^T
+          mma_tile_kk(tdP, sbase + kQO, sbase + kQV + vs * kTile, false);  // dP = dO V^T
           umma_commit(s_full);
+          umma_commit(&v_empty[vs]);
         }
         if (j > 0) {
-          const int jj = j - 1, st = jj & 1;
-          if (!mbar_wait(ds_full, (uint32_t)jj & 1u, abort_flag)) { ok = false; break; }
+          const int jj = j - 1, ks = jj % kDqKStages, sb = jj & 1;
+          if (!mbar_wait(&ds_full[sb], (uint32_t)(jj >> 1) & 1u, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          mma_tile_kmn(tdQ, sbase + kQDS, sbase + kQK + st * kTile, jj > 0);  // dQ += dS K
-          umma_commit(&kv_empty[st]);
-          umma_commit(ds_free);
+          mma_tile_tmn(tdQ, tmem + kDqColDS + (uint32_t)(sb * 64), sbase + kQK + ks * kTile, jj > 0);  // dQ += dS K
+          umma_commit(&k_empty[ks]);
+          umma_commit(&ds_free[sb]);
         }
       }
       if (ok) umma_commit(acc_full);
@@ -1240,7 +1294,7 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
     const int wg = (warp - 4) >> 2;
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_off, tdP = tmem + 128 + lane_off;
+    const uint32_t tS = tmem + kDqColS + lane_off, tdP = tmem + kDqColDP + lane_off;
     const float lse2 = p.lse2[(int64_t)h * p.T + t0 + r];
     const float dlt = p.delta[(int64_t)h * p.T + t0 + r];
     bool ok = true;
@@ -1259,20 +1313,23 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
       tmem_ld32x2(tS + c1 * 32, tdP + c1 * 32, s1, d1);
       tc_fence_before();
       mbar_arrive(s_free);
-      // the dS tile is rewritten once dQ += dS_{j-1} K_{j-1} has read it
-      if (!warp_wait(ds_free, par ^ 1u, abort_flag)) {
+      // dS buffer j & 1 is rewritten once dQ += dS_{j-2} K_{j-2} has read it
+      const int sb = j & 1;
+      if (!warp_wait(&ds_free[sb], ((uint32_t)(j >> 1) & 1u) ^ 1u, abort_flag)) {
         ok = false;
         break;
       }
+      const uint32_t tdS = tmem + kDqColDS + (uint32_t)(sb * 64) + lane_off;
       uint32_t w[16];
       if (diag) ds_row_chunk<true>(s0, d0, c0, r, p.scale_log2, lse2, dlt, w);
       else ds_row_chunk<false>(s0, d0, c0, r, p.scale_log2, lse2, dlt, w);
-      tile_put32(sbase + kQDS, r, c0, w);
+      tmem_st16(tdS + (uint32_t)(c0 * 16), w);
       if (diag) ds_row_chunk<true>(s1, d1, c1, r, p.scale_log2, lse2, dlt, w);
       else ds_row_chunk<false>(s1, d1, c1, r, p.scale_log2, lse2, dlt, w);
-      tile_put32(sbase + kQDS, r, c1, w);
-      fence_async_shared();
-      mbar_arrive(ds_full);
+      tmem_st16(tdS + (uint32_t)(c1 * 16), w);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&ds_full[sb]);
     }
     if (ok && !warp_wait(acc_full, 0, abort_flag)) ok = false;
     if (!ok) {
@@ -1282,7 +1339,7 @@ __global__ void __launch_bounds__(kAttnBwdThreads, 1)
     // dQ row (scaled by 1/sqrt(128)) out through the Q tile (every MMA has completed)
     if (ok) {
       tc_fence_after();
-      const uint32_t tdQ = tmem + 256 + lane_off;
+      const uint32_t tdQ = tmem + kDqColDQ + lane_off;
 #pragma unroll 1
       for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
         uint32_t qv[32], w[16];
