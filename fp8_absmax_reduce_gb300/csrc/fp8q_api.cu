@@ -40,27 +40,43 @@ struct Trace {
 };
 thread_local Trace t_trace;
 
+}  // namespace
+
+namespace fp8q {
+
+bool trace_step_begin(cudaStream_t s, int kind) {
+  nvtxRangePushA(kKindNames[kind]);
+  Trace& t = t_trace;
+  if (!t.on || t.n >= (int)t.kinds.size()) return false;
+  t.kinds[t.n] = kind;
+  cudaEventRecord(t.ev[2 * t.n], s);
+  return true;
+}
+
+void trace_step_end(cudaStream_t s, bool active) {
+  if (active) {
+    cudaEventRecord(t_trace.ev[2 * t_trace.n + 1], s);
+    ++t_trace.n;
+  }
+  nvtxRangePop();
+}
+
+void set_last_launch_count(int n) { t_last_launches = n; }
+
+}  // namespace fp8q
+
+namespace {
+
+static_assert((int)kKAbsmaxPartial == (int)kTraceAbsmaxPartial && (int)kKQuantCast == (int)kTraceQuantCast,
+              "trace kinds");
+
 // One kernel step: an NVTX range named for the kernel kind (seen by profilers, free otherwise)
 // and, while the trace is on, a pair of CUDA events around its launches.
 struct TraceScope {
   cudaStream_t s;
   bool active;
-  TraceScope(cudaStream_t st, int kind) : s(st), active(false) {
-    nvtxRangePushA(kKindNames[kind]);
-    Trace& t = t_trace;
-    if (t.on && t.n < (int)t.kinds.size()) {
-      active = true;
-      t.kinds[t.n] = kind;
-      cudaEventRecord(t.ev[2 * t.n], s);
-    }
-  }
-  ~TraceScope() {
-    if (active) {
-      cudaEventRecord(t_trace.ev[2 * t_trace.n + 1], s);
-      ++t_trace.n;
-    }
-    nvtxRangePop();
-  }
+  TraceScope(cudaStream_t st, int kind) : s(st), active(trace_step_begin(st, kind)) {}
+  ~TraceScope() { trace_step_end(s, active); }
 };
 
 struct DevInfo {

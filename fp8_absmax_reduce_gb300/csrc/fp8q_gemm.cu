@@ -55,7 +55,7 @@ constexpr int kGroupRows = 2048;                     // rows of A per rasterisat
 struct Args {
   int M, N, K;
   int m_tiles, n_tiles, k_blocks;
-  int m_units, num_tiles;  // scheduling units: M tiles (one CTA) or M-tile pairs (a 2-CTA cluster); units x n_tiles
+  int m_units, num_tiles;  // scheduling units: M tiles; num_tiles = m_units x n_tiles
   int group;               // M units per rasterisation group
   int b_step, b_half1;  // B's N coordinate of a tile = nb * b_step (+ b_half1 for the second half)
   int epi, out_f32;
@@ -208,20 +208,11 @@ __device__ __forceinline__ void load_h_chunk(const Args& p, int row, int col, in
 // ---------------------------------------------------------------------------
 // Output maps: tmC (C, or the gate half of H / dH), tmC2 (the up half), tmAux
 // (the SwiGLU output a); unused ones are copies of tmC.
-// CL = 2: the kernel runs as clusters of two CTAs on vertically adjacent tiles
-// (M tiles 2u and 2u + 1, the same N tile), which need the same B tile: CTA r
-// loads B half r once from L2 and TMA-multicasts it into both CTAs' shared
-// memory, so a stage costs the L2 32 KB per CTA instead of 48 KB (the 128 x 256
-// mainloop is bound by the GPU-wide operand traffic out of L2 when all SMs run
-// it).  Each stage slot is then written by both CTAs, so a slot is free once
-// both CTAs' MMAs have read it: each MMA commit arrives on the empty barrier of
-// both CTAs (count 2).  Everything else (accumulators, epilogue) is per CTA.
-template <int A_MN, int B_MN, int OP16, int CL>
+template <int A_MN, int B_MN, int OP16>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_f8(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
               const __grid_constant__ CUtensorMap tmAux, const Args p) {
-  static_assert(CL == 1 || (CL == 2 && !OP16), "clusters: FP8 operands only (one box per B half)");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOffset);
@@ -234,12 +225,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* cta_amax = reinterpret_cast<uint32_t*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int crank = CL == 2 ? (int)cluster_ctarank() : 0;
-  // this CTA's scheduling units: u = first, first + step, ...; M tile = u * CL + crank
-  const int u_first = CL == 2 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int u_step = CL == 2 ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  // this CTA's tiles: first, first + step, ...
+  const int u_first = (int)blockIdx.x;
+  const int u_step = (int)gridDim.x;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], CL); }
+    for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], kEpiThreads); }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -255,7 +245,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (CL == 2) cluster_sync_all();  // the peer's barriers are initialised before any multicast reaches them
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
@@ -269,14 +258,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = u_first; tile < p.num_tiles && ok; tile += u_step) {
         int mb, nb;
         tile_coords(tile, p, mb, nb);
-        const int m0 = (mb * CL + crank) * BM;
+        const int m0 = mb * BM;
         const int n0 = nb * p.b_step, n1 = n0 + p.b_half1;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
           uint8_t* sA = smem + stage * kStage;
           uint8_t* sB = sA + kATile;
-          // the whole stage lands here: this CTA's A tile and both B halves (one of them
-          // multicast by the peer when CL = 2)
+          // the whole stage lands here: the A tile and both B halves
           mbar_arrive_expect_tx(&full[stage], kStage);
           const int k0 = kb * (OP16 ? BK / 2 : BK);  // in elements
           if (A_MN) {
@@ -289,13 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             tma_load_2d(sA, &tmA, &full[stage], k0, m0);
           }
-          if (CL == 2) {
-            // B half `crank` into both CTAs
-            uint8_t* dst = sB + crank * kBHalf;
-            const int nh = crank ? n1 : n0;
-            if (B_MN) tma_load_2d_mc(dst, &tmB, &full[stage], nh, k0, 0x3);
-            else tma_load_2d_mc(dst, &tmB, &full[stage], k0, nh, 0x3);
-          } else if (B_MN) {
+          if (B_MN) {
             if (OP16) {
               tma_load_2d(sB, &tmB, &full[stage], n0, k0);
               tma_load_2d(sB + kBHalf / 2, &tmB, &full[stage], n0 + 64, k0);
@@ -354,8 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (OP16) umma_bf16(d_tmem, ad, bd, p.idesc, (kb | kk) != 0 ? 1u : 0u);
             else umma_f8(d_tmem, ad, bd, p.idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          if (CL == 2) umma_commit_mc(&empty[stage], 0x3);  // the slot holds data both CTAs wrote
-          else umma_commit(&empty[stage]);
+          umma_commit(&empty[stage]);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -383,7 +364,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = u_first; tile < p.num_tiles; tile += u_step) {
       int mb, nb;
       tile_coords(tile, p, mb, nb);
-      mb = mb * CL + crank;
       const int row0 = mb * BM + sub * 32;
       const int row = row0 + lane;
       const bool row_ok = row < p.M;
@@ -560,7 +540,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (threadIdx.x == 0 && p.amax_partial) p.amax_partial[blockIdx.x] = *cta_amax;
-  if (CL == 2) cluster_sync_all();  // the peer's multicasts and commit arrivals into this CTA are done
   if (warp == 2) tmem_dealloc(tmem_base, kTmemCols);
 }
 
@@ -883,13 +862,13 @@ uint32_t make_idesc(int fmtA, int fmtB, int a_mn, int b_mn) {
          ((uint32_t)b_mn << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
 
-template <int A_MN, int B_MN, int OP16, int CL>
+template <int A_MN, int B_MN, int OP16>
 cudaError_t configure_t() {
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_f8<A_MN, B_MN, OP16, CL>,
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_f8<A_MN, B_MN, OP16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
@@ -897,57 +876,13 @@ cudaError_t configure_t() {
   return cudaSuccess;
 }
 
-// A launch configuration of k_gemm_f8 as clusters of two CTAs.
-struct PairLaunch {
-  cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute attr[1];
-  PairLaunch(int grid, cudaStream_t s) {
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = s;
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  }
-};
-
-template <int A_MN, int B_MN, int OP16, int CL>
+template <int A_MN, int B_MN, int OP16>
 cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tc2,
                      const CUtensorMap& taux, const Args& a, int grid, cudaStream_t s) {
-  cudaError_t e = configure_t<A_MN, B_MN, OP16, CL>();
+  cudaError_t e = configure_t<A_MN, B_MN, OP16>();
   if (e != cudaSuccess) return e;
-  if (CL == 2) {
-    PairLaunch pl(grid, s);
-    return cudaLaunchKernelEx(&pl.cfg, k_gemm_f8<A_MN, B_MN, OP16, CL>, ta, tb, tc, tc2, taux, a);
-  }
-  k_gemm_f8<A_MN, B_MN, OP16, CL><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, tc, tc2, taux, a);
+  k_gemm_f8<A_MN, B_MN, OP16><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, tc, tc2, taux, a);
   return cudaGetLastError();
-}
-
-// How many two-CTA clusters of the FP8 128 x 256 kernel fit on the GPU at once (0: none, or the
-// query failed -- the single-CTA kernel is used then).
-template <int A_MN, int B_MN>
-int pair_clusters(int num_sms) {
-  static int cached_device = -1, cached = 0;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (cached_device != dev) {
-    int n = 0;
-    if (configure_t<A_MN, B_MN, 0, 2>() != cudaSuccess) {
-      n = 0;
-    } else {
-      PairLaunch pl(num_sms & ~1, nullptr);
-      if (cudaOccupancyMaxActiveClusters(&n, (const void*)k_gemm_f8<A_MN, B_MN, 0, 2>, &pl.cfg) != cudaSuccess) n = 0;
-    }
-    cudaGetLastError();  // a failed query leaves no sticky error
-    cached = n;
-    cached_device = dev;
-  }
-  return cached;
 }
 
 template <int A_MN, int B_MN>
@@ -1044,27 +979,11 @@ cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L) {
     a.num_tiles = a.m_tiles * a.n_tiles;
   }
   a.m_units = a.m_tiles;
-  // FP8 128 x 256 tiles: two-CTA clusters sharing the B tile by multicast when the M tiles pair
-  // up exactly (an even count; every block GEMM's M -- tokens, d, f -- is a multiple of 256)
-  int clusters = 0;
-  if (!wide && !g.op16 && a.m_tiles % 2 == 0) {
-    if (g.a_mn == 0 && g.b_mn == 1) clusters = pair_clusters<0, 1>(L.num_sms);
-    else if (g.a_mn == 0 && g.b_mn == 0) clusters = pair_clusters<0, 0>(L.num_sms);
-    else if (g.a_mn == 1 && g.b_mn == 1) clusters = pair_clusters<1, 1>(L.num_sms);
-    else clusters = pair_clusters<1, 0>(L.num_sms);
-  }
-  int grid;
-  if (clusters > 0) {
-    a.m_units = (a.m_tiles + 1) / 2;
-    a.num_tiles = a.m_units * a.n_tiles;
-    grid = 2 * (a.num_tiles < clusters ? a.num_tiles : clusters);
-  } else {
-    a.num_tiles = a.m_units * a.n_tiles;
-    grid = a.num_tiles < L.num_sms ? a.num_tiles : L.num_sms;
-  }
+  a.num_tiles = a.m_units * a.n_tiles;
+  const int grid = a.num_tiles < L.num_sms ? a.num_tiles : L.num_sms;
   const int64_t es_bytes = g.op16 ? 2 : 1;
   a.group = raster_group((int64_t)g.M * g.K * es_bytes, (int64_t)g.b_cols * g.K * es_bytes, a.m_units,
-                         wide ? 256 : (clusters > 0 ? 2 * BM : BM), g.epi == kEpiSwigluBwd);
+                         wide ? 256 : BM, g.epi == kEpiSwigluBwd);
   *P = grid;
   cudaError_t e;
   if (wide) {
@@ -1076,20 +995,15 @@ cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L) {
     return e;
   }
   if (g.op16) {  // the three layouts of the block (NN, NT, TN)
-    if (g.a_mn == 0 && g.b_mn == 1) e = launch_t<0, 1, 1, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
-    else if (g.a_mn == 0 && g.b_mn == 0) e = launch_t<0, 0, 1, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
-    else if (g.a_mn == 1 && g.b_mn == 1) e = launch_t<1, 1, 1, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
+    if (g.a_mn == 0 && g.b_mn == 1) e = launch_t<0, 1, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
+    else if (g.a_mn == 0 && g.b_mn == 0) e = launch_t<0, 0, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
+    else if (g.a_mn == 1 && g.b_mn == 1) e = launch_t<1, 1, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
     else return cudaErrorInvalidValue;
-  } else if (clusters > 0) {
-    if (g.a_mn == 0 && g.b_mn == 1) e = launch_t<0, 1, 0, 2>(ta, tb, tc, tc2, taux, a, grid, L.stream);
-    else if (g.a_mn == 0 && g.b_mn == 0) e = launch_t<0, 0, 0, 2>(ta, tb, tc, tc2, taux, a, grid, L.stream);
-    else if (g.a_mn == 1 && g.b_mn == 1) e = launch_t<1, 1, 0, 2>(ta, tb, tc, tc2, taux, a, grid, L.stream);
-    else e = launch_t<1, 0, 0, 2>(ta, tb, tc, tc2, taux, a, grid, L.stream);
   } else {
-    if (g.a_mn == 0 && g.b_mn == 1) e = launch_t<0, 1, 0, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
-    else if (g.a_mn == 0 && g.b_mn == 0) e = launch_t<0, 0, 0, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
-    else if (g.a_mn == 1 && g.b_mn == 1) e = launch_t<1, 1, 0, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
-    else e = launch_t<1, 0, 0, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
+    if (g.a_mn == 0 && g.b_mn == 1) e = launch_t<0, 1, 0>(ta, tb, tc, tc2, taux, a, grid, L.stream);
+    else if (g.a_mn == 0 && g.b_mn == 0) e = launch_t<0, 0, 0>(ta, tb, tc, tc2, taux, a, grid, L.stream);
+    else if (g.a_mn == 1 && g.b_mn == 1) e = launch_t<1, 1, 0>(ta, tb, tc, tc2, taux, a, grid, L.stream);
+    else e = launch_t<1, 0, 0>(ta, tb, tc, tc2, taux, a, grid, L.stream);
   }
   if (L.launches) ++*L.launches;
   return e;

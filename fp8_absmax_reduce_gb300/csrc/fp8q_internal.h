@@ -25,6 +25,9 @@ struct Launch {
 int device_status_and_sms(unsigned** status, int* num_sms);
 
 // Per-tensor absmax quantization: pass 1 writes *P partials, pass 2 casts.
+// absmax_partial_blocks: the number of partials pass 1 writes for n elements (its grid size;
+// never more than kMaxPartials).
+int absmax_partial_blocks(int dtype, int64_t n);
 cudaError_t launch_absmax_partial(const void* x, int dtype, int64_t n, uint32_t* partial, int* P,
                                   const Launch& L);
 cudaError_t launch_quant_cast(const void* x, int dtype, int64_t n, int fmt, const uint32_t* partial, int P,
@@ -64,6 +67,14 @@ cudaError_t launch_attn_bwd_dq(const uint16_t* qkv, const uint16_t* datt, int64_
 
 // Diagnostics: a bounded wait that is made to run out (see fp8q_selftest_bounded_wait).
 cudaError_t launch_selftest_bounded_wait(uint64_t limit_ns, const Launch& L);
+
+// Bookkeeping of the C ABI for entry points implemented outside fp8q_api.cu: the trace bracket
+// of one kernel step (an NVTX range, and CUDA events while the kernel trace is on) and the count
+// that fp8q_last_launch_count() reports.
+enum TraceKind { kTraceAbsmaxPartial = 0, kTraceQuantCast = 1 };
+bool trace_step_begin(cudaStream_t s, int kind);  // returns whether events were recorded
+void trace_step_end(cudaStream_t s, bool active);
+void set_last_launch_count(int n);
 
 // ---------------------------------------------------------------------------
 // GEMM

@@ -3,10 +3,10 @@
 //
 // The regular fp8_quantize_absmax asks its caller for a small workspace (the
 // per-block absmax partials of the first pass).  Some callers have no way to
-// provide one: code running while a CUDA graph is being captured (cudaMalloc
-// is not allowed during capture), code inside a framework that owns every
-// device allocation through its own pool, and latency-critical loops that
-// must not call cudaMalloc/cudaFree because those synchronize the device.
+// provide one: code inside a framework that owns every device allocation
+// through its own pool and hands out none to plug-ins, and latency-critical
+// loops that must not call cudaMalloc/cudaFree because those synchronize the
+// device and can stall every stream.
 // This entry point keeps its scratch in a fixed array that lives in the
 // library's own device memory, so the caller passes only the input and the
 // outputs.
@@ -62,14 +62,6 @@ int noalloc_device(NoallocDevice* out) {
   return FP8Q_OK;
 }
 
-// Number of partials the first pass writes for n elements (the rule of its launcher,
-// which also caps it at kMaxPartials).
-int64_t partials_needed(fp8q_dtype dtype, int64_t n) {
-  const int64_t nvec = dtype == FP8Q_BF16 ? n / 8 : n / 4;
-  int64_t blocks = ((nvec / 4 > 0 ? nvec / 4 : 1) + 255) / 256;
-  return blocks < kMaxPartials ? blocks : kMaxPartials;
-}
-
 }  // namespace
 
 extern "C" {
@@ -80,7 +72,8 @@ int fp8_quantize_absmax_noalloc(const void* x, fp8q_dtype x_dtype, int64_t n, fp
     return FP8Q_ERR_INVALID_ARG;
   if ((x_dtype != FP8Q_BF16 && x_dtype != FP8Q_F32) || (fmt != FP8Q_E4M3 && fmt != FP8Q_E5M2))
     return FP8Q_ERR_INVALID_ARG;
-  if (partials_needed(x_dtype, n) > kNoallocPartials) return FP8Q_ERR_INVALID_ARG;
+  // the first pass's own grid size (one partial per block) must fit the array
+  if (absmax_partial_blocks((int)x_dtype, n) > kNoallocPartials) return FP8Q_ERR_INVALID_ARG;
   NoallocDevice d;
   int e = noalloc_device(&d);
   if (e) return e;
@@ -93,9 +86,15 @@ int fp8_quantize_absmax_noalloc(const void* x, fp8q_dtype x_dtype, int64_t n, fp
   // The first pass overwrites partials [0, P) before the second pass reads
   // exactly those, so nothing left from an earlier call needs clearing.
   int P = 0;
-  if (launch_absmax_partial(x, (int)x_dtype, n, d.partials, &P, L) != cudaSuccess) return FP8Q_ERR_CUDA;
-  if (launch_quant_cast(x, (int)x_dtype, n, (int)fmt, d.partials, P, q, scal, L) != cudaSuccess)
-    return FP8Q_ERR_CUDA;
+  bool traced = trace_step_begin(L.stream, kTraceAbsmaxPartial);
+  cudaError_t e1 = launch_absmax_partial(x, (int)x_dtype, n, d.partials, &P, L);
+  trace_step_end(L.stream, traced);
+  if (e1 != cudaSuccess) return FP8Q_ERR_CUDA;
+  traced = trace_step_begin(L.stream, kTraceQuantCast);
+  cudaError_t e2 = launch_quant_cast(x, (int)x_dtype, n, (int)fmt, d.partials, P, q, scal, L);
+  trace_step_end(L.stream, traced);
+  if (e2 != cudaSuccess) return FP8Q_ERR_CUDA;
+  set_last_launch_count(launches);
   return FP8Q_OK;
 }
 

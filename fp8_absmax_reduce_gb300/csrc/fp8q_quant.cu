@@ -679,10 +679,14 @@ cudaError_t launch_selftest_bounded_wait(uint64_t limit_ns, const Launch& L) {
 // ---------------------------------------------------------------------------
 // Launchers
 // ---------------------------------------------------------------------------
+int absmax_partial_blocks(int dtype, int64_t n) {
+  const int64_t nvec = dtype == 0 ? n / 8 : n / 4;
+  return grid_for(nvec / 4 > 0 ? nvec / 4 : 1, kMaxPartials);
+}
+
 cudaError_t launch_absmax_partial(const void* x, int dtype, int64_t n, uint32_t* partial, int* P,
                                   const Launch& L) {
-  const int64_t nvec = dtype == 0 ? n / 8 : n / 4;
-  const int grid = grid_for(nvec / 4 > 0 ? nvec / 4 : 1, kMaxPartials);
+  const int grid = absmax_partial_blocks(dtype, n);
   *P = grid;
   if (dtype == 0)
     k_absmax_partial<0><<<grid, kThreads, 0, L.stream>>>((const uint8_t*)x, n, partial);

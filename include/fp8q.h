@@ -91,11 +91,11 @@ FP8Q_API int fp8_quantize_absmax(const void* x, fp8q_dtype x_dtype, int64_t n, f
                         float* scal, void* ws, size_t ws_bytes, fp8q_stream stream);
 
 /* The same quantization for callers that cannot allocate device memory, so
- * cannot provide the workspace above: code running while a CUDA graph is
- * being captured (cudaMalloc is not allowed then), code inside a framework
- * that owns every allocation through its own pool, and latency-critical loops
- * that must avoid cudaMalloc/cudaFree because they synchronize the device.
- * The pages have no counterpart; this is an interface convenience.
+ * cannot provide the workspace above: code inside a framework that owns every
+ * allocation through its own pool and gives none to plug-ins, and
+ * latency-critical loops that must avoid cudaMalloc/cudaFree because those
+ * synchronize the device.  The paper has no counterpart; this is an interface
+ * convenience.
  *
  * The scratch (1024 absmax partials, 4 KiB) is a fixed array in the library's
  * own device memory: one copy per GPU that loads the library, held until the

@@ -77,3 +77,18 @@ def test_attention_flops_closed_form():
     pairs = 2 * (4 * 5 // 2)  # two sequences of 4 tokens
     assert w.attention_flops() == pairs * 2 * 256 * 7
     assert dataclasses.replace(w, dy_std=0.0).attention_flops() == pairs * 2 * 256 * 2
+
+
+def test_peak_follows_the_run():
+    """A short timed region, or one held at the maximum clock, is held to the burst peak; a long
+    one that settled lower to the sustained peak; FP8 peaks are twice the bf16 ones."""
+    import bench
+    pk = {"bf16": 1900.0, "bf16_sustained": 1700.0, "source": "measured"}
+    short = bench.choose_peak(pk, 300.0, {"sm_mhz": 1500.0, "sm_max_mhz": 2070.0})
+    assert short["kind"] == "burst" and short["peak"] == 3800.0 and short["fp8_peak"] == 3800.0
+    at_max = bench.choose_peak(pk, 5000.0, {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0})
+    assert at_max["kind"] == "burst"
+    capped = bench.choose_peak(pk, 5000.0, {"sm_mhz": 1700.0, "sm_max_mhz": 2070.0})
+    assert capped["kind"] == "sustained" and capped["peak"] == 3400.0
+    assert bench.choose_peak(pk, 5000.0, {"sm_mhz": 1700.0, "sm_max_mhz": 2070.0}, bf16=True)["peak"] == 1700.0
+    assert bench.choose_peak(pk, 5000.0, None)["kind"] == "sustained"

@@ -92,10 +92,10 @@ def test_gemm_long_k_wide_tiles(layout, M, N, K, out, residual):
 
 @pytest.mark.parametrize("layout", [fq.NN, fq.NT, fq.TN])
 @pytest.mark.parametrize("M,N,K", [(912, 528, 512), (2048, 256, 384)])
-def test_gemm_cluster_pairs(layout, M, N, K):
-    """An even number of 128-row tiles (8 and 16 here, the first with a 16-row last tile) runs as
-    two-CTA clusters that share each B tile by multicast: every tile of a pair must match the
-    oracle, and repeated launches must agree bit for bit."""
+def test_gemm_many_m_tiles(layout, M, N, K):
+    """8 and 16 row tiles of 128 (the first with a 16-row last tile), more tiles than one
+    rasterisation group walks at once: every tile must match the oracle, and repeated launches
+    must agree bit for bit."""
     got, ref = run_case(layout, M, N, K, 0, 1 if layout == fq.TN else 0, "f32", False, seed=M + N + K + layout)
     assert row_rel(got, ref) < 2e-3
     got2, _ = run_case(layout, M, N, K, 0, 1 if layout == fq.TN else 0, "f32", False, seed=M + N + K + layout)
@@ -104,8 +104,7 @@ def test_gemm_cluster_pairs(layout, M, N, K):
 
 @pytest.mark.parametrize("layout", [fq.NN, fq.NT, fq.TN])
 @pytest.mark.parametrize("fa,fb", [(0, 0), (1, 0), (0, 1)])
-def test_gemm_cluster_formats(layout, fa, fb):
-    """The two-CTA cluster path (4 M tiles, the last ragged) with every E4M3/E5M2 operand mix and
-    bf16 output."""
+def test_gemm_formats_bf16_out(layout, fa, fb):
+    """Four row tiles (the last ragged) with every E4M3/E5M2 operand mix and bf16 output."""
     got, ref = run_case(layout, 400, 528, 272, fa, fb, "bf16", False, seed=7 * layout + 3 * fa + fb)
     assert row_rel(got, ref) < 2e-3

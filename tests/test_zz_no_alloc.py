@@ -1,12 +1,12 @@
 """fp8_quantize_absmax_noalloc: the quantizer for callers that cannot allocate device memory.
 
-Callers such as code running during CUDA-graph capture (where cudaMalloc is not allowed), code
-whose framework owns every device allocation, or latency-critical loops that must not trigger
-the device synchronisation of cudaMalloc/cudaFree cannot hand the regular entry point its
-workspace.  The no-allocation variant keeps that scratch in a fixed array inside the library.
+Callers such as code whose framework owns every device allocation and gives none to plug-ins,
+or latency-critical loops that must not trigger the device synchronisation of cudaMalloc/cudaFree,
+cannot hand the regular entry point its workspace.  The no-allocation variant keeps that scratch in a fixed array inside the library.
 This test calls it through the C ABI and requires the same bits as the regular entry point
-(whose tests require bit-exactness against the CPU oracle), on two calls in a row: a large
-tensor, then a small one that reads fewer partials than the first call left in the shared array.
+(whose tests require bit-exactness against the CPU oracle), on calls in a row: a large
+tensor, then smaller ones that read fewer partials than the earlier call left in the shared array
+(the last, 16 elements, a single partial).
 It is collected last so that a run stopping at the first failure has run everything else.
 """
 
@@ -42,7 +42,7 @@ def test_noalloc_matches_workspace_entry_point(dtype, fmt):
     L = c_lib()
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     dcode = 0 if dtype == torch.bfloat16 else 1
-    for seed, n in ((1, 3 * (1 << 20) + 5), (2, 40_001)):
+    for seed, n in ((1, 3 * (1 << 20) + 5), (2, 40_001), (3, 16)):
         x = device_input(n, dtype, seed + 10 * fmt)
         q_ref = torch.empty(n, dtype=torch.uint8, device="cuda")
         s_ref = torch.empty(3, dtype=torch.float32, device="cuda")
@@ -57,6 +57,7 @@ def test_noalloc_matches_workspace_entry_point(dtype, fmt):
         rc = L.fp8_quantize_absmax_noalloc(ctypes.c_void_p(x.data_ptr()), dcode, n, fmt,
                                            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(s.data_ptr()), stream)
         assert rc == 0
+        assert L.fp8q_last_launch_count() == 2  # the absmax pass and the cast pass
         torch.cuda.synchronize()
         assert torch.equal(s, s_ref)
         assert torch.equal(q, q_ref)
