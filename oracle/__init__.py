@@ -72,7 +72,14 @@ class _BlockIO(ctypes.Structure):
         ("dg", ctypes.c_void_p), ("dN", ctypes.c_void_p), ("dH", ctypes.c_void_p),
         ("dY8", ctypes.c_void_p), ("dH8", ctypes.c_void_p), ("scal_bwd", ctypes.c_void_p),
         ("bf16", ctypes.c_int), ("n16", ctypes.c_void_p), ("a16", ctypes.c_void_p),
+        ("mx", ctypes.c_int), ("mxq", ctypes.c_void_p * 12), ("mxs", ctypes.c_void_p * 12),
     ]
+
+
+# MX operand slots of the block (the oracle's MxSlot): tensor, then the direction of its blocks --
+# "_r" 32 consecutive columns of a row, "_c" 32 consecutive rows of a column.
+MX_SLOTS = ("Wgu_r", "Wgu_c", "Wd_r", "Wd_c", "n_r", "n_c", "a_r", "a_c", "dY_r", "dY_c", "dH_r", "dH_c")
+MX_BLOCK = 32
 
 
 class _FullIO(ctypes.Structure):
@@ -127,6 +134,9 @@ def lib() -> ctypes.CDLL:
             L.fo_block_forward.argtypes = [ctypes.POINTER(_BlockIO)]
             L.fo_block_forward_backward.argtypes = [ctypes.POINTER(_BlockIO)]
             L.fo_full_block.argtypes = [ctypes.POINTER(_FullIO), ctypes.c_int]
+            L.fo_mx_quantize.argtypes = [vp, ctypes.c_int, i64, i64, ctypes.c_int, ctypes.c_int, vp, vp]
+            L.fo_gemm_mx.argtypes = [ctypes.c_int, i64, i64, i64, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, vp,
+                                     ctypes.c_int, vp, ctypes.c_int]
             L.fo_attention.argtypes = [ctypes.POINTER(_AttnIO), ctypes.c_int]
             _lib = L
     return _lib
@@ -252,6 +262,62 @@ def gemm_scaled(layout: int, A: np.ndarray, fmtA: int, B: np.ndarray, fmtB: int,
     return C
 
 
+def mx_quantize(x: np.ndarray, fmt: int, along_rows: bool):
+    """Block-scaled (MXFP8) quantization of a 2-D tensor (bf16 bits as uint16, or float32).
+
+    along_rows=False: blocks of 32 consecutive columns of a row (the contraction runs along the
+    columns); scale codes [R, ceil(C/32)].  along_rows=True: blocks of 32 consecutive rows of a
+    column; scale codes [ceil(R/32), C].  Scale code = X + 127 (E8M0), X the smallest integer with
+    amax_block <= fmax 2^X; element code = fp8(fl32(v 2^-X)).  Returns (codes, scale codes, status).
+    """
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.uint16:
+        dtype = 0
+    elif x.dtype == np.float32:
+        dtype = 1
+    else:
+        raise TypeError("mx_quantize takes bf16 bits (uint16) or float32")
+    R, C = x.shape
+    q = np.empty((R, C), dtype=np.uint8)
+    sf = np.empty(((R + MX_BLOCK - 1) // MX_BLOCK, C) if along_rows else (R, (C + MX_BLOCK - 1) // MX_BLOCK),
+                  dtype=np.uint8)
+    st = lib().fo_mx_quantize(_c(x), dtype, R, C, fmt, int(along_rows), _c(q), _c(sf))
+    return q, sf, st
+
+
+def gemm_mx(layout: int, A: np.ndarray, fmtA: int, sfA: np.ndarray, B: np.ndarray, fmtB: int, sfB: np.ndarray,
+            out: str = "f32", residual=None, nthreads: int = 1):
+    """Block-scaled GEMM C = op(A) op(B) [+ residual] in fp64 (layouts as gemm_scaled).
+
+    sfA [M, ceil(K/32)] holds the scale code of row m's K-block, sfB [N, ceil(K/32)] that of column
+    n's, whatever the storage layout of A and B; an element is worth decode(code) 2^(sf - 127).
+    """
+    A = np.ascontiguousarray(A, dtype=np.uint8)
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    if layout == TN:
+        K, M = A.shape
+    else:
+        M, K = A.shape
+    N = B.shape[0] if layout == NT else B.shape[1]
+    if (B.shape[1] if layout == NT else B.shape[0]) != K:
+        raise ValueError("inner dimensions differ")
+    KB = (K + MX_BLOCK - 1) // MX_BLOCK
+    sfA = np.ascontiguousarray(sfA, dtype=np.uint8)
+    sfB = np.ascontiguousarray(sfB, dtype=np.uint8)
+    if sfA.shape != (M, KB) or sfB.shape != (N, KB):
+        raise ValueError("scale shapes: sfA [M, K/32], sfB [N, K/32]")
+    code = {"bf16": 0, "f32": 1, "f64": 2}[out]
+    C = np.empty((M, N), dtype={0: np.uint16, 1: np.float32, 2: np.float64}[code])
+    res = None
+    if residual is not None:
+        if code != 0:
+            raise ValueError("residual needs bf16 output")
+        res = np.ascontiguousarray(residual, dtype=np.uint16)
+    lib().fo_gemm_mx(layout, M, N, K, _c(A), fmtA, _c(sfA), _c(B), fmtB, _c(sfB),
+                     None if res is None else _c(res), code, _c(C), nthreads)
+    return C
+
+
 # ----------------------------------------------------------------------------
 # The MLP block
 # ----------------------------------------------------------------------------
@@ -262,7 +328,7 @@ def _as_f64(a, exact):
 
 
 def block(x, g, Wgu, Wd, dY=None, eps: float = 1e-6, exact: bool = False, nthreads: int = 1,
-          grad_fmt: int = E5M2, bf16: bool = False):
+          grad_fmt: int = E5M2, bf16: bool = False, mx: bool = False):
     """MLP block forward (and backward when dY is given).
 
     Quantized mode (exact=False): x, g, Wgu, Wd, dY are bf16 bit patterns
@@ -276,9 +342,16 @@ def block(x, g, Wgu, Wd, dY=None, eps: float = 1e-6, exact: bool = False, nthrea
     BF16 baseline (bf16=True, bf16 inputs): no quantization; n and a are stored
     as bf16 (returned as "n16", "a16") and every GEMM multiplies the bf16
     operands unscaled; the storage points are those of the FP8 block.
+
+    Block-scaled MXFP8 (mx=True, bf16 inputs): every GEMM operand is quantized in blocks of 32
+    along that GEMM's contraction dimension (mx_quantize), no per-tensor scales; the results hold
+    "mx_<slot>" (codes) and "mx_<slot>_sf" (E8M0 scale codes) for every slot of MX_SLOTS (the
+    backward's dY / dH slots only with dY).
     """
-    if bf16 and exact:
-        raise ValueError("bf16 and exact are separate modes")
+    if (bf16 or mx) and exact:
+        raise ValueError("bf16, mx and exact are separate modes")
+    if bf16 and mx:
+        raise ValueError("bf16 and mx are separate modes")
     x64, g64, Wgu64, Wd64 = (_as_f64(a, exact) for a in (x, g, Wgu, Wd))
     T, d = x64.shape
     f = Wd64.shape[0]
@@ -291,8 +364,20 @@ def block(x, g, Wgu, Wd, dY=None, eps: float = 1e-6, exact: bool = False, nthrea
         "scal_fwd": np.zeros((4, 3), np.float32),
     }
     io = _BlockIO(T=T, d=d, f=f, eps=eps, exact=int(exact), nthreads=int(nthreads), grad_fmt=int(grad_fmt),
-                  bf16=int(bf16))
+                  bf16=int(bf16), mx=int(mx))
     keep = [x64, g64, Wgu64, Wd64]
+    if mx:
+        shapes = {"Wgu": (d, 2 * f), "Wd": (f, d), "n": (T, d), "a": (T, f), "dY": (T, d), "dH": (T, 2 * f)}
+        for i, slot in enumerate(MX_SLOTS):
+            name, axis = slot.rsplit("_", 1)
+            if name in ("dY", "dH") and dY is None:
+                continue
+            R, C = shapes[name]
+            sfs = ((R + MX_BLOCK - 1) // MX_BLOCK, C) if axis == "c" else (R, (C + MX_BLOCK - 1) // MX_BLOCK)
+            out["mx_" + slot] = np.empty((R, C), np.uint8)
+            out["mx_" + slot + "_sf"] = np.empty(sfs, np.uint8)
+            io.mxq[i] = out["mx_" + slot].ctypes.data
+            io.mxs[i] = out["mx_" + slot + "_sf"].ctypes.data
     io.x, io.g, io.Wgu, io.Wd = (a.ctypes.data for a in keep)
     if bf16:
         out.update({"n16": np.empty((T, d)), "a16": np.empty((T, f))})

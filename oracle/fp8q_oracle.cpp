@@ -222,6 +222,84 @@ QTensor quantize(const std::vector<double>& v, int fmt, bool exact) {
 }
 
 // ----------------------------------------------------------------------------
+// Block scaling (MXFP8).  LLMQ §2 names inner-dimension (block) scaling as the
+// scaling Blackwell tensor cores support natively.  Its formats are those of
+// the OCP Microscaling (MX) specification: a block of 32 consecutive elements
+// along a GEMM's contraction dimension shares one scale 2^X stored as an
+// 8-bit E8M0 code X + 127 (0xFF is NaN); the elements are E4M3 or E5M2 codes.
+// Reading of the scale choice (the pages fix none; the FastML report's
+// "no clipping" rule carried from the tensor to the block): X is the smallest
+// integer with amax_block <= fmax * 2^X, clamped to the code range
+// [-127, 127]; an all-zero block takes X = -127 (code 0); a block holding NaN
+// or Inf takes code 0xFF and sets the status bit.  Element code =
+// fp8(fl32(v * 2^-X)), round to nearest even with saturation; its value is
+// decode(code) * 2^X.
+// ----------------------------------------------------------------------------
+constexpr int kMxBlock = 32;
+
+// The smallest X in [-127, 127] with amax <= fmax * 2^X (amax finite, >= 0).
+int mx_exponent(double amax, int fmt) {
+  const double fmax = fp8_format(fmt).maxv;
+  if (amax == 0.0) return -127;
+  int X = (int)std::ceil(std::log2(amax / fmax));  // an estimate; the loops make it exact
+  X = std::max(-127, std::min(127, X));
+  while (X > -127 && amax <= std::ldexp(fmax, X - 1)) --X;
+  while (X < 127 && amax > std::ldexp(fmax, X)) ++X;
+  return X;
+}
+
+// A block-scaled operand: element codes (same layout as the input), one E8M0
+// code per block, and each element's value decode(code) * 2^X as a double.
+struct MxTensor {
+  std::vector<uint8_t> code;
+  std::vector<uint8_t> sf;   // along_rows == 0: [R][ceil(C/32)]; along_rows == 1: [ceil(R/32)][C]
+  std::vector<double> deq;
+  int status = 0;
+};
+
+// Blocks of 32 consecutive elements of a row (along_rows == 0: the contraction
+// runs along the columns) or of a column (along_rows == 1: it runs along the
+// rows) of the R x C matrix v; a last partial block holds the remainder.
+MxTensor mx_quantize(const std::vector<double>& v, int64_t R, int64_t C, int fmt, bool along_rows) {
+  MxTensor q;
+  q.code.assign((size_t)(R * C), 0);
+  q.deq.assign((size_t)(R * C), 0.0);
+  const int64_t nb_r = along_rows ? (R + kMxBlock - 1) / kMxBlock : R;
+  const int64_t nb_c = along_rows ? C : (C + kMxBlock - 1) / kMxBlock;
+  q.sf.assign((size_t)(nb_r * nb_c), 0);
+  for (int64_t br = 0; br < nb_r; ++br)
+    for (int64_t bc = 0; bc < nb_c; ++bc) {
+      // the block's elements
+      std::vector<int64_t> idx;
+      if (along_rows) {
+        for (int64_t r = br * kMxBlock; r < std::min(R, (br + 1) * kMxBlock); ++r) idx.push_back(r * C + bc);
+      } else {
+        for (int64_t c = bc * kMxBlock; c < std::min(C, (bc + 1) * kMxBlock); ++c) idx.push_back(br * C + c);
+      }
+      double amax = 0.0;
+      bool finite = true;
+      for (int64_t i : idx) {
+        if (!std::isfinite(v[i])) finite = false;
+        else amax = std::max(amax, std::fabs(v[i]));
+      }
+      if (!finite) {
+        q.sf[br * nb_c + bc] = 0xFF;
+        q.status |= 1;
+        for (int64_t i : idx) { q.code[i] = fp8_format(fmt).nan_code; q.deq[i] = std::nan(""); }
+        continue;
+      }
+      const int X = mx_exponent(amax, fmt);
+      q.sf[br * nb_c + bc] = (uint8_t)(X + 127);
+      const float inv = (float)std::ldexp(1.0, -X);
+      for (int64_t i : idx) {
+        q.code[i] = fp8_encode((float)v[i] * inv, fmt);
+        q.deq[i] = std::ldexp(fp8_decode(q.code[i], fmt), X);
+      }
+    }
+  return q;
+}
+
+// ----------------------------------------------------------------------------
 // GEMM: C[M,N] = A[M,K] B[K,N] in fp64, row-major operands.  Rows of C may be
 // split over threads; every element's arithmetic and order is the same for
 // any thread count.
@@ -367,6 +445,32 @@ struct BlockIO {
   int bf16;
   double* n16;       // [T,d] the stored bf16 n (bf16 mode)
   double* a16;       // [T,f] the stored bf16 a (bf16 mode)
+  // Block-scaled MXFP8 (mx != 0; LLMQ §2): every GEMM operand is block-scaled
+  // along that GEMM's contraction dimension instead of per tensor, so a tensor
+  // that two GEMMs contract along different dimensions is quantized twice.
+  // Slots (kMx*): codes [same shape as the tensor] in mxq, E8M0 codes in mxs
+  // ([R][C/32] for blocks along a row, [R/32][C] for blocks along a column).
+  int mx;
+  uint8_t* mxq[12];
+  uint8_t* mxs[12];
+};
+
+// MX operand slots: tensor, then the direction of its blocks ("_r": 32
+// consecutive columns of a row, "_c": 32 consecutive rows of a column).
+enum MxSlot {
+  kMxWgu_r = 0,  // W_gu [d,2f] along 2f: the gate/up dgrad dN = dH W_gu^T
+  kMxWgu_c,      // along d: the gate/up GEMM H = n W_gu
+  kMxWd_r,       // W_d [f,d] along d: the down dgrad dA = dY W_d^T
+  kMxWd_c,       // along f: the down GEMM y = x + a W_d
+  kMxN_r,        // n [T,d] along d: the gate/up GEMM
+  kMxN_c,        // along T: the gate/up wgrad dW_gu = n^T dH
+  kMxA_r,        // a [T,f] along f: the down GEMM
+  kMxA_c,        // along T: the down wgrad dW_d = a^T dY
+  kMxDY_r,       // dY [T,d] along d: the down dgrad
+  kMxDY_c,       // along T: the down wgrad
+  kMxDH_r,       // dH [T,2f] along 2f: the gate/up dgrad
+  kMxDH_c,       // along T: the gate/up wgrad
+  kMxSlots
 };
 
 void put_scal(float* dst, const Scal& s) { dst[0] = s.amax; dst[1] = s.scale; dst[2] = s.scale_inv; }
@@ -390,11 +494,49 @@ QTensor operand(const std::vector<double>& v, int fmt, const BlockIO& io) {
 struct FwdState {
   QTensor Wgu, Wd, n, a;
   std::vector<double> nval, rstd, H, y;
+  MxTensor mx[kMxSlots];  // MX mode: the forward's slots (W_gu, W_d, n, a)
   int status = 0;
 };
 
+void put_mx(const BlockIO& io, int slot, const MxTensor& t) {
+  if (io.mxq[slot]) std::copy(t.code.begin(), t.code.end(), io.mxq[slot]);
+  if (io.mxs[slot]) std::copy(t.sf.begin(), t.sf.end(), io.mxs[slot]);
+}
+
+// The MX forward: the same steps as block_forward with every per-tensor
+// quantization replaced by the block quantization along the GEMM's contraction
+// dimension (no alpha: the block scales are part of each operand's value).
+FwdState block_forward_mx(const BlockIO& io) {
+  const int64_t T = io.T, d = io.d, f = io.f;
+  FwdState S;
+  std::vector<double> x(io.x, io.x + T * d), g(io.g, io.g + d);
+  std::vector<double> Wgu(io.Wgu, io.Wgu + d * 2 * f), Wd(io.Wd, io.Wd + f * d);
+  S.mx[kMxWgu_c] = mx_quantize(Wgu, d, 2 * f, FMT_E4M3, true);
+  S.mx[kMxWgu_r] = mx_quantize(Wgu, d, 2 * f, FMT_E4M3, false);
+  S.mx[kMxWd_c] = mx_quantize(Wd, f, d, FMT_E4M3, true);
+  S.mx[kMxWd_r] = mx_quantize(Wd, f, d, FMT_E4M3, false);
+  rmsnorm_fwd(x, g, T, d, io.eps, false, S.nval, S.rstd);
+  S.mx[kMxN_r] = mx_quantize(S.nval, T, d, FMT_E4M3, false);
+  S.mx[kMxN_c] = mx_quantize(S.nval, T, d, FMT_E4M3, true);
+
+  std::vector<double> acc1 = matmul(S.mx[kMxN_r].deq, S.mx[kMxWgu_c].deq, T, 2 * f, d, io.nthreads);
+  S.H.resize(acc1.size());
+  for (size_t i = 0; i < acc1.size(); ++i) S.H[i] = to_bf16(acc1[i]);
+
+  std::vector<double> a = swiglu_fwd(S.H, T, f, false);
+  S.mx[kMxA_r] = mx_quantize(a, T, f, FMT_E4M3, false);
+  S.mx[kMxA_c] = mx_quantize(a, T, f, FMT_E4M3, true);
+
+  std::vector<double> acc2 = matmul(S.mx[kMxA_r].deq, S.mx[kMxWd_c].deq, T, d, f, io.nthreads);
+  S.y.resize(acc2.size());
+  for (size_t i = 0; i < acc2.size(); ++i) S.y[i] = to_bf16(x[i] + acc2[i]);
+  for (int k = kMxWgu_r; k <= kMxA_c; ++k) S.status |= S.mx[k].status;
+  return S;
+}
+
 // status bit 1: a tensor's absmax was not finite
 FwdState block_forward(const BlockIO& io) {
+  if (io.mx) return block_forward_mx(io);
   const int64_t T = io.T, d = io.d, f = io.f;
   const bool ex = io.exact != 0;
   FwdState S;
@@ -428,6 +570,10 @@ void write_forward(const BlockIO& io, const FwdState& S) {
   put(io.y, S.y);
   put(io.H, S.H);
   put(io.rstd, S.rstd);
+  if (io.mx) {
+    for (int k = kMxWgu_r; k <= kMxA_c; ++k) put_mx(io, k, S.mx[k]);
+    return;
+  }
   if (!io.exact) {
     put(io.Wgu8, S.Wgu.code); put(io.Wd8, S.Wd.code);
     put(io.n8, S.n.code); put(io.a8, S.a.code);
@@ -439,7 +585,60 @@ void write_forward(const BlockIO& io, const FwdState& S) {
   }
 }
 
+// SwiGLU backward at the bf16 storage point: dH from dA and the stored H.
+std::vector<double> swiglu_bwd(const std::vector<double>& H, const std::vector<double>& dA, int64_t T, int64_t f,
+                               bool ex) {
+  std::vector<double> dH((size_t)(T * 2 * f));
+  for (int64_t t = 0; t < T; ++t)
+    for (int64_t j = 0; j < f; ++j) {
+      const double h = H[t * 2 * f + j], u = H[t * 2 * f + f + j];
+      const double da = dA[t * f + j];
+      const double sg = 1.0 / (1.0 + std::exp(-h));
+      const double dg_ = da * u * sg * (1.0 + h * (1.0 - sg));
+      const double du_ = da * h * sg;
+      dH[t * 2 * f + j] = ex ? dg_ : to_bf16(dg_);
+      dH[t * 2 * f + f + j] = ex ? du_ : to_bf16(du_);
+    }
+  return dH;
+}
+
+void rmsnorm_bwd(const std::vector<double>& x, const std::vector<double>& g, const std::vector<double>& rstd,
+                 const std::vector<double>& dN, const std::vector<double>& dres, int64_t T, int64_t d, bool ex,
+                 std::vector<double>& dX, std::vector<double>& dg);
+
+// The MX backward: the block_backward steps with block-scaled operands; each
+// GEMM takes the quantization of its operands along its own contraction
+// dimension (the wgrad GEMMs contract over tokens).
+int block_backward_mx(const BlockIO& io, const FwdState& S) {
+  const int64_t T = io.T, d = io.d, f = io.f;
+  int status = S.status;
+  std::vector<double> x(io.x, io.x + T * d), g(io.g, io.g + d), dY(io.dY, io.dY + T * d);
+  const int gf = io.grad_fmt;
+  MxTensor dY_r = mx_quantize(dY, T, d, gf, false), dY_c = mx_quantize(dY, T, d, gf, true);
+
+  std::vector<double> dA = matmul(dY_r.deq, transpose(S.mx[kMxWd_r].deq, f, d), T, f, d, io.nthreads);
+  std::vector<double> dH = swiglu_bwd(S.H, dA, T, f, false);
+  MxTensor dH_r = mx_quantize(dH, T, 2 * f, gf, false), dH_c = mx_quantize(dH, T, 2 * f, gf, true);
+
+  std::vector<double> dWd = matmul(transpose(S.mx[kMxA_c].deq, T, f), dY_c.deq, f, d, T, io.nthreads);
+  for (double& v : dWd) v = (double)(float)v;
+  std::vector<double> dN = matmul(dH_r.deq, transpose(S.mx[kMxWgu_r].deq, d, 2 * f), T, d, 2 * f, io.nthreads);
+  for (double& v : dN) v = (double)(float)v;
+  std::vector<double> dWgu = matmul(transpose(S.mx[kMxN_c].deq, T, d), dH_c.deq, d, 2 * f, T, io.nthreads);
+  for (double& v : dWgu) v = (double)(float)v;
+
+  std::vector<double> dX, dgv;
+  rmsnorm_bwd(x, g, S.rstd, dN, dY, T, d, false, dX, dgv);
+  for (const MxTensor* t : {&dY_r, &dY_c, &dH_r, &dH_c}) status |= t->status;
+
+  put(io.dX, dX); put(io.dWgu, dWgu); put(io.dWd, dWd); put(io.dg, dgv);
+  put(io.dN, dN); put(io.dH, dH);
+  put_mx(io, kMxDY_r, dY_r); put_mx(io, kMxDY_c, dY_c); put_mx(io, kMxDH_r, dH_r); put_mx(io, kMxDH_c, dH_c);
+  return status;
+}
+
 int block_backward(const BlockIO& io, const FwdState& S) {
+  if (io.mx) return block_backward_mx(io, S);
   const int64_t T = io.T, d = io.d, f = io.f;
   const bool ex = io.exact != 0;
   int status = S.status;
@@ -939,6 +1138,48 @@ int fo_gemm_scaled(int layout, int64_t M, int64_t N, int64_t K, const uint8_t* A
   const double alpha = (double)(sinvA * sinvB);
   for (int64_t i = 0; i < M * N; ++i) {
     double v = alpha * acc[i];
+    if (out_dtype == 0) {
+      if (residual) v += bf16_value(residual[i]);
+      ((uint16_t*)C)[i] = to_bf16_bits(v);
+    } else if (out_dtype == 1) {
+      ((float*)C)[i] = (float)v;
+    } else {
+      ((double*)C)[i] = v;
+    }
+  }
+  return 0;
+}
+
+// Block quantization (MXFP8) of an R x C tensor (dtype 0 bf16 bits, 1 fp32):
+// along_rows 0 = blocks of 32 consecutive columns of a row, sf [R][ceil(C/32)];
+// 1 = blocks of 32 consecutive rows of a column, sf [ceil(R/32)][C].
+int fo_mx_quantize(const void* x, int dtype, int64_t R, int64_t C, int fmt, int along_rows, uint8_t* q,
+                   uint8_t* sf) {
+  MxTensor t = mx_quantize(load_input(x, dtype, R * C), R, C, fmt, along_rows != 0);
+  std::copy(t.code.begin(), t.code.end(), q);
+  std::copy(t.sf.begin(), t.sf.end(), sf);
+  return t.status;
+}
+
+// Block-scaled GEMM: C = op(A) op(B) (+ residual) with every element of A and B
+// worth decode(code) * 2^(sf - 127) of its K-block of 32 (layouts as
+// fo_gemm_scaled).  sfA is [M][ceil(K/32)] (block m, k), sfB [N][ceil(K/32)]
+// (block n, k), whatever the operands' storage layout.
+int fo_gemm_mx(int layout, int64_t M, int64_t N, int64_t K, const uint8_t* A, int fmtA, const uint8_t* sfA,
+               const uint8_t* B, int fmtB, const uint8_t* sfB, const uint16_t* residual, int out_dtype, void* C,
+               int nthreads) {
+  const int64_t KB = (K + kMxBlock - 1) / kMxBlock;
+  auto sfval = [](uint8_t c) { return c == 0xFF ? std::nan("") : std::ldexp(1.0, (int)c - 127); };
+  std::vector<double> a((size_t)(M * K)), b((size_t)(K * N));
+  for (int64_t i = 0; i < M; ++i)
+    for (int64_t k = 0; k < K; ++k)
+      a[i * K + k] = fp8_decode(layout == 2 ? A[k * M + i] : A[i * K + k], fmtA) * sfval(sfA[i * KB + k / kMxBlock]);
+  for (int64_t k = 0; k < K; ++k)
+    for (int64_t j = 0; j < N; ++j)
+      b[k * N + j] = fp8_decode(layout == 1 ? B[j * K + k] : B[k * N + j], fmtB) * sfval(sfB[j * KB + k / kMxBlock]);
+  std::vector<double> acc = matmul(a, b, M, N, K, nthreads);
+  for (int64_t i = 0; i < M * N; ++i) {
+    double v = acc[i];
     if (out_dtype == 0) {
       if (residual) v += bf16_value(residual[i]);
       ((uint16_t*)C)[i] = to_bf16_bits(v);
