@@ -48,6 +48,10 @@ def _load() -> ctypes.CDLL:
     L.mlp_block_workspace_size.restype = sz
     L.mlp_block_workspace_size.argtypes = [i64, i64, i64, i32]
     L.mlp_block_fwd.argtypes = [ctypes.POINTER(FP8QMlp), vp, sz, vp]
+    L.mx_scale_bytes.restype = sz
+    L.mx_scale_bytes.argtypes = [i64, i64]
+    L.mx_quantize.argtypes = [vp, i32, i64, i64, i32, vp, vp, vp, vp, vp]
+    L.fp8_gemm_mx.argtypes = [i32, i64, i64, i64, vp, i32, i64, vp, vp, i32, i64, vp, vp, i32, i64, vp, i64, vp]
     L.attention_fwd.argtypes = [vp, i64, i64, i32, i32, i32, vp, vp, vp]
     L.attention_bwd_workspace_size.restype = sz
     L.attention_bwd_workspace_size.argtypes = [i64, i32]
@@ -67,6 +71,8 @@ def _load() -> ctypes.CDLL:
     L.block_run_steps.argtypes = [ctypes.POINTER(FP8QBlock), ctypes.POINTER(FP8QBlock),
                                   ctypes.POINTER(FP8QBlockHostIO), i32, i32, vp, sz, vp]
     L.fp8q_selftest_bounded_wait.argtypes = [i64, vp]
+    L.fp8q_selftest_gemm_wait_limit.argtypes = [i32, i64, i64, i64, vp, i32, i64, vp, i32, i64, vp, vp, i32, vp, vp,
+                                                vp, i32, i64, i64, vp]
     L.fp8q_trace_start.argtypes = [i32]
     L.fp8q_trace_read.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int), i32]
     L.fp8q_kernel_name.restype = ctypes.c_char_p
@@ -83,7 +89,21 @@ class FP8QMlp(ctypes.Structure):
     _fields_ = ([("T", ctypes.c_int64), ("d", ctypes.c_int64), ("f", ctypes.c_int64), ("eps", ctypes.c_float)]
                 + [(name, ctypes.c_void_p) for name in _MLP_PTRS]
                 + [("recompute", ctypes.c_int), ("grad_e4m3", ctypes.c_int), ("bf16", ctypes.c_int),
-                   ("n16", ctypes.c_void_p), ("a16", ctypes.c_void_p)])
+                   ("n16", ctypes.c_void_p), ("a16", ctypes.c_void_p), ("mx", ctypes.c_void_p)])
+
+
+class FP8QMxTensor(ctypes.Structure):
+    """Mirror of ``fp8q_mx_tensor``: codes and chunked E8M0 scales."""
+    _fields_ = [("q", ctypes.c_void_p), ("sf", ctypes.c_void_p)]
+
+
+# The block-scaled operands of the MXFP8 block, in the order of fp8q_mlp_mx.
+MX_SLOTS = ("W_gu_r", "W_gu_c", "W_d_r", "W_d_c", "n_r", "n_c", "a_r", "a_c", "dY_r", "dY_c", "dH_r", "dH_c")
+
+
+class FP8QMlpMx(ctypes.Structure):
+    """Mirror of ``fp8q_mlp_mx`` in include/fp8q.h."""
+    _fields_ = [(n, FP8QMxTensor) for n in MX_SLOTS]
 
 
 class FP8QMlpHostIO(ctypes.Structure):
@@ -201,6 +221,47 @@ def fp8_gemm_scaled(layout: int, A: torch.Tensor, fmtA: int, B: torch.Tensor, fm
     return C
 
 
+def mx_scale_bytes(rows: int, K: int) -> int:
+    """Bytes of the chunked E8M0 scales of an operand with `rows` rows and contraction length K."""
+    return lib.mx_scale_bytes(rows, K)
+
+
+def mx_quantize(x: torch.Tensor, fmt: int = E4M3, rows: bool = True, cols: bool = True, stream=None):
+    """Block-scaled (MXFP8) quantization of x [R, C] (bf16 or fp32; R, C multiples of 128).
+    Returns ((q_r, sf_r) or None, (q_c, sf_c) or None): blocks of 32 along each row (the operand of a
+    GEMM contracting over C) and down each column (contracting over R), scales in the chunked layout."""
+    dev = _dev(x)
+    R, C = x.shape
+    r = (torch.empty((R, C), dtype=torch.uint8, device=dev),
+         torch.empty(mx_scale_bytes(R, C), dtype=torch.uint8, device=dev)) if rows else None
+    c = (torch.empty((R, C), dtype=torch.uint8, device=dev),
+         torch.empty(mx_scale_bytes(C, R), dtype=torch.uint8, device=dev)) if cols else None
+    _check("mx_quantize", lib.mx_quantize(_ptr(x), _dtype_code(x), R, C, fmt, _ptr(r[0]) if r else None,
+                                          _ptr(r[1]) if r else None, _ptr(c[0]) if c else None,
+                                          _ptr(c[1]) if c else None, _stream(stream)))
+    return r, c
+
+
+def fp8_gemm_mx(layout: int, A: torch.Tensor, fmtA: int, sfA: torch.Tensor, B: torch.Tensor, fmtB: int,
+                sfB: torch.Tensor, out_dtype=torch.bfloat16, residual=None, C=None, stream=None):
+    """Block-scaled GEMM C = op(A) op(B) (+ residual); layouts as fp8_gemm_scaled, sfA / sfB the
+    operands' chunked scales (see fp8_gemm_mx in include/fp8q.h); K a multiple of 128."""
+    dev = _dev(A)
+    _dev(B)
+    if layout == TN:
+        K, M = A.shape
+    else:
+        M, K = A.shape
+    N = B.shape[0] if layout == NT else B.shape[1]
+    out_code = {torch.bfloat16: BF16, torch.float32: F32}[out_dtype]
+    C = torch.empty((M, N), dtype=out_dtype, device=dev) if C is None else C
+    ldr = residual.shape[1] if residual is not None else 0
+    _check("fp8_gemm_mx", lib.fp8_gemm_mx(layout, M, N, K, _ptr(A), fmtA, A.shape[1], _ptr(sfA), _ptr(B), fmtB,
+                                          B.shape[1], _ptr(sfB), _ptr(C), out_code, C.shape[1], _ptr(residual), ldr,
+                                          _stream(stream)))
+    return C
+
+
 def rmsnorm_quant(x: torch.Tensor, g: torch.Tensor, eps: float = 1e-6, q=None, scal=None, rstd=None, ws=None,
                   stream=None):
     """RMSNorm + E4M3 quantization. Returns (codes [T,d], scal[3], rstd[T])."""
@@ -290,20 +351,33 @@ class MlpBuffers:
     bf16: bool = False
     n16: torch.Tensor | None = None
     a16: torch.Tensor | None = None
+    mx: dict | None = None  # MXFP8 block: slot name -> (codes, chunked scales), see MX_SLOTS
+    _mx_struct: FP8QMlpMx | None = None
 
     @staticmethod
     def allocate(T: int, d: int, f: int, device="cuda", backward: bool = True, eps: float = 1e-6,
-                 keep_intermediates: bool = False, bf16: bool = False) -> "MlpBuffers":
-        """bf16=True: buffers of the BF16 baseline (n16, a16 instead of the FP8 codes and scales)."""
+                 keep_intermediates: bool = False, bf16: bool = False, mx: bool = False) -> "MlpBuffers":
+        """bf16=True: buffers of the BF16 baseline (n16, a16 instead of the FP8 codes and scales).
+        mx=True: the block-scaled MXFP8 block (the codes and scales of every slot of MX_SLOTS)."""
         e = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)
-        q8 = (lambda shape: None) if bf16 else (lambda shape: e(shape, torch.uint8))
+        q8 = (lambda shape: None) if (bf16 or mx) else (lambda shape: e(shape, torch.uint8))
         b = MlpBuffers(
             T=T, d=d, f=f, eps=eps,
             x=e((T, d), torch.bfloat16), g=e((d,), torch.bfloat16), W_gu=e((d, 2 * f), torch.bfloat16),
             W_d=e((f, d), torch.bfloat16), y=e((T, d), torch.bfloat16), W_gu8=q8((d, 2 * f)),
             W_d8=q8((f, d)), n8=q8((T, d)), rstd=e((T,), torch.float32),
             H=e((T, 2 * f), torch.bfloat16), a8=q8((T, f)),
-            scal=None if bf16 else torch.zeros((6, 3), device=device), bf16=bf16)
+            scal=None if (bf16 or mx) else torch.zeros((6, 3), device=device), bf16=bf16)
+        if mx:
+            shape = {"W_gu": (d, 2 * f), "W_d": (f, d), "n": (T, d), "a": (T, f), "dY": (T, d), "dH": (T, 2 * f)}
+            b.mx = {}
+            for slot in MX_SLOTS:
+                name, ax = slot.rsplit("_", 1)
+                if name in ("dY", "dH") and not backward:
+                    continue
+                R, C = shape[name]
+                b.mx[slot] = (e((R, C), torch.uint8),
+                              e((mx_scale_bytes(R, C) if ax == "r" else mx_scale_bytes(C, R),), torch.uint8))
         if bf16:
             b.n16 = e((T, d), torch.bfloat16)
             b.a16 = e((T, f), torch.bfloat16)
@@ -314,9 +388,9 @@ class MlpBuffers:
             b.dW_d = e((f, d), torch.float32)
             b.dg = e((d,), torch.float32)
             if keep_intermediates:
-                b.dY8 = q8((T, d))
+                b.dY8 = None if mx else q8((T, d))
                 b.dH = e((T, 2 * f), torch.bfloat16)
-                b.dH8 = q8((T, 2 * f))
+                b.dH8 = None if mx else q8((T, 2 * f))
                 b.dN = e((T, d), torch.float32)
         nb = lib.mlp_block_workspace_size(T, d, f, int(backward))
         b.ws = torch.empty(nb, dtype=torch.uint8, device=device)
@@ -328,6 +402,13 @@ class MlpBuffers:
         for name in _MLP_PTRS + ("n16", "a16"):
             t = getattr(self, name)
             setattr(s, name, None if t is None else t.data_ptr())
+        if self.mx is not None:
+            if self._mx_struct is None:
+                m = FP8QMlpMx()
+                for slot, (q, sf) in self.mx.items():
+                    setattr(m, slot, FP8QMxTensor(q.data_ptr(), sf.data_ptr()))
+                self._mx_struct = m
+            s.mx = ctypes.addressof(self._mx_struct)
         return s
 
 
@@ -498,6 +579,27 @@ def block_run_steps(b0: BlockBuffers, b1: BlockBuffers, host: list, backward: bo
     device.  Device sets b0, b1 alternate; b0's workspace is used."""
     _check("block_run_steps", lib.block_run_steps(*_steps_args(b0, b1, host, FP8QBlockHostIO), int(bool(backward)),
                                                   _ptr(b0.ws), b0.ws.numel(), _stream(stream)))
+
+
+def selftest_gemm_wait_limit(layout: int, A: torch.Tensor, fmtA: int, B: torch.Tensor, fmtB: int, limit_s: float,
+                             sinvA=None, sinvB=None, sfA=None, sfB=None, out_dtype=torch.float32, C=None,
+                             stream=None):
+    """fp8_gemm_scaled (sinvA/sinvB given) or fp8_gemm_mx (sfA/sfB given) with every pipeline wait of
+    the kernel limited to limit_s (fp8q_selftest_gemm_wait_limit in include/fp8q.h).  Returns C."""
+    dev = _dev(A)
+    if layout == TN:
+        K, M = A.shape
+    else:
+        M, K = A.shape
+    N = B.shape[0] if layout == NT else B.shape[1]
+    out_code = {torch.bfloat16: BF16, torch.float32: F32}[out_dtype]
+    C = torch.empty((M, N), dtype=out_dtype, device=dev) if C is None else C
+    mx = sfA is not None
+    _check("fp8q_selftest_gemm_wait_limit",
+           lib.fp8q_selftest_gemm_wait_limit(layout, M, N, K, _ptr(A), fmtA, A.shape[1], _ptr(B), fmtB, B.shape[1],
+                                             _ptr(sinvA), _ptr(sinvB), int(mx), _ptr(sfA), _ptr(sfB), _ptr(C),
+                                             out_code, C.shape[1], int(limit_s * 1e9), _stream(stream)))
+    return C
 
 
 def selftest_bounded_wait(limit_s: float = 0.02, stream=None):

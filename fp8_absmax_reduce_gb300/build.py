@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 OBJ_DIR = os.path.join(OUT_DIR, "obj")
 LIB = os.path.join(OUT_DIR, "libfp8q.so")
-SOURCES = ["fp8q_api.cu", "fp8q_quant.cu", "fp8q_gemm.cu", "fp8q_attn.cu", "fp8q_noalloc.cu"]
+SOURCES = ["fp8q_api.cu", "fp8q_quant.cu", "fp8q_gemm.cu", "fp8q_attn.cu", "fp8q_noalloc.cu", "fp8q_mx.cu"]
 HEADERS = ["fp8q_common.cuh", "fp8q_internal.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -16,6 +16,9 @@ using namespace fp8q;
 __device__ unsigned g_status_word;
 
 thread_local int t_last_launches = 0;
+// Pipeline-wait limit of the GEMMs enqueued by the next fp8_gemm_scaled / fp8_gemm_mx call on this
+// thread (0: the default); set only for the duration of fp8q_selftest_gemm_wait_limit.
+thread_local uint64_t t_gemm_wait_ns = 0;
 
 // ---- kernel-level trace (benchmarks) ------------------------------------------
 enum Kind {
@@ -23,6 +26,7 @@ enum Kind {
   kKGemmGateUp, kKGemmDown, kKGemmDownDgrad, kKGemmDownWgrad, kKGemmGateUpDgrad, kKGemmGateUpWgrad, kKGemm,
   kKGemmQkv, kKGemmOResidual, kKGemmODgrad, kKGemmOWgrad, kKGemmQkvDgrad, kKGemmQkvWgrad,
   kKGemmGateUpRecompute, kKRmsnormBf16, kKAttnFwd, kKAttnBwdDelta, kKAttnBwdDkdv, kKAttnBwdDq,
+  kKMxQuant,
   kKCount
 };
 const char* const kKindNames[kKCount] = {
@@ -30,7 +34,8 @@ const char* const kKindNames[kKCount] = {
     "rmsnorm_bwd", "gemm_gate_up_swiglu", "gemm_down_residual", "gemm_down_dgrad_swiglu_bwd",
     "gemm_down_wgrad", "gemm_gate_up_dgrad", "gemm_gate_up_wgrad", "gemm",
     "gemm_qkv", "gemm_o_residual", "gemm_o_dgrad", "gemm_o_wgrad", "gemm_qkv_dgrad", "gemm_qkv_wgrad",
-    "gemm_gate_up_recompute", "rmsnorm_bf16", "attn_fwd", "attn_bwd_delta", "attn_bwd_dkdv", "attn_bwd_dq"};
+    "gemm_gate_up_recompute", "rmsnorm_bf16", "attn_fwd", "attn_bwd_delta", "attn_bwd_dkdv", "attn_bwd_dq",
+    "mx_quant"};
 
 struct Trace {
   bool on = false;
@@ -185,10 +190,29 @@ size_t mlp_ws_layout(int64_t T, int64_t d, int64_t f, int backward, uint8_t* bas
   return c.off;
 }
 
+bool mx_ok(const fp8q_mx_tensor& t) { return al16(t.q) && al16(t.sf); }
+
 int validate_mlp(const fp8q_mlp* m, bool backward) {
   if (!m) return FP8Q_ERR_INVALID_ARG;
   if (m->T < 1 || m->d < 16 || m->f < 16 || m->d % 16 || m->f % 16 || m->d > 8192) return FP8Q_ERR_INVALID_ARG;
   if (m->T > (int64_t)1 << 24 || m->f > (int64_t)1 << 20) return FP8Q_ERR_INVALID_ARG;
+  if (m->mx) {
+    if (m->recompute || m->bf16) return FP8Q_ERR_UNSUPPORTED;
+    if (m->T % 128 || m->d % 128 || m->f % 128) return FP8Q_ERR_INVALID_ARG;
+    const fp8q_mlp_mx& x = *m->mx;
+    const void* must[] = {m->x, m->g, m->W_gu, m->W_d, m->rstd, m->H};
+    for (const void* p : must)
+      if (!al16(p)) return FP8Q_ERR_INVALID_ARG;
+    for (const fp8q_mx_tensor* t : {&x.W_gu_r, &x.W_gu_c, &x.W_d_r, &x.W_d_c, &x.n_r, &x.n_c, &x.a_r, &x.a_c})
+      if (!mx_ok(*t)) return FP8Q_ERR_INVALID_ARG;
+    if (!backward) return al16(m->y) ? FP8Q_OK : FP8Q_ERR_INVALID_ARG;
+    const void* must_b[] = {m->dY, m->dX, m->dW_gu, m->dW_d, m->dg};
+    for (const void* p : must_b)
+      if (!al16(p)) return FP8Q_ERR_INVALID_ARG;
+    for (const fp8q_mx_tensor* t : {&x.dY_r, &x.dY_c, &x.dH_r, &x.dH_c})
+      if (!mx_ok(*t)) return FP8Q_ERR_INVALID_ARG;
+    return ((m->dH && !al16(m->dH)) || (m->dN && !al16(m->dN))) ? FP8Q_ERR_INVALID_ARG : FP8Q_OK;
+  }
   if (m->bf16) {
     if (m->recompute || m->grad_e4m3) return FP8Q_ERR_UNSUPPORTED;
     const void* must16[] = {m->x, m->g, m->W_gu, m->W_d, m->n16, m->rstd, m->H, m->a16};
@@ -281,8 +305,89 @@ int mlp_bwd_run_bf16(const fp8q_mlp* m, const MlpWs& w, Ctx& c) {
 
 // The MLP block's kernel sequences, enqueued on c.L.stream (shared by
 // mlp_block_* and block_*).
+// A GEMM of the MXFP8 block: codes and chunked scales of both operands, no alpha.
+GemmProblem mx_gemm(int a_mn, int b_mn, int64_t M, int64_t N, int64_t K, const fp8q_mx_tensor& A, int fmtA,
+                    int64_t lda, const fp8q_mx_tensor& B, int fmtB, int64_t ldb, int64_t b_cols, int epi, int out_f32,
+                    void* C, int64_t ldc) {
+  GemmProblem g{};
+  g.mx = 1;
+  g.a_mn = a_mn;
+  g.b_mn = b_mn;
+  g.M = (int)M;
+  g.N = (int)N;
+  g.K = (int)K;
+  g.A = A.q;
+  g.sfA = A.sf;
+  g.lda = lda;
+  g.fmtA = fmtA;
+  g.B = B.q;
+  g.sfB = B.sf;
+  g.ldb = ldb;
+  g.fmtB = fmtB;
+  g.b_cols = b_cols;
+  g.epi = epi;
+  g.out_f32 = out_f32;
+  g.C = C;
+  g.ldc = ldc;
+  return g;
+}
+
+// The MXFP8 block's forward: weights and n quantized both ways (one pass each), the gate/up GEMM
+// with the SwiGLU epilogue writing H, a = SwiGLU(H) quantized both ways, the down GEMM + residual.
+int mlp_fwd_run_mx(const fp8q_mlp* m, const MlpWs& w, Ctx& c) {
+  const int64_t T = m->T, d = m->d, f = m->f;
+  const fp8q_mlp_mx& x = *m->mx;
+  int P = 0;
+  FP8Q_STEP(kKMxQuant, launch_mx_quant(kMxInBf16, m->W_gu, nullptr, nullptr, d, 2 * f, 0, x.W_gu_r.q, x.W_gu_r.sf,
+                                       x.W_gu_c.q, x.W_gu_c.sf, c.L));
+  FP8Q_STEP(kKMxQuant, launch_mx_quant(kMxInBf16, m->W_d, nullptr, nullptr, f, d, 0, x.W_d_r.q, x.W_d_r.sf, x.W_d_c.q,
+                                       x.W_d_c.sf, c.L));
+  FP8Q_STEP(kKRmsnormStats, launch_rmsnorm_stats((const uint16_t*)m->x, (const uint16_t*)m->g, T, (int)d, m->eps,
+                                                 m->rstd, w.part_q, &P, c.L));
+  FP8Q_STEP(kKMxQuant, launch_mx_quant(kMxInRmsnorm, m->x, (const uint16_t*)m->g, m->rstd, T, d, 0, x.n_r.q, x.n_r.sf,
+                                       x.n_c.q, x.n_c.sf, c.L));
+  GemmProblem g1 = mx_gemm(0, 1, T, f, d, x.n_r, 0, d, x.W_gu_c, 0, 2 * f, 2 * f, kEpiSwiglu, 0, m->H, 2 * f);
+  FP8Q_STEP(kKGemmGateUp, launch_gemm(g1, &P, c.L));
+  FP8Q_STEP(kKMxQuant, launch_mx_quant(kMxInSwiglu, m->H, nullptr, nullptr, T, f, 0, x.a_r.q, x.a_r.sf, x.a_c.q,
+                                       x.a_c.sf, c.L));
+  GemmProblem g2 = mx_gemm(0, 1, T, d, f, x.a_r, 0, f, x.W_d_c, 0, d, d, kEpiResidual, 0, m->y, d);
+  g2.R = (const uint16_t*)m->x;
+  g2.ldr = d;
+  FP8Q_STEP(kKGemmDown, launch_gemm(g2, &P, c.L));
+  return FP8Q_OK;
+}
+
+// The MXFP8 block's backward: each GEMM reads its operands quantized along its own contraction
+// dimension (the wgrads contract over tokens: the "_c" tensors).
+int mlp_bwd_run_mx(const fp8q_mlp* m, const MlpWs& w, Ctx& c) {
+  const int64_t T = m->T, d = m->d, f = m->f;
+  const fp8q_mlp_mx& x = *m->mx;
+  uint16_t* dH = m->dH ? (uint16_t*)m->dH : w.dH;
+  float* dN = m->dN ? m->dN : w.dN;
+  const int gf = m->grad_e4m3 ? 0 : 1;
+  int P = 0;
+  FP8Q_STEP(kKMxQuant, launch_mx_quant(kMxInBf16, m->dY, nullptr, nullptr, T, d, gf, x.dY_r.q, x.dY_r.sf, x.dY_c.q,
+                                       x.dY_c.sf, c.L));
+  GemmProblem g3 = mx_gemm(0, 0, T, f, d, x.dY_r, gf, d, x.W_d_r, 0, d, f, kEpiSwigluBwd, 0, dH, 2 * f);
+  g3.R = (const uint16_t*)m->H;
+  g3.ldr = 2 * f;
+  FP8Q_STEP(kKGemmDownDgrad, launch_gemm(g3, &P, c.L));
+  FP8Q_STEP(kKMxQuant, launch_mx_quant(kMxInBf16, dH, nullptr, nullptr, T, 2 * f, gf, x.dH_r.q, x.dH_r.sf, x.dH_c.q,
+                                       x.dH_c.sf, c.L));
+  GemmProblem g4 = mx_gemm(1, 1, f, d, T, x.a_c, 0, f, x.dY_c, gf, d, d, kEpiStore, 1, m->dW_d, d);
+  FP8Q_STEP(kKGemmDownWgrad, launch_gemm(g4, &P, c.L));
+  GemmProblem g5 = mx_gemm(0, 0, T, d, 2 * f, x.dH_r, gf, 2 * f, x.W_gu_r, 0, 2 * f, d, kEpiStore, 1, dN, d);
+  FP8Q_STEP(kKGemmGateUpDgrad, launch_gemm(g5, &P, c.L));
+  GemmProblem g6 = mx_gemm(1, 1, d, 2 * f, T, x.n_c, 0, d, x.dH_c, gf, 2 * f, 2 * f, kEpiStore, 1, m->dW_gu, 2 * f);
+  FP8Q_STEP(kKGemmGateUpWgrad, launch_gemm(g6, &P, c.L));
+  FP8Q_STEP(kKRmsnormBwd, launch_rmsnorm_bwd(dN, (const uint16_t*)m->x, (const uint16_t*)m->dY, (const uint16_t*)m->g,
+                                             m->rstd, T, (int)d, (uint16_t*)m->dX, w.dg_part, m->dg, c.L));
+  return FP8Q_OK;
+}
+
 int mlp_fwd_run(const fp8q_mlp* m, const MlpWs& w, Ctx& c) {
   if (m->bf16) return mlp_fwd_run_bf16(m, c);
+  if (m->mx) return mlp_fwd_run_mx(m, w, c);
   const int64_t T = m->T, d = m->d, f = m->f;
   float* s_wgu = m->scal + 0;
   float* s_wd = m->scal + 3;
@@ -350,6 +455,7 @@ int mlp_fwd_run(const fp8q_mlp* m, const MlpWs& w, Ctx& c) {
 
 int mlp_bwd_run(const fp8q_mlp* m, const MlpWs& w, Ctx& c) {
   if (m->bf16) return mlp_bwd_run_bf16(m, w, c);
+  if (m->mx) return mlp_bwd_run_mx(m, w, c);
   const int64_t T = m->T, d = m->d, f = m->f;
   const float* s_wgu = m->scal + 0;
   const float* s_wd = m->scal + 3;
@@ -530,6 +636,7 @@ int validate_block(const fp8q_block* b, bool backward) {
   if (!b) return FP8Q_ERR_INVALID_ARG;
   const fp8q_mlp& m = b->mlp;
   if (m.T != b->T || m.d != b->d || m.f != b->f || m.x != b->h) return FP8Q_ERR_INVALID_ARG;
+  if (m.mx) return FP8Q_ERR_UNSUPPORTED;  // the MXFP8 mode is built for the MLP block
   if (b->n_qkv < 16 || b->n_qkv % 16 || b->n_qkv > (int64_t)1 << 20) return FP8Q_ERR_INVALID_ARG;
   int e = validate_mlp(&m, backward);
   if (e) return e;
@@ -801,6 +908,72 @@ int fp8_gemm_scaled(fp8q_layout layout, int64_t M, int64_t N, int64_t K, const u
   g.ldc = ldc;
   g.R = static_cast<const uint16_t*>(residual);
   g.ldr = ldr;
+  g.wait_ns = t_gemm_wait_ns;
+  int P = 0;
+  FP8Q_STEP(kKGemm, launch_gemm(g, &P, c.L));
+  return finish(c);
+}
+
+// ---------------------------------------------------------------------------
+int fp8q_selftest_gemm_wait_limit(fp8q_layout layout, int64_t M, int64_t N, int64_t K, const uint8_t* A,
+                                  fp8q_fmt fmtA, int64_t lda, const uint8_t* B, fp8q_fmt fmtB, int64_t ldb,
+                                  const float* sinvA, const float* sinvB, int mx, const uint8_t* sfA,
+                                  const uint8_t* sfB, void* C, fp8q_dtype out_dtype, int64_t ldc, int64_t limit_ns,
+                                  fp8q_stream stream) {
+  if (limit_ns < 1000 || limit_ns > 10000000000ll) return FP8Q_ERR_INVALID_ARG;
+  t_gemm_wait_ns = (uint64_t)limit_ns;
+  const int rc = mx ? fp8_gemm_mx(layout, M, N, K, A, fmtA, lda, sfA, B, fmtB, ldb, sfB, C, out_dtype, ldc, nullptr,
+                                  0, stream)
+                    : fp8_gemm_scaled(layout, M, N, K, A, fmtA, lda, B, fmtB, ldb, sinvA, sinvB, C, out_dtype, ldc,
+                                      nullptr, 0, stream);
+  t_gemm_wait_ns = 0;
+  return rc;
+}
+
+// ---------------------------------------------------------------------------
+size_t mx_scale_bytes(int64_t rows, int64_t K) { return fp8q::mx_scale_bytes(rows, K); }
+
+int mx_quantize(const void* x, fp8q_dtype x_dtype, int64_t R, int64_t C, fp8q_fmt fmt, uint8_t* q_r, uint8_t* sf_r,
+                uint8_t* q_c, uint8_t* sf_c, fp8q_stream stream) {
+  if (!al16(x) || R < 128 || C < 128 || R % 128 || C % 128 || R > ((int64_t)1 << 30) || C > ((int64_t)1 << 30))
+    return FP8Q_ERR_INVALID_ARG;
+  if ((x_dtype != FP8Q_BF16 && x_dtype != FP8Q_F32) || (fmt != FP8Q_E4M3 && fmt != FP8Q_E5M2))
+    return FP8Q_ERR_INVALID_ARG;
+  if (!q_r && !q_c) return FP8Q_ERR_INVALID_ARG;
+  if ((q_r && (!al16(q_r) || !al16(sf_r))) || (q_c && (!al16(q_c) || !al16(sf_c)))) return FP8Q_ERR_INVALID_ARG;
+  Ctx c;
+  int e = make_ctx(&c, stream);
+  if (e) return e;
+  FP8Q_STEP(kKMxQuant, launch_mx_quant(x_dtype == FP8Q_BF16 ? kMxInBf16 : kMxInF32, x, nullptr, nullptr, R, C,
+                                       (int)fmt, q_r, q_r ? sf_r : nullptr, q_c, q_c ? sf_c : nullptr, c.L));
+  return finish(c);
+}
+
+int fp8_gemm_mx(fp8q_layout layout, int64_t M, int64_t N, int64_t K, const uint8_t* A, fp8q_fmt fmtA, int64_t lda,
+                const uint8_t* sfA, const uint8_t* B, fp8q_fmt fmtB, int64_t ldb, const uint8_t* sfB, void* C,
+                fp8q_dtype out_dtype, int64_t ldc, const void* residual, int64_t ldr, fp8q_stream stream) {
+  if (M < 1 || N < 1 || K < 128 || K % 128 || M > (1 << 30) || N > (1 << 30) || K > (1 << 30))
+    return FP8Q_ERR_INVALID_ARG;
+  if (!al16(A) || !al16(B) || !al16(C) || !al16(sfA) || !al16(sfB)) return FP8Q_ERR_INVALID_ARG;
+  if ((fmtA != FP8Q_E4M3 && fmtA != FP8Q_E5M2) || (fmtB != FP8Q_E4M3 && fmtB != FP8Q_E5M2))
+    return FP8Q_ERR_INVALID_ARG;
+  if (out_dtype != FP8Q_BF16 && out_dtype != FP8Q_F32) return FP8Q_ERR_INVALID_ARG;
+  if (layout != FP8Q_NN && layout != FP8Q_NT && layout != FP8Q_TN) return FP8Q_ERR_INVALID_ARG;
+  const int a_mn = layout == FP8Q_TN, b_mn = layout != FP8Q_NT;
+  const int64_t a_inner = a_mn ? M : K, b_inner = b_mn ? N : K;
+  if (a_inner % 16 || b_inner % 16 || lda < a_inner || ldb < b_inner || lda % 16 || ldb % 16)
+    return FP8Q_ERR_INVALID_ARG;
+  if (ldc < N || ldc % 8) return FP8Q_ERR_INVALID_ARG;
+  if (residual && (out_dtype != FP8Q_BF16 || !al16(residual) || ldr < N || ldr % 8)) return FP8Q_ERR_INVALID_ARG;
+  Ctx c;
+  int e = make_ctx(&c, stream);
+  if (e) return e;
+  GemmProblem g = mx_gemm(a_mn, b_mn, M, N, K, fp8q_mx_tensor{const_cast<uint8_t*>(A), const_cast<uint8_t*>(sfA)},
+                          (int)fmtA, lda, fp8q_mx_tensor{const_cast<uint8_t*>(B), const_cast<uint8_t*>(sfB)}, (int)fmtB,
+                          ldb, N, residual ? kEpiResidual : kEpiStore, out_dtype == FP8Q_F32, C, ldc);
+  g.R = static_cast<const uint16_t*>(residual);
+  g.ldr = ldr;
+  g.wait_ns = t_gemm_wait_ns;
   int P = 0;
   FP8Q_STEP(kKGemm, launch_gemm(g, &P, c.L));
   return finish(c);

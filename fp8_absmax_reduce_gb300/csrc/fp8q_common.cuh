@@ -254,6 +254,42 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
       ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Block-scaled MXFP8 MMA (kind::mxf8f6f4.block_scale, one E8M0 scale per 32 elements of K):
+// D[tmem] (+)= (A * 2^sfA) (B * 2^sfB) with the scales read from tensor memory at sfa / sfb; the
+// instruction descriptor's scale-factor ids pick the byte of each 32-bit scale word (the K block).
+__device__ __forceinline__ void umma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// Scale-factor ids of the instruction descriptor for the kk-th 32-element K block of a 128-byte
+// stage: the byte of B's scale word (bits 4-5) and of A's (bits 29-30).
+__device__ __forceinline__ uint32_t mx_sf_ids(int kk) { return ((uint32_t)kk << 4) | ((uint32_t)kk << 29); }
+// Copy of a 512-byte scale chunk (32 rows of 16 bytes in shared memory) into tensor memory: 4
+// columns of 32-bit words at taddr, the same 32 rows in each of the four 32-lane quarters, so that
+// quarter q's lane l, column j holds the codes of chunk row 32 j + l.
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+// Shared-memory descriptor of a scale chunk: no swizzle, 8-row core matrices of 16-byte rows, 128
+// bytes apart (the stride between core matrices; one core matrix wide, so the leading offset is
+// never stepped).
+__device__ __forceinline__ uint64_t smem_desc_sf(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(128 >> 4) << 32) |
+         (1ull << 46);
+}
+// 1D bulk copy global -> shared completing on an mbarrier (both addresses 16-byte aligned, bytes a
+// multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(

@@ -38,7 +38,7 @@ namespace fp8q {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;  // BK: bytes of K per stage
+constexpr int BM = 128, BN = 256, BK = 128;  // BK: bytes of K per stage
 constexpr int kATile = BM * BK;   // 16 KB
 constexpr int kBHalf = 128 * BK;  // 16 KB
 constexpr int kStage = kATile + 2 * kBHalf;
@@ -46,10 +46,29 @@ constexpr int kThreads = 384;   // warps 0-3: TMA / MMA / TMEM / idle; warps 4-1
 constexpr int kEpiThreads = 256;
 constexpr int kTmemCols = 512;
 constexpr int kStagingBytes = 4096;                  // per epilogue warp
-constexpr int kStagingOffset = STAGES * kStage;
-constexpr int kBarOffset = kStagingOffset + 8 * kStagingBytes;
-constexpr int kSmemBytes = kBarOffset + 256 + 1024;  // + barriers + alignment slack
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+constexpr int kSfChunk = 512;                        // E8M0 codes of 128 rows x 4 blocks of 32
+
+// Shared-memory and tensor-memory plan of the 128 x 256 kernel.  Per-tensor FP8 and bf16: a 4-stage
+// operand ring and two TMEM accumulators (the epilogue of one tile overlaps the next tile's MMAs).
+// Block-scaled MXFP8 (MX): each stage also carries the stage's scale chunks (A: 128 rows, B: two
+// 128-column halves, 4 blocks of 32 each), which the MMA thread copies into tensor memory next to
+// the accumulator; a 3-stage ring leaves room for them, and one accumulator (TMEM columns 0-255)
+// leaves the columns from 256 for the per-stage scale slots (32 columns each, A and B 16 apart).
+template <int MX>
+struct Plan {
+  static constexpr int kStages = MX ? 3 : 4;
+  static constexpr int kAcc = MX ? 1 : 2;
+  static constexpr int kSfStage = MX ? 3 * kSfChunk : 0;
+  static constexpr int kSfOffset = kStages * kStage;
+  static constexpr int kStagingOffset = kSfOffset + ((kStages * kSfStage + 1023) & ~1023);
+  static constexpr int kBarOffset = kStagingOffset + 8 * kStagingBytes;
+  static constexpr int kSmemBytes = kBarOffset + 256 + 1024;  // + barriers + alignment slack
+  static constexpr int kSfTmemCol = 256;                     // first scale column (MX)
+  static constexpr int kSfTmemStage = 32;                    // A: 4 columns at +0, B: 2 x 4 at +16
+  static constexpr int kSfTmemB = 16;
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+  static_assert(!MX || kSfTmemCol + kStages * kSfTmemStage <= kTmemCols, "tensor memory");
+};
 constexpr int kGroupRows = 2048;                     // rows of A per rasterisation group (the default)
 
 struct Args {
@@ -67,6 +86,11 @@ struct Args {
   const uint16_t* R;
   int64_t ldr;
   uint16_t* aux16;  // kEpiSwiglu: the bf16 SwiGLU output a [M, N] (ld = N), or null
+  const uint8_t* sfA;  // MX: E8M0 scale chunks of A (rows M) and B (rows b_cols), sf_kc chunks per row chunk
+  const uint8_t* sfB;
+  int sf_kc;
+  int b_cols;
+  uint64_t wait_ns;  // limit of every pipeline wait (the drains after a time-out keep kWaitLimitNs)
   const float* qscale;  // kEpiSwiglu: with it, a is written as E4M3 codes fp8(fl32(a * *qscale)) instead
   uint32_t* amax_partial;
   unsigned* status;
@@ -208,18 +232,23 @@ __device__ __forceinline__ void load_h_chunk(const Args& p, int row, int col, in
 // ---------------------------------------------------------------------------
 // Output maps: tmC (C, or the gate half of H / dH), tmC2 (the up half), tmAux
 // (the SwiGLU output a); unused ones are copies of tmC.
-template <int A_MN, int B_MN, int OP16>
+// MX: block-scaled MXFP8 operands (tcgen05.mma kind::mxf8f6f4.block_scale), alpha = 1.
+template <int A_MN, int B_MN, int OP16, int MX>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_f8(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2,
               const __grid_constant__ CUtensorMap tmAux, const Args p) {
+  static_assert(!(MX && OP16), "block scaling takes FP8 operands");
+  using PL = Plan<MX>;
+  constexpr int STAGES = PL::kStages;
+  constexpr int NACC = PL::kAcc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOffset);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + PL::kBarOffset);
   uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;   // [2]
-  uint64_t* tempty = tfull + 2;       // [2]
-  uint64_t* drain = tempty + 2;       // [1]
+  uint64_t* tfull = empty + STAGES;   // [NACC]
+  uint64_t* tempty = tfull + NACC;    // [NACC]
+  uint64_t* drain = tempty + NACC;    // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint32_t* cta_amax = reinterpret_cast<uint32_t*>(tmem_slot + 2);
@@ -230,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int u_step = (int)gridDim.x;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-    for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], kEpiThreads); }
+    for (int a = 0; a < NACC; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], kEpiThreads); }
     mbar_init(drain, 1);
     *abort_flag = 0;
     *cta_amax = 0;
@@ -261,12 +290,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m0 = mb * BM;
         const int n0 = nb * p.b_step, n1 = n0 + p.b_half1;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.wait_ns)) { ok = false; break; }
           uint8_t* sA = smem + stage * kStage;
           uint8_t* sB = sA + kATile;
-          // the whole stage lands here: the A tile and both B halves
-          mbar_arrive_expect_tx(&full[stage], kStage);
+          // the whole stage lands here: the A tile and both B halves (and their scale chunks)
+          mbar_arrive_expect_tx(&full[stage], kStage + PL::kSfStage);
           const int k0 = kb * (OP16 ? BK / 2 : BK);  // in elements
+          if (MX) {
+            // chunk (row chunk, kb) of each operand: A's 128 rows, B's two 128-column halves (a
+            // half past B's columns -- a ragged last tile -- repeats the first: its columns are
+            // zero-filled and never stored)
+            uint8_t* sSF = smem + PL::kSfOffset + stage * PL::kSfStage;
+            const int n1c = n1 < p.b_cols ? n1 : n0;
+            bulk_load(sSF, p.sfA + ((int64_t)(m0 >> 7) * p.sf_kc + kb) * kSfChunk, kSfChunk, &full[stage]);
+            bulk_load(sSF + kSfChunk, p.sfB + ((int64_t)(n0 >> 7) * p.sf_kc + kb) * kSfChunk, kSfChunk, &full[stage]);
+            bulk_load(sSF + 2 * kSfChunk, p.sfB + ((int64_t)(n1c >> 7) * p.sf_kc + kb) * kSfChunk, kSfChunk,
+                      &full[stage]);
+          }
           if (A_MN) {
             if (OP16) {  // two 64-element-wide MN boxes of 64 K rows
               tma_load_2d(sA, &tmA, &full[stage], m0, k0);
@@ -316,14 +356,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int tile = u_first; tile < p.num_tiles && ok; tile += u_step) {
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sA = smem_addr(smem + stage * kStage);
           const uint32_t sB = sA + kATile;
+          // MX: the stage's scale chunks into its tensor-memory slot (A: 4 columns, B: 2 x 4 from
+          // column 16 of the slot, the second half's chunk 4 columns after the first); a
+          // tcgen05.cp and the MMAs issued after it by this thread execute in order.  The slot was
+          // last read by the MMAs of this stage's previous fill, whose commit released the stage
+          // before its refill could complete.
+          const uint32_t t_sfa = tmem_base + (uint32_t)(PL::kSfTmemCol + stage * PL::kSfTmemStage);
+          const uint32_t t_sfb = t_sfa + PL::kSfTmemB;
+          if (MX) {
+            const uint32_t sSF = smem_addr(smem + PL::kSfOffset + stage * PL::kSfStage);
+            tc_cp_sf(t_sfa, smem_desc_sf(sSF));
+            tc_cp_sf(t_sfb, smem_desc_sf(sSF + kSfChunk));
+            tc_cp_sf(t_sfb + 4, smem_desc_sf(sSF + 2 * kSfChunk));
+          }
 #pragma unroll
           for (int kk = 0; kk < BK / 32; ++kk) {
             // One MMA consumes 32 bytes of K (32 FP8 or 16 bf16 elements).  K-major: advance
@@ -334,6 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t ad = A_MN ? smem_desc_sw128(sA + kk * kMnStep, kMnLbo, 1024) : smem_desc_sw128(sA + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? smem_desc_sw128(sB + kk * kMnStep, kMnLbo, 1024) : smem_desc_sw128(sB + kk * 32, 16, 1024);
             if (OP16) umma_bf16(d_tmem, ad, bd, p.idesc, (kb | kk) != 0 ? 1u : 0u);
+            else if (MX) umma_mx(d_tmem, ad, bd, p.idesc | mx_sf_ids(kk), t_sfa, t_sfb, (kb | kk) != 0 ? 1u : 0u);
             else umma_f8(d_tmem, ad, bd, p.idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           umma_commit(&empty[stage]);
@@ -341,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         umma_commit(&tfull[acc]);
-        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
       }
       if (!ok) {
         atomicOr(p.status, kStatusTimeout);
@@ -356,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue ----------------
     const int sub = warp & 3;
     const int half = (warp - 4) >> 2;  // which half of the accumulator columns
-    const uint32_t buf = smem_addr(smem + kStagingOffset + (warp - 4) * kStagingBytes);
+    const uint32_t buf = smem_addr(smem + PL::kStagingOffset + (warp - 4) * kStagingBytes);
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t amax = 0;
@@ -379,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // lane 0 waits and the warp follows its result: the tcgen05.ld below is warp-collective,
       // so a time-out must take the whole warp out together
       int full_ok = 0;
-      if (lane == 0) full_ok = mbar_wait(&tfull[acc], acc_phase, abort_flag) ? 1 : 0;
+      if (lane == 0) full_ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, p.wait_ns) ? 1 : 0;
       if (!__shfl_sync(0xFFFFFFFFu, full_ok, 0)) {
         atomicOr(p.status, kStatusTimeout);
         *abort_flag = 1;
@@ -529,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
     }
     if (lane == 0) bulk_wait_all();  // every TMA store of this warp has completed
     amax = warp_max_u32(amax);
@@ -621,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m0 = mb * 256;
         const int n0 = nb * p.b_step, n1 = n0 + p.b_half1;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.wait_ns)) { ok = false; break; }
           uint8_t* sA = smem + stage * kWideStage;
           uint8_t* sB = sA + 2 * kATile;
           mbar_arrive_expect_tx(&full[stage], kWideStage);
@@ -662,10 +716,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
-        if (!mbar_wait(tempty, acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(tempty, acc_phase ^ 1u, abort_flag, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sA = smem_addr(smem + stage * kWideStage);
           const uint32_t sB = sA + 2 * kATile;
@@ -723,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q = 0; q < 4; ++q) rn[q] = ld_v4(r + 8 * q);
       }
       int full_ok = 0;
-      if (lane == 0) full_ok = mbar_wait(tfull, acc_phase, abort_flag) ? 1 : 0;
+      if (lane == 0) full_ok = mbar_wait(tfull, acc_phase, abort_flag, p.wait_ns) ? 1 : 0;
       if (!__shfl_sync(0xFFFFFFFFu, full_ok, 0)) {
         atomicOr(p.status, kStatusTimeout);
         *abort_flag = 1;
@@ -861,27 +915,34 @@ uint32_t make_idesc(int fmtA, int fmtB, int a_mn, int b_mn) {
   return (1u << 4) | ((uint32_t)fmtA << 7) | ((uint32_t)fmtB << 10) | ((uint32_t)a_mn << 15) |
          ((uint32_t)b_mn << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
+// Instruction descriptor for kind::mxf8f6f4.block_scale: A/B formats, major-ness, N >> 3, M >> 4 as
+// above; bit 23 = the scale type E8M0; the accumulator is fp32 by definition, and bits 4-5 / 29-30
+// are the per-MMA scale-factor ids (mx_sf_ids), left zero here.
+uint32_t make_idesc_mx(int fmtA, int fmtB, int a_mn, int b_mn) {
+  return ((uint32_t)fmtA << 7) | ((uint32_t)fmtB << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(BN >> 3) << 17) | (1u << 23) | ((uint32_t)(BM >> 4) << 24);
+}
 
-template <int A_MN, int B_MN, int OP16>
+template <int A_MN, int B_MN, int OP16, int MX>
 cudaError_t configure_t() {
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_f8<A_MN, B_MN, OP16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_f8<A_MN, B_MN, OP16, MX>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Plan<MX>::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   return cudaSuccess;
 }
 
-template <int A_MN, int B_MN, int OP16>
+template <int A_MN, int B_MN, int OP16, int MX = 0>
 cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tc2,
                      const CUtensorMap& taux, const Args& a, int grid, cudaStream_t s) {
-  cudaError_t e = configure_t<A_MN, B_MN, OP16>();
+  cudaError_t e = configure_t<A_MN, B_MN, OP16, MX>();
   if (e != cudaSuccess) return e;
-  k_gemm_f8<A_MN, B_MN, OP16><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, tc, tc2, taux, a);
+  k_gemm_f8<A_MN, B_MN, OP16, MX><<<grid, kThreads, Plan<MX>::kSmemBytes, s>>>(ta, tb, tc, tc2, taux, a);
   return cudaGetLastError();
 }
 
@@ -936,7 +997,17 @@ cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L) {
   a.qscale = g.op16 ? nullptr : g.qscale;
   a.amax_partial = g.amax_partial;
   a.status = L.status;
-  a.idesc = g.op16 ? make_idesc(1, 1, g.a_mn, g.b_mn) : make_idesc(g.fmtA, g.fmtB, g.a_mn, g.b_mn);
+  a.idesc = g.op16 ? make_idesc(1, 1, g.a_mn, g.b_mn)
+                   : (g.mx ? make_idesc_mx(g.fmtA, g.fmtB, g.a_mn, g.b_mn) : make_idesc(g.fmtA, g.fmtB, g.a_mn, g.b_mn));
+  if (g.mx) {
+    if (g.op16 || g.K % 128 != 0 || !g.sfA || !g.sfB) return cudaErrorInvalidValue;
+    a.sinvA = a.sinvB = nullptr;  // alpha = 1: the block scales are part of the operands
+    a.sfA = g.sfA;
+    a.sfB = g.sfB;
+    a.sf_kc = g.K / 128;
+  }
+  a.b_cols = (int)g.b_cols;
+  a.wait_ns = g.wait_ns ? g.wait_ns : kWaitLimitNs;
   a.m_tiles = (g.M + BM - 1) / BM;
   if (g.epi == kEpiSwiglu) {
     a.n_tiles = (g.N + 127) / 128;  // 128 gate + the matching 128 up columns per tile
@@ -972,7 +1043,7 @@ cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L) {
   if (!ok_a || !ok_b || !ok_c) return cudaErrorInvalidValue;
 
   // long-K FP8 GEMMs with plain epilogues take the 256 x 256 tile
-  const bool wide = !g.op16 && (g.epi == kEpiStore || g.epi == kEpiResidual) && g.K >= kWideMinK && g.M >= 256 &&
+  const bool wide = !g.op16 && !g.mx && (g.epi == kEpiStore || g.epi == kEpiResidual) && g.K >= kWideMinK && g.M >= 256 &&
                     wide_pays(g.M, a.n_tiles, g.K, L.num_sms);
   if (wide) {
     a.m_tiles = (g.M + 255) / 256;
@@ -994,7 +1065,12 @@ cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L) {
     if (L.launches) ++*L.launches;
     return e;
   }
-  if (g.op16) {  // the three layouts of the block (NN, NT, TN)
+  if (g.mx) {  // the three layouts of the block (NN, NT, TN)
+    if (g.a_mn == 0 && g.b_mn == 1) e = launch_t<0, 1, 0, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
+    else if (g.a_mn == 0 && g.b_mn == 0) e = launch_t<0, 0, 0, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
+    else if (g.a_mn == 1 && g.b_mn == 1) e = launch_t<1, 1, 0, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
+    else return cudaErrorInvalidValue;
+  } else if (g.op16) {  // the three layouts of the block (NN, NT, TN)
     if (g.a_mn == 0 && g.b_mn == 1) e = launch_t<0, 1, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
     else if (g.a_mn == 0 && g.b_mn == 0) e = launch_t<0, 0, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);
     else if (g.a_mn == 1 && g.b_mn == 1) e = launch_t<1, 1, 1>(ta, tb, tc, tc2, taux, a, grid, L.stream);

@@ -68,6 +68,17 @@ cudaError_t launch_attn_bwd_dq(const uint16_t* qkv, const uint16_t* datt, int64_
 // Diagnostics: a bounded wait that is made to run out (see fp8q_selftest_bounded_wait).
 cudaError_t launch_selftest_bounded_wait(uint64_t limit_ns, const Launch& L);
 
+// Block-scaled (MXFP8) quantization of a [R, C] tensor, R and C multiples of 128, in one pass:
+// q_r/sf_r (blocks of 32 along each row; the operand of a GEMM contracting over C) and/or
+// q_c/sf_c (blocks of 32 down each column; contracting over R); either pair may be null.  Inputs:
+// kMxInBf16 / kMxInF32 x [R, C]; kMxInSwiglu: bf16 H [R, 2C] (gate | up) -> a = SwiGLU(H);
+// kMxInRmsnorm: bf16 x [R, C] with gain g [C] and rstd [R] -> n = fl32(fl32(x rstd) g).
+// Scale codes go to the chunked layout the block-scaled GEMM reads (mx_scale_bytes bytes).
+enum MxIn { kMxInBf16 = 0, kMxInF32 = 1, kMxInSwiglu = 2, kMxInRmsnorm = 3 };
+size_t mx_scale_bytes(int64_t rows, int64_t K);
+cudaError_t launch_mx_quant(int in_kind, const void* x, const uint16_t* g, const float* rstd, int64_t R, int64_t C,
+                            int fmt, uint8_t* q_r, uint8_t* sf_r, uint8_t* q_c, uint8_t* sf_c, const Launch& L);
+
 // Bookkeeping of the C ABI for entry points implemented outside fp8q_api.cu: the trace bracket
 // of one kernel step (an NVTX range, and CUDA events while the kernel trace is on) and the count
 // that fp8q_last_launch_count() reports.
@@ -101,6 +112,13 @@ struct GemmProblem {
   uint32_t* amax_partial;          // per-CTA partials for the two SwiGLU epilogues
   int op16;                        // 1: bf16 operands (lda/ldb in elements), no scales (alpha = 1)
   uint16_t* a16;                   // op16 with kEpiSwiglu: bf16 SwiGLU output a [M, N]
+  // Block-scaled MXFP8 (mx = 1): sinvA/sinvB unused (alpha = 1); sfA / sfB hold the E8M0 codes of
+  // A (rows M) and B (rows b_cols) in the chunked layout of launch_mx_quant; K a multiple of 128.
+  int mx;
+  const uint8_t* sfA; const uint8_t* sfB;
+  // Limit of the kernel's pipeline waits in ns (0: the default 2 s).  Only the GEMM self test sets
+  // it, to a few microseconds, so that ordinary waits give up and the abort sequence runs.
+  uint64_t wait_ns;
 };
 // Launches the persistent tcgen05 GEMM; *P receives the number of partials written.
 cudaError_t launch_gemm(const GemmProblem& g, int* P, const Launch& L);

@@ -157,6 +157,57 @@ FP8Q_API int swiglu_quant(const void* H, int64_t T, int64_t f, fp8q_fmt fmt, uin
                  void* ws, size_t ws_bytes, fp8q_stream stream);
 
 /* ------------------------------------------------------------------------ */
+/* Block-scaled MXFP8 (LLMQ §2: inner-dimension block scaling, which the    */
+/* Blackwell tensor cores support natively).                                */
+/* ------------------------------------------------------------------------ */
+/* Format (OCP Microscaling): 32 consecutive elements along a GEMM's
+ * contraction dimension share one scale 2^X, stored as the E8M0 code X + 127
+ * (0xFF = NaN); the elements are E4M3 or E5M2 codes worth decode(code) * 2^X.
+ * Scale rule (the per-tensor rule's "no clipping", per block): X is the
+ * smallest integer with amax_block <= fmt_max * 2^X, clamped to [-127, 127];
+ * an all-zero block has X = -127 (code 0); code = fp8_rne_satfinite(fl32(v *
+ * 2^-X)).  A block holding NaN or Inf gets scale code 0xFF, element codes 0x7F
+ * and sets FP8Q_STATUS_NONFINITE.
+ *
+ * Scale layout ("chunked"): an operand with `rows` rows along M (or N) and
+ * contraction length K keeps its codes in 512-byte chunks, one per 128 rows x
+ * 128 K (4 blocks), chunk (i, j) at byte (i * ceil(K/128) + j) * 512; row r,
+ * block b of a chunk at byte (r % 32) * 16 + (r / 32) * 4 + b.  This is the
+ * order in which the GEMM copies scales into tensor memory.  mx_scale_bytes
+ * returns the size. */
+FP8Q_API size_t mx_scale_bytes(int64_t rows, int64_t K);
+
+/* x [R,C] (bf16 or fp32) -> in one pass, either or both of
+ *   q_r [R,C] codes + sf_r: blocks of 32 consecutive columns of a row -- x as
+ *     a GEMM operand contracted over its columns (K = C, rows = R);
+ *   q_c [R,C] codes + sf_c: blocks of 32 consecutive rows of a column -- x as
+ *     an operand contracted over its rows (K = R, rows = C).
+ * Either pair may be NULL (not both).  Requirements: R, C multiples of 128;
+ * 16-byte aligned pointers; sf_r holds mx_scale_bytes(R, C) bytes, sf_c
+ * mx_scale_bytes(C, R).  Deterministic, no workspace. */
+FP8Q_API int mx_quantize(const void* x, fp8q_dtype x_dtype, int64_t R, int64_t C, fp8q_fmt fmt, uint8_t* q_r,
+                         uint8_t* sf_r, uint8_t* q_c, uint8_t* sf_c, fp8q_stream stream);
+
+/* Block-scaled GEMM C = op(A) op(B) (+ residual) on the tcgen05 tensor cores
+ * (kind::mxf8f6f4.block_scale, fp32 accumulation; no per-tensor alpha).
+ * Layouts and leading dimensions as fp8_gemm_scaled.  sfA: the chunked
+ * scales of A as an operand with M rows and contraction K (for NN / NT that is
+ * mx_quantize's sf_r of A [M,K]; for TN, sf_c of A [K,M]); sfB likewise with N
+ * rows (NN / TN: sf_c of B [K,N]; NT: sf_r of B [N,K]).  Requirements: K a
+ * multiple of 128; M, N >= 1 as fp8_gemm_scaled; scales of rows past M (N) in
+ * the last chunk are read but do not reach C. */
+FP8Q_API int fp8_gemm_mx(fp8q_layout layout, int64_t M, int64_t N, int64_t K, const uint8_t* A, fp8q_fmt fmtA,
+                         int64_t lda, const uint8_t* sfA, const uint8_t* B, fp8q_fmt fmtB, int64_t ldb,
+                         const uint8_t* sfB, void* C, fp8q_dtype out_dtype, int64_t ldc, const void* residual,
+                         int64_t ldr, fp8q_stream stream);
+
+/* One block-scaled operand: codes and chunked scales. */
+typedef struct fp8q_mx_tensor {
+  uint8_t* q;
+  uint8_t* sf;
+} fp8q_mx_tensor;
+
+/* ------------------------------------------------------------------------ */
 /* The MLP block, forward and backward (bias-free SwiGLU MLP with RMSNorm   */
 /* and bf16 residual; E4M3 activations/weights, E5M2 gradients).            */
 /* ------------------------------------------------------------------------ */
@@ -222,7 +273,36 @@ typedef struct fp8q_mlp {
   int bf16;
   void* n16;        /* [T,d]  bf16 normalized input (bf16 != 0) */
   void* a16;        /* [T,f]  bf16 SwiGLU output (bf16 != 0) */
+  /* Non-null: the block-scaled MXFP8 block (LLMQ §2: inner-dimension block
+   * scaling, native on Blackwell); see fp8q_mlp_mx below.  W_gu8, W_d8, n8,
+   * a8, dY8, dH8 and scal are then neither read nor written (may be NULL). */
+  const struct fp8q_mlp_mx* mx;
 } fp8q_mlp;
+
+/* The MXFP8 block (fp8q_mlp.mx).  The same steps as the per-tensor block with
+ * every quantization block-scaled along the contraction dimension of the GEMM
+ * that reads it, so a tensor two GEMMs contract differently is quantized both
+ * ways (one mx_quantize pass each; "_r" = blocks along a row, "_c" = down a
+ * column); the GEMMs take no alpha:
+ *   H = bf16(n_r @ W_gu_c),  a = SwiGLU(H),  y = bf16(x + a_r @ W_d_c);
+ *   dA = dY_r @ W_d_r^T,  dH = bf16(SwiGLU'(H) dA),  dW_d = a_c^T @ dY_c,
+ *   dN = dH_r @ W_gu_r^T,  dW_gu = n_c^T @ dH_c,  dX, dg as before.
+ * n = fl32(fl32(x rstd) g) with the per-tensor block's rstd.  Gradients
+ * (dY, dH) are E5M2 (E4M3 with grad_e4m3).  Every tensor here is caller
+ * memory: codes like the tensor they encode, scales in the chunked layout
+ * (sf of an "_r" tensor [R,C]: mx_scale_bytes(R, C); "_c": mx_scale_bytes(C, R)).
+ * The forward writes W_gu_*, W_d_*, n_*, a_*, which the backward reads; the
+ * backward writes dY_*, dH_*.  Requirements: T, d, f multiples of 128; not
+ * combinable with recompute or bf16 (FP8Q_ERR_UNSUPPORTED); the workspace is
+ * mlp_block_workspace_size's. */
+typedef struct fp8q_mlp_mx {
+  fp8q_mx_tensor W_gu_r, W_gu_c; /* [d,2f] E4M3 */
+  fp8q_mx_tensor W_d_r, W_d_c;   /* [f,d]  E4M3 */
+  fp8q_mx_tensor n_r, n_c;       /* [T,d]  E4M3 */
+  fp8q_mx_tensor a_r, a_c;       /* [T,f]  E4M3 */
+  fp8q_mx_tensor dY_r, dY_c;     /* [T,d]  E5M2 (E4M3 with grad_e4m3) */
+  fp8q_mx_tensor dH_r, dH_c;     /* [T,2f] E5M2 (E4M3 with grad_e4m3) */
+} fp8q_mlp_mx;
 
 /* backward != 0 sizes the workspace for mlp_block_bwd (which also suffices for mlp_block_fwd). */
 FP8Q_API size_t mlp_block_workspace_size(int64_t T, int64_t d, int64_t f, int backward);
@@ -412,6 +492,21 @@ FP8Q_API int fp8q_last_launch_count(void);
  * the kernel sets FP8Q_STATUS_TIMEOUT and returns; the context stays usable.
  * Returns FP8Q_OK once enqueued. */
 FP8Q_API int fp8q_selftest_bounded_wait(int64_t limit_ns, fp8q_stream stream);
+
+/* Diagnostics for the GEMM's abort sequence (no page counterpart): the same
+ * launch as fp8_gemm_scaled (mx == 0) or fp8_gemm_mx (mx != 0; sfA, sfB as
+ * there, sinvA, sinvB unused), except that every pipeline wait of the kernel
+ * (stage ring, accumulator hand-off) gives up after limit_ns (1 us .. 10 s)
+ * instead of 2 s.  With a limit of a few microseconds ordinary waits run out:
+ * the CTA records FP8Q_STATUS_TIMEOUT, stops issuing, waits (with the full
+ * 2 s limit) for the copies and MMAs it issued, frees its tensor memory and
+ * exits; C is then incomplete and the context stays usable.  Returns FP8Q_OK
+ * once enqueued (synchronous errors as the GEMM entry points). */
+FP8Q_API int fp8q_selftest_gemm_wait_limit(fp8q_layout layout, int64_t M, int64_t N, int64_t K, const uint8_t* A,
+                                           fp8q_fmt fmtA, int64_t lda, const uint8_t* B, fp8q_fmt fmtB, int64_t ldb,
+                                           const float* sinvA, const float* sinvB, int mx, const uint8_t* sfA,
+                                           const uint8_t* sfB, void* C, fp8q_dtype out_dtype, int64_t ldc,
+                                           int64_t limit_ns, fp8q_stream stream);
 
 /* Kernel-level timing for benchmarks.  While tracing is on for the calling
  * host thread, each kernel step the library enqueues is bracketed by two CUDA

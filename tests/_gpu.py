@@ -63,3 +63,25 @@ def fp8_table(fmt: int) -> np.ndarray:
 def bf16_np(t: torch.Tensor) -> np.ndarray:
     """CUDA bf16 tensor -> float64 values."""
     return host_f64(t)
+
+
+def _mx_offsets(rows: int, nb: int) -> np.ndarray:
+    """Byte offsets of (row r, K block b) in the chunked scale layout of include/fp8q.h: 512-byte
+    chunks of 128 rows x 4 blocks, row-chunk-major; inside a chunk (r % 32) * 16 + (r / 32) * 4 + b."""
+    nkc = (nb + 3) // 4
+    r = np.arange(rows)[:, None]
+    b = np.arange(nb)[None, :]
+    return ((r // 128) * nkc + b // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + b % 4
+
+
+def mx_sf_to_chunked(plain: np.ndarray) -> np.ndarray:
+    """Scale codes [rows, K/32] -> the chunked byte layout (padding rows / blocks hold 127, i.e. 1.0)."""
+    rows, nb = plain.shape
+    out = np.full(((rows + 127) // 128) * ((nb + 3) // 4) * 512, 127, dtype=np.uint8)
+    out[_mx_offsets(rows, nb)] = plain
+    return out
+
+
+def mx_sf_from_chunked(chunked: np.ndarray, rows: int, K: int) -> np.ndarray:
+    """The chunked layout -> scale codes [rows, K/32]."""
+    return np.asarray(chunked).ravel()[_mx_offsets(rows, (K + 31) // 32)]
