@@ -63,6 +63,8 @@ def parse_args():
                     help="E4M3 gradients (dY, dH; dh, dQKV in the full block) instead of E5M2")
     ap.add_argument("--bf16", action="store_true",
                     help="the BF16 baseline (same block, bf16 operands, tcgen05 kind::f16) for the FP8/BF16 speedup")
+    ap.add_argument("--mxfp8", action="store_true",
+                    help="the block-scaled MXFP8 MLP block (E8M0 scale per 32 elements, tcgen05 block_scale GEMMs)")
     ap.add_argument("--measure-fp8-peak", action="store_true",
                     help="time cuBLASLt FP8 (torch._scaled_mm) 8192^3, burst and sustained, and exit")
     ap.add_argument("--tokens", type=int, default=0,
@@ -158,10 +160,31 @@ def job_throughput(units_per_rank: float, world: int, max_ms: float) -> float:
 # ---------------------------------------------------------------------------
 # per-launch algorithmic work of one step (order = the library's launch order)
 # ---------------------------------------------------------------------------
-def step_work(w: synth.Workload, recompute: bool = False, bf16: bool = False):
+def step_work(w: synth.Workload, recompute: bool = False, bf16: bool = False, mx: bool = False):
     """(kernel kind, algorithmic bytes, flops) of every traced launch of one step (the recompute
     GEMM's flops are executed work on top of the algorithmic 18Tdf)."""
     T, d, f = w.T, w.d, w.f
+    if mx:  # the MXFP8 MLP block: each quantizer pass reads its input once and writes both code
+        # tensors (2 B per element) and both scale sets (2 / 32 B per element)
+        q = lambda n, rd: ("mx_quant", n * (rd + 2 + 2 / 32), 0)
+        sf = lambda n: n / 32   # scale bytes of one operand
+        fwd = [
+            q(d * 2 * f, 2), q(f * d, 2),
+            ("rmsnorm_stats", 2 * T * d + 2 * d + 4 * T, 0), ("mx_quant", T * d * (2 + 2 + 2 / 32) + 4 * T + 2 * d, 0),
+            ("gemm_gate_up_swiglu", T * d + d * 2 * f + sf(T * d) + sf(d * 2 * f) + 2 * T * 2 * f, 2.0 * T * d * 2 * f),
+            q(T * f, 4),
+            ("gemm_down_residual", T * f + f * d + sf(T * f) + sf(f * d) + 4 * T * d, 2.0 * T * f * d),
+        ]
+        bwd = [
+            q(T * d, 2),
+            ("gemm_down_dgrad_swiglu_bwd", T * d + f * d + sf(T * d) + sf(f * d) + 2 * T * 2 * f * 2, 2.0 * T * d * f),
+            q(T * 2 * f, 2),
+            ("gemm_down_wgrad", T * f + T * d + sf(T * f) + sf(T * d) + 4 * f * d, 2.0 * f * T * d),
+            ("gemm_gate_up_dgrad", T * 2 * f + d * 2 * f + sf(T * 2 * f) + sf(d * 2 * f) + 4 * T * d, 2.0 * T * 2 * f * d),
+            ("gemm_gate_up_wgrad", T * d + T * 2 * f + sf(T * d) + sf(T * 2 * f) + 4 * d * 2 * f, 2.0 * d * T * 2 * f),
+            ("rmsnorm_bwd", 10 * T * d, 0),
+        ]
+        return fwd + (bwd if w.backward else [])
     if bf16:  # the BF16 baseline: 2-byte operands, no casts
         fwd = [
             ("rmsnorm_bf16", 4 * T * d + 2 * d + 4 * T, 0),
@@ -281,7 +304,7 @@ def run_ours(args, rank, world, local_rank):
         fwd, bwd = fq.block_fwd, fq.block_bwd
     else:
         inp = synth.mlp_inputs(w, seed=rank)
-        b = fq.MlpBuffers.allocate(w.T, w.d, w.f, device=dev, backward=w.backward, bf16=args.bf16)
+        b = fq.MlpBuffers.allocate(w.T, w.d, w.f, device=dev, backward=w.backward, bf16=args.bf16, mx=args.mxfp8)
         dev_in = {k: getattr(b, k) for k in ["x", "g", "W_gu", "W_d"] + (["dY"] if w.backward else [])}
         dev_out = {"y": b.y}
         if w.backward:
@@ -313,7 +336,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
 
     K = args.steps
-    plan = step_work(w, args.recompute, args.bf16)
+    plan = step_work(w, args.recompute, args.bf16, args.mxfp8)
     if lib.fp8q_trace_start(K * len(plan)) != 0:
         raise RuntimeError("fp8q_trace_start failed")
     launches = 0
@@ -385,7 +408,8 @@ def run_ours(args, rank, world, local_rank):
             state = ("g1", "W_qkv", "W_o", "g", "W_gu", "W_d") + (
                 ("dW_qkv", "dW_o", "dg1", "dW_gu", "dW_d", "dg") if w.backward else ())
         else:
-            b2 = fq.MlpBuffers.allocate(w.T, w.d, w.f, device=dev, backward=w.backward, bf16=args.bf16)
+            b2 = fq.MlpBuffers.allocate(w.T, w.d, w.f, device=dev, backward=w.backward, bf16=args.bf16,
+                                        mx=args.mxfp8)
             if w.backward:
                 run, run_name = (lambda bb, steps: fq.mlp_block_run_steps(bb[0], bb[1], steps)), "mlp_block_run_steps"
             else:
@@ -501,7 +525,11 @@ def kernel_table(traced, plan, K, pk):
     return out, total
 
 
-def cpu_baseline(w, tokens, grad_e4m3=False, bf16=False):
+def precision_name(args) -> str:
+    return "bf16 baseline" if args.bf16 else ("mxfp8 (block-scaled)" if args.mxfp8 else "fp8")
+
+
+def cpu_baseline(w, tokens, grad_e4m3=False, bf16=False, mx=False):
     import oracle
     oracle.build()
     gf = oracle.E4M3 if grad_e4m3 else oracle.E5M2
@@ -520,7 +548,7 @@ def cpu_baseline(w, tokens, grad_e4m3=False, bf16=False):
         x = inp["x"][:tokens]
         dY = inp["dY"][:tokens] if w.backward else None
         t0 = time.perf_counter()
-        oracle.block(x, inp["g"], inp["W_gu"], inp["W_d"], dY=dY, nthreads=1, grad_fmt=gf, bf16=bf16)
+        oracle.block(x, inp["g"], inp["W_gu"], inp["W_d"], dY=dY, nthreads=1, grad_fmt=gf, bf16=bf16, mx=mx)
         dt = time.perf_counter() - t0
     import dataclasses
     sub = dataclasses.replace(w, T=tokens, seq_len=tokens if w.n_heads else 0)
@@ -582,6 +610,8 @@ def main():
         w = dataclasses.replace(w, T=args.tokens)
     if args.bf16 and (args.recompute or args.grad_e4m3):
         raise SystemExit("--bf16: without --recompute / --grad-e4m3")
+    if args.mxfp8 and (args.bf16 or args.recompute or w.qkv):
+        raise SystemExit("--mxfp8: an MLP workload, without --bf16 / --recompute")
     pk = peaks()
 
     if args.impl == "reference":
@@ -589,9 +619,9 @@ def main():
             return
         tokens = 2
         for _ in range(args.warmup):
-            cpu_baseline(w, tokens, args.grad_e4m3, args.bf16)
+            cpu_baseline(w, tokens, args.grad_e4m3, args.bf16, args.mxfp8)
         t0 = time.perf_counter()
-        res = [cpu_baseline(w, tokens, args.grad_e4m3, args.bf16) for _ in range(args.steps)]
+        res = [cpu_baseline(w, tokens, args.grad_e4m3, args.bf16, args.mxfp8) for _ in range(args.steps)]
         dt = time.perf_counter() - t0
         import dataclasses
         sub = dataclasses.replace(w, T=tokens, seq_len=tokens if w.n_heads else 0)
@@ -603,7 +633,7 @@ def main():
                 "data": "synthetic (seeded Philox, bf16)",
                 "config": {"workload": w.name, "T": w.T, "d": w.d, "f": w.f,
                            "gradients": "e4m3" if args.grad_e4m3 else "e5m2",
-                           "precision": "bf16 baseline" if args.bf16 else "fp8"},
+                           "precision": precision_name(args)},
                 "cpu_baseline": {"kind": "oracle", "cores": 1, "value": value, "unit": "TFLOP/s",
                                  "sample": res[0]["sample"]},
                 "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -640,13 +670,15 @@ def main():
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": r["K"],
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16 (bf16 operands, fp32 accumulation)" if args.bf16 else "fp8 (e4m3/e5m2 operands, fp32 accumulation)",
+        "dtype": ("bf16 (bf16 operands, fp32 accumulation)" if args.bf16 else
+                  "mxfp8 (e4m3/e5m2 operands with e8m0 scales per 32 elements, fp32 accumulation)" if args.mxfp8 else
+                  "fp8 (e4m3/e5m2 operands, fp32 accumulation)"),
         "data": "synthetic (seeded Philox, bf16 inputs)",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "f": w.f, "gemm_flops_per_step": w.gemm_flops(),
                    "attention_flops_per_step": w.attention_flops(),
                    "backward": "recompute H and a8 from n8 with the retained scale" if args.recompute else "stored H and a8",
                    "gradients": "bf16" if args.bf16 else ("e4m3" if args.grad_e4m3 else "e5m2"),
-                   "precision": "bf16 baseline" if args.bf16 else "fp8",
+                   "precision": precision_name(args),
                    "l2": (f"L2 flushed between steps (a 256 MB write outside the timed spans; bf16 weights "
                           f"{weight_bytes(w) / 1e6:.0f} MB)" if flush_l2(w) else
                           f"inputs larger than L2 (bf16 weights {weight_bytes(w) / 1e6:.0f} MB read per step), no flush"),
@@ -671,7 +703,7 @@ def main():
     if r["graph"]:
         line["graph_replay"] = r["graph"]
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, args.cpu_sample_tokens, args.grad_e4m3, args.bf16)
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_sample_tokens, args.grad_e4m3, args.bf16, args.mxfp8)
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -3,7 +3,8 @@ its algorithmic bytes and FLOPs, from which the bench derives the roofline and t
 table, so it must stay in step with the library and the workloads.
   * every plan entry names a kernel kind the library's trace reports;
   * the GEMM FLOPs of a step add up to the workload's algorithmic count (6Tdf forward, 18Tdf
-    forward + backward, plus the QKV and O projections), in every precision mode; the recompute
+    forward + backward, plus the QKV and O projections), in every precision mode (per-tensor FP8,
+    BF16, block-scaled MXFP8 for the MLP workloads); the recompute
     mode adds exactly one gate/up GEMM of executed work;
   * the attention kernels' executed FLOPs are 18 products per causal pair and head against the
     algorithmic 14 (the backward kernels recompute S and dP), 128 x 2 FLOPs each.
@@ -36,6 +37,8 @@ def modes(w):
     if w.backward:
         out += [dict(recompute=True)]
     out += [dict(bf16=True)]
+    if not w.qkv:
+        out += [dict(mx=True)]
     return out
 
 
