@@ -496,8 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bulk_commit();
               }
             }
-          } else {
-            // only the absmax of a (the cast pass recomputes a from the stored H)
+          } else if (p.amax_partial) {
+            // only the absmax of a (the cast pass recomputes a from the stored H); the block-scaled
+            // path has no per-tensor scale and skips it
 #pragma unroll
             for (int j = 0; j < 32; ++j)
               if (row_ok && j < ncol) amax = max(amax, abs_bits(swiglu_fast(hg[j], hu[j])));
