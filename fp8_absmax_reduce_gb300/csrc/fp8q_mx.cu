@@ -23,10 +23,12 @@
 // row-chunk-major order; inside a chunk, row r and block b of the chunk sit at
 // byte (r % 32) * 16 + (r / 32) * 4 + b.
 //
-// CTA tile: 32 rows x 128 columns, 256 threads; thread t holds row t / 8 and
-// the 16 columns 16 (t % 8) ..; a row block is a lane pair, a column block the
-// 32 rows of the tile (warp shuffles over the warp's 4 rows, then shared
-// memory over the 8 warps).
+// CTA tile: 32 rows x 128 columns, 256 threads; each thread holds 8 columns of
+// two rows, and a warp's load reads two whole 128-column row segments
+// (coalesced); a row block is 4 consecutive lanes, a column block the tile's 32
+// rows (a warp shuffle over its 4 rows, then shared memory over the 8 warps).
+// Each thread loads its next tile's inputs before it reduces and writes the
+// current one, so the loads stay in flight across the tile's barriers.
 #include "fp8q_common.cuh"
 #include "fp8q_internal.h"
 
@@ -74,17 +76,6 @@ __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t k, int64_t n_kch
   return ((r >> 7) * n_kchunks + (k >> 7)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + ((k >> 5) & 3);
 }
 
-// 16 codes of v * s (s = 2^-X) packed in a uint4.
-template <int FMT>
-__device__ __forceinline__ uint4 codes16(const float (&v)[16], float s) {
-  uint32_t w[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    w[q] = cvt_fp8x4<FMT>(__fmul_rn(v[4 * q], s), __fmul_rn(v[4 * q + 1], s), __fmul_rn(v[4 * q + 2], s),
-                          __fmul_rn(v[4 * q + 3], s));
-  return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
 struct MxArgs {
   const void* x;        // IN 0: bf16 [R, C]; 1: fp32 [R, C]; 2: bf16 H [R, 2C]; 3: bf16 x [R, C]
   const uint16_t* g;    // IN 3: RMSNorm gain [C]
@@ -95,141 +86,185 @@ struct MxArgs {
   unsigned* status;
 };
 
-// The 16 input values of (row, columns c .. c + 15): the tensor itself, SwiGLU of [gate | up]
-// (swiglu_fast, as the fused forward's a), or the RMSNorm output fl32(fl32(x rstd) g).
+// Thread layout of a 32 x 128 tile: warp w, lane l holds rows 2 (w + 8 k) + (l / 16), k = 0, 1, and
+// the 8 columns 8 (l % 16) ..; a warp's load instruction reads two whole 128-column row segments.
+__device__ __forceinline__ int tile_row(int warp, int lane, int k) { return 2 * (warp + 8 * k) + (lane >> 4); }
+
+// The raw words of one thread's inputs (8 columns of one row), loaded one tile ahead of their use:
+// bf16 x (1 vector), fp32 x (2), bf16 gate and up of H (1 + 1), bf16 x of the RMSNorm (1).
+struct Raw {
+  uint4 w[2][2];  // [row k][vector]
+};
+
 template <int IN>
-__device__ __forceinline__ void load16(const MxArgs& p, int64_t row, int64_t c, float (&v)[16]) {
-  if (IN == 1) {
-    const float* xr = static_cast<const float*>(p.x) + row * p.C + c;
+__device__ __forceinline__ uint4 raw_vec(const MxArgs& p, int64_t row, int64_t c, int i) {
+  if (IN == 1) return ld_nc_v4(static_cast<const float*>(p.x) + row * p.C + c + 4 * i);
+  const int64_t ld = IN == 2 ? 2 * p.C : p.C;
+  return ld_nc_v4(static_cast<const uint16_t*>(p.x) + row * ld + c + (i ? p.C : 0));
+}
+
+template <int IN>
+__device__ __forceinline__ Raw load_raw(const MxArgs& p, int64_t r0, int64_t c, int warp, int lane) {
+  Raw r;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 w = ld_nc_v4(xr + 4 * q);
-      v[4 * q] = __uint_as_float(w.x); v[4 * q + 1] = __uint_as_float(w.y);
-      v[4 * q + 2] = __uint_as_float(w.z); v[4 * q + 3] = __uint_as_float(w.w);
-    }
+  for (int k = 0; k < 2; ++k) {
+    const int64_t row = r0 + tile_row(warp, lane, k);
+    r.w[k][0] = raw_vec<IN>(p, row, c, 0);
+    if (IN == 1 || IN == 2) r.w[k][1] = raw_vec<IN>(p, row, c, 1);
+  }
+  return r;
+}
+
+// The 8 input values of one row: the tensor itself, SwiGLU of [gate | up] (swiglu_fast, as the
+// fused forward's a), or the RMSNorm output fl32(fl32(x rstd) g).
+template <int IN>
+__device__ __forceinline__ void decode8(const uint4 (&w)[2], const MxArgs& p, int64_t row, int64_t c, float (&v)[8]) {
+  if (IN == 1) {
+    v[0] = __uint_as_float(w[0].x); v[1] = __uint_as_float(w[0].y);
+    v[2] = __uint_as_float(w[0].z); v[3] = __uint_as_float(w[0].w);
+    v[4] = __uint_as_float(w[1].x); v[5] = __uint_as_float(w[1].y);
+    v[6] = __uint_as_float(w[1].z); v[7] = __uint_as_float(w[1].w);
     return;
   }
-  const int64_t ld = IN == 2 ? 2 * p.C : p.C;
-  const uint16_t* xr = static_cast<const uint16_t*>(p.x) + row * ld + c;
-  uint32_t xw[8];
-  {
-    const uint4 a = ld_nc_v4(xr), b = ld_nc_v4(xr + 8);
-    xw[0] = a.x; xw[1] = a.y; xw[2] = a.z; xw[3] = a.w; xw[4] = b.x; xw[5] = b.y; xw[6] = b.z; xw[7] = b.w;
-  }
+  const uint32_t xw[4] = {w[0].x, w[0].y, w[0].z, w[0].w};
   if (IN == 0) {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) { v[2 * k] = bf16_lo(xw[k]); v[2 * k + 1] = bf16_hi(xw[k]); }
+    for (int k = 0; k < 4; ++k) { v[2 * k] = bf16_lo(xw[k]); v[2 * k + 1] = bf16_hi(xw[k]); }
   } else if (IN == 2) {
-    const uint4 a = ld_nc_v4(xr + p.C), b = ld_nc_v4(xr + p.C + 8);
-    const uint32_t uw[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const uint32_t uw[4] = {w[1].x, w[1].y, w[1].z, w[1].w};
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < 4; ++k) {
       v[2 * k] = swiglu_fast(bf16_lo(xw[k]), bf16_lo(uw[k]));
       v[2 * k + 1] = swiglu_fast(bf16_hi(xw[k]), bf16_hi(uw[k]));
     }
   } else {
     const float rs = p.rstd[row];
-    const uint4 ga = ld_v4(p.g + c), gb = ld_v4(p.g + c + 8);
-    const uint32_t gw[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+    const uint4 gv = ld_v4(p.g + c);
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < 4; ++k) {
       v[2 * k] = __fmul_rn(__fmul_rn(bf16_lo(xw[k]), rs), bf16_lo(gw[k]));
       v[2 * k + 1] = __fmul_rn(__fmul_rn(bf16_hi(xw[k]), rs), bf16_hi(gw[k]));
     }
   }
 }
 
+// 8 codes of v[j] * s[j] packed in a uint2.
+template <int FMT>
+__device__ __forceinline__ uint2 codes8(const float (&v)[8], const float (&s)[8]) {
+  return make_uint2(cvt_fp8x4<FMT>(__fmul_rn(v[0], s[0]), __fmul_rn(v[1], s[1]), __fmul_rn(v[2], s[2]),
+                                   __fmul_rn(v[3], s[3])),
+                    cvt_fp8x4<FMT>(__fmul_rn(v[4], s[4]), __fmul_rn(v[5], s[5]), __fmul_rn(v[6], s[6]),
+                                   __fmul_rn(v[7], s[7])));
+}
+__device__ __forceinline__ void st_v2(void* p, uint2 v) { *reinterpret_cast<uint2*>(p) = v; }
+
 constexpr uint32_t kInfBits = 0x7F800000u;
 constexpr uint32_t kNanCodes4 = 0x7F7F7F7Fu;  // four NaN codes (0x7F in both formats)
+constexpr int kNonfiniteX = 1000;             // marks a non-finite column block in colx
 
 template <int IN, int FMT>
 __global__ void __launch_bounds__(kThreads) k_mx_quant(const MxArgs p) {
-  __shared__ uint32_t colmax[kThreads / 32][kTileCols];
-  __shared__ int colx[kTileCols];
+  // the column-block reduction's buffers, double-buffered by tile parity so that one barrier per
+  // phase suffices (a tile's reads of buffer b finish before the next tile but one rewrites it)
+  __shared__ __align__(16) uint32_t colmax[2][kThreads / 32][kTileCols];
+  __shared__ int colx[2][kTileCols];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int tr = t >> 3, seg = t & 7;
+  const int cseg = (lane & 15) * 8;  // this thread's first column in the tile
   const int64_t tiles_c = p.C / kTileCols;
   const int64_t tiles = (p.R / kTileRows) * tiles_c;
   bool nonfinite = false;
-  for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+  int64_t tile = blockIdx.x;
+  Raw raw;
+  if (tile < tiles) raw = load_raw<IN>(p, (tile / tiles_c) * kTileRows, (tile % tiles_c) * kTileCols + cseg, warp, lane);
+  for (int par = 0; tile < tiles; tile += gridDim.x, par ^= 1) {
     const int64_t r0 = (tile / tiles_c) * kTileRows, c0 = (tile % tiles_c) * kTileCols;
-    const int64_t row = r0 + tr, col = c0 + seg * 16;
-    float v[16];
-    load16<IN>(p, row, col, v);
-    uint32_t am[16];
-    uint32_t rmax = 0;
+    const int64_t col = c0 + cseg;
+    float v[2][8];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      am[j] = abs_bits(v[j]);
-      rmax = max(rmax, am[j]);
-    }
-    // ---- blocks along the row: 32 columns = this lane and its pair
+    for (int k = 0; k < 2; ++k) decode8<IN>(raw.w[k], p, r0 + tile_row(warp, lane, k), col, v[k]);
+    // the next tile's inputs are in flight while this one is reduced and written
+    const int64_t nt = tile + gridDim.x;
+    if (nt < tiles) raw = load_raw<IN>(p, (nt / tiles_c) * kTileRows, (nt % tiles_c) * kTileCols + cseg, warp, lane);
+    // ---- blocks along the row: 32 columns = 4 consecutive lanes
     if (p.q_r) {
-      rmax = max(rmax, __shfl_xor_sync(0xFFFFFFFFu, rmax, 1));
-      uint4 out;
-      uint8_t sfc;
-      if (rmax >= kInfBits) {
-        out = make_uint4(kNanCodes4, kNanCodes4, kNanCodes4, kNanCodes4);
-        sfc = 0xFF;
-        nonfinite = true;
-      } else {
-        const int X = mx_exponent<FMT>(rmax);
-        out = codes16<FMT>(v, pow2_neg(X));
-        sfc = (uint8_t)(X + 127);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        uint32_t m = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) m = max(m, abs_bits(v[k][j]));
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+        const int64_t row = r0 + tile_row(warp, lane, k);
+        uint2 out;
+        uint8_t sfc;
+        if (m >= kInfBits) {
+          out = make_uint2(kNanCodes4, kNanCodes4);
+          sfc = 0xFF;
+          nonfinite = true;
+        } else {
+          const int X = mx_exponent<FMT>(m);
+          const float sc = pow2_neg(X);
+          const float s8[8] = {sc, sc, sc, sc, sc, sc, sc, sc};
+          out = codes8<FMT>(v[k], s8);
+          sfc = (uint8_t)(X + 127);
+        }
+        st_v2(p.q_r + row * p.C + col, out);
+        if ((lane & 3) == 0) p.sf_r[sf_offset(row, col, p.C >> 7)] = sfc;
       }
-      st_v4(p.q_r + row * p.C + col, out);
-      if ((seg & 1) == 0) p.sf_r[sf_offset(row, col, p.C >> 7)] = sfc;
     }
-    // ---- blocks down the column: the tile's 32 rows
+    // ---- blocks down the column: the tile's 32 rows (2 per thread, 2 lanes per warp, 8 warps)
     if (p.q_c) {
+      uint32_t cm[8];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        uint32_t m = max(am[j], __shfl_xor_sync(0xFFFFFFFFu, am[j], 8));
-        am[j] = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t m = max(abs_bits(v[0][j]), abs_bits(v[1][j]));
+        cm[j] = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
       }
-      if (lane < 8) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) colmax[warp][lane * 16 + j] = am[j];
+      if (lane < 16) {
+        st_v4(&colmax[par][warp][cseg], make_uint4(cm[0], cm[1], cm[2], cm[3]));
+        st_v4(&colmax[par][warp][cseg + 4], make_uint4(cm[4], cm[5], cm[6], cm[7]));
       }
       __syncthreads();
       if (t < kTileCols) {
         uint32_t m = 0;
 #pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) m = max(m, colmax[w][t]);
+        for (int w = 0; w < kThreads / 32; ++w) m = max(m, colmax[par][w][t]);
         int X;
         uint8_t sfc;
         if (m >= kInfBits) {
-          X = 1000;  // marks a non-finite column block
+          X = kNonfiniteX;
           sfc = 0xFF;
           nonfinite = true;
         } else {
           X = mx_exponent<FMT>(m);
           sfc = (uint8_t)(X + 127);
         }
-        colx[t] = X;
+        colx[par][t] = X;
         p.sf_c[sf_offset(c0 + t, r0, p.R >> 7)] = sfc;
       }
       __syncthreads();
-      float s[16];
+      float s[8];
       bool bad = false;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int X = colx[seg * 16 + j];
-        bad |= X == 1000;
-        s[j] = X == 1000 ? 1.0f : pow2_neg(X);
+      for (int j = 0; j < 8; ++j) {
+        const int X = colx[par][cseg + j];
+        bad |= X == kNonfiniteX;
+        s[j] = X == kNonfiniteX ? 1.0f : pow2_neg(X);
       }
-      uint32_t w[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        w[q] = cvt_fp8x4<FMT>(__fmul_rn(v[4 * q], s[4 * q]), __fmul_rn(v[4 * q + 1], s[4 * q + 1]),
-                              __fmul_rn(v[4 * q + 2], s[4 * q + 2]), __fmul_rn(v[4 * q + 3], s[4 * q + 3]));
-      if (bad) {  // every element of a non-finite column block is the NaN code
+      for (int k = 0; k < 2; ++k) {
+        uint2 out = codes8<FMT>(v[k], s);
+        if (bad) {  // every element of a non-finite column block is the NaN code
+          uint32_t w2[2] = {out.x, out.y};
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (colx[seg * 16 + j] == 1000) w[j >> 2] = (w[j >> 2] & ~(0xFFu << (8 * (j & 3)))) | (0x7Fu << (8 * (j & 3)));
+          for (int j = 0; j < 8; ++j)
+            if (colx[par][cseg + j] == kNonfiniteX)
+              w2[j >> 2] = (w2[j >> 2] & ~(0xFFu << (8 * (j & 3)))) | (0x7Fu << (8 * (j & 3)));
+          out = make_uint2(w2[0], w2[1]);
+        }
+        st_v2(p.q_c + (r0 + tile_row(warp, lane, k)) * p.C + col, out);
       }
-      st_v4(p.q_c + row * p.C + col, make_uint4(w[0], w[1], w[2], w[3]));
-      __syncthreads();  // colmax / colx are rewritten by the next tile
     }
   }
   if (nonfinite) atomicOr(p.status, kStatusNonfinite);
