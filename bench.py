@@ -219,9 +219,9 @@ def step_work(w: synth.Workload, recompute: bool = False, bf16: bool = False, mx
                  ("rmsnorm_bwd", 10 * T * d, 0)]
         return a_fwd + fwd + (bwd + a_bwd if w.backward else [])
     mlp_fwd = [
-        ("absmax_partial", 2 * d * 2 * f, 0), ("quant_cast", 3 * d * 2 * f, 0),
-        ("absmax_partial", 2 * f * d, 0), ("quant_cast", 3 * f * d, 0),
-        ("rmsnorm_stats", 2 * T * d + 2 * d + 4 * T, 0), ("rmsnorm_cast", 3 * T * d + 4 * T + 2 * d, 0),
+        # the quantizer prologue: RMSNorm statistics beside the two weight absmax passes, then the casts
+        ("prologue_stats", 2 * d * 2 * f + 2 * f * d + 2 * T * d + 2 * d + 4 * T, 0),
+        ("prologue_cast", 3 * d * 2 * f + 3 * f * d + 3 * T * d + 4 * T + 2 * d, 0),
         ("gemm_gate_up_swiglu", T * d + d * 2 * f + 2 * T * 2 * f, 2.0 * T * d * 2 * f),
         ("swiglu_cast", 4 * T * f + T * f, 0),
         ("gemm_down_residual", T * f + f * d + 4 * T * d, 2.0 * T * f * d),

@@ -26,7 +26,7 @@ enum Kind {
   kKGemmGateUp, kKGemmDown, kKGemmDownDgrad, kKGemmDownWgrad, kKGemmGateUpDgrad, kKGemmGateUpWgrad, kKGemm,
   kKGemmQkv, kKGemmOResidual, kKGemmODgrad, kKGemmOWgrad, kKGemmQkvDgrad, kKGemmQkvWgrad,
   kKGemmGateUpRecompute, kKRmsnormBf16, kKAttnFwd, kKAttnBwdDelta, kKAttnBwdDkdv, kKAttnBwdDq,
-  kKMxQuant,
+  kKMxQuant, kKPrologueStats, kKPrologueCast,
   kKCount
 };
 const char* const kKindNames[kKCount] = {
@@ -35,7 +35,7 @@ const char* const kKindNames[kKCount] = {
     "gemm_down_wgrad", "gemm_gate_up_dgrad", "gemm_gate_up_wgrad", "gemm",
     "gemm_qkv", "gemm_o_residual", "gemm_o_dgrad", "gemm_o_wgrad", "gemm_qkv_dgrad", "gemm_qkv_wgrad",
     "gemm_gate_up_recompute", "rmsnorm_bf16", "attn_fwd", "attn_bwd_delta", "attn_bwd_dkdv", "attn_bwd_dq",
-    "mx_quant"};
+    "mx_quant", "prologue_stats", "prologue_cast"};
 
 struct Trace {
   bool on = false;
@@ -167,6 +167,7 @@ int check_ws(const void* ws, size_t ws_bytes, size_t need) {
 struct MlpWs {
   uint32_t* part_q;    // quantizer partials
   uint32_t* part_g;    // GEMM epilogue partials
+  uint32_t* part_w;    // the forward prologue's third partial array
   uint8_t* dY8;
   uint16_t* dH;
   uint8_t* dH8;
@@ -179,6 +180,7 @@ size_t mlp_ws_layout(int64_t T, int64_t d, int64_t f, int backward, uint8_t* bas
   MlpWs tmp{};
   tmp.part_q = (uint32_t*)c.take(kPartialBytes);
   tmp.part_g = (uint32_t*)c.take(kPartialBytes);
+  tmp.part_w = (uint32_t*)c.take(kPartialBytes);
   if (backward) {
     tmp.dY8 = (uint8_t*)c.take((size_t)(T * d));
     tmp.dH = (uint16_t*)c.take((size_t)(T * 2 * f) * 2);
@@ -394,16 +396,13 @@ int mlp_fwd_run(const fp8q_mlp* m, const MlpWs& w, Ctx& c) {
   float* s_n = m->scal + 6;
   float* s_a = m->scal + 9;
   int P = 0;
-  // weights: per-tensor E4M3 (re-quantized every step: weights change every step)
-  FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(m->W_gu, 0, d * 2 * f, w.part_q, &P, c.L));
-  FP8Q_STEP(kKQuantCast, launch_quant_cast(m->W_gu, 0, d * 2 * f, 0, w.part_q, P, m->W_gu8, s_wgu, c.L));
-  FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(m->W_d, 0, f * d, w.part_q, &P, c.L));
-  FP8Q_STEP(kKQuantCast, launch_quant_cast(m->W_d, 0, f * d, 0, w.part_q, P, m->W_d8, s_wd, c.L));
-  // RMSNorm + E4M3
-  FP8Q_STEP(kKRmsnormStats, launch_rmsnorm_stats((const uint16_t*)m->x, (const uint16_t*)m->g, T, (int)d, m->eps, m->rstd,
-                                w.part_q, &P, c.L));
-  FP8Q_STEP(kKRmsnormCast, launch_rmsnorm_cast((const uint16_t*)m->x, (const uint16_t*)m->g, m->rstd, T, (int)d, w.part_q, P,
-                               m->n8, s_n, c.L));
+  // weights (re-quantized every step: weights change every step) and RMSNorm, per-tensor E4M3: the
+  // RMSNorm statistics beside the two weight absmax reductions, then the three casts
+  for (int pass = 1; pass <= 2; ++pass)
+    FP8Q_STEP(pass == 1 ? kKPrologueStats : kKPrologueCast,
+              launch_prologue(pass, (const uint16_t*)m->x, (const uint16_t*)m->g, T, (int)d, m->eps, m->rstd,
+                              (const uint16_t*)m->W_gu, d * 2 * f, (const uint16_t*)m->W_d, f * d, w.part_q, w.part_g,
+                              w.part_w, m->n8, s_n, m->W_gu8, s_wgu, m->W_d8, s_wd, c.L));
   // G1: H = bf16(alpha n8 @ W_gu8) with the absmax of a = SwiGLU(H) fused in the epilogue
   GemmProblem g1{};
   g1.a_mn = 0;

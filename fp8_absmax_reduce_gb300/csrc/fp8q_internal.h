@@ -36,6 +36,14 @@ cudaError_t launch_quant_cast(const void* x, int dtype, int64_t n, int fmt, cons
 // RMSNorm: pass 1 (rstd + absmax partials), pass 2 (cast to E4M3).
 cudaError_t launch_rmsnorm_stats(const uint16_t* x, const uint16_t* g, int64_t T, int d, float eps, float* rstd,
                                  uint32_t* partial, int* P, const Launch& L);
+// The forward's quantizer prologue in two launches: pass 1 (RMSNorm statistics of x | absmax
+// partials of W_gu | of W_d), pass 2 (cast W_gu | cast W_d | cast n): the same results as the six
+// separate launches (bf16 weights of n_wgu / n_wd elements -> E4M3; n8 from x, g, rstd).  Each
+// partial array holds up to kMaxPartials.  Both passes take the same arguments.
+cudaError_t launch_prologue(int pass, const uint16_t* x, const uint16_t* g, int64_t T, int d, float eps, float* rstd,
+                            const uint16_t* W_gu, int64_t n_wgu, const uint16_t* W_d, int64_t n_wd,
+                            uint32_t* part_n, uint32_t* part_wgu, uint32_t* part_wd, uint8_t* n8, float* s_n,
+                            uint8_t* W_gu8, float* s_wgu, uint8_t* W_d8, float* s_wd, const Launch& L);
 // BF16 baseline: one pass, rstd and n = bf16((x rstd) g) (no absmax, no cast).
 cudaError_t launch_rmsnorm_bf16(const uint16_t* x, const uint16_t* g, int64_t T, int d, float eps, float* rstd,
                                 uint16_t* n16, const Launch& L);

@@ -74,14 +74,14 @@ __device__ __forceinline__ uint32_t elem_absbits(const uint8_t* x, int64_t e) {
   return reinterpret_cast<const uint32_t*>(x)[e] & 0x7FFFFFFFu;
 }
 
+// Block `bid` of `nblk` (the kernel's own grid, or a range of blocks of a combined launch).
 template <int DT>
-__global__ void __launch_bounds__(kThreads) k_absmax_partial(const uint8_t* __restrict__ x, int64_t n,
-                                                             uint32_t* __restrict__ partial) {
-  __shared__ uint32_t red[32];
+__device__ __forceinline__ void absmax_body(const uint8_t* __restrict__ x, int64_t n, uint32_t* __restrict__ partial,
+                                            int bid, int nblk, uint32_t* red) {
   constexpr int per = DT == 0 ? 8 : 4;  // elements per 16-byte vector
   const int64_t nvec = n / per;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t stride = (int64_t)nblk * blockDim.x;
+  int64_t i = (int64_t)bid * blockDim.x + threadIdx.x;
   uint32_t m = 0;
   for (; i + 3 * stride < nvec; i += 4 * stride) {
     const uint4 v0 = ld_nc_v4(x + 16 * i);
@@ -91,10 +91,17 @@ __global__ void __launch_bounds__(kThreads) k_absmax_partial(const uint8_t* __re
     m = max(m, max(max(vec_absmax<DT>(v0), vec_absmax<DT>(v1)), max(vec_absmax<DT>(v2), vec_absmax<DT>(v3))));
   }
   for (; i < nvec; i += stride) m = max(m, vec_absmax<DT>(ld_nc_v4(x + 16 * i)));
-  if (blockIdx.x == 0)
+  if (bid == 0)
     for (int64_t e = nvec * per + threadIdx.x; e < n; e += blockDim.x) m = max(m, elem_absbits<DT>(x, e));
   m = block_max_u32(m, red);
-  if (threadIdx.x == 0) partial[blockIdx.x] = m;
+  if (threadIdx.x == 0) partial[bid] = m;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads) k_absmax_partial(const uint8_t* __restrict__ x, int64_t n,
+                                                             uint32_t* __restrict__ partial) {
+  __shared__ uint32_t red[32];
+  absmax_body<DT>(x, n, partial, blockIdx.x, gridDim.x, red);
 }
 
 // ---------------------------------------------------------------------------
@@ -103,14 +110,14 @@ __global__ void __launch_bounds__(kThreads) k_absmax_partial(const uint8_t* __re
 // Reduces the partials in warp 0 and publishes the scale in shared memory; block 0
 // also writes {amax, scale, scale_inv} and flags a non-finite amax.
 __device__ __forceinline__ float finalize_scale(const uint32_t* partial, int P, int fmt, float* scal,
-                                                unsigned* status, float* s_shared) {
+                                                unsigned* status, float* s_shared, bool first) {
   if (threadIdx.x < 32) {
     const float amax = reduce_partials_warp(partial, P);
     if (threadIdx.x == 0) {
       float s, si;
       scale_from_amax(amax, fmt, s, si);
       *s_shared = s;
-      if (blockIdx.x == 0) {
+      if (first) {
         scal[0] = amax;
         scal[1] = s;
         scal[2] = si;
@@ -155,25 +162,33 @@ __device__ __forceinline__ uint8_t cvt_fp8(float v) {
 }
 
 template <int DT, int FMT>
-__global__ void __launch_bounds__(kThreads) k_quant_cast(const uint8_t* __restrict__ x, int64_t n,
-                                                         const uint32_t* __restrict__ partial, int P,
-                                                         uint8_t* __restrict__ q, float* __restrict__ scal,
-                                                         unsigned* status) {
-  __shared__ float s_sh;
-  const float s = finalize_scale(partial, P, FMT, scal, status, &s_sh);
+__device__ __forceinline__ void quant_cast_body(const uint8_t* __restrict__ x, int64_t n,
+                                                const uint32_t* __restrict__ partial, int P, uint8_t* __restrict__ q,
+                                                float* __restrict__ scal, unsigned* status, int bid, int nblk,
+                                                float* s_sh) {
+  const float s = finalize_scale(partial, P, FMT, scal, status, s_sh, bid == 0);
   const int64_t items = n / 16;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < items; i += stride) {
+  const int64_t stride = (int64_t)nblk * blockDim.x;
+  for (int64_t i = (int64_t)bid * blockDim.x + threadIdx.x; i < items; i += stride) {
     float v[16];
     load16<DT>(x, i, v);
     st_v4(q + 16 * i, cast16<FMT>(v, s));
   }
-  if (blockIdx.x == 0)
+  if (bid == 0)
     for (int64_t e = items * 16 + threadIdx.x; e < n; e += blockDim.x) {
       const float v = DT == 0 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(x)[e] << 16)
                               : reinterpret_cast<const float*>(x)[e];
       q[e] = cvt_fp8<FMT>(__fmul_rn(v, s));
     }
+}
+
+template <int DT, int FMT>
+__global__ void __launch_bounds__(kThreads) k_quant_cast(const uint8_t* __restrict__ x, int64_t n,
+                                                         const uint32_t* __restrict__ partial, int P,
+                                                         uint8_t* __restrict__ q, float* __restrict__ scal,
+                                                         unsigned* status) {
+  __shared__ float s_sh;
+  quant_cast_body<DT, FMT>(x, n, partial, P, q, scal, status, blockIdx.x, gridDim.x, &s_sh);
 }
 
 // ---------------------------------------------------------------------------
@@ -198,14 +213,14 @@ constexpr int kStatsWarps = 8;
 constexpr int stats_blocks_per_sm(int nc) { return nc <= 16 ? 4 : nc <= 24 ? 3 : 2; }
 
 template <bool OUT16, int NC>
-__global__ void __launch_bounds__(kStatsWarps * 32, stats_blocks_per_sm(NC))
-    k_rmsnorm_stats(const uint16_t* __restrict__ x, const uint16_t* __restrict__ g, int64_t T, int d, float eps,
-                    float* __restrict__ rstd, uint32_t* __restrict__ partial, uint16_t* __restrict__ n16) {
-  __shared__ uint32_t red[32];
+__device__ __forceinline__ void rmsnorm_stats_body(const uint16_t* __restrict__ x, const uint16_t* __restrict__ g,
+                                                   int64_t T, int d, float eps, float* __restrict__ rstd,
+                                                   uint32_t* __restrict__ partial, uint16_t* __restrict__ n16,
+                                                   int bid, int nblk, uint32_t* red) {
   const int lane = threadIdx.x & 31;
-  const int64_t nw = (int64_t)gridDim.x * kStatsWarps;
+  const int64_t nw = (int64_t)nblk * kStatsWarps;
   uint32_t m = 0;
-  for (int64_t row = (int64_t)blockIdx.x * kStatsWarps + (threadIdx.x >> 5); row < T; row += nw) {
+  for (int64_t row = (int64_t)bid * kStatsWarps + (threadIdx.x >> 5); row < T; row += nw) {
     const uint16_t* xr = x + row * d;
     float cs[NC];
 #pragma unroll
@@ -267,8 +282,16 @@ __global__ void __launch_bounds__(kStatsWarps * 32, stats_blocks_per_sm(NC))
   }
   if (!OUT16) {
     m = block_max_u32(m, red);
-    if (threadIdx.x == 0) partial[blockIdx.x] = m;
+    if (threadIdx.x == 0) partial[bid] = m;
   }
+}
+
+template <bool OUT16, int NC>
+__global__ void __launch_bounds__(kStatsWarps * 32, stats_blocks_per_sm(NC))
+    k_rmsnorm_stats(const uint16_t* __restrict__ x, const uint16_t* __restrict__ g, int64_t T, int d, float eps,
+                    float* __restrict__ rstd, uint32_t* __restrict__ partial, uint16_t* __restrict__ n16) {
+  __shared__ uint32_t red[32];
+  rmsnorm_stats_body<OUT16, NC>(x, g, T, d, eps, rstd, partial, n16, blockIdx.x, gridDim.x, red);
 }
 
 // Launches k_rmsnorm_stats with the smallest chunk bound that holds a row of d elements, on a
@@ -291,15 +314,13 @@ int rmsnorm_stats_dispatch(int64_t T, int d, int64_t cap, const Launch& L, const
   return grid;
 }
 
-__global__ void __launch_bounds__(kThreads) k_rmsnorm_cast(const uint16_t* __restrict__ x,
-                                                           const uint16_t* __restrict__ g,
-                                                           const float* __restrict__ rstd, int64_t T, int d,
-                                                           const uint32_t* __restrict__ partial, int P,
-                                                           uint8_t* __restrict__ q, float* __restrict__ scal,
-                                                           unsigned* status) {
-  __shared__ float s_sh;
-  const float s = finalize_scale(partial, P, 0, scal, status, &s_sh);
-  for (RowWalk w((int64_t)blockIdx.x * blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x, d / 16); w.row < T;
+__device__ __forceinline__ void rmsnorm_cast_body(const uint16_t* __restrict__ x, const uint16_t* __restrict__ g,
+                                                  const float* __restrict__ rstd, int64_t T, int d,
+                                                  const uint32_t* __restrict__ partial, int P, uint8_t* __restrict__ q,
+                                                  float* __restrict__ scal, unsigned* status, int bid, int nblk,
+                                                  float* s_sh) {
+  const float s = finalize_scale(partial, P, 0, scal, status, s_sh, bid == 0);
+  for (RowWalk w((int64_t)bid * blockDim.x + threadIdx.x, (int64_t)nblk * blockDim.x, d / 16); w.row < T;
        w.next()) {
     const int64_t row = w.row;
     const int j0 = w.col * 16;
@@ -316,6 +337,64 @@ __global__ void __launch_bounds__(kThreads) k_rmsnorm_cast(const uint16_t* __res
     }
     st_v4(q + row * d + j0, cast16<0>(v, s));
   }
+}
+
+__global__ void __launch_bounds__(kThreads) k_rmsnorm_cast(const uint16_t* __restrict__ x,
+                                                           const uint16_t* __restrict__ g,
+                                                           const float* __restrict__ rstd, int64_t T, int d,
+                                                           const uint32_t* __restrict__ partial, int P,
+                                                           uint8_t* __restrict__ q, float* __restrict__ scal,
+                                                           unsigned* status) {
+  __shared__ float s_sh;
+  rmsnorm_cast_body(x, g, rstd, T, d, partial, P, q, scal, status, blockIdx.x, gridDim.x, &s_sh);
+}
+
+// ---------------------------------------------------------------------------
+// The forward's quantizer prologue in two launches instead of six: pass 1 runs the RMSNorm
+// statistics of x (its first blocks, one per SM: latency-bound rows) beside the absmax reductions
+// of W_gu and W_d (bandwidth-bound), pass 2 the three casts.  The work of every block range is
+// exactly that of the separate kernels (the same bodies), so the results are identical.
+// ---------------------------------------------------------------------------
+struct Prologue {
+  const uint16_t* x; const uint16_t* g; int64_t T; int d; float eps; float* rstd;
+  uint32_t* part_n; int P_n;            // RMSNorm statistics blocks and partials
+  const uint8_t* wgu; int64_t n_wgu; uint32_t* part_wgu; int P_wgu;
+  const uint8_t* wd; int64_t n_wd; uint32_t* part_wd; int P_wd;
+  uint8_t* n8; float* s_n; int G_n;     // pass 2: casts and their block counts
+  uint8_t* wgu8; float* s_wgu; int G_wgu;
+  uint8_t* wd8; float* s_wd; int G_wd;
+  unsigned* status;
+};
+
+template <int NC>
+__global__ void __launch_bounds__(kStatsWarps * 32, stats_blocks_per_sm(NC)) k_prologue_stats(const Prologue a) {
+  __shared__ uint32_t red[32];
+  int b = blockIdx.x;
+  if (b < a.P_n) {
+    rmsnorm_stats_body<false, NC>(a.x, a.g, a.T, a.d, a.eps, a.rstd, a.part_n, nullptr, b, a.P_n, red);
+    return;
+  }
+  b -= a.P_n;
+  if (b < a.P_wgu) {
+    absmax_body<0>(a.wgu, a.n_wgu, a.part_wgu, b, a.P_wgu, red);
+    return;
+  }
+  absmax_body<0>(a.wd, a.n_wd, a.part_wd, b - a.P_wgu, a.P_wd, red);
+}
+
+__global__ void __launch_bounds__(kThreads) k_prologue_cast(const Prologue a) {
+  __shared__ float s_sh;
+  int b = blockIdx.x;
+  if (b < a.G_wgu) {
+    quant_cast_body<0, 0>(a.wgu, a.n_wgu, a.part_wgu, a.P_wgu, a.wgu8, a.s_wgu, a.status, b, a.G_wgu, &s_sh);
+    return;
+  }
+  b -= a.G_wgu;
+  if (b < a.G_wd) {
+    quant_cast_body<0, 0>(a.wd, a.n_wd, a.part_wd, a.P_wd, a.wd8, a.s_wd, a.status, b, a.G_wd, &s_sh);
+    return;
+  }
+  rmsnorm_cast_body(a.x, a.g, a.rstd, a.T, a.d, a.part_n, a.P_n, a.n8, a.s_n, a.status, b - a.G_wd, a.G_n, &s_sh);
 }
 
 // ---------------------------------------------------------------------------
@@ -360,7 +439,7 @@ __global__ void __launch_bounds__(kThreads) k_swiglu_cast(const uint16_t* __rest
                                                           uint8_t* __restrict__ q, float* __restrict__ scal,
                                                           unsigned* status) {
   __shared__ float s_sh;
-  const float s = finalize_scale(partial, P, FMT, scal, status, &s_sh);
+  const float s = finalize_scale(partial, P, FMT, scal, status, &s_sh, blockIdx.x == 0);
   for (RowWalk w((int64_t)blockIdx.x * blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x, f / 8); w.row < T;
        w.next()) {
     const int64_t row = w.row;
@@ -716,6 +795,36 @@ cudaError_t launch_rmsnorm_stats(const uint16_t* x, const uint16_t* g, int64_t T
   const int grid = rmsnorm_stats_dispatch<false>(T, d, kMaxPartials, L, x, g, eps, rstd, partial, nullptr);
   if (grid < 1) return cudaErrorInvalidConfiguration;
   *P = grid;
+  return post_launch(L);
+}
+
+cudaError_t launch_prologue(int pass, const uint16_t* x, const uint16_t* g, int64_t T, int d, float eps, float* rstd,
+                            const uint16_t* W_gu, int64_t n_wgu, const uint16_t* W_d, int64_t n_wd,
+                            uint32_t* part_n, uint32_t* part_wgu, uint32_t* part_wd, uint8_t* n8, float* s_n,
+                            uint8_t* W_gu8, float* s_wgu, uint8_t* W_d8, float* s_wd, const Launch& L) {
+  Prologue a{};
+  a.x = x; a.g = g; a.T = T; a.d = d; a.eps = eps; a.rstd = rstd;
+  a.part_n = part_n;
+  a.P_n = (int)std::min<int64_t>(L.num_sms, (T + kStatsWarps - 1) / kStatsWarps);
+  a.wgu = (const uint8_t*)W_gu; a.n_wgu = n_wgu; a.part_wgu = part_wgu; a.P_wgu = absmax_partial_blocks(0, n_wgu);
+  a.wd = (const uint8_t*)W_d; a.n_wd = n_wd; a.part_wd = part_wd; a.P_wd = absmax_partial_blocks(0, n_wd);
+  a.n8 = n8; a.s_n = s_n; a.G_n = grid_for(T * (d / 16), L.num_sms * 8);
+  a.wgu8 = W_gu8; a.s_wgu = s_wgu; a.G_wgu = grid_for(n_wgu / 16 > 0 ? n_wgu / 16 : 1, L.num_sms * 8);
+  a.wd8 = W_d8; a.s_wd = s_wd; a.G_wd = grid_for(n_wd / 16 > 0 ? n_wd / 16 : 1, L.num_sms * 8);
+  a.status = L.status;
+  if (pass == 2) {
+    k_prologue_cast<<<a.G_wgu + a.G_wd + a.G_n, kThreads, 0, L.stream>>>(a);
+    return post_launch(L);
+  }
+  const int nc = d <= 1024 ? 4 : d <= 2048 ? 8 : d <= 4096 ? 16 : d <= 6144 ? 24 : 32;
+  const int g1 = a.P_n + a.P_wgu + a.P_wd, th = kStatsWarps * 32;
+  switch (nc) {
+    case 4: k_prologue_stats<4><<<g1, th, 0, L.stream>>>(a); break;
+    case 8: k_prologue_stats<8><<<g1, th, 0, L.stream>>>(a); break;
+    case 16: k_prologue_stats<16><<<g1, th, 0, L.stream>>>(a); break;
+    case 24: k_prologue_stats<24><<<g1, th, 0, L.stream>>>(a); break;
+    default: k_prologue_stats<32><<<g1, th, 0, L.stream>>>(a); break;
+  }
   return post_launch(L);
 }
 
