@@ -13,10 +13,12 @@ from tests._gpu import dev_bf16
 pytestmark = pytest.mark.gpu
 
 
-def test_mlp_step_graph_replay_matches_direct_calls():
+@pytest.mark.parametrize("mx", [False, True])
+def test_mlp_step_graph_replay_matches_direct_calls(mx):
+    """mx: the block-scaled MXFP8 block."""
     w = synth.BY_NAME["7b-mlp-fwd-bwd"]
     T, d, f = 384, 512, 768
-    b = fq.MlpBuffers.allocate(T, d, f)
+    b = fq.MlpBuffers.allocate(T, d, f, mx=mx)
     inp = synth.mlp_inputs(w, seed=90, T=T, d=d, f=f)
     for k in ("x", "g", "W_gu", "W_d", "dY"):
         getattr(b, k).copy_(dev_bf16(inp[k]))

@@ -17,13 +17,14 @@ INPUTS = ("x", "g", "W_gu", "W_d", "dY")
 OUTPUTS = ("y", "dX", "dW_gu", "dW_d", "dg")
 
 
-@pytest.mark.parametrize("n_steps", [1, 2, 5])
-def test_run_steps_matches_separate_calls(n_steps):
+@pytest.mark.parametrize("n_steps,mx", [(1, False), (2, False), (5, False), (3, True)])
+def test_run_steps_matches_separate_calls(n_steps, mx):
+    """mx: the block-scaled MXFP8 block through the same executor."""
     w = synth.BY_NAME["7b-mlp-fwd-bwd"]
     T, d, f = 384, 512, 768
-    b0 = fq.MlpBuffers.allocate(T, d, f)
-    b1 = fq.MlpBuffers.allocate(T, d, f)
-    ref = fq.MlpBuffers.allocate(T, d, f)
+    b0 = fq.MlpBuffers.allocate(T, d, f, mx=mx)
+    b1 = fq.MlpBuffers.allocate(T, d, f, mx=mx)
+    ref = fq.MlpBuffers.allocate(T, d, f, mx=mx)
     host = []
     for i in range(n_steps):
         inp = synth.mlp_inputs(w, seed=10 + i, T=T, d=d, f=f)
