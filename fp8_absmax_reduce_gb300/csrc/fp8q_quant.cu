@@ -471,12 +471,13 @@ __global__ void __launch_bounds__(kThreads) k_swiglu_cast(const uint16_t* __rest
 // measured faster than the shared-memory ring below, which wins for longer rows.
 template <int NG>
 struct BwdRow {
-  uint4 d0[NG], d1[NG], xv[NG];
+  uint4 d0[NG], d1[NG], xv[NG], yv[NG];
 };
 
 template <int NG>
 __device__ __forceinline__ void bwd_load_row(BwdRow<NG>& r, const float* __restrict__ dN,
-                                             const uint16_t* __restrict__ x, int64_t row, int d, int t) {
+                                             const uint16_t* __restrict__ x, const uint16_t* __restrict__ dY,
+                                             int64_t row, int d, int t) {
 #pragma unroll
   for (int c = 0; c < NG; ++c) {
     const int j0 = 8 * (t + kThreads * c);
@@ -485,8 +486,9 @@ __device__ __forceinline__ void bwd_load_row(BwdRow<NG>& r, const float* __restr
       r.d0[c] = ld_nc_v4(dn);
       r.d1[c] = ld_nc_v4(dn + 4);
       r.xv[c] = ld_nc_v4(x + row * d + j0);
+      r.yv[c] = ld_nc_v4(dY + row * d + j0);
     } else {
-      r.d0[c] = r.d1[c] = r.xv[c] = make_uint4(0, 0, 0, 0);
+      r.d0[c] = r.d1[c] = r.xv[c] = r.yv[c] = make_uint4(0, 0, 0, 0);
     }
   }
 }
@@ -518,17 +520,12 @@ __global__ void __launch_bounds__(kThreads) k_rmsnorm_bwd_reg(const float* __res
   const int64_t r0 = (int64_t)blockIdx.x * rows;
   const int nrows = (int)((T - r0) < rows ? (T - r0) : rows);
   BwdRow<NG> cur;
-  bwd_load_row<NG>(cur, dN, x, r0, d, t);
+  bwd_load_row<NG>(cur, dN, x, dY, r0, d, t);
   for (int rr = 0; rr < nrows; ++rr) {
     const int64_t row = r0 + rr;
     BwdRow<NG> nxt;
-    if (rr + 1 < nrows) bwd_load_row<NG>(nxt, dN, x, row + 1, d, t);
-    uint4 yv[NG];
-#pragma unroll
-    for (int c = 0; c < NG; ++c) {
-      const int j0 = 8 * (t + kThreads * c);
-      yv[c] = j0 < d ? ld_nc_v4(dY + row * d + j0) : make_uint4(0, 0, 0, 0);
-    }
+    if (rr + 1 < nrows) bwd_load_row<NG>(nxt, dN, x, dY, row + 1, d, t);
+    const uint4* yv = cur.yv;
     const float rs = rstd[row];
     float nh[NG][8], u[NG][8];
     float dot = 0.0f;
