@@ -241,9 +241,10 @@ def step_work(w: synth.Workload, recompute: bool = False, bf16: bool = False, mx
         return mlp_fwd + (mlp_bwd if w.backward else [])
     q = w.qkv
     attn_fwd = [
-        ("absmax_partial", 2 * d * q, 0), ("quant_cast", 3 * d * q, 0),
-        ("absmax_partial", 2 * d * d, 0), ("quant_cast", 3 * d * d, 0),
-        ("rmsnorm_stats", 2 * T * d + 2 * d + 4 * T, 0), ("rmsnorm_cast", 3 * T * d + 4 * T + 2 * d, 0),
+        # the attention side's quantizer prologue: RMSNorm statistics beside the W_qkv and W_o
+        # absmax passes, then the three casts
+        ("prologue_stats", 2 * d * q + 2 * d * d + 2 * T * d + 2 * d + 4 * T, 0),
+        ("prologue_cast", 3 * d * q + 3 * d * d + 3 * T * d + 4 * T + 2 * d, 0),
         ("gemm_qkv", T * d + d * q + 2 * T * q, 2.0 * T * d * q),
         ("absmax_partial", 2 * T * d, 0), ("quant_cast", 3 * T * d, 0),
         ("gemm_o_residual", T * d + d * d + 4 * T * d, 2.0 * T * d * d),
@@ -261,7 +262,7 @@ def step_work(w: synth.Workload, recompute: bool = False, bf16: bool = False, mx
             ("attn_bwd_dkdv", 2 * T * q + 2 * T * d + 8 * T * hq + 4 * T * hkv * 128, 8.0 * 128 * pairs),
             ("attn_bwd_dq", 2 * T * q + 4 * T * d + 8 * T * hq, 6.0 * 128 * pairs),
         ]
-        attn_fwd = attn_fwd[:7] + core_fwd + attn_fwd[7:]
+        attn_fwd = attn_fwd[:3] + core_fwd + attn_fwd[3:]
     attn_bwd = [
         ("absmax_partial", 2 * T * d, 0), ("quant_cast", 3 * T * d, 0),
         ("gemm_o_dgrad", T * d + d * d + 2 * T * d, 2.0 * T * d * d),

@@ -749,14 +749,13 @@ int block_fwd_run(const fp8q_block* b, const BlockWs& w, Ctx& c) {
   float* s_n1 = b->scal + 6;
   float* s_att = b->scal + 9;
   int P = 0;
-  FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(b->W_qkv, 0, d * nq, w.part, &P, c.L));
-  FP8Q_STEP(kKQuantCast, launch_quant_cast(b->W_qkv, 0, d * nq, 0, w.part, P, b->W_qkv8, s_qkv, c.L));
-  FP8Q_STEP(kKAbsmaxPartial, launch_absmax_partial(b->W_o, 0, d * d, w.part, &P, c.L));
-  FP8Q_STEP(kKQuantCast, launch_quant_cast(b->W_o, 0, d * d, 0, w.part, P, b->W_o8, s_o, c.L));
-  FP8Q_STEP(kKRmsnormStats, launch_rmsnorm_stats((const uint16_t*)b->x, (const uint16_t*)b->g1, T, (int)d, b->eps,
-                                                 b->rstd1, w.part, &P, c.L));
-  FP8Q_STEP(kKRmsnormCast, launch_rmsnorm_cast((const uint16_t*)b->x, (const uint16_t*)b->g1, b->rstd1, T, (int)d,
-                                               w.part, P, b->n1_8, s_n1, c.L));
+  // W_qkv, W_o and the attention-side RMSNorm, per-tensor E4M3, through the two-launch prologue (the
+  // MLP's partial arrays are free until the MLP runs)
+  for (int pass = 1; pass <= 2; ++pass)
+    FP8Q_STEP(pass == 1 ? kKPrologueStats : kKPrologueCast,
+              launch_prologue(pass, (const uint16_t*)b->x, (const uint16_t*)b->g1, T, (int)d, b->eps, b->rstd1,
+                              (const uint16_t*)b->W_qkv, d * nq, (const uint16_t*)b->W_o, d * d, w.part,
+                              w.mlp.part_q, w.mlp.part_g, b->n1_8, s_n1, b->W_qkv8, s_qkv, b->W_o8, s_o, c.L));
   // qkv = bf16(alpha n1_8 @ W_qkv8)
   GemmProblem gq = gemm_problem(0, 1, T, nq, d, b->n1_8, d, 0, b->W_qkv8, nq, 0, nq, s_n1 + 2, s_qkv + 2, kEpiStore,
                                 0, b->qkv, nq);

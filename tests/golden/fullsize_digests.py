@@ -14,10 +14,13 @@ What a file holds (row indices are stored beside the rows):
   * sampled token rows of every per-token output (bf16 tensors as bit patterns, FP8 tensors as
     codes, fp32 tensors as fp32), chosen on both sides of the 128- and 256-row tile edges, the
     2048-row rasterisation-group edge and the last row;
-  * sampled rows of every weight gradient, and every gain gradient in full.
+  * sampled rows of every weight gradient, and every gain gradient in full;
+  * for ``<workload>-mx`` (the block-scaled MXFP8 block): SHA-256 of every block quantization of a
+    given tensor (codes and E8M0 scales), and the sampled rows (and their column blocks' scales) of
+    the requantized a and dH in both block directions.
 
-Usage: ``python tests/golden/fullsize_digests.py [--threads N] [workload ...]`` (default: all four
-workloads, one thread per core; the 32B-class block needs about 40 GB of host memory).
+Usage: ``python tests/golden/fullsize_digests.py [--threads N] [workload ...]`` (default: all five
+entries, one thread per core; the 32B-class block needs about 40 GB of host memory).
 """
 
 from __future__ import annotations
@@ -38,7 +41,8 @@ import oracle  # noqa: E402
 import synth  # noqa: E402
 
 OUT_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "fullsize")
-WORKLOADS = ("3b-mlp-fwd", "7b-mlp-fwd-bwd", "14b-mlp-fwd-bwd", "32b-block-fwd-bwd")
+WORKLOADS = ("3b-mlp-fwd", "7b-mlp-fwd-bwd", "14b-mlp-fwd-bwd", "32b-block-fwd-bwd", "7b-mlp-fwd-bwd-mx")
+MX_SUFFIX = "-mx"  # <workload>-mx: the block-scaled MXFP8 block on that workload's inputs
 
 
 def sha(a: np.ndarray) -> str:
@@ -91,6 +95,33 @@ def mlp_digest(w, threads: int) -> dict:
     return out
 
 
+def mlp_mx_digest(w, threads: int) -> dict:
+    """The block-scaled MXFP8 block (oracle.block(..., mx=True)) on the workload's inputs."""
+    inp = synth.mlp_inputs(w, seed=0)
+    t0 = time.time()
+    r = oracle.block(inp["x"], inp["g"], inp["W_gu"], inp["W_d"], dY=inp["dY"], nthreads=threads, mx=True)
+    secs = time.time() - t0
+    assert r["status"] == 0
+    rows = token_rows(w.T)
+    blocks = np.unique(rows // oracle.MX_BLOCK)  # the column blocks (32 tokens) holding the sampled rows
+    rd, rg = weight_rows(w.f), weight_rows(w.d)
+    out = {f"sha_in_{k}": sha(v) for k, v in inp.items()}
+    out.update(rows=rows, col_blocks=blocks, rows_dWd=rd, rows_dWgu=rg, sha_rstd=sha(f32(r["rstd"])),
+               H=bits(r["H"][rows]), y=bits(r["y"][rows]), dH=bits(r["dH"][rows]), dN=f32(r["dN"][rows]),
+               dX=bits(r["dX"][rows]), dWd=f32(r["dWd"][rd]), dWgu=f32(r["dWgu"][rg]), dg=f32(r["dg"]))
+    for slot in oracle.MX_SLOTS:
+        q, sf = r["mx_" + slot], r["mx_" + slot + "_sf"]
+        if slot.split("_")[0] in ("Wgu", "Wd", "n", "dY"):   # quantizers of given tensors: bit for bit
+            out["sha_mx_" + slot] = sha(q)
+            out["sha_mx_" + slot + "_sf"] = sha(sf)
+        else:                                                 # requantizations of GEMM outputs: sampled
+            out["mx_" + slot] = q[rows]
+            out["mx_" + slot + "_sf"] = sf[rows] if slot.endswith("_r") else sf[blocks]
+    out["oracle_seconds"] = np.float64(secs)
+    out["oracle_threads"] = np.int64(threads)
+    return out
+
+
 def block_digest(w, threads: int) -> dict:
     inp = synth.block_inputs(w, seed=0)
     t0 = time.time()
@@ -124,9 +155,13 @@ def main():
     args = ap.parse_args()
     os.makedirs(OUT_DIR, exist_ok=True)
     for name in args.workloads:
-        w = synth.BY_NAME[name]
+        mx = name.endswith(MX_SUFFIX)
+        w = synth.BY_NAME[name[: -len(MX_SUFFIX)] if mx else name]
         t0 = time.time()
-        dig = block_digest(w, args.threads) if w.qkv else mlp_digest(w, args.threads)
+        if mx:
+            dig = mlp_mx_digest(w, args.threads)
+        else:
+            dig = block_digest(w, args.threads) if w.qkv else mlp_digest(w, args.threads)
         dig["numpy_version"] = np.array(np.__version__)
         path = os.path.join(OUT_DIR, name + ".npz")
         np.savez_compressed(path, **dig)

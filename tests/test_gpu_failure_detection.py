@@ -83,6 +83,29 @@ def test_gemm_abort_sequence_on_short_waits(M, N, K):
     assert fq.get_status() == 0
 
 
+def test_mx_gemm_abort_sequence_on_short_waits():
+    """The block-scaled kernel (one accumulator, scale chunks staged and copied to tensor memory
+    each stage) through the same abort sequence, then a normal block-scaled GEMM on the context."""
+    from tests._gpu import mx_sf_to_chunked
+    rng = np.random.default_rng(3)
+    M, N, K = 2048, 2048, 1024
+    A, B = random_codes(rng, (M, K), 0), random_codes(rng, (K, N), 0)
+    sfA = rng.integers(120, 134, (M, K // 32)).astype(np.uint8)
+    sfB = rng.integers(120, 134, (N, K // 32)).astype(np.uint8)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dsA, dsB = torch.from_numpy(mx_sf_to_chunked(sfA)).cuda(), torch.from_numpy(mx_sf_to_chunked(sfB)).cuda()
+    fq.get_status(clear=True)
+    fq.selftest_gemm_wait_limit(fq.NN, dA, 0, dB, 0, 2e-6, sfA=dsA, sfB=dsB)
+    torch.cuda.synchronize()
+    assert fq.get_status(clear=True) & fq.STATUS_TIMEOUT
+    C = fq.fp8_gemm_mx(fq.NN, dA, 0, dsA, dB, 0, dsB, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert fq.get_status() == 0
+    rows = np.array([0, 127, 128, 1000, M - 1])
+    ref = oracle.gemm_mx(oracle.NN, A[rows], 0, sfA[rows], B, 0, sfB, out="f64", nthreads=8)
+    assert row_rel(C.cpu().numpy()[rows].astype(np.float64), ref) < 2e-3
+
+
 def test_gemm_wait_limit_is_validated():
     A = torch.zeros((128, 128), dtype=torch.uint8, device="cuda")
     s = torch.ones(2, dtype=torch.float32, device="cuda")

@@ -180,3 +180,70 @@ def test_full_size_32b_block():
     assert row_rel(f32(b.dW_qkv, rg), D["dWqkv"].astype(np.float64)) < 5e-3
     assert row_rel(b.mlp.dg.cpu().numpy()[None, :].astype(np.float64), D["dg"][None, :].astype(np.float64)) < 5e-3
     assert row_rel(b.dg1.cpu().numpy()[None, :].astype(np.float64), D["dg1"][None, :].astype(np.float64)) < 5e-3
+
+
+def mx_plain_sf(sf_chunked: torch.Tensor, R: int, C: int, along_rows: bool) -> np.ndarray:
+    """GPU scales (chunked layout) -> the oracle's plain layout: [R, C/32] for blocks along a row,
+    [R/32, C] for blocks down a column."""
+    from tests._gpu import mx_sf_from_chunked
+    sf = sf_chunked.cpu().numpy()
+    return mx_sf_from_chunked(sf, C, R).T if along_rows else mx_sf_from_chunked(sf, R, C)
+
+
+def mx_requant(q, rq, sf, rsf, block_of):
+    """Requantized MX codes (their input is a GEMM output): >= 99.9 % of the blocks have the oracle's
+    scale (the others one power of two away); inside the blocks whose scales agree >= 99.9 % identical
+    codes, every other one a step away.  block_of maps each code to its block's index in sf."""
+    sd = np.abs(sf.astype(int) - rsf.astype(int))
+    assert (sd == 0).mean() >= 0.999 and sd.max() <= 1, ((sd == 0).mean(), sd.max())
+    agree = (sd == 0).ravel()[block_of]
+    steps = code_step_diff(q, rq)[agree]
+    assert (steps == 0).mean() >= 0.999 and steps.max() <= 1, ((steps == 0).mean(), steps.max())
+
+
+def test_full_size_mlp_block_mxfp8():
+    """The block-scaled MXFP8 7B-class block against the oracle's full-size MX results."""
+    w = synth.BY_NAME["7b-mlp-fwd-bwd"]
+    T, d, f = w.T, w.d, w.f
+    inp = synth.mlp_inputs(w, seed=0)
+    D = digest("7b-mlp-fwd-bwd-mx", inp)
+    b = fq.MlpBuffers.allocate(T, d, f, backward=True, keep_intermediates=True, mx=True)
+    for k in ("x", "g", "W_gu", "W_d", "dY"):
+        getattr(b, k).copy_(dev_bf16(inp[k]))
+    fq.get_status(clear=True)
+    fq.mlp_block_fwd(b)
+    fq.mlp_block_bwd(b)
+    torch.cuda.synchronize()
+    assert fq.get_status() == 0
+    assert sha(b.rstd.cpu().numpy()) == str(D["sha_rstd"])
+    shapes = {"W_gu": (d, 2 * f), "W_d": (f, d), "n": (T, d), "a": (T, f), "dY": (T, d), "dH": (T, 2 * f)}
+    okey = {"W_gu": "Wgu", "W_d": "Wd", "n": "n", "a": "a", "dY": "dY", "dH": "dH"}
+    rows, blocks = D["rows"], D["col_blocks"]
+    for slot in fq.MX_SLOTS:
+        name, ax = slot.rsplit("_", 1)
+        R, C = shapes[name]
+        q, sfc = b.mx[slot]
+        key = f"mx_{okey[name]}_{ax}"
+        if name in ("W_gu", "W_d", "n", "dY"):
+            assert sha(q.cpu().numpy()) == str(D["sha_" + key]), slot
+            assert sha(mx_plain_sf(sfc, R, C, ax == "c")) == str(D["sha_" + key + "_sf"]), slot
+            continue
+        sf = mx_plain_sf(sfc, R, C, ax == "c")
+        qr = rows_of(q, rows).cpu().numpy()
+        if ax == "r":   # blocks along the row: block (i, j // 32) of sampled row i
+            block_of = (np.arange(len(rows))[:, None] * (C // 32) + np.arange(C)[None, :] // 32).ravel()
+            mx_requant(qr, D[key], sf[rows], D[key + "_sf"], block_of)
+        else:           # blocks down a column: block (row // 32, j)
+            pos = np.searchsorted(blocks, rows // 32)
+            block_of = (pos[:, None] * C + np.arange(C)[None, :]).ravel()
+            mx_requant(qr, D[key], sf[blocks], D[key + "_sf"], block_of)
+    assert row_rel(bf16_vals(bits(rows_of(b.H, rows))), bf16_vals(D["H"])) < 2e-3
+    assert row_rel(bf16_vals(bits(rows_of(b.y, rows))), bf16_vals(D["y"])) < 2e-3
+    assert row_rel(bf16_vals(bits(rows_of(b.dH, rows))), bf16_vals(D["dH"])) < 5e-3
+    assert row_rel(rows_of(b.dN, rows).cpu().numpy().astype(np.float64), D["dN"].astype(np.float64)) < 5e-3
+    assert row_rel(bf16_vals(bits(rows_of(b.dX, rows))), bf16_vals(D["dX"])) < 5e-3
+    assert row_rel(rows_of(b.dW_d, D["rows_dWd"]).cpu().numpy().astype(np.float64),
+                   D["dWd"].astype(np.float64)) < 5e-3
+    assert row_rel(rows_of(b.dW_gu, D["rows_dWgu"]).cpu().numpy().astype(np.float64),
+                   D["dWgu"].astype(np.float64)) < 5e-3
+    assert row_rel(b.dg.cpu().numpy()[None, :].astype(np.float64), D["dg"][None, :].astype(np.float64)) < 5e-3
