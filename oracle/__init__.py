@@ -15,7 +15,8 @@ Sources: "LLMQ: Efficient Lower-Precision Pretraining for Consumer GPUs"
 (fused non-matmul ops, retained absmax statistics), §5 Figure 2 (E4M3
 forward, E5M2 activation gradients); "Periodic Reporting for period 1 -
 FastML" (CORDIS), "FP8 training without delayed scaling" (just-in-time
-absmax scaling, no clipping).
+absmax scaling, no clipping); LLMQ §2 (inner-dimension block scaling: the MXFP8 mode, in the
+OCP Microscaling block format).
 
 Parity pins: ``tests/test_oracle_*.py``.  Every function here is pinned;
 see the header of each test file for what pins it.

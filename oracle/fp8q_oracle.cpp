@@ -20,6 +20,8 @@
 //     fused around the GEMMs; kernels are deterministic.
 //   * FP8 encodings follow the OCP 8-bit floating point specification
 //     (E4M3 "FN": no infinities, max 448; E5M2: IEEE-like, max 57344).
+//   * LLMQ §2: inner-dimension (block) scaling, native on Blackwell; the block
+//     format is the OCP Microscaling one (32 elements, E8M0 scale).
 // The pages give no formula beyond these sentences; every concrete choice
 // below (scale = fmax/amax, fp32 product before the cast, RNE with
 // saturation, RMSNorm epsilon and pairwise fp32 sum of squares, SwiGLU in
