@@ -69,6 +69,9 @@ def parse_args():
                     help="time cuBLASLt FP8 (torch._scaled_mm) 8192^3, burst and sustained, and exit")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the workload's T (same d, f, distributions); for small profiling runs")
+    ap.add_argument("--launch-log", default="",
+                    help="write the mean time of every launch position of the step (kernel, bytes, flops, us) "
+                         "to this JSON file")
     return ap.parse_args()
 
 
@@ -526,6 +529,19 @@ def kernel_table(traced, plan, K, pk):
     return out, total
 
 
+def launch_positions(traced, plan):
+    """Mean time of each launch position of the step over the timed steps, with its planned work."""
+    per = len(plan)
+    out = []
+    for i, (pname, pbytes, pflops) in enumerate(plan):
+        ts = [t for k, (_, t) in enumerate(traced) if k % per == i]
+        us = 1e3 * sum(ts) / len(ts) if ts else 0.0
+        out.append({"pos": i, "kernel": pname, "bytes": pbytes, "flops": pflops, "us": round(us, 2),
+                    "gbs": round(pbytes / (us * 1e-6) / 1e9, 1) if us and not pflops else None,
+                    "tflops": round(pflops / (us * 1e-6) / 1e12, 1) if us and pflops else None})
+    return out
+
+
 def precision_name(args) -> str:
     return "bf16 baseline" if args.bf16 else ("mxfp8 (block-scaled)" if args.mxfp8 else "fp8")
 
@@ -653,6 +669,9 @@ def main():
     ms_step = r["ms"] / r["K"]
     value = job_throughput(r["flops"], world, ms_step) / 1e12
     kernels, traced_total = kernel_table(r["traced"], r["plan"], r["K"], pk)
+    if args.launch_log:
+        with open(args.launch_log, "w") as fh:
+            json.dump(launch_positions(r["traced"], r["plan"]), fh, indent=1)
     gemm = {k: v for k, v in kernels.items() if k.startswith("gemm")}
     g_ms = sum(v["total_ms"] for v in gemm.values())
     g_launch = sum(v["launches"] for v in gemm.values())

@@ -42,6 +42,10 @@ def _load() -> ctypes.CDLL:
     L.rmsnorm_quant_workspace_size.restype = sz
     L.rmsnorm_quant_workspace_size.argtypes = [i64, i64]
     L.rmsnorm_quant.argtypes = [vp, vp, i64, i64, f32, vp, vp, vp, vp, sz, vp]
+    L.rmsnorm_bwd_workspace_size.restype = sz
+    L.rmsnorm_bwd_workspace_size.argtypes = [i64, i64]
+    L.rmsnorm_bwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, vp, vp, vp, sz, vp]
+    L.fp8q_selftest_rmsnorm_bwd_wait_limit.argtypes = [vp, vp, vp, vp, vp, i64, i64, vp, vp, vp, sz, i64, vp]
     L.swiglu_quant_workspace_size.restype = sz
     L.swiglu_quant_workspace_size.argtypes = [i64, i64]
     L.swiglu_quant.argtypes = [vp, i64, i64, i32, vp, vp, vp, sz, vp]
@@ -275,6 +279,32 @@ def rmsnorm_quant(x: torch.Tensor, g: torch.Tensor, eps: float = 1e-6, q=None, s
     _check("rmsnorm_quant", lib.rmsnorm_quant(_ptr(x), _ptr(g), T, d, eps, _ptr(q), _ptr(scal), _ptr(rstd),
                                               _ptr(w), nb, _stream(stream)))
     return q, scal, rstd
+
+
+def _rmsnorm_bwd_call(name, dN, x, dY, g, rstd, dX, dg, ws, stream, *limit):
+    dev = _dev(x)
+    T, d = x.shape
+    dX = torch.empty((T, d), dtype=torch.bfloat16, device=dev) if dX is None else dX
+    dg = torch.empty(d, dtype=torch.float32, device=dev) if dg is None else dg
+    nb = lib.rmsnorm_bwd_workspace_size(T, d)
+    w = _ws(nb, dev, ws)
+    _check(name, getattr(lib, name)(_ptr(dN), _ptr(x), _ptr(dY), _ptr(g), _ptr(rstd), T, d, _ptr(dX), _ptr(dg),
+                                    _ptr(w), nb, *limit, _stream(stream)))
+    return dX, dg
+
+
+def rmsnorm_bwd(dN: torch.Tensor, x: torch.Tensor, dY: torch.Tensor, g: torch.Tensor, rstd: torch.Tensor, dX=None,
+                dg=None, ws=None, stream=None):
+    """RMSNorm backward with the residual gradient: dN [T,d] fp32, x, dY [T,d] bf16, g [d] bf16,
+    rstd [T] fp32 -> (dX [T,d] bf16, dg [d] fp32)."""
+    return _rmsnorm_bwd_call("rmsnorm_bwd", dN, x, dY, g, rstd, dX, dg, ws, stream)
+
+
+def selftest_rmsnorm_bwd_wait_limit(dN, x, dY, g, rstd, limit_s: float, dX=None, dg=None, ws=None, stream=None):
+    """rmsnorm_bwd with every wait on a row's copies limited to limit_s
+    (fp8q_selftest_rmsnorm_bwd_wait_limit in include/fp8q.h).  Returns (dX, dg), incomplete on a time-out."""
+    return _rmsnorm_bwd_call("fp8q_selftest_rmsnorm_bwd_wait_limit", dN, x, dY, g, rstd, dX, dg, ws, stream,
+                             max(1, int(limit_s * 1e9)))
 
 
 def swiglu_quant(H: torch.Tensor, fmt: int = E4M3, q=None, scal=None, ws=None, stream=None):

@@ -1000,6 +1000,40 @@ int rmsnorm_quant(const void* x, const void* g, int64_t T, int64_t d, float eps,
 }
 
 // ---------------------------------------------------------------------------
+size_t rmsnorm_bwd_workspace_size(int64_t T, int64_t d) {
+  if (T < 1 || d < 1) return 0;
+  return round256((size_t)((T + kBwdRows - 1) / kBwdRows) * (size_t)d * 4);
+}
+
+namespace {
+int rmsnorm_bwd_run(const float* dN, const void* x, const void* dY, const void* g, const float* rstd, int64_t T,
+                    int64_t d, void* dX, float* dg, void* ws, size_t ws_bytes, fp8q_stream stream, uint64_t wait_ns) {
+  if (T < 1 || d < 16 || d % 16 || d > 8192 || T > ((int64_t)1 << 28)) return FP8Q_ERR_INVALID_ARG;
+  if (!al16(dN) || !al16(x) || !al16(dY) || !al16(g) || !al16(dX)) return FP8Q_ERR_INVALID_ARG;
+  if (!rstd || ((uintptr_t)rstd & 3u) || !dg || ((uintptr_t)dg & 3u)) return FP8Q_ERR_INVALID_ARG;
+  int e = check_ws(ws, ws_bytes, rmsnorm_bwd_workspace_size(T, d));
+  if (e) return e;
+  Ctx c;
+  if ((e = make_ctx(&c, stream))) return e;
+  FP8Q_STEP(kKRmsnormBwd, launch_rmsnorm_bwd(dN, (const uint16_t*)x, (const uint16_t*)dY, (const uint16_t*)g, rstd,
+                                             T, (int)d, (uint16_t*)dX, static_cast<float*>(ws), dg, c.L, wait_ns));
+  return finish(c);
+}
+}  // namespace
+
+int rmsnorm_bwd(const float* dN, const void* x, const void* dY, const void* g, const float* rstd, int64_t T,
+                int64_t d, void* dX, float* dg, void* ws, size_t ws_bytes, fp8q_stream stream) {
+  return rmsnorm_bwd_run(dN, x, dY, g, rstd, T, d, dX, dg, ws, ws_bytes, stream, 0);
+}
+
+int fp8q_selftest_rmsnorm_bwd_wait_limit(const float* dN, const void* x, const void* dY, const void* g,
+                                         const float* rstd, int64_t T, int64_t d, void* dX, float* dg, void* ws,
+                                         size_t ws_bytes, int64_t limit_ns, fp8q_stream stream) {
+  if (limit_ns < 1 || limit_ns > 10000000000LL) return FP8Q_ERR_INVALID_ARG;
+  return rmsnorm_bwd_run(dN, x, dY, g, rstd, T, d, dX, dg, ws, ws_bytes, stream, (uint64_t)limit_ns);
+}
+
+// ---------------------------------------------------------------------------
 size_t swiglu_quant_workspace_size(int64_t T, int64_t f) {
   (void)T;
   (void)f;

@@ -57,10 +57,12 @@ cudaError_t launch_swiglu_cast(const uint16_t* H, int64_t T, int f, int fmt, con
                                uint8_t* q, float* scal, const Launch& L, bool fast = false);
 
 // RMSNorm backward + residual: dX = dY + rstd (u - nh mean(u nh)), dg = sum_t dN nh.
-// dg_partial: ceil(T / kBwdRows) x d floats of workspace.
+// dg_partial: ceil(T / kBwdRows) x d floats of workspace.  wait_ns: the limit of every wait on a
+// row's copies (0: the default 2 s; otherwise the self-test of the abort sequence, whose waits
+// probe without suspending so that a limit of nanoseconds is honoured).
 cudaError_t launch_rmsnorm_bwd(const float* dN, const uint16_t* x, const uint16_t* dY, const uint16_t* g,
                                const float* rstd, int64_t T, int d, uint16_t* dX, float* dg_partial, float* dg,
-                               const Launch& L);
+                               const Launch& L, uint64_t wait_ns = 0);
 
 // Attention core (bf16, causal, grouped K/V heads, head dim 128, S a multiple of 128).
 cudaError_t launch_attn_fwd(const uint16_t* qkv, int64_t T, int S, int Hq, int Hkv, uint16_t* att, float* lse,

@@ -455,283 +455,188 @@ __global__ void __launch_bounds__(kThreads) k_swiglu_cast(const uint16_t* __rest
 
 // ---------------------------------------------------------------------------
 // RMSNorm backward + residual.  A block owns `rows` consecutive rows (one wave
-// of resident blocks covers all T rows); thread t owns the 8-column groups
-// j = 8 (t + 256 c), c < NG.  Per row: nh = x rstd, u = dN g,
+// of resident blocks covers all T rows).  Per row: nh = x rstd, u = dN g,
 // dot = sum_j u nh (block reduction, fixed order), dX = dY + rstd (u - nh dot/d).
-// A row's dN, x and dY reach shared memory through a ring of kBwdRing slots
-// filled by asynchronous 16-byte copies, kBwdRing - 1 rows ahead of their use
-// (one row of prefetch cannot cover the DRAM latency behind a row's short
-// dependent chain); each thread copies and reads back only its own pieces, so
-// the ring needs no barrier beyond the thread's cp.async.wait_group.
 // dg partials accumulate per block in registers (fixed row order) and are
 // reduced over blocks in a fixed order by k_dg_finalize.
 // ---------------------------------------------------------------------------
-// Rows of up to 4096 columns (at most two 8-column groups per thread): the next row's dN and x
-// in registers while the current one is reduced, two blocks per SM -- at these sizes this
-// measured faster than the shared-memory ring below, which wins for longer rows.
-template <int NG>
-struct BwdRow {
-  uint4 d0[NG], d1[NG], xv[NG], yv[NG];
-};
+// Rows staged whole in shared memory by the bulk-copy engine: thread t owns the one 8-column group
+// j0 = 8 t (the block is ceil(d / 8) threads rounded up to whole warps, at most 1024 for d <= 8192).
+// A ring of S row slots, each [dN row (4d B) | x row (2d B) | dY row (2d B)], is filled by
+// cp.async.bulk copies that one thread issues up to S rows ahead, completing on the slot's
+// mbarrier: the bytes in flight per SM are set by the ring, not by registers, and the block's
+// threads issue no load instructions for their inputs.  A thread takes its 8 values of each piece
+// into registers before the row's block barrier, so once every thread has passed that barrier the
+// slot is free and the issuing thread refills it with row rr + S.
+// Every wait is bounded; a thread whose wait expires flags its warp's entry of the row's reduction,
+// every thread sees the flag after the same barrier and leaves the loop, and the issuing thread
+// waits (again bounded) for the copies it still has in flight before the block exits.
+constexpr int kBwdSlotsMax = 8;
+constexpr int kBwdSmemBudget = 200 * 1024;  // per SM, shared by its resident blocks
 
-template <int NG>
-__device__ __forceinline__ void bwd_load_row(BwdRow<NG>& r, const float* __restrict__ dN,
-                                             const uint16_t* __restrict__ x, const uint16_t* __restrict__ dY,
-                                             int64_t row, int d, int t) {
-#pragma unroll
-  for (int c = 0; c < NG; ++c) {
-    const int j0 = 8 * (t + kThreads * c);
-    if (j0 < d) {
-      const float* dn = dN + row * d + j0;
-      r.d0[c] = ld_nc_v4(dn);
-      r.d1[c] = ld_nc_v4(dn + 4);
-      r.xv[c] = ld_nc_v4(x + row * d + j0);
-      r.yv[c] = ld_nc_v4(dY + row * d + j0);
-    } else {
-      r.d0[c] = r.d1[c] = r.xv[c] = r.yv[c] = make_uint4(0, 0, 0, 0);
-    }
-  }
+inline int bwd_tma_threads(int d) { return ((d / 8 + 31) / 32) * 32; }
+// Two blocks per SM (two independent row chains) where their threads' registers (at most 64
+// each) and two rings of three row slots fit, else one.
+inline int bwd_tma_blocks_per_sm(int d) {
+  return bwd_tma_threads(d) <= 512 && 2 * 3 * (size_t)8 * d <= (size_t)kBwdSmemBudget ? 2 : 1;
 }
 
-template <int NG>
-__global__ void __launch_bounds__(kThreads) k_rmsnorm_bwd_reg(const float* __restrict__ dN,
-                                                          const uint16_t* __restrict__ x,
-                                                          const uint16_t* __restrict__ dY,
-                                                          const uint16_t* __restrict__ g,
-                                                          const float* __restrict__ rstd, int64_t T, int d,
-                                                          int rows, uint16_t* __restrict__ dX,
-                                                          float* __restrict__ dg_partial) {
-  __shared__ float red[2][kThreads / 32];
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  float gv[NG][8], dga[NG][8];
-#pragma unroll
-  for (int c = 0; c < NG; ++c) {
-    const int j0 = 8 * (t + kThreads * c);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) { gv[c][k] = 0.0f; dga[c][k] = 0.0f; }
-    if (j0 < d) {
-      const uint4 w = ld_v4(g + j0);
-      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) { gv[c][2 * k] = bf16_lo(ww[k]); gv[c][2 * k + 1] = bf16_hi(ww[k]); }
-    }
-  }
-  const float inv_d = 1.0f / (float)d;
+// POLL: the waits probe without suspending (mbar_poll), for the self-test of the abort sequence.
+template <bool POLL>
+__global__ void __launch_bounds__(1024, 1) k_rmsnorm_bwd_tma(const float* __restrict__ dN,
+                                                              const uint16_t* __restrict__ x,
+                                                              const uint16_t* __restrict__ dY,
+                                                              const uint16_t* __restrict__ g,
+                                                              const float* __restrict__ rstd, int64_t T, int d,
+                                                              int rows, int S, uint16_t* __restrict__ dX,
+                                                              float* __restrict__ dg_partial, unsigned* status,
+                                                              uint64_t wait_ns) {
+  extern __shared__ __align__(128) uint8_t bwd_rows[];  // S slots of 8 d bytes
+  __shared__ uint64_t full[kBwdSlotsMax];
+  __shared__ float red[2][32];
+  __shared__ int bad[2][32];
+  __shared__ volatile int give_up;  // lets the other waiting threads stop early once one wait has expired
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5, nwarps = blockDim.x >> 5;
+  const int j0 = 8 * t;
+  const bool mine = j0 < d;
   const int64_t r0 = (int64_t)blockIdx.x * rows;
   const int nrows = (int)((T - r0) < rows ? (T - r0) : rows);
-  BwdRow<NG> cur;
-  bwd_load_row<NG>(cur, dN, x, dY, r0, d, t);
-  for (int rr = 0; rr < nrows; ++rr) {
+  const uint32_t slot_bytes = 8u * (uint32_t)d;
+  if (t == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+    give_up = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  auto issue = [&](int rr) {  // thread 0 only
+    const int s = rr % S;
     const int64_t row = r0 + rr;
-    BwdRow<NG> nxt;
-    if (rr + 1 < nrows) bwd_load_row<NG>(nxt, dN, x, dY, row + 1, d, t);
-    const uint4* yv = cur.yv;
-    const float rs = rstd[row];
-    float nh[NG][8], u[NG][8];
-    float dot = 0.0f;
-#pragma unroll
-    for (int c = 0; c < NG; ++c) {
-      const float dnv[8] = {__uint_as_float(cur.d0[c].x), __uint_as_float(cur.d0[c].y),
-                            __uint_as_float(cur.d0[c].z), __uint_as_float(cur.d0[c].w),
-                            __uint_as_float(cur.d1[c].x), __uint_as_float(cur.d1[c].y),
-                            __uint_as_float(cur.d1[c].z), __uint_as_float(cur.d1[c].w)};
-      const uint32_t xw[4] = {cur.xv[c].x, cur.xv[c].y, cur.xv[c].z, cur.xv[c].w};
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float xk = (k & 1) ? bf16_hi(xw[k >> 1]) : bf16_lo(xw[k >> 1]);
-        nh[c][k] = xk * rs;
-        u[c][k] = dnv[k] * gv[c][k];
-        dot += u[c][k] * nh[c][k];
-        dga[c][k] += dnv[k] * nh[c][k];
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
-    if (lane == 0) red[rr & 1][warp] = dot;
-    __syncthreads();
-    float tot = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) tot += red[rr & 1][w];
-    const float mean = tot * inv_d;
-#pragma unroll
-    for (int c = 0; c < NG; ++c) {
-      const int j0 = 8 * (t + kThreads * c);
-      if (j0 < d) {
-        const uint32_t yw[4] = {yv[c].x, yv[c].y, yv[c].z, yv[c].w};
-        uint32_t o[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float a = bf16_lo(yw[k]) + rs * (u[c][2 * k] - nh[c][2 * k] * mean);
-          const float b = bf16_hi(yw[k]) + rs * (u[c][2 * k + 1] - nh[c][2 * k + 1] * mean);
-          o[k] = pack_bf16x2(a, b);
-        }
-        st_v4(dX + row * d + j0, make_uint4(o[0], o[1], o[2], o[3]));
-      }
-    }
-    if (rr + 1 < nrows) cur = nxt;
-  }
-#pragma unroll
-  for (int c = 0; c < NG; ++c) {
-    const int j0 = 8 * (t + kThreads * c);
-    if (j0 < d) {
-      float* dst = dg_partial + (int64_t)blockIdx.x * d + j0;
-      st_v4(dst, make_uint4(__float_as_uint(dga[c][0]), __float_as_uint(dga[c][1]), __float_as_uint(dga[c][2]),
-                            __float_as_uint(dga[c][3])));
-      st_v4(dst + 4, make_uint4(__float_as_uint(dga[c][4]), __float_as_uint(dga[c][5]),
-                                __float_as_uint(dga[c][6]), __float_as_uint(dga[c][7])));
-    }
-  }
-}
-
-constexpr int kBwdRing = 3;
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Shared memory of one k_rmsnorm_bwd block: kBwdRing slots of NG x 4 pieces (dN lo, dN hi, x, dY)
-// of 16 bytes per thread.
-inline size_t rmsnorm_bwd_smem(int ng) { return (size_t)kBwdRing * ng * 4 * kThreads * 16; }
-
-template <int NG>
-__global__ void __launch_bounds__(kThreads, 2) k_rmsnorm_bwd(const float* __restrict__ dN,
-                                                             const uint16_t* __restrict__ x,
-                                                             const uint16_t* __restrict__ dY,
-                                                             const uint16_t* __restrict__ g,
-                                                             const float* __restrict__ rstd, int64_t T, int d,
-                                                             int rows, uint16_t* __restrict__ dX,
-                                                             float* __restrict__ dg_partial) {
-  extern __shared__ uint4 bwd_ring[];  // [slot][group][piece][thread]
-  __shared__ float red[2][kThreads / 32];
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  float gv[NG][8], dga[NG][8];
-#pragma unroll
-  for (int c = 0; c < NG; ++c) {
-    const int j0 = 8 * (t + kThreads * c);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) { gv[c][k] = 0.0f; dga[c][k] = 0.0f; }
-    if (j0 < d) {
-      const uint4 w = ld_v4(g + j0);
-      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) { gv[c][2 * k] = bf16_lo(ww[k]); gv[c][2 * k + 1] = bf16_hi(ww[k]); }
-    }
-  }
-  const float inv_d = 1.0f / (float)d;
-  const int64_t r0 = (int64_t)blockIdx.x * rows;
-  const int nrows = (int)((T - r0) < rows ? (T - r0) : rows);
-  const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(bwd_ring);
-  // piece q of group c of slot sl, this thread's 16 bytes
-  auto piece = [&](int sl, int c, int q) { return ((sl * NG + c) * 4 + q) * kThreads + t; };
-  auto issue = [&](int rr) {
-    if (rr < nrows) {
-      const int64_t row = r0 + rr;
-      const int sl = rr % kBwdRing;
-#pragma unroll
-      for (int c = 0; c < NG; ++c) {
-        const int j0 = 8 * (t + kThreads * c);
-        if (j0 < d) {
-          const float* dn = dN + row * d + j0;
-          cp_async16(ring_s + 16u * piece(sl, c, 0), dn);
-          cp_async16(ring_s + 16u * piece(sl, c, 1), dn + 4);
-          cp_async16(ring_s + 16u * piece(sl, c, 2), x + row * d + j0);
-          cp_async16(ring_s + 16u * piece(sl, c, 3), dY + row * d + j0);
-        }
-      }
-    }
-    cp_async_commit();  // an empty group keeps the group count uniform
+    uint8_t* slot = bwd_rows + (size_t)s * slot_bytes;
+    mbar_arrive_expect_tx(&full[s], slot_bytes);
+    bulk_load(slot, dN + row * d, 4u * d, &full[s]);
+    bulk_load(slot + 4 * d, x + row * d, 2u * d, &full[s]);
+    bulk_load(slot + 6 * d, dY + row * d, 2u * d, &full[s]);
   };
+  if (t == 0)
+    for (int k = 0; k < S && k < nrows; ++k) issue(k);
+  float gv[8], dga[8];
 #pragma unroll
-  for (int k = 0; k < kBwdRing - 1; ++k) issue(k);
-  for (int rr = 0; rr < nrows; ++rr) {
+  for (int k = 0; k < 8; ++k) { gv[k] = 0.0f; dga[k] = 0.0f; }
+  if (mine) {
+    const uint4 w = ld_v4(g + j0);
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) { gv[2 * k] = bf16_lo(ww[k]); gv[2 * k + 1] = bf16_hi(ww[k]); }
+  }
+  const float inv_d = 1.0f / (float)d;
+  int rr = 0;
+  bool aborted = false;
+  float rs_next = rstd[r0];  // a row's rstd is requested one row ahead, off the row's critical path
+  for (; rr < nrows; ++rr) {
+    const int s = rr % S;
+    const float rs = rs_next;
+    if (rr + 1 < nrows) rs_next = rstd[r0 + rr + 1];
+    const uint32_t par = (uint32_t)(rr / S) & 1u;
+    const bool ok = POLL ? mbar_poll(&full[s], par, &give_up, wait_ns) : mbar_wait(&full[s], par, &give_up, wait_ns);
+    if (!ok) give_up = 1;
+    const uint8_t* slot = bwd_rows + (size_t)s * slot_bytes;
     const int64_t row = r0 + rr;
-    issue(rr + kBwdRing - 1);
-    cp_async_wait<kBwdRing - 1>();  // this thread's pieces of row rr have landed
-    const int sl = rr % kBwdRing;
-    const float rs = rstd[row];
+    float dnv[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+    uint32_t xw[4] = {0u, 0u, 0u, 0u}, yw[4] = {0u, 0u, 0u, 0u};
     float dot = 0.0f;
-#pragma unroll
-    for (int c = 0; c < NG; ++c) {
-      const int j0 = 8 * (t + kThreads * c);
-      if (j0 >= d) continue;
-      const uint4 d0 = bwd_ring[piece(sl, c, 0)], d1 = bwd_ring[piece(sl, c, 1)], xv = bwd_ring[piece(sl, c, 2)];
-      const float dnv[8] = {__uint_as_float(d0.x), __uint_as_float(d0.y), __uint_as_float(d0.z), __uint_as_float(d0.w),
-                            __uint_as_float(d1.x), __uint_as_float(d1.y), __uint_as_float(d1.z), __uint_as_float(d1.w)};
-      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+    if (mine) {
+      const uint4 d0 = *reinterpret_cast<const uint4*>(slot + 4 * j0);
+      const uint4 d1 = *reinterpret_cast<const uint4*>(slot + 4 * j0 + 16);
+      const uint4 xv = *reinterpret_cast<const uint4*>(slot + 4 * d + 2 * j0);
+      const uint4 yv = *reinterpret_cast<const uint4*>(slot + 6 * d + 2 * j0);
+      dnv[0] = __uint_as_float(d0.x); dnv[1] = __uint_as_float(d0.y);
+      dnv[2] = __uint_as_float(d0.z); dnv[3] = __uint_as_float(d0.w);
+      dnv[4] = __uint_as_float(d1.x); dnv[5] = __uint_as_float(d1.y);
+      dnv[6] = __uint_as_float(d1.z); dnv[7] = __uint_as_float(d1.w);
+      xw[0] = xv.x; xw[1] = xv.y; xw[2] = xv.z; xw[3] = xv.w;
+      yw[0] = yv.x; yw[1] = yv.y; yw[2] = yv.z; yw[3] = yv.w;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const float xk = (k & 1) ? bf16_hi(xw[k >> 1]) : bf16_lo(xw[k >> 1]);
-        const float nh = xk * rs;
-        dot += (dnv[k] * gv[c][k]) * nh;
-        dga[c][k] += dnv[k] * nh;
+        const float nh = ((k & 1) ? bf16_hi(xw[k >> 1]) : bf16_lo(xw[k >> 1])) * rs;
+        dot += (dnv[k] * gv[k]) * nh;
+        dga[k] += dnv[k] * nh;
       }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
-    if (lane == 0) red[rr & 1][warp] = dot;
+    const int warp_bad = __any_sync(0xFFFFFFFFu, !ok);
+    if (lane == 0) {
+      red[rr & 1][warp] = dot;
+      bad[rr & 1][warp] = warp_bad;
+    }
     __syncthreads();
-    float tot = 0.0f;
+    // every warp sums the per-warp partials itself: lane w takes warp w's, then a butterfly (the
+    // same tree in every warp, so every thread holds the same total)
+    float tot = lane < nwarps ? red[rr & 1][lane] : 0.0f;
+    const int any_bad = __any_sync(0xFFFFFFFFu, lane < nwarps && bad[rr & 1][lane] != 0);
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) tot += red[rr & 1][w];
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xFFFFFFFFu, tot, o);
+    if (any_bad) {
+      aborted = true;
+      break;
+    }
+    // every thread has its values of row rr in registers: the slot takes row rr + S
+    if (t == 0 && rr + S < nrows) issue(rr + S);
     const float mean = tot * inv_d;
-#pragma unroll
-    for (int c = 0; c < NG; ++c) {
-      const int j0 = 8 * (t + kThreads * c);
-      if (j0 >= d) continue;
-      const uint4 d0 = bwd_ring[piece(sl, c, 0)], d1 = bwd_ring[piece(sl, c, 1)], xv = bwd_ring[piece(sl, c, 2)],
-                  yv = bwd_ring[piece(sl, c, 3)];
-      const float dnv[8] = {__uint_as_float(d0.x), __uint_as_float(d0.y), __uint_as_float(d0.z), __uint_as_float(d0.w),
-                            __uint_as_float(d1.x), __uint_as_float(d1.y), __uint_as_float(d1.z), __uint_as_float(d1.w)};
-      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, yw[4] = {yv.x, yv.y, yv.z, yv.w};
+    if (mine) {
       uint32_t o[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const float nlo = bf16_lo(xw[k]) * rs, nhi = bf16_hi(xw[k]) * rs;
-        const float a = bf16_lo(yw[k]) + rs * (dnv[2 * k] * gv[c][2 * k] - nlo * mean);
-        const float bb = bf16_hi(yw[k]) + rs * (dnv[2 * k + 1] * gv[c][2 * k + 1] - nhi * mean);
-        o[k] = pack_bf16x2(a, bb);
+        const float a = bf16_lo(yw[k]) + rs * (dnv[2 * k] * gv[2 * k] - nlo * mean);
+        const float b = bf16_hi(yw[k]) + rs * (dnv[2 * k + 1] * gv[2 * k + 1] - nhi * mean);
+        o[k] = pack_bf16x2(a, b);
       }
       st_v4(dX + row * d + j0, make_uint4(o[0], o[1], o[2], o[3]));
     }
   }
-  cp_async_wait<0>();
-#pragma unroll
-  for (int c = 0; c < NG; ++c) {
-    const int j0 = 8 * (t + kThreads * c);
-    if (j0 < d) {
-      float* dst = dg_partial + (int64_t)blockIdx.x * d + j0;
-      st_v4(dst, make_uint4(__float_as_uint(dga[c][0]), __float_as_uint(dga[c][1]), __float_as_uint(dga[c][2]),
-                            __float_as_uint(dga[c][3])));
-      st_v4(dst + 4, make_uint4(__float_as_uint(dga[c][4]), __float_as_uint(dga[c][5]),
-                                __float_as_uint(dga[c][6]), __float_as_uint(dga[c][7])));
+  if (aborted) {
+    if (t == 0) {
+      atomicOr(status, kStatusTimeout);
+      // rows rr .. rr + S - 1 may still have copies in flight into this block's ring
+      volatile int never = 0;
+      for (int k = rr; k < rr + S && k < nrows; ++k)
+        mbar_wait(&full[k % S], (uint32_t)(k / S) & 1u, &never);
     }
+    return;
+  }
+  if (mine) {
+    float* dst = dg_partial + (int64_t)blockIdx.x * d + j0;
+    st_v4(dst, make_uint4(__float_as_uint(dga[0]), __float_as_uint(dga[1]), __float_as_uint(dga[2]),
+                          __float_as_uint(dga[3])));
+    st_v4(dst + 4, make_uint4(__float_as_uint(dga[4]), __float_as_uint(dga[5]), __float_as_uint(dga[6]),
+                              __float_as_uint(dga[7])));
   }
 }
 
-// dg[j] = sum over the nblk partial rows, in a fixed order: a block owns 32 columns;
-// thread (ty, tx) sums rows ty, ty+8, ... of column j0+tx, then the 8 partial sums
-// are added in ty order.
-__global__ void __launch_bounds__(kThreads) k_dg_finalize(const float* __restrict__ dg_partial, int nblk, int d,
-                                                          float* __restrict__ dg) {
-  __shared__ float part[8][33];
+// dg[j] = sum over the nblk partial rows, in a fixed order: a block owns 32 columns; thread
+// (ty, tx) sums rows ty, ty + 32, ... of column j0 + tx (independent loads, several in flight per
+// thread), then the 32 partial sums of a column are added in a fixed tree over ty.
+constexpr int kFinRows = 32;
+
+__global__ void __launch_bounds__(32 * kFinRows) k_dg_finalize(const float* __restrict__ dg_partial, int nblk,
+                                                               int d, float* __restrict__ dg) {
+  __shared__ float part[kFinRows][33];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int j = blockIdx.x * 32 + tx;
   float s = 0.0f;
-  if (j < d)
-    for (int b = ty; b < nblk; b += 8) s += dg_partial[(int64_t)b * d + j];
+  if (j < d) {
+#pragma unroll 4
+    for (int b = ty; b < nblk; b += kFinRows) s += dg_partial[(int64_t)b * d + j];
+  }
   part[ty][tx] = s;
   __syncthreads();
-  if (ty == 0 && j < d) {
-    float tot = 0.0f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) tot += part[k][tx];
-    dg[j] = tot;
+  for (int w = kFinRows / 2; w > 0; w >>= 1) {
+    if (ty < w) part[ty][tx] += part[ty + w][tx];
+    __syncthreads();
   }
+  if (ty == 0 && j < d) dg[j] = part[0][tx];
 }
 
 // One thread waits on an mbarrier that nothing ever arrives at, through the
@@ -802,7 +707,15 @@ cudaError_t launch_prologue(int pass, const uint16_t* x, const uint16_t* g, int6
   Prologue a{};
   a.x = x; a.g = g; a.T = T; a.d = d; a.eps = eps; a.rstd = rstd;
   a.part_n = part_n;
-  a.P_n = (int)std::min<int64_t>(L.num_sms, (T + kStatsWarps - 1) / kStatsWarps);
+  // The statistics blocks are latency-bound (a warp's row is one long dependent chain) while the
+  // weight reductions stream: one statistics block per SM leaves the other slots to the weights,
+  // unless x is at least a third of the launch's bytes, when the statistics take every slot
+  // (measured on the 32B block: the attention side's prologue 143 -> 83 us, the MLP side's and the
+  // 7B block's slower with more than one).
+  const int nc = d <= 1024 ? 4 : d <= 2048 ? 8 : d <= 4096 ? 16 : d <= 6144 ? 24 : 32;
+  const bool x_heavy = 3 * T * (int64_t)d >= T * (int64_t)d + n_wgu + n_wd;
+  const int64_t stats_slots = (int64_t)L.num_sms * (x_heavy ? stats_blocks_per_sm(nc) : 1);
+  a.P_n = (int)std::min<int64_t>(std::min<int64_t>(stats_slots, kMaxPartials), (T + kStatsWarps - 1) / kStatsWarps);
   a.wgu = (const uint8_t*)W_gu; a.n_wgu = n_wgu; a.part_wgu = part_wgu; a.P_wgu = absmax_partial_blocks(0, n_wgu);
   a.wd = (const uint8_t*)W_d; a.n_wd = n_wd; a.part_wd = part_wd; a.P_wd = absmax_partial_blocks(0, n_wd);
   a.n8 = n8; a.s_n = s_n; a.G_n = grid_for(T * (d / 16), L.num_sms * 8);
@@ -813,7 +726,6 @@ cudaError_t launch_prologue(int pass, const uint16_t* x, const uint16_t* g, int6
     k_prologue_cast<<<a.G_wgu + a.G_wd + a.G_n, kThreads, 0, L.stream>>>(a);
     return post_launch(L);
   }
-  const int nc = d <= 1024 ? 4 : d <= 2048 ? 8 : d <= 4096 ? 16 : d <= 6144 ? 24 : 32;
   const int g1 = a.P_n + a.P_wgu + a.P_wd, th = kStatsWarps * 32;
   switch (nc) {
     case 4: k_prologue_stats<4><<<g1, th, 0, L.stream>>>(a); break;
@@ -860,50 +772,37 @@ cudaError_t launch_swiglu_cast(const uint16_t* H, int64_t T, int f, int fmt, con
 
 cudaError_t launch_rmsnorm_bwd(const float* dN, const uint16_t* x, const uint16_t* dY, const uint16_t* g,
                                const float* rstd, int64_t T, int d, uint16_t* dX, float* dg_partial, float* dg,
-                               const Launch& L) {
-  const int ng = (d + 8 * kThreads - 1) / (8 * kThreads);
-  if (ng <= 2) {
-    int per_sm = 0;
-    const void* fn = ng == 1 ? (const void*)k_rmsnorm_bwd_reg<1> : (const void*)k_rmsnorm_bwd_reg<2>;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, 0) != cudaSuccess || per_sm < 1)
-      per_sm = 1;
-    const int64_t wave = (int64_t)L.num_sms * per_sm;
-    const int rows = (int)std::max<int64_t>(kBwdRows, (T + wave - 1) / wave);
-    const int nblk = (int)((T + rows - 1) / rows);
-    if (ng == 1) k_rmsnorm_bwd_reg<1><<<nblk, kThreads, 0, L.stream>>>(dN, x, dY, g, rstd, T, d, rows, dX, dg_partial);
-    else k_rmsnorm_bwd_reg<2><<<nblk, kThreads, 0, L.stream>>>(dN, x, dY, g, rstd, T, d, rows, dX, dg_partial);
-    cudaError_t e = post_launch(L);
-    if (e != cudaSuccess) return e;
-    k_dg_finalize<<<(d + 31) / 32, kThreads, 0, L.stream>>>(dg_partial, nblk, d, dg);
-    return post_launch(L);
-  }
-  const size_t smem = rmsnorm_bwd_smem(ng <= 4 ? ng : 4);
-  // one wave of resident blocks (two per SM when their rings fit), consecutive rows each (at least
-  // kBwdRows: the dg partials' workspace holds ceil(T / kBwdRows) rows)
-  const int64_t wave = (int64_t)L.num_sms * (smem <= 110 * 1024 ? 2 : 1);
+                               const Launch& L, uint64_t wait_ns) {
+  // one wave of resident blocks, consecutive rows each (at least kBwdRows: the dg partials'
+  // workspace holds ceil(T / kBwdRows) rows); a block's ring takes as many row slots as its share
+  // of the budget holds
+  const size_t slot = (size_t)8 * d;
+  const int bps = bwd_tma_blocks_per_sm(d);
+  const int S = (int)std::min<size_t>(kBwdSlotsMax, kBwdSmemBudget / bps / slot);
+  if (S < 2) return cudaErrorInvalidConfiguration;
+  const size_t smem = (size_t)S * slot;
+  const int64_t wave = (int64_t)L.num_sms * bps;
   const int rows = (int)std::max<int64_t>(kBwdRows, (T + wave - 1) / wave);
   const int nblk = (int)((T + rows - 1) / rows);
-  static int configured_device[5] = {-1, -1, -1, -1, -1};
+  static int configured_device[2] = {-1, -1};
   int dev = 0;
   cudaGetDevice(&dev);
-  auto go = [&](auto kernel, int which) -> cudaError_t {
-    if (configured_device[which] != dev) {
-      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      configured_device[which] = dev;
-    }
-    kernel<<<nblk, kThreads, smem, L.stream>>>(dN, x, dY, g, rstd, T, d, rows, dX, dg_partial);
-    return cudaSuccess;
-  };
-  cudaError_t le;
-  switch (ng) {
-    case 3: le = go(k_rmsnorm_bwd<3>, 3); break;
-    default: le = go(k_rmsnorm_bwd<4>, 4); break;
+  const bool poll = wait_ns != 0;  // the self-test's short limits
+  const void* fn = poll ? (const void*)k_rmsnorm_bwd_tma<true> : (const void*)k_rmsnorm_bwd_tma<false>;
+  if (configured_device[poll] != dev) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmemBudget);
+    if (e != cudaSuccess) return e;
+    configured_device[poll] = dev;
   }
-  if (le != cudaSuccess) return le;
+  if (poll)
+    k_rmsnorm_bwd_tma<true><<<nblk, bwd_tma_threads(d), smem, L.stream>>>(dN, x, dY, g, rstd, T, d, rows, S, dX,
+                                                                          dg_partial, L.status, wait_ns);
+  else
+    k_rmsnorm_bwd_tma<false><<<nblk, bwd_tma_threads(d), smem, L.stream>>>(dN, x, dY, g, rstd, T, d, rows, S, dX,
+                                                                           dg_partial, L.status, kWaitLimitNs);
   cudaError_t e = post_launch(L);
   if (e != cudaSuccess) return e;
-  k_dg_finalize<<<(d + 31) / 32, kThreads, 0, L.stream>>>(dg_partial, nblk, d, dg);
+  k_dg_finalize<<<(d + 31) / 32, 32 * kFinRows, 0, L.stream>>>(dg_partial, nblk, d, dg);
   return post_launch(L);
 }
 

@@ -157,6 +157,31 @@ FP8Q_API int swiglu_quant(const void* H, int64_t T, int64_t f, fp8q_fmt fmt, uin
                  void* ws, size_t ws_bytes, fp8q_stream stream);
 
 /* ------------------------------------------------------------------------ */
+/* RMSNorm backward with the residual gradient: the last step of the        */
+/* block's backward (LLMQ §3: the non-matmul ops around the matmuls).       */
+/* ------------------------------------------------------------------------ */
+/* dN [T,d] fp32 (the gradient at the normalized output n = x rstd g), x [T,d]
+ * bf16 (the block input), dY [T,d] bf16 (the residual branch's gradient),
+ * g [d] bf16, rstd [T] fp32 (the forward's, as rmsnorm_quant writes it)
+ * -> dX [T,d] bf16 and dg [d] fp32, with nh = x rstd and u = dN g:
+ *   m_t  = (1/d) sum_j u_tj nh_tj,
+ *   dX   = bf16(dY + rstd (u - nh m_t)),
+ *   dg_j = sum_t dN_tj nh_tj.
+ * The sums are fp32 in a fixed order (a row: 8 columns per thread, a warp
+ * butterfly, a butterfly over the warps; dg: per-block partials over runs of
+ * consecutive rows, then over blocks in block order), so a result repeats bit
+ * for bit on one device and differs from the exact value by fp32 rounding.
+ * Requirements: 1 <= T <= 2^28, d a multiple of 16, 16 <= d <= 8192; dN, x,
+ * dY, g and dX 16-byte aligned; rstd and dg 4-byte aligned.  Workspace:
+ * rmsnorm_bwd_workspace_size(T, d) bytes, 256-byte aligned (the per-block dg
+ * partials; FP8Q_ERR_WORKSPACE when missing, misaligned or too small).  The
+ * caller owns every buffer; the call only enqueues work on `stream`. */
+FP8Q_API size_t rmsnorm_bwd_workspace_size(int64_t T, int64_t d);
+FP8Q_API int rmsnorm_bwd(const float* dN, const void* x, const void* dY, const void* g, const float* rstd,
+                         int64_t T, int64_t d, void* dX, float* dg, void* ws, size_t ws_bytes,
+                         fp8q_stream stream);
+
+/* ------------------------------------------------------------------------ */
 /* Block-scaled MXFP8 (LLMQ §2: inner-dimension block scaling, which the    */
 /* Blackwell tensor cores support natively).                                */
 /* ------------------------------------------------------------------------ */
@@ -507,6 +532,20 @@ FP8Q_API int fp8q_selftest_gemm_wait_limit(fp8q_layout layout, int64_t M, int64_
                                            const float* sinvA, const float* sinvB, int mx, const uint8_t* sfA,
                                            const uint8_t* sfB, void* C, fp8q_dtype out_dtype, int64_t ldc,
                                            int64_t limit_ns, fp8q_stream stream);
+
+/* Diagnostics for the RMSNorm backward's abort sequence (no page counterpart):
+ * rmsnorm_bwd, except that every wait of a block on the bulk copies of its
+ * rows probes the barrier without suspending and gives up after limit_ns
+ * (1 ns .. 10 s) instead of 2 s.  With a limit of a few nanoseconds the first
+ * waits run out: the block records
+ * FP8Q_STATUS_TIMEOUT, stops, waits (with the full 2 s limit) for the copies
+ * still in flight into its shared memory and exits; dX and dg are then
+ * incomplete and the context stays usable.  Returns FP8Q_OK once enqueued
+ * (synchronous errors as rmsnorm_bwd). */
+FP8Q_API int fp8q_selftest_rmsnorm_bwd_wait_limit(const float* dN, const void* x, const void* dY, const void* g,
+                                                  const float* rstd, int64_t T, int64_t d, void* dX, float* dg,
+                                                  void* ws, size_t ws_bytes, int64_t limit_ns,
+                                                  fp8q_stream stream);
 
 /* Kernel-level timing for benchmarks.  While tracing is on for the calling
  * host thread, each kernel step the library enqueues is bracketed by two CUDA

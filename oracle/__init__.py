@@ -130,6 +130,7 @@ def lib() -> ctypes.CDLL:
             L.fo_quantize_absmax.argtypes = [vp, ctypes.c_int, i64, ctypes.c_int, vp, vp]
             L.fo_rmsnorm_quant.argtypes = [vp, vp, i64, i64, f32, vp, vp, vp]
             L.fo_swiglu_quant.argtypes = [vp, i64, i64, ctypes.c_int, vp, vp]
+            L.fo_rmsnorm_bwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, ctypes.c_int, vp, vp]
             L.fo_gemm_scaled.argtypes = [ctypes.c_int, i64, i64, i64, vp, ctypes.c_int, vp,
                                          ctypes.c_int, f32, f32, vp, ctypes.c_int, vp, ctypes.c_int]
             L.fo_block_forward.argtypes = [ctypes.POINTER(_BlockIO)]
@@ -221,6 +222,21 @@ def rmsnorm_quant(x: np.ndarray, g: np.ndarray, eps: float):
     rstd = np.empty(T, dtype=np.float32)
     st = lib().fo_rmsnorm_quant(_c(x), _c(g), T, d, eps, _c(q), _c(scal), _c(rstd))
     return q, scal, rstd, st
+
+
+def rmsnorm_bwd(dN: np.ndarray, x: np.ndarray, g: np.ndarray, rstd: np.ndarray, dY: np.ndarray,
+                exact: bool = False):
+    """RMSNorm backward with the residual gradient dY, on values (float64: dN, x, dY [T,d], g [d],
+    rstd [T]): dX = dY + rstd (u - nh mean_j(u nh)), u = dN g, nh = x rstd; dg = sum_t dN nh.
+    Returns (dX [T,d], dg [d]) as float64: dX rounded to bf16 and dg to fp32 unless exact."""
+    dN, x, dY = (np.ascontiguousarray(a, dtype=np.float64) for a in (dN, x, dY))
+    g, rstd = np.ascontiguousarray(g, dtype=np.float64), np.ascontiguousarray(rstd, dtype=np.float64)
+    T, d = x.shape
+    assert dN.shape == (T, d) and dY.shape == (T, d) and g.shape == (d,) and rstd.shape == (T,)
+    dX = np.empty((T, d), dtype=np.float64)
+    dg = np.empty(d, dtype=np.float64)
+    lib().fo_rmsnorm_bwd(_c(dN), _c(x), _c(g), _c(rstd), _c(dY), T, d, int(exact), _c(dX), _c(dg))
+    return dX, dg
 
 
 def swiglu_quant(H: np.ndarray, fmt: int = E4M3):

@@ -1114,6 +1114,19 @@ int fo_rmsnorm_quant(const uint16_t* x, const uint16_t* g, int64_t T, int64_t d,
   return finite_scal(t.s) ? 0 : 1;
 }
 
+// RMSNorm backward with the residual gradient on given values: dX = dres + rstd (u - nh mean(u nh)),
+// u = dN g, nh = x rstd; dg = sum over rows of dN nh.  dX is rounded to bf16 and dg to fp32 unless
+// `exact` (then both are the fp64 values).
+int fo_rmsnorm_bwd(const double* dN, const double* x, const double* g, const double* rstd, const double* dres,
+                   int64_t T, int64_t d, int exact, double* dX, double* dg) {
+  std::vector<double> X, G;
+  rmsnorm_bwd(std::vector<double>(x, x + T * d), std::vector<double>(g, g + d), std::vector<double>(rstd, rstd + T),
+              std::vector<double>(dN, dN + T * d), std::vector<double>(dres, dres + T * d), T, d, exact != 0, X, G);
+  put(dX, X);
+  put(dg, G);
+  return 0;
+}
+
 // SwiGLU of H [T, 2f] (gate | up, bf16 bits) followed by per-tensor quantization.
 int fo_swiglu_quant(const uint16_t* H, int64_t T, int64_t f, int fmt, uint8_t* q, float* scal3) {
   QTensor t = quantize(swiglu_fwd(load_input(H, 0, T * 2 * f), T, f, false), fmt, false);

@@ -72,6 +72,14 @@ def test_invalid_arguments_rejected_without_device(lib):
     assert lib.swiglu_quant(fake, 4, 32, 0, fake, fake, fake, 16, None) == 6
     # block: null descriptor
     assert lib.mlp_block_fwd(None, fake, 1 << 20, None) == INVALID
+    # RMSNorm backward: d not a multiple of 16, misaligned x, workspace too small, a zero wait limit
+    ws = lib.rmsnorm_bwd_workspace_size(64, 32)
+    assert ws == ((64 + 15) // 16 * 32 * 4 + 255) // 256 * 256
+    assert lib.rmsnorm_bwd(fake, fake, fake, fake, fake, 64, 24, fake, fake, fake, 4096, None) == INVALID
+    assert lib.rmsnorm_bwd(fake, odd, fake, fake, fake, 64, 32, fake, fake, fake, ws, None) == INVALID
+    assert lib.rmsnorm_bwd(fake, fake, fake, fake, fake, 64, 32, fake, fake, fake, ws - 256, None) == 6
+    assert lib.fp8q_selftest_rmsnorm_bwd_wait_limit(fake, fake, fake, fake, fake, 64, 32, fake, fake, fake, ws,
+                                                    0, None) == INVALID
 
 
 def test_mx_arguments_rejected_without_device(lib):

@@ -6,6 +6,10 @@ SwiGLU: closed-form values (tests/golden/swiglu_closed_form.txt) within 2 ulp; s
 silu(h) = h once e^-h is below half an ulp.
 RMSNorm: hand-worked rows (golden), the pairwise order of the sum of squares (golden), the
 fp64 closed form on a 4x4 block within 2 ulp, scale invariance under powers of two (eps = 0).
+RMSNorm backward (with the residual gradient): in exact mode equal to central finite differences of
+L = sum dN (x rstd(x) g) + sum dY x for every element of x and g; the rounded mode is the exact
+result rounded once (dX to bf16, dg to fp32); dN = 0 passes dY through unchanged; with eps = 0
+the input gradient of the normalization is orthogonal to x (scale invariance).
 """
 
 import numpy as np
@@ -139,3 +143,58 @@ def test_rmsnorm_power_of_two_invariance():
     np.testing.assert_array_equal(q1, q2)
     np.testing.assert_array_equal(s1, s2)
     np.testing.assert_array_equal(r1, r2 * 8)
+
+
+def _rms_loss(x, g, dN, dY, eps):
+    rs = 1.0 / np.sqrt((x * x).mean(axis=1) + eps)
+    return float((dN * (x * rs[:, None] * g)).sum() + (dY * x).sum())
+
+
+def test_rmsnorm_bwd_exact_matches_finite_differences():
+    T, d, eps, h = 3, 8, 1e-3, 1e-6
+    rng = np.random.default_rng(11)
+    x, dN, dY = rng.standard_normal((T, d)), rng.standard_normal((T, d)), rng.standard_normal((T, d))
+    g = 1 + 0.2 * rng.standard_normal(d)
+    rstd = 1.0 / np.sqrt((x * x).mean(axis=1) + eps)
+    dX, dg = oracle.rmsnorm_bwd(dN, x, g, rstd, dY, exact=True)
+    fx = np.zeros_like(x)
+    for t in range(T):
+        for j in range(d):
+            xp, xm = x.copy(), x.copy()
+            xp[t, j] += h
+            xm[t, j] -= h
+            fx[t, j] = (_rms_loss(xp, g, dN, dY, eps) - _rms_loss(xm, g, dN, dY, eps)) / (2 * h)
+    fg = np.zeros_like(g)
+    for j in range(d):
+        gp, gm = g.copy(), g.copy()
+        gp[j] += h
+        gm[j] -= h
+        fg[j] = (_rms_loss(x, gp, dN, dY, eps) - _rms_loss(x, gm, dN, dY, eps)) / (2 * h)
+    np.testing.assert_allclose(dX, fx, rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(dg, fg, rtol=1e-6, atol=1e-7)
+
+
+def test_rmsnorm_bwd_rounds_once_and_passes_the_residual():
+    T, d = 5, 48
+    rng = np.random.default_rng(12)
+    x, dN = rng.standard_normal((T, d)), rng.standard_normal((T, d)).astype(np.float32).astype(np.float64)
+    dY = oracle.bf16_to_f64(oracle.bf16_round(rng.standard_normal((T, d))))
+    g = oracle.bf16_to_f64(oracle.bf16_round(1 + 0.1 * rng.standard_normal(d)))
+    rstd = (1.0 / np.sqrt((x * x).mean(axis=1) + 1e-6)).astype(np.float32).astype(np.float64)
+    ex, exg = oracle.rmsnorm_bwd(dN, x, g, rstd, dY, exact=True)
+    dX, dg = oracle.rmsnorm_bwd(dN, x, g, rstd, dY)
+    assert np.array_equal(dX, oracle.bf16_to_f64(oracle.bf16_round(ex)))
+    assert np.array_equal(dg, exg.astype(np.float32).astype(np.float64))
+    z, zg = oracle.rmsnorm_bwd(np.zeros((T, d)), x, g, rstd, dY)
+    assert np.array_equal(z, dY) and not zg.any()
+
+
+def test_rmsnorm_bwd_orthogonal_to_x_without_eps():
+    T, d = 4, 64
+    rng = np.random.default_rng(13)
+    x, dN = rng.standard_normal((T, d)), rng.standard_normal((T, d))
+    g = 1 + 0.1 * rng.standard_normal(d)
+    rstd = 1.0 / np.sqrt((x * x).mean(axis=1))
+    dX, _ = oracle.rmsnorm_bwd(dN, x, g, rstd, np.zeros((T, d)), exact=True)
+    dot = (dX * x).sum(axis=1)
+    assert np.all(np.abs(dot) <= 1e-12 * np.abs(dX).sum(axis=1) * np.abs(x).max(axis=1))
