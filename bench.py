@@ -682,7 +682,7 @@ def main():
     if os.path.exists(tpath):
         with open(tpath) as fh:
             tj = json.load(fh)
-        if tj.get("workload") == w.name and tj.get("T") == w.T and tj.get("kernel_hash") == kernel_hash() and not args.bf16:
+        if tj.get("workload") == w.name and tj.get("T") == w.T and tj.get("kernel_hash") == kernel_hash() and not args.bf16 and not args.mxfp8:
             traffic = tj.get("bytes_per_launch")
     pick = choose_peak(pk, r["ms"], r["clocks"], bf16=args.bf16)
     peak = pick["peak"]
