@@ -6,6 +6,7 @@ table, so it must stay in step with the library and the workloads.
     forward + backward, plus the QKV and O projections), in every precision mode (per-tensor FP8,
     BF16, block-scaled MXFP8 for the MLP workloads); the recompute
     mode adds exactly one gate/up GEMM of executed work;
+  * --launch-log folds the traced launches of K steps onto the plan's positions;
   * the attention kernels' executed FLOPs are 18 products per causal pair and head against the
     algorithmic 14 (the backward kernels recompute S and dP), 128 x 2 FLOPs each.
 """
@@ -95,3 +96,15 @@ def test_peak_follows_the_run():
     assert capped["kind"] == "sustained" and capped["peak"] == 3400.0
     assert bench.choose_peak(pk, 5000.0, {"sm_mhz": 1700.0, "sm_max_mhz": 2070.0}, bf16=True)["peak"] == 1700.0
     assert bench.choose_peak(pk, 5000.0, None)["kind"] == "sustained"
+
+
+def test_launch_positions_average_each_position():
+    """--launch-log: the traced launches of K steps fold onto the plan's positions, one mean per
+    position, with the rates from the plan's bytes or FLOPs."""
+    plan = [("quant_cast", 2e9, 0), ("gemm_x", 1e9, 4e12)]
+    traced = [("quant_cast", 1.0), ("gemm_x", 2.0), ("quant_cast", 3.0), ("gemm_x", 4.0)]  # ms, two steps
+    out = bench.launch_positions(traced, plan)
+    assert [o["pos"] for o in out] == [0, 1]
+    assert out[0]["us"] == 2000.0 and out[1]["us"] == 3000.0
+    assert out[0]["gbs"] == pytest.approx(2e9 / 2e-3 / 1e9, abs=0.1) and out[0]["tflops"] is None
+    assert out[1]["tflops"] == pytest.approx(4e12 / 3e-3 / 1e12, abs=0.1) and out[1]["gbs"] is None
