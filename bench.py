@@ -14,7 +14,9 @@ timed region, the model state resident in HBM; e2e_all_io = the same with
 every input and output, weights and weight gradients included, through the
 host.  The roofline object is for the dominant kernel (the
 tcgen05 GEMM), timed live with CUDA events recorded by the library around each
-of its launches inside the timed region.
+of its launches in the first --trace-steps steps of the timed region (the
+event pairs are stream work of their own, ~2 % of a step when every step is
+traced).
 
   python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -69,6 +71,9 @@ def parse_args():
                     help="time cuBLASLt FP8 (torch._scaled_mm) 8192^3, burst and sustained, and exit")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the workload's T (same d, f, distributions); for small profiling runs")
+    ap.add_argument("--trace-steps", type=int, default=10,
+                    help="timed steps whose kernel launches the per-launch trace brackets with CUDA events "
+                         "(the first ones of the timed region)")
     ap.add_argument("--launch-log", default="",
                     help="write the mean time of every launch position of the step (kernel, bytes, flops, us) "
                          "to this JSON file")
@@ -341,8 +346,27 @@ def run_ours(args, rank, world, local_rank):
 
     K = args.steps
     plan = step_work(w, args.recompute, args.bf16, args.mxfp8)
-    if lib.fp8q_trace_start(K * len(plan)) != 0:
+    # the per-launch CUDA events bracket every launch of a sample of the timed steps, spread evenly
+    # over the region (steps 0, stride, 2 stride, ...): an event pair is about 2 us of stream work,
+    # so tracing every step would itself lengthen the step by ~2 %
+    traced_steps = max(1, min(K, args.trace_steps))
+    stride = K // traced_steps
+    if lib.fp8q_trace_start(traced_steps * len(plan)) != 0:
         raise RuntimeError("fp8q_trace_start failed")
+    lib.fp8q_trace_stop()
+    count = [0]
+
+    def timed_step():
+        i = count[0]
+        count[0] += 1
+        on = i % stride == 0 and i // stride < traced_steps
+        if on:
+            lib.fp8q_trace_resume()
+        n = step()
+        if on:
+            lib.fp8q_trace_stop()
+        return n
+
     launches = 0
     if flush_l2(w):
         # weights that fit (nearly) in L2: a 256 MB write between steps, outside the timed spans
@@ -352,7 +376,7 @@ def run_ours(args, rank, world, local_rank):
             for e0, e1 in evs:
                 scratch.fill_(1)
                 e0.record(stream)
-                launches += step()
+                launches += timed_step()
                 e1.record(stream)
             torch.cuda.synchronize()
         ms = sum(e0.elapsed_time(e1) for e0, e1 in evs)
@@ -362,7 +386,7 @@ def run_ours(args, rank, world, local_rank):
         with ClockSampler(local_rank) as clk:
             ev0.record(stream)
             for _ in range(K):
-                launches += step()
+                launches += timed_step()
             ev1.record(stream)
             torch.cuda.synchronize()
         ms = ev0.elapsed_time(ev1)
@@ -675,7 +699,8 @@ def main():
     gemm = {k: v for k, v in kernels.items() if k.startswith("gemm")}
     g_ms = sum(v["total_ms"] for v in gemm.values())
     g_launch = sum(v["launches"] for v in gemm.values())
-    g_flops = sum(fl for (name, _, fl) in r["plan"] if name.startswith("gemm")) * r["K"]
+    t_steps = len(r["traced"]) // len(r["plan"])  # the timed steps the trace bracketed
+    g_flops = sum(fl for (name, _, fl) in r["plan"] if name.startswith("gemm")) * t_steps
     achieved = g_flops / (g_ms * 1e-3) / 1e12
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "gemm_traffic.json")
@@ -707,7 +732,7 @@ def main():
         "pct_fp8_peak": round(100.0 * value / world / pick["fp8_peak"], 2),
         "roofline": {"kernel": "k_gemm_f8 / k_gemm_f8_wide (the six block GEMMs)", "bound": "tensor", "achieved": round(achieved, 1),
                      "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic, "launches_per_step": g_launch // r["K"],
+                     "traffic": traffic, "launches_per_step": g_launch // t_steps, "traced_steps": t_steps,
                      "share_of_step": round(g_ms / traced_total, 4),
                      "peak_kind": pick["kind"], "peak_source": pick["source"],
                      "frac_burst": round(achieved / pick["burst"], 4),

@@ -49,18 +49,29 @@ thread_local Trace t_trace;
 
 namespace fp8q {
 
+// Under stream capture an event is recorded as an external record: it becomes an event-record node
+// of the graph, recorded each time the graph runs (a plain record would only order the capture's
+// own streams, and the external flag is refused outside a capture).
+static void trace_record(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, s);
+}
+
 bool trace_step_begin(cudaStream_t s, int kind) {
   nvtxRangePushA(kKindNames[kind]);
   Trace& t = t_trace;
   if (!t.on || t.n >= (int)t.kinds.size()) return false;
   t.kinds[t.n] = kind;
-  cudaEventRecord(t.ev[2 * t.n], s);
+  trace_record(t.ev[2 * t.n], s);
   return true;
 }
 
 void trace_step_end(cudaStream_t s, bool active) {
   if (active) {
-    cudaEventRecord(t_trace.ev[2 * t_trace.n + 1], s);
+    trace_record(t_trace.ev[2 * t_trace.n + 1], s);
     ++t_trace.n;
   }
   nvtxRangePop();
@@ -1459,6 +1470,12 @@ int fp8q_trace_start(int capacity) {
 
 int fp8q_trace_stop(void) {
   t_trace.on = false;
+  return FP8Q_OK;
+}
+
+int fp8q_trace_resume(void) {
+  if (t_trace.ev.empty()) return FP8Q_ERR_INVALID_ARG;
+  t_trace.on = true;
   return FP8Q_OK;
 }
 

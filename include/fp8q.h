@@ -552,12 +552,19 @@ FP8Q_API int fp8q_selftest_rmsnorm_bwd_wait_limit(const float* dN, const void* x
  * events recorded on the stream it is launched on (host-side CUDA objects; no
  * device memory).  fp8q_trace_start(capacity) creates 2*capacity events and
  * turns tracing on (FP8Q_ERR_CUDA if event creation fails); steps beyond
- * capacity are not traced.  fp8q_trace_stop() turns it off.
+ * capacity are not traced.  fp8q_trace_stop() turns it off;
+ * fp8q_trace_resume() turns it back on, keeping the steps recorded so far
+ * (FP8Q_ERR_INVALID_ARG before the first fp8q_trace_start), so that a
+ * caller can trace a sample of its steps.  Steps enqueued
+ * while the stream is being captured into a CUDA graph record their events as
+ * event-record nodes of the graph: each run of the graph records them again,
+ * and fp8q_trace_read() then reports the latest run.
  * fp8q_trace_read() waits for the recorded events, writes each step's
  * duration in milliseconds and its kernel kind, and returns the count.
  * fp8q_kernel_name(kind) names a kind (static storage). */
 FP8Q_API int fp8q_trace_start(int capacity);
 FP8Q_API int fp8q_trace_stop(void);
+FP8Q_API int fp8q_trace_resume(void);
 FP8Q_API int fp8q_trace_read(float* ms, int* kinds, int capacity);
 FP8Q_API const char* fp8q_kernel_name(int kind);
 
