@@ -75,7 +75,9 @@ def check_backward(b, ref):
     assert row_rel(host_f64(b.dg)[None, :], ref["dg"][None, :]) < 5e-3
 
 
-@pytest.mark.parametrize("T,d,f", [(192, 256, 384), (272, 528, 400), (1, 16, 16), (640, 1024, 1280)])
+# (2048, 256, 256): x is more than a third of the forward prologue's bytes, so the RMSNorm
+# statistics take every resident slot of their launch
+@pytest.mark.parametrize("T,d,f", [(192, 256, 384), (272, 528, 400), (1, 16, 16), (640, 1024, 1280), (2048, 256, 256)])
 def test_block_small_shapes(T, d, f):
     b, ref = run_block("7b-mlp-fwd-bwd", T, d, f)
     check_forward(b, ref)

@@ -55,7 +55,8 @@ def requant(gpu, ref, amax_gpu, amax_ref):
 
 
 @pytest.mark.parametrize("T,d,f,nq,e4m3", [(192, 256, 384, 384, False), (272, 528, 400, 336, False),
-                                            (64, 1024, 768, 1536, False), (256, 512, 640, 768, True)])
+                                            (64, 1024, 768, 1536, False), (256, 512, 640, 768, True),
+                                            (2048, 256, 256, 384, False)])  # x-dominated prologues
 def test_full_block_small_shapes(T, d, f, nq, e4m3):
     b, inp = run(T, d, f, nq, grad_e4m3=e4m3)
     ref = oracle.full_block(inp["x"], inp["g1"], inp["W_qkv"], inp["W_o"], inp["att"], inp["g"], inp["W_gu"],
